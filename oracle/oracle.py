@@ -1,0 +1,257 @@
+"""ctypes marshalling for the plain-C oracle (oracle.c).  Argument conversion only.
+
+TEST INFRASTRUCTURE ONLY: imported by the tests, the smoke check and the benchmark's
+CPU-baseline leg; never by the product path.
+
+Arrays are numpy arrays on the host: fp32 gradients/state as float32, bf16 gradients as
+uint16 bit patterns, digests as uint64.
+"""
+import ctypes as C
+
+import numpy as np
+
+from . import build as _build
+
+_lib = None
+
+F32 = 0
+BF16 = 1
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        path = _build.build()
+        L = C.CDLL(path)
+        fp = C.c_void_p
+        L.oracle_probe_mul_add.argtypes = [C.c_float, C.c_float, C.c_float]
+        L.oracle_probe_mul_add.restype = C.c_float
+        L.oracle_probe_subnormals.restype = C.c_int
+        L.oracle_tree_sum.argtypes = [fp, C.c_uint64]
+        L.oracle_tree_sum.restype = C.c_float
+        L.oracle_reduce.argtypes = [fp, C.c_int, C.c_uint32, C.c_uint64, fp]
+        L.oracle_reduce.restype = C.c_int
+        L.oracle_reduce_topology.argtypes = [fp, C.c_int, C.c_uint32, C.c_uint32, C.c_uint64, fp]
+        L.oracle_reduce_topology.restype = C.c_int
+        L.oracle_norm.argtypes = [fp, C.c_uint64, fp]
+        L.oracle_norm.restype = C.c_float
+        L.oracle_clip_scale.argtypes = [C.c_float, C.c_float]
+        L.oracle_clip_scale.restype = C.c_float
+        L.oracle_bias_corrections.argtypes = [C.c_float, C.c_float, C.c_int32,
+                                              C.POINTER(C.c_float), C.POINTER(C.c_float)]
+        L.oracle_bias_corrections.restype = None
+        L.oracle_adamw.argtypes = [fp, fp, fp, fp, C.c_uint64, C.c_float,
+                                   C.c_float, C.c_float, C.c_float, C.c_float, C.c_float,
+                                   C.c_float, C.c_float]
+        L.oracle_adamw.restype = None
+        L.oracle_pf61_constant.restype = C.c_uint64
+        L.oracle_pf61.argtypes = [fp, C.c_uint64]
+        L.oracle_pf61.restype = C.c_uint64
+        L.oracle_blake2b.argtypes = [fp, C.c_uint64, fp, C.c_uint32]
+        L.oracle_blake2b.restype = C.c_int
+        L.oracle_node.argtypes = [C.c_uint64, C.c_uint64]
+        L.oracle_node.restype = C.c_uint64
+        L.oracle_merkle_root.argtypes = [fp, C.c_uint64]
+        L.oracle_merkle_root.restype = C.c_uint64
+        L.oracle_image_bytes.argtypes = [C.c_uint64]
+        L.oracle_image_bytes.restype = C.c_uint64
+        L.oracle_image.argtypes = [C.c_int32, C.c_uint64, fp, fp, fp, fp]
+        L.oracle_image.restype = C.c_int
+        L.oracle_num_leaves.argtypes = [C.c_uint64]
+        L.oracle_num_leaves.restype = C.c_uint64
+        L.oracle_leaves.argtypes = [C.c_int32, C.c_uint64, fp, fp, fp, fp]
+        L.oracle_leaves.restype = C.c_int
+        L.oracle_state_hash.argtypes = [C.c_int32, C.c_uint64, fp, fp, fp, C.POINTER(C.c_uint64)]
+        L.oracle_state_hash.restype = C.c_int
+        L.oracle_step.argtypes = [fp, C.c_int, C.c_uint32, C.c_uint32, C.c_uint64, fp, fp, fp,
+                                  C.c_float, C.c_float, C.c_float, C.c_float, C.c_float,
+                                  C.c_float, C.c_int32, C.POINTER(C.c_float),
+                                  C.POINTER(C.c_float), C.POINTER(C.c_uint64)]
+        L.oracle_step.restype = C.c_int
+        _lib = L
+    return _lib
+
+
+def _p(a: np.ndarray):
+    assert a.flags.c_contiguous
+    return C.c_void_p(a.ctypes.data)
+
+
+def _f32(a):
+    a = np.ascontiguousarray(a)
+    assert a.dtype == np.float32, a.dtype
+    return a
+
+
+def _grad_arrays(grads):
+    """Return (dtype code, list of contiguous arrays, ctypes pointer array)."""
+    arrs = [np.ascontiguousarray(x) for x in grads]
+    if arrs[0].dtype == np.float32:
+        code = F32
+    elif arrs[0].dtype == np.uint16:
+        code = BF16
+    else:
+        raise TypeError(f"gradient dtype {arrs[0].dtype}: use float32 or uint16 (bf16 bits)")
+    n = arrs[0].size
+    for a in arrs:
+        if a.dtype != arrs[0].dtype or a.size != n:
+            raise ValueError("all replica gradients must share dtype and length")
+    ptrs = (C.c_void_p * len(arrs))(*[a.ctypes.data for a in arrs])
+    return code, arrs, ptrs
+
+
+def probe_mul_add(a, b, c) -> float:
+    return lib().oracle_probe_mul_add(a, b, c)
+
+
+def probe_subnormals() -> bool:
+    return bool(lib().oracle_probe_subnormals())
+
+
+def tree_sum(x) -> np.float32:
+    x = _f32(x)
+    return np.float32(lib().oracle_tree_sum(_p(x), x.size))
+
+
+def reduce(grads) -> np.ndarray:
+    code, arrs, ptrs = _grad_arrays(grads)
+    n = arrs[0].size
+    g = np.empty(n, np.float32)
+    rc = lib().oracle_reduce(C.cast(ptrs, C.c_void_p), code, len(arrs), n, _p(g))
+    if rc != 0:
+        raise ValueError(f"oracle_reduce rc={rc}")
+    return g
+
+
+def reduce_topology(grads, nodes: int, gpus_per_node: int) -> np.ndarray:
+    code, arrs, ptrs = _grad_arrays(grads)
+    if nodes * gpus_per_node != len(arrs):
+        raise ValueError("nodes * gpus_per_node must equal the replica count")
+    n = arrs[0].size
+    g = np.empty(n, np.float32)
+    rc = lib().oracle_reduce_topology(C.cast(ptrs, C.c_void_p), code, nodes, gpus_per_node,
+                                      n, _p(g))
+    if rc == -2:
+        raise ValueError("topology breaks the canonical tree")
+    if rc != 0:
+        raise ValueError(f"oracle_reduce_topology rc={rc}")
+    return g
+
+
+def norm(g, with_chunks: bool = False):
+    g = _f32(g)
+    c = (g.size + 4095) // 4096
+    chunks = np.empty(max(c, 1), np.float32)
+    nv = np.float32(lib().oracle_norm(_p(g), g.size, _p(chunks)))
+    if with_chunks:
+        return nv, chunks[:c].copy()
+    return nv
+
+
+def clip_scale(norm_value, clip) -> np.float32:
+    return np.float32(lib().oracle_clip_scale(float(np.float32(norm_value)), float(np.float32(clip))))
+
+
+def bias_corrections(beta1, beta2, t):
+    b1, b2 = C.c_float(), C.c_float()
+    lib().oracle_bias_corrections(float(np.float32(beta1)), float(np.float32(beta2)), int(t),
+                                  C.byref(b1), C.byref(b2))
+    return np.float32(b1.value), np.float32(b2.value)
+
+
+def adamw(w, m, v, g, scale, lr, beta1, beta2, eps, wd, bc1, bc2):
+    """In-place on copies; returns (w', m', v')."""
+    w = _f32(w).copy(); m = _f32(m).copy(); v = _f32(v).copy(); g = _f32(g)
+    n = w.size
+    assert m.size == n and v.size == n and g.size == n
+    f = lambda x: float(np.float32(x))  # noqa: E731
+    lib().oracle_adamw(_p(w), _p(m), _p(v), _p(g), n, f(scale), f(lr), f(beta1), f(beta2),
+                       f(eps), f(wd), f(bc1), f(bc2))
+    return w, m, v
+
+
+def pf61_constant() -> int:
+    return int(lib().oracle_pf61_constant())
+
+
+def pf61(words) -> int:
+    words = np.ascontiguousarray(words, dtype=np.uint32)
+    return int(lib().oracle_pf61(_p(words) if words.size else None, words.size))
+
+
+def blake2b(data: bytes, outlen: int = 64) -> bytes:
+    buf = np.frombuffer(bytes(data) + b"\0", dtype=np.uint8)
+    out = np.zeros(outlen, np.uint8)
+    rc = lib().oracle_blake2b(_p(buf), len(data), _p(out), outlen)
+    if rc != 0:
+        raise ValueError("bad outlen")
+    return out.tobytes()
+
+
+def node(a: int, b: int) -> int:
+    return int(lib().oracle_node(a, b))
+
+
+def merkle_root(leaves) -> int:
+    leaves = np.ascontiguousarray(leaves, dtype=np.uint64)
+    return int(lib().oracle_merkle_root(_p(leaves), leaves.size))
+
+
+def image_bytes(n: int) -> int:
+    return int(lib().oracle_image_bytes(n))
+
+
+def image(step: int, w, m, v) -> bytes:
+    w = _f32(w); m = _f32(m); v = _f32(v)
+    n = w.size
+    out = np.empty(image_bytes(n), np.uint8)
+    rc = lib().oracle_image(step, n, _p(w), _p(m), _p(v), _p(out))
+    if rc != 0:
+        raise ValueError("n too large for the header")
+    return out.tobytes()
+
+
+def num_leaves(n: int) -> int:
+    return int(lib().oracle_num_leaves(n))
+
+
+def leaves(step: int, w, m, v) -> np.ndarray:
+    w = _f32(w); m = _f32(m); v = _f32(v)
+    n = w.size
+    out = np.empty(num_leaves(n), np.uint64)
+    rc = lib().oracle_leaves(step, n, _p(w), _p(m), _p(v), _p(out))
+    if rc != 0:
+        raise ValueError("n too large for the header")
+    return out
+
+
+def state_hash(step: int, w, m, v) -> int:
+    w = _f32(w); m = _f32(m); v = _f32(v)
+    r = C.c_uint64()
+    rc = lib().oracle_state_hash(step, w.size, _p(w), _p(m), _p(v), C.byref(r))
+    if rc != 0:
+        raise ValueError("n too large for the header")
+    return int(r.value)
+
+
+def step(grads, w, m, v, *, lr, beta1, beta2, eps, wd, clip, t, nodes=1, gpus_per_node=None):
+    """One oracle step on copies of (w, m, v).  Returns dict(w, m, v, norm, scale, root)."""
+    code, arrs, ptrs = _grad_arrays(grads)
+    R = len(arrs)
+    if gpus_per_node is None:
+        gpus_per_node = R // nodes
+    if nodes * gpus_per_node != R:
+        raise ValueError("nodes * gpus_per_node must equal the replica count")
+    w = _f32(w).copy(); m = _f32(m).copy(); v = _f32(v).copy()
+    n = w.size
+    nv, sv, root = C.c_float(), C.c_float(), C.c_uint64()
+    f = lambda x: float(np.float32(x))  # noqa: E731
+    rc = lib().oracle_step(C.cast(ptrs, C.c_void_p), code, nodes, gpus_per_node, n,
+                           _p(w), _p(m), _p(v), f(lr), f(beta1), f(beta2), f(eps), f(wd),
+                           f(clip), int(t), C.byref(nv), C.byref(sv), C.byref(root))
+    if rc == -2:
+        raise ValueError("topology breaks the canonical tree")
+    if rc != 0:
+        raise ValueError(f"oracle_step rc={rc}")
+    return dict(w=w, m=m, v=v, norm=np.float32(nv.value), scale=np.float32(sv.value),
+                root=int(root.value))

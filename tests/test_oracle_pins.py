@@ -1,0 +1,550 @@
+"""Pins for the CPU oracle: every oracle function checked against something other than
+itself -- hand-derived golden values, exact rationals, closed forms, invariants, Python's
+hashlib and bigint arithmetic, and torch's float64 AdamW.  CPU only.
+"""
+import hashlib
+import math
+import os
+import random
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import oracle as O
+from tests import exact as X
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+P61 = (1 << 61) - 1
+
+
+def f32(x):
+    return np.float32(x)
+
+
+def rand_f32(rng, size, lo_exp=-30, hi_exp=10):
+    """Random fp32 with random signs and exponents spread over [2^lo_exp, 2^hi_exp)."""
+    mant = rng.random(size) + 1.0
+    ex = rng.integers(lo_exp, hi_exp, size)
+    sign = rng.choice([-1.0, 1.0], size)
+    return (sign * mant * np.exp2(ex)).astype(np.float32)
+
+
+# ----------------------------------------------------------------------------------
+# Arithmetic model
+# ----------------------------------------------------------------------------------
+def test_no_contraction():
+    # (1 + 2^-12)^2 = 1 + 2^-11 + 2^-24 rounds (tie to even) to 1 + 2^-11; adding
+    # -(1 + 2^-11) gives 0 unfused, 2^-24 if fused into one rounding.
+    a = 1.0 + 2.0 ** -12
+    c = -(1.0 + 2.0 ** -11)
+    assert O.probe_mul_add(a, a, c) == 0.0
+
+
+def test_subnormals_kept():
+    assert O.probe_subnormals()
+
+
+def test_pairwise_add_is_correctly_rounded():
+    rng = np.random.default_rng(1)
+    xs = np.concatenate([rand_f32(rng, 400, -149, 120), rand_f32(rng, 200, -140, -120)])
+    for i in range(0, len(xs) - 1, 2):
+        a, b = xs[i], xs[i + 1]
+        assert X.bits(O.tree_sum(np.array([a, b], np.float32))) == X.bits(X.add(a, b))
+
+
+# ----------------------------------------------------------------------------------
+# Canonical tree (shape)
+# ----------------------------------------------------------------------------------
+def test_tree_shapes_match_golden():
+    shapes = X.load_shapes(os.path.join(GOLDEN, "tree_shapes.txt"))
+    rng = np.random.default_rng(2)
+    for L, expr in shapes.items():
+        for trial in range(40):
+            x = rand_f32(rng, L, -26, 2)
+            want = X.eval_shape(expr, list(x), X.add)
+            got = O.tree_sum(x)
+            assert X.bits(got) == X.bits(want), (L, expr, x)
+
+
+def test_tree_shape_is_not_a_left_fold():
+    # negative control: the golden shapes really are distinguishable from a left fold
+    rng = np.random.default_rng(3)
+    differs = 0
+    for trial in range(200):
+        x = rand_f32(rng, 7, -26, 2)
+        left = x[0]
+        for v in x[1:]:
+            left = X.add(left, v)
+        differs += X.bits(O.tree_sum(x)) != X.bits(left)
+    assert differs > 0
+
+
+def treefold(parts, combine):
+    """Push-based binary-carry fold of the Open-1B paper, App. A.1 (Algorithm 2),
+    with Result folding the leftover blocks largest-first, lower replica on the left."""
+    stack = []
+    for p in parts:
+        level = 0
+        while stack and stack[-1][0] == level:
+            _, lower = stack.pop()
+            p = combine(lower, p)
+            level += 1
+        stack.append((level, p))
+    acc = stack[0][1]
+    for _, p in stack[1:]:
+        acc = combine(acc, p)
+    return acc
+
+
+@pytest.mark.parametrize("L", [1, 2, 3, 4, 5, 6, 8, 9, 10, 12, 16, 17, 20, 24, 32, 33, 48, 64])
+def test_tree_equals_treefold_when_at_most_two_set_bits(L):
+    assert bin(L).count("1") <= 2
+    rng = np.random.default_rng(L)
+    for trial in range(20):
+        x = rand_f32(rng, L, -26, 2)
+        assert X.bits(O.tree_sum(x)) == X.bits(treefold(list(x), X.add))
+
+
+def test_tree_reading_differs_from_treefold_at_seven():
+    # documented reading: with three set bits the recursive split groups the
+    # remainder (4,5,6) together; the TreeFold left fold does not.
+    x = np.array([1, 0, 0, 0, 2.0 ** -24, 0, 2.0 ** -24], np.float32)
+    assert float(O.tree_sum(x)) == 1 + 2.0 ** -23
+    assert float(treefold(list(x), X.add)) == 1.0
+
+
+def _rounding_cases():
+    cases = {}
+    for line in open(os.path.join(GOLDEN, "rounding_cases.txt")):
+        if not line.strip() or line.startswith("#"):
+            continue
+        name, ins, want, _why = [s.strip() for s in line.split("|")]
+        cases[name] = (ins, X.parse_exact(want))
+    return cases
+
+
+def test_golden_replica_sums():
+    cases = _rounding_cases()
+    for name in ["sum3", "sum3b", "sum5", "sum7"]:
+        ins, want = cases[name]
+        vals = [float(X.parse_exact(t)) for t in ins.split(",")]
+        R = len(vals)
+        grads = [np.full(3, v, np.float32) for v in vals]
+        g = O.reduce(grads)
+        rho = X.f32(Fraction(1, R))
+        expect = X.mul(np.float32(float(want)), rho)
+        assert all(X.bits(x) == X.bits(expect) for x in g), (name, g, expect)
+
+
+def test_golden_chunk_sum():
+    ins, want = _rounding_cases()["chunk4096"]
+    g = np.zeros(4096, np.float32)
+    g[0] = 1.0
+    g[2048] = 2.0 ** -12
+    g[2049] = 2.0 ** -12
+    _, chunks = O.norm(g, with_chunks=True)
+    assert Fraction(float(chunks[0])) == want
+
+
+# ----------------------------------------------------------------------------------
+# Replica reduce
+# ----------------------------------------------------------------------------------
+def test_reduce_single_replica_is_identity():
+    rng = np.random.default_rng(4)
+    x = rand_f32(rng, 1000, -149, 127)
+    assert np.array_equal(O.reduce([x]).view(np.uint32), x.view(np.uint32))
+
+
+def test_reduce_bf16_widening_matches_torch():
+    rng = np.random.default_rng(5)
+    xb = torch.from_numpy(rand_f32(rng, 2000, -130, 120)).to(torch.bfloat16)
+    bits = xb.view(torch.int16).numpy().view(np.uint16)
+    g = O.reduce([bits])
+    assert np.array_equal(g.view(np.uint32), xb.float().numpy().view(np.uint32))
+
+
+@pytest.mark.parametrize("R", [2, 4, 8, 16, 32])
+def test_reduce_exact_integers(R):
+    # all partial sums of small integers are exact; 1/R is exact for power-of-two R
+    rng = np.random.default_rng(R)
+    G = [rng.integers(-2 ** 18, 2 ** 18, 500).astype(np.float32) for _ in range(R)]
+    g = O.reduce(G)
+    for i in range(500):
+        exact = sum(Fraction(int(G[r][i])) for r in range(R)) / R
+        assert Fraction(float(g[i])) == exact
+
+
+@pytest.mark.parametrize("R", [1, 2, 3, 5, 6, 7, 8, 9, 13])
+def test_reduce_within_error_bound(R):
+    rng = np.random.default_rng(100 + R)
+    G = [(rng.standard_normal(2000) * 1e-3).astype(np.float32) for _ in range(R)]
+    g = O.reduce(G).astype(np.float64)
+    S = np.sum([x.astype(np.float64) for x in G], axis=0)
+    A = np.sum([np.abs(x.astype(np.float64)) for x in G], axis=0)
+    depth = math.ceil(math.log2(R)) if R > 1 else 0
+    u = 2.0 ** -24
+    bound = (depth * u * A + u * np.abs(S)) / R * 1.0001 + 1e-45
+    assert np.all(np.abs(g - S / R) <= bound)
+
+
+def test_reduce_replica_order_matters():
+    rng = np.random.default_rng(6)
+    G = [(rng.standard_normal(20000) * 10.0 ** rng.integers(-4, 4)).astype(np.float32)
+         for _ in range(8)]
+    a = O.reduce(G)
+    b = O.reduce(G[::-1][:1] + G[1:7] + G[:1])
+    assert not np.array_equal(a.view(np.uint32), b.view(np.uint32))
+
+
+def test_topologies_equal_flat():
+    rng = np.random.default_rng(7)
+    G = [(rng.standard_normal(3000) * 1e-3).astype(np.float32) for _ in range(32)]
+    flat = O.reduce(G).view(np.uint32)
+    for nodes, gpn in [(1, 32), (4, 8), (8, 4), (32, 1), (2, 16), (16, 2)]:
+        assert np.array_equal(O.reduce_topology(G, nodes, gpn).view(np.uint32), flat)
+
+
+def test_topology_non_power_of_two_rejected():
+    G = [np.zeros(4, np.float32)] * 6
+    with pytest.raises(ValueError):
+        O.reduce_topology(G, 2, 3)
+    # one node of any size is the flat tree
+    assert np.array_equal(O.reduce_topology(G, 1, 6), O.reduce(G))
+
+
+# ----------------------------------------------------------------------------------
+# Norm and clip
+# ----------------------------------------------------------------------------------
+def test_norm_single_nonzero():
+    for val in [3.0, -0.75, 1e-3, 1.2345678, 2.0 ** -60]:
+        for n, pos in [(1, 0), (5000, 4097), (4096, 4095), (9000, 8191)]:
+            g = np.zeros(n, np.float32)
+            g[pos] = val
+            assert O.norm(g) == abs(np.float32(val))
+
+
+@pytest.mark.parametrize("j,e", [(0, 3), (2, 10), (5, 4), (10, 7), (11, 20)])
+def test_norm_constant_power_of_two(j, e):
+    # g_i = 2^-e on n = 4^j elements: norm = 2^(j-e) exactly
+    n = 4 ** j
+    g = np.full(n, 2.0 ** -e, np.float32)
+    assert float(O.norm(g)) == 2.0 ** (j - e)
+
+
+def test_norm_within_error_bound():
+    rng = np.random.default_rng(8)
+    for n in [1, 7, 4095, 4096, 4097, 50000, 300001]:
+        g = (rng.standard_normal(n) * 1e-3).astype(np.float32)
+        exact = math.sqrt(math.fsum(float(x) * float(x) for x in g))
+        c = (n + 4095) // 4096
+        levels = 12 + (math.ceil(math.log2(c)) if c > 1 else 0) + 2
+        assert abs(float(O.norm(g)) - exact) <= levels * 2.0 ** -24 * exact
+
+
+def test_norm_empty_is_zero():
+    assert O.norm(np.zeros(0, np.float32)) == 0.0
+
+
+def test_norm_short_last_chunk_is_zero_padding():
+    rng = np.random.default_rng(9)
+    g = (rng.standard_normal(4096 + 1000) * 1e-2).astype(np.float32)
+    padded = np.concatenate([g, np.zeros(3096, np.float32)])
+    assert O.norm(g) == O.norm(padded)
+
+
+def test_clip_scale():
+    assert O.clip_scale(2.0, 1.0) == 0.5
+    assert O.clip_scale(0.5, 1.0) == 1.0
+    assert O.clip_scale(1.0, 1.0) == 1.0
+    assert O.clip_scale(np.nan, 1.0) == 1.0
+    assert X.bits(O.clip_scale(3.0, 1.0)) == X.bits(X.f32(Fraction(1, 3)))
+
+
+# ----------------------------------------------------------------------------------
+# AdamW
+# ----------------------------------------------------------------------------------
+B1, B2 = np.float32(0.9), np.float32(0.999)
+LR, EPS, WD = np.float32(3e-4), np.float32(1e-8), np.float32(0.1)
+
+
+def test_bias_corrections_step_one_and_bound():
+    bc1, bc2 = O.bias_corrections(B1, B2, 1)
+    assert X.bits(bc1) == X.bits(X.f32(1 - X.F(B1)))
+    assert X.bits(bc2) == X.bits(X.f32(1 - X.F(B2)))
+    for t in [1, 2, 3, 5, 10, 100, 1000]:
+        bc1, bc2 = O.bias_corrections(B1, B2, t)
+        for b, bc in [(B1, bc1), (B2, bc2)]:
+            exact = 1 - float(b) ** t
+            assert abs(float(bc) - exact) <= (t + 1) * 2.0 ** -24 * max(1.0, float(b) ** t) + 2 ** -24 * exact
+
+
+def test_adamw_first_step_closed_form():
+    rng = np.random.default_rng(10)
+    n = 3000
+    g = (rng.standard_normal(n) * 1e-2).astype(np.float32)
+    w = (rng.standard_normal(n) * 0.02).astype(np.float32)
+    z = np.zeros(n, np.float32)
+    bc1, bc2 = O.bias_corrections(B1, B2, 1)
+    w1, m1, v1 = O.adamw(w, z, z, g, 1.0, LR, B1, B2, EPS, WD, bc1, bc2)
+    om1 = X.f32(1 - X.F(B1))
+    om2 = X.f32(1 - X.F(B2))
+    for i in range(0, n, 7):
+        assert X.bits(m1[i]) == X.bits(X.mul(om1, g[i])) or (g[i] == 0 and m1[i] == 0)
+        assert X.bits(v1[i]) == X.bits(X.mul(om2, X.mul(g[i], g[i])))
+    # |g| >> eps: the first update is lr * sign(g) up to a few ulps
+    delta = float(X.f32(1 - X.F(X.mul(LR, WD))))
+    g64 = g.astype(np.float64)
+    approx = w.astype(np.float64) * delta - float(LR) * g64 / (np.abs(g64) + float(EPS))
+    assert np.all(np.abs(w1 - approx) <= 4 * 2.0 ** -24 * (np.abs(approx) + float(LR)))
+
+
+def test_adamw_no_lr_no_decay_keeps_w():
+    rng = np.random.default_rng(11)
+    n = 1000
+    g, w = (rng.standard_normal((2, n)) * 1e-2).astype(np.float32)
+    m = (rng.standard_normal(n) * 1e-3).astype(np.float32)
+    v = np.abs(rng.standard_normal(n) * 1e-6).astype(np.float32)
+    bc1, bc2 = O.bias_corrections(B1, B2, 4)
+    w1, _, _ = O.adamw(w, m, v, g, 1.0, 0.0, B1, B2, EPS, 0.0, bc1, bc2)
+    assert np.array_equal(w1.view(np.uint32), w.view(np.uint32))
+
+
+def test_adamw_zero_gradient_only_decays():
+    rng = np.random.default_rng(12)
+    n = 1000
+    w = (rng.standard_normal(n) * 0.02).astype(np.float32)
+    z = np.zeros(n, np.float32)
+    bc1, bc2 = O.bias_corrections(B1, B2, 1)
+    w1, m1, v1 = O.adamw(w, z, z, z, 1.0, LR, B1, B2, EPS, WD, bc1, bc2)
+    delta = X.f32(1 - X.F(X.mul(LR, WD)))
+    assert all(X.bits(w1[i]) == X.bits(X.mul(w[i], delta)) for i in range(n))
+    assert not m1.any() and not v1.any()
+
+
+def test_adamw_matches_torch_float64_over_steps():
+    rng = np.random.default_rng(13)
+    n, T = 4000, 6
+    w0 = (rng.standard_normal(n) * 0.02).astype(np.float32)
+    grads = [(rng.standard_normal(n) * 1e-3 * (1 + 9 * (t % 2))).astype(np.float32)
+             for t in range(T)]
+    # oracle
+    w, m, v = w0.copy(), np.zeros(n, np.float32), np.zeros(n, np.float32)
+    for t in range(1, T + 1):
+        bc1, bc2 = O.bias_corrections(B1, B2, t)
+        w, m, v = O.adamw(w, m, v, grads[t - 1], 1.0, LR, B1, B2, EPS, WD, bc1, bc2)
+    # torch float64 AdamW with the same fp32-valued hyperparameters
+    p = torch.nn.Parameter(torch.from_numpy(w0.astype(np.float64)))
+    opt = torch.optim.AdamW([p], lr=float(LR), betas=(float(B1), float(B2)), eps=float(EPS),
+                            weight_decay=float(WD), foreach=False)
+    # error model: fp32 rounding (u per op) relative to the MAGNITUDES of the terms, since
+    # beta1*m + (1-beta1)*g can cancel.  M bounds the m terms; the update u_t inherits
+    # m's absolute error divided by the denominator, plus a few relative roundings.
+    u = 2.0 ** -24
+    b1, b2, lr = float(B1), float(B2), float(LR)
+    M = np.zeros(n)
+    tol_w = np.zeros(n)
+    for t in range(1, T + 1):
+        g64 = grads[t - 1].astype(np.float64)
+        M = b1 * M + (1 - b1) * np.abs(g64)
+        p.grad = torch.from_numpy(g64)
+        opt.step()
+        st = opt.state[p]
+        mt, vt = st["exp_avg"].numpy(), st["exp_avg_sq"].numpy()
+        bc1t, bc2t = 1 - b1 ** t, 1 - b2 ** t
+        den = np.sqrt(vt / bc2t) + float(EPS)
+        ut = (mt / bc1t) / den
+        # fp32 bias corrections 1 - beta^t (repeated fp32 products) cancel: their
+        # relative error is about t*u*beta^t / (1 - beta^t), large for beta2 = 0.999
+        rel_bc1 = (2 * t * u * b1 ** t) / bc1t + u
+        rel_bc2 = (2 * t * u * b2 ** t) / bc2t + u
+        du = (4 * t * u * M / bc1t) / den + ((8 + 2 * t) * u + rel_bc1 + rel_bc2) * np.abs(ut)
+        tol_w = tol_w * (1 - lr * float(WD)) + lr * du + 3 * u * (np.abs(p.detach().numpy()) + lr * np.abs(ut))
+    wt = p.detach().numpy()
+    st = opt.state[p]
+    mt = st["exp_avg"].numpy()
+    vt = st["exp_avg_sq"].numpy()
+    assert np.all(np.abs(m - mt) <= 4 * T * u * M)
+    assert np.all(np.abs(v - vt) <= 4 * T * u * np.abs(vt) + 1e-37)
+    assert np.all(np.abs(w - wt) <= tol_w)
+    # the tolerance is tight enough to catch a dropped term: skipping the decay breaks it
+    w2 = w0.copy(); m2 = np.zeros(n, np.float32); v2 = np.zeros(n, np.float32)
+    for t in range(1, T + 1):
+        bc1, bc2 = O.bias_corrections(B1, B2, t)
+        w2, m2, v2 = O.adamw(w2, m2, v2, grads[t - 1], 1.0, LR, B1, B2, EPS, 0.0, bc1, bc2)
+    assert not np.all(np.abs(w2 - wt) <= tol_w)
+
+
+# ----------------------------------------------------------------------------------
+# PF61 leaf fingerprint
+# ----------------------------------------------------------------------------------
+def test_pf61_constant_definition():
+    K = (math.isqrt(5 * 2 ** 122) - 2 ** 61) >> 1
+    assert O.pf61_constant() == K
+    assert 0 < K < P61
+
+
+def test_pf61_empty_and_units():
+    K = O.pf61_constant()
+    assert O.pf61([]) == 0
+    assert O.pf61([0]) == 1
+    assert O.pf61([1]) == (1 + K) % P61
+    for W in [1, 2, 5, 4096]:
+        for i in sorted({0, min(1, W - 1), W // 2, W - 1}):
+            x = np.zeros(W, np.uint32)
+            x[i] = 1
+            assert O.pf61(x) == (W + pow(K, i + 1, P61)) % P61
+
+
+def test_pf61_brute_force_tiny():
+    K = O.pf61_constant()
+    rng = random.Random(14)
+    for W in range(0, 9):
+        for trial in range(30):
+            x = [rng.choice([0, 1, 0xFFFFFFFF, rng.getrandbits(32)]) for _ in range(W)]
+            want = (W + sum(xi * pow(K, i + 1, P61) for i, xi in enumerate(x))) % P61
+            assert O.pf61(x) == want
+
+
+def test_pf61_linear_and_shift():
+    K = O.pf61_constant()
+    rng = np.random.default_rng(15)
+    for W in [3, 100, 4096]:
+        x = rng.integers(0, 2 ** 31, W, dtype=np.uint64).astype(np.uint32)
+        y = rng.integers(0, 2 ** 31, W, dtype=np.uint64).astype(np.uint32)
+        fx, fy, fxy = O.pf61(x), O.pf61(y), O.pf61(x + y)
+        assert (fxy - W) % P61 == ((fx - W) + (fy - W)) % P61
+        shifted = np.concatenate([np.zeros(1, np.uint32), x])
+        assert (O.pf61(shifted) - (W + 1)) % P61 == (K * (fx - W)) % P61
+
+
+def test_pf61_single_word_change_always_changes_leaf():
+    rng = np.random.default_rng(16)
+    x = rng.integers(0, 2 ** 32, 4096, dtype=np.uint64).astype(np.uint32)
+    base = O.pf61(x)
+    for i in [0, 1, 2047, 4095]:
+        for delta in [1, 1 << 31]:
+            y = x.copy()
+            y[i] ^= np.uint32(delta)
+            assert O.pf61(y) != base
+
+
+# ----------------------------------------------------------------------------------
+# BLAKE2b nodes and the Merkle root
+# ----------------------------------------------------------------------------------
+@pytest.mark.parametrize("length", [0, 1, 3, 16, 64, 127, 128, 129, 255, 256, 257, 1000])
+@pytest.mark.parametrize("outlen", [1, 8, 20, 32, 64])
+def test_blake2b_matches_hashlib(length, outlen):
+    data = bytes((i * 131 + length) & 0xFF for i in range(length))
+    assert O.blake2b(data, outlen) == hashlib.blake2b(data, digest_size=outlen).digest()
+
+
+def hl_node(a, b):
+    d = hashlib.blake2b(a.to_bytes(8, "little") + b.to_bytes(8, "little"), digest_size=8)
+    return int.from_bytes(d.digest(), "little")
+
+
+def test_node_matches_hashlib():
+    rng = random.Random(17)
+    for _ in range(200):
+        a, b = rng.getrandbits(64), rng.getrandbits(64)
+        assert O.node(a, b) == hl_node(a, b)
+    assert O.node(1, 2) != O.node(2, 1)
+
+
+def test_merkle_shapes_match_golden():
+    shapes = X.load_shapes(os.path.join(GOLDEN, "tree_shapes.txt"))
+    rng = random.Random(18)
+    for L, expr in shapes.items():
+        leaves = [rng.getrandbits(61) for _ in range(L)]
+        want = X.eval_shape(expr, leaves, hl_node)
+        assert O.merkle_root(np.array(leaves, np.uint64)) == want
+
+
+# ----------------------------------------------------------------------------------
+# Checkpoint image and state hash
+# ----------------------------------------------------------------------------------
+def test_image_size_golden():
+    for line in open(os.path.join(GOLDEN, "checkpoint_sizes.txt")):
+        if not line.strip() or line.startswith("#"):
+            continue
+        n, b, mb, mib = [int(s) for s in line.split("|")]
+        assert O.image_bytes(n) == b == 8 + 12 * n
+        assert round(b / 1e6) == mb
+        assert math.ceil(b / 2 ** 20) == mib
+
+
+def test_image_layout():
+    rng = np.random.default_rng(19)
+    n = 5000
+    w, m, v = (rng.standard_normal((3, n))).astype(np.float32)
+    img = O.image(7, w, m, v)
+    assert len(img) == 8 + 12 * n
+    assert int.from_bytes(img[0:4], "little") == 7
+    assert int.from_bytes(img[4:8], "little") == n
+    assert img[8:] == w.astype("<f4").tobytes() + m.astype("<f4").tobytes() + v.astype("<f4").tobytes()
+    neg = O.image(-3, w[:1], m[:1], v[:1])
+    assert int.from_bytes(neg[0:4], "little", signed=True) == -3
+
+
+def test_state_hash_over_image_words():
+    # leaves = header words, then 4096-word chunks of w, m, v, read from the image bytes
+    rng = np.random.default_rng(20)
+    for n in [0, 1, 4095, 4096, 4097, 3 * 4096 + 17]:
+        w, m, v = (rng.standard_normal((3, n))).astype(np.float32)
+        img = np.frombuffer(O.image(11, w, m, v), dtype="<u4")
+        leaves = [O.pf61(img[0:2])]
+        for a in range(3):
+            arr = img[2 + a * n: 2 + (a + 1) * n]
+            for k in range(0, n, 4096):
+                leaves.append(O.pf61(arr[k:k + 4096]))
+        assert len(leaves) == O.num_leaves(n)
+        want = leaves[0] if len(leaves) == 1 else None
+        root = O.state_hash(11, w, m, v)
+        assert root == O.merkle_root(np.array(leaves, np.uint64))
+        if want is not None:
+            assert root == want
+
+
+def test_state_hash_bit_flips():
+    rng = np.random.default_rng(21)
+    n = 3 * 4096 + 5
+    w, m, v = (rng.standard_normal((3, n))).astype(np.float32)
+    base = O.state_hash(1, w, m, v)
+    assert O.state_hash(2, w, m, v) != base
+    for arr_i in range(3):
+        for pos in [0, 4096, n - 1]:
+            for bit in [0, 31]:
+                arrs = [w.copy(), m.copy(), v.copy()]
+                arrs[arr_i].view(np.uint32)[pos] ^= np.uint32(1 << bit)
+                assert O.state_hash(1, *arrs) != base
+
+
+# ----------------------------------------------------------------------------------
+# Whole step against torch float64 (clip + AdamW) within rounding error
+# ----------------------------------------------------------------------------------
+def test_step_matches_torch_float64():
+    rng = np.random.default_rng(22)
+    n, R, T = 9000, 4, 3
+    w0 = (rng.standard_normal(n) * 0.02).astype(np.float32)
+    Gs = [[(rng.standard_normal(n) * 0.05).astype(np.float32) for _ in range(R)]
+          for _ in range(T)]
+    w, m, v = w0, np.zeros(n, np.float32), np.zeros(n, np.float32)
+    norms = []
+    for t in range(1, T + 1):
+        out = O.step(Gs[t - 1], w, m, v, lr=LR, beta1=B1, beta2=B2, eps=EPS, wd=WD, clip=1.0, t=t)
+        w, m, v = out["w"], out["m"], out["v"]
+        norms.append(float(out["norm"]))
+    assert min(norms) > 1.0  # the clip is exercised
+    p = torch.nn.Parameter(torch.from_numpy(w0.astype(np.float64)))
+    opt = torch.optim.AdamW([p], lr=float(LR), betas=(float(B1), float(B2)), eps=float(EPS),
+                            weight_decay=float(WD), foreach=False)
+    for t in range(T):
+        gm = np.mean([x.astype(np.float64) for x in Gs[t]], axis=0)
+        nrm = np.sqrt(np.sum(gm * gm))
+        assert abs(nrm - norms[t]) <= 1e-6 * nrm
+        p.grad = torch.from_numpy(gm * min(1.0, 1.0 / nrm))
+        opt.step()
+    wt = p.detach().numpy()
+    assert np.all(np.abs(w - wt) <= 64 * T * 2.0 ** -24 * (np.abs(wt) + float(LR)))
