@@ -1,0 +1,452 @@
+#!/usr/bin/env python3
+"""Benchmark of the bitwise-reproducible optimizer step on GB300.
+
+One step = replica reduce (R gradient buffers, canonical tree, reciprocal multiply) +
+global norm + clip + fused AdamW + Merkle state hash, through the C ABI.  Default workload:
+n = 1,200,000,000 fp32 parameters, R = 8 fp32 replica gradients N(0, 1e-4) with per-4M-
+segment log-uniform scales, hyperparameters lr 3e-4, betas 0.9/0.999, eps 1e-8, wd 0.1,
+clip 1.0.  Inputs are synthetic (seeded) and resident in HBM for the device-timed value;
+the working set (~77 GB moved per step) is far larger than the 129 MB L2, so no flush is
+needed between steps.
+
+Prints ONE JSON line (rank 0).  Metric: parameters per second per bit-exact step, with
+the step's algorithmic HBM bytes R*b_g*n + 24n per step as GB/s.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the CPU oracle (the plain single-threaded restatement of the same
+step, the test suite's reference) on the host cores, on a bounded sample of the workload.
+Under torchrun with N > 1 every rank runs an independent replica of the whole step (the
+single-GPU path does not exchange data); value is the sum over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "params/s and HBM GB/s (% of roofline) per bit-exact reduce+clip+AdamW+hash step"
+UNIT = "params/s"
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCES = ["bitwise_reproducible_step_gb300/csrc/k_reduce.cu",
+                  "bitwise_reproducible_step_gb300/csrc/k_adamw.cu",
+                  "bitwise_reproducible_step_gb300/csrc/common.cuh"]
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+# ------------------------------------------------------------------------------------
+# distributed plumbing (one process per GPU; independent replicas)
+# ------------------------------------------------------------------------------------
+def dist_init(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------------------------
+# clocks during the timed region
+# ------------------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+                power.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------------------------
+# peaks, profiles
+# ------------------------------------------------------------------------------------
+def hbm_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs, STREAM-style copy)"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback (6.8 TB/s, one earlier GB300 copy measurement)"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        h.update(open(os.path.join(ROOT, rel), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel: str):
+    """Per-launch DRAM bytes recorded from an ncu capture in profiles/, if the kernel
+    sources are unchanged since (the summary stores their hash); else None."""
+    src_hash = kernel_source_hash()
+    pdir = os.path.join(ROOT, "profiles")
+    if not os.path.isdir(pdir):
+        return None
+    for fn in sorted(os.listdir(pdir)):
+        if not fn.endswith(".md"):
+            continue
+        for line in open(os.path.join(pdir, fn)):
+            m = re.match(r"\s*traffic_per_launch:\s*kernel=(\S+)\s+bytes=(\d+)\s+"
+                         r"source_hash=(\S+)", line)
+            if m and m.group(1) == kernel and m.group(3) == src_hash:
+                return int(m.group(2))
+    return None
+
+
+# ------------------------------------------------------------------------------------
+# our arm
+# ------------------------------------------------------------------------------------
+def run_ours(args, rank, world, local):
+    from bitwise_reproducible_step_gb300 import inputs as I
+    from bitwise_reproducible_step_gb300 import repstep as rs
+
+    wl = I.WORKLOADS[args.workload]
+    n, R = wl.n, wl.R
+    dev = torch.device("cuda", local)
+    gdt = torch.bfloat16 if wl.grad_dtype == "bf16" else torch.float32
+    b_g = 2 if wl.grad_dtype == "bf16" else 4
+    hpv = I.default_hparams()
+
+    log(f"[rank {rank}] generating {wl.name}: n={n:,} R={R} on {dev}")
+    grads = [I.gen_grad(wl, 1, r, device=dev) for r in range(R)]
+    w, m, v = I.gen_state(wl, device=dev)
+    ctx = rs.Repstep(n, grad_dtype=gdt, device=dev)
+    norm = torch.empty(1, dtype=torch.float32, device=dev)
+    root = torch.empty(1, dtype=torch.int64, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def hp(t):
+        return rs.hparams(lr=hpv["lr"], beta1=hpv["beta1"], beta2=hpv["beta2"], eps=hpv["eps"],
+                          weight_decay=hpv["wd"], clip=hpv["clip"], t=t)
+
+    t_step = [0]
+
+    def one_step():
+        t_step[0] += 1
+        ctx.step(grads, w, m, v, hp(t_step[0]), step=t_step[0], norm_out=norm, root_out=root)
+
+    # warm-up
+    for _ in range(args.warmup):
+        one_step()
+    ctx.sync()
+
+    # ---- timed region: K whole steps, inputs resident in HBM ------------------------
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    launches0 = ctx.launch_count()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        one_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clk = clocks.stop()
+    launches = ctx.launch_count() - launches0
+    ms_local = e0.elapsed_time(e1) / args.steps
+    ms = max_over_ranks(ms_local, world)
+    flags = ctx.sync()
+
+    # ---- per-kernel times (same calls, events between them, same stream) ------------
+    kt = {"reduce": [], "clip": [], "adamw": [], "root": []}
+    reps = max(3, min(args.steps, 20))
+    for _ in range(reps):
+        t_step[0] += 1
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+        h = hp(t_step[0])
+        ev[0].record(stream)
+        ctx.reduce(grads)
+        ev[1].record(stream)
+        ctx.clip(h.clip, norm_out=norm)
+        ev[2].record(stream)
+        ctx.adamw(w, m, v, h)
+        ev[3].record(stream)
+        ctx.root(t_step[0], root_out=root)
+        ev[4].record(stream)
+        torch.cuda.synchronize(dev)
+        for i, k in enumerate(kt):
+            kt[k].append(ev[i].elapsed_time(ev[i + 1]))
+    kms = {k: statistics.mean(v_) for k, v_ in kt.items()}
+    ctx.sync()
+
+    peak, peak_src = hbm_peak()
+    alg_step = (R * b_g + 24) * n
+    alg = {"reduce": (R * b_g + 4) * n, "adamw": 28 * n}
+    dom = max(("reduce", "adamw"), key=lambda k: kms[k])
+    achieved = alg[dom] / (kms[dom] * 1e-3) / 1e9
+    kname = {"reduce": "k_reduce", "adamw": "k_adamw"}[dom]
+    traffic = profiled_traffic(kname)
+
+    # ---- end to end: grads from pinned host memory each step, norm+root read back ----
+    e2e = run_e2e(args, ctx, wl, grads, w, m, v, hp, t_step, dev, R, b_g, n)
+
+    del grads
+    torch.cuda.empty_cache()
+    cpu = None
+    if rank == 0 and not args.skip_cpu_baseline:
+        cpu = cpu_baseline(wl, n, R, dev, args.cpu_seconds)
+
+    value = n / (ms * 1e-3) * world
+    step_gbs = alg_step / (ms * 1e-3) / 1e9
+    res = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": wl.name, "n_params": n, "replicas": R,
+                   "grad_dtype": wl.grad_dtype, "grad_dist": f"{wl.grad} sigma={wl.sigma}",
+                   "bytes_alg_per_step": alg_step,
+                   "l2": "inputs larger than L2 (no flush needed): "
+                         f"{(R * b_g + 32) * n / 1e9:.1f} GB moved per step",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "launch": "persistent grid (SM count x resident CTAs), 256/512 threads"},
+        "hbm_gbs_step": step_gbs,
+        "roofline_step": {"bound": "hbm", "achieved": step_gbs, "peak": peak,
+                          "unit": "GB/s", "frac": step_gbs / peak, "peak_source": peak_src,
+                          "bytes": "R*b_g*n + 24n algorithmic bytes per step"},
+        "roofline": {"bound": "hbm", "kernel": kname, "achieved": achieved, "peak": peak,
+                     "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
+                     "alg_bytes_per_launch": alg[dom], "avg_launch_ms": kms[dom],
+                     "peak_source": peak_src},
+        "kernel_ms": kms,
+        "clocks": clk,
+        "gpu_launches": launches,
+        "device_flags": flags,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+    }
+    return res
+
+
+def run_e2e(args, ctx, wl, grads, w, m, v, hp, t_step, dev, R, b_g, n):
+    """Same step through the public API with the gradients copied from pinned host memory
+    every step and the pre-clip norm and Merkle root read back to the host."""
+    need = R * b_g * n
+    try:
+        avail = int(re.search(r"MemAvailable:\s+(\d+)", open("/proc/meminfo").read()).group(1)) * 1024
+    except (OSError, AttributeError):
+        avail = 0
+    if avail and need > 0.6 * avail:
+        return {"value": None, "unit": UNIT, "skipped": f"pinned host gradients need {need / 1e9:.1f} GB, "
+                f"host has {avail / 1e9:.1f} GB available"}
+    host = [torch.empty(g.shape, dtype=g.dtype, pin_memory=True) for g in grads]
+    for h, g in zip(host, grads):
+        h.copy_(g)
+    out_h = torch.empty(2, dtype=torch.int64, pin_memory=True)
+    nr = torch.empty(1, dtype=torch.float32, device=dev)
+    rt = torch.empty(1, dtype=torch.int64, device=dev)
+    steps = max(2, min(args.e2e_steps, args.steps))
+    stream = torch.cuda.current_stream(dev)
+
+    def one():
+        for h, g in zip(host, grads):
+            g.copy_(h, non_blocking=True)
+        t_step[0] += 1
+        ctx.step(grads, w, m, v, hp(t_step[0]), step=t_step[0], norm_out=nr, root_out=rt)
+        out_h[0:1].view(torch.float32)[0:1].copy_(nr, non_blocking=True)
+        out_h[1:2].copy_(rt, non_blocking=True)
+        stream.synchronize()
+        return float(out_h[0:1].view(torch.float32)[0])
+
+    one()
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        one()
+    dt = (time.perf_counter() - t0) / steps
+    del host
+    return {"value": n / dt, "unit": UNIT, "ms_per_step": dt * 1e3, "steps": steps,
+            "h2d_bytes_per_step": need, "d2h_bytes_per_step": 8 + 4}
+
+
+def cpu_baseline(wl, n, R, dev, seconds):
+    """The oracle (plain C, one thread) on the host cores, on the first n_s elements of the
+    bench's own workload; repeated until about `seconds` of CPU work."""
+    from bitwise_reproducible_step_gb300 import inputs as I
+    from oracle import oracle as O
+
+    n_s = min(n, 1 << 24)
+    grads = [I.to_numpy(I.gen_grad(wl, 1, r, device=dev)[:n_s]) for r in range(R)]
+    w, m, v = (t[:n_s].cpu().numpy() for t in I.gen_state(wl, device=dev))
+    hpv = I.default_hparams()
+    done, t0, reps = 0, time.perf_counter(), 0
+    while True:
+        out = O.step(grads, w, m, v, lr=hpv["lr"], beta1=hpv["beta1"], beta2=hpv["beta2"],
+                     eps=hpv["eps"], wd=hpv["wd"], clip=hpv["clip"], t=reps + 1)
+        w, m, v = out["w"], out["m"], out["v"]
+        done += n_s
+        reps += 1
+        if time.perf_counter() - t0 > seconds or reps >= 8:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": done / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"first {n_s:,} of {n:,} params of the same workload, R={R}, "
+                      f"{reps} full steps (reduce+norm+clip+AdamW+hash) in {dt:.1f} s",
+            "host_cpu": _cpu_model(), "host_nproc": os.cpu_count()}
+
+
+def _cpu_model():
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True).stdout
+        m = re.search(r"Model name:\s*(.+)", out)
+        return m.group(1).strip() if m else None
+    except OSError:
+        return None
+
+
+# ------------------------------------------------------------------------------------
+# reference arm: the oracle on host cores
+# ------------------------------------------------------------------------------------
+def run_reference(args, rank, world, local):
+    from bitwise_reproducible_step_gb300 import inputs as I
+    from oracle import oracle as O
+
+    wl = I.WORKLOADS[args.workload]
+    n, R = wl.n, wl.R
+    n_s = min(n, 1 << 22)
+    hpv = I.default_hparams()
+    grads = [I.to_numpy(I.gen_grad(wl, 1, r, n=n_s, device="cpu")) for r in range(R)]
+    w, m, v = (t.numpy() for t in I.gen_state(wl, n=n_s, device="cpu"))
+
+    def one(t):
+        nonlocal w, m, v
+        out = O.step(grads, w, m, v, lr=hpv["lr"], beta1=hpv["beta1"], beta2=hpv["beta2"],
+                     eps=hpv["eps"], wd=hpv["wd"], clip=hpv["clip"], t=t)
+        w, m, v = out["w"], out["m"], out["v"]
+
+    for t in range(1, args.warmup + 1):
+        one(t)
+    t0 = time.perf_counter()
+    for t in range(args.warmup + 1, args.warmup + args.steps + 1):
+        one(t)
+    dt = (time.perf_counter() - t0) / args.steps
+    value = n_s / dt
+    sample = f"first {n_s:,} of {n:,} params per step (same workload, R={R}), seeded on the CPU"
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": {"workload": wl.name, "n_params": n, "replicas": R,
+                       "grad_dtype": wl.grad_dtype, "sample_params_per_step": n_s},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="flat1200m_r8_segscale")
+    ap.add_argument("--e2e-steps", type=int, default=4)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--skip-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    if args.impl == "reference":
+        world = int(os.environ.get("WORLD_SIZE", "1"))
+        rank = int(os.environ.get("RANK", "0"))
+        if rank != 0:
+            return
+        args.steps = min(args.steps, 5)
+        print(json.dumps(run_reference(args, 0, world, 0)), flush=True)
+        return
+
+    rank, world, local = dist_init(args.gpus)
+    res = run_ours(args, rank, world, local)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

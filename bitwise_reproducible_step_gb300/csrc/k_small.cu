@@ -1,0 +1,246 @@
+// k_small.cu -- the short kernels of the step: PF61 power table, global norm and clip
+// scale, Merkle levels, image header, and the fix-ups for chunks cut by range boundaries.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace repstep {
+
+namespace {
+
+// K^(i+1) mod p for i < 4096, by square-and-multiply.
+__global__ void k_init_powers(uint64_t *powers)
+{
+    const uint32_t i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= kChunk) return;
+    uint32_t e = i + 1;
+    uint64_t r = 1, b = kK61;
+    while (e) {
+        if (e & 1u) r = pf_mul(r, b);
+        b = pf_mul(b, b);
+        e >>= 1;
+    }
+    powers[i] = r;
+}
+
+struct ChunkList {
+    uint64_t idx[kFixMax];
+    int count;
+};
+
+// Sum of squares of whole chunks of g, for chunks a range boundary cut during reduce.
+// 256 threads per chunk, the same fixed tree as the reduce kernel (common.cuh).
+__global__ void __launch_bounds__(256) k_chunk_fix(const float *g, uint64_t n, float *chunk_sq,
+                                                   const ChunkList L)
+{
+    __shared__ float red[4 * 8];
+    const uint64_t k = L.idx[blockIdx.x];
+    const int tid = threadIdx.x;
+    float part[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        float q[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint64_t e = k * kChunk + uint64_t(j) * 1024 + 4u * tid + i;
+            const float x = e < n ? g[e] : 0.0f;
+            q[i] = e < n ? __fmul_rn(x, x) : 0.0f;
+        }
+        part[j] = sum4(q[0], q[1], q[2], q[3]);
+    }
+    const float total = chunk_tree<256, 4>(part, red, tid, [] { __syncthreads(); });
+    if (tid == 0) chunk_sq[k] = total;
+}
+
+// Leaf digests of whole chunks of w, m, v, for chunks a range boundary cut during AdamW.
+__global__ void __launch_bounds__(256) k_leaf_fix(const float *w, const float *m, const float *v,
+                                                  uint64_t n, uint64_t c, uint64_t *leaves,
+                                                  const uint64_t *powers, const ChunkList L)
+{
+    __shared__ uint64_t pb[3][256];
+    const uint64_t k = L.idx[blockIdx.x];
+    const int tid = threadIdx.x;
+    const float *arr[3] = {w, m, v};
+    uint32_t acc[3][4];
+#pragma unroll
+    for (int s = 0; s < 3; ++s)
+#pragma unroll
+        for (int t = 0; t < 4; ++t) acc[s][t] = 0u;
+    for (uint32_t p = tid; p < kChunk; p += 256) {
+        const uint64_t e = k * kChunk + p;
+        if (e >= n) break;
+        const uint64_t pk = powers[p];
+        const uint32_t p0 = uint32_t(pk), p1 = uint32_t(pk >> 32);
+#pragma unroll
+        for (int s = 0; s < 3; ++s) pf_mac(acc[s], __float_as_uint(arr[s][e]), p0, p1);
+    }
+#pragma unroll
+    for (int s = 0; s < 3; ++s) pb[s][tid] = pf_fold128(acc[s]);
+    __syncthreads();
+    const int warp = tid >> 5, lane = tid & 31;
+    if (warp < 3) {
+        uint64_t sum = 0;
+        for (int t = lane; t < 256; t += 32) sum = pf_add(sum, pb[warp][t]);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1)
+            sum = pf_add(sum, __shfl_xor_sync(0xffffffffu, sum, off));
+        if (lane == 0) {
+            const uint64_t c0 = k * kChunk;
+            const uint64_t c1 = c0 + kChunk < n ? c0 + kChunk : n;
+            leaves[1 + uint64_t(warp) * c + k] = pf_add(c1 - c0, sum);
+        }
+    }
+}
+
+// Global norm.  Block b reduces in[4096 b .. 4096 b + 4096) (zero past `count`) in the
+// fixed tree; with final_pass the single block's total S gives norm = sqrt(S) and the
+// clip scale, otherwise it writes the block partial.  Zero padding leaves the canonical
+// tree of non-negative sums unchanged, so two passes equal one tree over all chunks.
+__global__ void __launch_bounds__(256) k_norm(const float *in, uint64_t count, float *out,
+                                              Scalars *sc, int final_pass, float clip,
+                                              float *norm_out, float *scale_out)
+{
+    __shared__ float red[4 * 8];
+    const int tid = threadIdx.x;
+    const uint64_t base = uint64_t(blockIdx.x) * kChunk;
+    float part[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        float q[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint64_t e = base + uint64_t(j) * 1024 + 4u * tid + i;
+            q[i] = e < count ? in[e] : 0.0f;
+        }
+        part[j] = sum4(q[0], q[1], q[2], q[3]);
+    }
+    const float S = chunk_tree<256, 4>(part, red, tid, [] { __syncthreads(); });
+    if (tid != 0) return;
+    if (!final_pass) {
+        out[blockIdx.x] = S;
+        return;
+    }
+    const float norm = __fsqrt_rn(S);
+    // "OPEN-1B", §3.2: clipped to a global l2 norm (reading: scale = clip / norm when the
+    // norm exceeds the threshold, else 1; a NaN norm compares false)
+    const float scale = norm > clip ? __fdiv_rn(clip, norm) : 1.0f;
+    const bool finite = isfinite(norm);
+    sc->norm = norm;
+    sc->scale = scale;
+    sc->flags = (sc->flags & ~kFlagNonfinite) | (finite ? 0u : kFlagNonfinite);
+    if (norm_out) *norm_out = norm;
+    if (scale_out) *scale_out = scale;
+}
+
+// One Merkle block: the canonical tree over up to 4096 consecutive digests, level by level
+// (pair neighbours, carry an odd last node up unchanged), which is the same tree as the
+// recursive split T = T(first 2^k) + T(rest).  Aligned 4096-blocks are complete subtrees of
+// the whole tree, so a second pass over the block roots finishes it.  Block 0 of the leaf
+// pass computes the header leaf PF61({step, n}) itself.
+__global__ void __launch_bounds__(256) k_merkle(const uint64_t *in, uint64_t count, uint64_t *out,
+                                                int header_mode, uint64_t *leaves_rw,
+                                                uint32_t step, uint32_t n32,
+                                                const uint64_t *powers, Scalars *sc,
+                                                uint64_t *root_out, int final_pass)
+{
+    extern __shared__ uint64_t mk[];
+    uint64_t *buf0 = mk, *buf1 = mk + kChunk;
+    const int tid = threadIdx.x;
+    const uint64_t base = uint64_t(blockIdx.x) * kChunk;
+    uint32_t cnt = uint32_t(count - base < kChunk ? count - base : kChunk);
+    for (uint32_t i = tid; i < cnt; i += blockDim.x) buf0[i] = in[base + i];
+    __syncthreads();
+    if (header_mode && blockIdx.x == 0 && tid == 0) {
+        const uint64_t h = pf_add(pf_add(2, pf_mul(step, powers[0])), pf_mul(n32, powers[1]));
+        buf0[0] = h;
+        leaves_rw[0] = h;
+    }
+    __syncthreads();
+    while (cnt > 1) {
+        const uint32_t half = cnt >> 1;
+        for (uint32_t i = tid; i < half; i += blockDim.x) buf1[i] = b2_node(buf0[2 * i], buf0[2 * i + 1]);
+        if ((cnt & 1u) && tid == 0) buf1[half] = buf0[cnt - 1];
+        __syncthreads();
+        uint64_t *t = buf0;
+        buf0 = buf1;
+        buf1 = t;
+        cnt = half + (cnt & 1u);
+    }
+    if (tid == 0) {
+        if (final_pass) {
+            sc->root = buf0[0];
+            if (root_out) *root_out = buf0[0];
+        } else {
+            out[blockIdx.x] = buf0[0];
+        }
+    }
+}
+
+__global__ void k_write_header(void *dst, int32_t step, uint32_t n32)
+{
+    uint32_t *p = static_cast<uint32_t *>(dst);
+    p[0] = uint32_t(step);
+    p[1] = n32;
+}
+
+}  // namespace
+
+cudaError_t launch_init_powers(uint64_t *powers, cudaStream_t st)
+{
+    k_init_powers<<<kChunk / 256, 256, 0, st>>>(powers);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_chunk_fix(const float *g, uint64_t n, float *chunk_sq, const uint64_t *chunks,
+                             int count, cudaStream_t st)
+{
+    ChunkList L{};
+    for (int i = 0; i < count; ++i) L.idx[i] = chunks[i];
+    L.count = count;
+    k_chunk_fix<<<count, 256, 0, st>>>(g, n, chunk_sq, L);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_leaf_fix(const float *w, const float *m, const float *v, uint64_t n,
+                            uint64_t c, uint64_t *leaves, const uint64_t *powers,
+                            const uint64_t *chunks, int count, cudaStream_t st)
+{
+    ChunkList L{};
+    for (int i = 0; i < count; ++i) L.idx[i] = chunks[i];
+    L.count = count;
+    k_leaf_fix<<<count, 256, 0, st>>>(w, m, v, n, c, leaves, powers, L);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_norm(const float *in, uint64_t count, float *out, Scalars *sc, int final_pass,
+                        float clip, float *norm_out, float *scale_out, int blocks,
+                        cudaStream_t st)
+{
+    k_norm<<<blocks, 256, 0, st>>>(in, count, out, sc, final_pass, clip, norm_out, scale_out);
+    return cudaGetLastError();
+}
+
+cudaError_t merkle_prepare()
+{
+    // two 4096-digest buffers: 64 KB of dynamic shared memory needs the opt-in
+    return cudaFuncSetAttribute(reinterpret_cast<const void *>(k_merkle),
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                int(2 * kChunk * sizeof(uint64_t)));
+}
+
+cudaError_t launch_merkle(const uint64_t *in, uint64_t count, uint64_t *out, int header_mode,
+                          uint64_t *leaves_rw, uint32_t step, uint32_t n32, const uint64_t *powers,
+                          Scalars *sc, uint64_t *root_out, int blocks, cudaStream_t st)
+{
+    const size_t smem = 2 * kChunk * sizeof(uint64_t);
+    k_merkle<<<blocks, 256, smem, st>>>(in, count, out, header_mode, leaves_rw, step, n32, powers,
+                                        sc, root_out, blocks == 1 ? 1 : 0);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_write_header(void *dst, int32_t step, uint32_t n32, cudaStream_t st)
+{
+    k_write_header<<<1, 1, 0, st>>>(dst, step, n32);
+    return cudaGetLastError();
+}
+
+}  // namespace repstep

@@ -1,0 +1,80 @@
+// kernels.h -- host-side launch interface between the C ABI (repstep.cu) and the kernel
+// translation units.  Internal; not part of the public ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace repstep {
+
+struct Scalars;
+
+// Replica reduce + chunk sums of squares (k_reduce.cu).
+struct ReduceArgs {
+    const void *grads[256];   // R device pointers, global replica order
+    float *g;                 // workspace g[n]
+    float *chunk_sq;          // workspace fp32[c]
+    Scalars *sc;              // device scalars (flags)
+    uint64_t n, begin, end;   // active range [begin, end)
+    uint64_t chunk_lo, chunk_hi;
+    uint32_t R, nodes, gpn;
+    uint32_t stages;          // ring depth
+    uint32_t stage_stride;    // bytes per stage
+    float rho;                // fp32(1/R)
+};
+
+struct ReduceShape {
+    int nt;          // compute threads (128, 256, 512)
+    int dtype;       // 0 fp32, 1 bf16
+    int staged;      // topology-staged sum
+    int rg;          // replicas per stage group (4 or 8)
+    int maxlev;      // carry-stack depth (6 or 9)
+};
+
+// Chooses the kernel instantiation and ring depth for a reduce; returns the dynamic
+// shared-memory bytes and fills args.stages / args.stage_stride.
+size_t reduce_smem_bytes(const ReduceShape &s, ReduceArgs &args);
+cudaError_t reduce_prepare(const ReduceShape &s, size_t smem);   // raise the smem limit
+cudaError_t reduce_occupancy(const ReduceShape &s, size_t smem, int *blocks_per_sm);
+cudaError_t launch_reduce(const ReduceShape &s, const ReduceArgs &args, int grid, size_t smem,
+                          cudaStream_t st);
+
+// AdamW + leaf digests, or leaves only (k_adamw.cu).
+struct AdamwArgs {
+    const float *g;           // MODE adamw: workspace g
+    float *w, *m, *v;         // state (updated in place in MODE adamw)
+    uint64_t *leaves;         // workspace u64[1 + 3c]
+    const uint64_t *powers;   // workspace K^1..K^4096 mod p
+    Scalars *sc;              // device scalars (scale, flags)
+    uint64_t n, c, begin, end;
+    uint64_t chunk_lo, chunk_hi;
+    uint32_t stages, stage_stride;
+    float lr, beta1, beta2, eps, bc1, bc2, om1, om2, delta;
+};
+
+size_t adamw_smem_bytes(int nt, int mode, AdamwArgs &args);
+cudaError_t adamw_prepare(int nt, int mode, size_t smem);
+cudaError_t adamw_occupancy(int nt, int mode, size_t smem, int *blocks_per_sm);
+cudaError_t launch_adamw(int nt, int mode, const AdamwArgs &args, int grid, size_t smem,
+                         cudaStream_t st);
+
+// Small kernels (k_small.cu).
+cudaError_t launch_init_powers(uint64_t *powers, cudaStream_t st);
+cudaError_t launch_chunk_fix(const float *g, uint64_t n, float *chunk_sq, const uint64_t *chunks,
+                             int count, cudaStream_t st);
+cudaError_t launch_leaf_fix(const float *w, const float *m, const float *v, uint64_t n,
+                            uint64_t c, uint64_t *leaves, const uint64_t *powers,
+                            const uint64_t *chunks, int count, cudaStream_t st);
+cudaError_t launch_norm(const float *in, uint64_t count, float *out, Scalars *sc, int final_pass,
+                        float clip, float *norm_out, float *scale_out, int blocks,
+                        cudaStream_t st);
+cudaError_t merkle_prepare();
+cudaError_t launch_merkle(const uint64_t *in, uint64_t count, uint64_t *out, int header_mode,
+                          uint64_t *leaves_rw, uint32_t step, uint32_t n32, const uint64_t *powers,
+                          Scalars *sc, uint64_t *root_out, int blocks, cudaStream_t st);
+cudaError_t launch_write_header(void *dst, int32_t step, uint32_t n32, cudaStream_t st);
+
+constexpr int kFixMax = 64;   // chunk indices per fix-up launch
+
+}  // namespace repstep

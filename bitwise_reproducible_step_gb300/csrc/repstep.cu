@@ -1,0 +1,607 @@
+// repstep.cu -- host side of the C ABI declared in include/repstep.h: argument validation,
+// workspace layout, host-computed fp32 constants, call-order state, and the sequence of
+// kernel launches on the caller's stream.  No device memory is allocated here.
+//
+// Host fp32 constants are computed with plain IEEE single operations, one rounding each
+// (the library is built with -ffp-contract=off for host code too):
+//   rho = 1/R   ("OPEN-1B: A Fully Auditable Training Run", App. A.3: every average is a
+//                multiply by a host-computed reciprocal)
+//   1 - b1, 1 - b2, 1 - lr*wd, and the bias corrections 1 - b^t (t repeated products).
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "../../include/repstep.h"
+#include "common.cuh"
+#include "kernels.h"
+
+using namespace repstep;
+
+namespace {
+
+struct Layout {
+    uint64_t g, chunk_sq, norm_part, leaves, merkle_part, powers, scalars, total;
+};
+
+constexpr uint64_t kAlign = 256;
+
+uint64_t align_up(uint64_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+bool valid_config(const repstep_config *cfg)
+{
+    if (!cfg) return false;
+    if (cfg->n > 0xFFFFFFFFull) return false;
+    if (cfg->grad_dtype != REPSTEP_F32 && cfg->grad_dtype != REPSTEP_BF16) return false;
+    if (cfg->grid_blocks < 0) return false;
+    if (cfg->block_threads != 0 && cfg->block_threads != 128 && cfg->block_threads != 256 &&
+        cfg->block_threads != 512)
+        return false;
+    return cfg->reserved == 0;
+}
+
+Layout layout_of(uint64_t n)
+{
+    const uint64_t c = (n + kChunk - 1) / kChunk;
+    const uint64_t nb2 = c > kChunk ? (c + kChunk - 1) / kChunk : 1;
+    const uint64_t L = 1 + 3 * c;
+    const uint64_t nb4 = (L + kChunk - 1) / kChunk;
+    Layout l{};
+    uint64_t off = 0;
+    l.g = off;           off = align_up(off + 4 * (n ? n : 1));
+    l.chunk_sq = off;    off = align_up(off + 4 * (c ? c : 1));
+    l.norm_part = off;   off = align_up(off + 4 * nb2);
+    l.leaves = off;      off = align_up(off + 8 * L);
+    l.merkle_part = off; off = align_up(off + 8 * nb4);
+    l.powers = off;      off = align_up(off + 8 * kChunk);
+    l.scalars = off;     off = align_up(off + sizeof(Scalars));
+    l.total = off;
+    return l;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool finite_f(float x) { return std::isfinite(x); }
+
+}  // namespace
+
+struct repstep_ctx {
+    repstep_config cfg;
+    Layout lay;
+    unsigned char *ws;
+    cudaStream_t stream;
+    uint64_t n, c;
+    int sm_count;
+    int nt_reduce, nt_adamw;
+    uint64_t launches;
+    int last_err;
+    // call-order state of the current step
+    uint64_t reduced;        // elements reduced since the last clip
+    bool scale_ready;        // a clip followed the last reduce
+    uint64_t updated;        // elements updated by AdamW since the last clip
+    const float *sw, *sm, *sv;
+    std::vector<uint64_t> cut_norm, cut_leaf;   // chunks cut by range boundaries
+
+    float *g() const { return reinterpret_cast<float *>(ws + lay.g); }
+    float *chunk_sq() const { return reinterpret_cast<float *>(ws + lay.chunk_sq); }
+    float *norm_part() const { return reinterpret_cast<float *>(ws + lay.norm_part); }
+    uint64_t *leaves() const { return reinterpret_cast<uint64_t *>(ws + lay.leaves); }
+    uint64_t *merkle_part() const { return reinterpret_cast<uint64_t *>(ws + lay.merkle_part); }
+    uint64_t *powers() const { return reinterpret_cast<uint64_t *>(ws + lay.powers); }
+    Scalars *sc() const { return reinterpret_cast<Scalars *>(ws + lay.scalars); }
+
+    int cuda_fail(cudaError_t e)
+    {
+        last_err = int(e);
+        return REPSTEP_ERR_CUDA;
+    }
+};
+
+namespace {
+
+// Persistent grid: SM count x resident CTAs, never more CTAs than chunks to process.
+int grid_for(repstep_ctx *x, int blocks_per_sm, uint64_t chunks)
+{
+    uint64_t g = x->cfg.grid_blocks > 0 ? uint64_t(x->cfg.grid_blocks)
+                                        : uint64_t(x->sm_count) * uint64_t(blocks_per_sm > 0 ? blocks_per_sm : 1);
+    if (g > chunks) g = chunks;
+    if (g < 1) g = 1;
+    return int(g);
+}
+
+// Record the chunks a range [b, e) cuts (partly covered, so not summed in the kernel).
+void note_cut_chunks(std::vector<uint64_t> &v, uint64_t b, uint64_t e, uint64_t n)
+{
+    if (b >= e) return;
+    const uint64_t k0 = b / kChunk, k1 = (e - 1) / kChunk;
+    auto cut = [&](uint64_t k) {
+        const uint64_t c0 = k * kChunk, c1 = c0 + kChunk < n ? c0 + kChunk : n;
+        return !(c0 >= b && c1 <= e);
+    };
+    if (cut(k0)) v.push_back(k0);
+    if (k1 != k0 && cut(k1)) v.push_back(k1);
+}
+
+void unique_sort(std::vector<uint64_t> &v)
+{
+    std::vector<uint64_t> out;
+    for (uint64_t k : v) {
+        bool seen = false;
+        for (uint64_t o : out) seen = seen || (o == k);
+        if (!seen) out.push_back(k);
+    }
+    v.swap(out);
+}
+
+int check_hparams(const repstep_hparams *hp)
+{
+    if (!hp) return REPSTEP_ERR_ARG;
+    if (!finite_f(hp->lr) || !finite_f(hp->beta1) || !finite_f(hp->beta2) ||
+        !finite_f(hp->eps) || !finite_f(hp->weight_decay) || !finite_f(hp->bc1) ||
+        !finite_f(hp->bc2) || hp->bc1 == 0.0f || hp->bc2 == 0.0f)
+        return REPSTEP_ERR_ARG;
+    return REPSTEP_OK;
+}
+
+int do_reduce(repstep_ctx *x, const void *const *grads, uint32_t R, uint32_t nodes,
+              uint32_t gpn, uint64_t begin, uint64_t count)
+{
+    if (!grads || R == 0) return REPSTEP_ERR_ARG;
+    if (R > kMaxReplicas) return REPSTEP_ERR_SIZE;
+    if (nodes == 0 || gpn == 0 || uint64_t(nodes) * gpn != R) return REPSTEP_ERR_TOPOLOGY;
+    if (nodes > 1 && (gpn & (gpn - 1)) != 0) return REPSTEP_ERR_TOPOLOGY;
+    if (begin > x->n || count > x->n - begin) return REPSTEP_ERR_ARG;
+    for (uint32_t r = 0; r < R; ++r) {
+        if (!grads[r]) return REPSTEP_ERR_ARG;
+        if (!aligned(grads[r], 16)) return REPSTEP_ERR_ALIGN;
+    }
+    if (x->scale_ready || x->updated) {   // a new step starts
+        x->scale_ready = false;
+        x->updated = 0;
+        x->cut_leaf.clear();
+    }
+    x->reduced += count;
+    if (count == 0) return REPSTEP_OK;
+
+    const uint64_t end = begin + count;
+    ReduceArgs a{};
+    for (uint32_t r = 0; r < R; ++r) a.grads[r] = grads[r];
+    a.g = x->g();
+    a.chunk_sq = x->chunk_sq();
+    a.sc = x->sc();
+    a.n = x->n;
+    a.begin = begin;
+    a.end = end;
+    a.chunk_lo = begin / kChunk;
+    a.chunk_hi = (end + kChunk - 1) / kChunk;
+    a.R = R;
+    a.nodes = nodes;
+    a.gpn = gpn;
+    const float one = 1.0f;
+    a.rho = one / float(R);
+    ReduceShape s{};
+    s.nt = x->nt_reduce;
+    s.dtype = x->cfg.grad_dtype;
+    s.staged = nodes > 1 ? 1 : 0;
+    s.rg = R >= 8 ? 8 : 4;
+    s.maxlev = R <= 32 ? 6 : 9;
+    const size_t smem = reduce_smem_bytes(s, a);
+    cudaError_t e = reduce_prepare(s, smem);
+    if (e != cudaSuccess) return x->cuda_fail(e);
+    int bps = 1;
+    e = reduce_occupancy(s, smem, &bps);
+    if (e != cudaSuccess) return x->cuda_fail(e);
+    const int grid = grid_for(x, bps, a.chunk_hi - a.chunk_lo);
+    e = launch_reduce(s, a, grid, smem, x->stream);
+    if (e != cudaSuccess) return x->cuda_fail(e);
+    ++x->launches;
+    note_cut_chunks(x->cut_norm, begin, end, x->n);
+    return REPSTEP_OK;
+}
+
+int do_clip(repstep_ctx *x, float clip, float *norm_out, float *scale_out)
+{
+    if (!(clip > 0.0f)) return REPSTEP_ERR_ARG;   // also rejects NaN; +inf is allowed
+    if (norm_out && !aligned(norm_out, 4)) return REPSTEP_ERR_ALIGN;
+    if (scale_out && !aligned(scale_out, 4)) return REPSTEP_ERR_ALIGN;
+    if (x->reduced != x->n) return REPSTEP_ERR_STATE;
+    cudaError_t e;
+    unique_sort(x->cut_norm);
+    for (size_t i = 0; i < x->cut_norm.size(); i += kFixMax) {
+        const int cnt = int(x->cut_norm.size() - i < size_t(kFixMax) ? x->cut_norm.size() - i : kFixMax);
+        e = launch_chunk_fix(x->g(), x->n, x->chunk_sq(), x->cut_norm.data() + i, cnt, x->stream);
+        if (e != cudaSuccess) return x->cuda_fail(e);
+        ++x->launches;
+    }
+    x->cut_norm.clear();
+    const uint64_t c = x->c;
+    if (c > kChunk) {
+        const int nb = int((c + kChunk - 1) / kChunk);
+        e = launch_norm(x->chunk_sq(), c, x->norm_part(), x->sc(), 0, clip, nullptr, nullptr, nb,
+                        x->stream);
+        if (e != cudaSuccess) return x->cuda_fail(e);
+        ++x->launches;
+        e = launch_norm(x->norm_part(), uint64_t(nb), nullptr, x->sc(), 1, clip, norm_out,
+                        scale_out, 1, x->stream);
+    } else {
+        e = launch_norm(x->chunk_sq(), c, nullptr, x->sc(), 1, clip, norm_out, scale_out, 1,
+                        x->stream);
+    }
+    if (e != cudaSuccess) return x->cuda_fail(e);
+    ++x->launches;
+    x->reduced = 0;
+    x->scale_ready = true;
+    x->updated = 0;
+    x->cut_leaf.clear();
+    x->sw = x->sm = x->sv = nullptr;
+    return REPSTEP_OK;
+}
+
+int do_adamw(repstep_ctx *x, float *w, float *m, float *v, const repstep_hparams *hp,
+             uint64_t begin, uint64_t count)
+{
+    if (!w || !m || !v) return REPSTEP_ERR_ARG;
+    if (!aligned(w, 16) || !aligned(m, 16) || !aligned(v, 16)) return REPSTEP_ERR_ALIGN;
+    int rc = check_hparams(hp);
+    if (rc) return rc;
+    if (begin > x->n || count > x->n - begin) return REPSTEP_ERR_ARG;
+    if (!x->scale_ready) return REPSTEP_ERR_STATE;
+    if (x->sw && (x->sw != w || x->sm != m || x->sv != v)) return REPSTEP_ERR_ARG;
+    x->sw = w;
+    x->sm = m;
+    x->sv = v;
+    x->updated += count;
+    if (count == 0) return REPSTEP_OK;
+    const uint64_t end = begin + count;
+    AdamwArgs a{};
+    a.g = x->g();
+    a.w = w;
+    a.m = m;
+    a.v = v;
+    a.leaves = x->leaves();
+    a.powers = x->powers();
+    a.sc = x->sc();
+    a.n = x->n;
+    a.c = x->c;
+    a.begin = begin;
+    a.end = end;
+    a.chunk_lo = begin / kChunk;
+    a.chunk_hi = (end + kChunk - 1) / kChunk;
+    a.lr = hp->lr;
+    a.beta1 = hp->beta1;
+    a.beta2 = hp->beta2;
+    a.eps = hp->eps;
+    a.bc1 = hp->bc1;
+    a.bc2 = hp->bc2;
+    const float one = 1.0f;
+    a.om1 = one - hp->beta1;
+    a.om2 = one - hp->beta2;
+    const float lrwd = hp->lr * hp->weight_decay;
+    a.delta = one - lrwd;
+    const int nt = x->nt_adamw;
+    const size_t smem = adamw_smem_bytes(nt, 0, a);
+    cudaError_t e = adamw_prepare(nt, 0, smem);
+    if (e != cudaSuccess) return x->cuda_fail(e);
+    int bps = 1;
+    e = adamw_occupancy(nt, 0, smem, &bps);
+    if (e != cudaSuccess) return x->cuda_fail(e);
+    const int grid = grid_for(x, bps, a.chunk_hi - a.chunk_lo);
+    e = launch_adamw(nt, 0, a, grid, smem, x->stream);
+    if (e != cudaSuccess) return x->cuda_fail(e);
+    ++x->launches;
+    note_cut_chunks(x->cut_leaf, begin, end, x->n);
+    return REPSTEP_OK;
+}
+
+int merkle(repstep_ctx *x, int32_t step, uint64_t *root_out)
+{
+    const uint64_t L = 1 + 3 * x->c;
+    const int nb = int((L + kChunk - 1) / kChunk);
+    cudaError_t e;
+    if (nb == 1) {
+        e = launch_merkle(x->leaves(), L, nullptr, 1, x->leaves(), uint32_t(step), uint32_t(x->n),
+                          x->powers(), x->sc(), root_out, 1, x->stream);
+    } else {
+        e = launch_merkle(x->leaves(), L, x->merkle_part(), 1, x->leaves(), uint32_t(step),
+                          uint32_t(x->n), x->powers(), x->sc(), nullptr, nb, x->stream);
+        if (e != cudaSuccess) return x->cuda_fail(e);
+        ++x->launches;
+        e = launch_merkle(x->merkle_part(), uint64_t(nb), nullptr, 0, x->leaves(), 0, 0,
+                          x->powers(), x->sc(), root_out, 1, x->stream);
+    }
+    if (e != cudaSuccess) return x->cuda_fail(e);
+    ++x->launches;
+    return REPSTEP_OK;
+}
+
+int do_root(repstep_ctx *x, int32_t step, uint64_t *root_out)
+{
+    if (root_out && !aligned(root_out, 8)) return REPSTEP_ERR_ALIGN;
+    if (!x->scale_ready || x->updated != x->n) return REPSTEP_ERR_STATE;
+    unique_sort(x->cut_leaf);
+    for (size_t i = 0; i < x->cut_leaf.size(); i += kFixMax) {
+        const int cnt = int(x->cut_leaf.size() - i < size_t(kFixMax) ? x->cut_leaf.size() - i : kFixMax);
+        cudaError_t e = launch_leaf_fix(x->sw, x->sm, x->sv, x->n, x->c, x->leaves(), x->powers(),
+                                        x->cut_leaf.data() + i, cnt, x->stream);
+        if (e != cudaSuccess) return x->cuda_fail(e);
+        ++x->launches;
+    }
+    x->cut_leaf.clear();
+    return merkle(x, step, root_out);
+}
+
+int do_hash(repstep_ctx *x, int32_t step, const float *w, const float *m, const float *v,
+            uint64_t *root_out)
+{
+    if (!w || !m || !v) return REPSTEP_ERR_ARG;
+    if (!aligned(w, 16) || !aligned(m, 16) || !aligned(v, 16)) return REPSTEP_ERR_ALIGN;
+    if (root_out && !aligned(root_out, 8)) return REPSTEP_ERR_ALIGN;
+    if (x->n > 0) {
+        AdamwArgs a{};
+        a.w = const_cast<float *>(w);
+        a.m = const_cast<float *>(m);
+        a.v = const_cast<float *>(v);
+        a.leaves = x->leaves();
+        a.powers = x->powers();
+        a.sc = x->sc();
+        a.n = x->n;
+        a.c = x->c;
+        a.begin = 0;
+        a.end = x->n;
+        a.chunk_lo = 0;
+        a.chunk_hi = x->c;
+        const int nt = x->nt_adamw;
+        const size_t smem = adamw_smem_bytes(nt, 1, a);
+        cudaError_t e = adamw_prepare(nt, 1, smem);
+        if (e != cudaSuccess) return x->cuda_fail(e);
+        int bps = 1;
+        e = adamw_occupancy(nt, 1, smem, &bps);
+        if (e != cudaSuccess) return x->cuda_fail(e);
+        e = launch_adamw(nt, 1, a, grid_for(x, bps, x->c), smem, x->stream);
+        if (e != cudaSuccess) return x->cuda_fail(e);
+        ++x->launches;
+    }
+    return merkle(x, step, root_out);
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t repstep_workspace_bytes(const repstep_config *cfg)
+{
+    if (!valid_config(cfg)) return 0;
+    return size_t(layout_of(cfg->n).total);
+}
+
+int repstep_workspace_layout(const repstep_config *cfg, repstep_layout *out)
+{
+    if (!valid_config(cfg) || !out) return REPSTEP_ERR_ARG;
+    const Layout l = layout_of(cfg->n);
+    out->g = l.g;
+    out->chunk_sums = l.chunk_sq;
+    out->norm_partials = l.norm_part;
+    out->leaves = l.leaves;
+    out->merkle_partials = l.merkle_part;
+    out->pow_table = l.powers;
+    out->scalars = l.scalars;
+    out->total = l.total;
+    return REPSTEP_OK;
+}
+
+int repstep_create(const repstep_config *cfg, void *d_workspace, size_t workspace_bytes,
+                   void *stream, repstep_ctx **out)
+{
+    if (!out) return REPSTEP_ERR_ARG;
+    *out = nullptr;
+    if (!cfg || !d_workspace) return REPSTEP_ERR_ARG;
+    if (!valid_config(cfg)) return cfg->n > 0xFFFFFFFFull ? REPSTEP_ERR_SIZE : REPSTEP_ERR_ARG;
+    if (!aligned(d_workspace, kAlign)) return REPSTEP_ERR_ALIGN;
+    const Layout lay = layout_of(cfg->n);
+    if (workspace_bytes < lay.total) return REPSTEP_ERR_SIZE;
+    repstep_ctx *x = new (std::nothrow) repstep_ctx();
+    if (!x) return REPSTEP_ERR_ARG;
+    x->cfg = *cfg;
+    x->lay = lay;
+    x->ws = static_cast<unsigned char *>(d_workspace);
+    x->stream = static_cast<cudaStream_t>(stream);
+    x->n = cfg->n;
+    x->c = (cfg->n + kChunk - 1) / kChunk;
+    x->nt_reduce = cfg->block_threads ? cfg->block_threads : 256;
+    x->nt_adamw = cfg->block_threads ? cfg->block_threads : 512;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&x->sm_count, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess) e = merkle_prepare();
+    if (e == cudaSuccess) e = cudaMemsetAsync(x->ws + lay.scalars, 0, sizeof(Scalars), x->stream);
+    if (e == cudaSuccess) e = launch_init_powers(x->powers(), x->stream);
+    if (e != cudaSuccess) {
+        delete x;
+        return REPSTEP_ERR_CUDA;
+    }
+    x->launches = 1;
+    *out = x;
+    return REPSTEP_OK;
+}
+
+int repstep_destroy(repstep_ctx *ctx)
+{
+    if (!ctx) return REPSTEP_ERR_ARG;
+    delete ctx;
+    return REPSTEP_OK;
+}
+
+int repstep_set_stream(repstep_ctx *ctx, void *stream)
+{
+    if (!ctx) return REPSTEP_ERR_ARG;
+    ctx->stream = static_cast<cudaStream_t>(stream);
+    return REPSTEP_OK;
+}
+
+int repstep_reduce(repstep_ctx *ctx, const void *const *d_grads, uint32_t R, uint32_t nodes,
+                   uint32_t gpus_per_node, uint64_t begin, uint64_t count)
+{
+    if (!ctx) return REPSTEP_ERR_ARG;
+    return do_reduce(ctx, d_grads, R, nodes, gpus_per_node, begin, count);
+}
+
+int repstep_clip(repstep_ctx *ctx, float clip, float *d_norm_out, float *d_scale_out)
+{
+    if (!ctx) return REPSTEP_ERR_ARG;
+    return do_clip(ctx, clip, d_norm_out, d_scale_out);
+}
+
+int repstep_adamw(repstep_ctx *ctx, float *d_w, float *d_m, float *d_v, const repstep_hparams *hp,
+                  uint64_t begin, uint64_t count)
+{
+    if (!ctx) return REPSTEP_ERR_ARG;
+    return do_adamw(ctx, d_w, d_m, d_v, hp, begin, count);
+}
+
+int repstep_root(repstep_ctx *ctx, int32_t step, uint64_t *d_root_out)
+{
+    if (!ctx) return REPSTEP_ERR_ARG;
+    return do_root(ctx, step, d_root_out);
+}
+
+int repstep_hash(repstep_ctx *ctx, int32_t step, const float *d_w, const float *d_m,
+                 const float *d_v, uint64_t *d_root_out)
+{
+    if (!ctx) return REPSTEP_ERR_ARG;
+    return do_hash(ctx, step, d_w, d_m, d_v, d_root_out);
+}
+
+int repstep_step(repstep_ctx *ctx, const void *const *d_grads, uint32_t R, uint32_t nodes,
+                 uint32_t gpus_per_node, float *d_w, float *d_m, float *d_v,
+                 const repstep_hparams *hp, int32_t step, float *d_norm_out, uint64_t *d_root_out)
+{
+    if (!ctx) return REPSTEP_ERR_ARG;
+    // validate everything before launching anything
+    if (!d_w || !d_m || !d_v) return REPSTEP_ERR_ARG;
+    if (!aligned(d_w, 16) || !aligned(d_m, 16) || !aligned(d_v, 16)) return REPSTEP_ERR_ALIGN;
+    int rc = check_hparams(hp);
+    if (rc) return rc;
+    if (!(hp->clip > 0.0f)) return REPSTEP_ERR_ARG;
+    if (d_norm_out && !aligned(d_norm_out, 4)) return REPSTEP_ERR_ALIGN;
+    if (d_root_out && !aligned(d_root_out, 8)) return REPSTEP_ERR_ALIGN;
+    ctx->reduced = 0;
+    ctx->cut_norm.clear();
+    rc = do_reduce(ctx, d_grads, R, nodes, gpus_per_node, 0, ctx->n);
+    if (rc) return rc;
+    rc = do_clip(ctx, hp->clip, d_norm_out, nullptr);
+    if (rc) return rc;
+    rc = do_adamw(ctx, d_w, d_m, d_v, hp, 0, ctx->n);
+    if (rc) return rc;
+    return do_root(ctx, step, d_root_out);
+}
+
+uint64_t repstep_image_bytes(uint64_t n) { return 8 + 12 * n; }
+
+int repstep_image_write(repstep_ctx *ctx, int32_t step, const float *d_w, const float *d_m,
+                        const float *d_v, void *dst, uint64_t dst_bytes, int dst_is_host)
+{
+    if (!ctx || !d_w || !d_m || !d_v || !dst) return REPSTEP_ERR_ARG;
+    const uint64_t n = ctx->n;
+    if (dst_bytes < repstep_image_bytes(n)) return REPSTEP_ERR_SIZE;
+    unsigned char *d = static_cast<unsigned char *>(dst);
+    cudaError_t e;
+    const cudaMemcpyKind kind = dst_is_host ? cudaMemcpyDeviceToHost : cudaMemcpyDeviceToDevice;
+    if (dst_is_host) {
+        const uint32_t h[2] = {uint32_t(step), uint32_t(n)};
+        std::memcpy(d, h, 8);   // the header is little-endian on every supported host
+    } else {
+        if (!aligned(dst, 4)) return REPSTEP_ERR_ALIGN;
+        e = launch_write_header(dst, step, uint32_t(n), ctx->stream);
+        if (e != cudaSuccess) return ctx->cuda_fail(e);
+        ++ctx->launches;
+    }
+    const float *arrs[3] = {d_w, d_m, d_v};
+    for (int a = 0; a < 3; ++a) {
+        if (n == 0) break;
+        e = cudaMemcpyAsync(d + 8 + uint64_t(a) * 4 * n, arrs[a], 4 * n, kind, ctx->stream);
+        if (e != cudaSuccess) return ctx->cuda_fail(e);
+    }
+    return REPSTEP_OK;
+}
+
+int repstep_image_read(repstep_ctx *ctx, const void *src, uint64_t src_bytes, int src_is_host,
+                       int32_t *step_out, float *d_w, float *d_m, float *d_v)
+{
+    if (!ctx || !src || !d_w || !d_m || !d_v) return REPSTEP_ERR_ARG;
+    const uint64_t n = ctx->n;
+    if (src_bytes != repstep_image_bytes(n)) return REPSTEP_ERR_FORMAT;
+    uint32_t h[2];
+    cudaError_t e;
+    if (src_is_host) {
+        std::memcpy(h, src, 8);
+    } else {
+        e = cudaMemcpyAsync(h, src, 8, cudaMemcpyDeviceToHost, ctx->stream);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(ctx->stream);
+        if (e != cudaSuccess) return ctx->cuda_fail(e);
+    }
+    if (uint64_t(h[1]) != n) return REPSTEP_ERR_FORMAT;
+    if (step_out) *step_out = int32_t(h[0]);
+    const unsigned char *s = static_cast<const unsigned char *>(src);
+    const cudaMemcpyKind kind = src_is_host ? cudaMemcpyHostToDevice : cudaMemcpyDeviceToDevice;
+    float *arrs[3] = {d_w, d_m, d_v};
+    for (int a = 0; a < 3; ++a) {
+        if (n == 0) break;
+        e = cudaMemcpyAsync(arrs[a], s + 8 + uint64_t(a) * 4 * n, 4 * n, kind, ctx->stream);
+        if (e != cudaSuccess) return ctx->cuda_fail(e);
+    }
+    return REPSTEP_OK;
+}
+
+void repstep_bias_corrections(float beta1, float beta2, int32_t t, float *bc1, float *bc2)
+{
+    float p1 = 1.0f, p2 = 1.0f;
+    for (int32_t j = 0; j < t; ++j) {
+        p1 = p1 * beta1;
+        p2 = p2 * beta2;
+    }
+    const float one = 1.0f;
+    if (bc1) *bc1 = one - p1;
+    if (bc2) *bc2 = one - p2;
+}
+
+int repstep_sync(repstep_ctx *ctx, uint32_t *flags_out)
+{
+    if (!ctx) return REPSTEP_ERR_ARG;
+    cudaError_t e = cudaStreamSynchronize(ctx->stream);
+    if (e != cudaSuccess) return ctx->cuda_fail(e);
+    Scalars s;
+    e = cudaMemcpy(&s, ctx->sc(), sizeof s, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return ctx->cuda_fail(e);
+    if (flags_out) *flags_out = s.flags;
+    const uint32_t timeouts = kFlagTimeoutReduce | kFlagTimeoutAdamw | kFlagTimeoutLeaves;
+    if (s.flags & timeouts) {
+        const uint32_t keep = s.flags & ~timeouts;
+        e = cudaMemcpy(&ctx->sc()->flags, &keep, sizeof keep, cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) return ctx->cuda_fail(e);
+        return REPSTEP_ERR_TIMEOUT;
+    }
+    return REPSTEP_OK;
+}
+
+uint64_t repstep_launch_count(const repstep_ctx *ctx) { return ctx ? ctx->launches : 0; }
+
+int repstep_last_cuda_error(const repstep_ctx *ctx) { return ctx ? ctx->last_err : 0; }
+
+const char *repstep_strerror(int code)
+{
+    switch (code) {
+    case REPSTEP_OK: return "ok";
+    case REPSTEP_ERR_ARG: return "invalid argument";
+    case REPSTEP_ERR_ALIGN: return "misaligned device pointer";
+    case REPSTEP_ERR_SIZE: return "size out of range";
+    case REPSTEP_ERR_TOPOLOGY: return "replica topology breaks the canonical tree";
+    case REPSTEP_ERR_CUDA: return "CUDA runtime error";
+    case REPSTEP_ERR_TIMEOUT: return "a kernel wait timed out";
+    case REPSTEP_ERR_STATE: return "call order violated";
+    case REPSTEP_ERR_FORMAT: return "bad checkpoint image";
+    default: return "unknown status";
+    }
+}
+
+}  // extern "C"

@@ -1,0 +1,310 @@
+"""Python binding of librepstep.so (include/repstep.h): ctypes argument marshalling only.
+
+Every step of the optimizer step runs in the library's CUDA kernels; this module checks
+tensor devices, dtypes and sizes, passes raw device pointers and the current torch stream,
+and turns status codes into exceptions.  There is no CPU fallback: if the library is not
+built, importing the binding's functions raises.
+
+Typical use:
+    ctx = Repstep(n)                        # workspace allocated by torch on the device
+    hp = hparams(lr=..., beta1=..., beta2=..., eps=..., weight_decay=..., clip=1.0, t=1)
+    ctx.step(grads, w, m, v, hp, step=1, norm_out=norm, root_out=root)
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "librepstep.so")
+
+REPSTEP_F32 = 0
+REPSTEP_BF16 = 1
+CHUNK = 4096
+MAX_REPLICAS = 256
+
+FLAG_NONFINITE_NORM = 0x1
+FLAG_TIMEOUT_REDUCE = 0x2
+FLAG_TIMEOUT_ADAMW = 0x4
+FLAG_TIMEOUT_LEAVES = 0x8
+
+STATUS = {0: "REPSTEP_OK", 1: "REPSTEP_ERR_ARG", 2: "REPSTEP_ERR_ALIGN", 3: "REPSTEP_ERR_SIZE",
+          4: "REPSTEP_ERR_TOPOLOGY", 5: "REPSTEP_ERR_CUDA", 6: "REPSTEP_ERR_TIMEOUT",
+          7: "REPSTEP_ERR_STATE", 8: "REPSTEP_ERR_FORMAT"}
+
+
+class Config(C.Structure):
+    _fields_ = [("n", C.c_uint64), ("grad_dtype", C.c_int32), ("grid_blocks", C.c_int32),
+                ("block_threads", C.c_int32), ("reserved", C.c_int32)]
+
+
+class HParams(C.Structure):
+    _fields_ = [(k, C.c_float) for k in
+                ("lr", "beta1", "beta2", "eps", "weight_decay", "clip", "bc1", "bc2")]
+
+
+class Layout(C.Structure):
+    _fields_ = [(k, C.c_uint64) for k in
+                ("g", "chunk_sums", "norm_partials", "leaves", "merkle_partials", "pow_table",
+                 "scalars", "total")]
+
+
+class RepstepError(RuntimeError):
+    def __init__(self, code: int, what: str = ""):
+        self.code = code
+        super().__init__(f"{STATUS.get(code, code)}: {strerror(code)}{(' -- ' + what) if what else ''}")
+
+
+EXPORTS = [
+    "repstep_workspace_bytes", "repstep_workspace_layout", "repstep_create", "repstep_destroy",
+    "repstep_set_stream", "repstep_reduce", "repstep_clip", "repstep_adamw", "repstep_root",
+    "repstep_hash", "repstep_step", "repstep_image_bytes", "repstep_image_write",
+    "repstep_image_read", "repstep_bias_corrections", "repstep_sync", "repstep_launch_count",
+    "repstep_last_cuda_error", "repstep_strerror",
+]
+
+_lib = None
+
+
+def lib():
+    """Load librepstep.so (raises if it was not built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is missing: build it with `python -c \"import "
+                           "__graft_entry__ as g; g.build()\"` (needs nvcc)")
+    L = C.CDLL(LIB_PATH)
+    vp, u64, u32, i32 = C.c_void_p, C.c_uint64, C.c_uint32, C.c_int32
+    L.repstep_workspace_bytes.argtypes = [C.POINTER(Config)]
+    L.repstep_workspace_bytes.restype = C.c_size_t
+    L.repstep_workspace_layout.argtypes = [C.POINTER(Config), C.POINTER(Layout)]
+    L.repstep_create.argtypes = [C.POINTER(Config), vp, C.c_size_t, vp, C.POINTER(vp)]
+    L.repstep_destroy.argtypes = [vp]
+    L.repstep_set_stream.argtypes = [vp, vp]
+    L.repstep_reduce.argtypes = [vp, C.POINTER(vp), u32, u32, u32, u64, u64]
+    L.repstep_clip.argtypes = [vp, C.c_float, vp, vp]
+    L.repstep_adamw.argtypes = [vp, vp, vp, vp, C.POINTER(HParams), u64, u64]
+    L.repstep_root.argtypes = [vp, i32, vp]
+    L.repstep_hash.argtypes = [vp, i32, vp, vp, vp, vp]
+    L.repstep_step.argtypes = [vp, C.POINTER(vp), u32, u32, u32, vp, vp, vp, C.POINTER(HParams),
+                               i32, vp, vp]
+    L.repstep_image_bytes.argtypes = [u64]
+    L.repstep_image_bytes.restype = u64
+    L.repstep_image_write.argtypes = [vp, i32, vp, vp, vp, vp, u64, C.c_int]
+    L.repstep_image_read.argtypes = [vp, vp, u64, C.c_int, C.POINTER(i32), vp, vp, vp]
+    L.repstep_bias_corrections.argtypes = [C.c_float, C.c_float, i32, C.POINTER(C.c_float),
+                                           C.POINTER(C.c_float)]
+    L.repstep_bias_corrections.restype = None
+    L.repstep_sync.argtypes = [vp, C.POINTER(u32)]
+    L.repstep_launch_count.argtypes = [vp]
+    L.repstep_launch_count.restype = u64
+    L.repstep_last_cuda_error.argtypes = [vp]
+    L.repstep_strerror.argtypes = [C.c_int]
+    L.repstep_strerror.restype = C.c_char_p
+    _lib = L
+    return L
+
+
+def strerror(code: int) -> str:
+    return lib().repstep_strerror(int(code)).decode()
+
+
+def _check(rc: int, what: str = ""):
+    if rc != 0:
+        raise RepstepError(rc, what)
+
+
+def bias_corrections(beta1: float, beta2: float, t: int):
+    b1, b2 = C.c_float(), C.c_float()
+    lib().repstep_bias_corrections(beta1, beta2, int(t), C.byref(b1), C.byref(b2))
+    return b1.value, b2.value
+
+
+def hparams(*, lr, beta1, beta2, eps, weight_decay, clip, t) -> HParams:
+    """AdamW hyperparameters for step t (bias corrections from the library's host recipe)."""
+    bc1, bc2 = bias_corrections(beta1, beta2, t)
+    return HParams(lr, beta1, beta2, eps, weight_decay, clip, bc1, bc2)
+
+
+def image_bytes(n: int) -> int:
+    return int(lib().repstep_image_bytes(n))
+
+
+def workspace_bytes(n: int, grad_dtype=torch.float32, grid_blocks=0, block_threads=0) -> int:
+    cfg = Config(n, _dtype_code(grad_dtype), grid_blocks, block_threads, 0)
+    return int(lib().repstep_workspace_bytes(C.byref(cfg)))
+
+
+def _dtype_code(dt) -> int:
+    if dt == torch.float32:
+        return REPSTEP_F32
+    if dt == torch.bfloat16:
+        return REPSTEP_BF16
+    raise TypeError(f"gradient dtype {dt}: float32 or bfloat16")
+
+
+def _ptr(t: torch.Tensor | None):
+    return None if t is None else C.c_void_p(t.data_ptr())
+
+
+class Repstep:
+    """One context over a torch-allocated device workspace (see repstep_create)."""
+
+    def __init__(self, n: int, grad_dtype=torch.float32, device=None, grid_blocks: int = 0,
+                 block_threads: int = 0, stream: torch.cuda.Stream | None = None):
+        L = lib()
+        self.n = int(n)
+        self.grad_dtype = grad_dtype
+        self.device = torch.device("cuda", torch.cuda.current_device()) if device is None \
+            else torch.device(device)
+        self._fixed_stream = stream
+        self.cfg = Config(self.n, _dtype_code(grad_dtype), grid_blocks, block_threads, 0)
+        nbytes = int(L.repstep_workspace_bytes(C.byref(self.cfg)))
+        if nbytes == 0:
+            raise RepstepError(1, "bad configuration")
+        self.layout = Layout()
+        _check(L.repstep_workspace_layout(C.byref(self.cfg), C.byref(self.layout)))
+        self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=self.device)
+        self._ctx = C.c_void_p()
+        _check(L.repstep_create(C.byref(self.cfg), _ptr(self.workspace), nbytes,
+                                C.c_void_p(self._stream().cuda_stream), C.byref(self._ctx)))
+        self.c = (self.n + CHUNK - 1) // CHUNK
+
+    # ---------------------------------------------------------------- plumbing
+    def _stream(self):
+        return self._fixed_stream or torch.cuda.current_stream(self.device)
+
+    def _bind(self):
+        if not self._ctx:
+            raise RuntimeError("context destroyed")
+        lib().repstep_set_stream(self._ctx, C.c_void_p(self._stream().cuda_stream))
+
+    def _state(self, *ts):
+        for t in ts:
+            if t.device != self.device or t.dtype != torch.float32 or not t.is_contiguous() \
+                    or t.numel() < self.n:
+                raise ValueError("state arrays: contiguous float32 on the context's device, "
+                                 f"at least n={self.n} elements")
+
+    def _grads(self, grads):
+        grads = list(grads)
+        for t in grads:
+            if t.device != self.device or t.dtype != self.grad_dtype or not t.is_contiguous() \
+                    or t.numel() < self.n:
+                raise ValueError(f"gradients: contiguous {self.grad_dtype} on the context's "
+                                 f"device, at least n={self.n} elements")
+        arr = (C.c_void_p * max(len(grads), 1))(*[t.data_ptr() for t in grads])
+        return arr, len(grads)
+
+    @staticmethod
+    def _out(t, dtype, numel=1):
+        if t is not None and (t.dtype != dtype or t.numel() < numel or not t.is_cuda):
+            raise ValueError(f"output must be a CUDA {dtype} tensor")
+        return _ptr(t)
+
+    # ---------------------------------------------------------------- the C ABI
+    def reduce(self, grads, nodes: int = 1, gpus_per_node: int | None = None, begin: int = 0,
+               count: int | None = None):
+        arr, R = self._grads(grads)
+        gpn = R // max(nodes, 1) if gpus_per_node is None else gpus_per_node
+        count = self.n - begin if count is None else count
+        self._bind()
+        _check(lib().repstep_reduce(self._ctx, arr, R, nodes, gpn, begin, count), "reduce")
+
+    def clip(self, clip: float, norm_out=None, scale_out=None):
+        self._bind()
+        _check(lib().repstep_clip(self._ctx, clip, self._out(norm_out, torch.float32),
+                                  self._out(scale_out, torch.float32)), "clip")
+
+    def adamw(self, w, m, v, hp: HParams, begin: int = 0, count: int | None = None):
+        self._state(w, m, v)
+        count = self.n - begin if count is None else count
+        self._bind()
+        _check(lib().repstep_adamw(self._ctx, _ptr(w), _ptr(m), _ptr(v), C.byref(hp), begin,
+                                   count), "adamw")
+
+    def root(self, step: int, root_out=None):
+        self._bind()
+        _check(lib().repstep_root(self._ctx, int(step), self._out(root_out, torch.int64)), "root")
+
+    def hash(self, step: int, w, m, v, root_out=None):
+        self._state(w, m, v)
+        self._bind()
+        _check(lib().repstep_hash(self._ctx, int(step), _ptr(w), _ptr(m), _ptr(v),
+                                  self._out(root_out, torch.int64)), "hash")
+
+    def step(self, grads, w, m, v, hp: HParams, step: int, norm_out=None, root_out=None,
+             nodes: int = 1, gpus_per_node: int | None = None):
+        arr, R = self._grads(grads)
+        self._state(w, m, v)
+        gpn = R // max(nodes, 1) if gpus_per_node is None else gpus_per_node
+        self._bind()
+        _check(lib().repstep_step(self._ctx, arr, R, nodes, gpn, _ptr(w), _ptr(m), _ptr(v),
+                                  C.byref(hp), int(step), self._out(norm_out, torch.float32),
+                                  self._out(root_out, torch.int64)), "step")
+
+    def image_write(self, step: int, w, m, v, dst: torch.Tensor):
+        self._state(w, m, v)
+        if dst.dtype != torch.uint8 or not dst.is_contiguous():
+            raise ValueError("image buffer: contiguous uint8")
+        self._bind()
+        _check(lib().repstep_image_write(self._ctx, int(step), _ptr(w), _ptr(m), _ptr(v),
+                                         _ptr(dst), dst.numel(), 0 if dst.is_cuda else 1),
+               "image_write")
+
+    def image_read(self, src: torch.Tensor, w, m, v) -> int:
+        self._state(w, m, v)
+        if src.dtype != torch.uint8 or not src.is_contiguous():
+            raise ValueError("image buffer: contiguous uint8")
+        step = C.c_int32()
+        self._bind()
+        _check(lib().repstep_image_read(self._ctx, _ptr(src), src.numel(), 0 if src.is_cuda else 1,
+                                        C.byref(step), _ptr(w), _ptr(m), _ptr(v)), "image_read")
+        return int(step.value)
+
+    def sync(self) -> int:
+        """Synchronise the stream; return the device flags (raises on a kernel timeout)."""
+        flags = C.c_uint32()
+        self._bind()
+        rc = lib().repstep_sync(self._ctx, C.byref(flags))
+        if rc == 6:
+            raise RepstepError(rc, f"flags=0x{flags.value:x}")
+        _check(rc, "sync")
+        return int(flags.value)
+
+    def launch_count(self) -> int:
+        return int(lib().repstep_launch_count(self._ctx))
+
+    def last_cuda_error(self) -> int:
+        return int(lib().repstep_last_cuda_error(self._ctx))
+
+    # ---------------------------------------------------------------- workspace views
+    def _view(self, off: int, count: int, dtype):
+        item = torch.empty(0, dtype=dtype).element_size()
+        return self.workspace[off: off + count * item].view(dtype)
+
+    def g_view(self):
+        return self._view(self.layout.g, self.n, torch.float32)
+
+    def chunk_sums_view(self):
+        return self._view(self.layout.chunk_sums, self.c, torch.float32)
+
+    def leaves_view(self):
+        return self._view(self.layout.leaves, 1 + 3 * self.c, torch.int64)
+
+    def scalars_view(self):
+        return self._view(self.layout.scalars, 4, torch.int32)
+
+    def destroy(self):
+        if self._ctx:
+            lib().repstep_destroy(self._ctx)
+            self._ctx = C.c_void_p()
+
+    def __del__(self):
+        try:
+            self.destroy()
+        except Exception:
+            pass

@@ -1,0 +1,214 @@
+/*
+ * repstep.h -- C ABI of the bitwise-reproducible optimizer step for one GB300 (sm_103a).
+ *
+ * One optimizer step is: sum R replica gradients in one canonical tree and average them by
+ * a reciprocal multiply; compute the global l2 norm over fixed 4096-element chunks; clip;
+ * apply AdamW to flat fp32 weights and Adam moments; hash the checkpoint image
+ * [int32 step][uint32 n][w][m][v] with per-chunk digests combined in a Merkle tree.  Every
+ * output bit is fixed by the definition below, independent of the launch configuration,
+ * of how replicas are grouped into nodes, and of how the parameter range is split.
+ *
+ * Sources, by page title and section:
+ *   "OPEN-1B: A Fully Auditable Training Run" (Gensyn): §2.1 Reproducible Operations
+ *     (one fixed reduction order, no implicit fused multiply-add); §3.2 Training Recipe
+ *     (AdamW, decoupled weight decay, global-norm clipping at 1.0); §3.4.2 (pre-clip
+ *     gradient norm); App. A (deterministic gradient reduction: TreeFold over replicas
+ *     with the lower replica on the left, reduce-scatter over shards, App. A.3 average
+ *     via reciprocal multiply); App. B (per-step state hash).
+ *   "grow_a_language_model_checkpoints": Format and Total size (8 + 12 n bytes).
+ *   OLMo-core MoE §12 "Topology-agnostic checkpoint saving and loading" (FP32 weights and
+ *     both moments, canonical element order independent of topology).
+ *
+ * Definitions (every fp32 operation is IEEE binary32 round-to-nearest-even, rounded once,
+ * never contracted into a fused multiply-add; subnormals are kept):
+ *   T(x_0..x_{L-1})  canonical tree: x_0 if L == 1, else T(x_0..x_{k-1}) + T(x_k..x_{L-1})
+ *                    with k the largest power of two below L; lower indices on the left.
+ *   reduce           g_i = T_{r<R}(G_r[i]) * fp32(1/R); bf16 gradients widened exactly.
+ *   norm             s_k = T(g_i*g_i over chunk k = [4096k, min(4096k+4096, n)));
+ *                    S = T(s_0..s_{c-1}), c = ceil(n/4096); norm = sqrt(S)  (pre-clip).
+ *   clip             scale = norm > clip ? clip / norm : 1.
+ *   AdamW            gc = g*scale; m' = b1*m + (1-b1)*gc; v' = b2*v + (1-b2)*(gc*gc);
+ *                    u = (m'/bc1) / (sqrt(v'/bc2) + eps); w' = w*(1 - lr*wd) - lr*u,
+ *                    with 1-b1, 1-b2 and 1-lr*wd each rounded to fp32 once.
+ *   hash             leaves: PF61(header words {step, n}), then PF61 of each 4096-element
+ *                    chunk of w, of m, of v (as 32-bit words); PF61(x_0..x_{W-1}) =
+ *                    (W + sum x_i K^(i+1)) mod (2^61-1), K = floor(2^61 (sqrt5 - 1) / 2).
+ *                    Root = T(leaves) with node N(a,b) = LE64 of BLAKE2b-64(LE64 a||LE64 b).
+ *
+ * Conventions for every call:
+ *   - Device pointers are plain addresses in the current CUDA device's memory, owned by
+ *     the caller (for example PyTorch allocations).  The library allocates no device
+ *     memory: the caller provides one workspace of repstep_workspace_bytes() bytes.
+ *   - All device work is enqueued asynchronously on the context's stream (a cudaStream_t
+ *     passed as void*; NULL is the legacy default stream).  A returned REPSTEP_OK means
+ *     the arguments were valid and the kernels were launched; a fault inside a kernel
+ *     shows up at the next synchronisation, and repstep_sync() reports it.
+ *   - Gradient, weight and moment buffers must be 16-byte aligned; the workspace 256-byte
+ *     aligned.  Misalignment returns REPSTEP_ERR_ALIGN and launches nothing.
+ *   - No call throws; every call returns a status code (repstep_strerror names it).
+ *   - A context is not thread-safe; use one context per host thread or serialise.
+ */
+#ifndef REPSTEP_H
+#define REPSTEP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define REPSTEP_CHUNK 4096u          /* fixed chunk length of the norm and of the hash   */
+#define REPSTEP_MAX_REPLICAS 256u    /* largest R a single reduce accepts                */
+
+enum repstep_status {
+    REPSTEP_OK = 0,
+    REPSTEP_ERR_ARG = 1,       /* null pointer, R == 0, bad range, non-finite hyperparameter */
+    REPSTEP_ERR_ALIGN = 2,     /* a device pointer is not aligned as required               */
+    REPSTEP_ERR_SIZE = 3,      /* n >= 2^32, R > REPSTEP_MAX_REPLICAS, workspace too small   */
+    REPSTEP_ERR_TOPOLOGY = 4,  /* nodes*gpus_per_node != R, or gpus_per_node not a power of
+                                  two while nodes > 1 (the staged sum would leave the
+                                  canonical tree)                                         */
+    REPSTEP_ERR_CUDA = 5,      /* a CUDA runtime call failed; repstep_last_cuda_error()     */
+    REPSTEP_ERR_TIMEOUT = 6,   /* a kernel's bounded wait expired (reported by repstep_sync) */
+    REPSTEP_ERR_STATE = 7,     /* call order: clip before the whole range was reduced, AdamW
+                                  before clip, root before the whole range was updated      */
+    REPSTEP_ERR_FORMAT = 8     /* checkpoint image: wrong size or header                     */
+};
+
+enum repstep_dtype { REPSTEP_F32 = 0, REPSTEP_BF16 = 1 };
+
+/* Device flag bits reported by repstep_sync(). */
+#define REPSTEP_FLAG_NONFINITE_NORM  0x1u  /* the pre-clip norm is NaN or infinite        */
+#define REPSTEP_FLAG_TIMEOUT_REDUCE  0x2u  /* a bounded wait expired in the reduce kernel  */
+#define REPSTEP_FLAG_TIMEOUT_ADAMW   0x4u  /* ... in the AdamW / leaf kernel               */
+#define REPSTEP_FLAG_TIMEOUT_LEAVES  0x8u  /* ... in the standalone leaf kernel            */
+
+typedef struct repstep_ctx repstep_ctx;   /* opaque, host-side only */
+
+typedef struct {
+    uint64_t n;              /* number of fp32 parameters; n < 2^32 (0 is allowed)        */
+    int32_t grad_dtype;      /* enum repstep_dtype of the replica gradients                */
+    int32_t grid_blocks;     /* 0: persistent grid (SM count x resident CTAs); otherwise
+                                the CTA count of the streaming kernels.  Never changes bits. */
+    int32_t block_threads;   /* 0: default; else 128, 256 or 512 compute threads per CTA of
+                                the streaming kernels.  Never changes bits.                */
+    int32_t reserved;        /* must be 0                                                  */
+} repstep_config;
+
+typedef struct {
+    float lr, beta1, beta2, eps, weight_decay;
+    float clip;              /* clip threshold (> 0; +inf disables clipping)               */
+    float bc1, bc2;          /* bias corrections of this step, see repstep_bias_corrections */
+} repstep_hparams;
+
+/* Bytes of device workspace a context with this configuration needs (0 on a bad config).
+ * Layout: g[n] fp32 | chunk sums fp32[c] | norm partials | leaf digests u64[1+3c] |
+ * Merkle partials | PF61 power table u64[4096] | device scalars. */
+size_t repstep_workspace_bytes(const repstep_config *cfg);
+
+/* Byte offsets of the workspace regions (for inspection and tests): g fp32[n], chunk sums
+ * fp32[c], norm partials, leaf digests u64[1+3c] (header leaf first, then the w, m, v
+ * chunks), Merkle partials, PF61 power table u64[4096], device scalars (pre-clip norm fp32,
+ * clip scale fp32, flags u32, pad u32, root u64).  Returns REPSTEP_ERR_ARG on a bad config. */
+typedef struct {
+    uint64_t g, chunk_sums, norm_partials, leaves, merkle_partials, pow_table, scalars, total;
+} repstep_layout;
+int repstep_workspace_layout(const repstep_config *cfg, repstep_layout *out);
+
+/* Create a context over a caller-owned workspace (256-byte aligned, at least
+ * repstep_workspace_bytes(cfg) bytes) on `stream`.  Enqueues the initialisation of the
+ * PF61 power table on the stream.  The workspace must outlive the context. */
+int repstep_create(const repstep_config *cfg, void *d_workspace, size_t workspace_bytes,
+                   void *stream, repstep_ctx **out);
+
+/* Destroy the context (host memory only; does not synchronise the stream). */
+int repstep_destroy(repstep_ctx *ctx);
+
+/* Change the stream later calls enqueue on. */
+int repstep_set_stream(repstep_ctx *ctx, void *stream);
+
+/* Replica reduce (OPEN-1B App. A.1 and A.3) over the element range [begin, begin+count):
+ * g_i = T_{r<R}(G_r[i]) * fp32(1/R) into the workspace, plus the sum of squares of every
+ * 4096-chunk lying wholly inside the range.  d_grads is a HOST array of R device pointers
+ * to full-length gradient buffers (n elements of grad_dtype), in global replica order.
+ * nodes x gpus_per_node (replica r = node*gpus_per_node + gpu) selects a staged sum: each
+ * node's replicas first, then the node partials -- the same bits as the flat tree, which
+ * the call guarantees by rejecting shapes that would differ (REPSTEP_ERR_TOPOLOGY).
+ * Pass nodes = 1, gpus_per_node = R for the flat tree.  Ranges of one step may be reduced
+ * in separate calls (reduce-scatter into shards, OPEN-1B App. A.2); chunks cut by a range
+ * boundary are summed at clip time from the complete g. */
+int repstep_reduce(repstep_ctx *ctx, const void *const *d_grads, uint32_t R, uint32_t nodes,
+                   uint32_t gpus_per_node, uint64_t begin, uint64_t count);
+
+/* Global norm and clip scale (OPEN-1B §3.2, §3.4.2) from the chunk sums of the reduced g.
+ * Requires the reduce calls since the previous clip to have covered exactly n elements
+ * (else REPSTEP_ERR_STATE).  Writes the pre-clip norm and the scale to the optional device
+ * outputs (fp32, 4-byte aligned) and keeps them in the workspace for repstep_adamw.
+ * clip must be > 0 (+inf: never clip). */
+int repstep_clip(repstep_ctx *ctx, float clip, float *d_norm_out, float *d_scale_out);
+
+/* Clipped AdamW over [begin, begin+count) of the full-length fp32 arrays w, m, v (updated
+ * in place), using g and the scale from the last reduce/clip.  Also writes the PF61 leaf
+ * digest of every new w, m and v chunk lying wholly inside the range; repstep_root()
+ * completes the others.  All calls of one step must pass the same w, m, v base pointers.
+ * Requires repstep_clip() since the last reduce (else REPSTEP_ERR_STATE). */
+int repstep_adamw(repstep_ctx *ctx, float *d_w, float *d_m, float *d_v,
+                  const repstep_hparams *hp, uint64_t begin, uint64_t count);
+
+/* Merkle root of the state left by the repstep_adamw calls since the last clip, whose
+ * ranges must total n elements (else REPSTEP_ERR_STATE); the header carries `step`.
+ * Chunks cut by a range boundary get their leaves recomputed from the final w, m, v.
+ * Writes the u64 root to d_root_out (8-byte aligned device pointer). */
+int repstep_root(repstep_ctx *ctx, int32_t step, uint64_t *d_root_out);
+
+/* Standalone state hash (OPEN-1B App. B) of an arbitrary (step, w, m, v): every leaf is
+ * computed from the arrays, then the Merkle root.  Equals repstep_root() after a step. */
+int repstep_hash(repstep_ctx *ctx, int32_t step, const float *d_w, const float *d_m,
+                 const float *d_v, uint64_t *d_root_out);
+
+/* One whole step: reduce over [0, n) -> clip -> AdamW over [0, n) -> root, bit-identical
+ * to the four separate calls.  `step` is the header's step counter after the update; the
+ * caller sets hp->bc1/bc2 for it (repstep_bias_corrections).  d_norm_out (nullable)
+ * receives the pre-clip norm, d_root_out (nullable) the root. */
+int repstep_step(repstep_ctx *ctx, const void *const *d_grads, uint32_t R, uint32_t nodes,
+                 uint32_t gpus_per_node, float *d_w, float *d_m, float *d_v,
+                 const repstep_hparams *hp, int32_t step, float *d_norm_out,
+                 uint64_t *d_root_out);
+
+/* Checkpoint image ("grow_a_language_model_checkpoints", Format):
+ * [LE int32 step][LE uint32 n][n fp32 w][n fp32 m][n fp32 v], 8 + 12n bytes, written to
+ * dst (device memory, or host memory when dst_is_host != 0) on the context's stream. */
+uint64_t repstep_image_bytes(uint64_t n);
+int repstep_image_write(repstep_ctx *ctx, int32_t step, const float *d_w, const float *d_m,
+                        const float *d_v, void *dst, uint64_t dst_bytes, int dst_is_host);
+
+/* Load an image into w, m, v (device arrays of the context's n).  Rejects (with
+ * REPSTEP_ERR_FORMAT, before copying anything) a buffer whose size is not 8 + 12n or
+ * whose header n differs from the context's n.  *step_out receives the header step. */
+int repstep_image_read(repstep_ctx *ctx, const void *src, uint64_t src_bytes, int src_is_host,
+                       int32_t *step_out, float *d_w, float *d_m, float *d_v);
+
+/* Bias corrections for step t >= 1: p_j = beta_j^t as t repeated fp32 products,
+ * bc_j = 1 - p_j (the reading taken for AdamW's bias correction; computed on the host). */
+void repstep_bias_corrections(float beta1, float beta2, int32_t t, float *bc1, float *bc2);
+
+/* Synchronise the context's stream and read the device flags (REPSTEP_FLAG_*; nullable
+ * output).  Returns REPSTEP_ERR_CUDA if the stream reported an error, REPSTEP_ERR_TIMEOUT
+ * if a kernel's bounded wait expired, else REPSTEP_OK.  Clears the timeout flags. */
+int repstep_sync(repstep_ctx *ctx, uint32_t *flags_out);
+
+/* Kernels this context has launched so far. */
+uint64_t repstep_launch_count(const repstep_ctx *ctx);
+
+/* The cudaError_t of the last failed CUDA call (0 if none). */
+int repstep_last_cuda_error(const repstep_ctx *ctx);
+
+/* Static name of a status code. */
+const char *repstep_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* REPSTEP_H */

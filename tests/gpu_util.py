@@ -1,0 +1,78 @@
+"""Shared helpers for the GPU parity tests: build once, generate identical inputs for the
+CUDA path and the oracle, and compare bit patterns (0 ulp; NaNs compared by class)."""
+import numpy as np
+import torch
+
+from bitwise_reproducible_step_gb300 import inputs as I
+from bitwise_reproducible_step_gb300 import repstep as rs
+from oracle import oracle as O
+
+HP = I.default_hparams()
+F32_WL = I.WORKLOADS["flat1m_r4"]
+BF16_WL = I.WORKLOADS["flat3000m_r8_bf16_spiked_shards"]
+
+
+def ensure_built():
+    from bitwise_reproducible_step_gb300 import build
+    build.build()
+    rs.lib()
+
+
+def hp_for(t, clip=None):
+    return rs.hparams(lr=HP["lr"], beta1=HP["beta1"], beta2=HP["beta2"], eps=HP["eps"],
+                      weight_decay=HP["wd"], clip=HP["clip"] if clip is None else clip, t=t)
+
+
+def bits32(x) -> np.ndarray:
+    if isinstance(x, torch.Tensor):
+        x = x.detach().cpu().contiguous().numpy()
+    return np.ascontiguousarray(x).view(np.uint32)
+
+
+def diff_report(got, want):
+    """(differing slots, relFro, max|delta|) between two fp32 arrays -- the statistics of the
+    cross-process reproducibility note ("The measurement" section)."""
+    g = np.asarray(got, np.float32).astype(np.float64)
+    w = np.asarray(want, np.float32).astype(np.float64)
+    gb, wb = bits32(np.asarray(got, np.float32)), bits32(np.asarray(want, np.float32))
+    both_nan = np.isnan(g) & np.isnan(w)
+    differing = int(np.count_nonzero((gb != wb) & ~both_nan))
+    fin = np.isfinite(g) & np.isfinite(w)
+    d = np.where(fin, g - w, 0.0)
+    den = np.linalg.norm(np.where(fin, w, 0.0))
+    rel = float(np.linalg.norm(d) / den) if den > 0 else float(np.linalg.norm(d))
+    mx = float(np.max(np.abs(d))) if d.size else 0.0
+    return differing, rel, mx
+
+
+def assert_same_f32(got, want, what=""):
+    got = np.asarray(got.detach().cpu() if isinstance(got, torch.Tensor) else got, np.float32)
+    want = np.asarray(want, np.float32)
+    assert got.shape == want.shape, (what, got.shape, want.shape)
+    differing, rel, mx = diff_report(got, want)
+    assert differing == 0, f"{what}: {differing} differing slots, relFro {rel:.3e}, max|d| {mx:.3e}"
+
+
+def gen_grads(n, R, t, dtype=torch.float32, scale=1.0, device="cuda"):
+    wl = BF16_WL if dtype == torch.bfloat16 else F32_WL
+    out = []
+    for r in range(R):
+        g = I.gen_grad(wl, t, r, n=n, device=device)
+        if scale != 1.0:
+            g = (g.float() * scale).to(g.dtype)
+        out.append(g.contiguous())
+    return out
+
+
+def oracle_grads(grads):
+    return [I.to_numpy(g) for g in grads]
+
+
+def root_of(t: torch.Tensor) -> int:
+    return int(t.cpu().numpy().view(np.uint64)[0])
+
+
+def oracle_step(grads_np, w, m, v, t, nodes=1, clip=None):
+    return O.step(grads_np, w, m, v, lr=HP["lr"], beta1=HP["beta1"], beta2=HP["beta2"],
+                  eps=HP["eps"], wd=HP["wd"], clip=HP["clip"] if clip is None else clip, t=t,
+                  nodes=nodes)

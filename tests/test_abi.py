@@ -1,0 +1,99 @@
+"""The C ABI library loads and exports every function include/repstep.h declares; host-only
+entry points (sizes, layout, bias corrections, status names) behave as documented.  CPU
+only: no call here touches a GPU."""
+import ctypes as C
+import os
+import re
+import subprocess
+
+import numpy as np
+import pytest
+
+from bitwise_reproducible_step_gb300 import repstep as rs
+from oracle import oracle as O
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "repstep.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    from bitwise_reproducible_step_gb300 import build
+    build.build()
+    return rs.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(repstep_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_exports():
+    assert declared_functions() == sorted(rs.EXPORTS)
+
+
+def test_every_declared_symbol_is_exported(L):
+    out = subprocess.run(["nm", "-D", "--defined-only", rs.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\b(repstep_[a-z_]+)\b", out))
+    for name in declared_functions():
+        assert name in exported, name
+        assert getattr(L, name) is not None
+
+
+def test_status_strings(L):
+    for code in range(9):
+        assert rs.strerror(code) and rs.strerror(code) != "unknown status"
+    assert rs.strerror(99) == "unknown status"
+
+
+def test_bias_corrections_match_oracle(L):
+    for t in [1, 2, 3, 5, 10, 100, 4000]:
+        got = rs.bias_corrections(np.float32(0.9), np.float32(0.999), t)
+        want = O.bias_corrections(0.9, 0.999, t)
+        assert np.float32(got[0]).view(np.uint32) == want[0].view(np.uint32)
+        assert np.float32(got[1]).view(np.uint32) == want[1].view(np.uint32)
+
+
+def test_workspace_sizes_and_layout(L):
+    for n in [0, 1, 4095, 4096, 4097, 12_800_000, 1_200_000_000, 3_000_000_000, 2 ** 32 - 1]:
+        b = rs.workspace_bytes(n)
+        assert b >= 4 * n + 8 * (1 + 3 * ((n + 4095) // 4096))
+        cfg = rs.Config(n, 0, 0, 0, 0)
+        lay = rs.Layout()
+        assert L.repstep_workspace_layout(C.byref(cfg), C.byref(lay)) == 0
+        offs = [lay.g, lay.chunk_sums, lay.norm_partials, lay.leaves, lay.merkle_partials,
+                lay.pow_table, lay.scalars, lay.total]
+        assert offs == sorted(offs) and all(o % 256 == 0 for o in offs)
+        assert lay.total == b
+        assert lay.chunk_sums >= 4 * n and lay.leaves - lay.norm_partials >= 4
+
+
+def test_bad_configs_rejected(L):
+    assert rs.workspace_bytes(2 ** 32) == 0
+    cfg = rs.Config(10, 5, 0, 0, 0)
+    assert L.repstep_workspace_bytes(C.byref(cfg)) == 0
+    cfg = rs.Config(10, 0, 0, 300, 0)
+    assert L.repstep_workspace_bytes(C.byref(cfg)) == 0
+    cfg = rs.Config(10, 0, -1, 0, 0)
+    assert L.repstep_workspace_bytes(C.byref(cfg)) == 0
+
+
+def test_create_rejects_before_touching_a_device(L):
+    ctx = C.c_void_p()
+    cfg = rs.Config(100, 0, 0, 0, 0)
+    # null workspace, misaligned workspace, too small: all host-side checks
+    assert L.repstep_create(C.byref(cfg), None, 10 ** 6, None, C.byref(ctx)) == 1
+    assert L.repstep_create(C.byref(cfg), C.c_void_p(0x1000 + 8), 10 ** 6, None, C.byref(ctx)) == 2
+    assert L.repstep_create(C.byref(cfg), C.c_void_p(0x1000), 16, None, C.byref(ctx)) == 3
+    assert not ctx.value
+    # every entry point rejects a null context
+    assert L.repstep_reduce(None, None, 1, 1, 1, 0, 0) == 1
+    assert L.repstep_clip(None, 1.0, None, None) == 1
+    assert L.repstep_sync(None, None) == 1
+
+
+def test_image_bytes(L):
+    assert rs.image_bytes(12_800_000) == 153_600_008 == O.image_bytes(12_800_000)
+    assert rs.image_bytes(3_000_000_000) == 36_000_000_008

@@ -1,0 +1,182 @@
+"""Full-size workloads on one GB300, in the launch configuration the benchmark times.
+
+The oracle cannot redo a 1.2e9- or 3e9-parameter step in seconds, so each step is checked
+as a chain of pieces the oracle computes exactly:
+  * sampled whole chunks (first, last/ragged, and ~250 seeded random ones): g, the chunk
+    sum of squares, the AdamW outputs and the three leaf digests, from the same gathered
+    inputs, bit for bit;
+  * the pre-clip norm and clip scale: the oracle's canonical tree over ALL chunk sums;
+  * the Merkle root: the oracle's tree over ALL leaf digests;
+and every invariance (launch shape, topology, shard ranges) is checked on the full arrays
+by exact equality on the device.
+"""
+import numpy as np
+import pytest
+import torch
+
+from bitwise_reproducible_step_gb300 import inputs as I
+from bitwise_reproducible_step_gb300 import repstep as rs
+from oracle import oracle as O
+from tests import gpu_util as U
+
+pytestmark = [pytest.mark.gpu, pytest.mark.big]
+
+CH = 4096
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    U.ensure_built()
+    torch.cuda.set_device(0)
+    yield
+    torch.cuda.empty_cache()
+
+
+def sample_chunks(c, k=254, seed=0):
+    rng = np.random.default_rng(seed)
+    pick = set(rng.choice(c, size=min(k, c), replace=False).tolist())
+    pick.update([0, c - 1])
+    return np.array(sorted(pick), dtype=np.int64)
+
+
+def gather(t: torch.Tensor, chunks, n):
+    """Host copy of whole chunks of a device array (ragged last chunk kept short)."""
+    out = []
+    for k in chunks:
+        lo, hi = int(k) * CH, min(int(k) * CH + CH, n)
+        out.append(t[lo:hi])
+    return [x.cpu() for x in out]
+
+
+def check_step_chain(ctx, grads_before, state_before, w, m, v, t, chunks, n, norm_t, root_t):
+    """grads_before / state_before: host chunk lists gathered before the step."""
+    c = (n + CH - 1) // CH
+    chunk_sums = ctx.chunk_sums_view().cpu().numpy()
+    # norm and scale: oracle tree over all GPU chunk sums
+    S = O.tree_sum(chunk_sums)
+    norm = np.sqrt(S, dtype=np.float32)
+    norm_o = np.float32(np.sqrt(np.float32(S)))
+    assert np.float32(norm_t.item()) == norm_o == norm
+    scale = O.clip_scale(norm_o, U.HP["clip"])
+    bc1, bc2 = O.bias_corrections(U.HP["beta1"], U.HP["beta2"], t)
+    leaves = ctx.leaves_view().cpu().numpy().view(np.uint64)
+    g_dev = ctx.g_view()
+    new_w, new_m, new_v = gather(w, chunks, n), gather(m, chunks, n), gather(v, chunks, n)
+    g_got = gather(g_dev, chunks, n)
+    for i, k in enumerate(chunks):
+        G = [I.to_numpy(gr[i]) for gr in grads_before]
+        g = O.reduce(G)
+        U.assert_same_f32(g_got[i], g, f"g chunk {k}")
+        _, s = O.norm(g, with_chunks=True)
+        assert s.view(np.uint32)[0] == chunk_sums[k:k + 1].view(np.uint32)[0], f"chunk sum {k}"
+        w0, m0, v0 = (x[i].numpy() for x in state_before)
+        w1, m1, v1 = O.adamw(w0, m0, v0, g, scale, U.HP["lr"], U.HP["beta1"], U.HP["beta2"],
+                             U.HP["eps"], U.HP["wd"], bc1, bc2)
+        U.assert_same_f32(new_w[i], w1, f"w chunk {k}")
+        U.assert_same_f32(new_m[i], m1, f"m chunk {k}")
+        U.assert_same_f32(new_v[i], v1, f"v chunk {k}")
+        for a, arr in enumerate((w1, m1, v1)):
+            assert leaves[1 + a * c + k] == O.pf61(arr.view(np.uint32)), f"leaf {a} chunk {k}"
+    hdr = O.pf61(np.array([t, n], dtype=np.uint64).astype(np.uint32))
+    assert leaves[0] == hdr
+    assert U.root_of(root_t) == O.merkle_root(leaves)
+    return float(norm_o)
+
+
+def run_big(wl, steps, ranges=None, compare_unsharded=False):
+    n, R = wl.n, wl.R
+    dev = torch.device("cuda", 0)
+    gdt = torch.bfloat16 if wl.grad_dtype == "bf16" else torch.float32
+    c = (n + CH - 1) // CH
+    chunks = sample_chunks(c)
+    if ranges:   # also sample the chunks the shard boundaries cut
+        extra = {lo // CH for lo, _ in ranges[1:]}
+        chunks = np.array(sorted(set(chunks.tolist()) | extra), dtype=np.int64)
+    ctx = rs.Repstep(n, grad_dtype=gdt, device=dev)
+    w, m, v = I.gen_state(wl, device=dev)
+    twin = None
+    if compare_unsharded:
+        twin = (rs.Repstep(n, grad_dtype=gdt, device=dev), w.clone(), m.clone(), v.clone())
+    grads = [torch.empty(n, dtype=gdt, device=dev) for _ in range(R)]
+    norm = torch.empty(1, dtype=torch.float32, device=dev)
+    root = torch.empty(1, dtype=torch.int64, device=dev)
+    norms = []
+    for t in range(1, steps + 1):
+        for r in range(R):
+            I.gen_grad(wl, t, r, device=dev, out=grads[r])
+        g_before = [gather(gr, chunks, n) for gr in grads]
+        s_before = (gather(w, chunks, n), gather(m, chunks, n), gather(v, chunks, n))
+        hp = U.hp_for(t)
+        if ranges:
+            for lo, hi in ranges:
+                ctx.reduce(grads, begin=lo, count=hi - lo)
+            ctx.clip(hp.clip, norm_out=norm)
+            for lo, hi in ranges:
+                ctx.adamw(w, m, v, hp, begin=lo, count=hi - lo)
+            ctx.root(t, root_out=root)
+        else:
+            ctx.step(grads, w, m, v, hp, step=t, norm_out=norm, root_out=root)
+        assert ctx.sync() & ~rs.FLAG_NONFINITE_NORM == 0
+        norms.append(check_step_chain(ctx, g_before, s_before, w, m, v, t, chunks, n, norm, root))
+        if twin is not None:
+            tc, tw, tm, tv = twin
+            tn = torch.empty(1, dtype=torch.float32, device=dev)
+            tr = torch.empty(1, dtype=torch.int64, device=dev)
+            tc.step(grads, tw, tm, tv, hp, step=t, norm_out=tn, root_out=tr)
+            tc.sync()
+            assert torch.equal(tw.view(torch.int32), w.view(torch.int32))
+            assert torch.equal(tm.view(torch.int32), m.view(torch.int32))
+            assert torch.equal(tv.view(torch.int32), v.view(torch.int32))
+            assert tn.item() == norm.item() and U.root_of(tr) == U.root_of(root)
+    return norms
+
+
+def test_flat1200m_r8_segscale():
+    wl = I.WORKLOADS["flat1200m_r8_segscale"]
+    norms = run_big(wl, steps=2)
+    assert all(x < 1.0 for x in norms)              # tiny segment-scaled grads: no clip
+
+
+def test_flat3000m_r8_bf16_spiked_shards():
+    wl = I.WORKLOADS["flat3000m_r8_bf16_spiked_shards"]
+    norms = run_big(wl, steps=2, ranges=I.shard_ranges(wl.n, wl.shards), compare_unsharded=True)
+    assert all(x > 1.0 for x in norms)              # 1% spikes x 1e3 force the clip
+
+
+def test_flat268m_r32_topologies_grids_blocks():
+    """4 topologies x 5 grid sizes x 3 block sizes: every output bit equal, and the
+    default configuration equal to the oracle on the sampled chain."""
+    wl = I.WORKLOADS["flat268m_r32_topologies"]
+    n, R = wl.n, wl.R
+    dev = torch.device("cuda", 0)
+    c = (n + CH - 1) // CH
+    sm = torch.cuda.get_device_properties(0).multi_processor_count
+    grads = [I.gen_grad(wl, 1, r, device=dev) for r in range(R)]
+    w0, m0, v0 = I.gen_state(wl, device=dev)
+    m0.copy_(I.gen_grad(wl, 9, 0, device=dev))       # non-zero moments: a mid-run step
+    v0.copy_(I.gen_grad(wl, 9, 1, device=dev).square())
+    chunks = sample_chunks(c, k=126, seed=4)
+    g_before = [gather(gr, chunks, n) for gr in grads]
+    s_before = (gather(w0, chunks, n), gather(m0, chunks, n), gather(v0, chunks, n))
+    hp = U.hp_for(3)
+    w, m, v = w0.clone(), m0.clone(), v0.clone()
+    ref = None
+    for nodes, gpn in wl.topologies:
+        for grid in [0, 1, 7, sm, 2 * sm + 1, c]:
+            for nt in ([128, 256, 512] if grid in (0, sm) else [256]):
+                ctx = rs.Repstep(n, device=dev, grid_blocks=grid, block_threads=nt)
+                w.copy_(w0); m.copy_(m0); v.copy_(v0)
+                norm = torch.empty(1, dtype=torch.float32, device=dev)
+                root = torch.empty(1, dtype=torch.int64, device=dev)
+                ctx.step(grads, w, m, v, hp, step=3, norm_out=norm, root_out=root,
+                         nodes=nodes, gpus_per_node=gpn)
+                ctx.sync()
+                if ref is None:
+                    check_step_chain(ctx, g_before, s_before, w, m, v, 3, chunks, n, norm, root)
+                    ref = (w.clone(), m.clone(), v.clone(), norm.item(), U.root_of(root))
+                else:
+                    assert torch.equal(w.view(torch.int32), ref[0].view(torch.int32)), (nodes, grid, nt)
+                    assert torch.equal(m.view(torch.int32), ref[1].view(torch.int32))
+                    assert torch.equal(v.view(torch.int32), ref[2].view(torch.int32))
+                    assert norm.item() == ref[3] and U.root_of(root) == ref[4]
+                ctx.destroy()

@@ -1,0 +1,326 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle, bit for bit (0 ulp),
+on the same seeded inputs.  Sizes span several tiles and chunks with ragged tails."""
+import numpy as np
+import pytest
+import torch
+
+from bitwise_reproducible_step_gb300 import inputs as I
+from bitwise_reproducible_step_gb300 import repstep as rs
+from oracle import oracle as O
+from tests import gpu_util as U
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    U.ensure_built()
+    torch.cuda.set_device(0)
+
+
+def run_steps(n, R, dtype=torch.float32, steps=3, scales=(1.0, 3000.0, 1.0), ctx_kw=None,
+              nodes=1, check_intermediates=True):
+    """Run `steps` fused steps on the GPU and in the oracle; assert every output bit."""
+    dev = torch.device("cuda", 0)
+    ctx = rs.Repstep(n, grad_dtype=dtype, device=dev, **(ctx_kw or {}))
+    w, m, v = I.gen_state(U.F32_WL, n=n, device=dev)
+    ow, om, ov = w.cpu().numpy(), m.cpu().numpy(), v.cpu().numpy()
+    norm = torch.empty(1, dtype=torch.float32, device=dev)
+    root = torch.empty(1, dtype=torch.int64, device=dev)
+    out = []
+    for t in range(1, steps + 1):
+        grads = U.gen_grads(n, R, t, dtype, scale=scales[(t - 1) % len(scales)])
+        gnp = U.oracle_grads(grads)
+        ctx.step(grads, w, m, v, U.hp_for(t), step=t, norm_out=norm, root_out=root, nodes=nodes)
+        flags = ctx.sync()
+        ref = U.oracle_step(gnp, ow, om, ov, t, nodes=nodes)
+        ow, om, ov = ref["w"], ref["m"], ref["v"]
+        if check_intermediates and n > 0:
+            U.assert_same_f32(ctx.g_view(), O.reduce(gnp), f"g step {t}")
+            _, chunks = O.norm(O.reduce(gnp), with_chunks=True)
+            U.assert_same_f32(ctx.chunk_sums_view(), chunks, f"chunk sums step {t}")
+            leaves = ctx.leaves_view().cpu().numpy().view(np.uint64)
+            assert np.array_equal(leaves, O.leaves(t, ow, om, ov)), f"leaves step {t}"
+        U.assert_same_f32(w, ow, f"w step {t}")
+        U.assert_same_f32(m, om, f"m step {t}")
+        U.assert_same_f32(v, ov, f"v step {t}")
+        U.assert_same_f32(norm, np.array([ref["norm"]], np.float32), f"norm step {t}")
+        assert U.root_of(root) == ref["root"], f"root step {t}"
+        assert bool(flags & rs.FLAG_NONFINITE_NORM) == (not np.isfinite(ref["norm"]))
+        out.append(dict(norm=float(ref["norm"]), root=ref["root"]))
+    ctx.destroy()
+    return out
+
+
+@pytest.mark.parametrize("n,R,dtype", [
+    (1, 1, torch.float32),
+    (5, 3, torch.float32),
+    (4095, 4, torch.float32),
+    (4096, 8, torch.float32),
+    (4097, 5, torch.float32),
+    (3 * 4096 + 1234, 8, torch.bfloat16),
+    (65536 + 7, 9, torch.float32),
+    (100003, 16, torch.float32),
+    (50001, 32, torch.float32),
+    (200002, 2, torch.bfloat16),
+    (123457, 12, torch.bfloat16),
+    (40000, 33, torch.float32),
+])
+def test_step_matches_oracle(n, R, dtype):
+    res = run_steps(n, R, dtype)
+    if n >= 4096:
+        assert any(r["norm"] > 1.0 for r in res)  # the clip was exercised
+
+
+def test_empty_parameter_vector():
+    dev = torch.device("cuda", 0)
+    ctx = rs.Repstep(0, device=dev)
+    z = torch.zeros(1, dtype=torch.float32, device=dev)
+    grads = [torch.zeros(1, dtype=torch.float32, device=dev)] * 2
+    norm = torch.empty(1, dtype=torch.float32, device=dev)
+    root = torch.empty(1, dtype=torch.int64, device=dev)
+    ctx.step(grads, z, z.clone(), z.clone(), U.hp_for(1), step=1, norm_out=norm, root_out=root)
+    ctx.sync()
+    e = np.zeros(0, np.float32)
+    assert float(norm.item()) == 0.0
+    assert U.root_of(root) == O.state_hash(1, e, e, e)
+
+
+@pytest.mark.parametrize("nt", [128, 256, 512])
+def test_launch_shape_invariance(nt):
+    n, R = 7 * 4096 * 5 + 333, 8
+    c = (n + 4095) // 4096
+    sm = torch.cuda.get_device_properties(0).multi_processor_count
+    base = None
+    for grid in [1, 7, sm, 2 * sm + 1, c]:
+        res = run_steps(n, R, steps=2, ctx_kw=dict(grid_blocks=grid, block_threads=nt),
+                        check_intermediates=(grid == 7))
+        if base is None:
+            base = res
+        assert res == base
+
+
+def test_topologies_equal_flat_and_oracle():
+    n, R = 20000, 32
+    flat = run_steps(n, R, steps=2, check_intermediates=False)
+    for nodes in [4, 8, 32, 2, 16]:
+        assert run_steps(n, R, steps=2, nodes=nodes, check_intermediates=False) == flat
+
+
+def test_topology_rejected():
+    dev = torch.device("cuda", 0)
+    ctx = rs.Repstep(1000, device=dev)
+    grads = U.gen_grads(1000, 6, 1)
+    with pytest.raises(rs.RepstepError) as ei:
+        ctx.reduce(grads, nodes=2, gpus_per_node=3)
+    assert ei.value.code == 4
+    with pytest.raises(rs.RepstepError) as ei:
+        ctx.reduce(grads, nodes=4, gpus_per_node=2)      # 4 x 2 != 6
+    assert ei.value.code == 4
+
+
+def _shard_run(n, R, ranges, dtype=torch.float32, steps=2):
+    """Sharded reduce/AdamW calls vs one fused step: identical bits, and equal to the oracle."""
+    dev = torch.device("cuda", 0)
+    a = rs.Repstep(n, grad_dtype=dtype, device=dev)
+    b = rs.Repstep(n, grad_dtype=dtype, device=dev)
+    wa, ma, va = I.gen_state(U.F32_WL, n=n, device=dev)
+    wb, mb, vb = wa.clone(), ma.clone(), va.clone()
+    ow, om, ov = wa.cpu().numpy(), ma.cpu().numpy(), va.cpu().numpy()
+    na = torch.empty(1, dtype=torch.float32, device=dev)
+    nb = torch.empty(1, dtype=torch.float32, device=dev)
+    ra = torch.empty(1, dtype=torch.int64, device=dev)
+    rb = torch.empty(1, dtype=torch.int64, device=dev)
+    for t in range(1, steps + 1):
+        grads = U.gen_grads(n, R, t, dtype, scale=3000.0 if t == 1 else 1.0)
+        hp = U.hp_for(t)
+        a.step(grads, wa, ma, va, hp, step=t, norm_out=na, root_out=ra)
+        for lo, hi in ranges:
+            b.reduce(grads, begin=lo, count=hi - lo)
+        b.clip(hp.clip, norm_out=nb)
+        for lo, hi in reversed(ranges):
+            b.adamw(wb, mb, vb, hp, begin=lo, count=hi - lo)
+        b.root(t, root_out=rb)
+        a.sync(); b.sync()
+        ref = U.oracle_step(U.oracle_grads(grads), ow, om, ov, t)
+        ow, om, ov = ref["w"], ref["m"], ref["v"]
+        for x, y, name in [(wa, wb, "w"), (ma, mb, "m"), (va, vb, "v")]:
+            U.assert_same_f32(y, x.cpu().numpy(), f"sharded {name}")
+        U.assert_same_f32(wa, ow, "w vs oracle")
+        assert float(na.item()) == float(nb.item()) == float(ref["norm"])
+        assert U.root_of(ra) == U.root_of(rb) == ref["root"]
+
+
+def test_shard_ranges_equal_unsharded():
+    n = 8 * 37_501 + 5            # boundaries fall mid-chunk, not on 16-byte multiples
+    _shard_run(n, 8, I.shard_ranges(n, 8))
+    # ragged ranges, several inside one chunk
+    _shard_run(50_000, 4, [(0, 3), (3, 4100), (4100, 4101), (4101, 12_289), (12_289, 50_000)])
+
+
+def test_shard_ranges_bf16():
+    n = 3 * 4096 * 8 + 17
+    _shard_run(n, 8, I.shard_ranges(n, 8), dtype=torch.bfloat16)
+
+
+def test_fused_equals_separate_calls_and_standalone_hash():
+    n, R = 4096 * 9 + 100, 8
+    dev = torch.device("cuda", 0)
+    a = rs.Repstep(n, device=dev)
+    b = rs.Repstep(n, device=dev)
+    wa, ma, va = I.gen_state(U.F32_WL, n=n, device=dev)
+    wb, mb, vb = wa.clone(), ma.clone(), va.clone()
+    r = torch.empty(4, dtype=torch.int64, device=dev)
+    nrm = torch.empty(2, dtype=torch.float32, device=dev)
+    # hash of the initial state (step 0) equals the oracle's
+    a.hash(0, wa, ma, va, root_out=r[3:])
+    a.sync()
+    assert U.root_of(r[3:]) == O.state_hash(0, wa.cpu().numpy(), ma.cpu().numpy(), va.cpu().numpy())
+    for t in (1, 2):
+        grads = U.gen_grads(n, R, t, scale=2000.0)
+        hp = U.hp_for(t)
+        a.step(grads, wa, ma, va, hp, step=t, norm_out=nrm[0:1], root_out=r[0:1])
+        b.reduce(grads)
+        b.clip(hp.clip, norm_out=nrm[1:2])
+        b.adamw(wb, mb, vb, hp)
+        b.root(t, root_out=r[1:2])
+        b.hash(t, wb, mb, vb, root_out=r[2:3])
+        a.sync(); b.sync()
+        U.assert_same_f32(wb, wa.cpu().numpy(), "w")
+        assert nrm[0].item() == nrm[1].item()
+        rr = r.cpu().numpy().view(np.uint64)
+        assert rr[0] == rr[1] == rr[2]
+
+
+def test_call_order_is_enforced():
+    n = 5000
+    dev = torch.device("cuda", 0)
+    ctx = rs.Repstep(n, device=dev)
+    w, m, v = I.gen_state(U.F32_WL, n=n, device=dev)
+    grads = U.gen_grads(n, 2, 1)
+    with pytest.raises(rs.RepstepError) as ei:
+        ctx.adamw(w, m, v, U.hp_for(1))           # no clip yet
+    assert ei.value.code == 7
+    ctx.reduce(grads, begin=0, count=1000)
+    with pytest.raises(rs.RepstepError) as ei:
+        ctx.clip(1.0)                             # only part of the range reduced
+    assert ei.value.code == 7
+    ctx.reduce(grads, begin=1000, count=n - 1000)
+    ctx.clip(1.0)
+    ctx.adamw(w, m, v, U.hp_for(1), begin=0, count=10)
+    with pytest.raises(rs.RepstepError) as ei:
+        ctx.root(1)                               # AdamW covered 10 of n elements
+    assert ei.value.code == 7
+    with pytest.raises(rs.RepstepError) as ei:
+        ctx.reduce(grads, begin=n - 5, count=10)  # out of range
+    assert ei.value.code == 1
+    ctx.sync()
+
+
+def test_misaligned_pointers_rejected():
+    n = 1000
+    dev = torch.device("cuda", 0)
+    ctx = rs.Repstep(n, device=dev)
+    buf = torch.zeros(n + 8, dtype=torch.float32, device=dev)
+    grads = [buf[1:n + 1]]                        # 4-byte offset
+    with pytest.raises(rs.RepstepError) as ei:
+        ctx.reduce(grads)
+    assert ei.value.code == 2
+
+
+def test_image_round_trip_and_guards():
+    n = 3 * 4096 + 77
+    dev = torch.device("cuda", 0)
+    ctx = rs.Repstep(n, device=dev)
+    w, m, v = I.gen_state(U.F32_WL, n=n, device=dev)
+    m.normal_(); v.uniform_()
+    img_d = torch.empty(rs.image_bytes(n), dtype=torch.uint8, device=dev)
+    img_h = torch.empty(rs.image_bytes(n), dtype=torch.uint8).pin_memory()
+    ctx.image_write(7, w, m, v, img_d)
+    ctx.image_write(7, w, m, v, img_h)
+    ctx.sync()
+    want = O.image(7, w.cpu().numpy(), m.cpu().numpy(), v.cpu().numpy())
+    assert img_d.cpu().numpy().tobytes() == want
+    assert img_h.numpy().tobytes() == want
+    w2, m2, v2 = torch.empty_like(w), torch.empty_like(m), torch.empty_like(v)
+    assert ctx.image_read(img_d, w2, m2, v2) == 7
+    ctx.sync()
+    assert torch.equal(w2.view(torch.int32), w.view(torch.int32))
+    assert torch.equal(v2.view(torch.int32), v.view(torch.int32))
+    # the image hash equals the state hash of its contents
+    r = torch.empty(1, dtype=torch.int64, device=dev)
+    ctx.hash(7, w2, m2, v2, root_out=r)
+    ctx.sync()
+    assert U.root_of(r) == O.state_hash(7, w.cpu().numpy(), m.cpu().numpy(), v.cpu().numpy())
+    # a check that cannot fail is not a check: truncated, oversized, wrong header
+    with pytest.raises(rs.RepstepError) as ei:
+        ctx.image_read(img_h[:-4096], w2, m2, v2)
+    assert ei.value.code == 8
+    big = torch.zeros(rs.image_bytes(n) + 4, dtype=torch.uint8)
+    with pytest.raises(rs.RepstepError):
+        ctx.image_read(big, w2, m2, v2)
+    bad = img_h.clone()
+    bad[4] ^= 1                                   # header n off by one
+    with pytest.raises(rs.RepstepError) as ei:
+        ctx.image_read(bad, w2, m2, v2)
+    assert ei.value.code == 8
+
+
+def test_nonfinite_gradient_sets_flag():
+    n = 9000
+    dev = torch.device("cuda", 0)
+    grads = U.gen_grads(n, 4, 1)
+    grads[2][4321] = float("nan")
+    ctx = rs.Repstep(n, device=dev)
+    w, m, v = I.gen_state(U.F32_WL, n=n, device=dev)
+    ow, om, ov = w.cpu().numpy(), m.cpu().numpy(), v.cpu().numpy()
+    norm = torch.empty(1, dtype=torch.float32, device=dev)
+    ctx.step(grads, w, m, v, U.hp_for(1), step=1, norm_out=norm)
+    flags = ctx.sync()
+    assert flags & rs.FLAG_NONFINITE_NORM
+    assert np.isnan(norm.item())
+    ref = U.oracle_step(U.oracle_grads(grads), ow, om, ov, 1)
+    U.assert_same_f32(w, ref["w"], "w with a NaN gradient")   # NaN slots compared by class
+
+
+def test_relaunch_is_deterministic():
+    n, R = 77_777, 8
+    a = run_steps(n, R, steps=2, check_intermediates=False)
+    b = run_steps(n, R, steps=2, check_intermediates=False)
+    assert a == b
+
+
+def test_workload_flat1m_r4_full():
+    wl = I.WORKLOADS["flat1m_r4"]
+    res = run_steps(wl.n, wl.R, steps=wl.steps, scales=(1.0,))
+    assert all(r["norm"] < 1.0 for r in res)       # N(0, 1e-3) grads over 1M params: no clip
+
+
+def test_workload_flat12m8_student_t_full():
+    """12.8M parameters, 8 Student-t(3) replicas, 10 steps; the 8 + 12n checkpoint image and
+    its Merkle root every step, all bit-identical to the oracle."""
+    wl = I.WORKLOADS["flat12m8_r8_student_t"]
+    n, R = wl.n, wl.R
+    dev = torch.device("cuda", 0)
+    ctx = rs.Repstep(n, device=dev)
+    w, m, v = I.gen_state(wl, device=dev)
+    ow, om, ov = w.cpu().numpy(), m.cpu().numpy(), v.cpu().numpy()
+    norm = torch.empty(1, dtype=torch.float32, device=dev)
+    root = torch.empty(1, dtype=torch.int64, device=dev)
+    img = torch.empty(rs.image_bytes(n), dtype=torch.uint8, device=dev)
+    clipped = 0
+    for t in range(1, wl.steps + 1):
+        grads = [I.gen_grad(wl, t, r, device=dev) for r in range(R)]
+        ctx.step(grads, w, m, v, U.hp_for(t), step=t, norm_out=norm, root_out=root)
+        ctx.image_write(t, w, m, v, img)
+        ctx.sync()
+        ref = U.oracle_step(U.oracle_grads(grads), ow, om, ov, t)
+        ow, om, ov = ref["w"], ref["m"], ref["v"]
+        U.assert_same_f32(w, ow, f"w step {t}")
+        U.assert_same_f32(m, om, f"m step {t}")
+        U.assert_same_f32(v, ov, f"v step {t}")
+        assert float(norm.item()) == float(ref["norm"])
+        assert U.root_of(root) == ref["root"]
+        assert img.cpu().numpy().tobytes() == O.image(t, ow, om, ov)
+        clipped += ref["norm"] > 1.0
+    assert img.numel() == 153_600_008
