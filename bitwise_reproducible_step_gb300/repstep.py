@@ -62,8 +62,9 @@ EXPORTS = [
     "repstep_set_stream", "repstep_reduce", "repstep_clip", "repstep_adamw", "repstep_root",
     "repstep_hash", "repstep_step", "repstep_image_bytes", "repstep_image_write",
     "repstep_image_read", "repstep_bias_corrections", "repstep_sync", "repstep_launch_count",
-    "repstep_last_cuda_error", "repstep_strerror",
+    "repstep_last_cuda_error", "repstep_strerror", "repstep_reduce_norm_noalloc",
 ]
+NOALLOC_MAX_N = 1 << 30
 
 _lib = None
 
@@ -104,6 +105,8 @@ def lib():
     L.repstep_last_cuda_error.argtypes = [vp]
     L.repstep_strerror.argtypes = [C.c_int]
     L.repstep_strerror.restype = C.c_char_p
+    L.repstep_reduce_norm_noalloc.argtypes = [C.POINTER(vp), u32, i32, u64, C.c_float, vp, vp,
+                                              vp, vp]
     _lib = L
     return L
 
@@ -144,6 +147,27 @@ def _dtype_code(dt) -> int:
     if dt == torch.bfloat16:
         return REPSTEP_BF16
     raise TypeError(f"gradient dtype {dt}: float32 or bfloat16")
+
+
+def reduce_norm_noalloc(grads, clip: float, g_out: torch.Tensor, norm_out: torch.Tensor,
+                        scale_out: torch.Tensor | None = None, stream=None):
+    """repstep_reduce_norm_noalloc: averaged gradient and pre-clip norm using the library's
+    fixed scratch array instead of a workspace (for callers that may not allocate device
+    memory; n <= NOALLOC_MAX_N).  Calls whose GPU work overlaps must be serialised."""
+    grads = list(grads)
+    n = g_out.numel()
+    dt = grads[0].dtype
+    for t in grads:
+        if t.dtype != dt or not t.is_cuda or not t.is_contiguous() or t.numel() < n:
+            raise ValueError("gradients: contiguous CUDA tensors of one dtype, >= n elements")
+    for t, want in ((g_out, torch.float32), (norm_out, torch.float32), (scale_out, torch.float32)):
+        if t is not None and (t.dtype != want or not t.is_cuda):
+            raise ValueError("outputs: CUDA float32 tensors")
+    arr = (C.c_void_p * len(grads))(*[t.data_ptr() for t in grads])
+    st = stream or torch.cuda.current_stream(g_out.device)
+    _check(lib().repstep_reduce_norm_noalloc(arr, len(grads), _dtype_code(dt), n, clip,
+                                             _ptr(g_out), _ptr(norm_out), _ptr(scale_out),
+                                             C.c_void_p(st.cuda_stream)), "reduce_norm_noalloc")
 
 
 def _ptr(t: torch.Tensor | None):

@@ -207,6 +207,35 @@ int repstep_last_cuda_error(const repstep_ctx *ctx);
 /* Static name of a status code. */
 const char *repstep_strerror(int code);
 
+/* ---------------------------------------------------------------------------------------
+ * Replica reduce + global norm WITHOUT ANY DEVICE ALLOCATION.  The paper has no counterpart
+ * to this entry point; it serves callers that may not allocate device memory when they need
+ * the averaged gradient and its norm -- for example an audit replay running beside a
+ * training job that already holds almost all device memory through its own allocator, or
+ * an error path entered after an out-of-memory condition.  Such callers cannot provide the
+ * workspace the other entry points need.
+ *
+ * Computes g[i] = T_{r<R}(G_r[i]) * fp32(1/R) into d_g (n fp32, 16-byte aligned) and writes
+ * the pre-clip norm to *d_norm_out and, if d_scale_out is not NULL, the clip scale for
+ * `clip` -- bit for bit what repstep_reduce (flat tree) + repstep_clip produce with the
+ * default launch configuration.  d_grads is a host array of R device pointers, as for
+ * repstep_reduce.  Work is enqueued on `stream` (a cudaStream_t as void*).
+ *
+ * Scratch: one fixed array inside the library (about 1 MiB, held on every GPU that loads
+ * the library until the process exits), so n is limited to REPSTEP_NOALLOC_MAX_N; larger n
+ * returns REPSTEP_ERR_SIZE before any work is enqueued.  The call allocates nothing: no
+ * cudaMalloc, cudaFree or allocating library routine.  Every call on a device shares the
+ * same array and leaves its contents behind (each call clears what must start at zero), so
+ * calls whose GPU work overlaps -- on different streams or host threads -- race and give
+ * undefined results: serialise them.  The first call on each device looks up the array's
+ * device address (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.  Returns REPSTEP_OK, REPSTEP_ERR_ARG, REPSTEP_ERR_ALIGN,
+ * REPSTEP_ERR_SIZE or REPSTEP_ERR_CUDA. */
+#define REPSTEP_NOALLOC_MAX_N (1ull << 30)
+int repstep_reduce_norm_noalloc(const void *const *d_grads, uint32_t R, int32_t grad_dtype,
+                                uint64_t n, float clip, float *d_g, float *d_norm_out,
+                                float *d_scale_out, void *stream);
+
 #ifdef __cplusplus
 }
 #endif
