@@ -4,9 +4,9 @@
 // MODE 0 (AdamW): for every element of the active range, in this fixed order
 //     gc = g*scale;  m' = b1*m + (1-b1)*gc;  v' = b2*v + (1-b2)*(gc*gc)
 //     u = (m'/bc1) / (sqrt(v'/bc2) + eps);   w' = w*(1 - lr*wd) - lr*u
-// ("OPEN-1B: A Fully Auditable Training Run", §3.2: AdamW with decoupled weight decay,
-// gradients clipped to a global l2 norm; "Optimizer-state precision": the whole moment and
-// parameter update in FP32), writing w', m', v' in place; then the PF61 digest of every
+// ("OPEN-1B: A Fully Auditable Training Run", §3.2: AdamW with decoupled weight decay and
+// global-norm clipping; §3.2 paragraph on optimizer-state precision: moments and update in
+// FP32), writing w', m', v' in place; then the PF61 digest of every
 // 4096-element chunk of the NEW w', m', v' that lies wholly inside the range.
 // MODE 1 (leaves): the PF61 digests of the chunks of the given w, m, v, nothing written.
 //

@@ -4,8 +4,8 @@
 //     g_i = T_{r<R}(G_r[i]) * fp32(1/R)
 // with T the canonical tree over global replica index ("OPEN-1B: A Fully Auditable
 // Training Run", App. A.1: replicas paired, pairs paired again, lower replica on the
-// left; §5: a non-power-of-two count is split into its largest power-of-two block plus
-// a remainder; App. A.3: the average is a multiply by the reciprocal, never a divide),
+// left; §5: a non-power-of-two count is split into its largest power-of-two block and
+// the rest; App. A.3: the average is a multiply by the reciprocal, never a divide),
 // and, for every 4096-element chunk lying wholly inside the range, the chunk's sum of
 // squares s_k = T(g_i * g_i) in the fixed perfect tree of common.cuh.
 //

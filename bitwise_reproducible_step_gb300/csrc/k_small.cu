@@ -120,8 +120,9 @@ __global__ void __launch_bounds__(256) k_norm(const float *in, uint64_t count, f
         return;
     }
     const float norm = __fsqrt_rn(S);
-    // "OPEN-1B", §3.2: clipped to a global l2 norm (reading: scale = clip / norm when the
-    // norm exceeds the threshold, else 1; a NaN norm compares false)
+    // OPEN-1B §3.2 clips gradients by their global l2 norm; the formula is not given.
+    // Reading: scale = clip / norm when the norm exceeds the threshold, else 1 (a NaN norm
+    // compares false).
     const float scale = norm > clip ? __fdiv_rn(clip, norm) : 1.0f;
     const bool finite = isfinite(norm);
     sc->norm = norm;

@@ -14,8 +14,8 @@ for the initial weights and 0xFFFFE for per-run segment scales.  Long buffers ar
 fixed slices of 2^26 elements; slice j uses seed s | (j << 48).  The slice length is part
 of the recipe, so a buffer's bits depend on (workload, step, replica, n) only.
 
-Distributions (N(0, sigma) means standard deviation sigma, as the Open-1B paper's §3.1
-"standard deviation of 0.02" initialisation):
+Distributions (N(0, sigma) means standard deviation sigma, as in the Open-1B paper's §3.1,
+whose weights are initialised with a standard deviation of 0.02):
   * normal            g = z * sigma
   * student_t3        g = sigma * z0 / sqrt((z1^2 + z2^2 + z3^2) / 3), in fp64, cast to fp32
   * normal_segscale   g = z * (sigma * 10^(-6 + 4U_seg)) with one U_seg ~ U(0,1) per

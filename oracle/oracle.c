@@ -18,8 +18,9 @@
  *              (reduction order, fused multiply-add, subnormals), §3.2 Training Recipe
  *              (AdamW, global-norm clipping at 1.0), §3.4.2 (pre-clip norm), App. A.1
  *              (TreeFold, lower-replica operand on the left), App. A.3 (average via
- *              reciprocal multiply), App. B (per-step state hash), §5 (the butterfly folds
- *              a count into the largest power-of-two block plus a remainder).
+ *              reciprocal multiply), App. B (per-step state hash), §5 (for a count that
+ *              is not a power of two, the butterfly splits off its largest power-of-two
+ *              block and handles the rest separately).
  *   [CKPT]     "grow_a_language_model_checkpoints" -- Format / Total size sections:
  *              [int32 step][int32 n_params][w][m][v], total = 8 + 12 n bytes,
  *              beta1 = 0.9 for m and beta2 = 0.999 for v.
@@ -82,8 +83,8 @@ static uint64_t split_point(uint64_t L)
 /* L == 1: x_0.  Otherwise k = largest power of two < L and                          */
 /* T = T(x_0..x_{k-1}) + T(x_k..x_{L-1}), lower indices always the left operand.    */
 /* [OPEN-1B] App. A.1 pairs replicas, pairs the pairs, and keeps the lower-replica  */
-/* operand on the left; §5 folds a non-power-of-two count into the largest          */
-/* power-of-two block plus a remainder.  For power-of-two L this is the perfect     */
+/* operand on the left; §5 splits a non-power-of-two count into its largest        */
+/* power-of-two block and the rest.  For power-of-two L this is the perfect         */
 /* pairwise tree, identical to the App. A.1 TreeFold.  For counts with three or     */
 /* more set bits App. A.1's Result and this recursion group the leftover blocks     */
 /* differently; the recursive split is the reading taken here.                      */
