@@ -181,6 +181,9 @@ def run_ours(args, rank, world, local):
     from bitwise_reproducible_step_gb300 import repstep as rs
 
     wl = I.WORKLOADS[args.workload]
+    if args.n:
+        import dataclasses
+        wl = dataclasses.replace(wl, n=args.n)
     n, R = wl.n, wl.R
     dev = torch.device("cuda", local)
     gdt = torch.bfloat16 if wl.grad_dtype == "bf16" else torch.float32
@@ -261,7 +264,8 @@ def run_ours(args, rank, world, local):
     traffic = profiled_traffic(kname)
 
     # ---- end to end: grads from pinned host memory each step, norm+root read back ----
-    e2e = run_e2e(args, ctx, wl, grads, w, m, v, hp, t_step, dev, R, b_g, n)
+    e2e = None if args.skip_e2e else run_e2e(args, ctx, wl, grads, w, m, v, hp, t_step, dev,
+                                              R, b_g, n)
 
     del grads
     torch.cuda.empty_cache()
@@ -426,6 +430,9 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=4)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--skip-cpu-baseline", action="store_true")
+    ap.add_argument("--skip-e2e", action="store_true")
+    ap.add_argument("--n", type=int, default=0,
+                    help="override the workload's parameter count (small profiling cases)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -6,20 +6,26 @@
 //     u = (m'/bc1) / (sqrt(v'/bc2) + eps);   w' = w*(1 - lr*wd) - lr*u
 // ("OPEN-1B: A Fully Auditable Training Run", §3.2: AdamW with decoupled weight decay and
 // global-norm clipping; §3.2 paragraph on optimizer-state precision: moments and update in
-// FP32), writing w', m', v' in place; then the PF61 digest of every
-// 4096-element chunk of the NEW w', m', v' that lies wholly inside the range.
+// FP32), writing w', m', v' in place; then the PF61 digest of every 4096-element chunk of
+// the NEW w', m', v' that lies wholly inside the range.
 // MODE 1 (leaves): the PF61 digests of the chunks of the given w, m, v, nothing written.
 //
-// PF61 of a chunk of W 32-bit words x_i is (W + sum x_i K^(i+1)) mod (2^61 - 1): the
-// per-word terms are exact integers, so each thread accumulates its words' products in a
-// 128-bit register sum and the chunk total is an exact integer sum in any order -- the
-// digest cannot depend on the launch shape.  (App. B of the same paper anchors every
-// step with a hash of parameters and optimizer state; this is its on-device form.)
+// PF61 of a chunk of W 32-bit words x_i is (W + sum x_i K^(i+1)) mod (2^61 - 1).  Each
+// power P = K^(i+1) < 2^61 is split into three 21-bit limbs P = l0 + l1 2^21 + l2 2^42, and
+// a thread accumulates x * l_k in three 64-bit sums with one 32x32->64 multiply-add each:
+// with at most 32 words per thread per chunk the sums stay below 2^58, so no carries are
+// lost, and the thread folds them modulo p once per chunk.  The chunk total is an exact
+// integer sum of the thread partials, in any order, so the digest cannot depend on the
+// launch shape.  (App. B of the same paper anchors every step with a hash of parameters
+// and optimizer state; this is its on-device form.)
 //
-// GB300 design: as the reduce kernel -- a persistent grid, one producer lane streaming
-// 4 (or 3) arrays tile by tile into a shared-memory ring with 1-D bulk TMA copies on
-// mbarriers, NT compute threads taking one 16-byte group per array per tile, 16-byte
-// stores of the results.  Every fp32 operation is an explicitly rounded intrinsic.
+// GB300 design: a persistent grid of one CTA per SM.  One producer lane streams the 4 (or
+// 3) arrays tile by tile (TE = 8*NT elements) into a 192 KB shared-memory ring with 1-D
+// bulk TMA copies completing on mbarriers.  The NT compute threads each take two 16-byte
+// groups per array per tile (8 elements of independent AdamW chains), store the results
+// with 16-byte stores, and fold the words into the leaf sums.  Tiles lying wholly inside
+// the range take a fast path without per-element range checks.  Every fp32 operation is
+// an explicitly rounded intrinsic.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -27,40 +33,124 @@ namespace repstep {
 
 namespace {
 
-constexpr uint32_t kRingBytes = 128 * 1024;
+constexpr uint32_t kRingBytes = 192 * 1024;
 constexpr uint32_t kMaxStages = 12;
+constexpr int kEPT = 8;            // elements per compute thread per tile (two float4)
+constexpr uint64_t kM21 = (1ull << 21) - 1;
 
 template <int NT>
 __host__ __device__ constexpr uint32_t ring_offset()
 {
-    // barriers (2 x kMaxStages x 8) | abort flags (8) | leaf partials 2 x 3 x NT u64
+    // barriers (2 x kMaxStages x 8) | abort flags (16) | leaf partials 2 x 3 x NT u64
     return ((16 * kMaxStages + 16 + 2 * 3 * NT * 8) + 1023) / 1024 * 1024;
 }
 
-__device__ __forceinline__ void adamw_elem(float g, float &w, float &m, float &v, float scale,
-                                           const AdamwArgs &A)
+// Correctly rounded x / b for a divisor b fixed for the whole launch, by Markstein's
+// final correction (P. Markstein, "Computation of elementary functions on the IBM RISC
+// System/6000 processor", IBM J. Res. Dev. 34(1), 1990; stated as Markstein's theorem in
+// Muller et al., "Handbook of Floating-Point Arithmetic"): with y = RN(1/b) computed once
+// on the host and q = RN(x*y), the remainder r = x - q*b is exact (one fused multiply-add)
+// and RN(q + r*y) (one fused multiply-add) equals RN(x/b).  k_selftest_div checks this
+// against the IEEE division for all 2^46 significand pairs.  Valid ("fast_ok") for b in
+// [2^-40, 2] (checked on the host) and x zero or |x| in [2^-100, 2^60]: there every
+// intermediate is finite, the remainder is a multiple of at least 2^-149 and so exact, and
+// power-of-two exponents scale every step exactly.  A zero keeps its sign (x/b for b > 0).
+__device__ __forceinline__ float div_fast(float x, float b, float y)
 {
-    const float gc = __fmul_rn(g, scale);
-    const float m_new = __fadd_rn(__fmul_rn(A.beta1, m), __fmul_rn(A.om1, gc));
-    const float gsq = __fmul_rn(gc, gc);
-    const float v_new = __fadd_rn(__fmul_rn(A.beta2, v), __fmul_rn(A.om2, gsq));
-    const float mhat = __fdiv_rn(m_new, A.bc1);
-    const float vhat = __fdiv_rn(v_new, A.bc2);
-    const float denom = __fadd_rn(__fsqrt_rn(vhat), A.eps);
-    const float u = __fdiv_rn(mhat, denom);
-    w = __fsub_rn(__fmul_rn(w, A.delta), __fmul_rn(A.lr, u));
-    m = m_new;
-    v = v_new;
+    const float q = __fmul_rn(x, y);
+    const float r = __fmaf_rn(-q, b, x);
+    const float q2 = __fmaf_rn(r, y, q);
+    return x == 0.0f ? x : q2;
+}
+
+__device__ __forceinline__ bool fast_ok(float x)
+{
+    const float ax = fabsf(x);
+    return (ax >= 0x1p-100f && ax <= 0x1p60f) || ax == 0.0f;
+}
+
+// AdamW on the 8 elements a compute thread holds, in the fixed order of the definition.
+// The two divisions by the bias corrections take div_fast; if any lane of the warp holds an
+// operand outside its range (subnormal, huge, infinite, NaN) or the divisors are outside
+// theirs, those divisions are redone with the IEEE division.  Every lane of the warp calls
+// this together.
+__device__ __forceinline__ void adamw8(const float (&g)[8], float (&w)[8], float (&m)[8],
+                                       float (&v)[8], float scale, const AdamwArgs &A)
+{
+    float mn[8], vn[8], mh[8], vh[8];
+    bool bad = !A.fastdiv;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        const float gc = __fmul_rn(g[e], scale);
+        mn[e] = __fadd_rn(__fmul_rn(A.beta1, m[e]), __fmul_rn(A.om1, gc));
+        const float gsq = __fmul_rn(gc, gc);
+        vn[e] = __fadd_rn(__fmul_rn(A.beta2, v[e]), __fmul_rn(A.om2, gsq));
+        mh[e] = div_fast(mn[e], A.bc1, A.rbc1);
+        vh[e] = div_fast(vn[e], A.bc2, A.rbc2);
+        bad = bad || !fast_ok(mn[e]) || !fast_ok(vn[e]);
+    }
+    if (__any_sync(0xFFFFFFFFu, bad)) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            if (!A.fastdiv || !fast_ok(mn[e])) mh[e] = __fdiv_rn(mn[e], A.bc1);
+            if (!A.fastdiv || !fast_ok(vn[e])) vh[e] = __fdiv_rn(vn[e], A.bc2);
+        }
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        const float denom = __fadd_rn(__fsqrt_rn(vh[e]), A.eps);
+        const float u = __fdiv_rn(mh[e], denom);
+        w[e] = __fsub_rn(__fmul_rn(w[e], A.delta), __fmul_rn(A.lr, u));
+        m[e] = mn[e];
+        v[e] = vn[e];
+    }
+}
+
+// Three 21-bit limbs of a PF61 power.
+struct Limbs {
+    uint32_t l0, l1, l2;
+};
+
+__device__ __forceinline__ Limbs limbs_of(uint64_t p)
+{
+    return {uint32_t(p & kM21), uint32_t((p >> 21) & kM21), uint32_t(p >> 42)};
+}
+
+// a += x * l as a 32 x 32 -> 64-bit multiply-add.
+__device__ __forceinline__ void mac(uint64_t &a, uint32_t x, uint32_t l)
+{
+    asm("mad.wide.u32 %0, %1, %2, %0;" : "+l"(a) : "r"(x), "r"(l));
+}
+
+struct Acc3 {
+    uint64_t a0, a1, a2;   // sum x*l0, sum x*l1, sum x*l2
+};
+
+__device__ __forceinline__ void acc_word(Acc3 &s, uint32_t x, const Limbs &p)
+{
+    mac(s.a0, x, p.l0);
+    mac(s.a1, x, p.l1);
+    mac(s.a2, x, p.l2);
+}
+
+// (a0 + a1 2^21 + a2 2^42) mod p, for a_k < 2^58 (2^61 == 1 mod p).
+__device__ __forceinline__ uint64_t fold3(const Acc3 &s)
+{
+    const uint64_t t1 = ((s.a1 & ((1ull << 40) - 1)) << 21) + (s.a1 >> 40);
+    const uint64_t t2 = ((s.a2 & ((1ull << 19) - 1)) << 42) + (s.a2 >> 19);
+    const uint64_t r = s.a0 + t1 + t2;   // < 2^58 + 2^61 + 2^18 + 2^61 + 2^39 < 2^63
+    return pf_reduce64(pf_reduce64(r));
 }
 
 template <int NT, int MODE>
 __global__ void __launch_bounds__(NT + 32, 1) k_adamw(const __grid_constant__ AdamwArgs A)
 {
     constexpr int NS = MODE == 0 ? 4 : 3;        // streamed arrays
-    constexpr uint32_t TE = 4u * NT;
+    constexpr uint32_t TE = uint32_t(kEPT) * NT;
     constexpr int TPC = int(kChunk / TE);
     constexpr int W = NT / 32;
     static_assert(W >= 3, "three warps finish the three leaves of a chunk");
+    static_assert(TPC >= 1 && TPC * TE == kChunk, "tiles divide the chunk");
 
     extern __shared__ __align__(1024) unsigned char smem[];
     const uint32_t S = A.stages;
@@ -84,16 +174,16 @@ __global__ void __launch_bounds__(NT + 32, 1) k_adamw(const __grid_constant__ Ad
     __syncthreads();
 
     const uint32_t flag_bit = MODE == 0 ? kFlagTimeoutAdamw : kFlagTimeoutLeaves;
+    const float *src[4];
+    if (MODE == 0) {
+        src[0] = A.g; src[1] = A.w; src[2] = A.m; src[3] = A.v;
+    } else {
+        src[0] = A.w; src[1] = A.m; src[2] = A.v; src[3] = nullptr;
+    }
 
     if (tid >= NT) {
         // ------------------------------ producer warp ------------------------------
         if (tid != NT) return;
-        const void *src[4];
-        if (MODE == 0) {
-            src[0] = A.g; src[1] = A.w; src[2] = A.m; src[3] = A.v;
-        } else {
-            src[0] = A.w; src[1] = A.m; src[2] = A.v; src[3] = nullptr;
-        }
         const uint64_t pol = l2_evict_first();
         uint32_t it = 0;
         bool ok = true;
@@ -114,8 +204,7 @@ __global__ void __launch_bounds__(NT + 32, 1) k_adamw(const __grid_constant__ Ad
                     const uint32_t dst = smem_u32(ring + slot * A.stage_stride) + soff;
 #pragma unroll
                     for (int s = 0; s < NS; ++s)
-                        bulk_g2s(dst + s * TE * 4u,
-                                 static_cast<const float *>(src[s]) + tr.a16, bytes, fb, pol);
+                        bulk_g2s(dst + s * TE * 4u, src[s] + tr.a16, bytes, fb, pol);
                 }
                 ++it;
             }
@@ -124,6 +213,7 @@ __global__ void __launch_bounds__(NT + 32, 1) k_adamw(const __grid_constant__ Ad
             atomicOr(&A.sc->flags, flag_bit);
             *abort_flag = 1;
         }
+        // never leave while copies into the ring may be in flight (bounded waits)
         const uint32_t last = it < S ? it : S;
         for (uint32_t d = 0; d < last; ++d) {
             const uint32_t idx = it - 1 - d;
@@ -135,21 +225,26 @@ __global__ void __launch_bounds__(NT + 32, 1) k_adamw(const __grid_constant__ Ad
     // ------------------------------ compute threads -------------------------------
     const int lane = tid & 31, warp = tid >> 5;
     const float scale = MODE == 0 ? A.sc->scale : 1.0f;
+    // the two 4-element groups of this thread within a tile
+    const uint32_t goff[2] = {4u * tid, 4u * tid + 4u * NT};
+    // with one tile per chunk, the word positions -- hence the powers -- never change
+    Limbs pw_fixed[TPC == 1 ? 8 : 1];
+    if constexpr (TPC == 1) {
+#pragma unroll
+        for (int q = 0; q < 2; ++q)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) pw_fixed[q * 4 + i] = limbs_of(__ldg(A.powers + goff[q] + i));
+    }
+
     uint32_t it = 0;
     int cb = 0;
     bool aborted = false;
     for (uint64_t k = A.chunk_lo + blockIdx.x; k < A.chunk_hi; k += gridDim.x) {
-        uint32_t acc[3][4];
-#pragma unroll
-        for (int s = 0; s < 3; ++s)
-#pragma unroll
-            for (int t = 0; t < 4; ++t) acc[s][t] = 0u;
+        Acc3 acc[3] = {{0, 0, 0}, {0, 0, 0}, {0, 0, 0}};
 #pragma unroll
         for (int j = 0; j < TPC; ++j) {
             const TileRange tr = tile_range(k * kChunk + uint64_t(j) * TE, TE, A.begin, A.end, 4);
-            const uint32_t off = 4u * tid;
-            const uint64_t e0 = tr.base + off;
-            const bool in_bulk = e0 >= tr.a16 && e0 + 4 <= tr.b16;
+            const bool full_tile = tr.a == tr.base && tr.b == tr.base + TE;
             const uint32_t slot = it % S, round = it / S;
             if (!aborted && !mbar_wait_bounded(smem_u32(&full[slot]), round & 1u, abort_flag)) {
                 aborted = true;
@@ -159,91 +254,124 @@ __global__ void __launch_bounds__(NT + 32, 1) k_adamw(const __grid_constant__ Ad
                 }
             }
             const unsigned char *sb = ring + slot * A.stage_stride;
-            float4 x[NS];
-            uint32_t inmask = 0;
+            float4 x[2][NS];
+            uint32_t inmask[2] = {0xFu, 0xFu};
+            if (full_tile) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-                inmask |= (e0 + i >= tr.a && e0 + i < tr.b) ? (1u << i) : 0u;
-            if (in_bulk) {
+                for (int q = 0; q < 2; ++q)
 #pragma unroll
-                for (int s = 0; s < NS; ++s)
-                    x[s] = *reinterpret_cast<const float4 *>(sb + s * TE * 4u + off * 4u);
+                    for (int s = 0; s < NS; ++s)
+                        x[q][s] = *reinterpret_cast<const float4 *>(sb + s * TE * 4u + goff[q] * 4u);
             } else {
-                const float *srcs[4];
-                if (MODE == 0) {
-                    srcs[0] = A.g; srcs[1] = A.w; srcs[2] = A.m; srcs[3] = A.v;
-                } else {
-                    srcs[0] = A.w; srcs[1] = A.m; srcs[2] = A.v; srcs[3] = nullptr;
-                }
 #pragma unroll
-                for (int s = 0; s < NS; ++s) {
-                    float r[4];
+                for (int q = 0; q < 2; ++q) {
+                    const uint64_t e0 = tr.base + goff[q];
+                    const bool in_bulk = e0 >= tr.a16 && e0 + 4 <= tr.b16;
+                    uint32_t msk = 0;
 #pragma unroll
                     for (int i = 0; i < 4; ++i)
-                        r[i] = (inmask >> i) & 1u ? __ldg(srcs[s] + e0 + i) : 0.0f;
-                    x[s] = make_float4(r[0], r[1], r[2], r[3]);
+                        msk |= (e0 + i >= tr.a && e0 + i < tr.b) ? (1u << i) : 0u;
+                    inmask[q] = msk;
+#pragma unroll
+                    for (int s = 0; s < NS; ++s) {
+                        if (in_bulk) {
+                            x[q][s] = *reinterpret_cast<const float4 *>(sb + s * TE * 4u +
+                                                                        goff[q] * 4u);
+                        } else {
+                            float r[4];
+#pragma unroll
+                            for (int i = 0; i < 4; ++i)
+                                r[i] = (msk >> i) & 1u ? __ldg(src[s] + e0 + i) : 0.0f;
+                            x[q][s] = make_float4(r[0], r[1], r[2], r[3]);
+                        }
+                    }
                 }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&empty[slot]));
             ++it;
 
-            float4 ow, om, ov;   // the words hashed: new state (MODE 0) or given state
+            // the words hashed: the new state (MODE 0) or the given state (MODE 1)
+            float4 hw[2], hm[2], hv[2];
             if (MODE == 0) {
-                ow = x[1]; om = x[2]; ov = x[3];
-                adamw_elem(x[0].x, ow.x, om.x, ov.x, scale, A);
-                adamw_elem(x[0].y, ow.y, om.y, ov.y, scale, A);
-                adamw_elem(x[0].z, ow.z, om.z, ov.z, scale, A);
-                adamw_elem(x[0].w, ow.w, om.w, ov.w, scale, A);
-                if (inmask == 0xFu) {
-                    *reinterpret_cast<float4 *>(A.w + e0) = ow;
-                    *reinterpret_cast<float4 *>(A.m + e0) = om;
-                    *reinterpret_cast<float4 *>(A.v + e0) = ov;
-                } else {
-                    const float aw[4] = {ow.x, ow.y, ow.z, ow.w};
-                    const float am[4] = {om.x, om.y, om.z, om.w};
-                    const float av[4] = {ov.x, ov.y, ov.z, ov.w};
+                float g8[8], w8[8], m8[8], v8[8];
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        if ((inmask >> i) & 1u) {
-                            A.w[e0 + i] = aw[i];
-                            A.m[e0 + i] = am[i];
-                            A.v[e0 + i] = av[i];
+                for (int q = 0; q < 2; ++q) {
+                    g8[4 * q] = x[q][0].x; g8[4 * q + 1] = x[q][0].y; g8[4 * q + 2] = x[q][0].z; g8[4 * q + 3] = x[q][0].w;
+                    w8[4 * q] = x[q][1].x; w8[4 * q + 1] = x[q][1].y; w8[4 * q + 2] = x[q][1].z; w8[4 * q + 3] = x[q][1].w;
+                    m8[4 * q] = x[q][2].x; m8[4 * q + 1] = x[q][2].y; m8[4 * q + 2] = x[q][2].z; m8[4 * q + 3] = x[q][2].w;
+                    v8[4 * q] = x[q][3].x; v8[4 * q + 1] = x[q][3].y; v8[4 * q + 2] = x[q][3].z; v8[4 * q + 3] = x[q][3].w;
+                }
+                adamw8(g8, w8, m8, v8, scale, A);
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    hw[q] = make_float4(w8[4 * q], w8[4 * q + 1], w8[4 * q + 2], w8[4 * q + 3]);
+                    hm[q] = make_float4(m8[4 * q], m8[4 * q + 1], m8[4 * q + 2], m8[4 * q + 3]);
+                    hv[q] = make_float4(v8[4 * q], v8[4 * q + 1], v8[4 * q + 2], v8[4 * q + 3]);
+                }
+            } else {
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    hw[q] = x[q][0]; hm[q] = x[q][1]; hv[q] = x[q][2];
+                }
+            }
+            if (MODE == 0) {
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    const uint64_t e0 = tr.base + goff[q];
+                    if (inmask[q] == 0xFu) {
+                        *reinterpret_cast<float4 *>(A.w + e0) = hw[q];
+                        *reinterpret_cast<float4 *>(A.m + e0) = hm[q];
+                        *reinterpret_cast<float4 *>(A.v + e0) = hv[q];
+                    } else {
+                        const float aw[4] = {hw[q].x, hw[q].y, hw[q].z, hw[q].w};
+                        const float am[4] = {hm[q].x, hm[q].y, hm[q].z, hm[q].w};
+                        const float av[4] = {hv[q].x, hv[q].y, hv[q].z, hv[q].w};
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            if ((inmask[q] >> i) & 1u) {
+                                A.w[e0 + i] = aw[i];
+                                A.m[e0 + i] = am[i];
+                                A.v[e0 + i] = av[i];
+                            }
                         }
                     }
                 }
-            } else {
-                ow = x[0]; om = x[1]; ov = x[2];
             }
 
-            // PF61 terms x * K^(p+1) for word positions p = j*TE + off + i of the chunk
-            const ulonglong2 *pw =
-                reinterpret_cast<const ulonglong2 *>(A.powers + uint32_t(j) * TE + off);
-            const ulonglong2 p01 = __ldg(pw), p23 = __ldg(pw + 1);
-            const uint64_t pk[4] = {p01.x, p01.y, p23.x, p23.y};
-            const uint32_t wb[4] = {__float_as_uint(ow.x), __float_as_uint(ow.y),
-                                    __float_as_uint(ow.z), __float_as_uint(ow.w)};
-            const uint32_t mb[4] = {__float_as_uint(om.x), __float_as_uint(om.y),
-                                    __float_as_uint(om.z), __float_as_uint(om.w)};
-            const uint32_t vb[4] = {__float_as_uint(ov.x), __float_as_uint(ov.y),
-                                    __float_as_uint(ov.z), __float_as_uint(ov.w)};
+            // PF61 terms x * K^(pos+1) for the word positions pos = j*TE + goff[q] + i
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const uint32_t p0 = uint32_t(pk[i]), p1 = uint32_t(pk[i] >> 32);
-                const uint32_t on = (inmask >> i) & 1u ? 0xFFFFFFFFu : 0u;
-                pf_mac(acc[0], wb[i] & on, p0, p1);
-                pf_mac(acc[1], mb[i] & on, p0, p1);
-                pf_mac(acc[2], vb[i] & on, p0, p1);
+            for (int q = 0; q < 2; ++q) {
+                Limbs pw[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    if constexpr (TPC == 1) pw[i] = pw_fixed[q * 4 + i];
+                    else pw[i] = limbs_of(__ldg(A.powers + uint32_t(j) * TE + goff[q] + i));
+                }
+                const uint32_t wb[4] = {__float_as_uint(hw[q].x), __float_as_uint(hw[q].y),
+                                        __float_as_uint(hw[q].z), __float_as_uint(hw[q].w)};
+                const uint32_t mb[4] = {__float_as_uint(hm[q].x), __float_as_uint(hm[q].y),
+                                        __float_as_uint(hm[q].z), __float_as_uint(hm[q].w)};
+                const uint32_t vb[4] = {__float_as_uint(hv[q].x), __float_as_uint(hv[q].y),
+                                        __float_as_uint(hv[q].z), __float_as_uint(hv[q].w)};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const uint32_t on = (inmask[q] >> i) & 1u ? 0xFFFFFFFFu : 0u;
+                    acc_word(acc[0], wb[i] & on, pw[i]);
+                    acc_word(acc[1], mb[i] & on, pw[i]);
+                    acc_word(acc[2], vb[i] & on, pw[i]);
+                }
             }
         }
 
         // chunk leaves: exact integer sum of every thread's partial, then + W mod p
         uint64_t *pb = pfbuf + cb * 3 * NT;
 #pragma unroll
-        for (int s = 0; s < 3; ++s) pb[s * NT + tid] = pf_fold128(acc[s]);
+        for (int s = 0; s < 3; ++s) pb[s * NT + tid] = fold3(acc[s]);
         named_barrier(1, NT);
         if (warp < 3) {
             uint64_t sum = 0;
+#pragma unroll 4
             for (int t = lane; t < NT; t += 32) sum = pf_add(sum, pb[warp * NT + t]);
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1)
@@ -257,6 +385,25 @@ __global__ void __launch_bounds__(NT + 32, 1) k_adamw(const __grid_constant__ Ad
         }
         cb ^= 1;
     }
+}
+
+// Self-test of div_fast: every significand pair x, b in [1, 2) (2^23 x 2^23), with y the
+// correctly rounded reciprocal of b, against the IEEE division.  Exponents only scale the
+// operands and results by powers of two, exactly, inside the guarded range, so this
+// covers every x and b the fast path accepts.
+__global__ void __launch_bounds__(256) k_selftest_div(uint32_t b_begin, uint32_t b_count,
+                                                      unsigned long long *mismatches)
+{
+    unsigned long long bad = 0;
+    for (uint32_t bi = blockIdx.x; bi < b_count; bi += gridDim.x) {
+        const float b = __uint_as_float(0x3F800000u | ((b_begin + bi) & 0x7FFFFFu));
+        const float y = __frcp_rn(b);
+        for (uint32_t xs = threadIdx.x; xs < (1u << 23); xs += blockDim.x) {
+            const float x = __uint_as_float(0x3F800000u | xs);
+            bad += __float_as_uint(div_fast(x, b, y)) != __float_as_uint(__fdiv_rn(x, b));
+        }
+    }
+    if (bad) atomicAdd(mismatches, bad);
 }
 
 using KernelFn = void (*)(AdamwArgs);
@@ -281,7 +428,7 @@ uint32_t ring_off(int nt)
 size_t adamw_smem_bytes(int nt, int mode, AdamwArgs &args)
 {
     const uint32_t ns = mode == 0 ? 4u : 3u;
-    const uint32_t stride = ns * 4u * uint32_t(nt) * 4u;
+    const uint32_t stride = ns * uint32_t(kEPT) * uint32_t(nt) * 4u;
     uint32_t stages = kRingBytes / stride;
     if (stages > kMaxStages) stages = kMaxStages;
     if (stages < 2) stages = 2;
@@ -304,6 +451,13 @@ cudaError_t adamw_occupancy(int nt, int mode, size_t smem, int *blocks_per_sm)
     if (!f) return cudaErrorInvalidValue;
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
         blocks_per_sm, reinterpret_cast<const void *>(f), nt + 32, smem);
+}
+
+cudaError_t launch_selftest_div(uint32_t b_begin, uint32_t b_count, unsigned long long *mismatches,
+                               cudaStream_t st)
+{
+    k_selftest_div<<<152 * 8, 256, 0, st>>>(b_begin, b_count, mismatches);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_adamw(int nt, int mode, const AdamwArgs &args, int grid, size_t smem,

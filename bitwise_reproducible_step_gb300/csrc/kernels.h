@@ -51,6 +51,8 @@ struct AdamwArgs {
     uint64_t chunk_lo, chunk_hi;
     uint32_t stages, stage_stride;
     float lr, beta1, beta2, eps, bc1, bc2, om1, om2, delta;
+    float rbc1, rbc2;         // RN(1/bc1), RN(1/bc2): divisors fixed for the launch
+    int fastdiv;              // both bias corrections in [2^-40, 2]
 };
 
 size_t adamw_smem_bytes(int nt, int mode, AdamwArgs &args);
@@ -58,6 +60,8 @@ cudaError_t adamw_prepare(int nt, int mode, size_t smem);
 cudaError_t adamw_occupancy(int nt, int mode, size_t smem, int *blocks_per_sm);
 cudaError_t launch_adamw(int nt, int mode, const AdamwArgs &args, int grid, size_t smem,
                          cudaStream_t st);
+cudaError_t launch_selftest_div(uint32_t b_begin, uint32_t b_count, unsigned long long *mismatches,
+                               cudaStream_t st);
 
 // Small kernels (k_small.cu).
 cudaError_t launch_init_powers(uint64_t *powers, cudaStream_t st);

@@ -279,6 +279,11 @@ int do_adamw(repstep_ctx *x, float *w, float *m, float *v, const repstep_hparams
     a.om2 = one - hp->beta2;
     const float lrwd = hp->lr * hp->weight_decay;
     a.delta = one - lrwd;
+    // reciprocals of the bias corrections for the fixed-divisor division in k_adamw
+    a.rbc1 = one / hp->bc1;
+    a.rbc2 = one / hp->bc2;
+    const float lo = std::ldexp(1.0f, -40), hi = 2.0f;
+    a.fastdiv = (hp->bc1 >= lo && hp->bc1 <= hi && hp->bc2 >= lo && hp->bc2 <= hi) ? 1 : 0;
     const int nt = x->nt_adamw;
     const size_t smem = adamw_smem_bytes(nt, 0, a);
     cudaError_t e = adamw_prepare(nt, 0, smem);
@@ -582,6 +587,18 @@ int repstep_sync(repstep_ctx *ctx, uint32_t *flags_out)
         return REPSTEP_ERR_TIMEOUT;
     }
     return REPSTEP_OK;
+}
+
+int repstep_selftest_fixed_division(uint32_t b_sig_begin, uint32_t b_sig_count,
+                                    uint64_t *d_mismatches, void *stream)
+{
+    if (!d_mismatches || !aligned(d_mismatches, 8)) return REPSTEP_ERR_ARG;
+    if (b_sig_begin > (1u << 23) || b_sig_count > (1u << 23) - b_sig_begin) return REPSTEP_ERR_ARG;
+    if (b_sig_count == 0) return REPSTEP_OK;
+    const cudaError_t e = launch_selftest_div(b_sig_begin, b_sig_count,
+                                              reinterpret_cast<unsigned long long *>(d_mismatches),
+                                              static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? REPSTEP_OK : REPSTEP_ERR_CUDA;
 }
 
 uint64_t repstep_launch_count(const repstep_ctx *ctx) { return ctx ? ctx->launches : 0; }

@@ -63,6 +63,7 @@ EXPORTS = [
     "repstep_hash", "repstep_step", "repstep_image_bytes", "repstep_image_write",
     "repstep_image_read", "repstep_bias_corrections", "repstep_sync", "repstep_launch_count",
     "repstep_last_cuda_error", "repstep_strerror", "repstep_reduce_norm_noalloc",
+    "repstep_selftest_fixed_division",
 ]
 NOALLOC_MAX_N = 1 << 30
 
@@ -105,6 +106,7 @@ def lib():
     L.repstep_last_cuda_error.argtypes = [vp]
     L.repstep_strerror.argtypes = [C.c_int]
     L.repstep_strerror.restype = C.c_char_p
+    L.repstep_selftest_fixed_division.argtypes = [u32, u32, vp, vp]
     L.repstep_reduce_norm_noalloc.argtypes = [C.POINTER(vp), u32, i32, u64, C.c_float, vp, vp,
                                               vp, vp]
     _lib = L
@@ -168,6 +170,16 @@ def reduce_norm_noalloc(grads, clip: float, g_out: torch.Tensor, norm_out: torch
     _check(lib().repstep_reduce_norm_noalloc(arr, len(grads), _dtype_code(dt), n, clip,
                                              _ptr(g_out), _ptr(norm_out), _ptr(scale_out),
                                              C.c_void_p(st.cuda_stream)), "reduce_norm_noalloc")
+
+
+def selftest_fixed_division(b_sig_begin: int = 0, b_sig_count: int = 1 << 23) -> int:
+    """Mismatches between the AdamW kernel's fixed-divisor division and IEEE division over
+    all x significands and the given b significands (see repstep_selftest_fixed_division)."""
+    out = torch.zeros(1, dtype=torch.int64, device="cuda")
+    _check(lib().repstep_selftest_fixed_division(b_sig_begin, b_sig_count, _ptr(out),
+                                                 C.c_void_p(torch.cuda.current_stream().cuda_stream)),
+           "selftest_fixed_division")
+    return int(out.item())
 
 
 def _ptr(t: torch.Tensor | None):

@@ -198,6 +198,19 @@ void repstep_bias_corrections(float beta1, float beta2, int32_t t, float *bc1, f
  * if a kernel's bounded wait expired, else REPSTEP_OK.  Clears the timeout flags. */
 int repstep_sync(repstep_ctx *ctx, uint32_t *flags_out);
 
+/* Self-test of the fixed-divisor division inside the AdamW kernel.  The bias corrections
+ * bc1 and bc2 are the same for every element of a step, so the kernel divides by them as
+ * q = RN(x*y), r = x - q*b, RN(q + r*y) with y = RN(1/b) (Markstein's correction, two fused
+ * multiply-adds) instead of a full IEEE division, for b in [2^-40, 2] and |x| in
+ * [2^-100, 2^60]; other operands take the IEEE division.  This entry point compares that
+ * code with the IEEE division for every x significand in [1, 2) and every b significand in
+ * [1 + b_sig_begin 2^-23, 1 + (b_sig_begin + b_sig_count) 2^-23), adding the number of
+ * differing results to *d_mismatches (a device u64 the caller zeroes).  The whole range
+ * (begin 0, count 2^23; 2^46 pairs) takes well under a minute on a GB300 and finds none.
+ * Returns REPSTEP_ERR_ARG for a range outside [0, 2^23). */
+int repstep_selftest_fixed_division(uint32_t b_sig_begin, uint32_t b_sig_count,
+                                    uint64_t *d_mismatches, void *stream);
+
 /* Kernels this context has launched so far. */
 uint64_t repstep_launch_count(const repstep_ctx *ctx);
 

@@ -180,3 +180,9 @@ def test_flat268m_r32_topologies_grids_blocks():
                     assert torch.equal(v.view(torch.int32), ref[2].view(torch.int32))
                     assert norm.item() == ref[3] and U.root_of(root) == ref[4]
                 ctx.destroy()
+
+
+def test_fixed_division_is_ieee_for_every_significand_pair():
+    """The AdamW kernel divides by the step's bias corrections with Markstein's correction
+    from a precomputed reciprocal; compare it with IEEE division for all 2^46 pairs."""
+    assert rs.selftest_fixed_division(0, 1 << 23) == 0

@@ -283,6 +283,39 @@ def test_nonfinite_gradient_sets_flag():
     U.assert_same_f32(w, ref["w"], "w with a NaN gradient")   # NaN slots compared by class
 
 
+@pytest.mark.parametrize("t,bc_override", [(1, None), (2, None), (7, None), (3, (0.3, 1e-13)),
+                                           (4, (-0.5, 3.0))])
+def test_adamw_on_arbitrary_bit_patterns(t, bc_override):
+    """w, m, v and g drawn as random 32-bit patterns (zeros, subnormals, huge values,
+    infinities and NaNs included): every result bit equals the oracle (NaNs by class).
+    Covers the fixed-divisor fast path's fallbacks and divisors outside its range."""
+    n = 3 * 4096 + 11
+    dev = torch.device("cuda", 0)
+    rng = np.random.default_rng(100 + t)
+    bits = lambda: rng.integers(0, 2 ** 32, n, dtype=np.uint64).astype(np.uint32).view(np.float32)  # noqa: E731
+    w, m, g = bits(), bits(), bits()
+    v = (rng.integers(0, 2 ** 31, n, dtype=np.uint64).astype(np.uint32)).view(np.float32)
+    # plus plain values so most elements take the common path
+    w[::3] = rng.standard_normal(len(w[::3])).astype(np.float32) * 0.02
+    m[::3] = rng.standard_normal(len(m[::3])).astype(np.float32) * 1e-4
+    v[::3] = np.abs(rng.standard_normal(len(v[::3]))).astype(np.float32) * 1e-8
+    g[::3] = rng.standard_normal(len(g[::3])).astype(np.float32) * 1e-3
+    hp = U.hp_for(t, clip=float("inf"))
+    if bc_override:
+        hp.bc1, hp.bc2 = bc_override
+    ctx = rs.Repstep(n, device=dev)
+    W, M, V, G = (torch.from_numpy(a.copy()).to(dev) for a in (w, m, v, g))
+    ctx.reduce([G])
+    ctx.clip(float("inf"))
+    ctx.adamw(W, M, V, hp)
+    ctx.sync()
+    ow, om, ov = O.adamw(w, m, v, g, 1.0, U.HP["lr"], U.HP["beta1"], U.HP["beta2"], U.HP["eps"],
+                         U.HP["wd"], np.float32(hp.bc1), np.float32(hp.bc2))
+    U.assert_same_f32(W, ow, "w")
+    U.assert_same_f32(M, om, "m")
+    U.assert_same_f32(V, ov, "v")
+
+
 def test_relaunch_is_deterministic():
     n, R = 77_777, 8
     a = run_steps(n, R, steps=2, check_intermediates=False)
