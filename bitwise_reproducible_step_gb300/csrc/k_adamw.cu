@@ -33,16 +33,29 @@ namespace repstep {
 
 namespace {
 
-constexpr uint32_t kRingBytes = 192 * 1024;
 constexpr uint32_t kMaxStages = 12;
+
+// Ring size and CTAs per SM by compute-thread count: 512 threads run one CTA per SM with a
+// 192 KB ring; 256 and 128 threads run two CTAs per SM (96 KB rings), so that two CTAs'
+// chunk barriers overlap and an SM holds as many compute warps either way.
+template <int NT>
+struct Shape {
+    static constexpr uint32_t ring = NT == 512 ? 192 * 1024 : 96 * 1024;
+    static constexpr int min_blocks = NT == 512 ? 1 : 2;
+};
 constexpr int kEPT = 8;            // elements per compute thread per tile (two float4)
 constexpr uint64_t kM21 = (1ull << 21) - 1;
+
+constexpr int kLeafBufs = 4;       // chunks in flight between the compute warps and the leaf warp
+constexpr int kPieces = 27;        // 3 streams x 3 limbs x 3 pieces of 27 bits
 
 template <int NT>
 __host__ __device__ constexpr uint32_t ring_offset()
 {
-    // barriers (2 x kMaxStages x 8) | abort flags (16) | leaf partials 2 x 3 x NT u64
-    return ((16 * kMaxStages + 16 + 2 * 3 * NT * 8) + 1023) / 1024 * 1024;
+    // ring barriers (2 x kMaxStages x 8) | leaf barriers (2 x kLeafBufs x 8) | abort flags
+    // (16) | per-warp leaf pieces kLeafBufs x (NT/32) x kPieces u32 | ring
+    return ((16 * kMaxStages + 16 * kLeafBufs + 16 + kLeafBufs * (NT / 32) * kPieces * 4) + 1023) /
+           1024 * 1024;
 }
 
 // Correctly rounded x / b for a divisor b fixed for the whole launch, by Markstein's
@@ -133,32 +146,36 @@ __device__ __forceinline__ void acc_word(Acc3 &s, uint32_t x, const Limbs &p)
     mac(s.a2, x, p.l2);
 }
 
-// (a0 + a1 2^21 + a2 2^42) mod p, for a_k < 2^58 (2^61 == 1 mod p).
-__device__ __forceinline__ uint64_t fold3(const Acc3 &s)
+// x * 2^e mod p for x < p and 0 <= e < 61 (2^61 == 1 mod p): a 61-bit rotation.
+__device__ __forceinline__ uint64_t pf_shl(uint64_t x, int e)
 {
-    const uint64_t t1 = ((s.a1 & ((1ull << 40) - 1)) << 21) + (s.a1 >> 40);
-    const uint64_t t2 = ((s.a2 & ((1ull << 19) - 1)) << 42) + (s.a2 >> 19);
-    const uint64_t r = s.a0 + t1 + t2;   // < 2^58 + 2^61 + 2^18 + 2^61 + 2^39 < 2^63
-    return pf_reduce64(pf_reduce64(r));
+    return e == 0 ? x : (((x << e) & kP61) | (x >> (61 - e)));
 }
 
+// Block layout: warps 0..NT/32-1 compute, then one producer warp (TMA), then one leaf warp
+// that finishes the chunk digests from the compute warps' per-warp partial sums, so the
+// compute warps never wait for one another between chunks.
 template <int NT, int MODE>
-__global__ void __launch_bounds__(NT + 32, 1) k_adamw(const __grid_constant__ AdamwArgs A)
+__global__ void __launch_bounds__(NT + 64, Shape<NT>::min_blocks)
+k_adamw(const __grid_constant__ AdamwArgs A)
 {
     constexpr int NS = MODE == 0 ? 4 : 3;        // streamed arrays
     constexpr uint32_t TE = uint32_t(kEPT) * NT;
     constexpr int TPC = int(kChunk / TE);
     constexpr int W = NT / 32;
-    static_assert(W >= 3, "three warps finish the three leaves of a chunk");
     static_assert(TPC >= 1 && TPC * TE == kChunk, "tiles divide the chunk");
+    // words per thread per chunk: limb sums stay below 32 * 2^32 * 2^21 = 2^58
+    static_assert(TPC * kEPT <= 32, "limb sums must stay below 2^58");
 
     extern __shared__ __align__(1024) unsigned char smem[];
     const uint32_t S = A.stages;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem);
     uint64_t *empty = full + kMaxStages;
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + 16 * kMaxStages);
+    uint64_t *leaf_full = empty + kMaxStages;
+    uint64_t *leaf_empty = leaf_full + kLeafBufs;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(leaf_empty + kLeafBufs);
     volatile int *never_flag = abort_flag + 1;
-    uint64_t *pfbuf = reinterpret_cast<uint64_t *>(smem + 16 * kMaxStages + 16);
+    uint32_t *pieces_buf = reinterpret_cast<uint32_t *>(leaf_empty + kLeafBufs) + 4;
     unsigned char *ring = smem + ring_offset<NT>();
 
     const int tid = threadIdx.x;
@@ -166,6 +183,10 @@ __global__ void __launch_bounds__(NT + 32, 1) k_adamw(const __grid_constant__ Ad
         for (uint32_t s = 0; s < S; ++s) {
             mbar_init(smem_u32(&full[s]), 1);
             mbar_init(smem_u32(&empty[s]), W);
+        }
+        for (int b = 0; b < kLeafBufs; ++b) {
+            mbar_init(smem_u32(&leaf_full[b]), W);
+            mbar_init(smem_u32(&leaf_empty[b]), 1);
         }
         *abort_flag = 0;
         *never_flag = 0;
@@ -179,6 +200,50 @@ __global__ void __launch_bounds__(NT + 32, 1) k_adamw(const __grid_constant__ Ad
         src[0] = A.g; src[1] = A.w; src[2] = A.m; src[3] = A.v;
     } else {
         src[0] = A.w; src[1] = A.m; src[2] = A.v; src[3] = nullptr;
+    }
+
+    if (tid >= NT + 32) {
+        // -------------------------------- leaf warp --------------------------------
+        // Chunk k's three digests from the W x 27 per-warp piece sums: lane L = (stream s,
+        // limb l, piece j) adds its piece over the warps (exact, < 2^36), weighs it by
+        // 2^(21 l + 27 j) mod p, and lanes 9s..9s+8 sum to the stream's leaf.
+        const int lane = tid - NT - 32;
+        const int ls = lane / 9, ll = (lane / 3) % 3, lj = lane % 3;
+        const int shift = (21 * ll + 27 * lj) % 61;
+        uint32_t ci = 0;
+        bool aborted = false;
+        for (uint64_t k = A.chunk_lo + blockIdx.x; k < A.chunk_hi; k += gridDim.x, ++ci) {
+            const uint32_t b = ci % kLeafBufs, round = ci / kLeafBufs;
+            if (!aborted &&
+                !mbar_wait_bounded(smem_u32(&leaf_full[b]), round & 1u, abort_flag)) {
+                aborted = true;
+                if (lane == 0) {
+                    atomicOr(&A.sc->flags, flag_bit);
+                    *abort_flag = 1;
+                }
+            }
+            uint64_t sum = 0;
+            if (lane < kPieces) {
+                const uint32_t *pb = pieces_buf + b * W * kPieces + lane;
+#pragma unroll
+                for (int w = 0; w < W; ++w) sum += pb[w * kPieces];
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&leaf_empty[b]));
+            uint64_t term = lane < kPieces ? pf_shl(pf_reduce64(sum), shift) : 0;
+#pragma unroll
+            for (int d = 1; d < 9; ++d) {
+                const uint64_t o = __shfl_sync(0xFFFFFFFFu, term, (lane + d) & 31);
+                if (lane % 9 == 0 && lane < kPieces) term = pf_add(term, o);
+            }
+            if (lane % 9 == 0 && lane < kPieces) {
+                const uint64_t c0 = k * kChunk;
+                const uint64_t c1 = c0 + kChunk < A.n ? c0 + kChunk : A.n;
+                if (c0 >= A.begin && c1 <= A.end)
+                    A.leaves[1 + uint64_t(ls) * A.c + k] = pf_add(c1 - c0, term);
+            }
+        }
+        return;
     }
 
     if (tid >= NT) {
@@ -236,10 +301,9 @@ __global__ void __launch_bounds__(NT + 32, 1) k_adamw(const __grid_constant__ Ad
             for (int i = 0; i < 4; ++i) pw_fixed[q * 4 + i] = limbs_of(__ldg(A.powers + goff[q] + i));
     }
 
-    uint32_t it = 0;
-    int cb = 0;
+    uint32_t it = 0, ci = 0;
     bool aborted = false;
-    for (uint64_t k = A.chunk_lo + blockIdx.x; k < A.chunk_hi; k += gridDim.x) {
+    for (uint64_t k = A.chunk_lo + blockIdx.x; k < A.chunk_hi; k += gridDim.x, ++ci) {
         Acc3 acc[3] = {{0, 0, 0}, {0, 0, 0}, {0, 0, 0}};
 #pragma unroll
         for (int j = 0; j < TPC; ++j) {
@@ -364,26 +428,34 @@ __global__ void __launch_bounds__(NT + 32, 1) k_adamw(const __grid_constant__ Ad
             }
         }
 
-        // chunk leaves: exact integer sum of every thread's partial, then + W mod p
-        uint64_t *pb = pfbuf + cb * 3 * NT;
+        // chunk leaves: each warp sums its lanes' limb sums exactly (27-bit pieces, so 32
+        // lanes fit in 32 bits) and hands the 27 piece sums to the leaf warp
+        uint32_t part[kPieces];
 #pragma unroll
-        for (int s = 0; s < 3; ++s) pb[s * NT + tid] = fold3(acc[s]);
-        named_barrier(1, NT);
-        if (warp < 3) {
-            uint64_t sum = 0;
-#pragma unroll 4
-            for (int t = lane; t < NT; t += 32) sum = pf_add(sum, pb[warp * NT + t]);
+        for (int st = 0; st < 3; ++st) {
+            const uint64_t limb[3] = {acc[st].a0, acc[st].a1, acc[st].a2};
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1)
-                sum = pf_add(sum, __shfl_xor_sync(0xffffffffu, sum, off));
-            if (lane == 0) {
-                const uint64_t c0 = k * kChunk;
-                const uint64_t c1 = c0 + kChunk < A.n ? c0 + kChunk : A.n;
-                if (c0 >= A.begin && c1 <= A.end)
-                    A.leaves[1 + uint64_t(warp) * A.c + k] = pf_add(c1 - c0, sum);
+            for (int l = 0; l < 3; ++l) {
+                part[(st * 3 + l) * 3 + 0] = uint32_t(limb[l]) & ((1u << 27) - 1);
+                part[(st * 3 + l) * 3 + 1] = uint32_t(limb[l] >> 27) & ((1u << 27) - 1);
+                part[(st * 3 + l) * 3 + 2] = uint32_t(limb[l] >> 54);
             }
         }
-        cb ^= 1;
+#pragma unroll
+        for (int i = 0; i < kPieces; ++i) part[i] = __reduce_add_sync(0xFFFFFFFFu, part[i]);
+        if (lane == 0) {
+            const uint32_t b = ci % kLeafBufs, round = ci / kLeafBufs;
+            if (!aborted &&
+                !mbar_wait_bounded(smem_u32(&leaf_empty[b]), (round & 1u) ^ 1u, abort_flag)) {
+                aborted = true;
+                atomicOr(&A.sc->flags, flag_bit);
+                *abort_flag = 1;
+            }
+            uint32_t *pb = pieces_buf + (b * W + warp) * kPieces;
+#pragma unroll
+            for (int i = 0; i < kPieces; ++i) pb[i] = part[i];
+            mbar_arrive(smem_u32(&leaf_full[b]));
+        }
     }
 }
 
@@ -423,13 +495,18 @@ uint32_t ring_off(int nt)
     return nt == 128 ? ring_offset<128>() : (nt == 256 ? ring_offset<256>() : ring_offset<512>());
 }
 
+uint32_t ring_bytes(int nt)
+{
+    return nt == 128 ? Shape<128>::ring : (nt == 256 ? Shape<256>::ring : Shape<512>::ring);
+}
+
 }  // namespace
 
 size_t adamw_smem_bytes(int nt, int mode, AdamwArgs &args)
 {
     const uint32_t ns = mode == 0 ? 4u : 3u;
     const uint32_t stride = ns * uint32_t(kEPT) * uint32_t(nt) * 4u;
-    uint32_t stages = kRingBytes / stride;
+    uint32_t stages = ring_bytes(nt) / stride;
     if (stages > kMaxStages) stages = kMaxStages;
     if (stages < 2) stages = 2;
     args.stages = stages;
@@ -450,7 +527,7 @@ cudaError_t adamw_occupancy(int nt, int mode, size_t smem, int *blocks_per_sm)
     KernelFn f = pick(nt, mode);
     if (!f) return cudaErrorInvalidValue;
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-        blocks_per_sm, reinterpret_cast<const void *>(f), nt + 32, smem);
+        blocks_per_sm, reinterpret_cast<const void *>(f), nt + 64, smem);
 }
 
 cudaError_t launch_selftest_div(uint32_t b_begin, uint32_t b_count, unsigned long long *mismatches,
@@ -466,7 +543,7 @@ cudaError_t launch_adamw(int nt, int mode, const AdamwArgs &args, int grid, size
     KernelFn f = pick(nt, mode);
     if (!f) return cudaErrorInvalidValue;
     void *params[] = {const_cast<AdamwArgs *>(&args)};
-    return cudaLaunchKernel(reinterpret_cast<const void *>(f), dim3(grid), dim3(nt + 32),
+    return cudaLaunchKernel(reinterpret_cast<const void *>(f), dim3(grid), dim3(nt + 64),
                             params, smem, st);
 }
 

@@ -108,7 +108,7 @@ extern "C" int repstep_reduce_norm_noalloc(const void *const *d_grads, uint32_t 
         const float one = 1.0f;
         a.rho = one / float(R);
         ReduceShape s{};
-        s.nt = 256;
+        s.nt = 512;
         s.dtype = grad_dtype;
         s.staged = 0;
         s.rg = R >= 8 ? 8 : 4;

@@ -413,7 +413,7 @@ int repstep_create(const repstep_config *cfg, void *d_workspace, size_t workspac
     x->stream = static_cast<cudaStream_t>(stream);
     x->n = cfg->n;
     x->c = (cfg->n + kChunk - 1) / kChunk;
-    x->nt_reduce = cfg->block_threads ? cfg->block_threads : 256;
+    x->nt_reduce = cfg->block_threads ? cfg->block_threads : 512;
     x->nt_adamw = cfg->block_threads ? cfg->block_threads : 512;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
