@@ -282,6 +282,41 @@ class Repstep:
                                   C.byref(hp), int(step), self._out(norm_out, torch.float32),
                                   self._out(root_out, torch.int64)), "step")
 
+    def step_from_host(self, host_grads, staging, w, m, v, hp: HParams, step: int,
+                       norm_out=None, root_out=None, pieces: int = 8):
+        """One step whose replica gradients start in pinned host memory.
+
+        The parameter range is split into `pieces` chunk-aligned ranges; each range of every
+        replica is copied host-to-device on a side stream into `staging` (R device buffers of
+        n elements) and reduced as soon as it lands, so the reduce overlaps the copies.
+        Then clip, AdamW and the root run on the current stream.  Bit-identical to step()
+        on the same gradients (a reduce split into ranges gives the same bits)."""
+        host_grads, staging = list(host_grads), list(staging)
+        if len(host_grads) != len(staging):
+            raise ValueError("one staging buffer per replica")
+        for h in host_grads:
+            if h.is_cuda or not h.is_pinned() or not h.is_contiguous() or h.numel() < self.n:
+                raise ValueError("host gradients: contiguous pinned host tensors")
+        main = self._stream()
+        side = torch.cuda.Stream(self.device)
+        side.wait_stream(main)                       # staging buffers free to overwrite
+        per = -(-self.n // max(1, pieces))
+        per = -(-per // CHUNK) * CHUNK               # chunk-aligned ranges
+        for lo in range(0, self.n, per):
+            hi = min(self.n, lo + per)
+            with torch.cuda.stream(side):
+                for h, d in zip(host_grads, staging):
+                    d[lo:hi].copy_(h[lo:hi], non_blocking=True)
+                ev = torch.cuda.Event()
+                ev.record(side)
+            main.wait_event(ev)
+            self.reduce(staging, begin=lo, count=hi - lo)
+        for d in staging:
+            d.record_stream(side)
+        self.clip(hp.clip, norm_out=norm_out)
+        self.adamw(w, m, v, hp)
+        self.root(step, root_out=root_out)
+
     def image_write(self, step: int, w, m, v, dst: torch.Tensor):
         self._state(w, m, v)
         if dst.dtype != torch.uint8 or not dst.is_contiguous():
