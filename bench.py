@@ -71,13 +71,20 @@ def barrier(world):
         dist.barrier()
 
 
-def max_over_ranks(x: float, world: int) -> float:
+def max_over_ranks(x: float, world: int, device="cuda") -> float:
+    """Slowest rank's time (the job's time) for the weak-scaling replicas."""
     if world == 1:
         return x
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    t = torch.tensor([x], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_value(params_per_rank: int, ms_max: float, world: int) -> float:
+    """Whole-job params/s: every rank runs the whole step on its own replica of the
+    workload (no data-path exchange), so the job moves world x n params per step."""
+    return params_per_rank / (ms_max * 1e-3) * world
 
 
 # ------------------------------------------------------------------------------------
@@ -273,7 +280,7 @@ def run_ours(args, rank, world, local):
     if rank == 0 and not args.skip_cpu_baseline:
         cpu = cpu_baseline(wl, n, R, dev, args.cpu_seconds)
 
-    value = n / (ms * 1e-3) * world
+    value = job_value(n, ms, world)
     step_gbs = alg_step / (ms * 1e-3) / 1e9
     res = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
