@@ -499,6 +499,66 @@ int oracle_leaves(int32_t step, uint64_t n, const float *w, const float *m, cons
     return 0;
 }
 
+/* ------------------------------------------------------------------------------ */
+/* Audit-mode leaves: each leaf is BLAKE2b-64 of its bytes in the image -- the      */
+/* 8-byte header, then each 4096-element chunk of w, of m, of v as little-endian     */
+/* fp32 (the last chunk short).  [OPEN-1B] App. B hashes every step with host       */
+/* blake2b; this mode uses that function for the leaves as well as the nodes.       */
+/* hash_mode 0 = PF61 leaves (oracle_leaves), 1 = BLAKE2b-64 leaves.                */
+/* ------------------------------------------------------------------------------ */
+static uint64_t b2_64(const uint8_t *bytes, uint64_t len)
+{
+    uint8_t out[8];
+    oracle_blake2b(bytes, len, out, 8);
+    uint64_t r = 0;
+    for (int i = 7; i >= 0; --i) r = (r << 8) | out[i];
+    return r;
+}
+
+int oracle_leaves_mode(int32_t step, uint64_t n, const float *w, const float *m, const float *v,
+                       int hash_mode, uint64_t *leaves)
+{
+    if (hash_mode == 0) return oracle_leaves(step, n, w, m, v, leaves);
+    if (hash_mode != 1 || n > 0xFFFFFFFFull) return -1;
+    uint64_t c = (n + ORACLE_CHUNK - 1) / ORACLE_CHUNK;
+    uint8_t header[8];
+    uint32_t s = (uint32_t)step, nn = (uint32_t)n;
+    for (int i = 0; i < 4; ++i) {
+        header[i] = (uint8_t)(s >> (8 * i));
+        header[4 + i] = (uint8_t)(nn >> (8 * i));
+    }
+    leaves[0] = b2_64(header, 8);
+    const float *arrs[3] = { w, m, v };
+    uint8_t *buf = (uint8_t *)malloc(4 * ORACLE_CHUNK);
+    if (!buf) return -1;
+    for (int a = 0; a < 3; ++a) {
+        for (uint64_t k = 0; k < c; ++k) {
+            uint64_t lo = k * ORACLE_CHUNK;
+            uint64_t hi = lo + ORACLE_CHUNK < n ? lo + ORACLE_CHUNK : n;
+            for (uint64_t i = lo; i < hi; ++i) {
+                uint32_t u;
+                memcpy(&u, &arrs[a][i], 4);
+                for (int b = 0; b < 4; ++b) buf[4 * (i - lo) + b] = (uint8_t)(u >> (8 * b));
+            }
+            leaves[1 + (uint64_t)a * c + k] = b2_64(buf, 4 * (hi - lo));
+        }
+    }
+    free(buf);
+    return 0;
+}
+
+int oracle_state_hash_mode(int32_t step, uint64_t n, const float *w, const float *m,
+                           const float *v, int hash_mode, uint64_t *root)
+{
+    uint64_t L = oracle_num_leaves(n);
+    uint64_t *leaves = (uint64_t *)malloc(sizeof(uint64_t) * L);
+    if (!leaves) return -1;
+    if (oracle_leaves_mode(step, n, w, m, v, hash_mode, leaves) != 0) { free(leaves); return -1; }
+    *root = oracle_merkle_root(leaves, L);
+    free(leaves);
+    return 0;
+}
+
 /* State hash of (step, w, m, v): the Merkle root over oracle_leaves. */
 int oracle_state_hash(int32_t step, uint64_t n, const float *w, const float *m, const float *v,
                       uint64_t *root)
@@ -519,10 +579,26 @@ int oracle_state_hash(int32_t step, uint64_t n, const float *w, const float *m, 
 /* Outputs: pre-clip norm ([OPEN-1B] §3.4.2 logs the pre-clip norm), clip scale and  */
 /* Merkle root.  Returns 0, -1 (bad argument) or -2 (unsupported topology).          */
 /* ------------------------------------------------------------------------------ */
+int oracle_step_mode(const void *const *grads, int dtype, uint32_t nodes, uint32_t gpus_per_node,
+                     uint64_t n, float *w, float *m, float *v,
+                     float lr, float beta1, float beta2, float eps, float wd, float clip,
+                     int32_t t, int hash_mode, float *norm_out, float *scale_out,
+                     uint64_t *root_out);
+
 int oracle_step(const void *const *grads, int dtype, uint32_t nodes, uint32_t gpus_per_node,
                 uint64_t n, float *w, float *m, float *v,
                 float lr, float beta1, float beta2, float eps, float wd, float clip,
                 int32_t t, float *norm_out, float *scale_out, uint64_t *root_out)
+{
+    return oracle_step_mode(grads, dtype, nodes, gpus_per_node, n, w, m, v, lr, beta1, beta2,
+                            eps, wd, clip, t, 0, norm_out, scale_out, root_out);
+}
+
+int oracle_step_mode(const void *const *grads, int dtype, uint32_t nodes, uint32_t gpus_per_node,
+                     uint64_t n, float *w, float *m, float *v,
+                     float lr, float beta1, float beta2, float eps, float wd, float clip,
+                     int32_t t, int hash_mode, float *norm_out, float *scale_out,
+                     uint64_t *root_out)
 {
     float *g = (float *)malloc(sizeof(float) * (n ? n : 1));
     if (!g) return -1;
@@ -536,6 +612,6 @@ int oracle_step(const void *const *grads, int dtype, uint32_t nodes, uint32_t gp
     free(g);
     if (norm_out) *norm_out = norm;
     if (scale_out) *scale_out = scale;
-    if (root_out) return oracle_state_hash(t, n, w, m, v, root_out);
+    if (root_out) return oracle_state_hash_mode(t, n, w, m, v, hash_mode, root_out);
     return 0;
 }

@@ -68,6 +68,17 @@ def lib():
                                   C.c_float, C.c_int32, C.POINTER(C.c_float),
                                   C.POINTER(C.c_float), C.POINTER(C.c_uint64)]
         L.oracle_step.restype = C.c_int
+        L.oracle_leaves_mode.argtypes = [C.c_int32, C.c_uint64, fp, fp, fp, C.c_int, fp]
+        L.oracle_leaves_mode.restype = C.c_int
+        L.oracle_state_hash_mode.argtypes = [C.c_int32, C.c_uint64, fp, fp, fp, C.c_int,
+                                             C.POINTER(C.c_uint64)]
+        L.oracle_state_hash_mode.restype = C.c_int
+        L.oracle_step_mode.argtypes = [fp, C.c_int, C.c_uint32, C.c_uint32, C.c_uint64, fp, fp,
+                                       fp, C.c_float, C.c_float, C.c_float, C.c_float,
+                                       C.c_float, C.c_float, C.c_int32, C.c_int,
+                                       C.POINTER(C.c_float), C.POINTER(C.c_float),
+                                       C.POINTER(C.c_uint64)]
+        L.oracle_step_mode.restype = C.c_int
         _lib = L
     return _lib
 
@@ -215,26 +226,28 @@ def num_leaves(n: int) -> int:
     return int(lib().oracle_num_leaves(n))
 
 
-def leaves(step: int, w, m, v) -> np.ndarray:
+def leaves(step: int, w, m, v, hash_mode: int = 0) -> np.ndarray:
+    """Leaf digests: hash_mode 0 = PF61, 1 = BLAKE2b-64 (audit mode)."""
     w = _f32(w); m = _f32(m); v = _f32(v)
     n = w.size
     out = np.empty(num_leaves(n), np.uint64)
-    rc = lib().oracle_leaves(step, n, _p(w), _p(m), _p(v), _p(out))
+    rc = lib().oracle_leaves_mode(step, n, _p(w), _p(m), _p(v), hash_mode, _p(out))
     if rc != 0:
         raise ValueError("n too large for the header")
     return out
 
 
-def state_hash(step: int, w, m, v) -> int:
+def state_hash(step: int, w, m, v, hash_mode: int = 0) -> int:
     w = _f32(w); m = _f32(m); v = _f32(v)
     r = C.c_uint64()
-    rc = lib().oracle_state_hash(step, w.size, _p(w), _p(m), _p(v), C.byref(r))
+    rc = lib().oracle_state_hash_mode(step, w.size, _p(w), _p(m), _p(v), hash_mode, C.byref(r))
     if rc != 0:
         raise ValueError("n too large for the header")
     return int(r.value)
 
 
-def step(grads, w, m, v, *, lr, beta1, beta2, eps, wd, clip, t, nodes=1, gpus_per_node=None):
+def step(grads, w, m, v, *, lr, beta1, beta2, eps, wd, clip, t, nodes=1, gpus_per_node=None,
+         hash_mode=0):
     """One oracle step on copies of (w, m, v).  Returns dict(w, m, v, norm, scale, root)."""
     code, arrs, ptrs = _grad_arrays(grads)
     R = len(arrs)
@@ -246,9 +259,10 @@ def step(grads, w, m, v, *, lr, beta1, beta2, eps, wd, clip, t, nodes=1, gpus_pe
     n = w.size
     nv, sv, root = C.c_float(), C.c_float(), C.c_uint64()
     f = lambda x: float(np.float32(x))  # noqa: E731
-    rc = lib().oracle_step(C.cast(ptrs, C.c_void_p), code, nodes, gpus_per_node, n,
-                           _p(w), _p(m), _p(v), f(lr), f(beta1), f(beta2), f(eps), f(wd),
-                           f(clip), int(t), C.byref(nv), C.byref(sv), C.byref(root))
+    rc = lib().oracle_step_mode(C.cast(ptrs, C.c_void_p), code, nodes, gpus_per_node, n,
+                                _p(w), _p(m), _p(v), f(lr), f(beta1), f(beta2), f(eps), f(wd),
+                                f(clip), int(t), int(hash_mode), C.byref(nv), C.byref(sv),
+                                C.byref(root))
     if rc == -2:
         raise ValueError("topology breaks the canonical tree")
     if rc != 0:

@@ -548,3 +548,29 @@ def test_step_matches_torch_float64():
         opt.step()
     wt = p.detach().numpy()
     assert np.all(np.abs(w - wt) <= 64 * T * 2.0 ** -24 * (np.abs(wt) + float(LR)))
+
+
+# ----------------------------------------------------------------------------------
+# Audit-mode leaves (BLAKE2b-64 of each leaf's image bytes), pinned by hashlib
+# ----------------------------------------------------------------------------------
+def test_audit_leaves_match_hashlib_on_image_bytes():
+    rng = np.random.default_rng(23)
+    for n in [0, 1, 5, 32, 33, 4095, 4096, 4097, 2 * 4096 + 1000]:
+        w, m, v = (rng.standard_normal((3, n))).astype(np.float32)
+        img = O.image(9, w, m, v)
+        want = [hashlib.blake2b(img[0:8], digest_size=8).digest()]
+        for a in range(3):
+            arr = img[8 + 4 * n * a: 8 + 4 * n * (a + 1)]
+            for k in range(0, 4 * n, 4 * 4096):
+                want.append(hashlib.blake2b(arr[k:k + 4 * 4096], digest_size=8).digest())
+        want = [int.from_bytes(d, "little") for d in want]
+        got = O.leaves(9, w, m, v, hash_mode=1)
+        assert got.tolist() == want
+        assert O.state_hash(9, w, m, v, hash_mode=1) == O.merkle_root(np.array(want, np.uint64))
+
+
+def test_audit_and_pf61_modes_differ_but_share_the_tree():
+    rng = np.random.default_rng(24)
+    w, m, v = (rng.standard_normal((3, 9000))).astype(np.float32)
+    assert O.state_hash(1, w, m, v, 0) != O.state_hash(1, w, m, v, 1)
+    assert O.state_hash(1, w, m, v, 0) == O.merkle_root(O.leaves(1, w, m, v, 0))
