@@ -200,7 +200,8 @@ def run_ours(args, rank, world, local):
     log(f"[rank {rank}] generating {wl.name}: n={n:,} R={R} on {dev}")
     grads = [I.gen_grad(wl, 1, r, device=dev) for r in range(R)]
     w, m, v = I.gen_state(wl, device=dev)
-    ctx = rs.Repstep(n, grad_dtype=gdt, device=dev)
+    hash_mode = rs.HASH_BLAKE2B if args.hash_mode == "blake2b" else rs.HASH_PF61
+    ctx = rs.Repstep(n, grad_dtype=gdt, device=dev, hash_mode=hash_mode)
     norm = torch.empty(1, dtype=torch.float32, device=dev)
     root = torch.empty(1, dtype=torch.int64, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -292,7 +293,8 @@ def run_ours(args, rank, world, local):
                    "l2": "inputs larger than L2 (no flush needed): "
                          f"{(R * b_g + 32) * n / 1e9:.1f} GB moved per step",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "launch": "persistent grid (SM count x resident CTAs), 256/512 threads"},
+                   "launch": "persistent grid (SM count x resident CTAs), 512 compute threads",
+                   "hash_leaves": args.hash_mode},
         "hbm_gbs_step": step_gbs,
         "roofline_step": {"bound": "hbm", "achieved": step_gbs, "peak": peak,
                           "unit": "GB/s", "frac": step_gbs / peak, "peak_source": peak_src,
@@ -441,6 +443,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--skip-cpu-baseline", action="store_true")
     ap.add_argument("--skip-e2e", action="store_true")
+    ap.add_argument("--hash-mode", choices=["pf61", "blake2b"], default="pf61",
+                    help="leaf digest of the state hash (blake2b = audit mode)")
     ap.add_argument("--n", type=int, default=0,
                     help="override the workload's parameter count (small profiling cases)")
     args = ap.parse_args()

@@ -16,7 +16,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 OUT_DIR = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "librepstep.so")
-SOURCES = ["repstep.cu", "k_reduce.cu", "k_adamw.cu", "k_small.cu", "noalloc.cu"]
+SOURCES = ["repstep.cu", "k_reduce.cu", "k_adamw.cu", "k_small.cu", "k_blake2b.cu",
+           "noalloc.cu"]
 HEADERS = ["common.cuh", "kernels.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + [

@@ -333,6 +333,58 @@ __device__ __forceinline__ uint64_t b2_node(uint64_t ma, uint64_t mb)
 
 #undef REPSTEP_B2_ROUND
 #undef REPSTEP_B2_M
+
+// The full BLAKE2b compression F(h, m, t, last) of RFC 7693 §3.2 on one 128-byte block.
+#define REPSTEP_B2_RF(s0, s1, s2, s3, s4, s5, s6, s7, s8, s9, s10, s11, s12, s13, s14, s15) \
+    do {                                                                                \
+        REPSTEP_B2_G(0, 4, 8, 12, m[s0], m[s1]);                                        \
+        REPSTEP_B2_G(1, 5, 9, 13, m[s2], m[s3]);                                        \
+        REPSTEP_B2_G(2, 6, 10, 14, m[s4], m[s5]);                                       \
+        REPSTEP_B2_G(3, 7, 11, 15, m[s6], m[s7]);                                       \
+        REPSTEP_B2_G(0, 5, 10, 15, m[s8], m[s9]);                                       \
+        REPSTEP_B2_G(1, 6, 11, 12, m[s10], m[s11]);                                     \
+        REPSTEP_B2_G(2, 7, 8, 13, m[s12], m[s13]);                                      \
+        REPSTEP_B2_G(3, 4, 9, 14, m[s14], m[s15]);                                      \
+    } while (0)
+
+__device__ __forceinline__ void b2_compress(uint64_t (&h)[8], const uint64_t (&m)[16],
+                                            uint64_t t, bool last)
+{
+    uint64_t v[16] = {h[0], h[1], h[2], h[3], h[4], h[5], h[6], h[7],
+                      0x6A09E667F3BCC908ull, 0xBB67AE8584CAA73Bull, 0x3C6EF372FE94F82Bull,
+                      0xA54FF53A5F1D36F1ull, 0x510E527FADE682D1ull ^ t, 0x9B05688C2B3E6C1Full,
+                      0x1F83D9ABFB41BD6Bull, 0x5BE0CD19137E2179ull};
+    if (last) v[14] = ~v[14];
+    REPSTEP_B2_RF(0, 1, 2, 3, 4, 5, 6, 7, 8, 9, 10, 11, 12, 13, 14, 15);
+    REPSTEP_B2_RF(14, 10, 4, 8, 9, 15, 13, 6, 1, 12, 0, 2, 11, 7, 5, 3);
+    REPSTEP_B2_RF(11, 8, 12, 0, 5, 2, 15, 13, 10, 14, 3, 6, 7, 1, 9, 4);
+    REPSTEP_B2_RF(7, 9, 3, 1, 13, 12, 11, 14, 2, 6, 5, 10, 4, 0, 15, 8);
+    REPSTEP_B2_RF(9, 0, 5, 7, 2, 4, 10, 15, 14, 1, 11, 12, 6, 8, 3, 13);
+    REPSTEP_B2_RF(2, 12, 6, 10, 0, 11, 8, 3, 4, 13, 7, 5, 15, 14, 1, 9);
+    REPSTEP_B2_RF(12, 5, 1, 15, 14, 13, 4, 10, 0, 7, 6, 3, 9, 2, 8, 11);
+    REPSTEP_B2_RF(13, 11, 7, 14, 12, 1, 3, 9, 5, 0, 15, 4, 8, 6, 2, 10);
+    REPSTEP_B2_RF(6, 15, 14, 9, 11, 3, 0, 8, 12, 2, 13, 7, 1, 4, 10, 5);
+    REPSTEP_B2_RF(10, 2, 8, 4, 7, 6, 1, 5, 15, 11, 9, 14, 3, 12, 13, 0);
+    REPSTEP_B2_RF(0, 1, 2, 3, 4, 5, 6, 7, 8, 9, 10, 11, 12, 13, 14, 15);
+    REPSTEP_B2_RF(14, 10, 4, 8, 9, 15, 13, 6, 1, 12, 0, 2, 11, 7, 5, 3);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) h[i] ^= v[i] ^ v[i + 8];
+}
+
+// Unkeyed BLAKE2b-64 initial state (digest length 8 in the parameter block).
+__device__ __forceinline__ void b2_init64(uint64_t (&h)[8])
+{
+    h[0] = 0x6A09E667F3BCC908ull ^ 0x01010008ull;
+    h[1] = 0xBB67AE8584CAA73Bull;
+    h[2] = 0x3C6EF372FE94F82Bull;
+    h[3] = 0xA54FF53A5F1D36F1ull;
+    h[4] = 0x510E527FADE682D1ull;
+    h[5] = 0x9B05688C2B3E6C1Full;
+    h[6] = 0x1F83D9ABFB41BD6Bull;
+    h[7] = 0x5BE0CD19137E2179ull;
+}
+
+#undef REPSTEP_B2_RF
 #undef REPSTEP_B2_G
 
 }  // namespace repstep

@@ -9,6 +9,8 @@
 // FP32), writing w', m', v' in place; then the PF61 digest of every 4096-element chunk of
 // the NEW w', m', v' that lies wholly inside the range.
 // MODE 1 (leaves): the PF61 digests of the chunks of the given w, m, v, nothing written.
+// MODE 2 (AdamW only): MODE 0 without the digests (the audit hash mode digests the new
+// state with BLAKE2b afterwards).
 //
 // PF61 of a chunk of W 32-bit words x_i is (W + sum x_i K^(i+1)) mod (2^61 - 1).  Each
 // power P = K^(i+1) < 2^61 is split into three 21-bit limbs P = l0 + l1 2^21 + l2 2^42, and
@@ -159,7 +161,9 @@ template <int NT, int MODE>
 __global__ void __launch_bounds__(NT + 64, Shape<NT>::min_blocks)
 k_adamw(const __grid_constant__ AdamwArgs A)
 {
-    constexpr int NS = MODE == 0 ? 4 : 3;        // streamed arrays
+    constexpr bool UPDATE = MODE != 1;           // AdamW runs (modes 0 and 2)
+    constexpr bool LEAVES = MODE != 2;           // PF61 digests (modes 0 and 1)
+    constexpr int NS = UPDATE ? 4 : 3;           // streamed arrays
     constexpr uint32_t TE = uint32_t(kEPT) * NT;
     constexpr int TPC = int(kChunk / TE);
     constexpr int W = NT / 32;
@@ -194,9 +198,9 @@ k_adamw(const __grid_constant__ AdamwArgs A)
     }
     __syncthreads();
 
-    const uint32_t flag_bit = MODE == 0 ? kFlagTimeoutAdamw : kFlagTimeoutLeaves;
+    const uint32_t flag_bit = UPDATE ? kFlagTimeoutAdamw : kFlagTimeoutLeaves;
     const float *src[4];
-    if (MODE == 0) {
+    if (UPDATE) {
         src[0] = A.g; src[1] = A.w; src[2] = A.m; src[3] = A.v;
     } else {
         src[0] = A.w; src[1] = A.m; src[2] = A.v; src[3] = nullptr;
@@ -204,6 +208,7 @@ k_adamw(const __grid_constant__ AdamwArgs A)
 
     if (tid >= NT + 32) {
         // -------------------------------- leaf warp --------------------------------
+        if (!LEAVES) return;
         // Chunk k's three digests from the W x 27 per-warp piece sums: lane L = (stream s,
         // limb l, piece j) adds its piece over the warps (exact, < 2^36), weighs it by
         // 2^(21 l + 27 j) mod p, and lanes 9s..9s+8 sum to the stream's leaf.
@@ -289,7 +294,7 @@ k_adamw(const __grid_constant__ AdamwArgs A)
 
     // ------------------------------ compute threads -------------------------------
     const int lane = tid & 31, warp = tid >> 5;
-    const float scale = MODE == 0 ? A.sc->scale : 1.0f;
+    const float scale = UPDATE ? A.sc->scale : 1.0f;
     // the two 4-element groups of this thread within a tile
     const uint32_t goff[2] = {4u * tid, 4u * tid + 4u * NT};
     // with one tile per chunk, the word positions -- hence the powers -- never change
@@ -357,7 +362,7 @@ k_adamw(const __grid_constant__ AdamwArgs A)
 
             // the words hashed: the new state (MODE 0) or the given state (MODE 1)
             float4 hw[2], hm[2], hv[2];
-            if (MODE == 0) {
+            if (UPDATE) {
                 float g8[8], w8[8], m8[8], v8[8];
 #pragma unroll
                 for (int q = 0; q < 2; ++q) {
@@ -379,7 +384,7 @@ k_adamw(const __grid_constant__ AdamwArgs A)
                     hw[q] = x[q][0]; hm[q] = x[q][1]; hv[q] = x[q][2];
                 }
             }
-            if (MODE == 0) {
+            if (UPDATE) {
 #pragma unroll
                 for (int q = 0; q < 2; ++q) {
                     const uint64_t e0 = tr.base + goff[q];
@@ -404,6 +409,7 @@ k_adamw(const __grid_constant__ AdamwArgs A)
             }
 
             // PF61 terms x * K^(pos+1) for the word positions pos = j*TE + goff[q] + i
+            if (LEAVES)
 #pragma unroll
             for (int q = 0; q < 2; ++q) {
                 Limbs pw[4];
@@ -430,6 +436,7 @@ k_adamw(const __grid_constant__ AdamwArgs A)
 
         // chunk leaves: each warp sums its lanes' limb sums exactly (27-bit pieces, so 32
         // lanes fit in 32 bits) and hands the 27 piece sums to the leaf warp
+        if (!LEAVES) continue;
         uint32_t part[kPieces];
 #pragma unroll
         for (int st = 0; st < 3; ++st) {
@@ -483,9 +490,9 @@ using KernelFn = void (*)(AdamwArgs);
 KernelFn pick(int nt, int mode)
 {
     switch (nt) {
-    case 128: return mode ? k_adamw<128, 1> : k_adamw<128, 0>;
-    case 256: return mode ? k_adamw<256, 1> : k_adamw<256, 0>;
-    case 512: return mode ? k_adamw<512, 1> : k_adamw<512, 0>;
+    case 128: return mode == 1 ? k_adamw<128, 1> : (mode == 2 ? k_adamw<128, 2> : k_adamw<128, 0>);
+    case 256: return mode == 1 ? k_adamw<256, 1> : (mode == 2 ? k_adamw<256, 2> : k_adamw<256, 0>);
+    case 512: return mode == 1 ? k_adamw<512, 1> : (mode == 2 ? k_adamw<512, 2> : k_adamw<512, 0>);
     default: return nullptr;
     }
 }
@@ -504,7 +511,7 @@ uint32_t ring_bytes(int nt)
 
 size_t adamw_smem_bytes(int nt, int mode, AdamwArgs &args)
 {
-    const uint32_t ns = mode == 0 ? 4u : 3u;
+    const uint32_t ns = mode == 1 ? 3u : 4u;
     const uint32_t stride = ns * uint32_t(kEPT) * uint32_t(nt) * 4u;
     uint32_t stages = ring_bytes(nt) / stride;
     if (stages > kMaxStages) stages = kMaxStages;

@@ -79,6 +79,11 @@ cudaError_t launch_merkle(const uint64_t *in, uint64_t count, uint64_t *out, int
                           Scalars *sc, uint64_t *root_out, int blocks, cudaStream_t st);
 cudaError_t launch_write_header(void *dst, int32_t step, uint32_t n32, cudaStream_t st);
 
+// Audit-mode leaves: BLAKE2b-64 of the header and of every chunk of w, m, v (k_blake2b.cu).
+cudaError_t launch_leaves_b2(const float *w, const float *m, const float *v, uint64_t n,
+                             uint64_t c, uint64_t *leaves, uint32_t step, int sm_count,
+                             cudaStream_t st);
+
 constexpr int kFixMax = 64;   // chunk indices per fix-up launch
 
 }  // namespace repstep

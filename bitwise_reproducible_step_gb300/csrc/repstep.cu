@@ -38,7 +38,7 @@ bool valid_config(const repstep_config *cfg)
     if (cfg->block_threads != 0 && cfg->block_threads != 128 && cfg->block_threads != 256 &&
         cfg->block_threads != 512)
         return false;
-    return cfg->reserved == 0;
+    return cfg->hash_mode == REPSTEP_HASH_PF61 || cfg->hash_mode == REPSTEP_HASH_BLAKE2B;
 }
 
 Layout layout_of(uint64_t n)
@@ -285,30 +285,36 @@ int do_adamw(repstep_ctx *x, float *w, float *m, float *v, const repstep_hparams
     const float lo = std::ldexp(1.0f, -40), hi = 2.0f;
     a.fastdiv = (hp->bc1 >= lo && hp->bc1 <= hi && hp->bc2 >= lo && hp->bc2 <= hi) ? 1 : 0;
     const int nt = x->nt_adamw;
-    const size_t smem = adamw_smem_bytes(nt, 0, a);
-    cudaError_t e = adamw_prepare(nt, 0, smem);
+    // PF61 mode: AdamW fused with the leaf digests; audit mode: AdamW alone (the BLAKE2b
+    // leaves are computed from the final state by repstep_root)
+    const int mode = x->cfg.hash_mode == REPSTEP_HASH_BLAKE2B ? 2 : 0;
+    const size_t smem = adamw_smem_bytes(nt, mode, a);
+    cudaError_t e = adamw_prepare(nt, mode, smem);
     if (e != cudaSuccess) return x->cuda_fail(e);
     int bps = 1;
-    e = adamw_occupancy(nt, 0, smem, &bps);
+    e = adamw_occupancy(nt, mode, smem, &bps);
     if (e != cudaSuccess) return x->cuda_fail(e);
     const int grid = grid_for(x, bps, a.chunk_hi - a.chunk_lo);
-    e = launch_adamw(nt, 0, a, grid, smem, x->stream);
+    e = launch_adamw(nt, mode, a, grid, smem, x->stream);
     if (e != cudaSuccess) return x->cuda_fail(e);
     ++x->launches;
-    note_cut_chunks(x->cut_leaf, begin, end, x->n);
+    if (mode == 0) note_cut_chunks(x->cut_leaf, begin, end, x->n);
     return REPSTEP_OK;
 }
 
+// Merkle root over the leaves.  In the PF61 mode the first Merkle pass computes the header
+// leaf itself; in the audit mode the leaf kernel has already written it.
 int merkle(repstep_ctx *x, int32_t step, uint64_t *root_out)
 {
     const uint64_t L = 1 + 3 * x->c;
     const int nb = int((L + kChunk - 1) / kChunk);
+    const int header = x->cfg.hash_mode == REPSTEP_HASH_PF61 ? 1 : 0;
     cudaError_t e;
     if (nb == 1) {
-        e = launch_merkle(x->leaves(), L, nullptr, 1, x->leaves(), uint32_t(step), uint32_t(x->n),
-                          x->powers(), x->sc(), root_out, 1, x->stream);
+        e = launch_merkle(x->leaves(), L, nullptr, header, x->leaves(), uint32_t(step),
+                          uint32_t(x->n), x->powers(), x->sc(), root_out, 1, x->stream);
     } else {
-        e = launch_merkle(x->leaves(), L, x->merkle_part(), 1, x->leaves(), uint32_t(step),
+        e = launch_merkle(x->leaves(), L, x->merkle_part(), header, x->leaves(), uint32_t(step),
                           uint32_t(x->n), x->powers(), x->sc(), nullptr, nb, x->stream);
         if (e != cudaSuccess) return x->cuda_fail(e);
         ++x->launches;
@@ -320,10 +326,26 @@ int merkle(repstep_ctx *x, int32_t step, uint64_t *root_out)
     return REPSTEP_OK;
 }
 
+// Audit mode: BLAKE2b-64 leaves of the whole state (header included).
+int audit_leaves(repstep_ctx *x, int32_t step, const float *w, const float *m, const float *v)
+{
+    cudaError_t e = launch_leaves_b2(w, m, v, x->n, x->c, x->leaves(), uint32_t(step),
+                                     x->sm_count, x->stream);
+    if (e != cudaSuccess) return x->cuda_fail(e);
+    ++x->launches;
+    return REPSTEP_OK;
+}
+
 int do_root(repstep_ctx *x, int32_t step, uint64_t *root_out)
 {
     if (root_out && !aligned(root_out, 8)) return REPSTEP_ERR_ALIGN;
     if (!x->scale_ready || x->updated != x->n) return REPSTEP_ERR_STATE;
+    if (x->cfg.hash_mode == REPSTEP_HASH_BLAKE2B) {
+        x->cut_leaf.clear();
+        int rc = audit_leaves(x, step, x->sw, x->sm, x->sv);
+        if (rc) return rc;
+        return merkle(x, step, root_out);
+    }
     unique_sort(x->cut_leaf);
     for (size_t i = 0; i < x->cut_leaf.size(); i += kFixMax) {
         const int cnt = int(x->cut_leaf.size() - i < size_t(kFixMax) ? x->cut_leaf.size() - i : kFixMax);
@@ -342,6 +364,11 @@ int do_hash(repstep_ctx *x, int32_t step, const float *w, const float *m, const 
     if (!w || !m || !v) return REPSTEP_ERR_ARG;
     if (!aligned(w, 16) || !aligned(m, 16) || !aligned(v, 16)) return REPSTEP_ERR_ALIGN;
     if (root_out && !aligned(root_out, 8)) return REPSTEP_ERR_ALIGN;
+    if (x->cfg.hash_mode == REPSTEP_HASH_BLAKE2B) {
+        int rc = audit_leaves(x, step, w, m, v);
+        if (rc) return rc;
+        return merkle(x, step, root_out);
+    }
     if (x->n > 0) {
         AdamwArgs a{};
         a.w = const_cast<float *>(w);

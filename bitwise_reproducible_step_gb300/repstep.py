@@ -37,7 +37,11 @@ STATUS = {0: "REPSTEP_OK", 1: "REPSTEP_ERR_ARG", 2: "REPSTEP_ERR_ALIGN", 3: "REP
 
 class Config(C.Structure):
     _fields_ = [("n", C.c_uint64), ("grad_dtype", C.c_int32), ("grid_blocks", C.c_int32),
-                ("block_threads", C.c_int32), ("reserved", C.c_int32)]
+                ("block_threads", C.c_int32), ("hash_mode", C.c_int32)]
+
+
+HASH_PF61 = 0
+HASH_BLAKE2B = 1
 
 
 class HParams(C.Structure):
@@ -190,14 +194,16 @@ class Repstep:
     """One context over a torch-allocated device workspace (see repstep_create)."""
 
     def __init__(self, n: int, grad_dtype=torch.float32, device=None, grid_blocks: int = 0,
-                 block_threads: int = 0, stream: torch.cuda.Stream | None = None):
+                 block_threads: int = 0, stream: torch.cuda.Stream | None = None,
+                 hash_mode: int = HASH_PF61):
         L = lib()
         self.n = int(n)
         self.grad_dtype = grad_dtype
         self.device = torch.device("cuda", torch.cuda.current_device()) if device is None \
             else torch.device(device)
         self._fixed_stream = stream
-        self.cfg = Config(self.n, _dtype_code(grad_dtype), grid_blocks, block_threads, 0)
+        self.hash_mode = hash_mode
+        self.cfg = Config(self.n, _dtype_code(grad_dtype), grid_blocks, block_threads, hash_mode)
         nbytes = int(L.repstep_workspace_bytes(C.byref(self.cfg)))
         if nbytes == 0:
             raise RepstepError(1, "bad configuration")

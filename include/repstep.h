@@ -33,6 +33,8 @@
  *   hash             leaves: PF61(header words {step, n}), then PF61 of each 4096-element
  *                    chunk of w, of m, of v (as 32-bit words); PF61(x_0..x_{W-1}) =
  *                    (W + sum x_i K^(i+1)) mod (2^61-1), K = floor(2^61 (sqrt5 - 1) / 2).
+ *                    In audit mode (REPSTEP_HASH_BLAKE2B) each leaf is instead the LE u64
+ *                    BLAKE2b-64 of the same bytes: the 8-byte header, then each chunk.
  *                    Root = T(leaves) with node N(a,b) = LE64 of BLAKE2b-64(LE64 a||LE64 b).
  *
  * Conventions for every call:
@@ -78,6 +80,13 @@ enum repstep_status {
 
 enum repstep_dtype { REPSTEP_F32 = 0, REPSTEP_BF16 = 1 };
 
+/* Leaf digest of the state hash.  PF61 (default) is fused into the AdamW pass and stays
+ * under the HBM bound.  BLAKE2B ("audit mode") digests each leaf's image bytes with
+ * BLAKE2b-64 -- the function the OPEN-1B paper hashes its steps with (App. B) -- in a
+ * separate ALU-bound pass over the new state.  The Merkle tree and its BLAKE2b-64 nodes
+ * are the same in both modes. */
+enum repstep_hash_mode { REPSTEP_HASH_PF61 = 0, REPSTEP_HASH_BLAKE2B = 1 };
+
 /* Device flag bits reported by repstep_sync(). */
 #define REPSTEP_FLAG_NONFINITE_NORM  0x1u  /* the pre-clip norm is NaN or infinite        */
 #define REPSTEP_FLAG_TIMEOUT_REDUCE  0x2u  /* a bounded wait expired in the reduce kernel  */
@@ -93,7 +102,7 @@ typedef struct {
                                 the CTA count of the streaming kernels.  Never changes bits. */
     int32_t block_threads;   /* 0: default; else 128, 256 or 512 compute threads per CTA of
                                 the streaming kernels.  Never changes bits.                */
-    int32_t reserved;        /* must be 0                                                  */
+    int32_t hash_mode;       /* enum repstep_hash_mode (0 = PF61 leaves)                   */
 } repstep_config;
 
 typedef struct {

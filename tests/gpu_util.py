@@ -72,7 +72,7 @@ def root_of(t: torch.Tensor) -> int:
     return int(t.cpu().numpy().view(np.uint64)[0])
 
 
-def oracle_step(grads_np, w, m, v, t, nodes=1, clip=None):
+def oracle_step(grads_np, w, m, v, t, nodes=1, clip=None, hash_mode=0):
     return O.step(grads_np, w, m, v, lr=HP["lr"], beta1=HP["beta1"], beta2=HP["beta2"],
                   eps=HP["eps"], wd=HP["wd"], clip=HP["clip"] if clip is None else clip, t=t,
-                  nodes=nodes)
+                  nodes=nodes, hash_mode=hash_mode)

@@ -10,6 +10,8 @@ as a chain of pieces the oracle computes exactly:
 and every invariance (launch shape, topology, shard ranges) is checked on the full arrays
 by exact equality on the device.
 """
+import hashlib
+
 import numpy as np
 import pytest
 import torch
@@ -48,7 +50,15 @@ def gather(t: torch.Tensor, chunks, n):
     return [x.cpu() for x in out]
 
 
-def check_step_chain(ctx, grads_before, state_before, w, m, v, t, chunks, n, norm_t, root_t):
+def leaf_of(words: np.ndarray, hash_mode: int) -> int:
+    if hash_mode == 0:
+        return O.pf61(words.view(np.uint32))
+    return int.from_bytes(hashlib.blake2b(words.astype("<f4").tobytes(), digest_size=8).digest(),
+                          "little")
+
+
+def check_step_chain(ctx, grads_before, state_before, w, m, v, t, chunks, n, norm_t, root_t,
+                     hash_mode=0):
     """grads_before / state_before: host chunk lists gathered before the step."""
     c = (n + CH - 1) // CH
     chunk_sums = ctx.chunk_sums_view().cpu().numpy()
@@ -76,14 +86,16 @@ def check_step_chain(ctx, grads_before, state_before, w, m, v, t, chunks, n, nor
         U.assert_same_f32(new_m[i], m1, f"m chunk {k}")
         U.assert_same_f32(new_v[i], v1, f"v chunk {k}")
         for a, arr in enumerate((w1, m1, v1)):
-            assert leaves[1 + a * c + k] == O.pf61(arr.view(np.uint32)), f"leaf {a} chunk {k}"
-    hdr = O.pf61(np.array([t, n], dtype=np.uint64).astype(np.uint32))
+            assert leaves[1 + a * c + k] == leaf_of(arr, hash_mode), f"leaf {a} chunk {k}"
+    hdr_words = np.array([t, n], dtype=np.uint64).astype(np.uint32)
+    hdr = O.pf61(hdr_words) if hash_mode == 0 else int.from_bytes(
+        hashlib.blake2b(hdr_words.astype("<u4").tobytes(), digest_size=8).digest(), "little")
     assert leaves[0] == hdr
     assert U.root_of(root_t) == O.merkle_root(leaves)
     return float(norm_o)
 
 
-def run_big(wl, steps, ranges=None, compare_unsharded=False):
+def run_big(wl, steps, ranges=None, compare_unsharded=False, hash_mode=0):
     n, R = wl.n, wl.R
     dev = torch.device("cuda", 0)
     gdt = torch.bfloat16 if wl.grad_dtype == "bf16" else torch.float32
@@ -92,7 +104,7 @@ def run_big(wl, steps, ranges=None, compare_unsharded=False):
     if ranges:   # also sample the chunks the shard boundaries cut
         extra = {lo // CH for lo, _ in ranges[1:]}
         chunks = np.array(sorted(set(chunks.tolist()) | extra), dtype=np.int64)
-    ctx = rs.Repstep(n, grad_dtype=gdt, device=dev)
+    ctx = rs.Repstep(n, grad_dtype=gdt, device=dev, hash_mode=hash_mode)
     w, m, v = I.gen_state(wl, device=dev)
     twin = None
     if compare_unsharded:
@@ -117,7 +129,8 @@ def run_big(wl, steps, ranges=None, compare_unsharded=False):
         else:
             ctx.step(grads, w, m, v, hp, step=t, norm_out=norm, root_out=root)
         assert ctx.sync() & ~rs.FLAG_NONFINITE_NORM == 0
-        norms.append(check_step_chain(ctx, g_before, s_before, w, m, v, t, chunks, n, norm, root))
+        norms.append(check_step_chain(ctx, g_before, s_before, w, m, v, t, chunks, n, norm, root,
+                                      hash_mode))
         if twin is not None:
             tc, tw, tm, tv = twin
             tn = torch.empty(1, dtype=torch.float32, device=dev)
@@ -135,6 +148,12 @@ def test_flat1200m_r8_segscale():
     wl = I.WORKLOADS["flat1200m_r8_segscale"]
     norms = run_big(wl, steps=2)
     assert all(x < 1.0 for x in norms)              # tiny segment-scaled grads: no clip
+
+
+def test_flat1200m_r8_segscale_audit_mode():
+    """The bench workload with BLAKE2b-64 audit-mode leaves, one step."""
+    wl = I.WORKLOADS["flat1200m_r8_segscale"]
+    run_big(wl, steps=1, hash_mode=rs.HASH_BLAKE2B)
 
 
 def test_flat3000m_r8_bf16_spiked_shards():

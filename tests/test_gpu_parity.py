@@ -19,10 +19,10 @@ def _built():
 
 
 def run_steps(n, R, dtype=torch.float32, steps=3, scales=(1.0, 3000.0, 1.0), ctx_kw=None,
-              nodes=1, check_intermediates=True):
+              nodes=1, check_intermediates=True, hash_mode=0):
     """Run `steps` fused steps on the GPU and in the oracle; assert every output bit."""
     dev = torch.device("cuda", 0)
-    ctx = rs.Repstep(n, grad_dtype=dtype, device=dev, **(ctx_kw or {}))
+    ctx = rs.Repstep(n, grad_dtype=dtype, device=dev, hash_mode=hash_mode, **(ctx_kw or {}))
     w, m, v = I.gen_state(U.F32_WL, n=n, device=dev)
     ow, om, ov = w.cpu().numpy(), m.cpu().numpy(), v.cpu().numpy()
     norm = torch.empty(1, dtype=torch.float32, device=dev)
@@ -33,14 +33,14 @@ def run_steps(n, R, dtype=torch.float32, steps=3, scales=(1.0, 3000.0, 1.0), ctx
         gnp = U.oracle_grads(grads)
         ctx.step(grads, w, m, v, U.hp_for(t), step=t, norm_out=norm, root_out=root, nodes=nodes)
         flags = ctx.sync()
-        ref = U.oracle_step(gnp, ow, om, ov, t, nodes=nodes)
+        ref = U.oracle_step(gnp, ow, om, ov, t, nodes=nodes, hash_mode=hash_mode)
         ow, om, ov = ref["w"], ref["m"], ref["v"]
         if check_intermediates and n > 0:
             U.assert_same_f32(ctx.g_view(), O.reduce(gnp), f"g step {t}")
             _, chunks = O.norm(O.reduce(gnp), with_chunks=True)
             U.assert_same_f32(ctx.chunk_sums_view(), chunks, f"chunk sums step {t}")
             leaves = ctx.leaves_view().cpu().numpy().view(np.uint64)
-            assert np.array_equal(leaves, O.leaves(t, ow, om, ov)), f"leaves step {t}"
+            assert np.array_equal(leaves, O.leaves(t, ow, om, ov, hash_mode)), f"leaves step {t}"
         U.assert_same_f32(w, ow, f"w step {t}")
         U.assert_same_f32(m, om, f"m step {t}")
         U.assert_same_f32(v, ov, f"v step {t}")
@@ -72,6 +72,43 @@ def test_step_matches_oracle(n, R, dtype):
         assert any(r["norm"] > 1.0 for r in res)  # the clip was exercised
 
 
+@pytest.mark.parametrize("n,R,dtype", [
+    (1, 2, torch.float32),
+    (33, 3, torch.float32),
+    (4096, 8, torch.float32),
+    (3 * 4096 + 1234, 8, torch.bfloat16),
+    (100003, 16, torch.float32),
+])
+def test_audit_mode_step_matches_oracle(n, R, dtype):
+    """Audit mode: BLAKE2b-64 leaves over the image bytes (short final blocks included)."""
+    run_steps(n, R, dtype, hash_mode=rs.HASH_BLAKE2B)
+
+
+def test_audit_mode_shards_and_standalone_hash():
+    n = 8 * 37_501 + 5
+    dev = torch.device("cuda", 0)
+    a = rs.Repstep(n, device=dev, hash_mode=rs.HASH_BLAKE2B)
+    b = rs.Repstep(n, device=dev, hash_mode=rs.HASH_BLAKE2B)
+    wa, ma, va = I.gen_state(U.F32_WL, n=n, device=dev)
+    wb, mb, vb = wa.clone(), ma.clone(), va.clone()
+    r = torch.empty(3, dtype=torch.int64, device=dev)
+    grads = U.gen_grads(n, 8, 1, scale=3000.0)
+    hp = U.hp_for(1)
+    a.step(grads, wa, ma, va, hp, step=1, root_out=r[0:1])
+    for lo, hi in I.shard_ranges(n, 8):
+        b.reduce(grads, begin=lo, count=hi - lo)
+    b.clip(hp.clip)
+    for lo, hi in I.shard_ranges(n, 8):
+        b.adamw(wb, mb, vb, hp, begin=lo, count=hi - lo)
+    b.root(1, root_out=r[1:2])
+    b.hash(1, wb, mb, vb, root_out=r[2:3])
+    a.sync(); b.sync()
+    rr = r.cpu().numpy().view(np.uint64)
+    want = O.state_hash(1, wa.cpu().numpy(), ma.cpu().numpy(), va.cpu().numpy(), hash_mode=1)
+    assert rr[0] == rr[1] == rr[2] == want
+    U.assert_same_f32(wb, wa.cpu().numpy(), "w")
+
+
 def test_empty_parameter_vector():
     dev = torch.device("cuda", 0)
     ctx = rs.Repstep(0, device=dev)
@@ -84,6 +121,10 @@ def test_empty_parameter_vector():
     e = np.zeros(0, np.float32)
     assert float(norm.item()) == 0.0
     assert U.root_of(root) == O.state_hash(1, e, e, e)
+    ctx_a = rs.Repstep(0, device=dev, hash_mode=rs.HASH_BLAKE2B)
+    ctx_a.step(grads, z, z.clone(), z.clone(), U.hp_for(1), step=1, norm_out=norm, root_out=root)
+    ctx_a.sync()
+    assert U.root_of(root) == O.state_hash(1, e, e, e, hash_mode=1)
 
 
 @pytest.mark.parametrize("nt", [128, 256, 512])
