@@ -179,6 +179,59 @@ int oracle_reduce_topology(const void *const *grads, int dtype, uint32_t nodes,
 }
 
 /* ------------------------------------------------------------------------------ */
+/* Paper-exact reduction: [OPEN-1B] §6 Algorithm 1 with App. A.1-A.3.  The R inputs   */
+/* are the gradients of the virtual ranks in mesh order r = rep * dp_shard + shard.  */
+/* For each replica, its dp_shard shard gradients are summed in ascending shard     */
+/* order (App. A.2: the deterministic reduce-scatter's local sum) and multiplied by  */
+/* fp32(1/dp_shard) (App. A.3); the result is pushed into the TreeFold of App. A.1: */
+/* a binary-carry stack of (level, partial) where equal levels combine with the      */
+/* lower-replica partial on the left.  Result: the leftover blocks (one per set bit  */
+/* of dp_replicate) are combined starting from the largest block, each later block   */
+/* added on the right -- the reading that keeps both of App. A.1's stated rules      */
+/* (largest block first; lower-replica block on the left), whose level wording       */
+/* contradicts itself.  Finally g = Result * fp32(1/dp_replicate).                   */
+/* ------------------------------------------------------------------------------ */
+int oracle_reduce_alg1(const void *const *grads, int dtype, uint32_t R, uint32_t dp_shard,
+                       uint64_t n, float *g)
+{
+    if (R == 0 || dp_shard == 0 || R % dp_shard != 0 || (dtype != 0 && dtype != 1)) return -1;
+    uint32_t dp_rep = R / dp_shard;
+    float rho_shard = 1.0f / (float)dp_shard;
+    float rho_rep = 1.0f / (float)dp_rep;
+    /* the stack: at most one entry per level, 64 levels is more than any R */
+    float part[64];
+    int level[64];
+    for (uint64_t i = 0; i < n; ++i) {
+        int depth = 0;
+        float inner = 0.0f;
+        for (uint32_t r = 0; r < R; ++r) {
+            uint32_t shard = r % dp_shard;
+            float x = load_grad(grads[r], dtype, i);
+            if (shard == 0) inner = x;
+            else inner = inner + x;
+            if (shard == dp_shard - 1) {
+                float p = inner * rho_shard;
+                int lv = 0;
+                while (depth > 0 && level[depth - 1] == lv) {
+                    float lower = part[depth - 1];
+                    --depth;
+                    p = lower + p;        /* lower-replica operand on the left */
+                    ++lv;
+                }
+                part[depth] = p;
+                level[depth] = lv;
+                ++depth;
+            }
+        }
+        /* stack bottom = largest (earliest) block; left fold upward in the stack */
+        float acc = part[0];
+        for (int d = 1; d < depth; ++d) acc = acc + part[d];
+        g[i] = acc * rho_rep;
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------------ */
 /* Global gradient norm over fixed 4096-element chunks.                              */
 /* q_i = g_i * g_i; s_k = T(q over chunk k in index order); S = T(s_0..s_{c-1});     */
 /* norm = sqrt(S).  Chunk k = [4096k, min(4096k + 4096, n)); the last chunk uses its */

@@ -79,6 +79,8 @@ def lib():
                                        C.POINTER(C.c_float), C.POINTER(C.c_float),
                                        C.POINTER(C.c_uint64)]
         L.oracle_step_mode.restype = C.c_int
+        L.oracle_reduce_alg1.argtypes = [fp, C.c_int, C.c_uint32, C.c_uint32, C.c_uint64, fp]
+        L.oracle_reduce_alg1.restype = C.c_int
         _lib = L
     return _lib
 
@@ -146,6 +148,18 @@ def reduce_topology(grads, nodes: int, gpus_per_node: int) -> np.ndarray:
         raise ValueError("topology breaks the canonical tree")
     if rc != 0:
         raise ValueError(f"oracle_reduce_topology rc={rc}")
+    return g
+
+
+def reduce_alg1(grads, dp_shard: int) -> np.ndarray:
+    """Paper-exact reduction (OPEN-1B §6 Algorithm 1) over R = dp_replicate * dp_shard
+    virtual-rank gradients in mesh order."""
+    code, arrs, ptrs = _grad_arrays(grads)
+    n = arrs[0].size
+    g = np.empty(n, np.float32)
+    rc = lib().oracle_reduce_alg1(C.cast(ptrs, C.c_void_p), code, len(arrs), dp_shard, n, _p(g))
+    if rc != 0:
+        raise ValueError(f"oracle_reduce_alg1 rc={rc}")
     return g
 
 

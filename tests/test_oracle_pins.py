@@ -118,7 +118,7 @@ def test_tree_reading_differs_from_treefold_at_seven():
 def _rounding_cases():
     cases = {}
     for line in open(os.path.join(GOLDEN, "rounding_cases.txt")):
-        if not line.strip() or line.startswith("#"):
+        if not line.strip() or line.startswith("#") or line.startswith("alg1_"):
             continue
         name, ins, want, _why = [s.strip() for s in line.split("|")]
         cases[name] = (ins, X.parse_exact(want))
@@ -136,6 +136,42 @@ def test_golden_replica_sums():
         rho = X.f32(Fraction(1, R))
         expect = X.mul(np.float32(float(want)), rho)
         assert all(X.bits(x) == X.bits(expect) for x in g), (name, g, expect)
+
+
+def test_golden_alg1_reductions():
+    for line in open(os.path.join(GOLDEN, "rounding_cases.txt")):
+        if not line.startswith("alg1_"):
+            continue
+        name, dps, ins, want, _why = [x.strip() for x in line.split("|")]
+        dp_shard = int(dps)
+        vals = [float(X.parse_exact(t)) for t in ins.split(",")]
+        R = len(vals)
+        g = O.reduce_alg1([np.full(3, v, np.float32) for v in vals], dp_shard)
+        rho_rep = X.f32(Fraction(1, R // dp_shard))
+        expect = X.mul(np.float32(float(X.parse_exact(want))), rho_rep)
+        assert all(X.bits(x) == X.bits(expect) for x in g), (name, g, expect)
+
+
+@pytest.mark.parametrize("R", [1, 2, 4, 8, 16, 32])
+def test_alg1_one_shard_power_of_two_equals_canonical_tree(R):
+    # dp_shard = 1 and a power-of-two replica count: TreeFold is the perfect tree
+    rng = np.random.default_rng(200 + R)
+    G = [rand_f32(rng, 500, -26, 2) for _ in range(R)]
+    assert np.array_equal(O.reduce_alg1(G, 1).view(np.uint32), O.reduce(G).view(np.uint32))
+
+
+def test_alg1_within_error_bound_and_order_sensitive():
+    rng = np.random.default_rng(31)
+    for R, dps in [(6, 2), (12, 4), (12, 3), (9, 9), (10, 5)]:
+        G = [(rng.standard_normal(3000) * 1e-3).astype(np.float32) for _ in range(R)]
+        g = O.reduce_alg1(G, dps).astype(np.float64)
+        S = np.sum([x.astype(np.float64) for x in G], axis=0)
+        A = np.sum([np.abs(x.astype(np.float64)) for x in G], axis=0)
+        u = 2.0 ** -24
+        bound = (R + 3) * u * A / R * 1.0001 + 1e-45
+        assert np.all(np.abs(g - S / R) <= bound)
+    G = [rand_f32(rng, 4000, -26, 2) for _ in range(12)]
+    assert not np.array_equal(O.reduce_alg1(G, 4), O.reduce_alg1(G, 3))
 
 
 def test_golden_chunk_sum():
