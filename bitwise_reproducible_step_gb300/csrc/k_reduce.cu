@@ -78,6 +78,28 @@ __device__ __forceinline__ float4 stack_result(const float4 (&st)[MAXLEV], uint3
     return acc;
 }
 
+// TreeFold's Result in the paper-exact mode: the leftover blocks, one per set bit of
+// `count`, combined starting from the largest (lowest replicas, highest level), each later
+// block added on the right.
+template <int MAXLEV>
+__device__ __forceinline__ float4 stack_result_leftfold(const float4 (&st)[MAXLEV], uint32_t count)
+{
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    bool have = false;
+#pragma unroll
+    for (int L = MAXLEV - 1; L >= 0; --L) {
+        if ((count >> L) & 1u) {
+            if (have) {
+                acc = add4(acc, st[L]);
+            } else {
+                acc = st[L];
+                have = true;
+            }
+        }
+    }
+    return acc;
+}
+
 template <int RG>
 __device__ __forceinline__ float4 tree_group(float4 (&x)[RG])
 {
@@ -119,7 +141,12 @@ __device__ __forceinline__ float4 load_group(const unsigned char *tile, uint32_t
     return make_float4(r[0], r[1], r[2], r[3]);
 }
 
-template <int NT, int DT, bool STAGED, int RG, int MAXLEV>
+// MODE 0: the canonical tree over all R replicas.  MODE 1: the same tree staged as a
+// cluster would run it (each node's replicas, then the node partials).  MODE 2: the
+// paper-exact order of OPEN-1B §6 Algorithm 1 (ascending shard sums times fp32(1/dp_shard),
+// TreeFold over replicas, Result times fp32(1/dp_replicate)); A.gpn = dp_shard,
+// A.nodes = dp_replicate, A.rho2 = fp32(1/dp_shard), A.rho = fp32(1/dp_replicate).
+template <int NT, int DT, int MODE, int RG, int MAXLEV>
 __global__ void __launch_bounds__(NT + 32, 1) k_reduce(const __grid_constant__ ReduceArgs A)
 {
     constexpr int W = NT / 32;
@@ -220,6 +247,8 @@ __global__ void __launch_bounds__(NT + 32, 1) k_reduce(const __grid_constant__ R
             const bool in_bulk = e0 >= tr.a16 && e0 + 4 <= tr.b16;
             float4 st[MAXLEV];
             float4 sto[MAXLEV];   // node partials (staged sum only)
+            float4 inner = make_float4(0.f, 0.f, 0.f, 0.f);   // running shard sum (MODE 2)
+            uint32_t c_in = 0, c_out = 0;   // position within a node / replica, and its index
             for (uint32_t q = 0; q < NG; ++q) {
                 const uint32_t slot = it % S, round = it / S;
                 if (!aborted &&
@@ -232,41 +261,59 @@ __global__ void __launch_bounds__(NT + 32, 1) k_reduce(const __grid_constant__ R
                 }
                 const unsigned char *sb = ring + slot * A.stage_stride;
                 const uint32_t nr = min(uint32_t(RG), R - q * RG);
-                float4 x[RG];
+                if constexpr (MODE == 0) {
+                    float4 x[RG];
 #pragma unroll
-                for (int i = 0; i < RG; ++i) {
-                    if (uint32_t(i) < nr)
-                        x[i] = load_group<DT>(sb + i * TE * ESZ, off, in_bulk,
-                                              A.grads[q * RG + i], e0, tr.a, tr.b);
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&empty[slot]));
-                ++it;
-                if constexpr (STAGED) {
-                    // per node first, then over nodes (a two-level cluster reduction)
+                    for (int i = 0; i < RG; ++i) {
+                        if (uint32_t(i) < nr)
+                            x[i] = load_group<DT>(sb + i * TE * ESZ, off, in_bulk,
+                                                  A.grads[q * RG + i], e0, tr.a, tr.b);
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&empty[slot]));
+                    ++it;
+                    if (nr == uint32_t(RG)) {
+                        push_block<MAXLEV, LOG2RG>(st, q, tree_group<RG>(x));
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < RG; ++i)
+                            if (uint32_t(i) < nr) push_block<MAXLEV, 0>(st, q * RG + i, x[i]);
+                    }
+                } else {
+                    // one replica at a time straight from the staged tile
+#pragma unroll 1
                     for (uint32_t i = 0; i < nr; ++i) {
-                        float4 xi = x[0];
-#pragma unroll
-                        for (int t = 1; t < RG; ++t)
-                            if (uint32_t(t) == i) xi = x[t];
-                        const uint32_t r = q * RG + i;
-                        const uint32_t node = r / A.gpn, gi = r % A.gpn;
-                        push_block<MAXLEV, 0>(st, gi, xi);
-                        if (gi == A.gpn - 1) {
-                            const float4 p = stack_result<MAXLEV>(st, A.gpn);
-                            push_block<MAXLEV, 0>(sto, node, p);
+                        const float4 xi = load_group<DT>(sb + i * TE * ESZ, off, in_bulk,
+                                                         A.grads[q * RG + i], e0, tr.a, tr.b);
+                        if constexpr (MODE == 2) {
+                            // virtual ranks in mesh order: ascending sum over a replica's
+                            // shards, times fp32(1/dp_shard), then into the TreeFold
+                            inner = c_in == 0 ? xi : add4(inner, xi);
+                            if (++c_in == A.gpn) {
+                                const float4 p = make_float4(
+                                    __fmul_rn(inner.x, A.rho2), __fmul_rn(inner.y, A.rho2),
+                                    __fmul_rn(inner.z, A.rho2), __fmul_rn(inner.w, A.rho2));
+                                push_block<MAXLEV, 0>(st, c_out++, p);
+                                c_in = 0;
+                            }
+                        } else {
+                            // per node first, then over nodes (a two-level cluster reduction)
+                            push_block<MAXLEV, 0>(st, c_in, xi);
+                            if (++c_in == A.gpn) {
+                                const float4 p = stack_result<MAXLEV>(st, A.gpn);
+                                push_block<MAXLEV, 0>(sto, c_out++, p);
+                                c_in = 0;
+                            }
                         }
                     }
-                } else if (nr == uint32_t(RG)) {
-                    push_block<MAXLEV, LOG2RG>(st, q, tree_group<RG>(x));
-                } else {
-#pragma unroll
-                    for (int i = 0; i < RG; ++i)
-                        if (uint32_t(i) < nr) push_block<MAXLEV, 0>(st, q * RG + i, x[i]);
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&empty[slot]));
+                    ++it;
                 }
             }
             float4 s;
-            if constexpr (STAGED) s = stack_result<MAXLEV>(sto, A.nodes);
+            if constexpr (MODE == 2) s = stack_result_leftfold<MAXLEV>(st, A.nodes);
+            else if constexpr (MODE == 1) s = stack_result<MAXLEV>(sto, A.nodes);
             else s = stack_result<MAXLEV>(st, R);
             const float4 gv = make_float4(__fmul_rn(s.x, rho), __fmul_rn(s.y, rho),
                                           __fmul_rn(s.z, rho), __fmul_rn(s.w, rho));
@@ -307,10 +354,11 @@ using KernelFn = void (*)(ReduceArgs);
 template <int NT, int DT>
 KernelFn pick_dt(const ReduceShape &s)
 {
-    if (s.staged) return k_reduce<NT, DT, true, 8, 9>;
-    if (s.rg == 4) return k_reduce<NT, DT, false, 4, 6>;
-    if (s.maxlev == 6) return k_reduce<NT, DT, false, 8, 6>;
-    return k_reduce<NT, DT, false, 8, 9>;
+    if (s.mode == 2) return s.maxlev == 6 ? k_reduce<NT, DT, 2, 8, 6> : k_reduce<NT, DT, 2, 8, 9>;
+    if (s.mode == 1) return s.maxlev == 6 ? k_reduce<NT, DT, 1, 8, 6> : k_reduce<NT, DT, 1, 8, 9>;
+    if (s.rg == 4) return k_reduce<NT, DT, 0, 4, 6>;
+    if (s.maxlev == 6) return k_reduce<NT, DT, 0, 8, 6>;
+    return k_reduce<NT, DT, 0, 8, 9>;
 }
 
 KernelFn pick(const ReduceShape &s)
@@ -331,7 +379,7 @@ size_t reduce_smem_bytes(const ReduceShape &s, ReduceArgs &args)
     const uint32_t esz = s.dtype == 1 ? 2u : 4u;
     const uint32_t te = 4u * uint32_t(s.nt);
     const uint32_t per_stage = (args.R < uint32_t(s.rg) ? args.R : uint32_t(s.rg));
-    const uint32_t stride = (s.staged ? 8u : per_stage) * te * esz;
+    const uint32_t stride = (s.mode != 0 ? 8u : per_stage) * te * esz;
     uint32_t stages = kRingBytes / stride;
     if (stages > kMaxStages) stages = kMaxStages;
     if (stages < 2) stages = 2;

@@ -21,13 +21,14 @@ struct ReduceArgs {
     uint32_t R, nodes, gpn;
     uint32_t stages;          // ring depth
     uint32_t stage_stride;    // bytes per stage
-    float rho;                // fp32(1/R)
+    float rho;                // fp32(1/R); fp32(1/dp_replicate) in the paper-exact mode
+    float rho2;               // fp32(1/dp_shard) in the paper-exact mode
 };
 
 struct ReduceShape {
     int nt;          // compute threads (128, 256, 512)
     int dtype;       // 0 fp32, 1 bf16
-    int staged;      // topology-staged sum
+    int mode;        // 0 canonical tree, 1 topology-staged, 2 paper-exact (Algorithm 1)
     int rg;          // replicas per stage group (4 or 8)
     int maxlev;      // carry-stack depth (6 or 9)
 };

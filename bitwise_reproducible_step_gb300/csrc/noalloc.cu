@@ -110,7 +110,7 @@ extern "C" int repstep_reduce_norm_noalloc(const void *const *d_grads, uint32_t 
         ReduceShape s{};
         s.nt = 512;
         s.dtype = grad_dtype;
-        s.staged = 0;
+        s.mode = 0;
         s.rg = R >= 8 ? 8 : 4;
         s.maxlev = R <= 32 ? 6 : 9;
         const size_t smem = reduce_smem_bytes(s, a);

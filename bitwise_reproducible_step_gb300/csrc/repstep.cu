@@ -144,13 +144,15 @@ int check_hparams(const repstep_hparams *hp)
     return REPSTEP_OK;
 }
 
+// mode 0: canonical tree (nodes x gpn staged when nodes > 1); mode 2: paper-exact order of
+// OPEN-1B Algorithm 1 with dp_replicate = nodes and dp_shard = gpn.
 int do_reduce(repstep_ctx *x, const void *const *grads, uint32_t R, uint32_t nodes,
-              uint32_t gpn, uint64_t begin, uint64_t count)
+              uint32_t gpn, uint64_t begin, uint64_t count, int paper = 0)
 {
     if (!grads || R == 0) return REPSTEP_ERR_ARG;
     if (R > kMaxReplicas) return REPSTEP_ERR_SIZE;
     if (nodes == 0 || gpn == 0 || uint64_t(nodes) * gpn != R) return REPSTEP_ERR_TOPOLOGY;
-    if (nodes > 1 && (gpn & (gpn - 1)) != 0) return REPSTEP_ERR_TOPOLOGY;
+    if (!paper && nodes > 1 && (gpn & (gpn - 1)) != 0) return REPSTEP_ERR_TOPOLOGY;
     if (begin > x->n || count > x->n - begin) return REPSTEP_ERR_ARG;
     for (uint32_t r = 0; r < R; ++r) {
         if (!grads[r]) return REPSTEP_ERR_ARG;
@@ -179,11 +181,12 @@ int do_reduce(repstep_ctx *x, const void *const *grads, uint32_t R, uint32_t nod
     a.nodes = nodes;
     a.gpn = gpn;
     const float one = 1.0f;
-    a.rho = one / float(R);
+    a.rho = paper ? one / float(nodes) : one / float(R);
+    a.rho2 = paper ? one / float(gpn) : one;
     ReduceShape s{};
     s.nt = x->nt_reduce;
     s.dtype = x->cfg.grad_dtype;
-    s.staged = nodes > 1 ? 1 : 0;
+    s.mode = paper ? 2 : (nodes > 1 ? 1 : 0);
     s.rg = R >= 8 ? 8 : 4;
     s.maxlev = R <= 32 ? 6 : 9;
     const size_t smem = reduce_smem_bytes(s, a);
@@ -476,6 +479,14 @@ int repstep_reduce(repstep_ctx *ctx, const void *const *d_grads, uint32_t R, uin
 {
     if (!ctx) return REPSTEP_ERR_ARG;
     return do_reduce(ctx, d_grads, R, nodes, gpus_per_node, begin, count);
+}
+
+int repstep_reduce_paper(repstep_ctx *ctx, const void *const *d_grads, uint32_t R,
+                         uint32_t dp_shard, uint64_t begin, uint64_t count)
+{
+    if (!ctx) return REPSTEP_ERR_ARG;
+    if (dp_shard == 0 || R % dp_shard != 0) return REPSTEP_ERR_TOPOLOGY;
+    return do_reduce(ctx, d_grads, R, R / dp_shard, dp_shard, begin, count, 1);
 }
 
 int repstep_clip(repstep_ctx *ctx, float clip, float *d_norm_out, float *d_scale_out)

@@ -67,7 +67,7 @@ EXPORTS = [
     "repstep_hash", "repstep_step", "repstep_image_bytes", "repstep_image_write",
     "repstep_image_read", "repstep_bias_corrections", "repstep_sync", "repstep_launch_count",
     "repstep_last_cuda_error", "repstep_strerror", "repstep_reduce_norm_noalloc",
-    "repstep_selftest_fixed_division",
+    "repstep_selftest_fixed_division", "repstep_reduce_paper",
 ]
 NOALLOC_MAX_N = 1 << 30
 
@@ -111,6 +111,7 @@ def lib():
     L.repstep_strerror.argtypes = [C.c_int]
     L.repstep_strerror.restype = C.c_char_p
     L.repstep_selftest_fixed_division.argtypes = [u32, u32, vp, vp]
+    L.repstep_reduce_paper.argtypes = [vp, C.POINTER(vp), u32, u32, u64, u64]
     L.repstep_reduce_norm_noalloc.argtypes = [C.POINTER(vp), u32, i32, u64, C.c_float, vp, vp,
                                               vp, vp]
     _lib = L
@@ -255,6 +256,15 @@ class Repstep:
         count = self.n - begin if count is None else count
         self._bind()
         _check(lib().repstep_reduce(self._ctx, arr, R, nodes, gpn, begin, count), "reduce")
+
+    def reduce_paper(self, grads, dp_shard: int, begin: int = 0, count: int | None = None):
+        """Paper-exact reduce (OPEN-1B Algorithm 1): grads are the virtual-rank gradients
+        in mesh order, R = dp_replicate * dp_shard (see repstep_reduce_paper)."""
+        arr, R = self._grads(grads)
+        count = self.n - begin if count is None else count
+        self._bind()
+        _check(lib().repstep_reduce_paper(self._ctx, arr, R, dp_shard, begin, count),
+               "reduce_paper")
 
     def clip(self, clip: float, norm_out=None, scale_out=None):
         self._bind()

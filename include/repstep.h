@@ -150,6 +150,20 @@ int repstep_set_stream(repstep_ctx *ctx, void *stream);
 int repstep_reduce(repstep_ctx *ctx, const void *const *d_grads, uint32_t R, uint32_t nodes,
                    uint32_t gpus_per_node, uint64_t begin, uint64_t count);
 
+/* Paper-exact replica reduce: the order of OPEN-1B §6 Algorithm 1 (App. A), for replaying
+ * a cluster run bit for bit.  d_grads holds the R = dp_replicate * dp_shard virtual-rank
+ * gradients in mesh order (r = replica * dp_shard + shard).  Per replica: its dp_shard
+ * gradients summed in ascending shard order (App. A.2), times fp32(1/dp_shard) (App. A.3);
+ * the replica partials folded by TreeFold (App. A.1: binary carry, lower replica on the
+ * left; Result combines the leftover blocks from the largest, each later block on the
+ * right -- the reading taken of App. A.1's self-contradictory level wording); times
+ * fp32(1/dp_replicate).  Any dp_shard dividing R (REPSTEP_ERR_TOPOLOGY otherwise);
+ * dp_replicate <= 256.  It writes the same workspace as repstep_reduce (g and the chunk sums)
+ * and is followed by repstep_clip / repstep_adamw / repstep_root as usual.  For dp_shard = 1
+ * and a power-of-two R it equals repstep_reduce bit for bit. */
+int repstep_reduce_paper(repstep_ctx *ctx, const void *const *d_grads, uint32_t R,
+                         uint32_t dp_shard, uint64_t begin, uint64_t count);
+
 /* Global norm and clip scale (OPEN-1B §3.2, §3.4.2) from the chunk sums of the reduced g.
  * Requires the reduce calls since the previous clip to have covered exactly n elements
  * (else REPSTEP_ERR_STATE).  Writes the pre-clip norm and the scale to the optional device

@@ -58,7 +58,7 @@ def leaf_of(words: np.ndarray, hash_mode: int) -> int:
 
 
 def check_step_chain(ctx, grads_before, state_before, w, m, v, t, chunks, n, norm_t, root_t,
-                     hash_mode=0):
+                     hash_mode=0, reducer=O.reduce):
     """grads_before / state_before: host chunk lists gathered before the step."""
     c = (n + CH - 1) // CH
     chunk_sums = ctx.chunk_sums_view().cpu().numpy()
@@ -75,7 +75,7 @@ def check_step_chain(ctx, grads_before, state_before, w, m, v, t, chunks, n, nor
     g_got = gather(g_dev, chunks, n)
     for i, k in enumerate(chunks):
         G = [I.to_numpy(gr[i]) for gr in grads_before]
-        g = O.reduce(G)
+        g = reducer(G)
         U.assert_same_f32(g_got[i], g, f"g chunk {k}")
         _, s = O.norm(g, with_chunks=True)
         assert s.view(np.uint32)[0] == chunk_sums[k:k + 1].view(np.uint32)[0], f"chunk sum {k}"
@@ -205,3 +205,28 @@ def test_fixed_division_is_ieee_for_every_significand_pair():
     """The AdamW kernel divides by the step's bias corrections with Markstein's correction
     from a precomputed reciprocal; compare it with IEEE division for all 2^46 pairs."""
     assert rs.selftest_fixed_division(0, 1 << 23) == 0
+
+
+def test_flat268m_r32_paper_exact_order():
+    """OPEN-1B Algorithm 1 order on 268M parameters: 4 replicas x 8 shards (linear shard
+    sums, TreeFold over replicas), sampled chunks against the oracle's restatement."""
+    wl = I.WORKLOADS["flat268m_r32_topologies"]
+    n, R, dps = wl.n, wl.R, 8
+    dev = torch.device("cuda", 0)
+    c = (n + CH - 1) // CH
+    grads = [I.gen_grad(wl, 1, r, device=dev) for r in range(R)]
+    w, m, v = I.gen_state(wl, device=dev)
+    chunks = sample_chunks(c, k=126, seed=5)
+    g_before = [gather(gr, chunks, n) for gr in grads]
+    s_before = (gather(w, chunks, n), gather(m, chunks, n), gather(v, chunks, n))
+    ctx = rs.Repstep(n, device=dev)
+    hp = U.hp_for(1)
+    norm = torch.empty(1, dtype=torch.float32, device=dev)
+    root = torch.empty(1, dtype=torch.int64, device=dev)
+    ctx.reduce_paper(grads, dps)
+    ctx.clip(hp.clip, norm_out=norm)
+    ctx.adamw(w, m, v, hp)
+    ctx.root(1, root_out=root)
+    ctx.sync()
+    check_step_chain(ctx, g_before, s_before, w, m, v, 1, chunks, n, norm, root,
+                     reducer=lambda G: O.reduce_alg1(G, dps))

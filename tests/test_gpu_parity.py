@@ -109,6 +109,67 @@ def test_audit_mode_shards_and_standalone_hash():
     U.assert_same_f32(wb, wa.cpu().numpy(), "w")
 
 
+@pytest.mark.parametrize("R,dp_shard,dtype", [
+    (1, 1, torch.float32), (6, 2, torch.float32), (6, 3, torch.float32), (7, 1, torch.float32),
+    (12, 4, torch.float32), (9, 9, torch.float32), (40, 8, torch.float32), (24, 3, torch.bfloat16),
+    (8, 1, torch.float32),
+])
+def test_paper_exact_reduce_matches_oracle(R, dp_shard, dtype):
+    """OPEN-1B Algorithm 1 order: g bit-identical to the oracle's restatement, then the
+    rest of the step (norm, clip, AdamW, root) on that g."""
+    n = 2 * 4096 + 333
+    dev = torch.device("cuda", 0)
+    ctx = rs.Repstep(n, grad_dtype=dtype, device=dev)
+    w, m, v = I.gen_state(U.F32_WL, n=n, device=dev)
+    ow, om, ov = w.cpu().numpy(), m.cpu().numpy(), v.cpu().numpy()
+    norm = torch.empty(1, dtype=torch.float32, device=dev)
+    root = torch.empty(1, dtype=torch.int64, device=dev)
+    for t in (1, 2):
+        grads = U.gen_grads(n, R, t, dtype, scale=3000.0 if t == 2 else 1.0)
+        hp = U.hp_for(t)
+        ctx.reduce_paper(grads, dp_shard)
+        ctx.clip(hp.clip, norm_out=norm)
+        ctx.adamw(w, m, v, hp)
+        ctx.root(t, root_out=root)
+        ctx.sync()
+        g = O.reduce_alg1(U.oracle_grads(grads), dp_shard)
+        U.assert_same_f32(ctx.g_view(), g, f"g step {t}")
+        nv = O.norm(g)
+        bc1, bc2 = O.bias_corrections(U.HP["beta1"], U.HP["beta2"], t)
+        ow, om, ov = O.adamw(ow, om, ov, g, O.clip_scale(nv, U.HP["clip"]), U.HP["lr"],
+                             U.HP["beta1"], U.HP["beta2"], U.HP["eps"], U.HP["wd"], bc1, bc2)
+        assert np.float32(norm.item()) == nv
+        U.assert_same_f32(w, ow, f"w step {t}")
+        U.assert_same_f32(v, ov, f"v step {t}")
+        assert U.root_of(root) == O.state_hash(t, ow, om, ov)
+    if dp_shard == 1 and R & (R - 1) == 0:
+        # one shard, power-of-two replicas: the canonical tree exactly
+        b = rs.Repstep(n, grad_dtype=dtype, device=dev)
+        b.reduce(grads)
+        b.clip(1.0)
+        b.sync()
+        assert torch.equal(b.g_view().view(torch.int32), ctx.g_view().view(torch.int32))
+
+
+def test_paper_exact_reduce_in_ranges():
+    n, R, dps = 50_000, 12, 4
+    dev = torch.device("cuda", 0)
+    a, b = rs.Repstep(n, device=dev), rs.Repstep(n, device=dev)
+    grads = U.gen_grads(n, R, 3)
+    a.reduce_paper(grads, dps)
+    for lo, hi in [(0, 3), (3, 4100), (4100, 33_333), (33_333, n)]:
+        b.reduce_paper(grads, dps, begin=lo, count=hi - lo)
+    na, nb = (torch.empty(1, dtype=torch.float32, device=dev) for _ in range(2))
+    a.clip(1.0, norm_out=na)
+    b.clip(1.0, norm_out=nb)
+    a.sync(); b.sync()
+    assert torch.equal(a.g_view().view(torch.int32), b.g_view().view(torch.int32))
+    assert na.item() == nb.item()
+    with pytest.raises(rs.RepstepError) as ei:
+        a.reduce_paper(grads, 5)            # 5 does not divide 12
+    assert ei.value.code == 4
+
+
 def test_empty_parameter_vector():
     dev = torch.device("cuda", 0)
     ctx = rs.Repstep(0, device=dev)
