@@ -9,8 +9,10 @@
 //   1 - b1, 1 - b2, 1 - lr*wd, and the bias corrections 1 - b^t (t repeated products).
 #include <cmath>
 #include <cstdint>
+#include <cstdio>
 #include <cstring>
 #include <new>
+#include <string>
 #include <vector>
 
 #include "../../include/repstep.h"
@@ -594,6 +596,99 @@ int repstep_image_read(repstep_ctx *ctx, const void *src, uint64_t src_bytes, in
         if (e != cudaSuccess) return ctx->cuda_fail(e);
     }
     return REPSTEP_OK;
+}
+
+// ----------------------------------------------------------------------------------------
+// Checkpoint files: the image streamed between the device arrays and a file through one
+// reusable pinned host buffer ("grow_a_language_model_checkpoints": step_NNNNNN.bin).
+// ----------------------------------------------------------------------------------------
+namespace {
+
+constexpr uint64_t kIoChunk = 64ull << 20;   // bytes per staged transfer
+
+struct PinnedBuf {
+    void *p = nullptr;
+    ~PinnedBuf()
+    {
+        if (p) cudaFreeHost(p);
+    }
+};
+
+}  // namespace
+
+int repstep_checkpoint_save(repstep_ctx *ctx, const char *path, int32_t step, const float *d_w,
+                            const float *d_m, const float *d_v)
+{
+    if (!ctx || !path || !d_w || !d_m || !d_v) return REPSTEP_ERR_ARG;
+    const uint64_t n = ctx->n;
+    const std::string tmp = std::string(path) + ".tmp";
+    FILE *f = std::fopen(tmp.c_str(), "wb");
+    if (!f) return REPSTEP_ERR_ARG;
+    int rc = REPSTEP_OK;
+    const uint32_t header[2] = {uint32_t(step), uint32_t(n)};   // little-endian hosts
+    if (std::fwrite(header, 4, 2, f) != 2) rc = REPSTEP_ERR_ARG;
+    PinnedBuf buf;
+    if (rc == REPSTEP_OK && n > 0) {
+        cudaError_t e = cudaMallocHost(&buf.p, kIoChunk);
+        if (e != cudaSuccess) rc = ctx->cuda_fail(e);
+    }
+    const float *arrs[3] = {d_w, d_m, d_v};
+    for (int a = 0; a < 3 && rc == REPSTEP_OK; ++a) {
+        const unsigned char *src = reinterpret_cast<const unsigned char *>(arrs[a]);
+        for (uint64_t off = 0; off < 4 * n && rc == REPSTEP_OK; off += kIoChunk) {
+            const uint64_t len = 4 * n - off < kIoChunk ? 4 * n - off : kIoChunk;
+            cudaError_t e = cudaMemcpyAsync(buf.p, src + off, len, cudaMemcpyDeviceToHost,
+                                            ctx->stream);
+            if (e == cudaSuccess) e = cudaStreamSynchronize(ctx->stream);
+            if (e != cudaSuccess) rc = ctx->cuda_fail(e);
+            else if (std::fwrite(buf.p, 1, len, f) != len) rc = REPSTEP_ERR_ARG;
+        }
+    }
+    if (std::fclose(f) != 0 && rc == REPSTEP_OK) rc = REPSTEP_ERR_ARG;
+    if (rc == REPSTEP_OK && std::rename(tmp.c_str(), path) != 0) rc = REPSTEP_ERR_ARG;
+    if (rc != REPSTEP_OK) std::remove(tmp.c_str());
+    return rc;
+}
+
+int repstep_checkpoint_load(repstep_ctx *ctx, const char *path, int32_t *step_out, float *d_w,
+                            float *d_m, float *d_v)
+{
+    if (!ctx || !path || !d_w || !d_m || !d_v) return REPSTEP_ERR_ARG;
+    const uint64_t n = ctx->n;
+    FILE *f = std::fopen(path, "rb");
+    if (!f) return REPSTEP_ERR_ARG;
+    // guards first, before anything is copied: exact size, then the header's n
+    int rc = REPSTEP_OK;
+    if (std::fseek(f, 0, SEEK_END) != 0) rc = REPSTEP_ERR_FORMAT;
+    const long long size = rc == REPSTEP_OK ? std::ftell(f) : -1;
+    if (size < 0 || uint64_t(size) != repstep_image_bytes(n)) rc = REPSTEP_ERR_FORMAT;
+    uint32_t header[2] = {0, 0};
+    if (rc == REPSTEP_OK && (std::fseek(f, 0, SEEK_SET) != 0 || std::fread(header, 4, 2, f) != 2))
+        rc = REPSTEP_ERR_FORMAT;
+    if (rc == REPSTEP_OK && uint64_t(header[1]) != n) rc = REPSTEP_ERR_FORMAT;
+    PinnedBuf buf;
+    if (rc == REPSTEP_OK && n > 0) {
+        cudaError_t e = cudaMallocHost(&buf.p, kIoChunk);
+        if (e != cudaSuccess) rc = ctx->cuda_fail(e);
+    }
+    float *arrs[3] = {d_w, d_m, d_v};
+    for (int a = 0; a < 3 && rc == REPSTEP_OK; ++a) {
+        unsigned char *dst = reinterpret_cast<unsigned char *>(arrs[a]);
+        for (uint64_t off = 0; off < 4 * n && rc == REPSTEP_OK; off += kIoChunk) {
+            const uint64_t len = 4 * n - off < kIoChunk ? 4 * n - off : kIoChunk;
+            if (std::fread(buf.p, 1, len, f) != len) {
+                rc = REPSTEP_ERR_FORMAT;
+                break;
+            }
+            cudaError_t e = cudaMemcpyAsync(dst + off, buf.p, len, cudaMemcpyHostToDevice,
+                                            ctx->stream);
+            if (e == cudaSuccess) e = cudaStreamSynchronize(ctx->stream);
+            if (e != cudaSuccess) rc = ctx->cuda_fail(e);
+        }
+    }
+    std::fclose(f);
+    if (rc == REPSTEP_OK && step_out) *step_out = int32_t(header[0]);
+    return rc;
 }
 
 void repstep_bias_corrections(float beta1, float beta2, int32_t t, float *bc1, float *bc2)

@@ -67,7 +67,8 @@ EXPORTS = [
     "repstep_hash", "repstep_step", "repstep_image_bytes", "repstep_image_write",
     "repstep_image_read", "repstep_bias_corrections", "repstep_sync", "repstep_launch_count",
     "repstep_last_cuda_error", "repstep_strerror", "repstep_reduce_norm_noalloc",
-    "repstep_selftest_fixed_division", "repstep_reduce_paper",
+    "repstep_selftest_fixed_division", "repstep_reduce_paper", "repstep_checkpoint_save",
+    "repstep_checkpoint_load",
 ]
 NOALLOC_MAX_N = 1 << 30
 
@@ -112,6 +113,8 @@ def lib():
     L.repstep_strerror.restype = C.c_char_p
     L.repstep_selftest_fixed_division.argtypes = [u32, u32, vp, vp]
     L.repstep_reduce_paper.argtypes = [vp, C.POINTER(vp), u32, u32, u64, u64]
+    L.repstep_checkpoint_save.argtypes = [vp, C.c_char_p, i32, vp, vp, vp]
+    L.repstep_checkpoint_load.argtypes = [vp, C.c_char_p, C.POINTER(i32), vp, vp, vp]
     L.repstep_reduce_norm_noalloc.argtypes = [C.POINTER(vp), u32, i32, u64, C.c_float, vp, vp,
                                               vp, vp]
     _lib = L
@@ -137,6 +140,14 @@ def hparams(*, lr, beta1, beta2, eps, weight_decay, clip, t) -> HParams:
     """AdamW hyperparameters for step t (bias corrections from the library's host recipe)."""
     bc1, bc2 = bias_corrections(beta1, beta2, t)
     return HParams(lr, beta1, beta2, eps, weight_decay, clip, bc1, bc2)
+
+
+def checkpoint_name(step: int) -> str:
+    """File name of the checkpoint written after `step` ("grow_a_language_model_checkpoints":
+    step_NNNNNN.bin, six digits, zero padded)."""
+    if step < 0:
+        raise ValueError("step must be >= 0")
+    return f"step_{step:06d}.bin"
 
 
 def image_bytes(n: int) -> int:
@@ -350,6 +361,23 @@ class Repstep:
         self._bind()
         _check(lib().repstep_image_read(self._ctx, _ptr(src), src.numel(), 0 if src.is_cuda else 1,
                                         C.byref(step), _ptr(w), _ptr(m), _ptr(v)), "image_read")
+        return int(step.value)
+
+    def save_checkpoint(self, path: str, step: int, w, m, v):
+        """Write the 8 + 12n-byte image of (step, w, m, v) to `path` (atomic rename)."""
+        self._state(w, m, v)
+        self._bind()
+        _check(lib().repstep_checkpoint_save(self._ctx, os.fsencode(path), int(step), _ptr(w),
+                                             _ptr(m), _ptr(v)), "checkpoint_save")
+
+    def load_checkpoint(self, path: str, w, m, v) -> int:
+        """Load an image file into (w, m, v); returns its step.  Size and header checked
+        before anything is copied."""
+        self._state(w, m, v)
+        step = C.c_int32()
+        self._bind()
+        _check(lib().repstep_checkpoint_load(self._ctx, os.fsencode(path), C.byref(step), _ptr(w),
+                                             _ptr(m), _ptr(v)), "checkpoint_load")
         return int(step.value)
 
     def sync(self) -> int:

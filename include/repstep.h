@@ -212,6 +212,20 @@ int repstep_image_write(repstep_ctx *ctx, int32_t step, const float *d_w, const 
 int repstep_image_read(repstep_ctx *ctx, const void *src, uint64_t src_bytes, int src_is_host,
                        int32_t *step_out, float *d_w, float *d_m, float *d_v);
 
+/* Checkpoint files ("grow_a_language_model_checkpoints", step_NNNNNN.bin): the image above,
+ * streamed between the device arrays w, m, v (the context's n) and `path` through one
+ * pinned host buffer of 64 MiB (host memory only; no device allocation).  Synchronous on
+ * the context's stream.  Save writes `path`.tmp and renames it over `path` only when every
+ * byte was written, so a crash never leaves a truncated file under the final name.  Load
+ * rejects, before copying anything, a file whose size is not 8 + 12n or whose header n
+ * differs (REPSTEP_ERR_FORMAT) -- a check that cannot fail is not a check, so the tests
+ * feed it truncated, oversized and mismatched files.  REPSTEP_ERR_ARG if the file cannot
+ * be opened or written. */
+int repstep_checkpoint_save(repstep_ctx *ctx, const char *path, int32_t step, const float *d_w,
+                            const float *d_m, const float *d_v);
+int repstep_checkpoint_load(repstep_ctx *ctx, const char *path, int32_t *step_out, float *d_w,
+                            float *d_m, float *d_v);
+
 /* Bias corrections for step t >= 1: p_j = beta_j^t as t repeated fp32 products,
  * bc_j = 1 - p_j (the reading taken for AdamW's bias correction; computed on the host). */
 void repstep_bias_corrections(float beta1, float beta2, int32_t t, float *bc1, float *bc2);
