@@ -334,6 +334,39 @@ void oracle_adamw(float *w, float *m, float *v, const float *g, uint64_t n, floa
 }
 
 /* ------------------------------------------------------------------------------ */
+/* bf16 parameters ([OPEN-1B] §3.2, paragraph on optimizer-state precision: the      */
+/* parameters are held in BF16, the fused optimizer step widens parameter and        */
+/* gradient to FP32, does the whole moment and parameter update in FP32, and rounds  */
+/* the result back to BF16 once per step; m and v stay FP32).                         */
+/* Rounding fp32 -> bf16 to nearest, ties to even, on the bit pattern: keep the top   */
+/* 16 bits after adding half of the dropped range plus the kept lowest bit.  NaN      */
+/* stays a NaN (its payload is outside the contract).                                */
+/* ------------------------------------------------------------------------------ */
+uint16_t oracle_f32_to_bf16(float x)
+{
+    uint32_t u;
+    memcpy(&u, &x, 4);
+    if ((u & 0x7F800000u) == 0x7F800000u && (u & 0x007FFFFFu) != 0)
+        return (uint16_t)((u >> 16) | 0x0040u);          /* quiet NaN */
+    uint32_t lsb = (u >> 16) & 1u;
+    u += 0x7FFFu + lsb;
+    return (uint16_t)(u >> 16);
+}
+
+/* AdamW with bf16 parameters: w16 in place, m and v fp32; the update of oracle_adamw  */
+/* on the widened parameter, rounded once back to bf16.                               */
+void oracle_adamw_bf16w(uint16_t *w16, float *m, float *v, const float *g, uint64_t n,
+                        float scale, float lr, float beta1, float beta2, float eps, float wd,
+                        float bc1, float bc2)
+{
+    for (uint64_t i = 0; i < n; ++i) {
+        float w32 = bf16_to_f32(w16[i]);
+        oracle_adamw(&w32, m + i, v + i, g + i, 1, scale, lr, beta1, beta2, eps, wd, bc1, bc2);
+        w16[i] = oracle_f32_to_bf16(w32);
+    }
+}
+
+/* ------------------------------------------------------------------------------ */
 /* PF61 leaf digest over a sequence of 32-bit words:                                 */
 /*   F(x_0..x_{W-1}) = (W + sum_{i<W} x_i * K^(i+1)) mod p,  p = 2^61 - 1,          */
 /*   K = (isqrt(5 * 2^122) - 2^61) >> 1 (floor of 2^61 (sqrt5 - 1)/2).               */

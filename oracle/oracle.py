@@ -81,6 +81,12 @@ def lib():
         L.oracle_step_mode.restype = C.c_int
         L.oracle_reduce_alg1.argtypes = [fp, C.c_int, C.c_uint32, C.c_uint32, C.c_uint64, fp]
         L.oracle_reduce_alg1.restype = C.c_int
+        L.oracle_f32_to_bf16.argtypes = [C.c_float]
+        L.oracle_f32_to_bf16.restype = C.c_uint16
+        L.oracle_adamw_bf16w.argtypes = [fp, fp, fp, fp, C.c_uint64, C.c_float, C.c_float,
+                                         C.c_float, C.c_float, C.c_float, C.c_float, C.c_float,
+                                         C.c_float]
+        L.oracle_adamw_bf16w.restype = None
         _lib = L
     return _lib
 
@@ -193,6 +199,25 @@ def adamw(w, m, v, g, scale, lr, beta1, beta2, eps, wd, bc1, bc2):
     lib().oracle_adamw(_p(w), _p(m), _p(v), _p(g), n, f(scale), f(lr), f(beta1), f(beta2),
                        f(eps), f(wd), f(bc1), f(bc2))
     return w, m, v
+
+
+def f32_to_bf16(x) -> int:
+    return int(lib().oracle_f32_to_bf16(float(np.float32(x))))
+
+
+def adamw_bf16w(w16, m, v, g, scale, lr, beta1, beta2, eps, wd, bc1, bc2):
+    """bf16 parameters (uint16 bit patterns): returns (w16', m', v') on copies."""
+    w16 = np.ascontiguousarray(w16, dtype=np.uint16).copy()
+    m = _f32(m).copy(); v = _f32(v).copy(); g = _f32(g)
+    f = lambda x: float(np.float32(x))  # noqa: E731
+    lib().oracle_adamw_bf16w(_p(w16), _p(m), _p(v), _p(g), w16.size, f(scale), f(lr), f(beta1),
+                             f(beta2), f(eps), f(wd), f(bc1), f(bc2))
+    return w16, m, v
+
+
+def widen_bf16(w16) -> np.ndarray:
+    """bf16 bit patterns -> the fp32 values they denote (exact)."""
+    return (np.ascontiguousarray(w16, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
 
 
 def pf61_constant() -> int:

@@ -610,3 +610,38 @@ def test_audit_and_pf61_modes_differ_but_share_the_tree():
     w, m, v = (rng.standard_normal((3, 9000))).astype(np.float32)
     assert O.state_hash(1, w, m, v, 0) != O.state_hash(1, w, m, v, 1)
     assert O.state_hash(1, w, m, v, 0) == O.merkle_root(O.leaves(1, w, m, v, 0))
+
+
+# ----------------------------------------------------------------------------------
+# bf16 parameters: the rounding to bf16 against torch's conversion, the update against
+# the fp32 oracle on the widened value
+# ----------------------------------------------------------------------------------
+def test_f32_to_bf16_matches_torch_rne():
+    rng = np.random.default_rng(40)
+    x = np.concatenate([rand_f32(rng, 20000, -149, 127),
+                        np.array([0.0, -0.0, np.inf, -np.inf, 3.4028235e38, 1.0039062,
+                                  1.0117188, 2.0 ** -133, -(2.0 ** -149)], np.float32)])
+    # ties: exactly half way between two bf16 neighbours
+    ties = (rng.integers(0, 2 ** 16, 2000, dtype=np.uint64).astype(np.uint32) << 16 | 0x8000).view(np.float32)
+    x = np.concatenate([x, ties[np.isfinite(ties)]]).astype(np.float32)
+    want = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got = np.array([O.f32_to_bf16(v) for v in x], np.uint16)
+    assert np.array_equal(got, want)
+    assert (O.f32_to_bf16(np.float32(np.nan)) & 0x7FC0) == 0x7FC0
+
+
+def test_adamw_bf16w_is_fp32_update_rounded_once():
+    rng = np.random.default_rng(41)
+    n = 5000
+    w16 = torch.from_numpy((rng.standard_normal(n) * 0.02).astype(np.float32)).to(torch.bfloat16)
+    w16 = w16.view(torch.int16).numpy().view(np.uint16)
+    m = (rng.standard_normal(n) * 1e-4).astype(np.float32)
+    v = np.abs(rng.standard_normal(n) * 1e-7).astype(np.float32)
+    g = (rng.standard_normal(n) * 1e-3).astype(np.float32)
+    bc1, bc2 = O.bias_corrections(B1, B2, 3)
+    w1, m1, v1 = O.adamw_bf16w(w16, m, v, g, 1.0, LR, B1, B2, EPS, WD, bc1, bc2)
+    wf, mf, vf = O.adamw(O.widen_bf16(w16), m, v, g, 1.0, LR, B1, B2, EPS, WD, bc1, bc2)
+    assert np.array_equal(m1.view(np.uint32), mf.view(np.uint32))
+    assert np.array_equal(v1.view(np.uint32), vf.view(np.uint32))
+    want = torch.from_numpy(wf).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(w1, want)
