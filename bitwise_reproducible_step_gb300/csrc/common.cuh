@@ -36,7 +36,7 @@ struct Scalars {
     float norm;        // pre-clip global norm of the last clip
     float scale;       // clip scale of the last clip
     uint32_t flags;    // REPSTEP_FLAG_* bits
-    uint32_t pad;
+    uint32_t aux;      // scratch flag of host-driven checks (image narrowing)
     uint64_t root;     // last Merkle root
 };
 

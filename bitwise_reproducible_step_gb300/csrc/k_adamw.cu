@@ -11,6 +11,10 @@
 // MODE 1 (leaves): the PF61 digests of the chunks of the given w, m, v, nothing written.
 // MODE 2 (AdamW only): MODE 0 without the digests (the audit hash mode digests the new
 // state with BLAKE2b afterwards).
+// PT 1 (bf16 parameters): w is held in bf16 ("OPEN-1B", §3.2 paragraph on optimizer-state
+// precision): it is widened exactly, updated in fp32, and rounded back to bf16 once, to
+// nearest even; m and v stay fp32.  The hash digests w as its exactly widened fp32 words,
+// so the image and its leaves keep the fp32 layout.
 //
 // PF61 of a chunk of W 32-bit words x_i is (W + sum x_i K^(i+1)) mod (2^61 - 1).  Each
 // power P = K^(i+1) < 2^61 is split into three 21-bit limbs P = l0 + l1 2^21 + l2 2^42, and
@@ -28,6 +32,8 @@
 // with 16-byte stores, and fold the words into the leaf sums.  Tiles lying wholly inside
 // the range take a fast path without per-element range checks.  Every fp32 operation is
 // an explicitly rounded intrinsic.
+#include <cuda_bf16.h>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -154,16 +160,54 @@ __device__ __forceinline__ uint64_t pf_shl(uint64_t x, int e)
     return e == 0 ? x : (((x << e) & kP61) | (x >> (61 - e)));
 }
 
+// Bytes per element and byte offset within a stage of stream s; ws is the index of the
+// stream holding w, pt whether w is bf16.
+__host__ __device__ constexpr uint32_t stream_es(int s, int ws, int pt)
+{
+    return (s == ws && pt) ? 2u : 4u;
+}
+
+__host__ __device__ constexpr uint32_t stream_off(int s, int ws, int pt, uint32_t te)
+{
+    uint32_t o = 0;
+    for (int t = 0; t < s; ++t) o += stream_es(t, ws, pt) * te;
+    return o;
+}
+
+__device__ __forceinline__ float4 widen4(uint2 u)
+{
+    return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u),
+                       __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xFFFF0000u));
+}
+
+// A 4-element group of stream s from the staged tile.
+template <uint32_t ES>
+__device__ __forceinline__ float4 stage_group(const unsigned char *p)
+{
+    if constexpr (ES == 4) return *reinterpret_cast<const float4 *>(p);
+    else return widen4(*reinterpret_cast<const uint2 *>(p));
+}
+
+// One element of a stream from global memory (fp32, or bf16 widened exactly).
+template <uint32_t ES>
+__device__ __forceinline__ float load_one(const void *p, uint64_t e)
+{
+    if constexpr (ES == 4) return __ldg(static_cast<const float *>(p) + e);
+    else return __uint_as_float(uint32_t(__ldg(static_cast<const unsigned short *>(p) + e)) << 16);
+}
+
 // Block layout: warps 0..NT/32-1 compute, then one producer warp (TMA), then one leaf warp
 // that finishes the chunk digests from the compute warps' per-warp partial sums, so the
 // compute warps never wait for one another between chunks.
-template <int NT, int MODE>
+template <int NT, int MODE, int PT>
 __global__ void __launch_bounds__(NT + 64, Shape<NT>::min_blocks)
 k_adamw(const __grid_constant__ AdamwArgs A)
 {
     constexpr bool UPDATE = MODE != 1;           // AdamW runs (modes 0 and 2)
     constexpr bool LEAVES = MODE != 2;           // PF61 digests (modes 0 and 1)
     constexpr int NS = UPDATE ? 4 : 3;           // streamed arrays
+    constexpr int WS = UPDATE ? 1 : 0;           // index of the w stream
+    constexpr uint32_t VEC = PT ? 8u : 4u;       // elements per 16 bytes of the narrowest stream
     constexpr uint32_t TE = uint32_t(kEPT) * NT;
     constexpr int TPC = int(kChunk / TE);
     constexpr int W = NT / 32;
@@ -199,7 +243,7 @@ k_adamw(const __grid_constant__ AdamwArgs A)
     __syncthreads();
 
     const uint32_t flag_bit = UPDATE ? kFlagTimeoutAdamw : kFlagTimeoutLeaves;
-    const float *src[4];
+    const void *src[4];
     if (UPDATE) {
         src[0] = A.g; src[1] = A.w; src[2] = A.m; src[3] = A.v;
     } else {
@@ -260,21 +304,28 @@ k_adamw(const __grid_constant__ AdamwArgs A)
         for (uint64_t k = A.chunk_lo + blockIdx.x; ok && k < A.chunk_hi; k += gridDim.x) {
             for (int j = 0; j < TPC; ++j) {
                 const TileRange tr =
-                    tile_range(k * kChunk + uint64_t(j) * TE, TE, A.begin, A.end, 4);
-                const uint32_t bytes = uint32_t(tr.b16 - tr.a16) * 4u;
-                const uint32_t soff = uint32_t(tr.a16 - tr.base) * 4u;
+                    tile_range(k * kChunk + uint64_t(j) * TE, TE, A.begin, A.end, VEC);
+                const uint32_t elems = uint32_t(tr.b16 - tr.a16);
+                const uint32_t skip = uint32_t(tr.a16 - tr.base);
                 const uint32_t slot = it % S, round = it / S;
                 if (!mbar_wait_bounded(smem_u32(&empty[slot]), (round & 1u) ^ 1u, abort_flag)) {
                     ok = false;
                     break;
                 }
                 const uint32_t fb = smem_u32(&full[slot]);
-                mbar_arrive_expect_tx(fb, bytes * NS);
-                if (bytes) {
-                    const uint32_t dst = smem_u32(ring + slot * A.stage_stride) + soff;
+                uint32_t total = 0;
 #pragma unroll
-                    for (int s = 0; s < NS; ++s)
-                        bulk_g2s(dst + s * TE * 4u, src[s] + tr.a16, bytes, fb, pol);
+                for (int s = 0; s < NS; ++s) total += elems * stream_es(s, WS, PT);
+                mbar_arrive_expect_tx(fb, total);
+                if (elems) {
+                    const uint32_t dst = smem_u32(ring + slot * A.stage_stride);
+#pragma unroll
+                    for (int s = 0; s < NS; ++s) {
+                        const uint32_t es = stream_es(s, WS, PT);
+                        bulk_g2s(dst + stream_off(s, WS, PT, TE) + skip * es,
+                                 static_cast<const unsigned char *>(src[s]) + tr.a16 * es,
+                                 elems * es, fb, pol);
+                    }
                 }
                 ++it;
             }
@@ -312,7 +363,7 @@ k_adamw(const __grid_constant__ AdamwArgs A)
         Acc3 acc[3] = {{0, 0, 0}, {0, 0, 0}, {0, 0, 0}};
 #pragma unroll
         for (int j = 0; j < TPC; ++j) {
-            const TileRange tr = tile_range(k * kChunk + uint64_t(j) * TE, TE, A.begin, A.end, 4);
+            const TileRange tr = tile_range(k * kChunk + uint64_t(j) * TE, TE, A.begin, A.end, VEC);
             const bool full_tile = tr.a == tr.base && tr.b == tr.base + TE;
             const uint32_t slot = it % S, round = it / S;
             if (!aborted && !mbar_wait_bounded(smem_u32(&full[slot]), round & 1u, abort_flag)) {
@@ -329,8 +380,11 @@ k_adamw(const __grid_constant__ AdamwArgs A)
 #pragma unroll
                 for (int q = 0; q < 2; ++q)
 #pragma unroll
-                    for (int s = 0; s < NS; ++s)
-                        x[q][s] = *reinterpret_cast<const float4 *>(sb + s * TE * 4u + goff[q] * 4u);
+                    for (int s = 0; s < NS; ++s) {
+                        x[q][s] = stream_es(s, WS, PT) == 4u
+                                      ? stage_group<4>(sb + stream_off(s, WS, PT, TE) + goff[q] * 4u)
+                                      : stage_group<2>(sb + stream_off(s, WS, PT, TE) + goff[q] * 2u);
+                    }
             } else {
 #pragma unroll
                 for (int q = 0; q < 2; ++q) {
@@ -343,14 +397,18 @@ k_adamw(const __grid_constant__ AdamwArgs A)
                     inmask[q] = msk;
 #pragma unroll
                     for (int s = 0; s < NS; ++s) {
+                        const bool narrow = stream_es(s, WS, PT) == 2u;
                         if (in_bulk) {
-                            x[q][s] = *reinterpret_cast<const float4 *>(sb + s * TE * 4u +
-                                                                        goff[q] * 4u);
+                            x[q][s] = narrow
+                                ? stage_group<2>(sb + stream_off(s, WS, PT, TE) + goff[q] * 2u)
+                                : stage_group<4>(sb + stream_off(s, WS, PT, TE) + goff[q] * 4u);
                         } else {
                             float r[4];
 #pragma unroll
                             for (int i = 0; i < 4; ++i)
-                                r[i] = (msk >> i) & 1u ? __ldg(src[s] + e0 + i) : 0.0f;
+                                r[i] = (msk >> i) & 1u ? (narrow ? load_one<2>(src[s], e0 + i)
+                                                                 : load_one<4>(src[s], e0 + i))
+                                                       : 0.0f;
                             x[q][s] = make_float4(r[0], r[1], r[2], r[3]);
                         }
                     }
@@ -372,6 +430,13 @@ k_adamw(const __grid_constant__ AdamwArgs A)
                     v8[4 * q] = x[q][3].x; v8[4 * q + 1] = x[q][3].y; v8[4 * q + 2] = x[q][3].z; v8[4 * q + 3] = x[q][3].w;
                 }
                 adamw8(g8, w8, m8, v8, scale, A);
+                if (PT) {
+                    // one rounding of the fp32 result back to bf16; the hash sees the
+                    // rounded parameter, widened exactly
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        w8[e] = __bfloat162float(__float2bfloat16_rn(w8[e]));
+                }
 #pragma unroll
                 for (int q = 0; q < 2; ++q) {
                     hw[q] = make_float4(w8[4 * q], w8[4 * q + 1], w8[4 * q + 2], w8[4 * q + 3]);
@@ -388,8 +453,18 @@ k_adamw(const __grid_constant__ AdamwArgs A)
 #pragma unroll
                 for (int q = 0; q < 2; ++q) {
                     const uint64_t e0 = tr.base + goff[q];
+                    float *W32 = static_cast<float *>(A.w);
+                    unsigned short *W16 = static_cast<unsigned short *>(A.w);
                     if (inmask[q] == 0xFu) {
-                        *reinterpret_cast<float4 *>(A.w + e0) = hw[q];
+                        if (PT) {
+                            // the widened bf16 values' top halves are the bf16 bits
+                            const uint2 u = make_uint2(
+                                (__float_as_uint(hw[q].x) >> 16) | (__float_as_uint(hw[q].y) & 0xFFFF0000u),
+                                (__float_as_uint(hw[q].z) >> 16) | (__float_as_uint(hw[q].w) & 0xFFFF0000u));
+                            *reinterpret_cast<uint2 *>(W16 + e0) = u;
+                        } else {
+                            *reinterpret_cast<float4 *>(W32 + e0) = hw[q];
+                        }
                         *reinterpret_cast<float4 *>(A.m + e0) = hm[q];
                         *reinterpret_cast<float4 *>(A.v + e0) = hv[q];
                     } else {
@@ -399,7 +474,8 @@ k_adamw(const __grid_constant__ AdamwArgs A)
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
                             if ((inmask[q] >> i) & 1u) {
-                                A.w[e0 + i] = aw[i];
+                                if (PT) W16[e0 + i] = (unsigned short)(__float_as_uint(aw[i]) >> 16);
+                                else W32[e0 + i] = aw[i];
                                 A.m[e0 + i] = am[i];
                                 A.v[e0 + i] = av[i];
                             }
@@ -487,12 +563,18 @@ __global__ void __launch_bounds__(256) k_selftest_div(uint32_t b_begin, uint32_t
 
 using KernelFn = void (*)(AdamwArgs);
 
-KernelFn pick(int nt, int mode)
+template <int NT, int PT>
+KernelFn pick_nt(int mode)
+{
+    return mode == 1 ? k_adamw<NT, 1, PT> : (mode == 2 ? k_adamw<NT, 2, PT> : k_adamw<NT, 0, PT>);
+}
+
+KernelFn pick(int nt, int mode, int pt)
 {
     switch (nt) {
-    case 128: return mode == 1 ? k_adamw<128, 1> : (mode == 2 ? k_adamw<128, 2> : k_adamw<128, 0>);
-    case 256: return mode == 1 ? k_adamw<256, 1> : (mode == 2 ? k_adamw<256, 2> : k_adamw<256, 0>);
-    case 512: return mode == 1 ? k_adamw<512, 1> : (mode == 2 ? k_adamw<512, 2> : k_adamw<512, 0>);
+    case 128: return pt ? pick_nt<128, 1>(mode) : pick_nt<128, 0>(mode);
+    case 256: return pt ? pick_nt<256, 1>(mode) : pick_nt<256, 0>(mode);
+    case 512: return pt ? pick_nt<512, 1>(mode) : pick_nt<512, 0>(mode);
     default: return nullptr;
     }
 }
@@ -509,10 +591,11 @@ uint32_t ring_bytes(int nt)
 
 }  // namespace
 
-size_t adamw_smem_bytes(int nt, int mode, AdamwArgs &args)
+size_t adamw_smem_bytes(int nt, int mode, int pt, AdamwArgs &args)
 {
     const uint32_t ns = mode == 1 ? 3u : 4u;
-    const uint32_t stride = ns * uint32_t(kEPT) * uint32_t(nt) * 4u;
+    const uint32_t per_elem = 4u * ns - (pt ? 2u : 0u);     // w is 2 bytes when bf16
+    const uint32_t stride = per_elem * uint32_t(kEPT) * uint32_t(nt);
     uint32_t stages = ring_bytes(nt) / stride;
     if (stages > kMaxStages) stages = kMaxStages;
     if (stages < 2) stages = 2;
@@ -521,17 +604,17 @@ size_t adamw_smem_bytes(int nt, int mode, AdamwArgs &args)
     return size_t(ring_off(nt)) + size_t(stages) * stride;
 }
 
-cudaError_t adamw_prepare(int nt, int mode, size_t smem)
+cudaError_t adamw_prepare(int nt, int mode, int pt, size_t smem)
 {
-    KernelFn f = pick(nt, mode);
+    KernelFn f = pick(nt, mode, pt);
     if (!f) return cudaErrorInvalidValue;
     return cudaFuncSetAttribute(reinterpret_cast<const void *>(f),
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
 }
 
-cudaError_t adamw_occupancy(int nt, int mode, size_t smem, int *blocks_per_sm)
+cudaError_t adamw_occupancy(int nt, int mode, int pt, size_t smem, int *blocks_per_sm)
 {
-    KernelFn f = pick(nt, mode);
+    KernelFn f = pick(nt, mode, pt);
     if (!f) return cudaErrorInvalidValue;
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
         blocks_per_sm, reinterpret_cast<const void *>(f), nt + 64, smem);
@@ -544,10 +627,10 @@ cudaError_t launch_selftest_div(uint32_t b_begin, uint32_t b_count, unsigned lon
     return cudaGetLastError();
 }
 
-cudaError_t launch_adamw(int nt, int mode, const AdamwArgs &args, int grid, size_t smem,
+cudaError_t launch_adamw(int nt, int mode, int pt, const AdamwArgs &args, int grid, size_t smem,
                          cudaStream_t st)
 {
-    KernelFn f = pick(nt, mode);
+    KernelFn f = pick(nt, mode, pt);
     if (!f) return cudaErrorInvalidValue;
     void *params[] = {const_cast<AdamwArgs *>(&args)};
     return cudaLaunchKernel(reinterpret_cast<const void *>(f), dim3(grid), dim3(nt + 64),

@@ -52,14 +52,17 @@ __global__ void __launch_bounds__(256) k_chunk_fix(const float *g, uint64_t n, f
 }
 
 // Leaf digests of whole chunks of w, m, v, for chunks a range boundary cut during AdamW.
-__global__ void __launch_bounds__(256) k_leaf_fix(const float *w, const float *m, const float *v,
-                                                  uint64_t n, uint64_t c, uint64_t *leaves,
-                                                  const uint64_t *powers, const ChunkList L)
+// A bf16 w is digested as its exactly widened fp32 words.
+__global__ void __launch_bounds__(256) k_leaf_fix(const void *w, int w_bf16, const float *m,
+                                                  const float *v, uint64_t n, uint64_t c,
+                                                  uint64_t *leaves, const uint64_t *powers,
+                                                  const ChunkList L)
 {
     __shared__ uint64_t pb[3][256];
     const uint64_t k = L.idx[blockIdx.x];
     const int tid = threadIdx.x;
-    const float *arr[3] = {w, m, v};
+    const float *arr[3] = {static_cast<const float *>(w), m, v};
+    const unsigned short *w16 = static_cast<const unsigned short *>(w);
     uint32_t acc[3][4];
 #pragma unroll
     for (int s = 0; s < 3; ++s)
@@ -70,8 +73,10 @@ __global__ void __launch_bounds__(256) k_leaf_fix(const float *w, const float *m
         if (e >= n) break;
         const uint64_t pk = powers[p];
         const uint32_t p0 = uint32_t(pk), p1 = uint32_t(pk >> 32);
+        const uint32_t w0 = w_bf16 ? uint32_t(w16[e]) << 16 : __float_as_uint(arr[0][e]);
+        pf_mac(acc[0], w0, p0, p1);
 #pragma unroll
-        for (int s = 0; s < 3; ++s) pf_mac(acc[s], __float_as_uint(arr[s][e]), p0, p1);
+        for (int s = 1; s < 3; ++s) pf_mac(acc[s], __float_as_uint(arr[s][e]), p0, p1);
     }
 #pragma unroll
     for (int s = 0; s < 3; ++s) pb[s][tid] = pf_fold128(acc[s]);
@@ -201,14 +206,14 @@ cudaError_t launch_chunk_fix(const float *g, uint64_t n, float *chunk_sq, const 
     return cudaGetLastError();
 }
 
-cudaError_t launch_leaf_fix(const float *w, const float *m, const float *v, uint64_t n,
+cudaError_t launch_leaf_fix(const void *w, int w_bf16, const float *m, const float *v, uint64_t n,
                             uint64_t c, uint64_t *leaves, const uint64_t *powers,
                             const uint64_t *chunks, int count, cudaStream_t st)
 {
     ChunkList L{};
     for (int i = 0; i < count; ++i) L.idx[i] = chunks[i];
     L.count = count;
-    k_leaf_fix<<<count, 256, 0, st>>>(w, m, v, n, c, leaves, powers, L);
+    k_leaf_fix<<<count, 256, 0, st>>>(w, w_bf16, m, v, n, c, leaves, powers, L);
     return cudaGetLastError();
 }
 
@@ -241,6 +246,56 @@ cudaError_t launch_merkle(const uint64_t *in, uint64_t count, uint64_t *out, int
 cudaError_t launch_write_header(void *dst, int32_t step, uint32_t n32, cudaStream_t st)
 {
     k_write_header<<<1, 1, 0, st>>>(dst, step, n32);
+    return cudaGetLastError();
+}
+
+namespace {
+
+// bf16 -> fp32 is exact: the bf16 bits are the top half of the fp32 word.
+__global__ void __launch_bounds__(256) k_widen_bf16(float *dst, const unsigned short *src,
+                                                    uint64_t n)
+{
+    const uint64_t stride = uint64_t(gridDim.x) * blockDim.x;
+    for (uint64_t e = uint64_t(blockIdx.x) * blockDim.x + threadIdx.x; e < n; e += stride)
+        dst[e] = __uint_as_float(uint32_t(src[e]) << 16);
+}
+
+// fp32 -> bf16 by dropping the low half, valid only when that half is zero (the value is a
+// bf16 exactly).  With dst null it only checks; any other word sets *bad.
+__global__ void __launch_bounds__(256) k_narrow_bf16(unsigned short *dst, const float *src,
+                                                     uint64_t n, uint32_t *bad)
+{
+    const uint64_t stride = uint64_t(gridDim.x) * blockDim.x;
+    uint32_t mine = 0;
+    for (uint64_t e = uint64_t(blockIdx.x) * blockDim.x + threadIdx.x; e < n; e += stride) {
+        const uint32_t u = __float_as_uint(src[e]);
+        mine |= u & 0xFFFFu;
+        if (dst) dst[e] = (unsigned short)(u >> 16);
+    }
+    if (mine && bad) atomicOr(bad, 1u);
+}
+
+unsigned elementwise_blocks(uint64_t n)
+{
+    uint64_t b = (n + 255) / 256;
+    if (b > 152u * 16u) b = 152u * 16u;
+    return unsigned(b > 0 ? b : 1);
+}
+
+}  // namespace
+
+cudaError_t launch_widen_bf16(float *dst, const unsigned short *src, uint64_t n, cudaStream_t st)
+{
+    if (n == 0) return cudaSuccess;
+    k_widen_bf16<<<elementwise_blocks(n), 256, 0, st>>>(dst, src, n);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_narrow_bf16(unsigned short *dst, const float *src, uint64_t n, uint32_t *bad,
+                               cudaStream_t st)
+{
+    if (n == 0) return cudaSuccess;
+    k_narrow_bf16<<<elementwise_blocks(n), 256, 0, st>>>(dst, src, n, bad);
     return cudaGetLastError();
 }
 

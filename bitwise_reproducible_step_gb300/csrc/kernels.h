@@ -44,7 +44,8 @@ cudaError_t launch_reduce(const ReduceShape &s, const ReduceArgs &args, int grid
 // AdamW + leaf digests, or leaves only (k_adamw.cu).
 struct AdamwArgs {
     const float *g;           // MODE adamw: workspace g
-    float *w, *m, *v;         // state (updated in place in MODE adamw)
+    void *w;                  // parameters: fp32, or bf16 when the kernel's PT is 1
+    float *m, *v;             // Adam moments (fp32); updated in place in the AdamW modes
     uint64_t *leaves;         // workspace u64[1 + 3c]
     const uint64_t *powers;   // workspace K^1..K^4096 mod p
     Scalars *sc;              // device scalars (scale, flags)
@@ -56,10 +57,11 @@ struct AdamwArgs {
     int fastdiv;              // both bias corrections in [2^-40, 2]
 };
 
-size_t adamw_smem_bytes(int nt, int mode, AdamwArgs &args);
-cudaError_t adamw_prepare(int nt, int mode, size_t smem);
-cudaError_t adamw_occupancy(int nt, int mode, size_t smem, int *blocks_per_sm);
-cudaError_t launch_adamw(int nt, int mode, const AdamwArgs &args, int grid, size_t smem,
+// mode 0 AdamW + PF61 leaves, 1 leaves only, 2 AdamW only; pt 1 = bf16 parameters
+size_t adamw_smem_bytes(int nt, int mode, int pt, AdamwArgs &args);
+cudaError_t adamw_prepare(int nt, int mode, int pt, size_t smem);
+cudaError_t adamw_occupancy(int nt, int mode, int pt, size_t smem, int *blocks_per_sm);
+cudaError_t launch_adamw(int nt, int mode, int pt, const AdamwArgs &args, int grid, size_t smem,
                          cudaStream_t st);
 cudaError_t launch_selftest_div(uint32_t b_begin, uint32_t b_count, unsigned long long *mismatches,
                                cudaStream_t st);
@@ -68,7 +70,7 @@ cudaError_t launch_selftest_div(uint32_t b_begin, uint32_t b_count, unsigned lon
 cudaError_t launch_init_powers(uint64_t *powers, cudaStream_t st);
 cudaError_t launch_chunk_fix(const float *g, uint64_t n, float *chunk_sq, const uint64_t *chunks,
                              int count, cudaStream_t st);
-cudaError_t launch_leaf_fix(const float *w, const float *m, const float *v, uint64_t n,
+cudaError_t launch_leaf_fix(const void *w, int w_bf16, const float *m, const float *v, uint64_t n,
                             uint64_t c, uint64_t *leaves, const uint64_t *powers,
                             const uint64_t *chunks, int count, cudaStream_t st);
 cudaError_t launch_norm(const float *in, uint64_t count, float *out, Scalars *sc, int final_pass,
@@ -79,9 +81,14 @@ cudaError_t launch_merkle(const uint64_t *in, uint64_t count, uint64_t *out, int
                           uint64_t *leaves_rw, uint32_t step, uint32_t n32, const uint64_t *powers,
                           Scalars *sc, uint64_t *root_out, int blocks, cudaStream_t st);
 cudaError_t launch_write_header(void *dst, int32_t step, uint32_t n32, cudaStream_t st);
+// bf16 -> fp32 (exact) into an image's w region.  fp32 -> bf16 by dropping the low half
+// (dst nullable: check only); a word whose low half is not zero sets *bad (nullable) to 1.
+cudaError_t launch_widen_bf16(float *dst, const unsigned short *src, uint64_t n, cudaStream_t st);
+cudaError_t launch_narrow_bf16(unsigned short *dst, const float *src, uint64_t n, uint32_t *bad,
+                               cudaStream_t st);
 
 // Audit-mode leaves: BLAKE2b-64 of the header and of every chunk of w, m, v (k_blake2b.cu).
-cudaError_t launch_leaves_b2(const float *w, const float *m, const float *v, uint64_t n,
+cudaError_t launch_leaves_b2(const void *w, int w_bf16, const float *m, const float *v, uint64_t n,
                              uint64_t c, uint64_t *leaves, uint32_t step, int sm_count,
                              cudaStream_t st);
 

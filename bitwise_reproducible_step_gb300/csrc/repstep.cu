@@ -36,6 +36,8 @@ bool valid_config(const repstep_config *cfg)
     if (!cfg) return false;
     if (cfg->n > 0xFFFFFFFFull) return false;
     if (cfg->grad_dtype != REPSTEP_F32 && cfg->grad_dtype != REPSTEP_BF16) return false;
+    if (cfg->param_dtype != REPSTEP_F32 && cfg->param_dtype != REPSTEP_BF16) return false;
+    if (cfg->reserved != 0) return false;
     if (cfg->grid_blocks < 0) return false;
     if (cfg->block_threads != 0 && cfg->block_threads != 128 && cfg->block_threads != 256 &&
         cfg->block_threads != 512)
@@ -82,7 +84,8 @@ struct repstep_ctx {
     uint64_t reduced;        // elements reduced since the last clip
     bool scale_ready;        // a clip followed the last reduce
     uint64_t updated;        // elements updated by AdamW since the last clip
-    const float *sw, *sm, *sv;
+    const void *sw;
+    const float *sm, *sv;
     std::vector<uint64_t> cut_norm, cut_leaf;   // chunks cut by range boundaries
 
     float *g() const { return reinterpret_cast<float *>(ws + lay.g); }
@@ -92,6 +95,8 @@ struct repstep_ctx {
     uint64_t *merkle_part() const { return reinterpret_cast<uint64_t *>(ws + lay.merkle_part); }
     uint64_t *powers() const { return reinterpret_cast<uint64_t *>(ws + lay.powers); }
     Scalars *sc() const { return reinterpret_cast<Scalars *>(ws + lay.scalars); }
+    int w_bf16() const { return cfg.param_dtype == REPSTEP_BF16 ? 1 : 0; }
+    uint64_t w_bytes() const { return n * (w_bf16() ? 2 : 4); }
 
     int cuda_fail(cudaError_t e)
     {
@@ -243,7 +248,7 @@ int do_clip(repstep_ctx *x, float clip, float *norm_out, float *scale_out)
     return REPSTEP_OK;
 }
 
-int do_adamw(repstep_ctx *x, float *w, float *m, float *v, const repstep_hparams *hp,
+int do_adamw(repstep_ctx *x, void *w, float *m, float *v, const repstep_hparams *hp,
              uint64_t begin, uint64_t count)
 {
     if (!w || !m || !v) return REPSTEP_ERR_ARG;
@@ -293,14 +298,15 @@ int do_adamw(repstep_ctx *x, float *w, float *m, float *v, const repstep_hparams
     // PF61 mode: AdamW fused with the leaf digests; audit mode: AdamW alone (the BLAKE2b
     // leaves are computed from the final state by repstep_root)
     const int mode = x->cfg.hash_mode == REPSTEP_HASH_BLAKE2B ? 2 : 0;
-    const size_t smem = adamw_smem_bytes(nt, mode, a);
-    cudaError_t e = adamw_prepare(nt, mode, smem);
+    const int pt = x->w_bf16();
+    const size_t smem = adamw_smem_bytes(nt, mode, pt, a);
+    cudaError_t e = adamw_prepare(nt, mode, pt, smem);
     if (e != cudaSuccess) return x->cuda_fail(e);
     int bps = 1;
-    e = adamw_occupancy(nt, mode, smem, &bps);
+    e = adamw_occupancy(nt, mode, pt, smem, &bps);
     if (e != cudaSuccess) return x->cuda_fail(e);
     const int grid = grid_for(x, bps, a.chunk_hi - a.chunk_lo);
-    e = launch_adamw(nt, mode, a, grid, smem, x->stream);
+    e = launch_adamw(nt, mode, pt, a, grid, smem, x->stream);
     if (e != cudaSuccess) return x->cuda_fail(e);
     ++x->launches;
     if (mode == 0) note_cut_chunks(x->cut_leaf, begin, end, x->n);
@@ -332,9 +338,9 @@ int merkle(repstep_ctx *x, int32_t step, uint64_t *root_out)
 }
 
 // Audit mode: BLAKE2b-64 leaves of the whole state (header included).
-int audit_leaves(repstep_ctx *x, int32_t step, const float *w, const float *m, const float *v)
+int audit_leaves(repstep_ctx *x, int32_t step, const void *w, const float *m, const float *v)
 {
-    cudaError_t e = launch_leaves_b2(w, m, v, x->n, x->c, x->leaves(), uint32_t(step),
+    cudaError_t e = launch_leaves_b2(w, x->w_bf16(), m, v, x->n, x->c, x->leaves(), uint32_t(step),
                                      x->sm_count, x->stream);
     if (e != cudaSuccess) return x->cuda_fail(e);
     ++x->launches;
@@ -354,7 +360,8 @@ int do_root(repstep_ctx *x, int32_t step, uint64_t *root_out)
     unique_sort(x->cut_leaf);
     for (size_t i = 0; i < x->cut_leaf.size(); i += kFixMax) {
         const int cnt = int(x->cut_leaf.size() - i < size_t(kFixMax) ? x->cut_leaf.size() - i : kFixMax);
-        cudaError_t e = launch_leaf_fix(x->sw, x->sm, x->sv, x->n, x->c, x->leaves(), x->powers(),
+        cudaError_t e = launch_leaf_fix(x->sw, x->w_bf16(), x->sm, x->sv, x->n, x->c, x->leaves(),
+                                        x->powers(),
                                         x->cut_leaf.data() + i, cnt, x->stream);
         if (e != cudaSuccess) return x->cuda_fail(e);
         ++x->launches;
@@ -363,7 +370,7 @@ int do_root(repstep_ctx *x, int32_t step, uint64_t *root_out)
     return merkle(x, step, root_out);
 }
 
-int do_hash(repstep_ctx *x, int32_t step, const float *w, const float *m, const float *v,
+int do_hash(repstep_ctx *x, int32_t step, const void *w, const float *m, const float *v,
             uint64_t *root_out)
 {
     if (!w || !m || !v) return REPSTEP_ERR_ARG;
@@ -376,7 +383,7 @@ int do_hash(repstep_ctx *x, int32_t step, const float *w, const float *m, const 
     }
     if (x->n > 0) {
         AdamwArgs a{};
-        a.w = const_cast<float *>(w);
+        a.w = const_cast<void *>(w);
         a.m = const_cast<float *>(m);
         a.v = const_cast<float *>(v);
         a.leaves = x->leaves();
@@ -388,18 +395,87 @@ int do_hash(repstep_ctx *x, int32_t step, const float *w, const float *m, const 
         a.end = x->n;
         a.chunk_lo = 0;
         a.chunk_hi = x->c;
-        const int nt = x->nt_adamw;
-        const size_t smem = adamw_smem_bytes(nt, 1, a);
-        cudaError_t e = adamw_prepare(nt, 1, smem);
+        const int nt = x->nt_adamw, pt = x->w_bf16();
+        const size_t smem = adamw_smem_bytes(nt, 1, pt, a);
+        cudaError_t e = adamw_prepare(nt, 1, pt, smem);
         if (e != cudaSuccess) return x->cuda_fail(e);
         int bps = 1;
-        e = adamw_occupancy(nt, 1, smem, &bps);
+        e = adamw_occupancy(nt, 1, pt, smem, &bps);
         if (e != cudaSuccess) return x->cuda_fail(e);
-        e = launch_adamw(nt, 1, a, grid_for(x, bps, x->c), smem, x->stream);
+        e = launch_adamw(nt, 1, pt, a, grid_for(x, bps, x->c), smem, x->stream);
         if (e != cudaSuccess) return x->cuda_fail(e);
         ++x->launches;
     }
     return merkle(x, step, root_out);
+}
+
+// ---- bf16 parameters in the fp32 image -------------------------------------------------
+// The image always holds w as fp32 words.  A bf16 value widens exactly (its bits are the
+// top half of the fp32 word); an fp32 word narrows back only when its low half is zero.
+
+// n bf16 values sit at p + 2n; widen them into the fp32 words at p, in place.  Going
+// upward, word i overwrites bytes [4i, 4i+4), which hold only bf16 values of index <= i,
+// all of them read already.
+void widen_bf16_in_place(unsigned char *p, uint64_t n)
+{
+    for (uint64_t i = 0; i < n; ++i) {
+        uint16_t h;
+        std::memcpy(&h, p + 2 * n + 2 * i, 2);
+        const uint32_t u = uint32_t(h) << 16;
+        std::memcpy(p + 4 * i, &u, 4);
+    }
+}
+
+// fp32 words at p narrowed to bf16 at p, in place (value i moves from 4i to 2i, below it).
+void narrow_bf16_in_place(unsigned char *p, uint64_t n)
+{
+    for (uint64_t i = 0; i < n; ++i) {
+        uint32_t u;
+        std::memcpy(&u, p + 4 * i, 4);
+        const uint16_t h = uint16_t(u >> 16);
+        std::memcpy(p + 2 * i, &h, 2);
+    }
+}
+
+bool all_bf16_exact(const unsigned char *p, uint64_t n)
+{
+    for (uint64_t i = 0; i < n; ++i) {
+        uint32_t u;
+        std::memcpy(&u, p + 4 * i, 4);
+        if (u & 0xFFFFu) return false;
+    }
+    return true;
+}
+
+constexpr uint64_t kIoChunk = 64ull << 20;   // bytes per staged host transfer
+
+struct PinnedBuf {
+    void *p = nullptr;
+    ~PinnedBuf()
+    {
+        if (p) cudaFreeHost(p);
+    }
+};
+
+// Host fp32 words (checked exact by the caller) -> device bf16, through a pinned buffer;
+// synchronous on the context's stream.
+cudaError_t narrow_host_to_device(repstep_ctx *x, unsigned short *d_w, const unsigned char *src,
+                                  uint64_t n)
+{
+    PinnedBuf buf;
+    cudaError_t e = cudaMallocHost(&buf.p, kIoChunk);
+    if (e != cudaSuccess) return e;
+    unsigned char *b = static_cast<unsigned char *>(buf.p);
+    const uint64_t per = kIoChunk / 4;
+    for (uint64_t i = 0; i < n; i += per) {
+        const uint64_t cnt = n - i < per ? n - i : per;
+        std::memcpy(b, src + 4 * i, 4 * cnt);
+        narrow_bf16_in_place(b, cnt);
+        e = cudaMemcpyAsync(d_w + i, b, 2 * cnt, cudaMemcpyHostToDevice, x->stream);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(x->stream);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 }  // namespace
@@ -497,7 +573,7 @@ int repstep_clip(repstep_ctx *ctx, float clip, float *d_norm_out, float *d_scale
     return do_clip(ctx, clip, d_norm_out, d_scale_out);
 }
 
-int repstep_adamw(repstep_ctx *ctx, float *d_w, float *d_m, float *d_v, const repstep_hparams *hp,
+int repstep_adamw(repstep_ctx *ctx, void *d_w, float *d_m, float *d_v, const repstep_hparams *hp,
                   uint64_t begin, uint64_t count)
 {
     if (!ctx) return REPSTEP_ERR_ARG;
@@ -510,7 +586,7 @@ int repstep_root(repstep_ctx *ctx, int32_t step, uint64_t *d_root_out)
     return do_root(ctx, step, d_root_out);
 }
 
-int repstep_hash(repstep_ctx *ctx, int32_t step, const float *d_w, const float *d_m,
+int repstep_hash(repstep_ctx *ctx, int32_t step, const void *d_w, const float *d_m,
                  const float *d_v, uint64_t *d_root_out)
 {
     if (!ctx) return REPSTEP_ERR_ARG;
@@ -518,7 +594,7 @@ int repstep_hash(repstep_ctx *ctx, int32_t step, const float *d_w, const float *
 }
 
 int repstep_step(repstep_ctx *ctx, const void *const *d_grads, uint32_t R, uint32_t nodes,
-                 uint32_t gpus_per_node, float *d_w, float *d_m, float *d_v,
+                 uint32_t gpus_per_node, void *d_w, float *d_m, float *d_v,
                  const repstep_hparams *hp, int32_t step, float *d_norm_out, uint64_t *d_root_out)
 {
     if (!ctx) return REPSTEP_ERR_ARG;
@@ -543,7 +619,7 @@ int repstep_step(repstep_ctx *ctx, const void *const *d_grads, uint32_t R, uint3
 
 uint64_t repstep_image_bytes(uint64_t n) { return 8 + 12 * n; }
 
-int repstep_image_write(repstep_ctx *ctx, int32_t step, const float *d_w, const float *d_m,
+int repstep_image_write(repstep_ctx *ctx, int32_t step, const void *d_w, const float *d_m,
                         const float *d_v, void *dst, uint64_t dst_bytes, int dst_is_host)
 {
     if (!ctx || !d_w || !d_m || !d_v || !dst) return REPSTEP_ERR_ARG;
@@ -561,17 +637,32 @@ int repstep_image_write(repstep_ctx *ctx, int32_t step, const float *d_w, const 
         if (e != cudaSuccess) return ctx->cuda_fail(e);
         ++ctx->launches;
     }
-    const float *arrs[3] = {d_w, d_m, d_v};
-    for (int a = 0; a < 3; ++a) {
-        if (n == 0) break;
-        e = cudaMemcpyAsync(d + 8 + uint64_t(a) * 4 * n, arrs[a], 4 * n, kind, ctx->stream);
+    if (n == 0) return REPSTEP_OK;
+    // w: fp32 bytes as they are, or bf16 widened exactly to fp32
+    if (!ctx->w_bf16()) {
+        e = cudaMemcpyAsync(d + 8, d_w, 4 * n, kind, ctx->stream);
+    } else if (!dst_is_host) {
+        e = launch_widen_bf16(reinterpret_cast<float *>(d + 8),
+                              static_cast<const unsigned short *>(d_w), n, ctx->stream);
+        ++ctx->launches;
+    } else {
+        // the bf16 values land in the upper half of the image's w region and are widened in
+        // place on the host (synchronous)
+        e = cudaMemcpyAsync(d + 8 + 2 * n, d_w, 2 * n, cudaMemcpyDeviceToHost, ctx->stream);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(ctx->stream);
+        if (e == cudaSuccess) widen_bf16_in_place(d + 8, n);
+    }
+    if (e != cudaSuccess) return ctx->cuda_fail(e);
+    const float *arrs[2] = {d_m, d_v};
+    for (int a = 0; a < 2; ++a) {
+        e = cudaMemcpyAsync(d + 8 + uint64_t(a + 1) * 4 * n, arrs[a], 4 * n, kind, ctx->stream);
         if (e != cudaSuccess) return ctx->cuda_fail(e);
     }
     return REPSTEP_OK;
 }
 
 int repstep_image_read(repstep_ctx *ctx, const void *src, uint64_t src_bytes, int src_is_host,
-                       int32_t *step_out, float *d_w, float *d_m, float *d_v)
+                       int32_t *step_out, void *d_w, float *d_m, float *d_v)
 {
     if (!ctx || !src || !d_w || !d_m || !d_v) return REPSTEP_ERR_ARG;
     const uint64_t n = ctx->n;
@@ -586,13 +677,46 @@ int repstep_image_read(repstep_ctx *ctx, const void *src, uint64_t src_bytes, in
         if (e != cudaSuccess) return ctx->cuda_fail(e);
     }
     if (uint64_t(h[1]) != n) return REPSTEP_ERR_FORMAT;
-    if (step_out) *step_out = int32_t(h[0]);
     const unsigned char *s = static_cast<const unsigned char *>(src);
+    // bf16 parameters: every w word of the image must be a bf16 value exactly; checked
+    // before anything is copied
+    if (ctx->w_bf16() && n > 0) {
+        bool exact = true;
+        if (src_is_host) {
+            exact = all_bf16_exact(s + 8, n);
+        } else {
+            if (!aligned(src, 4)) return REPSTEP_ERR_ALIGN;
+            uint32_t bad = 0;
+            Scalars *sc = ctx->sc();
+            e = cudaMemsetAsync(&sc->aux, 0, sizeof(uint32_t), ctx->stream);
+            if (e == cudaSuccess)
+                e = launch_narrow_bf16(nullptr, reinterpret_cast<const float *>(s + 8), n, &sc->aux,
+                                       ctx->stream);
+            if (e == cudaSuccess)
+                e = cudaMemcpyAsync(&bad, &sc->aux, sizeof bad, cudaMemcpyDeviceToHost, ctx->stream);
+            if (e == cudaSuccess) e = cudaStreamSynchronize(ctx->stream);
+            if (e != cudaSuccess) return ctx->cuda_fail(e);
+            ++ctx->launches;
+            exact = bad == 0;
+        }
+        if (!exact) return REPSTEP_ERR_FORMAT;
+    }
+    if (step_out) *step_out = int32_t(h[0]);
+    if (n == 0) return REPSTEP_OK;
     const cudaMemcpyKind kind = src_is_host ? cudaMemcpyHostToDevice : cudaMemcpyDeviceToDevice;
-    float *arrs[3] = {d_w, d_m, d_v};
-    for (int a = 0; a < 3; ++a) {
-        if (n == 0) break;
-        e = cudaMemcpyAsync(arrs[a], s + 8 + uint64_t(a) * 4 * n, 4 * n, kind, ctx->stream);
+    if (!ctx->w_bf16()) {
+        e = cudaMemcpyAsync(d_w, s + 8, 4 * n, kind, ctx->stream);
+    } else if (!src_is_host) {
+        e = launch_narrow_bf16(static_cast<unsigned short *>(d_w),
+                               reinterpret_cast<const float *>(s + 8), n, nullptr, ctx->stream);
+        ++ctx->launches;
+    } else {
+        e = narrow_host_to_device(ctx, static_cast<unsigned short *>(d_w), s + 8, n);
+    }
+    if (e != cudaSuccess) return ctx->cuda_fail(e);
+    float *arrs[2] = {d_m, d_v};
+    for (int a = 0; a < 2; ++a) {
+        e = cudaMemcpyAsync(arrs[a], s + 8 + uint64_t(a + 1) * 4 * n, 4 * n, kind, ctx->stream);
         if (e != cudaSuccess) return ctx->cuda_fail(e);
     }
     return REPSTEP_OK;
@@ -602,21 +726,7 @@ int repstep_image_read(repstep_ctx *ctx, const void *src, uint64_t src_bytes, in
 // Checkpoint files: the image streamed between the device arrays and a file through one
 // reusable pinned host buffer ("grow_a_language_model_checkpoints": step_NNNNNN.bin).
 // ----------------------------------------------------------------------------------------
-namespace {
-
-constexpr uint64_t kIoChunk = 64ull << 20;   // bytes per staged transfer
-
-struct PinnedBuf {
-    void *p = nullptr;
-    ~PinnedBuf()
-    {
-        if (p) cudaFreeHost(p);
-    }
-};
-
-}  // namespace
-
-int repstep_checkpoint_save(repstep_ctx *ctx, const char *path, int32_t step, const float *d_w,
+int repstep_checkpoint_save(repstep_ctx *ctx, const char *path, int32_t step, const void *d_w,
                             const float *d_m, const float *d_v)
 {
     if (!ctx || !path || !d_w || !d_m || !d_v) return REPSTEP_ERR_ARG;
@@ -632,9 +742,27 @@ int repstep_checkpoint_save(repstep_ctx *ctx, const char *path, int32_t step, co
         cudaError_t e = cudaMallocHost(&buf.p, kIoChunk);
         if (e != cudaSuccess) rc = ctx->cuda_fail(e);
     }
-    const float *arrs[3] = {d_w, d_m, d_v};
-    for (int a = 0; a < 3 && rc == REPSTEP_OK; ++a) {
-        const unsigned char *src = reinterpret_cast<const unsigned char *>(arrs[a]);
+    if (ctx->w_bf16() && rc == REPSTEP_OK) {
+        // bf16 w: each piece lands in the upper half of the buffer and is widened in place
+        unsigned char *b = static_cast<unsigned char *>(buf.p);
+        const unsigned short *w16 = static_cast<const unsigned short *>(d_w);
+        const uint64_t per = kIoChunk / 4;
+        for (uint64_t i = 0; i < n && rc == REPSTEP_OK; i += per) {
+            const uint64_t cnt = n - i < per ? n - i : per;
+            cudaError_t e = cudaMemcpyAsync(b + 2 * cnt, w16 + i, 2 * cnt, cudaMemcpyDeviceToHost,
+                                            ctx->stream);
+            if (e == cudaSuccess) e = cudaStreamSynchronize(ctx->stream);
+            if (e != cudaSuccess) {
+                rc = ctx->cuda_fail(e);
+                break;
+            }
+            widen_bf16_in_place(b, cnt);
+            if (std::fwrite(b, 1, 4 * cnt, f) != 4 * cnt) rc = REPSTEP_ERR_ARG;
+        }
+    }
+    const void *arrs[3] = {d_w, d_m, d_v};
+    for (int a = ctx->w_bf16() ? 1 : 0; a < 3 && rc == REPSTEP_OK; ++a) {
+        const unsigned char *src = static_cast<const unsigned char *>(arrs[a]);
         for (uint64_t off = 0; off < 4 * n && rc == REPSTEP_OK; off += kIoChunk) {
             const uint64_t len = 4 * n - off < kIoChunk ? 4 * n - off : kIoChunk;
             cudaError_t e = cudaMemcpyAsync(buf.p, src + off, len, cudaMemcpyDeviceToHost,
@@ -650,7 +778,7 @@ int repstep_checkpoint_save(repstep_ctx *ctx, const char *path, int32_t step, co
     return rc;
 }
 
-int repstep_checkpoint_load(repstep_ctx *ctx, const char *path, int32_t *step_out, float *d_w,
+int repstep_checkpoint_load(repstep_ctx *ctx, const char *path, int32_t *step_out, void *d_w,
                             float *d_m, float *d_v)
 {
     if (!ctx || !path || !d_w || !d_m || !d_v) return REPSTEP_ERR_ARG;
@@ -671,9 +799,34 @@ int repstep_checkpoint_load(repstep_ctx *ctx, const char *path, int32_t *step_ou
         cudaError_t e = cudaMallocHost(&buf.p, kIoChunk);
         if (e != cudaSuccess) rc = ctx->cuda_fail(e);
     }
-    float *arrs[3] = {d_w, d_m, d_v};
-    for (int a = 0; a < 3 && rc == REPSTEP_OK; ++a) {
-        unsigned char *dst = reinterpret_cast<unsigned char *>(arrs[a]);
+    unsigned char *b = static_cast<unsigned char *>(buf.p);
+    if (ctx->w_bf16() && rc == REPSTEP_OK && n > 0) {
+        // bf16 parameters: first a pass over the file's w words -- each must be a bf16
+        // value exactly -- so that nothing is copied from an image that cannot be loaded
+        for (uint64_t off = 0; off < 4 * n && rc == REPSTEP_OK; off += kIoChunk) {
+            const uint64_t len = 4 * n - off < kIoChunk ? 4 * n - off : kIoChunk;
+            if (std::fread(b, 1, len, f) != len || !all_bf16_exact(b, len / 4))
+                rc = REPSTEP_ERR_FORMAT;
+        }
+        if (rc == REPSTEP_OK && std::fseek(f, 8, SEEK_SET) != 0) rc = REPSTEP_ERR_FORMAT;
+        unsigned short *w16 = static_cast<unsigned short *>(d_w);
+        const uint64_t per = kIoChunk / 4;
+        for (uint64_t i = 0; i < n && rc == REPSTEP_OK; i += per) {
+            const uint64_t cnt = n - i < per ? n - i : per;
+            if (std::fread(b, 1, 4 * cnt, f) != 4 * cnt) {
+                rc = REPSTEP_ERR_FORMAT;
+                break;
+            }
+            narrow_bf16_in_place(b, cnt);
+            cudaError_t e = cudaMemcpyAsync(w16 + i, b, 2 * cnt, cudaMemcpyHostToDevice,
+                                            ctx->stream);
+            if (e == cudaSuccess) e = cudaStreamSynchronize(ctx->stream);
+            if (e != cudaSuccess) rc = ctx->cuda_fail(e);
+        }
+    }
+    void *arrs[3] = {d_w, d_m, d_v};
+    for (int a = ctx->w_bf16() ? 1 : 0; a < 3 && rc == REPSTEP_OK; ++a) {
+        unsigned char *dst = static_cast<unsigned char *>(arrs[a]);
         for (uint64_t off = 0; off < 4 * n && rc == REPSTEP_OK; off += kIoChunk) {
             const uint64_t len = 4 * n - off < kIoChunk ? 4 * n - off : kIoChunk;
             if (std::fread(buf.p, 1, len, f) != len) {

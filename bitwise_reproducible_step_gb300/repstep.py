@@ -37,7 +37,8 @@ STATUS = {0: "REPSTEP_OK", 1: "REPSTEP_ERR_ARG", 2: "REPSTEP_ERR_ALIGN", 3: "REP
 
 class Config(C.Structure):
     _fields_ = [("n", C.c_uint64), ("grad_dtype", C.c_int32), ("grid_blocks", C.c_int32),
-                ("block_threads", C.c_int32), ("hash_mode", C.c_int32)]
+                ("block_threads", C.c_int32), ("hash_mode", C.c_int32),
+                ("param_dtype", C.c_int32), ("reserved", C.c_int32)]
 
 
 HASH_PF61 = 0
@@ -155,7 +156,7 @@ def image_bytes(n: int) -> int:
 
 
 def workspace_bytes(n: int, grad_dtype=torch.float32, grid_blocks=0, block_threads=0) -> int:
-    cfg = Config(n, _dtype_code(grad_dtype), grid_blocks, block_threads, 0)
+    cfg = Config(n, _dtype_code(grad_dtype), grid_blocks, block_threads, 0, REPSTEP_F32, 0)
     return int(lib().repstep_workspace_bytes(C.byref(cfg)))
 
 
@@ -164,7 +165,7 @@ def _dtype_code(dt) -> int:
         return REPSTEP_F32
     if dt == torch.bfloat16:
         return REPSTEP_BF16
-    raise TypeError(f"gradient dtype {dt}: float32 or bfloat16")
+    raise TypeError(f"dtype {dt}: float32 or bfloat16")
 
 
 def reduce_norm_noalloc(grads, clip: float, g_out: torch.Tensor, norm_out: torch.Tensor,
@@ -207,15 +208,17 @@ class Repstep:
 
     def __init__(self, n: int, grad_dtype=torch.float32, device=None, grid_blocks: int = 0,
                  block_threads: int = 0, stream: torch.cuda.Stream | None = None,
-                 hash_mode: int = HASH_PF61):
+                 hash_mode: int = HASH_PF61, param_dtype=torch.float32):
         L = lib()
         self.n = int(n)
         self.grad_dtype = grad_dtype
+        self.param_dtype = param_dtype
         self.device = torch.device("cuda", torch.cuda.current_device()) if device is None \
             else torch.device(device)
         self._fixed_stream = stream
         self.hash_mode = hash_mode
-        self.cfg = Config(self.n, _dtype_code(grad_dtype), grid_blocks, block_threads, hash_mode)
+        self.cfg = Config(self.n, _dtype_code(grad_dtype), grid_blocks, block_threads, hash_mode,
+                          _dtype_code(param_dtype), 0)
         nbytes = int(L.repstep_workspace_bytes(C.byref(self.cfg)))
         if nbytes == 0:
             raise RepstepError(1, "bad configuration")
@@ -236,11 +239,11 @@ class Repstep:
             raise RuntimeError("context destroyed")
         lib().repstep_set_stream(self._ctx, C.c_void_p(self._stream().cuda_stream))
 
-    def _state(self, *ts):
-        for t in ts:
-            if t.device != self.device or t.dtype != torch.float32 or not t.is_contiguous() \
+    def _state(self, w, m, v):
+        for t, want in ((w, self.param_dtype), (m, torch.float32), (v, torch.float32)):
+            if t.device != self.device or t.dtype != want or not t.is_contiguous() \
                     or t.numel() < self.n:
-                raise ValueError("state arrays: contiguous float32 on the context's device, "
+                raise ValueError(f"state arrays: contiguous {want} on the context's device, "
                                  f"at least n={self.n} elements")
 
     def _grads(self, grads):

@@ -103,6 +103,12 @@ typedef struct {
     int32_t block_threads;   /* 0: default; else 128, 256 or 512 compute threads per CTA of
                                 the streaming kernels.  Never changes bits.                */
     int32_t hash_mode;       /* enum repstep_hash_mode (0 = PF61 leaves)                   */
+    int32_t param_dtype;     /* enum repstep_dtype of the parameters w.  REPSTEP_BF16: w is
+                                bf16, widened exactly for the update, which runs in fp32,
+                                and rounded back to bf16 once, to nearest even (OPEN-1B
+                                §3.2, optimizer-state precision).  m and v are fp32 either
+                                way; the image and the hash hold w widened to fp32.        */
+    int32_t reserved;        /* must be 0                                                  */
 } repstep_config;
 
 typedef struct {
@@ -119,7 +125,7 @@ size_t repstep_workspace_bytes(const repstep_config *cfg);
 /* Byte offsets of the workspace regions (for inspection and tests): g fp32[n], chunk sums
  * fp32[c], norm partials, leaf digests u64[1+3c] (header leaf first, then the w, m, v
  * chunks), Merkle partials, PF61 power table u64[4096], device scalars (pre-clip norm fp32,
- * clip scale fp32, flags u32, pad u32, root u64).  Returns REPSTEP_ERR_ARG on a bad config. */
+ * clip scale fp32, flags u32, aux u32, root u64).  Returns REPSTEP_ERR_ARG on a bad config. */
 typedef struct {
     uint64_t g, chunk_sums, norm_partials, leaves, merkle_partials, pow_table, scalars, total;
 } repstep_layout;
@@ -171,12 +177,13 @@ int repstep_reduce_paper(repstep_ctx *ctx, const void *const *d_grads, uint32_t 
  * clip must be > 0 (+inf: never clip). */
 int repstep_clip(repstep_ctx *ctx, float clip, float *d_norm_out, float *d_scale_out);
 
-/* Clipped AdamW over [begin, begin+count) of the full-length fp32 arrays w, m, v (updated
- * in place), using g and the scale from the last reduce/clip.  Also writes the PF61 leaf
+/* Clipped AdamW over [begin, begin+count) of the full-length arrays w (param_dtype), m, v
+ * (fp32), updated in place, using g and the scale from the last reduce/clip.  All three
+ * pointers 16-byte aligned.  Also writes the PF61 leaf
  * digest of every new w, m and v chunk lying wholly inside the range; repstep_root()
  * completes the others.  All calls of one step must pass the same w, m, v base pointers.
  * Requires repstep_clip() since the last reduce (else REPSTEP_ERR_STATE). */
-int repstep_adamw(repstep_ctx *ctx, float *d_w, float *d_m, float *d_v,
+int repstep_adamw(repstep_ctx *ctx, void *d_w, float *d_m, float *d_v,
                   const repstep_hparams *hp, uint64_t begin, uint64_t count);
 
 /* Merkle root of the state left by the repstep_adamw calls since the last clip, whose
@@ -186,8 +193,9 @@ int repstep_adamw(repstep_ctx *ctx, float *d_w, float *d_m, float *d_v,
 int repstep_root(repstep_ctx *ctx, int32_t step, uint64_t *d_root_out);
 
 /* Standalone state hash (OPEN-1B App. B) of an arbitrary (step, w, m, v): every leaf is
- * computed from the arrays, then the Merkle root.  Equals repstep_root() after a step. */
-int repstep_hash(repstep_ctx *ctx, int32_t step, const float *d_w, const float *d_m,
+ * computed from the arrays (w of param_dtype, hashed as its fp32 image words), then the
+ * Merkle root.  Equals repstep_root() after a step. */
+int repstep_hash(repstep_ctx *ctx, int32_t step, const void *d_w, const float *d_m,
                  const float *d_v, uint64_t *d_root_out);
 
 /* One whole step: reduce over [0, n) -> clip -> AdamW over [0, n) -> root, bit-identical
@@ -195,22 +203,26 @@ int repstep_hash(repstep_ctx *ctx, int32_t step, const float *d_w, const float *
  * caller sets hp->bc1/bc2 for it (repstep_bias_corrections).  d_norm_out (nullable)
  * receives the pre-clip norm, d_root_out (nullable) the root. */
 int repstep_step(repstep_ctx *ctx, const void *const *d_grads, uint32_t R, uint32_t nodes,
-                 uint32_t gpus_per_node, float *d_w, float *d_m, float *d_v,
+                 uint32_t gpus_per_node, void *d_w, float *d_m, float *d_v,
                  const repstep_hparams *hp, int32_t step, float *d_norm_out,
                  uint64_t *d_root_out);
 
 /* Checkpoint image ("grow_a_language_model_checkpoints", Format):
  * [LE int32 step][LE uint32 n][n fp32 w][n fp32 m][n fp32 v], 8 + 12n bytes, written to
- * dst (device memory, or host memory when dst_is_host != 0) on the context's stream. */
+ * dst (device memory, 4-byte aligned, or host memory when dst_is_host != 0) on the
+ * context's stream.  bf16 parameters are written widened to fp32 (exact); to a host dst
+ * that part is synchronous. */
 uint64_t repstep_image_bytes(uint64_t n);
-int repstep_image_write(repstep_ctx *ctx, int32_t step, const float *d_w, const float *d_m,
+int repstep_image_write(repstep_ctx *ctx, int32_t step, const void *d_w, const float *d_m,
                         const float *d_v, void *dst, uint64_t dst_bytes, int dst_is_host);
 
 /* Load an image into w, m, v (device arrays of the context's n).  Rejects (with
- * REPSTEP_ERR_FORMAT, before copying anything) a buffer whose size is not 8 + 12n or
- * whose header n differs from the context's n.  *step_out receives the header step. */
+ * REPSTEP_ERR_FORMAT, before copying anything) a buffer whose size is not 8 + 12n, whose
+ * header n differs from the context's n, or -- with bf16 parameters -- whose w holds a
+ * word that is not a bf16 value exactly (low 16 bits not zero).  *step_out receives the
+ * header step. */
 int repstep_image_read(repstep_ctx *ctx, const void *src, uint64_t src_bytes, int src_is_host,
-                       int32_t *step_out, float *d_w, float *d_m, float *d_v);
+                       int32_t *step_out, void *d_w, float *d_m, float *d_v);
 
 /* Checkpoint files ("grow_a_language_model_checkpoints", step_NNNNNN.bin): the image above,
  * streamed between the device arrays w, m, v (the context's n) and `path` through one
@@ -219,11 +231,13 @@ int repstep_image_read(repstep_ctx *ctx, const void *src, uint64_t src_bytes, in
  * byte was written, so a crash never leaves a truncated file under the final name.  Load
  * rejects, before copying anything, a file whose size is not 8 + 12n or whose header n
  * differs (REPSTEP_ERR_FORMAT) -- a check that cannot fail is not a check, so the tests
- * feed it truncated, oversized and mismatched files.  REPSTEP_ERR_ARG if the file cannot
- * be opened or written. */
-int repstep_checkpoint_save(repstep_ctx *ctx, const char *path, int32_t step, const float *d_w,
+ * feed it truncated, oversized and mismatched files.  bf16 parameters are widened on save;
+ * load first reads the file's w words once and rejects (REPSTEP_ERR_FORMAT) a file with
+ * any word that is not a bf16 value exactly.  REPSTEP_ERR_ARG if the file cannot be opened
+ * or written. */
+int repstep_checkpoint_save(repstep_ctx *ctx, const char *path, int32_t step, const void *d_w,
                             const float *d_m, const float *d_v);
-int repstep_checkpoint_load(repstep_ctx *ctx, const char *path, int32_t *step_out, float *d_w,
+int repstep_checkpoint_load(repstep_ctx *ctx, const char *path, int32_t *step_out, void *d_w,
                             float *d_m, float *d_v);
 
 /* Bias corrections for step t >= 1: p_j = beta_j^t as t repeated fp32 products,

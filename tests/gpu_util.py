@@ -76,3 +76,36 @@ def oracle_step(grads_np, w, m, v, t, nodes=1, clip=None, hash_mode=0):
     return O.step(grads_np, w, m, v, lr=HP["lr"], beta1=HP["beta1"], beta2=HP["beta2"],
                   eps=HP["eps"], wd=HP["wd"], clip=HP["clip"] if clip is None else clip, t=t,
                   nodes=nodes, hash_mode=hash_mode)
+
+
+def oracle_step_bf16w(grads_np, w16, m, v, t, clip=None, hash_mode=0):
+    """One oracle step with bf16 parameters, composed from the oracle's pieces: reduce,
+    norm, clip scale, AdamW on widened bf16 parameters with one rounding back, and the state
+    hash over the widened parameters."""
+    clip = HP["clip"] if clip is None else clip
+    g = O.reduce(grads_np)
+    nv = O.norm(g)
+    sc = O.clip_scale(nv, clip)
+    bc1, bc2 = O.bias_corrections(HP["beta1"], HP["beta2"], t)
+    w16, m, v = O.adamw_bf16w(w16, m, v, g, sc, HP["lr"], HP["beta1"], HP["beta2"], HP["eps"],
+                              HP["wd"], bc1, bc2)
+    wide = O.widen_bf16(w16)
+    return dict(w16=w16, m=m, v=v, norm=nv, scale=sc, g=g,
+                root=O.state_hash(t, wide, m, v, hash_mode),
+                leaves=O.leaves(t, wide, m, v, hash_mode))
+
+
+def bits16(x) -> np.ndarray:
+    if isinstance(x, torch.Tensor):
+        x = x.detach().cpu().contiguous().view(torch.int16).numpy()
+    return np.ascontiguousarray(x).view(np.uint16)
+
+
+def assert_same_bf16(got, want, what=""):
+    """bf16 bit patterns equal, NaNs compared by class."""
+    gb, wb = bits16(got), bits16(want)
+    assert gb.shape == wb.shape, (what, gb.shape, wb.shape)
+    nan = lambda b: (b & 0x7FFF) > 0x7F80  # noqa: E731
+    bad = (gb != wb) & ~(nan(gb) & nan(wb))
+    assert not bad.any(), f"{what}: {int(bad.sum())} differing bf16 slots, first at " \
+                          f"{int(np.argmax(bad))}"

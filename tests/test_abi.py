@@ -78,6 +78,18 @@ def test_bad_configs_rejected(L):
     assert L.repstep_workspace_bytes(C.byref(cfg)) == 0
     cfg = rs.Config(10, 0, -1, 0, 0)
     assert L.repstep_workspace_bytes(C.byref(cfg)) == 0
+    cfg = rs.Config(10, 0, 0, 0, 0, 2, 0)     # parameter dtype neither fp32 nor bf16
+    assert L.repstep_workspace_bytes(C.byref(cfg)) == 0
+    cfg = rs.Config(10, 0, 0, 0, 0, 0, 1)     # reserved field not zero
+    assert L.repstep_workspace_bytes(C.byref(cfg)) == 0
+
+
+def test_bf16_parameters_need_no_more_workspace(L):
+    # w lives in the caller's buffer either way; the workspace holds g (fp32) and digests
+    for n in [0, 4097, 12_800_000]:
+        f32 = rs.Config(n, 1, 0, 0, 0, 0, 0)
+        b16 = rs.Config(n, 1, 0, 0, 0, 1, 0)
+        assert L.repstep_workspace_bytes(C.byref(b16)) == L.repstep_workspace_bytes(C.byref(f32)) > 0
 
 
 def test_create_rejects_before_touching_a_device(L):
