@@ -367,6 +367,56 @@ void oracle_adamw_bf16w(uint16_t *w16, float *m, float *v, const float *g, uint6
 }
 
 /* ------------------------------------------------------------------------------ */
+/* Per-segment weight decay ([OPEN-1B] §3.2, optimizer paragraph: no weight decay on  */
+/* the embeddings, the normalisation gains or RoPE).  The flat parameter vector is   */
+/* cut into `count` segments: segment s covers [seg_begin[s], seg_begin[s+1]), the   */
+/* last one ends at n; seg_begin[0] is 0 and the starts increase strictly.  An       */
+/* element of a segment with decay[s] != 0 takes the update with weight decay wd,    */
+/* any other element the same update with weight decay 0.                            */
+/* Returns 0, or -1 on a bad segment list.                                           */
+/* ------------------------------------------------------------------------------ */
+static int segments_ok(uint64_t n, const uint64_t *seg_begin, uint32_t count)
+{
+    if (count == 0) return n == 0;
+    if (seg_begin[0] != 0) return 0;
+    for (uint32_t s = 1; s < count; ++s)
+        if (seg_begin[s] <= seg_begin[s - 1] || seg_begin[s] >= n) return 0;
+    return 1;
+}
+
+static float segment_wd(uint64_t i, const uint64_t *seg_begin, const uint8_t *decay,
+                        uint32_t count, float wd)
+{
+    uint32_t s = 0;
+    while (s + 1 < count && seg_begin[s + 1] <= i) ++s;
+    return decay[s] ? wd : 0.0f;
+}
+
+int oracle_adamw_segments(float *w, float *m, float *v, const float *g, uint64_t n, float scale,
+                          float lr, float beta1, float beta2, float eps, float wd, float bc1,
+                          float bc2, const uint64_t *seg_begin, const uint8_t *decay,
+                          uint32_t count)
+{
+    if (!segments_ok(n, seg_begin, count)) return -1;
+    for (uint64_t i = 0; i < n; ++i)
+        oracle_adamw(w + i, m + i, v + i, g + i, 1, scale, lr, beta1, beta2, eps,
+                     segment_wd(i, seg_begin, decay, count, wd), bc1, bc2);
+    return 0;
+}
+
+int oracle_adamw_bf16w_segments(uint16_t *w16, float *m, float *v, const float *g, uint64_t n,
+                                float scale, float lr, float beta1, float beta2, float eps,
+                                float wd, float bc1, float bc2, const uint64_t *seg_begin,
+                                const uint8_t *decay, uint32_t count)
+{
+    if (!segments_ok(n, seg_begin, count)) return -1;
+    for (uint64_t i = 0; i < n; ++i)
+        oracle_adamw_bf16w(w16 + i, m + i, v + i, g + i, 1, scale, lr, beta1, beta2, eps,
+                           segment_wd(i, seg_begin, decay, count, wd), bc1, bc2);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------------ */
 /* PF61 leaf digest over a sequence of 32-bit words:                                 */
 /*   F(x_0..x_{W-1}) = (W + sum_{i<W} x_i * K^(i+1)) mod p,  p = 2^61 - 1,          */
 /*   K = (isqrt(5 * 2^122) - 2^61) >> 1 (floor of 2^61 (sqrt5 - 1)/2).               */

@@ -87,6 +87,11 @@ def lib():
                                          C.c_float, C.c_float, C.c_float, C.c_float, C.c_float,
                                          C.c_float]
         L.oracle_adamw_bf16w.restype = None
+        seg = [fp, fp, fp, fp, C.c_uint64] + [C.c_float] * 8 + [fp, fp, C.c_uint32]
+        L.oracle_adamw_segments.argtypes = seg
+        L.oracle_adamw_segments.restype = C.c_int
+        L.oracle_adamw_bf16w_segments.argtypes = seg
+        L.oracle_adamw_bf16w_segments.restype = C.c_int
         _lib = L
     return _lib
 
@@ -212,6 +217,41 @@ def adamw_bf16w(w16, m, v, g, scale, lr, beta1, beta2, eps, wd, bc1, bc2):
     f = lambda x: float(np.float32(x))  # noqa: E731
     lib().oracle_adamw_bf16w(_p(w16), _p(m), _p(v), _p(g), w16.size, f(scale), f(lr), f(beta1),
                              f(beta2), f(eps), f(wd), f(bc1), f(bc2))
+    return w16, m, v
+
+
+def _segments(segments):
+    """[(begin, decays), ...] -> (uint64 starts, uint8 flags)."""
+    b = np.ascontiguousarray([int(s[0]) for s in segments] or [0], dtype=np.uint64)
+    d = np.ascontiguousarray([1 if s[1] else 0 for s in segments] or [0], dtype=np.uint8)
+    return b, d, len(segments)
+
+
+def adamw_segments(w, m, v, g, scale, lr, beta1, beta2, eps, wd, bc1, bc2, segments):
+    """AdamW with per-segment weight decay: segments = [(begin, decays), ...] cutting
+    [0, n) in increasing order from 0; returns (w', m', v') on copies."""
+    w = _f32(w).copy(); m = _f32(m).copy(); v = _f32(v).copy(); g = _f32(g)
+    b, d, cnt = _segments(segments)
+    f = lambda x: float(np.float32(x))  # noqa: E731
+    rc = lib().oracle_adamw_segments(_p(w), _p(m), _p(v), _p(g), w.size, f(scale), f(lr),
+                                     f(beta1), f(beta2), f(eps), f(wd), f(bc1), f(bc2), _p(b),
+                                     _p(d), cnt)
+    if rc != 0:
+        raise ValueError("bad segment list")
+    return w, m, v
+
+
+def adamw_bf16w_segments(w16, m, v, g, scale, lr, beta1, beta2, eps, wd, bc1, bc2, segments):
+    """bf16 parameters with per-segment weight decay; returns (w16', m', v') on copies."""
+    w16 = np.ascontiguousarray(w16, dtype=np.uint16).copy()
+    m = _f32(m).copy(); v = _f32(v).copy(); g = _f32(g)
+    b, d, cnt = _segments(segments)
+    f = lambda x: float(np.float32(x))  # noqa: E731
+    rc = lib().oracle_adamw_bf16w_segments(_p(w16), _p(m), _p(v), _p(g), w16.size, f(scale),
+                                           f(lr), f(beta1), f(beta2), f(eps), f(wd), f(bc1),
+                                           f(bc2), _p(b), _p(d), cnt)
+    if rc != 0:
+        raise ValueError("bad segment list")
     return w16, m, v
 
 

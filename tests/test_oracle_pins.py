@@ -645,3 +645,70 @@ def test_adamw_bf16w_is_fp32_update_rounded_once():
     assert np.array_equal(v1.view(np.uint32), vf.view(np.uint32))
     want = torch.from_numpy(wf).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
     assert np.array_equal(w1, want)
+
+
+# ----------------------------------------------------------------------------------
+# Per-segment weight decay ("OPEN-1B", §3.2 optimizer paragraph: no decay on embeddings,
+# normalisation gains or RoPE)
+# ----------------------------------------------------------------------------------
+SEGS = [(0, True), (5, False), (4096, True), (4100, False), (9000, True), (12_000, False)]
+
+
+def _decays(n, segs):
+    out = np.zeros(n, bool)
+    for k, (b, d) in enumerate(segs):
+        e = segs[k + 1][0] if k + 1 < len(segs) else n
+        out[b:e] = d
+    return out
+
+
+def test_segments_zero_gradient_decays_exactly_the_decay_segments():
+    # g = m = v = 0: u = 0, so a decaying element becomes w * (1 - lr wd) and any other
+    # element keeps its bits -- which pins the segment lookup element by element
+    n = 12_345
+    rng = np.random.default_rng(50)
+    w = (rng.standard_normal(n) * 0.02).astype(np.float32)
+    z = np.zeros(n, np.float32)
+    bc1, bc2 = O.bias_corrections(B1, B2, 1)
+    w1, _, _ = O.adamw_segments(w, z, z, z, 1.0, LR, B1, B2, EPS, WD, bc1, bc2, SEGS)
+    delta = X.f32(1 - X.F(X.mul(LR, WD)))
+    dec = _decays(n, SEGS)
+    want = np.where(dec, np.array([X.mul(x, delta) for x in w], np.float32), w)
+    assert np.array_equal(w1.view(np.uint32), want.view(np.uint32))
+    assert dec.any() and (~dec).any()
+
+
+def test_segments_reduce_to_plain_adamw_per_element():
+    n = 12_345
+    rng = np.random.default_rng(51)
+    w = (rng.standard_normal(n) * 0.02).astype(np.float32)
+    m = (rng.standard_normal(n) * 1e-4).astype(np.float32)
+    v = np.abs(rng.standard_normal(n) * 1e-7).astype(np.float32)
+    g = (rng.standard_normal(n) * 1e-3).astype(np.float32)
+    bc1, bc2 = O.bias_corrections(B1, B2, 3)
+    args = (1.0, LR, B1, B2, EPS)
+    ws, ms, vs = O.adamw_segments(w, m, v, g, *args, WD, bc1, bc2, SEGS)
+    wd_, md, vd = O.adamw(w, m, v, g, *args, WD, bc1, bc2)
+    w0, _, _ = O.adamw(w, m, v, g, *args, 0.0, bc1, bc2)
+    dec = _decays(n, SEGS)
+    assert np.array_equal(ws.view(np.uint32), np.where(dec, wd_, w0).view(np.uint32))
+    assert np.array_equal(ms.view(np.uint32), md.view(np.uint32))
+    assert np.array_equal(vs.view(np.uint32), vd.view(np.uint32))
+    # one decaying segment is plain AdamW; one non-decaying segment is AdamW with wd = 0
+    assert np.array_equal(O.adamw_segments(w, m, v, g, *args, WD, bc1, bc2, [(0, 1)])[0], wd_)
+    assert np.array_equal(O.adamw_segments(w, m, v, g, *args, WD, bc1, bc2, [(0, 0)])[0], w0)
+    # bf16 parameters: the same choice, then one rounding
+    w16 = torch.from_numpy(w).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    b16, _, _ = O.adamw_bf16w_segments(w16, m, v, g, *args, WD, bc1, bc2, SEGS)
+    d16 = O.adamw_bf16w(w16, m, v, g, *args, WD, bc1, bc2)[0]
+    z16 = O.adamw_bf16w(w16, m, v, g, *args, 0.0, bc1, bc2)[0]
+    assert np.array_equal(b16, np.where(dec, d16, z16))
+
+
+@pytest.mark.parametrize("segs", [[(1, True)], [(0, True), (0, False)], [(0, True), (9, False), (7, True)],
+                                  [(0, True), (100, False)], []])
+def test_segments_bad_lists_rejected(segs):
+    n = 100
+    z = np.zeros(n, np.float32)
+    with pytest.raises(ValueError):
+        O.adamw_segments(z, z, z, z, 1.0, LR, B1, B2, EPS, WD, 1.0, 1.0, segs)
