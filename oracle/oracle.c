@@ -191,13 +191,32 @@ int oracle_reduce_topology(const void *const *grads, int dtype, uint32_t nodes,
 /* (largest block first; lower-replica block on the left), whose level wording       */
 /* contradicts itself.  Finally g = Result * fp32(1/dp_replicate).                   */
 /* ------------------------------------------------------------------------------ */
-int oracle_reduce_alg1(const void *const *grads, int dtype, uint32_t R, uint32_t dp_shard,
-                       uint64_t n, float *g)
+/* The gradient of virtual rank r at element i.  accum == 0: the rank's gradient as  */
+/* given (one input per rank).  accum >= 1: [OPEN-1B] §6 Algorithm 1's microbatch    */
+/* accumulation on a single device, taken literally -- g_r starts at +0 and each of  */
+/* the rank's accum microbatch gradients (inputs r*accum .. r*accum + accum - 1, in  */
+/* order) is added after multiplying by fp32(1/accum) (App. A.3: every average is a   */
+/* reciprocal multiply).                                                             */
+static float rank_grad(const void *const *grads, int dtype, uint32_t r, uint32_t accum,
+                       float rho_acc, uint64_t i)
+{
+    if (accum == 0) return load_grad(grads[r], dtype, i);
+    float gr = 0.0f;
+    for (uint32_t k = 0; k < accum; ++k) {
+        float term = load_grad(grads[(uint64_t)r * accum + k], dtype, i) * rho_acc;
+        gr = gr + term;
+    }
+    return gr;
+}
+
+static int reduce_alg1(const void *const *grads, int dtype, uint32_t R, uint32_t dp_shard,
+                       uint32_t accum, uint64_t n, float *g)
 {
     if (R == 0 || dp_shard == 0 || R % dp_shard != 0 || (dtype != 0 && dtype != 1)) return -1;
     uint32_t dp_rep = R / dp_shard;
     float rho_shard = 1.0f / (float)dp_shard;
     float rho_rep = 1.0f / (float)dp_rep;
+    float rho_acc = accum ? 1.0f / (float)accum : 1.0f;
     /* the stack: at most one entry per level, 64 levels is more than any R */
     float part[64];
     int level[64];
@@ -206,7 +225,7 @@ int oracle_reduce_alg1(const void *const *grads, int dtype, uint32_t R, uint32_t
         float inner = 0.0f;
         for (uint32_t r = 0; r < R; ++r) {
             uint32_t shard = r % dp_shard;
-            float x = load_grad(grads[r], dtype, i);
+            float x = rank_grad(grads, dtype, r, accum, rho_acc, i);
             if (shard == 0) inner = x;
             else inner = inner + x;
             if (shard == dp_shard - 1) {
@@ -229,6 +248,22 @@ int oracle_reduce_alg1(const void *const *grads, int dtype, uint32_t R, uint32_t
         g[i] = acc * rho_rep;
     }
     return 0;
+}
+
+int oracle_reduce_alg1(const void *const *grads, int dtype, uint32_t R, uint32_t dp_shard,
+                       uint64_t n, float *g)
+{
+    return reduce_alg1(grads, dtype, R, dp_shard, 0, n, g);
+}
+
+/* The same with the microbatch accumulation of Algorithm 1's inner loop: grads holds  */
+/* R * accum microbatch gradients, rank-major (input r*accum + k is microbatch k of    */
+/* virtual rank r).  accum >= 1.                                                     */
+int oracle_reduce_alg1_accum(const void *const *grads, int dtype, uint32_t R, uint32_t dp_shard,
+                             uint32_t accum, uint64_t n, float *g)
+{
+    if (accum == 0) return -1;
+    return reduce_alg1(grads, dtype, R, dp_shard, accum, n, g);
 }
 
 /* ------------------------------------------------------------------------------ */

@@ -81,6 +81,9 @@ def lib():
         L.oracle_step_mode.restype = C.c_int
         L.oracle_reduce_alg1.argtypes = [fp, C.c_int, C.c_uint32, C.c_uint32, C.c_uint64, fp]
         L.oracle_reduce_alg1.restype = C.c_int
+        L.oracle_reduce_alg1_accum.argtypes = [fp, C.c_int, C.c_uint32, C.c_uint32, C.c_uint32,
+                                               C.c_uint64, fp]
+        L.oracle_reduce_alg1_accum.restype = C.c_int
         L.oracle_f32_to_bf16.argtypes = [C.c_float]
         L.oracle_f32_to_bf16.restype = C.c_uint16
         L.oracle_adamw_bf16w.argtypes = [fp, fp, fp, fp, C.c_uint64, C.c_float, C.c_float,
@@ -171,6 +174,21 @@ def reduce_alg1(grads, dp_shard: int) -> np.ndarray:
     rc = lib().oracle_reduce_alg1(C.cast(ptrs, C.c_void_p), code, len(arrs), dp_shard, n, _p(g))
     if rc != 0:
         raise ValueError(f"oracle_reduce_alg1 rc={rc}")
+    return g
+
+
+def reduce_alg1_accum(grads, dp_shard: int, accum: int) -> np.ndarray:
+    """Paper-exact reduction with Algorithm 1's microbatch accumulation: grads holds
+    R * accum microbatch gradients, rank-major (index r * accum + k)."""
+    code, arrs, ptrs = _grad_arrays(grads)
+    if accum < 1 or len(arrs) % accum:
+        raise ValueError("the input count must be a multiple of accum >= 1")
+    n = arrs[0].size
+    g = np.empty(n, np.float32)
+    rc = lib().oracle_reduce_alg1_accum(C.cast(ptrs, C.c_void_p), code, len(arrs) // accum,
+                                        dp_shard, accum, n, _p(g))
+    if rc != 0:
+        raise ValueError(f"oracle_reduce_alg1_accum rc={rc}")
     return g
 
 

@@ -57,15 +57,19 @@ def bits(x) -> int:
 
 
 def parse_exact(tok: str) -> Fraction:
-    """'1', '0', '2^-24', '1+2^-23', '2^-12' -> Fraction."""
+    """'1', '0', '2^-24', '1+2^-23', '2^-12', '11184813*2^-25' -> Fraction."""
     tot = Fraction(0)
     for part in tok.split("+"):
         part = part.strip()
+        coef = Fraction(1)
+        if "*" in part:
+            c, part = part.split("*")
+            coef = Fraction(int(c))
         if "^" in part:
             base, ex = part.split("^")
-            tot += Fraction(int(base)) ** int(ex)
+            tot += coef * Fraction(int(base)) ** int(ex)
         else:
-            tot += Fraction(part)
+            tot += coef * Fraction(part)
     return tot
 
 

@@ -118,7 +118,7 @@ def test_tree_reading_differs_from_treefold_at_seven():
 def _rounding_cases():
     cases = {}
     for line in open(os.path.join(GOLDEN, "rounding_cases.txt")):
-        if not line.strip() or line.startswith("#") or line.startswith("alg1_"):
+        if not line.strip() or line.startswith("#") or line.startswith(("alg1_", "acc_")):
             continue
         name, ins, want, _why = [s.strip() for s in line.split("|")]
         cases[name] = (ins, X.parse_exact(want))
@@ -150,6 +150,52 @@ def test_golden_alg1_reductions():
         rho_rep = X.f32(Fraction(1, R // dp_shard))
         expect = X.mul(np.float32(float(X.parse_exact(want))), rho_rep)
         assert all(X.bits(x) == X.bits(expect) for x in g), (name, g, expect)
+
+
+def test_golden_microbatch_accumulation():
+    seen = 0
+    for line in open(os.path.join(GOLDEN, "rounding_cases.txt")):
+        if not line.startswith("acc_"):
+            continue
+        name, dps, acc, ins, want, _why = [x.strip() for x in line.split("|")]
+        vals = [float(X.parse_exact(t)) for t in ins.split(",")]
+        g = O.reduce_alg1_accum([np.full(3, v, np.float32) for v in vals], int(dps), int(acc))
+        expect = np.float32(float(X.parse_exact(want)))
+        assert all(X.bits(x) == X.bits(expect) for x in g), (name, g, expect)
+        seen += 1
+    assert seen >= 1
+
+
+def test_accumulation_starts_from_positive_zero():
+    # g_r <- 0 then g_r + x*rho: microbatches that are all -0 give +0 (IEEE: +0 + -0 = +0);
+    # starting from the first term instead would keep -0
+    mz = np.full(5, -0.0, np.float32)
+    for acc in (1, 2, 3):
+        g = O.reduce_alg1_accum([mz] * acc, 1, acc)
+        assert np.all(g.view(np.uint32) == 0)
+
+
+def test_accumulation_exact_mean_for_dyadic_inputs():
+    # small integers times 2^-10 with power-of-two accum, dp_shard and dp_replicate: every
+    # partial sum and every reciprocal multiply is exact, so g is the exact mean
+    rng = np.random.default_rng(60)
+    for rep, dps, acc in [(2, 2, 2), (4, 1, 4), (1, 4, 8), (2, 4, 2)]:
+        N = rep * dps * acc
+        G = [(rng.integers(-500, 500, 300) * 2.0 ** -10).astype(np.float32) for _ in range(N)]
+        g = O.reduce_alg1_accum(G, dps, acc)
+        for i in range(0, 300, 17):
+            mean = sum(Fraction(float(x[i])) for x in G) / N
+            assert Fraction(float(g[i])) == mean
+
+
+def test_accumulation_with_one_microbatch_is_the_rank_gradient():
+    rng = np.random.default_rng(61)
+    G = [rand_f32(rng, 700, -26, 2) for _ in range(12)]
+    for x in G:
+        x[x == 0] = 1.0                         # no signed zeros: then 0 + x*1 = x exactly
+    for dps in (1, 3, 4, 12):
+        assert np.array_equal(O.reduce_alg1_accum(G, dps, 1).view(np.uint32),
+                              O.reduce_alg1(G, dps).view(np.uint32))
 
 
 @pytest.mark.parametrize("R", [1, 2, 4, 8, 16, 32])
