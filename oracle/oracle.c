@@ -452,6 +452,184 @@ int oracle_adamw_bf16w_segments(uint16_t *w16, float *m, float *v, const float *
 }
 
 /* ------------------------------------------------------------------------------ */
+/* Software flush-to-zero mode ([OPEN-1B] §2.1 "Subnormals": two modes discard       */
+/* subnormals -- FTZ zeroes a subnormal result, DAZ a subnormal input -- and RepOps  */
+/* applies both on every backend to match the least permissive one).  Readings:     */
+/*   - every fp32 operation of the step flushes its operands and its result;        */
+/*   - a flushed value becomes a zero of the same sign;                              */
+/*   - "subnormal result" means the correctly rounded result is subnormal (tininess  */
+/*     after rounding): a value that rounds up to the smallest normal is kept;      */
+/*   - the rounding of a bf16 parameter is an operation too, but its input is then  */
+/*     zero or at least the smallest normal, so it never yields a subnormal.          */
+/* The functions below repeat the IEEE-mode definitions above with every operation  */
+/* written through these helpers, in the same order.                                */
+/* ------------------------------------------------------------------------------ */
+static float flush(float x)
+{
+    if (fpclassify(x) == FP_SUBNORMAL) return copysignf(0.0f, x);
+    return x;
+}
+
+static float fz_add(float a, float b) { return flush(flush(a) + flush(b)); }
+static float fz_sub(float a, float b) { return flush(flush(a) - flush(b)); }
+static float fz_mul(float a, float b) { return flush(flush(a) * flush(b)); }
+static float fz_div(float a, float b) { return flush(flush(a) / flush(b)); }
+static float fz_sqrt(float a) { return flush(sqrtf(flush(a))); }
+
+float oracle_flush(float x) { return flush(x); }
+
+static float fz_tree_sum_rec(const float *x, uint64_t L)
+{
+    if (L == 1) return flush(x[0]);
+    uint64_t k = split_point(L);
+    float left = fz_tree_sum_rec(x, k);
+    float right = fz_tree_sum_rec(x + k, L - k);
+    return fz_add(left, right);
+}
+
+float oracle_tree_sum_ftz(const float *x, uint64_t L)
+{
+    if (L == 0) return 0.0f;
+    return fz_tree_sum_rec(x, L);
+}
+
+/* Replica reduce in FTZ mode: g_i = T_{r<R}(G_r[i]) * fp32(1/R), every op flushed.   */
+int oracle_reduce_ftz(const void *const *grads, int dtype, uint32_t R, uint64_t n, float *g)
+{
+    if (R == 0 || (dtype != 0 && dtype != 1)) return -1;
+    float rho = fz_div(1.0f, (float)R);
+    float *vals = (float *)malloc(sizeof(float) * R);
+    if (!vals) return -1;
+    for (uint64_t i = 0; i < n; ++i) {
+        for (uint32_t r = 0; r < R; ++r) vals[r] = load_grad(grads[r], dtype, i);
+        g[i] = fz_mul(fz_tree_sum_rec(vals, R), rho);
+    }
+    free(vals);
+    return 0;
+}
+
+/* Paper-exact reduction (Algorithm 1, accum 0 = rank gradients given) in FTZ mode. */
+int oracle_reduce_alg1_ftz(const void *const *grads, int dtype, uint32_t R, uint32_t dp_shard,
+                           uint32_t accum, uint64_t n, float *g)
+{
+    if (R == 0 || dp_shard == 0 || R % dp_shard != 0 || (dtype != 0 && dtype != 1)) return -1;
+    uint32_t dp_rep = R / dp_shard;
+    float rho_shard = fz_div(1.0f, (float)dp_shard);
+    float rho_rep = fz_div(1.0f, (float)dp_rep);
+    float rho_acc = accum ? fz_div(1.0f, (float)accum) : 1.0f;
+    float part[64];
+    int level[64];
+    for (uint64_t i = 0; i < n; ++i) {
+        int depth = 0;
+        float inner = 0.0f;
+        for (uint32_t r = 0; r < R; ++r) {
+            uint32_t shard = r % dp_shard;
+            float x;
+            if (accum == 0) {
+                x = flush(load_grad(grads[r], dtype, i));
+            } else {
+                x = 0.0f;
+                for (uint32_t k = 0; k < accum; ++k)
+                    x = fz_add(x, fz_mul(load_grad(grads[(uint64_t)r * accum + k], dtype, i),
+                                         rho_acc));
+            }
+            if (shard == 0) inner = x;
+            else inner = fz_add(inner, x);
+            if (shard == dp_shard - 1) {
+                float p = fz_mul(inner, rho_shard);
+                int lv = 0;
+                while (depth > 0 && level[depth - 1] == lv) {
+                    float lower = part[depth - 1];
+                    --depth;
+                    p = fz_add(lower, p);
+                    ++lv;
+                }
+                part[depth] = p;
+                level[depth] = lv;
+                ++depth;
+            }
+        }
+        float acc = part[0];
+        for (int d = 1; d < depth; ++d) acc = fz_add(acc, part[d]);
+        g[i] = fz_mul(acc, rho_rep);
+    }
+    return 0;
+}
+
+/* Global norm in FTZ mode: squares, chunk trees, the tree over chunks, sqrt.         */
+float oracle_norm_ftz(const float *g, uint64_t n, float *chunk_sums)
+{
+    uint64_t c = (n + ORACLE_CHUNK - 1) / ORACLE_CHUNK;
+    if (c == 0) return 0.0f;
+    float *s = (float *)malloc(sizeof(float) * c);
+    float *q = (float *)malloc(sizeof(float) * ORACLE_CHUNK);
+    if (!s || !q) { free(s); free(q); return NAN; }
+    for (uint64_t k = 0; k < c; ++k) {
+        uint64_t lo = k * ORACLE_CHUNK;
+        uint64_t hi = lo + ORACLE_CHUNK < n ? lo + ORACLE_CHUNK : n;
+        for (uint64_t i = lo; i < hi; ++i) q[i - lo] = fz_mul(g[i], g[i]);
+        s[k] = fz_tree_sum_rec(q, hi - lo);
+        if (chunk_sums) chunk_sums[k] = s[k];
+    }
+    float norm = fz_sqrt(fz_tree_sum_rec(s, c));
+    free(s);
+    free(q);
+    return norm;
+}
+
+float oracle_clip_scale_ftz(float norm, float clip)
+{
+    if (flush(norm) > flush(clip)) return fz_div(clip, norm);
+    return 1.0f;
+}
+
+void oracle_bias_corrections_ftz(float beta1, float beta2, int32_t t, float *bc1, float *bc2)
+{
+    float p1 = 1.0f, p2 = 1.0f;
+    for (int32_t j = 0; j < t; ++j) {
+        p1 = fz_mul(p1, beta1);
+        p2 = fz_mul(p2, beta2);
+    }
+    *bc1 = fz_sub(1.0f, p1);
+    *bc2 = fz_sub(1.0f, p2);
+}
+
+/* AdamW in FTZ mode, same op order as oracle_adamw; w is fp32 (w_bf16 == 0) or bf16  */
+/* bit patterns (widened, updated, rounded once to nearest even); optional            */
+/* decay segments as in oracle_adamw_segments (count 0: every element decays).       */
+int oracle_adamw_ftz(void *w, int w_bf16, float *m, float *v, const float *g, uint64_t n,
+                     float scale, float lr, float beta1, float beta2, float eps, float wd,
+                     float bc1, float bc2, const uint64_t *seg_begin, const uint8_t *decay,
+                     uint32_t count)
+{
+    if (count > 0 && !segments_ok(n, seg_begin, count)) return -1;
+    float omega1 = fz_sub(1.0f, beta1);
+    float omega2 = fz_sub(1.0f, beta2);
+    for (uint64_t i = 0; i < n; ++i) {
+        float wd_i = count > 0 ? segment_wd(i, seg_begin, decay, count, wd) : wd;
+        float delta = fz_sub(1.0f, fz_mul(lr, wd_i));
+        float wi = w_bf16 ? bf16_to_f32(((uint16_t *)w)[i]) : ((float *)w)[i];
+        float gc = fz_mul(g[i], scale);
+        float m_new = fz_add(fz_mul(beta1, m[i]), fz_mul(omega1, gc));
+        float v_new = fz_add(fz_mul(beta2, v[i]), fz_mul(omega2, fz_mul(gc, gc)));
+        float mhat = fz_div(m_new, bc1);
+        float vhat = fz_div(v_new, bc2);
+        float u = fz_div(mhat, fz_add(fz_sqrt(vhat), eps));
+        float w_new = fz_sub(fz_mul(wi, delta), fz_mul(lr, u));
+        if (w_bf16) {
+            /* w_new is zero or at least 2^-126 in magnitude, a bf16 value itself, so the
+               rounding cannot produce a bf16 subnormal and needs no flush */
+            ((uint16_t *)w)[i] = oracle_f32_to_bf16(w_new);
+        } else {
+            ((float *)w)[i] = w_new;
+        }
+        m[i] = m_new;
+        v[i] = v_new;
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------------ */
 /* PF61 leaf digest over a sequence of 32-bit words:                                 */
 /*   F(x_0..x_{W-1}) = (W + sum_{i<W} x_i * K^(i+1)) mod p,  p = 2^61 - 1,          */
 /*   K = (isqrt(5 * 2^122) - 2^61) >> 1 (floor of 2^61 (sqrt5 - 1)/2).               */

@@ -90,6 +90,25 @@ def lib():
                                          C.c_float, C.c_float, C.c_float, C.c_float, C.c_float,
                                          C.c_float]
         L.oracle_adamw_bf16w.restype = None
+        L.oracle_flush.argtypes = [C.c_float]
+        L.oracle_flush.restype = C.c_float
+        L.oracle_tree_sum_ftz.argtypes = [fp, C.c_uint64]
+        L.oracle_tree_sum_ftz.restype = C.c_float
+        L.oracle_reduce_ftz.argtypes = [fp, C.c_int, C.c_uint32, C.c_uint64, fp]
+        L.oracle_reduce_ftz.restype = C.c_int
+        L.oracle_reduce_alg1_ftz.argtypes = [fp, C.c_int, C.c_uint32, C.c_uint32, C.c_uint32,
+                                             C.c_uint64, fp]
+        L.oracle_reduce_alg1_ftz.restype = C.c_int
+        L.oracle_norm_ftz.argtypes = [fp, C.c_uint64, fp]
+        L.oracle_norm_ftz.restype = C.c_float
+        L.oracle_clip_scale_ftz.argtypes = [C.c_float, C.c_float]
+        L.oracle_clip_scale_ftz.restype = C.c_float
+        L.oracle_bias_corrections_ftz.argtypes = [C.c_float, C.c_float, C.c_int32,
+                                                  C.POINTER(C.c_float), C.POINTER(C.c_float)]
+        L.oracle_bias_corrections_ftz.restype = None
+        L.oracle_adamw_ftz.argtypes = [fp, C.c_int, fp, fp, fp, C.c_uint64] + [C.c_float] * 8 + \
+            [fp, fp, C.c_uint32]
+        L.oracle_adamw_ftz.restype = C.c_int
         seg = [fp, fp, fp, fp, C.c_uint64] + [C.c_float] * 8 + [fp, fp, C.c_uint32]
         L.oracle_adamw_segments.argtypes = seg
         L.oracle_adamw_segments.restype = C.c_int
@@ -271,6 +290,76 @@ def adamw_bf16w_segments(w16, m, v, g, scale, lr, beta1, beta2, eps, wd, bc1, bc
     if rc != 0:
         raise ValueError("bad segment list")
     return w16, m, v
+
+
+# ---------------------------------------------------------------- software FTZ mode
+def flush(x) -> np.float32:
+    """A subnormal becomes a zero of the same sign; everything else is unchanged."""
+    return np.float32(lib().oracle_flush(float(np.float32(x))))
+
+
+def tree_sum_ftz(x) -> np.float32:
+    x = _f32(x)
+    return np.float32(lib().oracle_tree_sum_ftz(_p(x), x.size))
+
+
+def reduce_ftz(grads) -> np.ndarray:
+    code, arrs, ptrs = _grad_arrays(grads)
+    g = np.empty(arrs[0].size, np.float32)
+    if lib().oracle_reduce_ftz(C.cast(ptrs, C.c_void_p), code, len(arrs), g.size, _p(g)) != 0:
+        raise ValueError("bad arguments")
+    return g
+
+
+def reduce_alg1_ftz(grads, dp_shard: int, accum: int = 0) -> np.ndarray:
+    code, arrs, ptrs = _grad_arrays(grads)
+    if accum and len(arrs) % accum:
+        raise ValueError("the input count must be a multiple of accum")
+    g = np.empty(arrs[0].size, np.float32)
+    R = len(arrs) // accum if accum else len(arrs)
+    if lib().oracle_reduce_alg1_ftz(C.cast(ptrs, C.c_void_p), code, R, dp_shard, accum, g.size,
+                                    _p(g)) != 0:
+        raise ValueError("bad arguments")
+    return g
+
+
+def norm_ftz(g, with_chunks: bool = False):
+    g = _f32(g)
+    c = (g.size + 4095) // 4096
+    chunks = np.empty(max(c, 1), np.float32)
+    nv = np.float32(lib().oracle_norm_ftz(_p(g), g.size, _p(chunks)))
+    return (nv, chunks[:c].copy()) if with_chunks else nv
+
+
+def clip_scale_ftz(norm_value, clip) -> np.float32:
+    return np.float32(lib().oracle_clip_scale_ftz(float(np.float32(norm_value)),
+                                                  float(np.float32(clip))))
+
+
+def bias_corrections_ftz(beta1, beta2, t):
+    b1, b2 = C.c_float(), C.c_float()
+    lib().oracle_bias_corrections_ftz(float(np.float32(beta1)), float(np.float32(beta2)), int(t),
+                                      C.byref(b1), C.byref(b2))
+    return np.float32(b1.value), np.float32(b2.value)
+
+
+def adamw_ftz(w, m, v, g, scale, lr, beta1, beta2, eps, wd, bc1, bc2, segments=None):
+    """FTZ-mode AdamW on copies; w float32, or uint16 bf16 bit patterns (bf16 parameters);
+    segments as in adamw_segments (None: every element decays).  Returns (w', m', v')."""
+    w = np.ascontiguousarray(w).copy()
+    bf = w.dtype == np.uint16
+    if not bf:
+        w = _f32(w).copy()
+    m = _f32(m).copy(); v = _f32(v).copy(); g = _f32(g)
+    b, d, cnt = _segments(segments) if segments else (np.zeros(1, np.uint64),
+                                                      np.zeros(1, np.uint8), 0)
+    f = lambda x: float(np.float32(x))  # noqa: E731
+    rc = lib().oracle_adamw_ftz(_p(w), 1 if bf else 0, _p(m), _p(v), _p(g), w.size, f(scale),
+                                f(lr), f(beta1), f(beta2), f(eps), f(wd), f(bc1), f(bc2), _p(b),
+                                _p(d), cnt)
+    if rc != 0:
+        raise ValueError("bad segment list")
+    return w, m, v
 
 
 def widen_bf16(w16) -> np.ndarray:

@@ -758,3 +758,89 @@ def test_segments_bad_lists_rejected(segs):
     z = np.zeros(n, np.float32)
     with pytest.raises(ValueError):
         O.adamw_segments(z, z, z, z, 1.0, LR, B1, B2, EPS, WD, 1.0, 1.0, segs)
+
+
+# ----------------------------------------------------------------------------------
+# Software flush-to-zero mode ("OPEN-1B", §2.1 "Subnormals": FTZ zeroes subnormal
+# results, DAZ subnormal inputs)
+# ----------------------------------------------------------------------------------
+TINY = np.float32(np.finfo(np.float32).tiny)        # 2^-126, the smallest normal
+
+
+def test_flush_definition():
+    rng = np.random.default_rng(70)
+    bits = rng.integers(0, 2 ** 32, 20000, dtype=np.uint64).astype(np.uint32)
+    bits[:2000] &= 0x807FFFFF                         # plenty of subnormals and zeros
+    for x in bits.view(np.float32):
+        y = O.flush(x)
+        if np.isnan(x):
+            assert np.isnan(y)
+        elif x != 0 and abs(x) < TINY:
+            assert y == 0 and np.signbit(y) == np.signbit(x)
+        else:
+            assert X.bits(y) == X.bits(x)
+
+
+def test_ftz_equals_ieee_when_nothing_is_subnormal():
+    # magnitudes far from the subnormal range: every FTZ function takes exactly the IEEE
+    # function's operations
+    rng = np.random.default_rng(71)
+    n = 9000
+    G = [(rng.standard_normal(n) * 1e-3).astype(np.float32) for _ in range(6)]
+    assert np.array_equal(O.reduce_ftz(G), O.reduce(G))
+    assert np.array_equal(O.reduce_alg1_ftz(G, 3), O.reduce_alg1(G, 3))
+    assert np.array_equal(O.reduce_alg1_ftz(G, 1, accum=2), O.reduce_alg1_accum(G, 1, 2))
+    g = O.reduce(G)
+    nf, cf = O.norm_ftz(g, with_chunks=True)
+    ni, ci = O.norm(g, with_chunks=True)
+    assert nf == ni and np.array_equal(cf, ci)
+    assert O.clip_scale_ftz(np.float32(3.0), 1.0) == O.clip_scale(np.float32(3.0), 1.0)
+    for t in (1, 5, 100):
+        assert O.bias_corrections_ftz(B1, B2, t) == O.bias_corrections(B1, B2, t)
+    w = (rng.standard_normal(n) * 0.02).astype(np.float32)
+    m = (rng.standard_normal(n) * 1e-4).astype(np.float32)
+    v = np.abs(rng.standard_normal(n) * 1e-7).astype(np.float32) + 1e-9
+    bc1, bc2 = O.bias_corrections(B1, B2, 3)
+    a = O.adamw_ftz(w, m, v, g, 0.5, LR, B1, B2, EPS, WD, bc1, bc2)
+    b = O.adamw(w, m, v, g, 0.5, LR, B1, B2, EPS, WD, bc1, bc2)
+    for x, y in zip(a, b):
+        assert np.array_equal(x.view(np.uint32), y.view(np.uint32))
+    w16 = torch.from_numpy(w).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    a16 = O.adamw_ftz(w16, m, v, g, 0.5, LR, B1, B2, EPS, WD, bc1, bc2, segments=SEGS[:3])
+    b16 = O.adamw_bf16w_segments(w16, m, v, g, 0.5, LR, B1, B2, EPS, WD, bc1, bc2, SEGS[:3])
+    assert np.array_equal(a16[0], b16[0]) and np.array_equal(a16[1], b16[1])
+
+
+def test_ftz_golden_cases():
+    z = np.zeros(4, np.float32)
+    # a subnormal sum is flushed: 1.5*2^-126 + (-2^-126) = 2^-127, then times 1/2
+    x0, x1 = np.full(4, 1.5 * 2.0 ** -126, np.float32), np.full(4, -(2.0 ** -126), np.float32)
+    assert np.all(O.reduce([x0, x1]) == np.float32(2.0 ** -128))
+    g = O.reduce_ftz([x0, x1])
+    assert np.all(g.view(np.uint32) == 0)                       # +0
+    # DAZ on a subnormal gradient, sign kept
+    g = O.reduce_ftz([np.full(4, -(2.0 ** -140), np.float32)])
+    assert np.all(g.view(np.uint32) == 0x80000000)              # -0
+    # tininess after rounding: T = (3*2^22 - 1)*2^-148 times fp32(1/3) = (2^25+1)/3 * 2^-25
+    # is exactly 2^-126 - (5/12)*2^-149, below the smallest normal, but rounds UP to it;
+    # the rounded result is normal and kept
+    T = np.full(4, float((3 * 2 ** 22 - 1) * Fraction(2) ** -148), np.float32)
+    assert Fraction(float(T[0])) == (3 * 2 ** 22 - 1) * Fraction(2) ** -148
+    g = O.reduce_ftz([T, z, z])
+    assert np.all(g == TINY)
+    # squares below the normal range vanish: a norm of 2^-70 entries is 0 in FTZ mode
+    g = np.full(5000, 2.0 ** -70, np.float32)
+    assert O.norm(g) > 0 and O.norm_ftz(g) == 0
+    # subnormal moments are flushed: with g = 0 the update is w*(1 - lr*wd) exactly and the
+    # new moments are +0 (IEEE keeps a tiny update)
+    n = 6
+    w = np.full(n, 0.0123, np.float32)
+    m = np.full(n, 2.0 ** -130, np.float32)
+    bc1, bc2 = O.bias_corrections(B1, B2, 2)
+    w1, m1, v1 = O.adamw_ftz(w, m, z[:1].repeat(n), z[:1].repeat(n), 1.0, LR, B1, B2, EPS, WD,
+                             bc1, bc2)
+    delta = X.f32(1 - X.F(X.mul(LR, WD)))
+    assert np.all(w1 == X.mul(w[0], delta))
+    assert not m1.view(np.uint32).any() and not v1.view(np.uint32).any()
+    wi, mi, _ = O.adamw(w, m, z[:1].repeat(n), z[:1].repeat(n), 1.0, LR, B1, B2, EPS, WD, bc1, bc2)
+    assert np.all(mi != 0)
