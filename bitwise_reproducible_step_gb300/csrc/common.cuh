@@ -9,10 +9,11 @@
 // * PF61 arithmetic modulo 2^61 - 1 and the BLAKE2b compression (RFC 7693) used for
 //   Merkle nodes.
 //
-// All fp32 arithmetic uses the explicitly rounded intrinsics (__fadd_rn, __fmul_rn,
-// __fdiv_rn, __fsqrt_rn), which the compiler never contracts into FMA ("OPEN-1B: A Fully
-// Auditable Training Run", §2.1 "Fused multiply-add": explicitly unfused multiply and add
-// on the GPU).  The library is also built with -fmad=false.
+// All fp32 arithmetic of the step goes through Ar<FZ> below: the explicitly rounded
+// intrinsics (__fadd_rn, __fmul_rn, __fdiv_rn, __fsqrt_rn), which the compiler never
+// contracts into FMA ("OPEN-1B: A Fully Auditable Training Run", §2.1 "Fused multiply-add":
+// explicitly unfused multiply and add on the GPU), optionally followed by a software
+// flush of subnormal results (§2.1 "Subnormals").  The library is built with -fmad=false.
 #pragma once
 
 #include <cstdint>
@@ -30,6 +31,36 @@ constexpr uint32_t kFlagTimeoutLeaves = 0x8u;
 // PF61 modulus p = 2^61 - 1 and multiplier K = floor(2^61 (sqrt5 - 1)/2).
 constexpr uint64_t kP61 = 0x1FFFFFFFFFFFFFFFull;
 constexpr uint64_t kK61 = 0x13C6EF372FE94F82ull;
+
+// ----------------------------------------------------------------------------------
+// Arithmetic policy.  FZ = 0: IEEE binary32 with gradual underflow.  FZ = 1: software
+// flush-to-zero ("OPEN-1B", §2.1 "Subnormals": FTZ zeroes a subnormal result, DAZ a
+// subnormal input), read as: every operation's correctly rounded result, and every
+// operand read from memory, is flushed to a zero of the same sign when subnormal.  The
+// flush is one mul.rn.ftz.f32 by 1.0: its .ftz flushes a subnormal operand, and any other
+// value times 1.0 is exact (NaN stays NaN).  Inputs produced by a previous operation are
+// already flushed, so flushing results and loads is the same as flushing every operand.
+// ----------------------------------------------------------------------------------
+__device__ __forceinline__ float flush_subnormal(float x)
+{
+    float r;
+    asm("mul.rn.ftz.f32 %0, %1, 0f3F800000;" : "=f"(r) : "f"(x));
+    return r;
+}
+
+template <int FZ>
+struct Ar {
+    static __device__ __forceinline__ float in(float x)
+    {
+        if constexpr (FZ != 0) return flush_subnormal(x);
+        else return x;
+    }
+    static __device__ __forceinline__ float add(float a, float b) { return in(__fadd_rn(a, b)); }
+    static __device__ __forceinline__ float sub(float a, float b) { return in(__fsub_rn(a, b)); }
+    static __device__ __forceinline__ float mul(float a, float b) { return in(__fmul_rn(a, b)); }
+    static __device__ __forceinline__ float div(float a, float b) { return in(__fdiv_rn(a, b)); }
+    static __device__ __forceinline__ float sqrt(float a) { return in(__fsqrt_rn(a)); }
+};
 
 // Device-side scalars kept in the workspace.
 struct Scalars {
@@ -170,25 +201,26 @@ __device__ __forceinline__ TileRange tile_range(uint64_t base, uint32_t te, uint
 // Elements past n contribute +0, which equals the canonical tree over the short chunk
 // because every term is >= +0.
 // ----------------------------------------------------------------------------------
-template <int W>
+template <int W, int FZ>
 __device__ __forceinline__ float tree_pow2(float *x)
 {
 #pragma unroll
     for (int s = 1; s < W; s <<= 1) {
 #pragma unroll
-        for (int i = 0; i < W; i += 2 * s) x[i] = __fadd_rn(x[i], x[i + s]);
+        for (int i = 0; i < W; i += 2 * s) x[i] = Ar<FZ>::add(x[i], x[i + s]);
     }
     return x[0];
 }
 
+template <int FZ>
 __device__ __forceinline__ float sum4(float a, float b, float c, float d)
 {
-    return __fadd_rn(__fadd_rn(a, b), __fadd_rn(c, d));
+    return Ar<FZ>::add(Ar<FZ>::add(a, b), Ar<FZ>::add(c, d));
 }
 
 // red: shared scratch of TPC * (NT/32) floats.  All NT compute threads call this; the
 // chunk total is returned in thread 0.  `sync` synchronises exactly the NT threads.
-template <int NT, int TPC, typename Sync>
+template <int NT, int TPC, int FZ, typename Sync>
 __device__ __forceinline__ float chunk_tree(float (&part)[TPC], float *red, int tid, Sync sync)
 {
     constexpr int W = NT / 32;
@@ -197,7 +229,7 @@ __device__ __forceinline__ float chunk_tree(float (&part)[TPC], float *red, int 
         float v = part[j];
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1)
-            v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, off));
+            v = Ar<FZ>::add(v, __shfl_xor_sync(0xffffffffu, v, off));
         part[j] = v;
     }
     const int warp = tid >> 5;
@@ -214,9 +246,9 @@ __device__ __forceinline__ float chunk_tree(float (&part)[TPC], float *red, int 
             float w[W];
 #pragma unroll
             for (int i = 0; i < W; ++i) w[i] = red[j * W + i];
-            tiles[j] = tree_pow2<W>(w);
+            tiles[j] = tree_pow2<W, FZ>(w);
         }
-        total = tree_pow2<TPC>(tiles);
+        total = tree_pow2<TPC, FZ>(tiles);
     }
     return total;
 }

@@ -1,546 +1,13 @@
-// k_adamw.cu -- clipped AdamW fused with the state-hash leaf digests (one HBM pass), and a
-// leaves-only mode for the standalone hash.
-//
-// MODE 0 (AdamW): for every element of the active range, in this fixed order
-//     gc = g*scale;  m' = b1*m + (1-b1)*gc;  v' = b2*v + (1-b2)*(gc*gc)
-//     u = (m'/bc1) / (sqrt(v'/bc2) + eps);   w' = w*(1 - lr*wd) - lr*u
-// ("OPEN-1B: A Fully Auditable Training Run", §3.2: AdamW with decoupled weight decay and
-// global-norm clipping; §3.2 paragraph on optimizer-state precision: moments and update in
-// FP32), writing w', m', v' in place; then the PF61 digest of every 4096-element chunk of
-// the NEW w', m', v' that lies wholly inside the range.
-// MODE 1 (leaves): the PF61 digests of the chunks of the given w, m, v, nothing written.
-// MODE 2 (AdamW only): MODE 0 without the digests (the audit hash mode digests the new
-// state with BLAKE2b afterwards).
-// PT 1 (bf16 parameters): w is held in bf16 ("OPEN-1B", §3.2 paragraph on optimizer-state
-// precision): it is widened exactly, updated in fp32, and rounded back to bf16 once, to
-// nearest even; m and v stay fp32.  The hash digests w as its exactly widened fp32 words,
-// so the image and its leaves keep the fp32 layout.
-//
-// PF61 of a chunk of W 32-bit words x_i is (W + sum x_i K^(i+1)) mod (2^61 - 1).  Each
-// power P = K^(i+1) < 2^61 is split into three 21-bit limbs P = l0 + l1 2^21 + l2 2^42, and
-// a thread accumulates x * l_k in three 64-bit sums with one 32x32->64 multiply-add each:
-// with at most 32 words per thread per chunk the sums stay below 2^58, so no carries are
-// lost, and the thread folds them modulo p once per chunk.  The chunk total is an exact
-// integer sum of the thread partials, in any order, so the digest cannot depend on the
-// launch shape.  (App. B of the same paper anchors every step with a hash of parameters
-// and optimizer state; this is its on-device form.)
-//
-// GB300 design: a persistent grid of one CTA per SM.  One producer lane streams the 4 (or
-// 3) arrays tile by tile (TE = 8*NT elements) into a 192 KB shared-memory ring with 1-D
-// bulk TMA copies completing on mbarriers.  The NT compute threads each take two 16-byte
-// groups per array per tile (8 elements of independent AdamW chains), store the results
-// with 16-byte stores, and fold the words into the leaf sums.  Tiles lying wholly inside
-// the range take a fast path without per-element range checks.  Every fp32 operation is
-// an explicitly rounded intrinsic.
-#include <cuda_bf16.h>
-
-#include "common.cuh"
-#include "kernels.h"
+// k_adamw.cu -- the IEEE instantiations of the AdamW / leaf kernel (k_adamw.cuh), the
+// self-test of its fixed-divisor division, and the host-side helpers that size, prepare
+// and launch any AdamW variant.
+#include "k_adamw.cuh"
 
 namespace repstep {
 
+AdamwKernelFn pick_adamw_ieee(const AdamwShape &s) { return pick_adamw<0>(s); }
+
 namespace {
-
-constexpr uint32_t kMaxStages = 12;
-
-// Ring size and CTAs per SM by compute-thread count: 512 threads run one CTA per SM with a
-// 192 KB ring; 256 and 128 threads run two CTAs per SM (96 KB rings), so that two CTAs'
-// chunk barriers overlap and an SM holds as many compute warps either way.
-template <int NT>
-struct Shape {
-    static constexpr uint32_t ring = NT == 512 ? 192 * 1024 : 96 * 1024;
-    static constexpr int min_blocks = NT == 512 ? 1 : 2;
-};
-constexpr int kEPT = 8;            // elements per compute thread per tile (two float4)
-constexpr uint64_t kM21 = (1ull << 21) - 1;
-
-constexpr int kLeafBufs = 4;       // chunks in flight between the compute warps and the leaf warp
-constexpr int kPieces = 27;        // 3 streams x 3 limbs x 3 pieces of 27 bits
-
-template <int NT>
-__host__ __device__ constexpr uint32_t ring_offset()
-{
-    // ring barriers (2 x kMaxStages x 8) | leaf barriers (2 x kLeafBufs x 8) | abort flags
-    // (16) | per-warp leaf pieces kLeafBufs x (NT/32) x kPieces u32 | ring
-    return ((16 * kMaxStages + 16 * kLeafBufs + 16 + kLeafBufs * (NT / 32) * kPieces * 4) + 1023) /
-           1024 * 1024;
-}
-
-// Correctly rounded x / b for a divisor b fixed for the whole launch, by Markstein's
-// final correction (P. Markstein, "Computation of elementary functions on the IBM RISC
-// System/6000 processor", IBM J. Res. Dev. 34(1), 1990; stated as Markstein's theorem in
-// Muller et al., "Handbook of Floating-Point Arithmetic"): with y = RN(1/b) computed once
-// on the host and q = RN(x*y), the remainder r = x - q*b is exact (one fused multiply-add)
-// and RN(q + r*y) (one fused multiply-add) equals RN(x/b).  k_selftest_div checks this
-// against the IEEE division for all 2^46 significand pairs.  Valid ("fast_ok") for b in
-// [2^-40, 2] (checked on the host) and x zero or |x| in [2^-100, 2^60]: there every
-// intermediate is finite, the remainder is a multiple of at least 2^-149 and so exact, and
-// power-of-two exponents scale every step exactly.  A zero keeps its sign (x/b for b > 0).
-__device__ __forceinline__ float div_fast(float x, float b, float y)
-{
-    const float q = __fmul_rn(x, y);
-    const float r = __fmaf_rn(-q, b, x);
-    const float q2 = __fmaf_rn(r, y, q);
-    return x == 0.0f ? x : q2;
-}
-
-__device__ __forceinline__ bool fast_ok(float x)
-{
-    const float ax = fabsf(x);
-    return (ax >= 0x1p-100f && ax <= 0x1p60f) || ax == 0.0f;
-}
-
-// AdamW on the 8 elements a compute thread holds, in the fixed order of the definition.
-// The two divisions by the bias corrections take div_fast; if any lane of the warp holds an
-// operand outside its range (subnormal, huge, infinite, NaN) or the divisors are outside
-// theirs, those divisions are redone with the IEEE division.  Every lane of the warp calls
-// this together.
-__device__ __forceinline__ void adamw8(const float (&g)[8], float (&w)[8], float (&m)[8],
-                                       float (&v)[8], float scale, const AdamwArgs &A)
-{
-    float mn[8], vn[8], mh[8], vh[8];
-    bool bad = !A.fastdiv;
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-        const float gc = __fmul_rn(g[e], scale);
-        mn[e] = __fadd_rn(__fmul_rn(A.beta1, m[e]), __fmul_rn(A.om1, gc));
-        const float gsq = __fmul_rn(gc, gc);
-        vn[e] = __fadd_rn(__fmul_rn(A.beta2, v[e]), __fmul_rn(A.om2, gsq));
-        mh[e] = div_fast(mn[e], A.bc1, A.rbc1);
-        vh[e] = div_fast(vn[e], A.bc2, A.rbc2);
-        bad = bad || !fast_ok(mn[e]) || !fast_ok(vn[e]);
-    }
-    if (__any_sync(0xFFFFFFFFu, bad)) {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            if (!A.fastdiv || !fast_ok(mn[e])) mh[e] = __fdiv_rn(mn[e], A.bc1);
-            if (!A.fastdiv || !fast_ok(vn[e])) vh[e] = __fdiv_rn(vn[e], A.bc2);
-        }
-    }
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-        const float denom = __fadd_rn(__fsqrt_rn(vh[e]), A.eps);
-        const float u = __fdiv_rn(mh[e], denom);
-        w[e] = __fsub_rn(__fmul_rn(w[e], A.delta), __fmul_rn(A.lr, u));
-        m[e] = mn[e];
-        v[e] = vn[e];
-    }
-}
-
-// Three 21-bit limbs of a PF61 power.
-struct Limbs {
-    uint32_t l0, l1, l2;
-};
-
-__device__ __forceinline__ Limbs limbs_of(uint64_t p)
-{
-    return {uint32_t(p & kM21), uint32_t((p >> 21) & kM21), uint32_t(p >> 42)};
-}
-
-// a += x * l as a 32 x 32 -> 64-bit multiply-add.
-__device__ __forceinline__ void mac(uint64_t &a, uint32_t x, uint32_t l)
-{
-    asm("mad.wide.u32 %0, %1, %2, %0;" : "+l"(a) : "r"(x), "r"(l));
-}
-
-struct Acc3 {
-    uint64_t a0, a1, a2;   // sum x*l0, sum x*l1, sum x*l2
-};
-
-__device__ __forceinline__ void acc_word(Acc3 &s, uint32_t x, const Limbs &p)
-{
-    mac(s.a0, x, p.l0);
-    mac(s.a1, x, p.l1);
-    mac(s.a2, x, p.l2);
-}
-
-// x * 2^e mod p for x < p and 0 <= e < 61 (2^61 == 1 mod p): a 61-bit rotation.
-__device__ __forceinline__ uint64_t pf_shl(uint64_t x, int e)
-{
-    return e == 0 ? x : (((x << e) & kP61) | (x >> (61 - e)));
-}
-
-// Bytes per element and byte offset within a stage of stream s; ws is the index of the
-// stream holding w, pt whether w is bf16.
-__host__ __device__ constexpr uint32_t stream_es(int s, int ws, int pt)
-{
-    return (s == ws && pt) ? 2u : 4u;
-}
-
-__host__ __device__ constexpr uint32_t stream_off(int s, int ws, int pt, uint32_t te)
-{
-    uint32_t o = 0;
-    for (int t = 0; t < s; ++t) o += stream_es(t, ws, pt) * te;
-    return o;
-}
-
-__device__ __forceinline__ float4 widen4(uint2 u)
-{
-    return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u),
-                       __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xFFFF0000u));
-}
-
-// A 4-element group of stream s from the staged tile.
-template <uint32_t ES>
-__device__ __forceinline__ float4 stage_group(const unsigned char *p)
-{
-    if constexpr (ES == 4) return *reinterpret_cast<const float4 *>(p);
-    else return widen4(*reinterpret_cast<const uint2 *>(p));
-}
-
-// One element of a stream from global memory (fp32, or bf16 widened exactly).
-template <uint32_t ES>
-__device__ __forceinline__ float load_one(const void *p, uint64_t e)
-{
-    if constexpr (ES == 4) return __ldg(static_cast<const float *>(p) + e);
-    else return __uint_as_float(uint32_t(__ldg(static_cast<const unsigned short *>(p) + e)) << 16);
-}
-
-// Block layout: warps 0..NT/32-1 compute, then one producer warp (TMA), then one leaf warp
-// that finishes the chunk digests from the compute warps' per-warp partial sums, so the
-// compute warps never wait for one another between chunks.
-template <int NT, int MODE, int PT>
-__global__ void __launch_bounds__(NT + 64, Shape<NT>::min_blocks)
-k_adamw(const __grid_constant__ AdamwArgs A)
-{
-    constexpr bool UPDATE = MODE != 1;           // AdamW runs (modes 0 and 2)
-    constexpr bool LEAVES = MODE != 2;           // PF61 digests (modes 0 and 1)
-    constexpr int NS = UPDATE ? 4 : 3;           // streamed arrays
-    constexpr int WS = UPDATE ? 1 : 0;           // index of the w stream
-    constexpr uint32_t VEC = PT ? 8u : 4u;       // elements per 16 bytes of the narrowest stream
-    constexpr uint32_t TE = uint32_t(kEPT) * NT;
-    constexpr int TPC = int(kChunk / TE);
-    constexpr int W = NT / 32;
-    static_assert(TPC >= 1 && TPC * TE == kChunk, "tiles divide the chunk");
-    // words per thread per chunk: limb sums stay below 32 * 2^32 * 2^21 = 2^58
-    static_assert(TPC * kEPT <= 32, "limb sums must stay below 2^58");
-
-    extern __shared__ __align__(1024) unsigned char smem[];
-    const uint32_t S = A.stages;
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem);
-    uint64_t *empty = full + kMaxStages;
-    uint64_t *leaf_full = empty + kMaxStages;
-    uint64_t *leaf_empty = leaf_full + kLeafBufs;
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(leaf_empty + kLeafBufs);
-    volatile int *never_flag = abort_flag + 1;
-    uint32_t *pieces_buf = reinterpret_cast<uint32_t *>(leaf_empty + kLeafBufs) + 4;
-    unsigned char *ring = smem + ring_offset<NT>();
-
-    const int tid = threadIdx.x;
-    if (tid == 0) {
-        for (uint32_t s = 0; s < S; ++s) {
-            mbar_init(smem_u32(&full[s]), 1);
-            mbar_init(smem_u32(&empty[s]), W);
-        }
-        for (int b = 0; b < kLeafBufs; ++b) {
-            mbar_init(smem_u32(&leaf_full[b]), W);
-            mbar_init(smem_u32(&leaf_empty[b]), 1);
-        }
-        *abort_flag = 0;
-        *never_flag = 0;
-        fence_mbar_init();
-    }
-    __syncthreads();
-
-    const uint32_t flag_bit = UPDATE ? kFlagTimeoutAdamw : kFlagTimeoutLeaves;
-    const void *src[4];
-    if (UPDATE) {
-        src[0] = A.g; src[1] = A.w; src[2] = A.m; src[3] = A.v;
-    } else {
-        src[0] = A.w; src[1] = A.m; src[2] = A.v; src[3] = nullptr;
-    }
-
-    if (tid >= NT + 32) {
-        // -------------------------------- leaf warp --------------------------------
-        if (!LEAVES) return;
-        // Chunk k's three digests from the W x 27 per-warp piece sums: lane L = (stream s,
-        // limb l, piece j) adds its piece over the warps (exact, < 2^36), weighs it by
-        // 2^(21 l + 27 j) mod p, and lanes 9s..9s+8 sum to the stream's leaf.
-        const int lane = tid - NT - 32;
-        const int ls = lane / 9, ll = (lane / 3) % 3, lj = lane % 3;
-        const int shift = (21 * ll + 27 * lj) % 61;
-        uint32_t ci = 0;
-        bool aborted = false;
-        for (uint64_t k = A.chunk_lo + blockIdx.x; k < A.chunk_hi; k += gridDim.x, ++ci) {
-            const uint32_t b = ci % kLeafBufs, round = ci / kLeafBufs;
-            if (!aborted &&
-                !mbar_wait_bounded(smem_u32(&leaf_full[b]), round & 1u, abort_flag)) {
-                aborted = true;
-                if (lane == 0) {
-                    atomicOr(&A.sc->flags, flag_bit);
-                    *abort_flag = 1;
-                }
-            }
-            uint64_t sum = 0;
-            if (lane < kPieces) {
-                const uint32_t *pb = pieces_buf + b * W * kPieces + lane;
-#pragma unroll
-                for (int w = 0; w < W; ++w) sum += pb[w * kPieces];
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&leaf_empty[b]));
-            uint64_t term = lane < kPieces ? pf_shl(pf_reduce64(sum), shift) : 0;
-#pragma unroll
-            for (int d = 1; d < 9; ++d) {
-                const uint64_t o = __shfl_sync(0xFFFFFFFFu, term, (lane + d) & 31);
-                if (lane % 9 == 0 && lane < kPieces) term = pf_add(term, o);
-            }
-            if (lane % 9 == 0 && lane < kPieces) {
-                const uint64_t c0 = k * kChunk;
-                const uint64_t c1 = c0 + kChunk < A.n ? c0 + kChunk : A.n;
-                if (c0 >= A.begin && c1 <= A.end)
-                    A.leaves[1 + uint64_t(ls) * A.c + k] = pf_add(c1 - c0, term);
-            }
-        }
-        return;
-    }
-
-    if (tid >= NT) {
-        // ------------------------------ producer warp ------------------------------
-        if (tid != NT) return;
-        const uint64_t pol = l2_evict_first();
-        uint32_t it = 0;
-        bool ok = true;
-        for (uint64_t k = A.chunk_lo + blockIdx.x; ok && k < A.chunk_hi; k += gridDim.x) {
-            for (int j = 0; j < TPC; ++j) {
-                const TileRange tr =
-                    tile_range(k * kChunk + uint64_t(j) * TE, TE, A.begin, A.end, VEC);
-                const uint32_t elems = uint32_t(tr.b16 - tr.a16);
-                const uint32_t skip = uint32_t(tr.a16 - tr.base);
-                const uint32_t slot = it % S, round = it / S;
-                if (!mbar_wait_bounded(smem_u32(&empty[slot]), (round & 1u) ^ 1u, abort_flag)) {
-                    ok = false;
-                    break;
-                }
-                const uint32_t fb = smem_u32(&full[slot]);
-                uint32_t total = 0;
-#pragma unroll
-                for (int s = 0; s < NS; ++s) total += elems * stream_es(s, WS, PT);
-                mbar_arrive_expect_tx(fb, total);
-                if (elems) {
-                    const uint32_t dst = smem_u32(ring + slot * A.stage_stride);
-#pragma unroll
-                    for (int s = 0; s < NS; ++s) {
-                        const uint32_t es = stream_es(s, WS, PT);
-                        bulk_g2s(dst + stream_off(s, WS, PT, TE) + skip * es,
-                                 static_cast<const unsigned char *>(src[s]) + tr.a16 * es,
-                                 elems * es, fb, pol);
-                    }
-                }
-                ++it;
-            }
-        }
-        if (!ok) {
-            atomicOr(&A.sc->flags, flag_bit);
-            *abort_flag = 1;
-        }
-        // never leave while copies into the ring may be in flight (bounded waits)
-        const uint32_t last = it < S ? it : S;
-        for (uint32_t d = 0; d < last; ++d) {
-            const uint32_t idx = it - 1 - d;
-            mbar_wait_bounded(smem_u32(&full[idx % S]), (idx / S) & 1u, never_flag);
-        }
-        return;
-    }
-
-    // ------------------------------ compute threads -------------------------------
-    const int lane = tid & 31, warp = tid >> 5;
-    const float scale = UPDATE ? A.sc->scale : 1.0f;
-    // the two 4-element groups of this thread within a tile
-    const uint32_t goff[2] = {4u * tid, 4u * tid + 4u * NT};
-    // with one tile per chunk, the word positions -- hence the powers -- never change
-    Limbs pw_fixed[TPC == 1 ? 8 : 1];
-    if constexpr (TPC == 1) {
-#pragma unroll
-        for (int q = 0; q < 2; ++q)
-#pragma unroll
-            for (int i = 0; i < 4; ++i) pw_fixed[q * 4 + i] = limbs_of(__ldg(A.powers + goff[q] + i));
-    }
-
-    uint32_t it = 0, ci = 0;
-    bool aborted = false;
-    for (uint64_t k = A.chunk_lo + blockIdx.x; k < A.chunk_hi; k += gridDim.x, ++ci) {
-        Acc3 acc[3] = {{0, 0, 0}, {0, 0, 0}, {0, 0, 0}};
-#pragma unroll
-        for (int j = 0; j < TPC; ++j) {
-            const TileRange tr = tile_range(k * kChunk + uint64_t(j) * TE, TE, A.begin, A.end, VEC);
-            const bool full_tile = tr.a == tr.base && tr.b == tr.base + TE;
-            const uint32_t slot = it % S, round = it / S;
-            if (!aborted && !mbar_wait_bounded(smem_u32(&full[slot]), round & 1u, abort_flag)) {
-                aborted = true;
-                if (lane == 0) {
-                    atomicOr(&A.sc->flags, flag_bit);
-                    *abort_flag = 1;
-                }
-            }
-            const unsigned char *sb = ring + slot * A.stage_stride;
-            float4 x[2][NS];
-            uint32_t inmask[2] = {0xFu, 0xFu};
-            if (full_tile) {
-#pragma unroll
-                for (int q = 0; q < 2; ++q)
-#pragma unroll
-                    for (int s = 0; s < NS; ++s) {
-                        x[q][s] = stream_es(s, WS, PT) == 4u
-                                      ? stage_group<4>(sb + stream_off(s, WS, PT, TE) + goff[q] * 4u)
-                                      : stage_group<2>(sb + stream_off(s, WS, PT, TE) + goff[q] * 2u);
-                    }
-            } else {
-#pragma unroll
-                for (int q = 0; q < 2; ++q) {
-                    const uint64_t e0 = tr.base + goff[q];
-                    const bool in_bulk = e0 >= tr.a16 && e0 + 4 <= tr.b16;
-                    uint32_t msk = 0;
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        msk |= (e0 + i >= tr.a && e0 + i < tr.b) ? (1u << i) : 0u;
-                    inmask[q] = msk;
-#pragma unroll
-                    for (int s = 0; s < NS; ++s) {
-                        const bool narrow = stream_es(s, WS, PT) == 2u;
-                        if (in_bulk) {
-                            x[q][s] = narrow
-                                ? stage_group<2>(sb + stream_off(s, WS, PT, TE) + goff[q] * 2u)
-                                : stage_group<4>(sb + stream_off(s, WS, PT, TE) + goff[q] * 4u);
-                        } else {
-                            float r[4];
-#pragma unroll
-                            for (int i = 0; i < 4; ++i)
-                                r[i] = (msk >> i) & 1u ? (narrow ? load_one<2>(src[s], e0 + i)
-                                                                 : load_one<4>(src[s], e0 + i))
-                                                       : 0.0f;
-                            x[q][s] = make_float4(r[0], r[1], r[2], r[3]);
-                        }
-                    }
-                }
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&empty[slot]));
-            ++it;
-
-            // the words hashed: the new state (MODE 0) or the given state (MODE 1)
-            float4 hw[2], hm[2], hv[2];
-            if (UPDATE) {
-                float g8[8], w8[8], m8[8], v8[8];
-#pragma unroll
-                for (int q = 0; q < 2; ++q) {
-                    g8[4 * q] = x[q][0].x; g8[4 * q + 1] = x[q][0].y; g8[4 * q + 2] = x[q][0].z; g8[4 * q + 3] = x[q][0].w;
-                    w8[4 * q] = x[q][1].x; w8[4 * q + 1] = x[q][1].y; w8[4 * q + 2] = x[q][1].z; w8[4 * q + 3] = x[q][1].w;
-                    m8[4 * q] = x[q][2].x; m8[4 * q + 1] = x[q][2].y; m8[4 * q + 2] = x[q][2].z; m8[4 * q + 3] = x[q][2].w;
-                    v8[4 * q] = x[q][3].x; v8[4 * q + 1] = x[q][3].y; v8[4 * q + 2] = x[q][3].z; v8[4 * q + 3] = x[q][3].w;
-                }
-                adamw8(g8, w8, m8, v8, scale, A);
-                if (PT) {
-                    // one rounding of the fp32 result back to bf16; the hash sees the
-                    // rounded parameter, widened exactly
-#pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        w8[e] = __bfloat162float(__float2bfloat16_rn(w8[e]));
-                }
-#pragma unroll
-                for (int q = 0; q < 2; ++q) {
-                    hw[q] = make_float4(w8[4 * q], w8[4 * q + 1], w8[4 * q + 2], w8[4 * q + 3]);
-                    hm[q] = make_float4(m8[4 * q], m8[4 * q + 1], m8[4 * q + 2], m8[4 * q + 3]);
-                    hv[q] = make_float4(v8[4 * q], v8[4 * q + 1], v8[4 * q + 2], v8[4 * q + 3]);
-                }
-            } else {
-#pragma unroll
-                for (int q = 0; q < 2; ++q) {
-                    hw[q] = x[q][0]; hm[q] = x[q][1]; hv[q] = x[q][2];
-                }
-            }
-            if (UPDATE) {
-#pragma unroll
-                for (int q = 0; q < 2; ++q) {
-                    const uint64_t e0 = tr.base + goff[q];
-                    float *W32 = static_cast<float *>(A.w);
-                    unsigned short *W16 = static_cast<unsigned short *>(A.w);
-                    if (inmask[q] == 0xFu) {
-                        if (PT) {
-                            // the widened bf16 values' top halves are the bf16 bits
-                            const uint2 u = make_uint2(
-                                (__float_as_uint(hw[q].x) >> 16) | (__float_as_uint(hw[q].y) & 0xFFFF0000u),
-                                (__float_as_uint(hw[q].z) >> 16) | (__float_as_uint(hw[q].w) & 0xFFFF0000u));
-                            *reinterpret_cast<uint2 *>(W16 + e0) = u;
-                        } else {
-                            *reinterpret_cast<float4 *>(W32 + e0) = hw[q];
-                        }
-                        *reinterpret_cast<float4 *>(A.m + e0) = hm[q];
-                        *reinterpret_cast<float4 *>(A.v + e0) = hv[q];
-                    } else {
-                        const float aw[4] = {hw[q].x, hw[q].y, hw[q].z, hw[q].w};
-                        const float am[4] = {hm[q].x, hm[q].y, hm[q].z, hm[q].w};
-                        const float av[4] = {hv[q].x, hv[q].y, hv[q].z, hv[q].w};
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            if ((inmask[q] >> i) & 1u) {
-                                if (PT) W16[e0 + i] = (unsigned short)(__float_as_uint(aw[i]) >> 16);
-                                else W32[e0 + i] = aw[i];
-                                A.m[e0 + i] = am[i];
-                                A.v[e0 + i] = av[i];
-                            }
-                        }
-                    }
-                }
-            }
-
-            // PF61 terms x * K^(pos+1) for the word positions pos = j*TE + goff[q] + i
-            if (LEAVES)
-#pragma unroll
-            for (int q = 0; q < 2; ++q) {
-                Limbs pw[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    if constexpr (TPC == 1) pw[i] = pw_fixed[q * 4 + i];
-                    else pw[i] = limbs_of(__ldg(A.powers + uint32_t(j) * TE + goff[q] + i));
-                }
-                const uint32_t wb[4] = {__float_as_uint(hw[q].x), __float_as_uint(hw[q].y),
-                                        __float_as_uint(hw[q].z), __float_as_uint(hw[q].w)};
-                const uint32_t mb[4] = {__float_as_uint(hm[q].x), __float_as_uint(hm[q].y),
-                                        __float_as_uint(hm[q].z), __float_as_uint(hm[q].w)};
-                const uint32_t vb[4] = {__float_as_uint(hv[q].x), __float_as_uint(hv[q].y),
-                                        __float_as_uint(hv[q].z), __float_as_uint(hv[q].w)};
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const uint32_t on = (inmask[q] >> i) & 1u ? 0xFFFFFFFFu : 0u;
-                    acc_word(acc[0], wb[i] & on, pw[i]);
-                    acc_word(acc[1], mb[i] & on, pw[i]);
-                    acc_word(acc[2], vb[i] & on, pw[i]);
-                }
-            }
-        }
-
-        // chunk leaves: each warp sums its lanes' limb sums exactly (27-bit pieces, so 32
-        // lanes fit in 32 bits) and hands the 27 piece sums to the leaf warp
-        if (!LEAVES) continue;
-        uint32_t part[kPieces];
-#pragma unroll
-        for (int st = 0; st < 3; ++st) {
-            const uint64_t limb[3] = {acc[st].a0, acc[st].a1, acc[st].a2};
-#pragma unroll
-            for (int l = 0; l < 3; ++l) {
-                part[(st * 3 + l) * 3 + 0] = uint32_t(limb[l]) & ((1u << 27) - 1);
-                part[(st * 3 + l) * 3 + 1] = uint32_t(limb[l] >> 27) & ((1u << 27) - 1);
-                part[(st * 3 + l) * 3 + 2] = uint32_t(limb[l] >> 54);
-            }
-        }
-#pragma unroll
-        for (int i = 0; i < kPieces; ++i) part[i] = __reduce_add_sync(0xFFFFFFFFu, part[i]);
-        if (lane == 0) {
-            const uint32_t b = ci % kLeafBufs, round = ci / kLeafBufs;
-            if (!aborted &&
-                !mbar_wait_bounded(smem_u32(&leaf_empty[b]), (round & 1u) ^ 1u, abort_flag)) {
-                aborted = true;
-                atomicOr(&A.sc->flags, flag_bit);
-                *abort_flag = 1;
-            }
-            uint32_t *pb = pieces_buf + (b * W + warp) * kPieces;
-#pragma unroll
-            for (int i = 0; i < kPieces; ++i) pb[i] = part[i];
-            mbar_arrive(smem_u32(&leaf_full[b]));
-        }
-    }
-}
 
 // Self-test of div_fast: every significand pair x, b in [1, 2) (2^23 x 2^23), with y the
 // correctly rounded reciprocal of b, against the IEEE division.  Exponents only scale the
@@ -561,22 +28,10 @@ __global__ void __launch_bounds__(256) k_selftest_div(uint32_t b_begin, uint32_t
     if (bad) atomicAdd(mismatches, bad);
 }
 
-using KernelFn = void (*)(AdamwArgs);
-
-template <int NT, int PT>
-KernelFn pick_nt(int mode)
+// The leaves-only mode has one (IEEE) instantiation; the others follow the arithmetic mode.
+AdamwKernelFn pick(const AdamwShape &s)
 {
-    return mode == 1 ? k_adamw<NT, 1, PT> : (mode == 2 ? k_adamw<NT, 2, PT> : k_adamw<NT, 0, PT>);
-}
-
-KernelFn pick(int nt, int mode, int pt)
-{
-    switch (nt) {
-    case 128: return pt ? pick_nt<128, 1>(mode) : pick_nt<128, 0>(mode);
-    case 256: return pt ? pick_nt<256, 1>(mode) : pick_nt<256, 0>(mode);
-    case 512: return pt ? pick_nt<512, 1>(mode) : pick_nt<512, 0>(mode);
-    default: return nullptr;
-    }
+    return (s.fz && s.mode != 1) ? pick_adamw_ftz(s) : pick_adamw_ieee(s);
 }
 
 uint32_t ring_off(int nt)
@@ -591,33 +46,36 @@ uint32_t ring_bytes(int nt)
 
 }  // namespace
 
-size_t adamw_smem_bytes(int nt, int mode, int pt, AdamwArgs &args)
+size_t adamw_smem_bytes(const AdamwShape &s, AdamwArgs &args)
 {
-    const uint32_t ns = mode == 1 ? 3u : 4u;
-    const uint32_t per_elem = 4u * ns - (pt ? 2u : 0u);     // w is 2 bytes when bf16
-    const uint32_t stride = per_elem * uint32_t(kEPT) * uint32_t(nt);
-    uint32_t stages = ring_bytes(nt) / stride;
+    const uint32_t ns = s.mode == 1 ? 3u : 4u;
+    const uint32_t per_elem = 4u * ns - (s.pt ? 2u : 0u);     // w is 2 bytes when bf16
+    const uint32_t te = uint32_t(kEPT) * uint32_t(s.nt);
+    // a stage holds the streams' tiles, plus the tile's decay bits when a mask is set
+    const uint32_t mask_bytes = (s.mode != 1 && s.mk) ? te / 8u : 0u;
+    const uint32_t stride = per_elem * te + mask_bytes;
+    uint32_t stages = ring_bytes(s.nt) / (per_elem * te);
     if (stages > kMaxStages) stages = kMaxStages;
     if (stages < 2) stages = 2;
     args.stages = stages;
     args.stage_stride = stride;
-    return size_t(ring_off(nt)) + size_t(stages) * stride;
+    return size_t(ring_off(s.nt)) + size_t(stages) * stride;
 }
 
-cudaError_t adamw_prepare(int nt, int mode, int pt, size_t smem)
+cudaError_t adamw_prepare(const AdamwShape &s, size_t smem)
 {
-    KernelFn f = pick(nt, mode, pt);
+    AdamwKernelFn f = pick(s);
     if (!f) return cudaErrorInvalidValue;
     return cudaFuncSetAttribute(reinterpret_cast<const void *>(f),
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
 }
 
-cudaError_t adamw_occupancy(int nt, int mode, int pt, size_t smem, int *blocks_per_sm)
+cudaError_t adamw_occupancy(const AdamwShape &s, size_t smem, int *blocks_per_sm)
 {
-    KernelFn f = pick(nt, mode, pt);
+    AdamwKernelFn f = pick(s);
     if (!f) return cudaErrorInvalidValue;
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-        blocks_per_sm, reinterpret_cast<const void *>(f), nt + 64, smem);
+        blocks_per_sm, reinterpret_cast<const void *>(f), s.nt + 64, smem);
 }
 
 cudaError_t launch_selftest_div(uint32_t b_begin, uint32_t b_count, unsigned long long *mismatches,
@@ -627,13 +85,13 @@ cudaError_t launch_selftest_div(uint32_t b_begin, uint32_t b_count, unsigned lon
     return cudaGetLastError();
 }
 
-cudaError_t launch_adamw(int nt, int mode, int pt, const AdamwArgs &args, int grid, size_t smem,
+cudaError_t launch_adamw(const AdamwShape &s, const AdamwArgs &args, int grid, size_t smem,
                          cudaStream_t st)
 {
-    KernelFn f = pick(nt, mode, pt);
+    AdamwKernelFn f = pick(s);
     if (!f) return cudaErrorInvalidValue;
     void *params[] = {const_cast<AdamwArgs *>(&args)};
-    return cudaLaunchKernel(reinterpret_cast<const void *>(f), dim3(grid), dim3(nt + 64),
+    return cudaLaunchKernel(reinterpret_cast<const void *>(f), dim3(grid), dim3(s.nt + 64),
                             params, smem, st);
 }
 

@@ -1,0 +1,415 @@
+// k_reduce.cuh -- replica reduce + per-chunk sum of squares (one HBM pass over R gradients).
+// The kernel template; k_reduce.cu instantiates the IEEE variants (FZ = 0) and holds the
+// host-side launch helpers, k_reduce_ftz.cu the software flush-to-zero variants (FZ = 1).
+//
+// Computes, for every element i of the active range,
+//     g_i = T_{r<R}(G_r[i]) * fp32(1/R)
+// with T the canonical tree over global replica index ("OPEN-1B: A Fully Auditable
+// Training Run", App. A.1: replicas paired, pairs paired again, lower replica on the
+// left; §5: a non-power-of-two count is split into its largest power-of-two block and
+// the rest; App. A.3: the average is a multiply by the reciprocal, never a divide),
+// and, for every 4096-element chunk lying wholly inside the range, the chunk's sum of
+// squares s_k = T(g_i * g_i) in the fixed perfect tree of common.cuh.
+//
+// GB300 design: a persistent grid of one CTA per SM (192 KB ring).  The last warp is the
+// producer: one lane streams tiles of TE = 4*NT elements of up to RG replicas at a time
+// from HBM into a shared-memory ring with 1-D bulk TMA copies (cp.async.bulk, L2
+// evict-first), completing on an mbarrier per stage.  The NT compute threads each take
+// one 4-element group (a 16-byte float4, or 8 bytes of bf16) per replica per tile, sum
+// the replicas in registers with a binary-carry stack that reproduces the canonical tree
+// for any R, multiply by fp32(1/R), store g with 16-byte stores and fold g*g into the
+// chunk tree.  No atomics touch data: every sum has one fixed order.  The grid size and
+// NT change which CTA does which chunk, never any rounding.
+#pragma once
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace repstep {
+
+namespace {
+
+constexpr uint32_t kRingBytes = 192 * 1024;
+constexpr uint32_t kMaxStages = 12;
+constexpr uint32_t kRingOffset = 1024;   // barriers, chunk-tree scratch and abort flag first
+
+template <int FZ>
+__device__ __forceinline__ float4 add4(float4 a, float4 b)
+{
+    return make_float4(Ar<FZ>::add(a.x, b.x), Ar<FZ>::add(a.y, b.y), Ar<FZ>::add(a.z, b.z),
+                       Ar<FZ>::add(a.w, b.w));
+}
+
+template <int FZ>
+__device__ __forceinline__ float4 mul4(float4 a, float b)
+{
+    return make_float4(Ar<FZ>::mul(a.x, b), Ar<FZ>::mul(a.y, b), Ar<FZ>::mul(a.z, b),
+                       Ar<FZ>::mul(a.w, b));
+}
+
+// Push a complete block of 2^BASE replicas, the `cnt`-th such block, onto the carry
+// stack: while the stack holds a block of the same size, combine (lower block on the
+// left) and move up a level -- binary counting, as in TreeFold.
+template <int MAXLEV, int BASE, int FZ>
+__device__ __forceinline__ void push_block(float4 (&st)[MAXLEV], uint32_t cnt, float4 a)
+{
+    bool carry = true;
+#pragma unroll
+    for (int L = BASE; L < MAXLEV; ++L) {
+        if (carry) {
+            if ((cnt >> (L - BASE)) & 1u) {
+                a = add4<FZ>(st[L], a);
+            } else {
+                st[L] = a;
+                carry = false;
+            }
+        }
+    }
+}
+
+// Canonical-tree result of `count` pushed items: the stack holds one block per set bit
+// of count (largest block = lowest replicas at the highest level).  The recursive split
+// T = T(first 2^k) + T(rest) combines them from the smallest block upward, each larger
+// (lower-replica) block on the left.
+template <int MAXLEV, int FZ>
+__device__ __forceinline__ float4 stack_result(const float4 (&st)[MAXLEV], uint32_t count)
+{
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    bool have = false;
+#pragma unroll
+    for (int L = 0; L < MAXLEV; ++L) {
+        if ((count >> L) & 1u) {
+            if (have) {
+                acc = add4<FZ>(st[L], acc);
+            } else {
+                acc = st[L];
+                have = true;
+            }
+        }
+    }
+    return acc;
+}
+
+// TreeFold's Result in the paper-exact mode: the leftover blocks, one per set bit of
+// `count`, combined starting from the largest (lowest replicas, highest level), each later
+// block added on the right.
+template <int MAXLEV, int FZ>
+__device__ __forceinline__ float4 stack_result_leftfold(const float4 (&st)[MAXLEV], uint32_t count)
+{
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    bool have = false;
+#pragma unroll
+    for (int L = MAXLEV - 1; L >= 0; --L) {
+        if ((count >> L) & 1u) {
+            if (have) {
+                acc = add4<FZ>(acc, st[L]);
+            } else {
+                acc = st[L];
+                have = true;
+            }
+        }
+    }
+    return acc;
+}
+
+template <int RG, int FZ>
+__device__ __forceinline__ float4 tree_group(float4 (&x)[RG])
+{
+#pragma unroll
+    for (int s = 1; s < RG; s <<= 1) {
+#pragma unroll
+        for (int i = 0; i < RG; i += 2 * s) x[i] = add4<FZ>(x[i], x[i + s]);
+    }
+    return x[0];
+}
+
+template <int DT>
+__device__ __forceinline__ float load_elem(const void *p, uint64_t e)
+{
+    if (DT == 0) return __ldg(static_cast<const float *>(p) + e);
+    const uint16_t b = __ldg(static_cast<const unsigned short *>(p) + e);
+    return __uint_as_float(uint32_t(b) << 16);   // bf16 -> fp32 exactly
+}
+
+template <int DT>
+__device__ __forceinline__ float4 load_group_raw(const unsigned char *tile, uint32_t off,
+                                                 bool in_bulk, const void *src, uint64_t e0,
+                                                 uint64_t a, uint64_t b)
+{
+    if (in_bulk) {
+        if (DT == 0) return *reinterpret_cast<const float4 *>(tile + off * 4u);
+        const uint2 u = *reinterpret_cast<const uint2 *>(tile + off * 2u);
+        return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u),
+                           __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xFFFF0000u));
+    }
+    float r[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint64_t e = e0 + i;
+        r[i] = (e >= a && e < b) ? load_elem<DT>(src, e) : 0.0f;
+    }
+    return make_float4(r[0], r[1], r[2], r[3]);
+}
+
+// One 4-element group of one replica: from the staged tile when the group lies in the
+// bulk-copied interior, else element by element from global memory (zero outside [a, b)).
+// In the flush-to-zero mode every value read is flushed (DAZ).
+template <int DT, int FZ>
+__device__ __forceinline__ float4 load_group(const unsigned char *tile, uint32_t off,
+                                             bool in_bulk, const void *src, uint64_t e0,
+                                             uint64_t a, uint64_t b)
+{
+    const float4 x = load_group_raw<DT>(tile, off, in_bulk, src, e0, a, b);
+    return make_float4(Ar<FZ>::in(x.x), Ar<FZ>::in(x.y), Ar<FZ>::in(x.z), Ar<FZ>::in(x.w));
+}
+
+// MODE 0: the canonical tree over all R replicas.  MODE 1: the same tree staged as a
+// cluster would run it (each node's replicas, then the node partials).  MODE 2: the
+// paper-exact order of OPEN-1B §6 Algorithm 1 (ascending shard sums times fp32(1/dp_shard),
+// TreeFold over replicas, Result times fp32(1/dp_replicate)); A.gpn = dp_shard,
+// A.nodes = dp_replicate, A.rho2 = fp32(1/dp_shard), A.rho = fp32(1/dp_replicate).  With
+// A.accum > 0 the R inputs are microbatch gradients, A.accum per virtual rank in order,
+// and each rank's gradient is the accumulation +0 + x_1*rho3 + x_2*rho3 + ... (the
+// algorithm's inner loop; rho3 = fp32(1/accum)).
+template <int NT, int DT, int MODE, int RG, int MAXLEV, int FZ>
+__global__ void __launch_bounds__(NT + 32, 1) k_reduce(const __grid_constant__ ReduceArgs A)
+{
+    constexpr int W = NT / 32;
+    constexpr uint32_t TE = 4u * NT;
+    constexpr int TPC = int(kChunk / TE);
+    constexpr uint32_t ESZ = DT == 0 ? 4u : 2u;
+    constexpr uint32_t VEC = 16u / ESZ;
+    constexpr int LOG2RG = RG == 8 ? 3 : (RG == 4 ? 2 : (RG == 2 ? 1 : 0));
+    static_assert(16 * kMaxStages + 2 * TPC * W * 4 + 8 <= kRingOffset, "smem header");
+
+    extern __shared__ __align__(1024) unsigned char smem[];
+    const uint32_t S = A.stages;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem);
+    uint64_t *empty = full + kMaxStages;
+    float *red = reinterpret_cast<float *>(smem + 16 * kMaxStages);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(red + 2 * TPC * W);
+    volatile int *never_flag = abort_flag + 1;   // stays 0: drain waits ignore the abort
+    unsigned char *ring = smem + kRingOffset;
+
+    const int tid = threadIdx.x;
+    if (tid == 0) {
+        for (uint32_t s = 0; s < S; ++s) {
+            mbar_init(smem_u32(&full[s]), 1);
+            mbar_init(smem_u32(&empty[s]), W);
+        }
+        *abort_flag = 0;
+        *never_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    const uint32_t R = A.R;
+    const uint32_t NG = (R + RG - 1) / RG;
+
+    if (tid >= NT) {
+        // ------------------------------ producer warp ------------------------------
+        if (tid != NT) return;
+        const uint64_t pol = l2_evict_first();
+        uint32_t it = 0;
+        bool ok = true;
+        for (uint64_t k = A.chunk_lo + blockIdx.x; ok && k < A.chunk_hi; k += gridDim.x) {
+            for (int j = 0; ok && j < TPC; ++j) {
+                const TileRange tr = tile_range(k * kChunk + uint64_t(j) * TE, TE, A.begin,
+                                                A.end, VEC);
+                const uint32_t bytes = uint32_t(tr.b16 - tr.a16) * ESZ;
+                const uint32_t soff = uint32_t(tr.a16 - tr.base) * ESZ;
+                for (uint32_t q = 0; q < NG; ++q) {
+                    const uint32_t slot = it % S, round = it / S;
+                    if (!mbar_wait_bounded(smem_u32(&empty[slot]), (round & 1u) ^ 1u,
+                                           abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t nr = min(uint32_t(RG), R - q * RG);
+                    const uint32_t fb = smem_u32(&full[slot]);
+                    mbar_arrive_expect_tx(fb, bytes * nr);
+                    if (bytes) {
+                        const uint32_t dst = smem_u32(ring + slot * A.stage_stride) + soff;
+                        for (uint32_t i = 0; i < nr; ++i) {
+                            const unsigned char *src =
+                                static_cast<const unsigned char *>(A.grads[q * RG + i]) +
+                                tr.a16 * ESZ;
+                            bulk_g2s(dst + i * TE * ESZ, src, bytes, fb, pol);
+                        }
+                    }
+                    ++it;
+                }
+            }
+        }
+        if (!ok) {
+            atomicOr(&A.sc->flags, kFlagTimeoutReduce);
+            *abort_flag = 1;
+        }
+        // Never leave the CTA while copies into its ring may be in flight: wait (bounded)
+        // for the most recent stage issued into every slot.
+        const uint32_t last = it < S ? it : S;
+        for (uint32_t d = 0; d < last; ++d) {
+            const uint32_t idx = it - 1 - d;
+            mbar_wait_bounded(smem_u32(&full[idx % S]), (idx / S) & 1u, never_flag);
+        }
+        return;
+    }
+
+    // ------------------------------ compute threads -------------------------------
+    const int lane = tid & 31;
+    const float rho = A.rho;
+    uint32_t it = 0;
+    int cb = 0;
+    bool aborted = false;
+    for (uint64_t k = A.chunk_lo + blockIdx.x; k < A.chunk_hi; k += gridDim.x) {
+        float part[TPC];
+#pragma unroll
+        for (int j = 0; j < TPC; ++j) {
+            const TileRange tr = tile_range(k * kChunk + uint64_t(j) * TE, TE, A.begin, A.end,
+                                            VEC);
+            const uint32_t off = 4u * tid;
+            const uint64_t e0 = tr.base + off;
+            const bool in_bulk = e0 >= tr.a16 && e0 + 4 <= tr.b16;
+            float4 st[MAXLEV];
+            float4 sto[MAXLEV];   // node partials (staged sum only)
+            float4 inner = make_float4(0.f, 0.f, 0.f, 0.f);   // running shard sum (MODE 2)
+            float4 macc = make_float4(0.f, 0.f, 0.f, 0.f);    // microbatch sum (MODE 2)
+            uint32_t c_in = 0, c_out = 0;   // position within a node / replica, and its index
+            uint32_t c_mb = 0;              // microbatch within the virtual rank (MODE 2)
+            for (uint32_t q = 0; q < NG; ++q) {
+                const uint32_t slot = it % S, round = it / S;
+                if (!aborted &&
+                    !mbar_wait_bounded(smem_u32(&full[slot]), round & 1u, abort_flag)) {
+                    aborted = true;
+                    if (lane == 0) {
+                        atomicOr(&A.sc->flags, kFlagTimeoutReduce);
+                        *abort_flag = 1;
+                    }
+                }
+                const unsigned char *sb = ring + slot * A.stage_stride;
+                const uint32_t nr = min(uint32_t(RG), R - q * RG);
+                if constexpr (MODE == 0) {
+                    float4 x[RG];
+#pragma unroll
+                    for (int i = 0; i < RG; ++i) {
+                        if (uint32_t(i) < nr)
+                            x[i] = load_group<DT, FZ>(sb + i * TE * ESZ, off, in_bulk,
+                                                  A.grads[q * RG + i], e0, tr.a, tr.b);
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&empty[slot]));
+                    ++it;
+                    if (nr == uint32_t(RG)) {
+                        push_block<MAXLEV, LOG2RG, FZ>(st, q, tree_group<RG, FZ>(x));
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < RG; ++i)
+                            if (uint32_t(i) < nr) push_block<MAXLEV, 0, FZ>(st, q * RG + i, x[i]);
+                    }
+                } else {
+                    // one replica at a time straight from the staged tile
+#pragma unroll 1
+                    for (uint32_t i = 0; i < nr; ++i) {
+                        const float4 xi = load_group<DT, FZ>(sb + i * TE * ESZ, off, in_bulk,
+                                                         A.grads[q * RG + i], e0, tr.a, tr.b);
+                        if constexpr (MODE == 2) {
+                            // microbatches of a virtual rank: g_r <- g_r + x * fp32(1/accum)
+                            // from g_r = +0 (an explicit add, so -0 becomes +0)
+                            float4 xr = xi;
+                            bool rank_ready = true;
+                            if (A.accum) {
+                                const float4 t = mul4<FZ>(xi, A.rho3);
+                                macc = add4<FZ>(c_mb == 0 ? make_float4(0.f, 0.f, 0.f, 0.f) : macc, t);
+                                rank_ready = ++c_mb == A.accum;
+                                if (rank_ready) {
+                                    c_mb = 0;
+                                    xr = macc;
+                                }
+                            }
+                            // virtual ranks in mesh order: ascending sum over a replica's
+                            // shards, times fp32(1/dp_shard), then into the TreeFold
+                            if (rank_ready) inner = c_in == 0 ? xr : add4<FZ>(inner, xr);
+                            if (rank_ready && ++c_in == A.gpn) {
+                                const float4 p = mul4<FZ>(inner, A.rho2);
+                                push_block<MAXLEV, 0, FZ>(st, c_out++, p);
+                                c_in = 0;
+                            }
+                        } else {
+                            // per node first, then over nodes (a two-level cluster reduction)
+                            push_block<MAXLEV, 0, FZ>(st, c_in, xi);
+                            if (++c_in == A.gpn) {
+                                const float4 p = stack_result<MAXLEV, FZ>(st, A.gpn);
+                                push_block<MAXLEV, 0, FZ>(sto, c_out++, p);
+                                c_in = 0;
+                            }
+                        }
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&empty[slot]));
+                    ++it;
+                }
+            }
+            float4 s;
+            if constexpr (MODE == 2) s = stack_result_leftfold<MAXLEV, FZ>(st, A.nodes);
+            else if constexpr (MODE == 1) s = stack_result<MAXLEV, FZ>(sto, A.nodes);
+            else s = stack_result<MAXLEV, FZ>(st, R);
+            const float4 gv = mul4<FZ>(s, rho);
+            const bool all_in = e0 >= tr.a && e0 + 4 <= tr.b;
+            float q4[4];
+            if (all_in) {
+                *reinterpret_cast<float4 *>(A.g + e0) = gv;
+                q4[0] = Ar<FZ>::mul(gv.x, gv.x);
+                q4[1] = Ar<FZ>::mul(gv.y, gv.y);
+                q4[2] = Ar<FZ>::mul(gv.z, gv.z);
+                q4[3] = Ar<FZ>::mul(gv.w, gv.w);
+            } else {
+                const float gg[4] = {gv.x, gv.y, gv.z, gv.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const uint64_t e = e0 + i;
+                    const bool in = e >= tr.a && e < tr.b;
+                    if (in) A.g[e] = gg[i];
+                    q4[i] = in ? Ar<FZ>::mul(gg[i], gg[i]) : 0.0f;
+                }
+            }
+            part[j] = sum4<FZ>(q4[0], q4[1], q4[2], q4[3]);
+        }
+        float *redb = red + cb * TPC * W;
+        const float total =
+            chunk_tree<NT, TPC, FZ>(part, redb, tid, [] { named_barrier(1, NT); });
+        if (tid == 0) {
+            const uint64_t c0 = k * kChunk;
+            const uint64_t c1 = c0 + kChunk < A.n ? c0 + kChunk : A.n;
+            if (c0 >= A.begin && c1 <= A.end) A.chunk_sq[k] = total;
+        }
+        cb ^= 1;
+    }
+}
+
+template <int NT, int DT, int FZ>
+ReduceKernelFn pick_dt(const ReduceShape &s)
+{
+    if (s.mode == 2)
+        return s.maxlev == 6 ? k_reduce<NT, DT, 2, 8, 6, FZ> : k_reduce<NT, DT, 2, 8, 9, FZ>;
+    if (s.mode == 1)
+        return s.maxlev == 6 ? k_reduce<NT, DT, 1, 8, 6, FZ> : k_reduce<NT, DT, 1, 8, 9, FZ>;
+    if (s.rg == 4) return k_reduce<NT, DT, 0, 4, 6, FZ>;
+    if (s.maxlev == 6) return k_reduce<NT, DT, 0, 8, 6, FZ>;
+    return k_reduce<NT, DT, 0, 8, 9, FZ>;
+}
+
+template <int FZ>
+ReduceKernelFn pick_reduce(const ReduceShape &s)
+{
+    const bool bf = s.dtype == 1;
+    switch (s.nt) {
+    case 128: return bf ? pick_dt<128, 1, FZ>(s) : pick_dt<128, 0, FZ>(s);
+    case 256: return bf ? pick_dt<256, 1, FZ>(s) : pick_dt<256, 0, FZ>(s);
+    case 512: return bf ? pick_dt<512, 1, FZ>(s) : pick_dt<512, 0, FZ>(s);
+    default: return nullptr;
+    }
+}
+
+}  // namespace
+
+}  // namespace repstep

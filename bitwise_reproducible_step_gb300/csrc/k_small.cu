@@ -28,7 +28,9 @@ struct ChunkList {
 };
 
 // Sum of squares of whole chunks of g, for chunks a range boundary cut during reduce.
-// 256 threads per chunk, the same fixed tree as the reduce kernel (common.cuh).
+// 256 threads per chunk, the same fixed tree as the reduce kernel (common.cuh), in the
+// arithmetic mode FZ.
+template <int FZ>
 __global__ void __launch_bounds__(256) k_chunk_fix(const float *g, uint64_t n, float *chunk_sq,
                                                    const ChunkList L)
 {
@@ -42,12 +44,12 @@ __global__ void __launch_bounds__(256) k_chunk_fix(const float *g, uint64_t n, f
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const uint64_t e = k * kChunk + uint64_t(j) * 1024 + 4u * tid + i;
-            const float x = e < n ? g[e] : 0.0f;
-            q[i] = e < n ? __fmul_rn(x, x) : 0.0f;
+            const float x = e < n ? Ar<FZ>::in(g[e]) : 0.0f;
+            q[i] = e < n ? Ar<FZ>::mul(x, x) : 0.0f;
         }
-        part[j] = sum4(q[0], q[1], q[2], q[3]);
+        part[j] = sum4<FZ>(q[0], q[1], q[2], q[3]);
     }
-    const float total = chunk_tree<256, 4>(part, red, tid, [] { __syncthreads(); });
+    const float total = chunk_tree<256, 4, FZ>(part, red, tid, [] { __syncthreads(); });
     if (tid == 0) chunk_sq[k] = total;
 }
 
@@ -100,6 +102,7 @@ __global__ void __launch_bounds__(256) k_leaf_fix(const void *w, int w_bf16, con
 // fixed tree; with final_pass the single block's total S gives norm = sqrt(S) and the
 // clip scale, otherwise it writes the block partial.  Zero padding leaves the canonical
 // tree of non-negative sums unchanged, so two passes equal one tree over all chunks.
+template <int FZ>
 __global__ void __launch_bounds__(256) k_norm(const float *in, uint64_t count, float *out,
                                               Scalars *sc, int final_pass, float clip,
                                               float *norm_out, float *scale_out)
@@ -114,21 +117,21 @@ __global__ void __launch_bounds__(256) k_norm(const float *in, uint64_t count, f
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const uint64_t e = base + uint64_t(j) * 1024 + 4u * tid + i;
-            q[i] = e < count ? in[e] : 0.0f;
+            q[i] = e < count ? Ar<FZ>::in(in[e]) : 0.0f;
         }
-        part[j] = sum4(q[0], q[1], q[2], q[3]);
+        part[j] = sum4<FZ>(q[0], q[1], q[2], q[3]);
     }
-    const float S = chunk_tree<256, 4>(part, red, tid, [] { __syncthreads(); });
+    const float S = chunk_tree<256, 4, FZ>(part, red, tid, [] { __syncthreads(); });
     if (tid != 0) return;
     if (!final_pass) {
         out[blockIdx.x] = S;
         return;
     }
-    const float norm = __fsqrt_rn(S);
+    const float norm = Ar<FZ>::sqrt(S);
     // OPEN-1B §3.2 clips gradients by their global l2 norm; the formula is not given.
     // Reading: scale = clip / norm when the norm exceeds the threshold, else 1 (a NaN norm
     // compares false).
-    const float scale = norm > clip ? __fdiv_rn(clip, norm) : 1.0f;
+    const float scale = norm > clip ? Ar<FZ>::div(clip, norm) : 1.0f;
     const bool finite = isfinite(norm);
     sc->norm = norm;
     sc->scale = scale;
@@ -197,12 +200,13 @@ cudaError_t launch_init_powers(uint64_t *powers, cudaStream_t st)
 }
 
 cudaError_t launch_chunk_fix(const float *g, uint64_t n, float *chunk_sq, const uint64_t *chunks,
-                             int count, cudaStream_t st)
+                             int count, int fz, cudaStream_t st)
 {
     ChunkList L{};
     for (int i = 0; i < count; ++i) L.idx[i] = chunks[i];
     L.count = count;
-    k_chunk_fix<<<count, 256, 0, st>>>(g, n, chunk_sq, L);
+    if (fz) k_chunk_fix<1><<<count, 256, 0, st>>>(g, n, chunk_sq, L);
+    else k_chunk_fix<0><<<count, 256, 0, st>>>(g, n, chunk_sq, L);
     return cudaGetLastError();
 }
 
@@ -218,10 +222,13 @@ cudaError_t launch_leaf_fix(const void *w, int w_bf16, const float *m, const flo
 }
 
 cudaError_t launch_norm(const float *in, uint64_t count, float *out, Scalars *sc, int final_pass,
-                        float clip, float *norm_out, float *scale_out, int blocks,
+                        float clip, float *norm_out, float *scale_out, int blocks, int fz,
                         cudaStream_t st)
 {
-    k_norm<<<blocks, 256, 0, st>>>(in, count, out, sc, final_pass, clip, norm_out, scale_out);
+    if (fz)
+        k_norm<1><<<blocks, 256, 0, st>>>(in, count, out, sc, final_pass, clip, norm_out, scale_out);
+    else
+        k_norm<0><<<blocks, 256, 0, st>>>(in, count, out, sc, final_pass, clip, norm_out, scale_out);
     return cudaGetLastError();
 }
 

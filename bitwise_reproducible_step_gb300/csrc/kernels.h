@@ -23,6 +23,9 @@ struct ReduceArgs {
     uint32_t stage_stride;    // bytes per stage
     float rho;                // fp32(1/R); fp32(1/dp_replicate) in the paper-exact mode
     float rho2;               // fp32(1/dp_shard) in the paper-exact mode
+    uint32_t accum;           // paper-exact mode: 0 = one gradient per virtual rank; else
+                              // microbatches per rank, accumulated from +0
+    float rho3;               // fp32(1/accum)
 };
 
 struct ReduceShape {
@@ -31,7 +34,13 @@ struct ReduceShape {
     int mode;        // 0 canonical tree, 1 topology-staged, 2 paper-exact (Algorithm 1)
     int rg;          // replicas per stage group (4 or 8)
     int maxlev;      // carry-stack depth (6 or 9)
+    int fz;          // 0 IEEE, 1 software flush-to-zero
 };
+
+using ReduceKernelFn = void (*)(ReduceArgs);
+// The instantiation for a shape, from the translation unit of its arithmetic mode.
+ReduceKernelFn pick_reduce_ieee(const ReduceShape &s);
+ReduceKernelFn pick_reduce_ftz(const ReduceShape &s);
 
 // Chooses the kernel instantiation and ring depth for a reduce; returns the dynamic
 // shared-memory bytes and fills args.stages / args.stage_stride.
@@ -55,26 +64,37 @@ struct AdamwArgs {
     float lr, beta1, beta2, eps, bc1, bc2, om1, om2, delta;
     float rbc1, rbc2;         // RN(1/bc1), RN(1/bc2): divisors fixed for the launch
     int fastdiv;              // both bias corrections in [2^-40, 2]
+    const uint32_t *decay_mask;   // null: every element decays; else bit e%32 of word e/32
 };
 
-// mode 0 AdamW + PF61 leaves, 1 leaves only, 2 AdamW only; pt 1 = bf16 parameters
-size_t adamw_smem_bytes(int nt, int mode, int pt, AdamwArgs &args);
-cudaError_t adamw_prepare(int nt, int mode, int pt, size_t smem);
-cudaError_t adamw_occupancy(int nt, int mode, int pt, size_t smem, int *blocks_per_sm);
-cudaError_t launch_adamw(int nt, int mode, int pt, const AdamwArgs &args, int grid, size_t smem,
+// The AdamW / leaf kernel variant of a launch.
+struct AdamwShape {
+    int nt;     // compute threads (128, 256, 512)
+    int mode;   // 0 AdamW + PF61 leaves, 1 leaves only, 2 AdamW only
+    int pt;     // 1: bf16 parameters
+    int fz;     // 1: software flush-to-zero arithmetic
+    int mk;     // 1: per-element weight-decay mask (args.decay_mask)
+};
+size_t adamw_smem_bytes(const AdamwShape &s, AdamwArgs &args);
+cudaError_t adamw_prepare(const AdamwShape &s, size_t smem);
+cudaError_t adamw_occupancy(const AdamwShape &s, size_t smem, int *blocks_per_sm);
+cudaError_t launch_adamw(const AdamwShape &s, const AdamwArgs &args, int grid, size_t smem,
                          cudaStream_t st);
+using AdamwKernelFn = void (*)(AdamwArgs);
+AdamwKernelFn pick_adamw_ieee(const AdamwShape &s);
+AdamwKernelFn pick_adamw_ftz(const AdamwShape &s);
 cudaError_t launch_selftest_div(uint32_t b_begin, uint32_t b_count, unsigned long long *mismatches,
                                cudaStream_t st);
 
 // Small kernels (k_small.cu).
 cudaError_t launch_init_powers(uint64_t *powers, cudaStream_t st);
 cudaError_t launch_chunk_fix(const float *g, uint64_t n, float *chunk_sq, const uint64_t *chunks,
-                             int count, cudaStream_t st);
+                             int count, int fz, cudaStream_t st);
 cudaError_t launch_leaf_fix(const void *w, int w_bf16, const float *m, const float *v, uint64_t n,
                             uint64_t c, uint64_t *leaves, const uint64_t *powers,
                             const uint64_t *chunks, int count, cudaStream_t st);
 cudaError_t launch_norm(const float *in, uint64_t count, float *out, Scalars *sc, int final_pass,
-                        float clip, float *norm_out, float *scale_out, int blocks,
+                        float clip, float *norm_out, float *scale_out, int blocks, int fz,
                         cudaStream_t st);
 cudaError_t merkle_prepare();
 cudaError_t launch_merkle(const uint64_t *in, uint64_t count, uint64_t *out, int header_mode,

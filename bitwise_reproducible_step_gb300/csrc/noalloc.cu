@@ -113,6 +113,7 @@ extern "C" int repstep_reduce_norm_noalloc(const void *const *d_grads, uint32_t 
         s.mode = 0;
         s.rg = R >= 8 ? 8 : 4;
         s.maxlev = R <= 32 ? 6 : 9;
+        s.fz = 0;
         const size_t smem = reduce_smem_bytes(s, a);
         if (reduce_prepare(s, smem) != cudaSuccess) return REPSTEP_ERR_CUDA;
         int bps = 1, dev = 0, sms = 1;
@@ -127,12 +128,12 @@ extern "C" int repstep_reduce_norm_noalloc(const void *const *d_grads, uint32_t 
     cudaError_t e;
     if (c > kChunk) {
         const int nb = int((c + kChunk - 1) / kChunk);
-        e = launch_norm(chunk_sums, c, partials, sc, 0, clip, nullptr, nullptr, nb, st);
+        e = launch_norm(chunk_sums, c, partials, sc, 0, clip, nullptr, nullptr, nb, 0, st);
         if (e == cudaSuccess)
             e = launch_norm(partials, uint64_t(nb), nullptr, sc, 1, clip, d_norm_out, d_scale_out,
-                            1, st);
+                            1, 0, st);
     } else {
-        e = launch_norm(chunk_sums, c, nullptr, sc, 1, clip, d_norm_out, d_scale_out, 1, st);
+        e = launch_norm(chunk_sums, c, nullptr, sc, 1, clip, d_norm_out, d_scale_out, 1, 0, st);
     }
     return e == cudaSuccess ? REPSTEP_OK : REPSTEP_ERR_CUDA;
 }

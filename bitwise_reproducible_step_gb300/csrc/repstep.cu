@@ -37,7 +37,8 @@ bool valid_config(const repstep_config *cfg)
     if (cfg->n > 0xFFFFFFFFull) return false;
     if (cfg->grad_dtype != REPSTEP_F32 && cfg->grad_dtype != REPSTEP_BF16) return false;
     if (cfg->param_dtype != REPSTEP_F32 && cfg->param_dtype != REPSTEP_BF16) return false;
-    if (cfg->reserved != 0) return false;
+    if (cfg->subnormals != REPSTEP_SUBNORMALS_IEEE && cfg->subnormals != REPSTEP_SUBNORMALS_FTZ)
+        return false;
     if (cfg->grid_blocks < 0) return false;
     if (cfg->block_threads != 0 && cfg->block_threads != 128 && cfg->block_threads != 256 &&
         cfg->block_threads != 512)
@@ -68,6 +69,13 @@ bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 bool finite_f(float x) { return std::isfinite(x); }
 
+// Host side of the software flush-to-zero mode: a subnormal becomes a zero of the same
+// sign (fz != 0); used for the hyperparameters and the constants derived from them.
+float hflush(int fz, float x)
+{
+    return (fz && std::fpclassify(x) == FP_SUBNORMAL) ? std::copysign(0.0f, x) : x;
+}
+
 }  // namespace
 
 struct repstep_ctx {
@@ -86,6 +94,7 @@ struct repstep_ctx {
     uint64_t updated;        // elements updated by AdamW since the last clip
     const void *sw;
     const float *sm, *sv;
+    const uint32_t *decay_mask = nullptr;     // per-element weight-decay bits (caller-owned)
     std::vector<uint64_t> cut_norm, cut_leaf;   // chunks cut by range boundaries
 
     float *g() const { return reinterpret_cast<float *>(ws + lay.g); }
@@ -96,6 +105,7 @@ struct repstep_ctx {
     uint64_t *powers() const { return reinterpret_cast<uint64_t *>(ws + lay.powers); }
     Scalars *sc() const { return reinterpret_cast<Scalars *>(ws + lay.scalars); }
     int w_bf16() const { return cfg.param_dtype == REPSTEP_BF16 ? 1 : 0; }
+    int fz() const { return cfg.subnormals == REPSTEP_SUBNORMALS_FTZ ? 1 : 0; }
     uint64_t w_bytes() const { return n * (w_bf16() ? 2 : 4); }
 
     int cuda_fail(cudaError_t e)
@@ -153,14 +163,18 @@ int check_hparams(const repstep_hparams *hp)
 
 // mode 0: canonical tree (nodes x gpn staged when nodes > 1); mode 2: paper-exact order of
 // OPEN-1B Algorithm 1 with dp_replicate = nodes and dp_shard = gpn.
+// R replicas (virtual ranks) = nodes x gpn; with accum > 0 (paper mode only) `grads`
+// holds R * accum microbatch gradients, rank-major.
 int do_reduce(repstep_ctx *x, const void *const *grads, uint32_t R, uint32_t nodes,
-              uint32_t gpn, uint64_t begin, uint64_t count, int paper = 0)
+              uint32_t gpn, uint64_t begin, uint64_t count, int paper = 0, uint32_t accum = 0)
 {
     if (!grads || R == 0) return REPSTEP_ERR_ARG;
-    if (R > kMaxReplicas) return REPSTEP_ERR_SIZE;
+    const uint64_t inputs = uint64_t(R) * (accum ? accum : 1);
+    if (inputs > kMaxReplicas) return REPSTEP_ERR_SIZE;
     if (nodes == 0 || gpn == 0 || uint64_t(nodes) * gpn != R) return REPSTEP_ERR_TOPOLOGY;
     if (!paper && nodes > 1 && (gpn & (gpn - 1)) != 0) return REPSTEP_ERR_TOPOLOGY;
     if (begin > x->n || count > x->n - begin) return REPSTEP_ERR_ARG;
+    R = uint32_t(inputs);     // the kernel streams every input
     for (uint32_t r = 0; r < R; ++r) {
         if (!grads[r]) return REPSTEP_ERR_ARG;
         if (!aligned(grads[r], 16)) return REPSTEP_ERR_ALIGN;
@@ -188,14 +202,18 @@ int do_reduce(repstep_ctx *x, const void *const *grads, uint32_t R, uint32_t nod
     a.nodes = nodes;
     a.gpn = gpn;
     const float one = 1.0f;
-    a.rho = paper ? one / float(nodes) : one / float(R);
-    a.rho2 = paper ? one / float(gpn) : one;
+    const int fz = x->fz();
+    a.rho = hflush(fz, paper ? one / float(nodes) : one / float(R));
+    a.rho2 = hflush(fz, paper ? one / float(gpn) : one);
+    a.accum = paper ? accum : 0;
+    a.rho3 = hflush(fz, accum ? one / float(accum) : one);
     ReduceShape s{};
     s.nt = x->nt_reduce;
     s.dtype = x->cfg.grad_dtype;
     s.mode = paper ? 2 : (nodes > 1 ? 1 : 0);
     s.rg = R >= 8 ? 8 : 4;
     s.maxlev = R <= 32 ? 6 : 9;
+    s.fz = fz;
     const size_t smem = reduce_smem_bytes(s, a);
     cudaError_t e = reduce_prepare(s, smem);
     if (e != cudaSuccess) return x->cuda_fail(e);
@@ -216,11 +234,14 @@ int do_clip(repstep_ctx *x, float clip, float *norm_out, float *scale_out)
     if (norm_out && !aligned(norm_out, 4)) return REPSTEP_ERR_ALIGN;
     if (scale_out && !aligned(scale_out, 4)) return REPSTEP_ERR_ALIGN;
     if (x->reduced != x->n) return REPSTEP_ERR_STATE;
+    const int fz = x->fz();
+    clip = hflush(fz, clip);
     cudaError_t e;
     unique_sort(x->cut_norm);
     for (size_t i = 0; i < x->cut_norm.size(); i += kFixMax) {
         const int cnt = int(x->cut_norm.size() - i < size_t(kFixMax) ? x->cut_norm.size() - i : kFixMax);
-        e = launch_chunk_fix(x->g(), x->n, x->chunk_sq(), x->cut_norm.data() + i, cnt, x->stream);
+        e = launch_chunk_fix(x->g(), x->n, x->chunk_sq(), x->cut_norm.data() + i, cnt, fz,
+                             x->stream);
         if (e != cudaSuccess) return x->cuda_fail(e);
         ++x->launches;
     }
@@ -229,14 +250,14 @@ int do_clip(repstep_ctx *x, float clip, float *norm_out, float *scale_out)
     if (c > kChunk) {
         const int nb = int((c + kChunk - 1) / kChunk);
         e = launch_norm(x->chunk_sq(), c, x->norm_part(), x->sc(), 0, clip, nullptr, nullptr, nb,
-                        x->stream);
+                        fz, x->stream);
         if (e != cudaSuccess) return x->cuda_fail(e);
         ++x->launches;
         e = launch_norm(x->norm_part(), uint64_t(nb), nullptr, x->sc(), 1, clip, norm_out,
-                        scale_out, 1, x->stream);
+                        scale_out, 1, fz, x->stream);
     } else {
         e = launch_norm(x->chunk_sq(), c, nullptr, x->sc(), 1, clip, norm_out, scale_out, 1,
-                        x->stream);
+                        fz, x->stream);
     }
     if (e != cudaSuccess) return x->cuda_fail(e);
     ++x->launches;
@@ -278,35 +299,39 @@ int do_adamw(repstep_ctx *x, void *w, float *m, float *v, const repstep_hparams 
     a.end = end;
     a.chunk_lo = begin / kChunk;
     a.chunk_hi = (end + kChunk - 1) / kChunk;
-    a.lr = hp->lr;
-    a.beta1 = hp->beta1;
-    a.beta2 = hp->beta2;
-    a.eps = hp->eps;
-    a.bc1 = hp->bc1;
-    a.bc2 = hp->bc2;
+    // hyperparameters and the constants derived from them, each operation flushed in the
+    // flush-to-zero mode like every device operation
+    const int fz = x->fz();
+    a.lr = hflush(fz, hp->lr);
+    a.beta1 = hflush(fz, hp->beta1);
+    a.beta2 = hflush(fz, hp->beta2);
+    a.eps = hflush(fz, hp->eps);
+    a.bc1 = hflush(fz, hp->bc1);
+    a.bc2 = hflush(fz, hp->bc2);
     const float one = 1.0f;
-    a.om1 = one - hp->beta1;
-    a.om2 = one - hp->beta2;
-    const float lrwd = hp->lr * hp->weight_decay;
-    a.delta = one - lrwd;
+    a.om1 = hflush(fz, one - a.beta1);
+    a.om2 = hflush(fz, one - a.beta2);
+    const float lrwd = hflush(fz, a.lr * hflush(fz, hp->weight_decay));
+    a.delta = hflush(fz, one - lrwd);
     // reciprocals of the bias corrections for the fixed-divisor division in k_adamw
-    a.rbc1 = one / hp->bc1;
-    a.rbc2 = one / hp->bc2;
+    a.rbc1 = one / a.bc1;
+    a.rbc2 = one / a.bc2;
     const float lo = std::ldexp(1.0f, -40), hi = 2.0f;
-    a.fastdiv = (hp->bc1 >= lo && hp->bc1 <= hi && hp->bc2 >= lo && hp->bc2 <= hi) ? 1 : 0;
+    a.fastdiv = (a.bc1 >= lo && a.bc1 <= hi && a.bc2 >= lo && a.bc2 <= hi) ? 1 : 0;
+    a.decay_mask = x->decay_mask;
     const int nt = x->nt_adamw;
     // PF61 mode: AdamW fused with the leaf digests; audit mode: AdamW alone (the BLAKE2b
     // leaves are computed from the final state by repstep_root)
     const int mode = x->cfg.hash_mode == REPSTEP_HASH_BLAKE2B ? 2 : 0;
-    const int pt = x->w_bf16();
-    const size_t smem = adamw_smem_bytes(nt, mode, pt, a);
-    cudaError_t e = adamw_prepare(nt, mode, pt, smem);
+    const AdamwShape shape{nt, mode, x->w_bf16(), fz, a.decay_mask ? 1 : 0};
+    const size_t smem = adamw_smem_bytes(shape, a);
+    cudaError_t e = adamw_prepare(shape, smem);
     if (e != cudaSuccess) return x->cuda_fail(e);
     int bps = 1;
-    e = adamw_occupancy(nt, mode, pt, smem, &bps);
+    e = adamw_occupancy(shape, smem, &bps);
     if (e != cudaSuccess) return x->cuda_fail(e);
     const int grid = grid_for(x, bps, a.chunk_hi - a.chunk_lo);
-    e = launch_adamw(nt, mode, pt, a, grid, smem, x->stream);
+    e = launch_adamw(shape, a, grid, smem, x->stream);
     if (e != cudaSuccess) return x->cuda_fail(e);
     ++x->launches;
     if (mode == 0) note_cut_chunks(x->cut_leaf, begin, end, x->n);
@@ -395,14 +420,15 @@ int do_hash(repstep_ctx *x, int32_t step, const void *w, const float *m, const f
         a.end = x->n;
         a.chunk_lo = 0;
         a.chunk_hi = x->c;
-        const int nt = x->nt_adamw, pt = x->w_bf16();
-        const size_t smem = adamw_smem_bytes(nt, 1, pt, a);
-        cudaError_t e = adamw_prepare(nt, 1, pt, smem);
+        // the leaves-only mode reads bits and does no float arithmetic: one variant
+        const AdamwShape shape{x->nt_adamw, 1, x->w_bf16(), 0, 0};
+        const size_t smem = adamw_smem_bytes(shape, a);
+        cudaError_t e = adamw_prepare(shape, smem);
         if (e != cudaSuccess) return x->cuda_fail(e);
         int bps = 1;
-        e = adamw_occupancy(nt, 1, pt, smem, &bps);
+        e = adamw_occupancy(shape, smem, &bps);
         if (e != cudaSuccess) return x->cuda_fail(e);
-        e = launch_adamw(nt, 1, pt, a, grid_for(x, bps, x->c), smem, x->stream);
+        e = launch_adamw(shape, a, grid_for(x, bps, x->c), smem, x->stream);
         if (e != cudaSuccess) return x->cuda_fail(e);
         ++x->launches;
     }
@@ -567,6 +593,15 @@ int repstep_reduce_paper(repstep_ctx *ctx, const void *const *d_grads, uint32_t 
     return do_reduce(ctx, d_grads, R, R / dp_shard, dp_shard, begin, count, 1);
 }
 
+int repstep_reduce_paper_accum(repstep_ctx *ctx, const void *const *d_grads, uint32_t R,
+                               uint32_t dp_shard, uint32_t accum, uint64_t begin, uint64_t count)
+{
+    if (!ctx) return REPSTEP_ERR_ARG;
+    if (accum == 0) return REPSTEP_ERR_ARG;
+    if (dp_shard == 0 || R % dp_shard != 0) return REPSTEP_ERR_TOPOLOGY;
+    return do_reduce(ctx, d_grads, R, R / dp_shard, dp_shard, begin, count, 1, accum);
+}
+
 int repstep_clip(repstep_ctx *ctx, float clip, float *d_norm_out, float *d_scale_out)
 {
     if (!ctx) return REPSTEP_ERR_ARG;
@@ -615,6 +650,36 @@ int repstep_step(repstep_ctx *ctx, const void *const *d_grads, uint32_t R, uint3
     rc = do_adamw(ctx, d_w, d_m, d_v, hp, 0, ctx->n);
     if (rc) return rc;
     return do_root(ctx, step, d_root_out);
+}
+
+int repstep_set_decay_mask(repstep_ctx *ctx, const uint32_t *d_mask)
+{
+    if (!ctx) return REPSTEP_ERR_ARG;
+    if (d_mask && !aligned(d_mask, 16)) return REPSTEP_ERR_ALIGN;
+    ctx->decay_mask = d_mask;
+    return REPSTEP_OK;
+}
+
+int repstep_decay_mask_from_segments(uint64_t n, const uint64_t *seg_begin, const uint8_t *decay,
+                                     uint32_t count, uint32_t *h_mask)
+{
+    if (count > 0 && (!seg_begin || !decay)) return REPSTEP_ERR_ARG;
+    if (n > 0 && !h_mask) return REPSTEP_ERR_ARG;
+    if (count == 0) return n == 0 ? REPSTEP_OK : REPSTEP_ERR_ARG;
+    if (seg_begin[0] != 0) return REPSTEP_ERR_ARG;
+    for (uint32_t s = 1; s < count; ++s)
+        if (seg_begin[s] <= seg_begin[s - 1] || seg_begin[s] >= n) return REPSTEP_ERR_ARG;
+    const uint64_t words = (n + 31) / 32;
+    std::memset(h_mask, 0, words * sizeof(uint32_t));
+    for (uint32_t s = 0; s < count; ++s) {
+        if (!decay[s]) continue;
+        const uint64_t lo = seg_begin[s], hi = s + 1 < count ? seg_begin[s + 1] : n;
+        uint64_t e = lo;
+        for (; e < hi && (e & 31); ++e) h_mask[e >> 5] |= 1u << (e & 31);      // head bits
+        for (; e + 32 <= hi; e += 32) h_mask[e >> 5] = 0xFFFFFFFFu;             // whole words
+        for (; e < hi; ++e) h_mask[e >> 5] |= 1u << (e & 31);                  // tail bits
+    }
+    return REPSTEP_OK;
 }
 
 uint64_t repstep_image_bytes(uint64_t n) { return 8 + 12 * n; }

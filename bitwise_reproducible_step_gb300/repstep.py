@@ -38,11 +38,13 @@ STATUS = {0: "REPSTEP_OK", 1: "REPSTEP_ERR_ARG", 2: "REPSTEP_ERR_ALIGN", 3: "REP
 class Config(C.Structure):
     _fields_ = [("n", C.c_uint64), ("grad_dtype", C.c_int32), ("grid_blocks", C.c_int32),
                 ("block_threads", C.c_int32), ("hash_mode", C.c_int32),
-                ("param_dtype", C.c_int32), ("reserved", C.c_int32)]
+                ("param_dtype", C.c_int32), ("subnormals", C.c_int32)]
 
 
 HASH_PF61 = 0
 HASH_BLAKE2B = 1
+SUBNORMALS_IEEE = 0
+SUBNORMALS_FTZ = 1
 
 
 class HParams(C.Structure):
@@ -69,7 +71,8 @@ EXPORTS = [
     "repstep_image_read", "repstep_bias_corrections", "repstep_sync", "repstep_launch_count",
     "repstep_last_cuda_error", "repstep_strerror", "repstep_reduce_norm_noalloc",
     "repstep_selftest_fixed_division", "repstep_reduce_paper", "repstep_checkpoint_save",
-    "repstep_checkpoint_load",
+    "repstep_checkpoint_load", "repstep_set_decay_mask", "repstep_decay_mask_from_segments",
+    "repstep_reduce_paper_accum",
 ]
 NOALLOC_MAX_N = 1 << 30
 
@@ -118,6 +121,9 @@ def lib():
     L.repstep_checkpoint_load.argtypes = [vp, C.c_char_p, C.POINTER(i32), vp, vp, vp]
     L.repstep_reduce_norm_noalloc.argtypes = [C.POINTER(vp), u32, i32, u64, C.c_float, vp, vp,
                                               vp, vp]
+    L.repstep_set_decay_mask.argtypes = [vp, vp]
+    L.repstep_reduce_paper_accum.argtypes = [vp, C.POINTER(vp), u32, u32, u32, u64, u64]
+    L.repstep_decay_mask_from_segments.argtypes = [u64, vp, vp, u32, vp]
     _lib = L
     return L
 
@@ -199,6 +205,21 @@ def selftest_fixed_division(b_sig_begin: int = 0, b_sig_count: int = 1 << 23) ->
     return int(out.item())
 
 
+def decay_mask_from_segments(n: int, segments) -> torch.Tensor:
+    """Host int32 tensor of ceil(n/32) words: the weight-decay bitmask of a segment list
+    [(begin, decays), ...] cutting [0, n) in increasing order from 0 (see
+    repstep_decay_mask_from_segments).  Upload it and pass it to Repstep.set_decay_mask."""
+    import numpy as np
+    b = np.ascontiguousarray([int(s[0]) for s in segments] or [0], dtype=np.uint64)
+    d = np.ascontiguousarray([1 if s[1] else 0 for s in segments] or [0], dtype=np.uint8)
+    out = torch.zeros(max((n + 31) // 32, 1), dtype=torch.int32)
+    _check(lib().repstep_decay_mask_from_segments(n, C.c_void_p(b.ctypes.data),
+                                                  C.c_void_p(d.ctypes.data), len(segments),
+                                                  C.c_void_p(out.data_ptr())),
+           "decay_mask_from_segments")
+    return out[:(n + 31) // 32]
+
+
 def _ptr(t: torch.Tensor | None):
     return None if t is None else C.c_void_p(t.data_ptr())
 
@@ -208,7 +229,8 @@ class Repstep:
 
     def __init__(self, n: int, grad_dtype=torch.float32, device=None, grid_blocks: int = 0,
                  block_threads: int = 0, stream: torch.cuda.Stream | None = None,
-                 hash_mode: int = HASH_PF61, param_dtype=torch.float32):
+                 hash_mode: int = HASH_PF61, param_dtype=torch.float32,
+                 subnormals: int = SUBNORMALS_IEEE):
         L = lib()
         self.n = int(n)
         self.grad_dtype = grad_dtype
@@ -217,8 +239,9 @@ class Repstep:
             else torch.device(device)
         self._fixed_stream = stream
         self.hash_mode = hash_mode
+        self.subnormals = subnormals
         self.cfg = Config(self.n, _dtype_code(grad_dtype), grid_blocks, block_threads, hash_mode,
-                          _dtype_code(param_dtype), 0)
+                          _dtype_code(param_dtype), subnormals)
         nbytes = int(L.repstep_workspace_bytes(C.byref(self.cfg)))
         if nbytes == 0:
             raise RepstepError(1, "bad configuration")
@@ -271,14 +294,23 @@ class Repstep:
         self._bind()
         _check(lib().repstep_reduce(self._ctx, arr, R, nodes, gpn, begin, count), "reduce")
 
-    def reduce_paper(self, grads, dp_shard: int, begin: int = 0, count: int | None = None):
+    def reduce_paper(self, grads, dp_shard: int, begin: int = 0, count: int | None = None,
+                     accum: int | None = None):
         """Paper-exact reduce (OPEN-1B Algorithm 1): grads are the virtual-rank gradients
-        in mesh order, R = dp_replicate * dp_shard (see repstep_reduce_paper)."""
+        in mesh order, R = dp_replicate * dp_shard (see repstep_reduce_paper).  With
+        `accum`, grads are R * accum microbatch gradients, rank-major, accumulated first
+        (repstep_reduce_paper_accum)."""
         arr, R = self._grads(grads)
         count = self.n - begin if count is None else count
         self._bind()
-        _check(lib().repstep_reduce_paper(self._ctx, arr, R, dp_shard, begin, count),
-               "reduce_paper")
+        if accum is None:
+            _check(lib().repstep_reduce_paper(self._ctx, arr, R, dp_shard, begin, count),
+                   "reduce_paper")
+            return
+        if accum < 1 or R % accum:
+            raise ValueError("the gradient count must be a multiple of accum >= 1")
+        _check(lib().repstep_reduce_paper_accum(self._ctx, arr, R // accum, dp_shard, accum,
+                                                begin, count), "reduce_paper_accum")
 
     def clip(self, clip: float, norm_out=None, scale_out=None):
         self._bind()
@@ -346,6 +378,18 @@ class Repstep:
         self.clip(hp.clip, norm_out=norm_out)
         self.adamw(w, m, v, hp)
         self.root(step, root_out=root_out)
+
+    def set_decay_mask(self, mask: torch.Tensor | None):
+        """Per-element weight decay for later adamw/step calls: a CUDA int32 tensor of
+        ceil(n/32) words from decay_mask_from_segments (bit set = decays), or None for
+        decay everywhere.  The context keeps a reference to the tensor."""
+        if mask is not None and (not mask.is_cuda or mask.dtype != torch.int32
+                                 or not mask.is_contiguous() or mask.numel() < (self.n + 31) // 32
+                                 or mask.device != self.device):
+            raise ValueError("decay mask: contiguous CUDA int32 on the context's device, "
+                             "ceil(n/32) words")
+        _check(lib().repstep_set_decay_mask(self._ctx, _ptr(mask)), "set_decay_mask")
+        self._decay_mask = mask
 
     def image_write(self, step: int, w, m, v, dst: torch.Tensor):
         self._state(w, m, v)

@@ -80,6 +80,8 @@ enum repstep_status {
 
 enum repstep_dtype { REPSTEP_F32 = 0, REPSTEP_BF16 = 1 };
 
+enum repstep_subnormals { REPSTEP_SUBNORMALS_IEEE = 0, REPSTEP_SUBNORMALS_FTZ = 1 };
+
 /* Leaf digest of the state hash.  PF61 (default) is fused into the AdamW pass and stays
  * under the HBM bound.  BLAKE2B ("audit mode") digests each leaf's image bytes with
  * BLAKE2b-64 -- the function the OPEN-1B paper hashes its steps with (App. B) -- in a
@@ -108,7 +110,13 @@ typedef struct {
                                 and rounded back to bf16 once, to nearest even (OPEN-1B
                                 §3.2, optimizer-state precision).  m and v are fp32 either
                                 way; the image and the hash hold w widened to fp32.        */
-    int32_t reserved;        /* must be 0                                                  */
+    int32_t subnormals;      /* enum repstep_subnormals: 0 IEEE gradual underflow (default);
+                                1 software flush-to-zero -- every fp32 operation of the
+                                step flushes subnormal operands and results to a zero of the
+                                same sign (OPEN-1B §2.1 "Subnormals", FTZ + DAZ), tininess
+                                judged on the rounded result.  Also the hyperparameters and
+                                the constants derived from them on the host.  Never changes
+                                the hash function, only the values hashed.               */
 } repstep_config;
 
 typedef struct {
@@ -170,6 +178,17 @@ int repstep_reduce(repstep_ctx *ctx, const void *const *d_grads, uint32_t R, uin
 int repstep_reduce_paper(repstep_ctx *ctx, const void *const *d_grads, uint32_t R,
                          uint32_t dp_shard, uint64_t begin, uint64_t count);
 
+/* Paper-exact reduce with the microbatch accumulation of OPEN-1B §6 Algorithm 1's inner
+ * loop: d_grads holds R * accum microbatch gradients, rank-major (pointer r*accum + k is
+ * microbatch k of virtual rank r, r in mesh order as above); R * accum <= 256.  Each
+ * virtual rank's gradient starts at +0 and adds its microbatches in order, each times
+ * fp32(1/accum) (App. A.3) -- an explicit add, so with accum = 1 a -0 gradient element
+ * becomes +0, the only difference from repstep_reduce_paper on the same pointers.  Then as
+ * repstep_reduce_paper.  accum = 0 is REPSTEP_ERR_ARG. */
+int repstep_reduce_paper_accum(repstep_ctx *ctx, const void *const *d_grads, uint32_t R,
+                               uint32_t dp_shard, uint32_t accum, uint64_t begin,
+                               uint64_t count);
+
 /* Global norm and clip scale (OPEN-1B §3.2, §3.4.2) from the chunk sums of the reduced g.
  * Requires the reduce calls since the previous clip to have covered exactly n elements
  * (else REPSTEP_ERR_STATE).  Writes the pre-clip norm and the scale to the optional device
@@ -185,6 +204,23 @@ int repstep_clip(repstep_ctx *ctx, float clip, float *d_norm_out, float *d_scale
  * Requires repstep_clip() since the last reduce (else REPSTEP_ERR_STATE). */
 int repstep_adamw(repstep_ctx *ctx, void *d_w, float *d_m, float *d_v,
                   const repstep_hparams *hp, uint64_t begin, uint64_t count);
+
+/* Per-segment weight decay (OPEN-1B §3.2, optimizer paragraph: the embeddings, the
+ * normalisation gains and RoPE take no weight decay).  d_mask is a device bitmask of
+ * ceil(n/32) uint32 words (16-byte aligned, caller-owned, read by every later repstep_adamw
+ * and repstep_step until replaced): bit e % 32 of word e / 32 set means element e decays,
+ * w * (1 - lr*wd); clear means it does not, w * 1 (the update with wd = 0, bit for bit).
+ * NULL (the default) makes every element decay.  Costs n/8 bytes of extra reads: the bits
+ * of each whole tile are bulk-copied into shared memory with the tile. */
+int repstep_set_decay_mask(repstep_ctx *ctx, const uint32_t *d_mask);
+
+/* Host helper (no device access): the bitmask above from a segment list.  Segment s covers
+ * [seg_begin[s], seg_begin[s+1]), the last one ends at n; seg_begin[0] must be 0 and the
+ * starts strictly increasing and below n (REPSTEP_ERR_ARG otherwise; count 0 only for
+ * n = 0).  decay[s] != 0 sets the segment's bits.  Writes all ceil(n/32) words of h_mask,
+ * bits past n zero. */
+int repstep_decay_mask_from_segments(uint64_t n, const uint64_t *seg_begin, const uint8_t *decay,
+                                     uint32_t count, uint32_t *h_mask);
 
 /* Merkle root of the state left by the repstep_adamw calls since the last clip, whose
  * ranges must total n elements (else REPSTEP_ERR_STATE); the header carries `step`.

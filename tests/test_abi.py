@@ -80,8 +80,10 @@ def test_bad_configs_rejected(L):
     assert L.repstep_workspace_bytes(C.byref(cfg)) == 0
     cfg = rs.Config(10, 0, 0, 0, 0, 2, 0)     # parameter dtype neither fp32 nor bf16
     assert L.repstep_workspace_bytes(C.byref(cfg)) == 0
-    cfg = rs.Config(10, 0, 0, 0, 0, 0, 1)     # reserved field not zero
+    cfg = rs.Config(10, 0, 0, 0, 0, 0, 2)     # subnormal mode neither IEEE nor FTZ
     assert L.repstep_workspace_bytes(C.byref(cfg)) == 0
+    cfg = rs.Config(10, 0, 0, 0, 0, 0, 1)     # software flush-to-zero: a valid mode
+    assert L.repstep_workspace_bytes(C.byref(cfg)) > 0
 
 
 def test_bf16_parameters_need_no_more_workspace(L):
@@ -109,3 +111,30 @@ def test_create_rejects_before_touching_a_device(L):
 def test_image_bytes(L):
     assert rs.image_bytes(12_800_000) == 153_600_008 == O.image_bytes(12_800_000)
     assert rs.image_bytes(3_000_000_000) == 36_000_000_008
+
+
+@pytest.mark.parametrize("n,segs", [
+    (1, [(0, True)]), (1, [(0, False)]), (31, [(0, True), (3, False), (30, True)]),
+    (32, [(0, False), (31, True)]), (33, [(0, True), (32, False)]),
+    (1000, [(0, True), (5, False), (64, True), (65, False), (100, True), (999, False)]),
+    (100_003, [(0, False), (4096, True), (4100, False), (9000, True), (70_001, False)]),
+])
+def test_decay_mask_from_segments_brute_force(L, n, segs):
+    got = rs.decay_mask_from_segments(n, segs).numpy().view(np.uint32)
+    assert got.size == (n + 31) // 32
+    want = np.zeros(got.size, np.uint32)
+    for k, (b, d) in enumerate(segs):
+        e = segs[k + 1][0] if k + 1 < len(segs) else n
+        for i in range(b, e):
+            if d:
+                want[i // 32] |= np.uint32(1 << (i % 32))
+    assert np.array_equal(got, want)
+
+
+@pytest.mark.parametrize("segs", [[(1, True)], [(0, True), (0, False)], [(0, True), (9, False), (7, True)],
+                                  [(0, True), (100, False)], []])
+def test_decay_mask_bad_segments_rejected(L, segs):
+    with pytest.raises(rs.RepstepError) as ei:
+        rs.decay_mask_from_segments(100, segs)
+    assert ei.value.code == 1
+    assert rs.decay_mask_from_segments(0, []).numel() == 0

@@ -151,6 +151,33 @@ def test_paper_exact_reduce_matches_oracle(R, dp_shard, dtype):
         assert torch.equal(b.g_view().view(torch.int32), ctx.g_view().view(torch.int32))
 
 
+@pytest.mark.parametrize("N,dp_shard,accum,dtype", [
+    (1, 1, 1, torch.float32), (1, 1, 3, torch.float32), (6, 2, 2, torch.float32),
+    (3, 3, 5, torch.float32), (12, 4, 4, torch.bfloat16), (7, 1, 6, torch.float32),
+    (8, 2, 32, torch.float32), (64, 8, 4, torch.float32),
+])
+def test_paper_exact_reduce_with_accumulation(N, dp_shard, accum, dtype):
+    """Algorithm 1 with its microbatch loop: N * accum microbatch gradients, rank-major;
+    g and the chunk sums bit-identical to the oracle.  Signed zeros are planted so the
+    +0 start of every rank's accumulation is exercised."""
+    n = 2 * 4096 + 333
+    dev = torch.device("cuda", 0)
+    ctx = rs.Repstep(n, grad_dtype=dtype, device=dev)
+    grads = U.gen_grads(n, N * accum, 1, dtype)
+    for k, x in enumerate(grads):
+        x[k % 97::97] = -0.0
+    ctx.reduce_paper(grads, dp_shard, accum=accum)
+    ctx.clip(1.0)
+    ctx.sync()
+    g = O.reduce_alg1_accum(U.oracle_grads(grads), dp_shard, accum)
+    U.assert_same_f32(ctx.g_view(), g, "g")
+    _, chunks = O.norm(g, with_chunks=True)
+    U.assert_same_f32(ctx.chunk_sums_view(), chunks, "chunk sums")
+    with pytest.raises(ValueError):
+        ctx.reduce_paper(grads[:-1], dp_shard, accum=accum) if accum > 1 else \
+            ctx.reduce_paper(grads, dp_shard, accum=0)
+
+
 def test_paper_exact_reduce_in_ranges():
     n, R, dps = 50_000, 12, 4
     dev = torch.device("cuda", 0)
