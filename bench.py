@@ -40,9 +40,10 @@ import torch  # noqa: E402
 METRIC = "params/s and HBM GB/s (% of roofline) per bit-exact reduce+clip+AdamW+hash step"
 UNIT = "params/s"
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_SOURCES = ["bitwise_reproducible_step_gb300/csrc/k_reduce.cu",
-                  "bitwise_reproducible_step_gb300/csrc/k_adamw.cu",
-                  "bitwise_reproducible_step_gb300/csrc/common.cuh"]
+KERNEL_SOURCES = ["bitwise_reproducible_step_gb300/csrc/k_reduce.cuh",
+                  "bitwise_reproducible_step_gb300/csrc/k_adamw.cuh",
+                  "bitwise_reproducible_step_gb300/csrc/common.cuh",
+                  "bitwise_reproducible_step_gb300/csrc/kernels.h"]
 
 
 def log(*a):
@@ -200,8 +201,25 @@ def run_ours(args, rank, world, local):
     log(f"[rank {rank}] generating {wl.name}: n={n:,} R={R} on {dev}")
     grads = [I.gen_grad(wl, 1, r, device=dev) for r in range(R)]
     w, m, v = I.gen_state(wl, device=dev)
+    pdt = torch.bfloat16 if args.param_dtype == "bf16" else torch.float32
+    b_w = 2 if args.param_dtype == "bf16" else 4
+    if args.param_dtype == "bf16":
+        w = w.to(torch.bfloat16)
     hash_mode = rs.HASH_BLAKE2B if args.hash_mode == "blake2b" else rs.HASH_PF61
-    ctx = rs.Repstep(n, grad_dtype=gdt, device=dev, hash_mode=hash_mode)
+    sub_mode = rs.SUBNORMALS_FTZ if args.subnormals == "ftz" else rs.SUBNORMALS_IEEE
+    ctx = rs.Repstep(n, grad_dtype=gdt, device=dev, hash_mode=hash_mode, param_dtype=pdt,
+                     subnormals=sub_mode)
+    if args.decay_mask:
+        # a transformer-like layout: no decay on the embedding (first 5%) and on a
+        # 4096-element norm gain after every 16.7M-element block of matrices
+        segs, e = [(0, False)], n // 20 | 1
+        while e < n:
+            segs.append((e, True))
+            e += 16_777_216 + 3
+            if e < n:
+                segs.append((e, False))
+                e += 4096
+        ctx.set_decay_mask(rs.decay_mask_from_segments(n, segs).to(dev))
     norm = torch.empty(1, dtype=torch.float32, device=dev)
     root = torch.empty(1, dtype=torch.int64, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -264,8 +282,9 @@ def run_ours(args, rank, world, local):
     ctx.sync()
 
     peak, peak_src = hbm_peak()
-    alg_step = (R * b_g + 24) * n
-    alg = {"reduce": (R * b_g + 4) * n, "adamw": 28 * n}
+    mask_b = 0.125 if args.decay_mask else 0.0
+    alg_step = int((R * b_g + 16 + 2 * b_w + mask_b) * n)
+    alg = {"reduce": (R * b_g + 4) * n, "adamw": int((20 + 2 * b_w + mask_b) * n)}
     dom = max(("reduce", "adamw"), key=lambda k: kms[k])
     achieved = alg[dom] / (kms[dom] * 1e-3) / 1e9
     kname = {"reduce": "k_reduce", "adamw": "k_adamw"}[dom]
@@ -278,7 +297,9 @@ def run_ours(args, rank, world, local):
     del grads
     torch.cuda.empty_cache()
     cpu = None
-    if rank == 0 and not args.skip_cpu_baseline:
+    variant = (args.param_dtype != "f32" or args.decay_mask or args.hash_mode != "pf61"
+               or args.subnormals != "ieee")
+    if rank == 0 and not args.skip_cpu_baseline and not variant:
         cpu = cpu_baseline(wl, n, R, dev, args.cpu_seconds)
 
     value = job_value(n, ms, world)
@@ -294,11 +315,13 @@ def run_ours(args, rank, world, local):
                          f"{(R * b_g + 32) * n / 1e9:.1f} GB moved per step",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "launch": "persistent grid (SM count x resident CTAs), 512 compute threads",
-                   "hash_leaves": args.hash_mode},
+                   "hash_leaves": args.hash_mode, "param_dtype": args.param_dtype,
+                   "decay_mask": bool(args.decay_mask), "subnormals": args.subnormals},
         "hbm_gbs_step": step_gbs,
         "roofline_step": {"bound": "hbm", "achieved": step_gbs, "peak": peak,
                           "unit": "GB/s", "frac": step_gbs / peak, "peak_source": peak_src,
-                          "bytes": "R*b_g*n + 24n algorithmic bytes per step"},
+                          "bytes": "R*b_g*n + (16 + 2*b_w)n (+ n/8 with a decay mask) "
+                                   "algorithmic bytes per step"},
         "roofline": {"bound": "hbm", "kernel": kname, "achieved": achieved, "peak": peak,
                      "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
                      "alg_bytes_per_launch": alg[dom], "avg_launch_ms": kms[dom],
@@ -443,6 +466,12 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--skip-cpu-baseline", action="store_true")
     ap.add_argument("--skip-e2e", action="store_true")
+    ap.add_argument("--param-dtype", choices=["f32", "bf16"], default="f32",
+                    help="parameter dtype (bf16: widened, updated in fp32, rounded once)")
+    ap.add_argument("--subnormals", choices=["ieee", "ftz"], default="ieee",
+                    help="ftz: software flush-to-zero of every operand and result")
+    ap.add_argument("--decay-mask", action="store_true",
+                    help="per-segment weight decay through a device bitmask")
     ap.add_argument("--hash-mode", choices=["pf61", "blake2b"], default="pf61",
                     help="leaf digest of the state hash (blake2b = audit mode)")
     ap.add_argument("--n", type=int, default=0,
