@@ -230,3 +230,82 @@ def test_flat268m_r32_paper_exact_order():
     ctx.sync()
     check_step_chain(ctx, g_before, s_before, w, m, v, 1, chunks, n, norm, root,
                      reducer=lambda G: O.reduce_alg1(G, dps))
+
+
+def bench_segments(n):
+    """The decay segments of the benchmark's --decay-mask: no decay on a 5% embedding and
+    on a 4096-element gain after every 16.7M-element block of matrices."""
+    segs, e = [(0, False)], n // 20 | 1
+    while e < n:
+        segs.append((e, True))
+        e += 16_777_216 + 3
+        if e < n:
+            segs.append((e, False))
+            e += 4096
+    return segs
+
+
+def local_segments(segs, lo, hi):
+    """The segment list restricted to [lo, hi), re-based to lo."""
+    starts = [b for b, _ in segs]
+    k = int(np.searchsorted(starts, lo, side="right")) - 1
+    out = [(0, segs[k][1])]
+    for b, d in segs[k + 1:]:
+        if b >= hi:
+            break
+        out.append((b - lo, d))
+    return out
+
+
+def test_flat1200m_r8_bf16w_decay_mask_ftz():
+    """The bench workload with all three optimizer variants at once -- bf16 parameters,
+    the benchmark's decay segments and software flush-to-zero -- one step, checked on
+    sampled whole chunks against the oracle's FTZ functions, the norm over all chunk sums
+    and the root over all leaves."""
+    wl = I.WORKLOADS["flat1200m_r8_segscale"]
+    n, R = wl.n, wl.R
+    dev = torch.device("cuda", 0)
+    c = (n + CH - 1) // CH
+    chunks = sample_chunks(c, k=190, seed=7)
+    segs = bench_segments(n)
+    # also sample the chunks that hold segment boundaries
+    chunks = np.array(sorted(set(chunks.tolist()) | {b // CH for b, _ in segs[1:8]}), np.int64)
+    ctx = rs.Repstep(n, device=dev, param_dtype=torch.bfloat16, subnormals=rs.SUBNORMALS_FTZ)
+    ctx.set_decay_mask(rs.decay_mask_from_segments(n, segs).to(dev))
+    w32, m, v = I.gen_state(wl, device=dev)
+    w = w32.to(torch.bfloat16)
+    del w32
+    m.copy_(I.gen_grad(wl, 9, 0, device=dev))           # non-zero moments: a mid-run step
+    v.copy_(I.gen_grad(wl, 9, 1, device=dev).square())
+    grads = [I.gen_grad(wl, 3, r, device=dev) for r in range(R)]
+    g_before = [gather(gr, chunks, n) for gr in grads]
+    s_before = (gather(w, chunks, n), gather(m, chunks, n), gather(v, chunks, n))
+    hp = U.hp_for(3)
+    norm = torch.empty(1, dtype=torch.float32, device=dev)
+    root = torch.empty(1, dtype=torch.int64, device=dev)
+    ctx.step(grads, w, m, v, hp, step=3, norm_out=norm, root_out=root)
+    assert ctx.sync() & ~rs.FLAG_NONFINITE_NORM == 0
+    chunk_sums = ctx.chunk_sums_view().cpu().numpy()
+    norm_o = O.flush(np.sqrt(O.tree_sum_ftz(chunk_sums), dtype=np.float32))
+    assert np.float32(norm.item()) == norm_o
+    scale = O.clip_scale_ftz(norm_o, U.HP["clip"])
+    bc1, bc2 = O.bias_corrections_ftz(U.HP["beta1"], U.HP["beta2"], 3)
+    leaves = ctx.leaves_view().cpu().numpy().view(np.uint64)
+    new_w, new_m, new_v = gather(w, chunks, n), gather(m, chunks, n), gather(v, chunks, n)
+    g_got = gather(ctx.g_view(), chunks, n)
+    for i, k in enumerate(chunks):
+        lo, hi = int(k) * CH, min(int(k) * CH + CH, n)
+        g = O.reduce_ftz([I.to_numpy(gr[i]) for gr in g_before])
+        U.assert_same_f32(g_got[i], g, f"g chunk {k}")
+        _, s = O.norm_ftz(g, with_chunks=True)
+        assert s.view(np.uint32)[0] == chunk_sums[k:k + 1].view(np.uint32)[0], f"chunk sum {k}"
+        w0 = I.to_numpy(s_before[0][i])
+        w1, m1, v1 = O.adamw_ftz(w0, s_before[1][i].numpy(), s_before[2][i].numpy(), g, scale,
+                                 U.HP["lr"], U.HP["beta1"], U.HP["beta2"], U.HP["eps"],
+                                 U.HP["wd"], bc1, bc2, segments=local_segments(segs, lo, hi))
+        U.assert_same_bf16(new_w[i], w1, f"w chunk {k}")
+        U.assert_same_f32(new_m[i], m1, f"m chunk {k}")
+        U.assert_same_f32(new_v[i], v1, f"v chunk {k}")
+        for a, arr in enumerate((O.widen_bf16(w1), m1, v1)):
+            assert leaves[1 + a * c + k] == O.pf61(arr.view(np.uint32)), f"leaf {a} chunk {k}"
+    assert U.root_of(root) == O.merkle_root(leaves)
