@@ -366,15 +366,32 @@ def run_e2e(args, ctx, wl, grads, w, m, v, hp, t_step, dev, R, b_g, n):
         stream.synchronize()
         return float(out_h[0:1].view(torch.float32)[0])
 
+    # the copy floor on this machine: the same bytes host-to-device with nothing else running
+    side = torch.cuda.Stream(dev)
+    floor = []
+    for _ in range(2):
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        with torch.cuda.stream(side):
+            for h, g in zip(host, grads):
+                g.copy_(h, non_blocking=True)
+        side.synchronize()
+        floor.append(time.perf_counter() - t0)
     one()
     torch.cuda.synchronize(dev)
+    per_step = []
     t0 = time.perf_counter()
     for _ in range(steps):
+        t1 = time.perf_counter()
         one()
+        per_step.append((time.perf_counter() - t1) * 1e3)
     dt = (time.perf_counter() - t0) / steps
     del host
     return {"value": n / dt, "unit": UNIT, "ms_per_step": dt * 1e3, "steps": steps,
-            "h2d_bytes_per_step": need, "d2h_bytes_per_step": 8 + 4}
+            "h2d_bytes_per_step": need, "d2h_bytes_per_step": 8 + 4,
+            "step_ms": [round(x, 2) for x in per_step],
+            "h2d_copy_floor_ms": round(min(floor) * 1e3, 2),
+            "h2d_copy_gbs": round(need / min(floor) / 1e9, 1)}
 
 
 def cpu_baseline(wl, n, R, dev, seconds):
@@ -462,7 +479,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="flat1200m_r8_segscale")
-    ap.add_argument("--e2e-steps", type=int, default=4)
+    ap.add_argument("--e2e-steps", type=int, default=6)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--skip-cpu-baseline", action="store_true")
     ap.add_argument("--skip-e2e", action="store_true")

@@ -18,7 +18,7 @@ OUT_DIR = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "librepstep.so")
 SOURCES = ["repstep.cu", "k_reduce.cu", "k_reduce_ftz.cu", "k_adamw.cu", "k_adamw_ftz.cu",
            "k_small.cu", "k_blake2b.cu", "noalloc.cu"]
-HEADERS = ["common.cuh", "kernels.h", "k_reduce.cuh", "k_adamw.cuh"]
+HEADERS = ["common.cuh", "kernels.h", "k_reduce.cuh", "k_adamw.cuh", "merkle.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + [
     "-O3", "-std=c++17", "-lineinfo", "-fmad=false", "-Xptxas=-v",

@@ -2,6 +2,7 @@
 // scale, Merkle levels, image header, and the fix-ups for chunks cut by range boundaries.
 #include "common.cuh"
 #include "kernels.h"
+#include "merkle.h"
 
 namespace repstep {
 
@@ -140,22 +141,25 @@ __global__ void __launch_bounds__(256) k_norm(const float *in, uint64_t count, f
     if (scale_out) *scale_out = scale;
 }
 
-// One Merkle block: the canonical tree over up to 4096 consecutive digests, level by level
-// (pair neighbours, carry an odd last node up unchanged), which is the same tree as the
-// recursive split T = T(first 2^k) + T(rest).  Aligned 4096-blocks are complete subtrees of
-// the whole tree, so a second pass over the block roots finishes it.  Block 0 of the leaf
-// pass computes the header leaf PF61({step, n}) itself.
+// One Merkle block: the canonical tree over up to kMerkleBlock consecutive digests, level by
+// level (pair neighbours, carry an odd last node up unchanged), which is the same tree as
+// the recursive split T = T(first 2^k) + T(rest).  Aligned power-of-two blocks are complete
+// subtrees of the whole tree (a short last block included), so further passes over the
+// block roots finish it.  1024-digest blocks give the leaf pass of a 1.2e9-parameter state
+// 859 blocks, about 5.7 per SM, where 4096-digest blocks gave 215 and left the SMs that
+// held two of them as the tail.  Block 0 of the leaf pass computes the header leaf
+// PF61({step, n}) itself.
 __global__ void __launch_bounds__(256) k_merkle(const uint64_t *in, uint64_t count, uint64_t *out,
                                                 int header_mode, uint64_t *leaves_rw,
                                                 uint32_t step, uint32_t n32,
                                                 const uint64_t *powers, Scalars *sc,
                                                 uint64_t *root_out, int final_pass)
 {
-    extern __shared__ uint64_t mk[];
-    uint64_t *buf0 = mk, *buf1 = mk + kChunk;
+    __shared__ uint64_t mk[2][kMerkleBlock];
+    uint64_t *buf0 = mk[0], *buf1 = mk[1];
     const int tid = threadIdx.x;
-    const uint64_t base = uint64_t(blockIdx.x) * kChunk;
-    uint32_t cnt = uint32_t(count - base < kChunk ? count - base : kChunk);
+    const uint64_t base = uint64_t(blockIdx.x) * kMerkleBlock;
+    uint32_t cnt = uint32_t(count - base < kMerkleBlock ? count - base : kMerkleBlock);
     for (uint32_t i = tid; i < cnt; i += blockDim.x) buf0[i] = in[base + i];
     __syncthreads();
     if (header_mode && blockIdx.x == 0 && tid == 0) {
@@ -234,19 +238,16 @@ cudaError_t launch_norm(const float *in, uint64_t count, float *out, Scalars *sc
 
 cudaError_t merkle_prepare()
 {
-    // two 4096-digest buffers: 64 KB of dynamic shared memory needs the opt-in
-    return cudaFuncSetAttribute(reinterpret_cast<const void *>(k_merkle),
-                                cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                int(2 * kChunk * sizeof(uint64_t)));
+    // two 1024-digest buffers are 16 KB of static shared memory: nothing to opt into
+    return cudaSuccess;
 }
 
 cudaError_t launch_merkle(const uint64_t *in, uint64_t count, uint64_t *out, int header_mode,
                           uint64_t *leaves_rw, uint32_t step, uint32_t n32, const uint64_t *powers,
                           Scalars *sc, uint64_t *root_out, int blocks, cudaStream_t st)
 {
-    const size_t smem = 2 * kChunk * sizeof(uint64_t);
-    k_merkle<<<blocks, 256, smem, st>>>(in, count, out, header_mode, leaves_rw, step, n32, powers,
-                                        sc, root_out, blocks == 1 ? 1 : 0);
+    k_merkle<<<blocks, 256, 0, st>>>(in, count, out, header_mode, leaves_rw, step, n32, powers,
+                                     sc, root_out, blocks == 1 ? 1 : 0);
     return cudaGetLastError();
 }
 

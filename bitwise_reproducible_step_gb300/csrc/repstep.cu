@@ -18,6 +18,7 @@
 #include "../../include/repstep.h"
 #include "common.cuh"
 #include "kernels.h"
+#include "merkle.h"
 
 using namespace repstep;
 
@@ -51,14 +52,16 @@ Layout layout_of(uint64_t n)
     const uint64_t c = (n + kChunk - 1) / kChunk;
     const uint64_t nb2 = c > kChunk ? (c + kChunk - 1) / kChunk : 1;
     const uint64_t L = 1 + 3 * c;
-    const uint64_t nb4 = (L + kChunk - 1) / kChunk;
+    // Merkle partials, ping-pong: the first pass's block roots, then the second pass's
+    const uint64_t mb1 = (L + kMerkleBlock - 1) / kMerkleBlock;
+    const uint64_t mb2 = (mb1 + kMerkleBlock - 1) / kMerkleBlock;
     Layout l{};
     uint64_t off = 0;
     l.g = off;           off = align_up(off + 4 * (n ? n : 1));
     l.chunk_sq = off;    off = align_up(off + 4 * (c ? c : 1));
     l.norm_part = off;   off = align_up(off + 4 * nb2);
     l.leaves = off;      off = align_up(off + 8 * L);
-    l.merkle_part = off; off = align_up(off + 8 * nb4);
+    l.merkle_part = off; off = align_up(off + 8 * (mb1 + mb2));
     l.powers = off;      off = align_up(off + 8 * kChunk);
     l.scalars = off;     off = align_up(off + sizeof(Scalars));
     l.total = off;
@@ -343,23 +346,27 @@ int do_adamw(repstep_ctx *x, void *w, float *m, float *v, const repstep_hparams 
 int merkle(repstep_ctx *x, int32_t step, uint64_t *root_out)
 {
     const uint64_t L = 1 + 3 * x->c;
-    const int nb = int((L + kChunk - 1) / kChunk);
-    const int header = x->cfg.hash_mode == REPSTEP_HASH_PF61 ? 1 : 0;
-    cudaError_t e;
-    if (nb == 1) {
-        e = launch_merkle(x->leaves(), L, nullptr, header, x->leaves(), uint32_t(step),
-                          uint32_t(x->n), x->powers(), x->sc(), root_out, 1, x->stream);
-    } else {
-        e = launch_merkle(x->leaves(), L, x->merkle_part(), header, x->leaves(), uint32_t(step),
-                          uint32_t(x->n), x->powers(), x->sc(), nullptr, nb, x->stream);
+    const uint64_t mb1 = (L + kMerkleBlock - 1) / kMerkleBlock;
+    // passes until one block remains; the block roots alternate between two regions (the
+    // second pass's roots fit the second region, and every later pass's fit either)
+    uint64_t *part[2] = {x->merkle_part(), x->merkle_part() + mb1};
+    const uint64_t *in = x->leaves();
+    uint64_t count = L;
+    int header = x->cfg.hash_mode == REPSTEP_HASH_PF61 ? 1 : 0;
+    for (int pass = 0;; ++pass) {
+        const uint64_t nb = (count + kMerkleBlock - 1) / kMerkleBlock;
+        const bool last = nb == 1;
+        uint64_t *out = last ? nullptr : part[pass & 1];
+        cudaError_t e = launch_merkle(in, count, out, header, x->leaves(), uint32_t(step),
+                                      uint32_t(x->n), x->powers(), x->sc(),
+                                      last ? root_out : nullptr, int(nb), x->stream);
         if (e != cudaSuccess) return x->cuda_fail(e);
         ++x->launches;
-        e = launch_merkle(x->merkle_part(), uint64_t(nb), nullptr, 0, x->leaves(), 0, 0,
-                          x->powers(), x->sc(), root_out, 1, x->stream);
+        if (last) return REPSTEP_OK;
+        in = out;
+        count = nb;
+        header = 0;
     }
-    if (e != cudaSuccess) return x->cuda_fail(e);
-    ++x->launches;
-    return REPSTEP_OK;
 }
 
 // Audit mode: BLAKE2b-64 leaves of the whole state (header included).

@@ -163,3 +163,44 @@ def test_ieee_mode_keeps_subnormals_on_the_same_inputs():
     assert U.root_of(root) == ref["root"]
     g = ctx.g_view().cpu().numpy()
     assert ((g != 0) & (np.abs(g) < np.finfo(np.float32).tiny)).any()   # subnormals survive
+
+
+@pytest.mark.parametrize("bf16w", [False, True])
+def test_ftz_audit_mode(bf16w):
+    """FTZ arithmetic with BLAKE2b-64 audit leaves (the AdamW-only kernel variant)."""
+    n, R = 3 * 4096 + 77, 4
+    pdt = torch.bfloat16 if bf16w else torch.float32
+    ctx = rs.Repstep(n, device=DEV, param_dtype=pdt, subnormals=rs.SUBNORMALS_FTZ,
+                     hash_mode=rs.HASH_BLAKE2B)
+    w, m, v = plant_state(*I.gen_state(U.F32_WL, n=n, device=DEV))
+    w = w.to(pdt)
+    ow = U.bits16(w) if bf16w else w.cpu().numpy()
+    om, ov = m.cpu().numpy(), v.cpu().numpy()
+    root = torch.empty(1, dtype=torch.int64, device=DEV)
+    grads = plant_grads(U.gen_grads(n, R, 1))
+    ctx.step(grads, w, m, v, U.hp_for(1), step=1, root_out=root)
+    ctx.sync()
+    ref = oracle_ftz_step(U.oracle_grads(grads), ow, om, ov, 1)
+    wide = O.widen_bf16(ref["w"]) if bf16w else ref["w"]
+    assert U.root_of(root) == O.state_hash(1, wide, ref["m"], ref["v"], hash_mode=1)
+    U.assert_same_f32(m, ref["m"], "m")
+
+
+@pytest.mark.parametrize("nt,grid", [(128, 0), (256, 0), (512, 7), (256, 333)])
+def test_ftz_launch_shape_invariance(nt, grid):
+    """The FTZ instantiations for every block size give the default shape's bits."""
+    n, R = 70_001, 8
+    grads = plant_grads(U.gen_grads(n, R, 2))
+    out = []
+    for kw in ({}, dict(block_threads=nt, grid_blocks=grid)):
+        ctx = rs.Repstep(n, device=DEV, subnormals=rs.SUBNORMALS_FTZ, **kw)
+        w, m, v = plant_state(*I.gen_state(U.F32_WL, n=n, device=DEV))
+        root = torch.empty(1, dtype=torch.int64, device=DEV)
+        ctx.step(grads, w, m, v, U.hp_for(2), step=2, root_out=root)
+        ctx.sync()
+        out.append((w, m, v, U.root_of(root), ctx.g_view().clone()))
+    a, b = out
+    for x, y in zip(a[:3], b[:3]):
+        assert torch.equal(x.view(torch.int32), y.view(torch.int32))
+    assert a[3] == b[3]
+    assert torch.equal(a[4].view(torch.int32), b[4].view(torch.int32))
