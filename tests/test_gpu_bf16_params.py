@@ -114,6 +114,10 @@ def test_bf16_param_adamw_on_arbitrary_bit_patterns(t):
     m[plain] = rng.standard_normal(len(m[plain])).astype(np.float32) * 1e-4
     v[plain] = np.abs(rng.standard_normal(len(v[plain]))).astype(np.float32) * 1e-8
     g[plain] = rng.standard_normal(len(g[plain])).astype(np.float32) * 1e-3
+    for a in (m, g):
+        a[7::101] = -0.0
+    w16[7::101] = 0x8000                                 # bf16 -0
+    v[7::101] = 0.0
     hp = U.hp_for(t, clip=float("inf"))
     ctx = rs.Repstep(n, device=DEV, param_dtype=torch.bfloat16)
     W = torch.from_numpy(w16.view(np.int16).copy()).view(torch.bfloat16).to(DEV)

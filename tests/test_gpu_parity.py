@@ -455,6 +455,12 @@ def test_adamw_on_arbitrary_bit_patterns(t, bc_override):
     m[::3] = rng.standard_normal(len(m[::3])).astype(np.float32) * 1e-4
     v[::3] = np.abs(rng.standard_normal(len(v[::3]))).astype(np.float32) * 1e-8
     g[::3] = rng.standard_normal(len(g[::3])).astype(np.float32) * 1e-3
+    # signed zeros where the sign of a zero quotient reaches w': w = m = g = -0, v = +0
+    # gives u = -0 and w' = -0 - lr*(-0) = +0 (a quotient of +0 would leave -0)
+    for a in (w, m, g):
+        a[7::101] = -0.0
+    v[7::101] = 0.0
+    m[9::101] = -0.0                                     # -0 moments beside normal values
     hp = U.hp_for(t, clip=float("inf"))
     if bc_override:
         hp.bc1, hp.bc2 = bc_override
