@@ -208,7 +208,7 @@ def run_ours(args, rank, world, local):
     hash_mode = rs.HASH_BLAKE2B if args.hash_mode == "blake2b" else rs.HASH_PF61
     sub_mode = rs.SUBNORMALS_FTZ if args.subnormals == "ftz" else rs.SUBNORMALS_IEEE
     ctx = rs.Repstep(n, grad_dtype=gdt, device=dev, hash_mode=hash_mode, param_dtype=pdt,
-                     subnormals=sub_mode)
+                     subnormals=sub_mode, block_threads=args.block_threads)
     if args.decay_mask:
         # a transformer-like layout: no decay on the embedding (first 5%) and on a
         # 4096-element norm gain after every 16.7M-element block of matrices
@@ -314,7 +314,8 @@ def run_ours(args, rank, world, local):
                    "l2": "inputs larger than L2 (no flush needed): "
                          f"{(R * b_g + 32) * n / 1e9:.1f} GB moved per step",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "launch": "persistent grid (SM count x resident CTAs), 512 compute threads",
+                   "launch": "persistent grid (SM count x resident CTAs), "
+                             f"{args.block_threads or 512} compute threads",
                    "hash_leaves": args.hash_mode, "param_dtype": args.param_dtype,
                    "decay_mask": bool(args.decay_mask), "subnormals": args.subnormals},
         "hbm_gbs_step": step_gbs,
@@ -491,6 +492,8 @@ def main():
                     help="per-segment weight decay through a device bitmask")
     ap.add_argument("--hash-mode", choices=["pf61", "blake2b"], default="pf61",
                     help="leaf digest of the state hash (blake2b = audit mode)")
+    ap.add_argument("--block-threads", type=int, default=0, choices=[0, 128, 256, 512],
+                    help="compute threads per CTA of the streaming kernels (0: default)")
     ap.add_argument("--n", type=int, default=0,
                     help="override the workload's parameter count (small profiling cases)")
     args = ap.parse_args()
