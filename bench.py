@@ -228,6 +228,9 @@ def run_ours(args, rank, world, local):
         return rs.hparams(lr=hpv["lr"], beta1=hpv["beta1"], beta2=hpv["beta2"], eps=hpv["eps"],
                           weight_decay=hpv["wd"], clip=hpv["clip"], t=t)
 
+    # the root passes on a second stream, beside the next step's reduce (same bits)
+    hash_side = torch.cuda.Stream(dev) if args.hash_stream else None
+    ctx.set_hash_stream(hash_side)
     t_step = [0]
 
     def one_step():
@@ -260,6 +263,7 @@ def run_ours(args, rank, world, local):
     flags = ctx.sync()
 
     # ---- per-kernel times (same calls, events between them, same stream) ------------
+    ctx.set_hash_stream(None)          # the root passes on the timed stream here
     kt = {"reduce": [], "clip": [], "adamw": [], "root": []}
     reps = max(3, min(args.steps, 20))
     for _ in range(reps):
@@ -291,6 +295,7 @@ def run_ours(args, rank, world, local):
     traffic = profiled_traffic(kname)
 
     # ---- end to end: grads from pinned host memory each step, norm+root read back ----
+    ctx.set_hash_stream(hash_side)
     e2e = None if args.skip_e2e else run_e2e(args, ctx, wl, grads, w, m, v, hp, t_step, dev,
                                               R, b_g, n)
 
@@ -317,7 +322,8 @@ def run_ours(args, rank, world, local):
                    "launch": "persistent grid (SM count x resident CTAs), "
                              f"{args.block_threads or 512} compute threads",
                    "hash_leaves": args.hash_mode, "param_dtype": args.param_dtype,
-                   "decay_mask": bool(args.decay_mask), "subnormals": args.subnormals},
+                   "decay_mask": bool(args.decay_mask), "subnormals": args.subnormals,
+                   "hash_stream": bool(args.hash_stream)},
         "hbm_gbs_step": step_gbs,
         "roofline_step": {"bound": "hbm", "achieved": step_gbs, "peak": peak,
                           "unit": "GB/s", "frac": step_gbs / peak, "peak_source": peak_src,
@@ -363,6 +369,7 @@ def run_e2e(args, ctx, wl, grads, w, m, v, hp, t_step, dev, R, b_g, n):
         ctx.step_from_host(host, grads, w, m, v, hp(t_step[0]), step=t_step[0], norm_out=nr,
                            root_out=rt)
         out_h[0:1].view(torch.float32)[0:1].copy_(nr, non_blocking=True)
+        ctx.wait_hash(stream)          # the root is read after the root passes
         out_h[1:2].copy_(rt, non_blocking=True)
         stream.synchronize()
         return float(out_h[0:1].view(torch.float32)[0])
@@ -492,6 +499,9 @@ def main():
                     help="per-segment weight decay through a device bitmask")
     ap.add_argument("--hash-mode", choices=["pf61", "blake2b"], default="pf61",
                     help="leaf digest of the state hash (blake2b = audit mode)")
+    ap.add_argument("--no-hash-stream", dest="hash_stream", action="store_false",
+                    help="run the root passes on the step's own stream (no overlap with the "
+                         "next step's reduce)")
     ap.add_argument("--block-threads", type=int, default=0, choices=[0, 128, 256, 512],
                     help="compute threads per CTA of the streaming kernels (0: default)")
     ap.add_argument("--n", type=int, default=0,

@@ -98,6 +98,11 @@ struct repstep_ctx {
     const void *sw;
     const float *sm, *sv;
     const uint32_t *decay_mask = nullptr;     // per-element weight-decay bits (caller-owned)
+    // optional second stream for the root passes (repstep_set_hash_stream): ev_state marks
+    // the state they read, ev_hash their end, which later writers of that state wait for
+    cudaStream_t hash_stream = nullptr;
+    cudaEvent_t ev_state = nullptr, ev_hash = nullptr;
+    bool hash_pending = false;
     std::vector<uint64_t> cut_norm, cut_leaf;   // chunks cut by range boundaries
 
     float *g() const { return reinterpret_cast<float *>(ws + lay.g); }
@@ -119,6 +124,17 @@ struct repstep_ctx {
 };
 
 namespace {
+
+// Order the context's stream after a root still running on the hash stream: called before
+// anything that writes the leaves, the Merkle partials or the state the root passes read.
+int join_hash(repstep_ctx *x)
+{
+    if (!x->hash_pending) return REPSTEP_OK;
+    const cudaError_t e = cudaStreamWaitEvent(x->stream, x->ev_hash, 0);
+    if (e != cudaSuccess) return x->cuda_fail(e);
+    x->hash_pending = false;
+    return REPSTEP_OK;
+}
 
 // Persistent grid: SM count x resident CTAs, never more CTAs than chunks to process.
 int grid_for(repstep_ctx *x, int blocks_per_sm, uint64_t chunks)
@@ -281,6 +297,8 @@ int do_adamw(repstep_ctx *x, void *w, float *m, float *v, const repstep_hparams 
     if (rc) return rc;
     if (begin > x->n || count > x->n - begin) return REPSTEP_ERR_ARG;
     if (!x->scale_ready) return REPSTEP_ERR_STATE;
+    rc = join_hash(x);      // the update rewrites the state and leaves a pending root reads
+    if (rc) return rc;
     if (x->sw && (x->sw != w || x->sm != m || x->sv != v)) return REPSTEP_ERR_ARG;
     x->sw = w;
     x->sm = m;
@@ -343,7 +361,7 @@ int do_adamw(repstep_ctx *x, void *w, float *m, float *v, const repstep_hparams 
 
 // Merkle root over the leaves.  In the PF61 mode the first Merkle pass computes the header
 // leaf itself; in the audit mode the leaf kernel has already written it.
-int merkle(repstep_ctx *x, int32_t step, uint64_t *root_out)
+int merkle(repstep_ctx *x, int32_t step, uint64_t *root_out, cudaStream_t st)
 {
     const uint64_t L = 1 + 3 * x->c;
     const uint64_t mb1 = (L + kMerkleBlock - 1) / kMerkleBlock;
@@ -359,7 +377,7 @@ int merkle(repstep_ctx *x, int32_t step, uint64_t *root_out)
         uint64_t *out = last ? nullptr : part[pass & 1];
         cudaError_t e = launch_merkle(in, count, out, header, x->leaves(), uint32_t(step),
                                       uint32_t(x->n), x->powers(), x->sc(),
-                                      last ? root_out : nullptr, int(nb), x->stream);
+                                      last ? root_out : nullptr, int(nb), st);
         if (e != cudaSuccess) return x->cuda_fail(e);
         ++x->launches;
         if (last) return REPSTEP_OK;
@@ -370,36 +388,58 @@ int merkle(repstep_ctx *x, int32_t step, uint64_t *root_out)
 }
 
 // Audit mode: BLAKE2b-64 leaves of the whole state (header included).
-int audit_leaves(repstep_ctx *x, int32_t step, const void *w, const float *m, const float *v)
+int audit_leaves(repstep_ctx *x, int32_t step, const void *w, const float *m, const float *v,
+                 cudaStream_t st)
 {
     cudaError_t e = launch_leaves_b2(w, x->w_bf16(), m, v, x->n, x->c, x->leaves(), uint32_t(step),
-                                     x->sm_count, x->stream);
+                                     x->sm_count, st);
     if (e != cudaSuccess) return x->cuda_fail(e);
     ++x->launches;
     return REPSTEP_OK;
 }
 
+int root_passes(repstep_ctx *x, int32_t step, uint64_t *root_out, cudaStream_t st);
+
 int do_root(repstep_ctx *x, int32_t step, uint64_t *root_out)
 {
     if (root_out && !aligned(root_out, 8)) return REPSTEP_ERR_ALIGN;
     if (!x->scale_ready || x->updated != x->n) return REPSTEP_ERR_STATE;
+    int rc = join_hash(x);
+    if (rc) return rc;
+    if (!x->hash_stream) return root_passes(x, step, root_out, x->stream);
+    // the passes wait for the state on the context's stream, then run on the hash stream;
+    // the context's stream goes on without them (join_hash orders later writers)
+    cudaError_t e = cudaEventRecord(x->ev_state, x->stream);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(x->hash_stream, x->ev_state, 0);
+    if (e != cudaSuccess) return x->cuda_fail(e);
+    rc = root_passes(x, step, root_out, x->hash_stream);
+    if (rc) return rc;
+    e = cudaEventRecord(x->ev_hash, x->hash_stream);
+    if (e != cudaSuccess) return x->cuda_fail(e);
+    x->hash_pending = true;
+    return REPSTEP_OK;
+}
+
+// The leaf fix-ups (or the audit-mode leaves) and the Merkle passes of repstep_root, on st.
+int root_passes(repstep_ctx *x, int32_t step, uint64_t *root_out, cudaStream_t st)
+{
     if (x->cfg.hash_mode == REPSTEP_HASH_BLAKE2B) {
         x->cut_leaf.clear();
-        int rc = audit_leaves(x, step, x->sw, x->sm, x->sv);
+        int rc = audit_leaves(x, step, x->sw, x->sm, x->sv, st);
         if (rc) return rc;
-        return merkle(x, step, root_out);
+        return merkle(x, step, root_out, st);
     }
     unique_sort(x->cut_leaf);
     for (size_t i = 0; i < x->cut_leaf.size(); i += kFixMax) {
         const int cnt = int(x->cut_leaf.size() - i < size_t(kFixMax) ? x->cut_leaf.size() - i : kFixMax);
         cudaError_t e = launch_leaf_fix(x->sw, x->w_bf16(), x->sm, x->sv, x->n, x->c, x->leaves(),
                                         x->powers(),
-                                        x->cut_leaf.data() + i, cnt, x->stream);
+                                        x->cut_leaf.data() + i, cnt, st);
         if (e != cudaSuccess) return x->cuda_fail(e);
         ++x->launches;
     }
     x->cut_leaf.clear();
-    return merkle(x, step, root_out);
+    return merkle(x, step, root_out, st);
 }
 
 int do_hash(repstep_ctx *x, int32_t step, const void *w, const float *m, const float *v,
@@ -408,10 +448,12 @@ int do_hash(repstep_ctx *x, int32_t step, const void *w, const float *m, const f
     if (!w || !m || !v) return REPSTEP_ERR_ARG;
     if (!aligned(w, 16) || !aligned(m, 16) || !aligned(v, 16)) return REPSTEP_ERR_ALIGN;
     if (root_out && !aligned(root_out, 8)) return REPSTEP_ERR_ALIGN;
+    int rc = join_hash(x);
+    if (rc) return rc;
     if (x->cfg.hash_mode == REPSTEP_HASH_BLAKE2B) {
-        int rc = audit_leaves(x, step, w, m, v);
+        rc = audit_leaves(x, step, w, m, v, x->stream);
         if (rc) return rc;
-        return merkle(x, step, root_out);
+        return merkle(x, step, root_out, x->stream);
     }
     if (x->n > 0) {
         AdamwArgs a{};
@@ -439,7 +481,7 @@ int do_hash(repstep_ctx *x, int32_t step, const void *w, const float *m, const f
         if (e != cudaSuccess) return x->cuda_fail(e);
         ++x->launches;
     }
-    return merkle(x, step, root_out);
+    return merkle(x, step, root_out, x->stream);
 }
 
 // ---- bf16 parameters in the fp32 image -------------------------------------------------
@@ -574,8 +616,30 @@ int repstep_create(const repstep_config *cfg, void *d_workspace, size_t workspac
 int repstep_destroy(repstep_ctx *ctx)
 {
     if (!ctx) return REPSTEP_ERR_ARG;
+    if (ctx->ev_state) cudaEventDestroy(ctx->ev_state);
+    if (ctx->ev_hash) cudaEventDestroy(ctx->ev_hash);
     delete ctx;
     return REPSTEP_OK;
+}
+
+int repstep_set_hash_stream(repstep_ctx *ctx, void *hash_stream)
+{
+    if (!ctx) return REPSTEP_ERR_ARG;
+    if (hash_stream && !ctx->ev_state) {
+        cudaError_t e = cudaEventCreateWithFlags(&ctx->ev_state, cudaEventDisableTiming);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ctx->ev_hash, cudaEventDisableTiming);
+        if (e != cudaSuccess) return ctx->cuda_fail(e);
+    }
+    ctx->hash_stream = static_cast<cudaStream_t>(hash_stream);
+    return REPSTEP_OK;
+}
+
+int repstep_wait_hash(repstep_ctx *ctx, void *stream)
+{
+    if (!ctx) return REPSTEP_ERR_ARG;
+    if (!ctx->hash_pending) return REPSTEP_OK;
+    const cudaError_t e = cudaStreamWaitEvent(static_cast<cudaStream_t>(stream), ctx->ev_hash, 0);
+    return e == cudaSuccess ? REPSTEP_OK : ctx->cuda_fail(e);
 }
 
 int repstep_set_stream(repstep_ctx *ctx, void *stream)
@@ -749,6 +813,8 @@ int repstep_image_read(repstep_ctx *ctx, const void *src, uint64_t src_bytes, in
         if (e != cudaSuccess) return ctx->cuda_fail(e);
     }
     if (uint64_t(h[1]) != n) return REPSTEP_ERR_FORMAT;
+    int rc = join_hash(ctx);      // a pending root may still read the state
+    if (rc) return rc;
     const unsigned char *s = static_cast<const unsigned char *>(src);
     // bf16 parameters: every w word of the image must be a bf16 value exactly; checked
     // before anything is copied
@@ -866,6 +932,7 @@ int repstep_checkpoint_load(repstep_ctx *ctx, const char *path, int32_t *step_ou
     if (rc == REPSTEP_OK && (std::fseek(f, 0, SEEK_SET) != 0 || std::fread(header, 4, 2, f) != 2))
         rc = REPSTEP_ERR_FORMAT;
     if (rc == REPSTEP_OK && uint64_t(header[1]) != n) rc = REPSTEP_ERR_FORMAT;
+    if (rc == REPSTEP_OK) rc = join_hash(ctx);      // a pending root may still read the state
     PinnedBuf buf;
     if (rc == REPSTEP_OK && n > 0) {
         cudaError_t e = cudaMallocHost(&buf.p, kIoChunk);
@@ -932,7 +999,9 @@ int repstep_sync(repstep_ctx *ctx, uint32_t *flags_out)
 {
     if (!ctx) return REPSTEP_ERR_ARG;
     cudaError_t e = cudaStreamSynchronize(ctx->stream);
+    if (e == cudaSuccess && ctx->hash_pending) e = cudaEventSynchronize(ctx->ev_hash);
     if (e != cudaSuccess) return ctx->cuda_fail(e);
+    ctx->hash_pending = false;
     Scalars s;
     e = cudaMemcpy(&s, ctx->sc(), sizeof s, cudaMemcpyDeviceToHost);
     if (e != cudaSuccess) return ctx->cuda_fail(e);

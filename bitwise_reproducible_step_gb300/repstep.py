@@ -72,7 +72,7 @@ EXPORTS = [
     "repstep_last_cuda_error", "repstep_strerror", "repstep_reduce_norm_noalloc",
     "repstep_selftest_fixed_division", "repstep_reduce_paper", "repstep_checkpoint_save",
     "repstep_checkpoint_load", "repstep_set_decay_mask", "repstep_decay_mask_from_segments",
-    "repstep_reduce_paper_accum",
+    "repstep_reduce_paper_accum", "repstep_set_hash_stream", "repstep_wait_hash",
 ]
 NOALLOC_MAX_N = 1 << 30
 
@@ -122,6 +122,8 @@ def lib():
     L.repstep_reduce_norm_noalloc.argtypes = [C.POINTER(vp), u32, i32, u64, C.c_float, vp, vp,
                                               vp, vp]
     L.repstep_set_decay_mask.argtypes = [vp, vp]
+    L.repstep_set_hash_stream.argtypes = [vp, vp]
+    L.repstep_wait_hash.argtypes = [vp, vp]
     L.repstep_reduce_paper_accum.argtypes = [vp, C.POINTER(vp), u32, u32, u32, u64, u64]
     L.repstep_decay_mask_from_segments.argtypes = [u64, vp, vp, u32, vp]
     _lib = L
@@ -378,6 +380,20 @@ class Repstep:
         self.clip(hp.clip, norm_out=norm_out)
         self.adamw(w, m, v, hp)
         self.root(step, root_out=root_out)
+
+    def set_hash_stream(self, stream: torch.cuda.Stream | None):
+        """Run the root passes on `stream`, beside the next step's work on the context's
+        stream (see repstep_set_hash_stream); None returns to one stream.  The root output
+        is complete after wait_hash() or sync()."""
+        _check(lib().repstep_set_hash_stream(
+            self._ctx, None if stream is None else C.c_void_p(stream.cuda_stream)),
+            "set_hash_stream")
+        self._hash_stream = stream
+
+    def wait_hash(self, stream: torch.cuda.Stream | None = None):
+        """Make `stream` (default: the current stream) wait for the pending root passes."""
+        st = stream or torch.cuda.current_stream(self.device)
+        _check(lib().repstep_wait_hash(self._ctx, C.c_void_p(st.cuda_stream)), "wait_hash")
 
     def set_decay_mask(self, mask: torch.Tensor | None):
         """Per-element weight decay for later adamw/step calls: a CUDA int32 tensor of

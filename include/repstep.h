@@ -151,6 +151,26 @@ int repstep_destroy(repstep_ctx *ctx);
 /* Change the stream later calls enqueue on. */
 int repstep_set_stream(repstep_ctx *ctx, void *stream);
 
+/* Optional second stream for the state hash (NULL, the default: none).  When set,
+ * repstep_root (and the root of repstep_step) waits on the hash stream for the work
+ * already on the context's stream, then runs its passes there: the leaf fix-ups of cut
+ * chunks (or the audit-mode leaves) and the Merkle passes.  The context's stream does not
+ * wait for them, so the next step's reduce overlaps them; it is the ALU-bound hash beside
+ * an HBM-bound reduce.  The bits are the same either way.
+ * Ordering, handled by the library: the next call that writes the leaves or the state
+ * (repstep_adamw, repstep_step, repstep_hash, repstep_root, repstep_image_read,
+ * repstep_checkpoint_load) first makes the context's stream wait for the pending passes.
+ * Ordering left to the caller: d_root_out is complete when the hash stream reaches the
+ * end of the passes -- order a stream after them with repstep_wait_hash, or call
+ * repstep_sync, which waits for both streams -- and w, m, v must not be written by other
+ * code until then, because the leaf fix-ups and the audit leaves read them.
+ * Creates two CUDA events on first use (host resources; no device memory). */
+int repstep_set_hash_stream(repstep_ctx *ctx, void *hash_stream);
+
+/* Make `stream` wait for the root passes last enqueued on the hash stream (no-op when none
+ * is pending). */
+int repstep_wait_hash(repstep_ctx *ctx, void *stream);
+
 /* Replica reduce (OPEN-1B App. A.1 and A.3) over the element range [begin, begin+count):
  * g_i = T_{r<R}(G_r[i]) * fp32(1/R) into the workspace, plus the sum of squares of every
  * 4096-chunk lying wholly inside the range.  d_grads is a HOST array of R device pointers
@@ -280,8 +300,8 @@ int repstep_checkpoint_load(repstep_ctx *ctx, const char *path, int32_t *step_ou
  * bc_j = 1 - p_j (the reading taken for AdamW's bias correction; computed on the host). */
 void repstep_bias_corrections(float beta1, float beta2, int32_t t, float *bc1, float *bc2);
 
-/* Synchronise the context's stream and read the device flags (REPSTEP_FLAG_*; nullable
- * output).  Returns REPSTEP_ERR_CUDA if the stream reported an error, REPSTEP_ERR_TIMEOUT
+/* Synchronise the context's stream (and the pending root passes of the hash stream, if
+ * any) and read the device flags (REPSTEP_FLAG_*; nullable output).  Returns REPSTEP_ERR_CUDA if the stream reported an error, REPSTEP_ERR_TIMEOUT
  * if a kernel's bounded wait expired, else REPSTEP_OK.  Clears the timeout flags. */
 int repstep_sync(repstep_ctx *ctx, uint32_t *flags_out);
 
