@@ -215,6 +215,32 @@ def test_empty_parameter_vector():
     assert U.root_of(root) == O.state_hash(1, e, e, e, hash_mode=1)
 
 
+@pytest.mark.parametrize("kw", [dict(param_dtype=torch.bfloat16), dict(subnormals=rs.SUBNORMALS_FTZ),
+                                dict(hash_mode=rs.HASH_BLAKE2B, param_dtype=torch.bfloat16,
+                                     subnormals=rs.SUBNORMALS_FTZ)])
+def test_empty_parameter_vector_every_mode(kw):
+    """n = 0 in the bf16-parameter, FTZ and audit modes, with a decay mask and the hash on
+    a second stream: the root of the empty state, nothing launched over elements."""
+    dev = torch.device("cuda", 0)
+    ctx = rs.Repstep(0, device=dev, **kw)
+    ctx.set_decay_mask(rs.decay_mask_from_segments(0, []).to(dev))
+    ctx.set_hash_stream(torch.cuda.Stream(dev))
+    pdt = kw.get("param_dtype", torch.float32)
+    w = torch.zeros(1, dtype=pdt, device=dev)
+    z = torch.zeros(1, dtype=torch.float32, device=dev)
+    grads = [torch.zeros(1, dtype=torch.float32, device=dev)] * 3
+    norm = torch.empty(1, dtype=torch.float32, device=dev)
+    root = torch.empty(1, dtype=torch.int64, device=dev)
+    ctx.step(grads, w, z.clone(), z.clone(), U.hp_for(1), step=1, norm_out=norm, root_out=root)
+    ctx.sync()
+    e = np.zeros(0, np.float32)
+    assert float(norm.item()) == 0.0
+    assert U.root_of(root) == O.state_hash(1, e, e, e, hash_mode=kw.get("hash_mode", 0))
+    ctx.reduce_paper(grads, 1, accum=3)
+    ctx.clip(1.0)
+    ctx.sync()
+
+
 @pytest.mark.parametrize("nt", [128, 256, 512])
 def test_launch_shape_invariance(nt):
     n, R = 7 * 4096 * 5 + 333, 8
