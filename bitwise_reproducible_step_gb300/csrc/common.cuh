@@ -173,6 +173,26 @@ struct TileRange {
     uint64_t base, a, b, a16, b16;
 };
 
+// The range of a tile that lies wholly inside the active range (every chunk of the range
+// but the two at its ends).
+__device__ __forceinline__ TileRange whole_tile(uint64_t base, uint32_t te)
+{
+    return TileRange{base, base, base + te, base, base + te};
+}
+
+// Position in a ring of S stages: the slot and the parity of its current round, advanced
+// without the division that it % S and it / S would cost per stage.
+struct RingPos {
+    uint32_t slot = 0, phase = 0;
+    __device__ __forceinline__ void advance(uint32_t S)
+    {
+        if (++slot == S) {
+            slot = 0;
+            phase ^= 1u;
+        }
+    }
+};
+
 __device__ __forceinline__ TileRange tile_range(uint64_t base, uint32_t te, uint64_t lo,
                                                 uint64_t hi, uint32_t vec)
 {

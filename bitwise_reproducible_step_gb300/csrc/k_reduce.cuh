@@ -211,16 +211,19 @@ __global__ void __launch_bounds__(NT + 32, 1) k_reduce(const __grid_constant__ R
         if (tid != NT) return;
         const uint64_t pol = l2_evict_first();
         uint32_t it = 0;
+        RingPos pos;
         bool ok = true;
         for (uint64_t k = A.chunk_lo + blockIdx.x; ok && k < A.chunk_hi; k += gridDim.x) {
+            const bool whole = k * kChunk >= A.begin && k * kChunk + kChunk <= A.end;
             for (int j = 0; ok && j < TPC; ++j) {
-                const TileRange tr = tile_range(k * kChunk + uint64_t(j) * TE, TE, A.begin,
-                                                A.end, VEC);
+                const uint64_t tb = k * kChunk + uint64_t(j) * TE;
+                const TileRange tr = whole ? whole_tile(tb, TE)
+                                           : tile_range(tb, TE, A.begin, A.end, VEC);
                 const uint32_t bytes = uint32_t(tr.b16 - tr.a16) * ESZ;
                 const uint32_t soff = uint32_t(tr.a16 - tr.base) * ESZ;
                 for (uint32_t q = 0; q < NG; ++q) {
-                    const uint32_t slot = it % S, round = it / S;
-                    if (!mbar_wait_bounded(smem_u32(&empty[slot]), (round & 1u) ^ 1u,
+                    const uint32_t slot = pos.slot;
+                    if (!mbar_wait_bounded(smem_u32(&empty[slot]), pos.phase ^ 1u,
                                            abort_flag)) {
                         ok = false;
                         break;
@@ -238,6 +241,7 @@ __global__ void __launch_bounds__(NT + 32, 1) k_reduce(const __grid_constant__ R
                         }
                     }
                     ++it;
+                    pos.advance(S);
                 }
             }
         }
@@ -258,15 +262,16 @@ __global__ void __launch_bounds__(NT + 32, 1) k_reduce(const __grid_constant__ R
     // ------------------------------ compute threads -------------------------------
     const int lane = tid & 31;
     const float rho = A.rho;
-    uint32_t it = 0;
+    RingPos pos;
     int cb = 0;
     bool aborted = false;
     for (uint64_t k = A.chunk_lo + blockIdx.x; k < A.chunk_hi; k += gridDim.x) {
         float part[TPC];
+        const bool whole = k * kChunk >= A.begin && k * kChunk + kChunk <= A.end;
 #pragma unroll
         for (int j = 0; j < TPC; ++j) {
-            const TileRange tr = tile_range(k * kChunk + uint64_t(j) * TE, TE, A.begin, A.end,
-                                            VEC);
+            const uint64_t tb = k * kChunk + uint64_t(j) * TE;
+            const TileRange tr = whole ? whole_tile(tb, TE) : tile_range(tb, TE, A.begin, A.end, VEC);
             const uint32_t off = 4u * tid;
             const uint64_t e0 = tr.base + off;
             const bool in_bulk = e0 >= tr.a16 && e0 + 4 <= tr.b16;
@@ -277,9 +282,9 @@ __global__ void __launch_bounds__(NT + 32, 1) k_reduce(const __grid_constant__ R
             uint32_t c_in = 0, c_out = 0;   // position within a node / replica, and its index
             uint32_t c_mb = 0;              // microbatch within the virtual rank (MODE 2)
             for (uint32_t q = 0; q < NG; ++q) {
-                const uint32_t slot = it % S, round = it / S;
+                const uint32_t slot = pos.slot;
                 if (!aborted &&
-                    !mbar_wait_bounded(smem_u32(&full[slot]), round & 1u, abort_flag)) {
+                    !mbar_wait_bounded(smem_u32(&full[slot]), pos.phase, abort_flag)) {
                     aborted = true;
                     if (lane == 0) {
                         atomicOr(&A.sc->flags, kFlagTimeoutReduce);
@@ -290,16 +295,28 @@ __global__ void __launch_bounds__(NT + 32, 1) k_reduce(const __grid_constant__ R
                 const uint32_t nr = min(uint32_t(RG), R - q * RG);
                 if constexpr (MODE == 0) {
                     float4 x[RG];
+                    if (whole && nr == uint32_t(RG)) {
+                        // a whole tile of a full group: every value is in the staged tile
 #pragma unroll
-                    for (int i = 0; i < RG; ++i) {
-                        if (uint32_t(i) < nr)
-                            x[i] = load_group<DT, FZ>(sb + i * TE * ESZ, off, in_bulk,
-                                                  A.grads[q * RG + i], e0, tr.a, tr.b);
+                        for (int i = 0; i < RG; ++i)
+                            x[i] = load_group<DT, FZ>(sb + i * TE * ESZ, off, true, nullptr, 0,
+                                                      0, 0);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < RG; ++i) {
+                            if (uint32_t(i) < nr)
+                                x[i] = load_group<DT, FZ>(sb + i * TE * ESZ, off, in_bulk,
+                                                          A.grads[q * RG + i], e0, tr.a, tr.b);
+                        }
                     }
                     __syncwarp();
                     if (lane == 0) mbar_arrive(smem_u32(&empty[slot]));
-                    ++it;
-                    if (nr == uint32_t(RG)) {
+                    pos.advance(S);
+                    if (R == uint32_t(RG)) {
+                        // one full group: the carry stack would hold exactly this block at
+                        // level log2(RG) and return it
+                        st[LOG2RG] = tree_group<RG, FZ>(x);
+                    } else if (nr == uint32_t(RG)) {
                         push_block<MAXLEV, LOG2RG, FZ>(st, q, tree_group<RG, FZ>(x));
                     } else {
 #pragma unroll
@@ -346,13 +363,13 @@ __global__ void __launch_bounds__(NT + 32, 1) k_reduce(const __grid_constant__ R
                     }
                     __syncwarp();
                     if (lane == 0) mbar_arrive(smem_u32(&empty[slot]));
-                    ++it;
+                    pos.advance(S);
                 }
             }
             float4 s;
             if constexpr (MODE == 2) s = stack_result_leftfold<MAXLEV, FZ>(st, A.nodes);
             else if constexpr (MODE == 1) s = stack_result<MAXLEV, FZ>(sto, A.nodes);
-            else s = stack_result<MAXLEV, FZ>(st, R);
+            else s = R == uint32_t(RG) ? st[LOG2RG] : stack_result<MAXLEV, FZ>(st, R);
             const float4 gv = mul4<FZ>(s, rho);
             const bool all_in = e0 >= tr.a && e0 + 4 <= tr.b;
             float q4[4];
