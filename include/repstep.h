@@ -3,10 +3,12 @@
  *
  * One optimizer step is: sum R replica gradients in one canonical tree and average them by
  * a reciprocal multiply; compute the global l2 norm over fixed 4096-element chunks; clip;
- * apply AdamW to flat fp32 weights and Adam moments; hash the checkpoint image
- * [int32 step][uint32 n][w][m][v] with per-chunk digests combined in a Merkle tree.  Every
- * output bit is fixed by the definition below, independent of the launch configuration,
- * of how replicas are grouped into nodes, and of how the parameter range is split.
+ * apply AdamW to flat weights (fp32, or bf16 updated in fp32) and fp32 Adam moments; hash
+ * the checkpoint image [int32 step][uint32 n][w][m][v] with per-chunk digests combined in
+ * a Merkle tree.  Every output bit is fixed by the definition below, independent of the
+ * launch configuration, of how replicas are grouped into nodes, and of how the parameter
+ * range is split.  Options: per-segment weight decay, a software flush-to-zero mode, the
+ * paper-exact reduction order of OPEN-1B's audit replay, and the hash on a second stream.
  *
  * Sources, by page title and section:
  *   "OPEN-1B: A Fully Auditable Training Run" (Gensyn): §2.1 Reproducible Operations
@@ -20,7 +22,8 @@
  *     both moments, canonical element order independent of topology).
  *
  * Definitions (every fp32 operation is IEEE binary32 round-to-nearest-even, rounded once,
- * never contracted into a fused multiply-add; subnormals are kept):
+ * never contracted into a fused multiply-add; subnormals are kept, unless the context's
+ * subnormal mode is REPSTEP_SUBNORMALS_FTZ, which flushes every operand and result):
  *   T(x_0..x_{L-1})  canonical tree: x_0 if L == 1, else T(x_0..x_{k-1}) + T(x_k..x_{L-1})
  *                    with k the largest power of two below L; lower indices on the left.
  *   reduce           g_i = T_{r<R}(G_r[i]) * fp32(1/R); bf16 gradients widened exactly.
@@ -29,7 +32,9 @@
  *   clip             scale = norm > clip ? clip / norm : 1.
  *   AdamW            gc = g*scale; m' = b1*m + (1-b1)*gc; v' = b2*v + (1-b2)*(gc*gc);
  *                    u = (m'/bc1) / (sqrt(v'/bc2) + eps); w' = w*(1 - lr*wd) - lr*u,
- *                    with 1-b1, 1-b2 and 1-lr*wd each rounded to fp32 once.
+ *                    with 1-b1, 1-b2 and 1-lr*wd each rounded to fp32 once; wd = 0 for
+ *                    elements a decay mask excludes; a bf16 w is widened first and w'
+ *                    rounded to bf16 (nearest even) once.
  *   hash             leaves: PF61(header words {step, n}), then PF61 of each 4096-element
  *                    chunk of w, of m, of v (as 32-bit words); PF61(x_0..x_{W-1}) =
  *                    (W + sum x_i K^(i+1)) mod (2^61-1), K = floor(2^61 (sqrt5 - 1) / 2).
