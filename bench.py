@@ -233,9 +233,24 @@ def run_ours(args, rank, world, local):
     ctx.set_hash_stream(hash_side)
     t_step = [0]
 
+    def reduce_only():
+        # the paper-exact order (Algorithm 1) when asked for, else the canonical tree
+        if args.paper_shard:
+            ctx.reduce_paper(grads, args.paper_shard, accum=args.accum or None)
+        else:
+            ctx.reduce(grads, nodes=args.nodes)
+
     def one_step():
         t_step[0] += 1
-        ctx.step(grads, w, m, v, hp(t_step[0]), step=t_step[0], norm_out=norm, root_out=root)
+        if not args.paper_shard:
+            ctx.step(grads, w, m, v, hp(t_step[0]), step=t_step[0], norm_out=norm, root_out=root,
+                     nodes=args.nodes)
+            return
+        h = hp(t_step[0])
+        reduce_only()
+        ctx.clip(h.clip, norm_out=norm)
+        ctx.adamw(w, m, v, h)
+        ctx.root(t_step[0], root_out=root)
 
     # warm-up
     for _ in range(args.warmup):
@@ -271,7 +286,7 @@ def run_ours(args, rank, world, local):
         ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
         h = hp(t_step[0])
         ev[0].record(stream)
-        ctx.reduce(grads)
+        reduce_only()
         ev[1].record(stream)
         ctx.clip(h.clip, norm_out=norm)
         ev[2].record(stream)
@@ -303,7 +318,7 @@ def run_ours(args, rank, world, local):
     torch.cuda.empty_cache()
     cpu = None
     variant = (args.param_dtype != "f32" or args.decay_mask or args.hash_mode != "pf61"
-               or args.subnormals != "ieee")
+               or args.subnormals != "ieee" or bool(args.paper_shard) or args.nodes > 1)
     if rank == 0 and not args.skip_cpu_baseline and not variant:
         cpu = cpu_baseline(wl, n, R, dev, args.cpu_seconds)
 
@@ -323,7 +338,12 @@ def run_ours(args, rank, world, local):
                              f"{args.block_threads or 512} compute threads",
                    "hash_leaves": args.hash_mode, "param_dtype": args.param_dtype,
                    "decay_mask": bool(args.decay_mask), "subnormals": args.subnormals,
-                   "hash_stream": bool(args.hash_stream)},
+                   "hash_stream": bool(args.hash_stream),
+                   "reduce_order": (f"paper-exact, dp_shard {args.paper_shard}"
+                                    + (f", accum {args.accum}" if args.accum else "")
+                                    if args.paper_shard else
+                                    "canonical tree" + (f", staged over {args.nodes} nodes"
+                                                        if args.nodes > 1 else ""))},
         "hbm_gbs_step": step_gbs,
         "roofline_step": {"bound": "hbm", "achieved": step_gbs, "peak": peak,
                           "unit": "GB/s", "frac": step_gbs / peak, "peak_source": peak_src,
@@ -502,6 +522,12 @@ def main():
     ap.add_argument("--no-hash-stream", dest="hash_stream", action="store_false",
                     help="run the root passes on the step's own stream (no overlap with the "
                          "next step's reduce)")
+    ap.add_argument("--nodes", type=int, default=1,
+                    help="stage the canonical reduce over this many nodes (same bits)")
+    ap.add_argument("--paper-shard", type=int, default=0,
+                    help="reduce in the paper-exact order (Algorithm 1) with this dp_shard")
+    ap.add_argument("--accum", type=int, default=0,
+                    help="with --paper-shard: the replicas are microbatches, accum per rank")
     ap.add_argument("--block-threads", type=int, default=0, choices=[0, 128, 256, 512],
                     help="compute threads per CTA of the streaming kernels (0: default)")
     ap.add_argument("--n", type=int, default=0,

@@ -67,6 +67,45 @@ __device__ __forceinline__ void push_block(float4 (&st)[MAXLEV], uint32_t cnt, f
     }
 }
 
+// The same push for the paper-exact mode, where every virtual rank's partial is pushed on
+// its own.  The number of carries is the number of trailing one bits of cnt, the same for
+// every thread of the warp, so a switch runs exactly those folds as straight-line code
+// instead of a predicated pass over every level.  fold_carries<L0, K> computes
+// a = st[L0] + a, then st[L0+1] + a, ... K times, and stores the result at level L0 + K:
+// the order of push_block.  (The other modes keep push_block: with two stacks live, as in
+// the staged mode, the switch's code raises register spills.)
+template <int L0, int K, int MAXLEV, int FZ>
+__device__ __forceinline__ void fold_carries(float4 (&st)[MAXLEV], float4 a)
+{
+    if constexpr (K == 0) st[L0] = a;
+    else fold_carries<L0 + 1, K - 1, MAXLEV, FZ>(st, add4<FZ>(st[L0], a));
+}
+
+#define REPSTEP_PUSH_CASE(K)                                                              \
+    case K:                                                                               \
+        if constexpr (K < MAXLEV) fold_carries<0, K, MAXLEV, FZ>(st, a);                   \
+        break;
+
+template <int MAXLEV, int FZ>
+__device__ __forceinline__ void push_one_switched(float4 (&st)[MAXLEV], uint32_t cnt, float4 a)
+{
+    const uint32_t carries = uint32_t(__ffs(int(~cnt))) - 1u;   // trailing ones of cnt
+    switch (carries) {
+        REPSTEP_PUSH_CASE(0)
+        REPSTEP_PUSH_CASE(1)
+        REPSTEP_PUSH_CASE(2)
+        REPSTEP_PUSH_CASE(3)
+        REPSTEP_PUSH_CASE(4)
+        REPSTEP_PUSH_CASE(5)
+        REPSTEP_PUSH_CASE(6)
+        REPSTEP_PUSH_CASE(7)
+        REPSTEP_PUSH_CASE(8)
+    default: break;
+    }
+}
+
+#undef REPSTEP_PUSH_CASE
+
 // Canonical-tree result of `count` pushed items: the stack holds one block per set bit
 // of count (largest block = lowest replicas at the highest level).  The recursive split
 // T = T(first 2^k) + T(rest) combines them from the smallest block upward, each larger
@@ -348,7 +387,7 @@ __global__ void __launch_bounds__(NT + 32, 1) k_reduce(const __grid_constant__ R
                             if (rank_ready) inner = c_in == 0 ? xr : add4<FZ>(inner, xr);
                             if (rank_ready && ++c_in == A.gpn) {
                                 const float4 p = mul4<FZ>(inner, A.rho2);
-                                push_block<MAXLEV, 0, FZ>(st, c_out++, p);
+                                push_one_switched<MAXLEV, FZ>(st, c_out++, p);
                                 c_in = 0;
                             }
                         } else {
