@@ -38,7 +38,8 @@ def diff_report(got, want):
     both_nan = np.isnan(g) & np.isnan(w)
     differing = int(np.count_nonzero((gb != wb) & ~both_nan))
     fin = np.isfinite(g) & np.isfinite(w)
-    d = np.where(fin, g - w, 0.0)
+    with np.errstate(invalid="ignore"):          # inf - inf in the slots fin excludes
+        d = np.where(fin, g - w, 0.0)
     den = np.linalg.norm(np.where(fin, w, 0.0))
     rel = float(np.linalg.norm(d) / den) if den > 0 else float(np.linalg.norm(d))
     mx = float(np.max(np.abs(d))) if d.size else 0.0
