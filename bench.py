@@ -40,10 +40,18 @@ import torch  # noqa: E402
 METRIC = "params/s and HBM GB/s (% of roofline) per bit-exact reduce+clip+AdamW+hash step"
 UNIT = "params/s"
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_SOURCES = ["bitwise_reproducible_step_gb300/csrc/k_reduce.cuh",
-                  "bitwise_reproducible_step_gb300/csrc/k_adamw.cuh",
-                  "bitwise_reproducible_step_gb300/csrc/common.cuh",
-                  "bitwise_reproducible_step_gb300/csrc/kernels.h"]
+_CSRC = "bitwise_reproducible_step_gb300/csrc/"
+# the sources each profiled kernel is built from: a traffic figure recorded under their
+# hash stays valid until one of them changes
+KERNEL_SOURCES = {k: [_CSRC + f for f in (src, "common.cuh", "kernels.h")]
+                  for k, src in (("k_reduce", "k_reduce.cuh"), ("k_adamw", "k_adamw.cuh"),
+                                 ("k_leaves_b2", "k_blake2b.cu"))}
+# BLAKE2b-64 leaves (audit mode) are bound by the SM's integer ALU pipe: per 128-byte block,
+# 12 rounds x 8 G functions x 22 32-bit operations (two 3-input and two 2-input 64-bit
+# additions at 2 each, four 64-bit XORs at 2, rotations by 24, 16 and 63 at 2 funnel shifts
+# each; the rotation by 32 is a word swap), plus the 16 XORs of the feed-forward.
+B2_OPS_PER_BLOCK = 12 * 8 * 22 + 16
+ALU_LANES_PER_SM = 64           # 4 sub-partitions x 16 lanes of the integer ALU pipe
 
 
 def log(*a):
@@ -156,17 +164,34 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback (6.8 TB/s, one earlier GB300 copy measurement)"
 
 
-def kernel_source_hash():
+def kernel_source_hash(kernel: str):
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in KERNEL_SOURCES[kernel]:
         h.update(open(os.path.join(ROOT, rel), "rb").read())
     return h.hexdigest()[:16]
+
+
+def alu_peak(dev):
+    """Integer ALU pipe peak in T ops/s: SMs x 64 lanes x the maximum SM clock."""
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    try:
+        mhz = float(json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))["sm_max_mhz"])
+        src = "derived: SMs x 64 ALU lanes x sm_max_mhz of MEASURED_PEAKS.json"
+    except (OSError, KeyError, ValueError):
+        mhz, src = 2070.0, "derived: SMs x 64 ALU lanes x 2070 MHz (nominal maximum)"
+    return sms * ALU_LANES_PER_SM * mhz * 1e6 / 1e12, src
+
+
+def b2_blocks(n: int) -> int:
+    """128-byte BLAKE2b blocks of the audit-mode leaves: the header's one, and ceil(n/32)
+    per array (a chunk's 16 KB are 128 blocks, a short last chunk rounds up)."""
+    return 1 + 3 * ((n + 31) // 32)
 
 
 def profiled_traffic(kernel: str):
     """Per-launch DRAM bytes recorded from an ncu capture in profiles/, if the kernel
     sources are unchanged since (the summary stores their hash); else None."""
-    src_hash = kernel_source_hash()
+    src_hash = kernel_source_hash(kernel)
     pdir = os.path.join(ROOT, "profiles")
     if not os.path.isdir(pdir):
         return None
@@ -279,11 +304,14 @@ def run_ours(args, rank, world, local):
 
     # ---- per-kernel times (same calls, events between them, same stream) ------------
     ctx.set_hash_stream(None)          # the root passes on the timed stream here
+    audit = args.hash_mode == "blake2b"
     kt = {"reduce": [], "clip": [], "adamw": [], "root": []}
+    if audit:
+        kt["leaves"] = []           # the BLAKE2b leaf kernel alone (repstep_leaves)
     reps = max(3, min(args.steps, 20))
     for _ in range(reps):
         t_step[0] += 1
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(len(kt) + 1)]
         h = hp(t_step[0])
         ev[0].record(stream)
         reduce_only()
@@ -294,6 +322,9 @@ def run_ours(args, rank, world, local):
         ev[3].record(stream)
         ctx.root(t_step[0], root_out=root)
         ev[4].record(stream)
+        if audit:
+            ctx.leaves(t_step[0], w, m, v)
+            ev[5].record(stream)
         torch.cuda.synchronize(dev)
         for i, k in enumerate(kt):
             kt[k].append(ev[i].elapsed_time(ev[i + 1]))
@@ -304,10 +335,24 @@ def run_ours(args, rank, world, local):
     mask_b = 0.125 if args.decay_mask else 0.0
     alg_step = int((R * b_g + 16 + 2 * b_w + mask_b) * n)
     alg = {"reduce": (R * b_g + 4) * n, "adamw": int((20 + 2 * b_w + mask_b) * n)}
-    dom = max(("reduce", "adamw"), key=lambda k: kms[k])
-    achieved = alg[dom] / (kms[dom] * 1e-3) / 1e9
-    kname = {"reduce": "k_reduce", "adamw": "k_adamw"}[dom]
+    dom = max(("reduce", "adamw", "leaves") if audit else ("reduce", "adamw"),
+              key=lambda k: kms[k])
+    kname = {"reduce": "k_reduce", "adamw": "k_adamw", "leaves": "k_leaves_b2"}[dom]
     traffic = profiled_traffic(kname)
+    if dom == "leaves":
+        apeak, apeak_src = alu_peak(dev)
+        ops = b2_blocks(n) * B2_OPS_PER_BLOCK
+        achieved = ops / (kms[dom] * 1e-3) / 1e12
+        roofline = {"bound": "alu", "kernel": kname, "achieved": achieved, "peak": apeak,
+                    "unit": "Tops/s", "frac": achieved / apeak, "traffic": traffic,
+                    "alg_ops_per_launch": ops, "ops_per_128B_block": B2_OPS_PER_BLOCK,
+                    "avg_launch_ms": kms[dom], "peak_source": apeak_src}
+    else:
+        achieved = alg[dom] / (kms[dom] * 1e-3) / 1e9
+        roofline = {"bound": "hbm", "kernel": kname, "achieved": achieved, "peak": peak,
+                    "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
+                    "alg_bytes_per_launch": alg[dom], "avg_launch_ms": kms[dom],
+                    "peak_source": peak_src}
 
     # ---- end to end: grads from pinned host memory each step, norm+root read back ----
     ctx.set_hash_stream(hash_side)
@@ -349,10 +394,7 @@ def run_ours(args, rank, world, local):
                           "unit": "GB/s", "frac": step_gbs / peak, "peak_source": peak_src,
                           "bytes": "R*b_g*n + (16 + 2*b_w)n (+ n/8 with a decay mask) "
                                    "algorithmic bytes per step"},
-        "roofline": {"bound": "hbm", "kernel": kname, "achieved": achieved, "peak": peak,
-                     "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
-                     "alg_bytes_per_launch": alg[dom], "avg_launch_ms": kms[dom],
-                     "peak_source": peak_src},
+        "roofline": roofline,
         "kernel_ms": kms,
         "clocks": clk,
         "gpu_launches": launches,

@@ -141,6 +141,12 @@ __global__ void __launch_bounds__(256) k_norm(const float *in, uint64_t count, f
     if (scale_out) *scale_out = scale;
 }
 
+// PF61 of the header words {step, n}: (2 + step K + n K^2) mod p.
+__device__ __forceinline__ uint64_t header_leaf(uint32_t step, uint32_t n32, const uint64_t *powers)
+{
+    return pf_add(pf_add(2, pf_mul(step, powers[0])), pf_mul(n32, powers[1]));
+}
+
 // One Merkle block: the canonical tree over up to kMerkleBlock consecutive digests, level by
 // level (pair neighbours, carry an odd last node up unchanged), which is the same tree as
 // the recursive split T = T(first 2^k) + T(rest).  Aligned power-of-two blocks are complete
@@ -163,7 +169,7 @@ __global__ void __launch_bounds__(256) k_merkle(const uint64_t *in, uint64_t cou
     for (uint32_t i = tid; i < cnt; i += blockDim.x) buf0[i] = in[base + i];
     __syncthreads();
     if (header_mode && blockIdx.x == 0 && tid == 0) {
-        const uint64_t h = pf_add(pf_add(2, pf_mul(step, powers[0])), pf_mul(n32, powers[1]));
+        const uint64_t h = header_leaf(step, n32, powers);
         buf0[0] = h;
         leaves_rw[0] = h;
     }
@@ -186,6 +192,14 @@ __global__ void __launch_bounds__(256) k_merkle(const uint64_t *in, uint64_t cou
             out[blockIdx.x] = buf0[0];
         }
     }
+}
+
+// The PF61 header leaf alone (the standalone leaves call; the Merkle pass computes it
+// otherwise).
+__global__ void k_header_leaf(uint64_t *leaves, uint32_t step, uint32_t n32,
+                              const uint64_t *powers)
+{
+    leaves[0] = header_leaf(step, n32, powers);
 }
 
 __global__ void k_write_header(void *dst, int32_t step, uint32_t n32)
@@ -248,6 +262,13 @@ cudaError_t launch_merkle(const uint64_t *in, uint64_t count, uint64_t *out, int
 {
     k_merkle<<<blocks, 256, 0, st>>>(in, count, out, header_mode, leaves_rw, step, n32, powers,
                                      sc, root_out, blocks == 1 ? 1 : 0);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_header_leaf(uint64_t *leaves, int32_t step, uint32_t n32, const uint64_t *powers,
+                               cudaStream_t st)
+{
+    k_header_leaf<<<1, 1, 0, st>>>(leaves, uint32_t(step), n32, powers);
     return cudaGetLastError();
 }
 

@@ -100,6 +100,8 @@ cudaError_t merkle_prepare();
 cudaError_t launch_merkle(const uint64_t *in, uint64_t count, uint64_t *out, int header_mode,
                           uint64_t *leaves_rw, uint32_t step, uint32_t n32, const uint64_t *powers,
                           Scalars *sc, uint64_t *root_out, int blocks, cudaStream_t st);
+cudaError_t launch_header_leaf(uint64_t *leaves, int32_t step, uint32_t n32, const uint64_t *powers,
+                               cudaStream_t st);
 cudaError_t launch_write_header(void *dst, int32_t step, uint32_t n32, cudaStream_t st);
 // bf16 -> fp32 (exact) into an image's w region.  fp32 -> bf16 by dropping the low half
 // (dst nullable: check only); a word whose low half is not zero sets *bad (nullable) to 1.

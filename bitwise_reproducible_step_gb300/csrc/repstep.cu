@@ -442,19 +442,16 @@ int root_passes(repstep_ctx *x, int32_t step, uint64_t *root_out, cudaStream_t s
     return merkle(x, step, root_out, st);
 }
 
-int do_hash(repstep_ctx *x, int32_t step, const void *w, const float *m, const float *v,
-            uint64_t *root_out)
+// The leaves of (step, w, m, v) into the workspace, on the context's stream: all 1 + 3c in
+// the audit mode; in the PF61 mode the chunk leaves only (the header leaf is the first
+// Merkle pass's, or the caller's to add).
+int hash_leaves(repstep_ctx *x, int32_t step, const void *w, const float *m, const float *v)
 {
-    if (!w || !m || !v) return REPSTEP_ERR_ARG;
+    if (x->n > 0 && (!w || !m || !v)) return REPSTEP_ERR_ARG;   // n = 0 reads no array
     if (!aligned(w, 16) || !aligned(m, 16) || !aligned(v, 16)) return REPSTEP_ERR_ALIGN;
-    if (root_out && !aligned(root_out, 8)) return REPSTEP_ERR_ALIGN;
     int rc = join_hash(x);
     if (rc) return rc;
-    if (x->cfg.hash_mode == REPSTEP_HASH_BLAKE2B) {
-        rc = audit_leaves(x, step, w, m, v, x->stream);
-        if (rc) return rc;
-        return merkle(x, step, root_out, x->stream);
-    }
+    if (x->cfg.hash_mode == REPSTEP_HASH_BLAKE2B) return audit_leaves(x, step, w, m, v, x->stream);
     if (x->n > 0) {
         AdamwArgs a{};
         a.w = const_cast<void *>(w);
@@ -481,7 +478,26 @@ int do_hash(repstep_ctx *x, int32_t step, const void *w, const float *m, const f
         if (e != cudaSuccess) return x->cuda_fail(e);
         ++x->launches;
     }
+    return REPSTEP_OK;
+}
+
+int do_hash(repstep_ctx *x, int32_t step, const void *w, const float *m, const float *v,
+            uint64_t *root_out)
+{
+    if (root_out && !aligned(root_out, 8)) return REPSTEP_ERR_ALIGN;
+    const int rc = hash_leaves(x, step, w, m, v);
+    if (rc) return rc;
     return merkle(x, step, root_out, x->stream);
+}
+
+int do_leaves(repstep_ctx *x, int32_t step, const void *w, const float *m, const float *v)
+{
+    const int rc = hash_leaves(x, step, w, m, v);
+    if (rc || x->cfg.hash_mode == REPSTEP_HASH_BLAKE2B) return rc;
+    const cudaError_t e = launch_header_leaf(x->leaves(), step, uint32_t(x->n), x->powers(), x->stream);
+    if (e != cudaSuccess) return x->cuda_fail(e);
+    ++x->launches;
+    return REPSTEP_OK;
 }
 
 // ---- bf16 parameters in the fp32 image -------------------------------------------------
@@ -690,6 +706,13 @@ int repstep_root(repstep_ctx *ctx, int32_t step, uint64_t *d_root_out)
 {
     if (!ctx) return REPSTEP_ERR_ARG;
     return do_root(ctx, step, d_root_out);
+}
+
+int repstep_leaves(repstep_ctx *ctx, int32_t step, const void *d_w, const float *d_m,
+                   const float *d_v)
+{
+    if (!ctx) return REPSTEP_ERR_ARG;
+    return do_leaves(ctx, step, d_w, d_m, d_v);
 }
 
 int repstep_hash(repstep_ctx *ctx, int32_t step, const void *d_w, const float *d_m,

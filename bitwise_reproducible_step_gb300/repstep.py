@@ -73,6 +73,7 @@ EXPORTS = [
     "repstep_selftest_fixed_division", "repstep_reduce_paper", "repstep_checkpoint_save",
     "repstep_checkpoint_load", "repstep_set_decay_mask", "repstep_decay_mask_from_segments",
     "repstep_reduce_paper_accum", "repstep_set_hash_stream", "repstep_wait_hash",
+    "repstep_leaves",
 ]
 NOALLOC_MAX_N = 1 << 30
 
@@ -100,6 +101,7 @@ def lib():
     L.repstep_adamw.argtypes = [vp, vp, vp, vp, C.POINTER(HParams), u64, u64]
     L.repstep_root.argtypes = [vp, i32, vp]
     L.repstep_hash.argtypes = [vp, i32, vp, vp, vp, vp]
+    L.repstep_leaves.argtypes = [vp, i32, vp, vp, vp]
     L.repstep_step.argtypes = [vp, C.POINTER(vp), u32, u32, u32, vp, vp, vp, C.POINTER(HParams),
                                i32, vp, vp]
     L.repstep_image_bytes.argtypes = [u64]
@@ -335,6 +337,15 @@ class Repstep:
         self._bind()
         _check(lib().repstep_hash(self._ctx, int(step), _ptr(w), _ptr(m), _ptr(v),
                                   self._out(root_out, torch.int64)), "hash")
+
+    def leaves(self, step: int, w, m, v) -> torch.Tensor:
+        """The hash's 1 + 3c leaf digests of (step, w, m, v), without the Merkle passes: a
+        view of the workspace's leaf array (int64 bits of the u64 digests), valid until the
+        next call that hashes."""
+        self._state(w, m, v)
+        self._bind()
+        _check(lib().repstep_leaves(self._ctx, int(step), _ptr(w), _ptr(m), _ptr(v)), "leaves")
+        return self.leaves_view()
 
     def step(self, grads, w, m, v, hp: HParams, step: int, norm_out=None, root_out=None,
              nodes: int = 1, gpus_per_node: int | None = None):

@@ -255,9 +255,19 @@ int repstep_root(repstep_ctx *ctx, int32_t step, uint64_t *d_root_out);
 
 /* Standalone state hash (OPEN-1B App. B) of an arbitrary (step, w, m, v): every leaf is
  * computed from the arrays (w of param_dtype, hashed as its fp32 image words), then the
- * Merkle root.  Equals repstep_root() after a step. */
+ * Merkle root.  Equals repstep_root() after a step.  The arrays must be non-null and
+ * 16-byte aligned (REPSTEP_ERR_ARG, REPSTEP_ERR_ALIGN) unless n = 0, where only the header
+ * is hashed. */
 int repstep_hash(repstep_ctx *ctx, int32_t step, const void *d_w, const float *d_m,
                  const float *d_v, uint64_t *d_root_out);
+
+/* The leaves of repstep_hash without the Merkle passes: the 1 + 3c digests of (step, w, m,
+ * v) -- header leaf first, then the chunks of w, of m, of v -- written as LE u64 words to
+ * the workspace's leaf array (repstep_layout.leaves), where they stay until the next call
+ * that hashes.  Comparing two states' leaf arrays locates the chunks where they differ.
+ * Same arguments, alignment rules and errors as repstep_hash. */
+int repstep_leaves(repstep_ctx *ctx, int32_t step, const void *d_w, const float *d_m,
+                   const float *d_v);
 
 /* One whole step: reduce over [0, n) -> clip -> AdamW over [0, n) -> root, bit-identical
  * to the four separate calls.  `step` is the header's step counter after the update; the
