@@ -40,6 +40,7 @@ import torch  # noqa: E402
 METRIC = "params/s and HBM GB/s (% of roofline) per bit-exact reduce+clip+AdamW+hash step"
 UNIT = "params/s"
 FALLBACK_HBM_GBS = 6800.0
+SPEC_HBM_GBS = 8000.0          # the HBM3e figure the metric's own percentage is quoted against
 _CSRC = "bitwise_reproducible_step_gb300/csrc/"
 # the sources each profiled kernel is built from: a traffic figure recorded under their
 # hash stays valid until one of them changes
@@ -265,21 +266,39 @@ def run_ours(args, rank, world, local):
         else:
             ctx.reduce(grads, nodes=args.nodes)
 
-    def one_step():
+    # one norm and root slot per timed step, read after the timed region
+    norms = torch.empty(max(args.steps, 1), dtype=torch.float32, device=dev)
+    roots = torch.empty(max(args.steps, 1), dtype=torch.int64, device=dev)
+
+    def one_step(slot=None):
         t_step[0] += 1
+        nr = norm if slot is None else norms[slot:slot + 1]
+        rt = root if slot is None else roots[slot:slot + 1]
         if not args.paper_shard:
-            ctx.step(grads, w, m, v, hp(t_step[0]), step=t_step[0], norm_out=norm, root_out=root,
+            ctx.step(grads, w, m, v, hp(t_step[0]), step=t_step[0], norm_out=nr, root_out=rt,
                      nodes=args.nodes)
             return
         h = hp(t_step[0])
         reduce_only()
-        ctx.clip(h.clip, norm_out=norm)
+        ctx.clip(h.clip, norm_out=nr)
         ctx.adamw(w, m, v, h)
-        ctx.root(t_step[0], root_out=root)
+        ctx.root(t_step[0], root_out=rt)
 
-    # warm-up
-    for _ in range(args.warmup):
+    # fingerprints that fix the run's bits: the state hash of the initial (w, m, v), and
+    # the pre-clip norm and state root after step 1.  They depend only on the workload and
+    # the reduction order, so every box and every launch shape must print the same values.
+    ctx.hash(0, w, m, v, root_out=root)
+    ctx.sync()
+    repro = {"initial_state_root": f"{int(root.item()) & (2**64 - 1):016x}"}
+
+    # warm-up (its first step is step 1)
+    for i in range(args.warmup):
         one_step()
+        if i == 0:
+            ctx.sync()
+            repro["step1_norm_bits"] = f"{int(norm.view(torch.int32).item()) & 0xFFFFFFFF:08x}"
+            repro["step1_norm"] = float(norm.item())
+            repro["step1_root"] = f"{int(root.item()) & (2**64 - 1):016x}"
     ctx.sync()
 
     # ---- timed region: K whole steps, inputs resident in HBM ------------------------
@@ -290,9 +309,13 @@ def run_ours(args, rank, world, local):
     launches0 = ctx.launch_count()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+    step_ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)] if args.log else []
+    t_first = t_step[0] + 1
     e0.record(stream)
-    for _ in range(args.steps):
-        one_step()
+    for i in range(args.steps):
+        one_step(i)
+        if step_ev:
+            step_ev[i].record(stream)
     e1.record(stream)
     torch.cuda.synchronize(dev)
     barrier(world)
@@ -301,6 +324,16 @@ def run_ours(args, rank, world, local):
     ms_local = e0.elapsed_time(e1) / args.steps
     ms = max_over_ranks(ms_local, world)
     flags = ctx.sync()
+    step_records = []
+    if step_ev:
+        from bitwise_reproducible_step_gb300.policy import f32_bits, root_hex
+        nh, rh = norms.cpu().tolist(), roots.cpu().tolist()
+        prev = e0
+        for i in range(args.steps):
+            step_records.append({"workload": wl.name, "step": t_first + i, "norm": nh[i],
+                                 "norm_bits": f32_bits(nh[i]), "root": root_hex(rh[i]),
+                                 "ms": prev.elapsed_time(step_ev[i])})
+            prev = step_ev[i]
 
     # ---- per-kernel times (same calls, events between them, same stream) ------------
     ctx.set_hash_stream(None)          # the root passes on the timed stream here
@@ -330,6 +363,22 @@ def run_ours(args, rank, world, local):
             kt[k].append(ev[i].elapsed_time(ev[i + 1]))
     kms = {k: statistics.mean(v_) for k, v_ in kt.items()}
     ctx.sync()
+
+    # ---- checkpoint image emit (timed on its own; not part of the step's bytes) --------
+    img = torch.empty(rs.image_bytes(n), dtype=torch.uint8, device=dev)
+    ims = []
+    for _ in range(3):
+        e_a = torch.cuda.Event(enable_timing=True)
+        e_b = torch.cuda.Event(enable_timing=True)
+        e_a.record(stream)
+        ctx.image_write(t_step[0], w, m, v, img)
+        e_b.record(stream)
+        torch.cuda.synchronize(dev)
+        ims.append(e_a.elapsed_time(e_b))
+    del img
+    im_ms = statistics.mean(ims)
+    image_emit = {"bytes": rs.image_bytes(n), "dst": "device buffer", "ms": im_ms,
+                  "gbs_read_plus_write": (b_w + 8 + 12) * n / (im_ms * 1e-3) / 1e9}
 
     peak, peak_src = hbm_peak()
     mask_b = 0.125 if args.decay_mask else 0.0
@@ -393,15 +442,24 @@ def run_ours(args, rank, world, local):
         "roofline_step": {"bound": "hbm", "achieved": step_gbs, "peak": peak,
                           "unit": "GB/s", "frac": step_gbs / peak, "peak_source": peak_src,
                           "bytes": "R*b_g*n + (16 + 2*b_w)n (+ n/8 with a decay mask) "
-                                   "algorithmic bytes per step"},
+                                   "algorithmic bytes per step",
+                          "spec_peak": SPEC_HBM_GBS, "frac_of_spec": step_gbs / SPEC_HBM_GBS},
         "roofline": roofline,
         "kernel_ms": kms,
         "clocks": clk,
         "gpu_launches": launches,
         "device_flags": flags,
+        "repro": repro,
+        "image_emit": image_emit,
         "e2e": e2e,
         "cpu_baseline": cpu,
     }
+    if args.log and rank == 0:
+        from bitwise_reproducible_step_gb300.policy import StepLog
+        log_ = StepLog(args.log)
+        for r in step_records:
+            log_.write(r)
+        log_.write({"summary": res})
     return res
 
 
@@ -572,6 +630,9 @@ def main():
                     help="with --paper-shard: the replicas are microbatches, accum per rank")
     ap.add_argument("--block-threads", type=int, default=0, choices=[0, 128, 256, 512],
                     help="compute threads per CTA of the streaming kernels (0: default)")
+    ap.add_argument("--log", default="",
+                    help="append a JSON-lines record per timed step (norm, its bits, root, "
+                         "event time) and the summary line to this file")
     ap.add_argument("--n", type=int, default=0,
                     help="override the workload's parameter count (small profiling cases)")
     args = ap.parse_args()

@@ -15,6 +15,8 @@
 #include <string>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "../../include/repstep.h"
 #include "common.cuh"
 #include "kernels.h"
@@ -26,6 +28,14 @@ namespace {
 
 struct Layout {
     uint64_t g, chunk_sq, norm_part, leaves, merkle_part, powers, scalars, total;
+};
+
+// An NVTX range over one public call, for timeline tools (a no-op when none is attached).
+struct NvtxRange {
+    explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange &) = delete;
+    NvtxRange &operator=(const NvtxRange &) = delete;
 };
 
 constexpr uint64_t kAlign = 256;
@@ -668,6 +678,7 @@ int repstep_set_stream(repstep_ctx *ctx, void *stream)
 int repstep_reduce(repstep_ctx *ctx, const void *const *d_grads, uint32_t R, uint32_t nodes,
                    uint32_t gpus_per_node, uint64_t begin, uint64_t count)
 {
+    const NvtxRange nvtx_("repstep_reduce");
     if (!ctx) return REPSTEP_ERR_ARG;
     return do_reduce(ctx, d_grads, R, nodes, gpus_per_node, begin, count);
 }
@@ -675,6 +686,7 @@ int repstep_reduce(repstep_ctx *ctx, const void *const *d_grads, uint32_t R, uin
 int repstep_reduce_paper(repstep_ctx *ctx, const void *const *d_grads, uint32_t R,
                          uint32_t dp_shard, uint64_t begin, uint64_t count)
 {
+    const NvtxRange nvtx_("repstep_reduce_paper");
     if (!ctx) return REPSTEP_ERR_ARG;
     if (dp_shard == 0 || R % dp_shard != 0) return REPSTEP_ERR_TOPOLOGY;
     return do_reduce(ctx, d_grads, R, R / dp_shard, dp_shard, begin, count, 1);
@@ -683,6 +695,7 @@ int repstep_reduce_paper(repstep_ctx *ctx, const void *const *d_grads, uint32_t 
 int repstep_reduce_paper_accum(repstep_ctx *ctx, const void *const *d_grads, uint32_t R,
                                uint32_t dp_shard, uint32_t accum, uint64_t begin, uint64_t count)
 {
+    const NvtxRange nvtx_("repstep_reduce_paper_accum");
     if (!ctx) return REPSTEP_ERR_ARG;
     if (accum == 0) return REPSTEP_ERR_ARG;
     if (dp_shard == 0 || R % dp_shard != 0) return REPSTEP_ERR_TOPOLOGY;
@@ -691,6 +704,7 @@ int repstep_reduce_paper_accum(repstep_ctx *ctx, const void *const *d_grads, uin
 
 int repstep_clip(repstep_ctx *ctx, float clip, float *d_norm_out, float *d_scale_out)
 {
+    const NvtxRange nvtx_("repstep_clip");
     if (!ctx) return REPSTEP_ERR_ARG;
     return do_clip(ctx, clip, d_norm_out, d_scale_out);
 }
@@ -698,12 +712,14 @@ int repstep_clip(repstep_ctx *ctx, float clip, float *d_norm_out, float *d_scale
 int repstep_adamw(repstep_ctx *ctx, void *d_w, float *d_m, float *d_v, const repstep_hparams *hp,
                   uint64_t begin, uint64_t count)
 {
+    const NvtxRange nvtx_("repstep_adamw");
     if (!ctx) return REPSTEP_ERR_ARG;
     return do_adamw(ctx, d_w, d_m, d_v, hp, begin, count);
 }
 
 int repstep_root(repstep_ctx *ctx, int32_t step, uint64_t *d_root_out)
 {
+    const NvtxRange nvtx_("repstep_root");
     if (!ctx) return REPSTEP_ERR_ARG;
     return do_root(ctx, step, d_root_out);
 }
@@ -711,6 +727,7 @@ int repstep_root(repstep_ctx *ctx, int32_t step, uint64_t *d_root_out)
 int repstep_leaves(repstep_ctx *ctx, int32_t step, const void *d_w, const float *d_m,
                    const float *d_v)
 {
+    const NvtxRange nvtx_("repstep_leaves");
     if (!ctx) return REPSTEP_ERR_ARG;
     return do_leaves(ctx, step, d_w, d_m, d_v);
 }
@@ -718,6 +735,7 @@ int repstep_leaves(repstep_ctx *ctx, int32_t step, const void *d_w, const float 
 int repstep_hash(repstep_ctx *ctx, int32_t step, const void *d_w, const float *d_m,
                  const float *d_v, uint64_t *d_root_out)
 {
+    const NvtxRange nvtx_("repstep_hash");
     if (!ctx) return REPSTEP_ERR_ARG;
     return do_hash(ctx, step, d_w, d_m, d_v, d_root_out);
 }
@@ -726,6 +744,7 @@ int repstep_step(repstep_ctx *ctx, const void *const *d_grads, uint32_t R, uint3
                  uint32_t gpus_per_node, void *d_w, float *d_m, float *d_v,
                  const repstep_hparams *hp, int32_t step, float *d_norm_out, uint64_t *d_root_out)
 {
+    const NvtxRange nvtx_("repstep_step");
     if (!ctx) return REPSTEP_ERR_ARG;
     // validate everything before launching anything
     if (!d_w || !d_m || !d_v) return REPSTEP_ERR_ARG;
@@ -781,6 +800,7 @@ uint64_t repstep_image_bytes(uint64_t n) { return 8 + 12 * n; }
 int repstep_image_write(repstep_ctx *ctx, int32_t step, const void *d_w, const float *d_m,
                         const float *d_v, void *dst, uint64_t dst_bytes, int dst_is_host)
 {
+    const NvtxRange nvtx_("repstep_image_write");
     if (!ctx || !d_w || !d_m || !d_v || !dst) return REPSTEP_ERR_ARG;
     const uint64_t n = ctx->n;
     if (dst_bytes < repstep_image_bytes(n)) return REPSTEP_ERR_SIZE;
@@ -823,6 +843,7 @@ int repstep_image_write(repstep_ctx *ctx, int32_t step, const void *d_w, const f
 int repstep_image_read(repstep_ctx *ctx, const void *src, uint64_t src_bytes, int src_is_host,
                        int32_t *step_out, void *d_w, float *d_m, float *d_v)
 {
+    const NvtxRange nvtx_("repstep_image_read");
     if (!ctx || !src || !d_w || !d_m || !d_v) return REPSTEP_ERR_ARG;
     const uint64_t n = ctx->n;
     if (src_bytes != repstep_image_bytes(n)) return REPSTEP_ERR_FORMAT;
@@ -890,6 +911,7 @@ int repstep_image_read(repstep_ctx *ctx, const void *src, uint64_t src_bytes, in
 int repstep_checkpoint_save(repstep_ctx *ctx, const char *path, int32_t step, const void *d_w,
                             const float *d_m, const float *d_v)
 {
+    const NvtxRange nvtx_("repstep_checkpoint_save");
     if (!ctx || !path || !d_w || !d_m || !d_v) return REPSTEP_ERR_ARG;
     const uint64_t n = ctx->n;
     const std::string tmp = std::string(path) + ".tmp";
@@ -942,6 +964,7 @@ int repstep_checkpoint_save(repstep_ctx *ctx, const char *path, int32_t step, co
 int repstep_checkpoint_load(repstep_ctx *ctx, const char *path, int32_t *step_out, void *d_w,
                             float *d_m, float *d_v)
 {
+    const NvtxRange nvtx_("repstep_checkpoint_load");
     if (!ctx || !path || !d_w || !d_m || !d_v) return REPSTEP_ERR_ARG;
     const uint64_t n = ctx->n;
     FILE *f = std::fopen(path, "rb");

@@ -234,7 +234,9 @@ class Repstep:
     def __init__(self, n: int, grad_dtype=torch.float32, device=None, grid_blocks: int = 0,
                  block_threads: int = 0, stream: torch.cuda.Stream | None = None,
                  hash_mode: int = HASH_PF61, param_dtype=torch.float32,
-                 subnormals: int = SUBNORMALS_IEEE):
+                 subnormals: int = SUBNORMALS_IEEE, workspace: torch.Tensor | None = None):
+        """workspace: an optional caller-owned uint8 device tensor of at least
+        workspace_bytes() bytes (256-byte aligned); by default one is allocated here."""
         L = lib()
         self.n = int(n)
         self.grad_dtype = grad_dtype
@@ -251,7 +253,13 @@ class Repstep:
             raise RepstepError(1, "bad configuration")
         self.layout = Layout()
         _check(L.repstep_workspace_layout(C.byref(self.cfg), C.byref(self.layout)))
-        self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=self.device)
+        if workspace is None:
+            workspace = torch.empty(nbytes, dtype=torch.uint8, device=self.device)
+        elif (workspace.dtype != torch.uint8 or workspace.device != self.device
+              or not workspace.is_contiguous() or workspace.numel() < nbytes):
+            raise ValueError(f"workspace: contiguous uint8 on the context's device, at least "
+                             f"{nbytes} bytes")
+        self.workspace = workspace
         self._ctx = C.c_void_p()
         _check(L.repstep_create(C.byref(self.cfg), _ptr(self.workspace), nbytes,
                                 C.c_void_p(self._stream().cuda_stream), C.byref(self._ctx)))

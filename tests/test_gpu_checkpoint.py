@@ -79,7 +79,7 @@ def test_resume_from_checkpoint_is_bit_exact(tmp_path):
         assert torch.equal(x.view(torch.int32), y.view(torch.int32))
 
 
-def test_spike_protocol_matches_oracle():
+def test_spike_protocol_matches_oracle(tmp_path):
     """A spike (pre-clip norm > 5) at training step 3 skips steps 3..7: the state stays
     bit-identical, the hash advances its header step, and AdamW resumes with t = 3."""
     n, R = 2 * 4096 + 5, 4
@@ -87,7 +87,8 @@ def test_spike_protocol_matches_oracle():
     ctx = rs.Repstep(n, device=dev)
     w, m, v = I.gen_state(U.F32_WL, n=n, device=dev)
     ow, om, ov = w.cpu().numpy(), m.cpu().numpy(), v.cpu().numpy()
-    stepper = P.Stepper(ctx, U.HP)
+    log = P.StepLog(tmp_path / "steps.jsonl")
+    stepper = P.Stepper(ctx, U.HP, log=log)
     root = torch.empty(1, dtype=torch.int64, device=dev)
     adam_t = 0
     for t in range(1, 11):
@@ -108,3 +109,9 @@ def test_spike_protocol_matches_oracle():
         U.assert_same_f32(w, ow, f"w step {t}")
         U.assert_same_f32(v, ov, f"v step {t}")
         assert U.root_of(root) == O.state_hash(t, ow, om, ov)
+    # the log holds one record per step, with the norm's bits and the root of each step
+    recs = log.records()
+    assert [r["train_step"] for r in recs] == list(range(1, 11))
+    assert [r["applied"] for r in recs] == [t < 3 or t > 7 for t in range(1, 11)]
+    assert recs[-1]["root"] == P.root_hex(U.root_of(root))
+    assert all(r["norm_bits"] == P.f32_bits(r["norm"]) for r in recs)

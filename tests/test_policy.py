@@ -40,3 +40,25 @@ def test_checkpoint_names():
     assert rs.checkpoint_name(1234567) == "step_1234567.bin"
     with pytest.raises(ValueError):
         rs.checkpoint_name(-1)
+
+
+def test_step_log_appends_one_line_per_record(tmp_path):
+    p = tmp_path / "run.jsonl"
+    log = P.StepLog(p)
+    assert log.records() == []
+    log.write({"train_step": 1, "norm": 0.5, "root": P.root_hex(-2)})
+    P.StepLog(p).write({"train_step": 2, "norm": math.nan})      # reopened: appends
+    lines = p.read_text().splitlines()
+    assert len(lines) == 2
+    recs = log.records()
+    assert recs[0] == {"norm": 0.5, "root": "fffffffffffffffe", "train_step": 1}
+    assert recs[1]["train_step"] == 2 and math.isnan(recs[1]["norm"])
+
+
+def test_step_log_bit_formats():
+    assert P.f32_bits(1.0) == "3f800000"
+    assert P.f32_bits(-0.0) == "80000000"
+    assert P.f32_bits(2.0 ** -149) == "00000001"
+    assert P.root_hex(0) == "0" * 16
+    assert P.root_hex(2**63) == "8000000000000000"
+    assert P.root_hex(-1) == "f" * 16
