@@ -614,7 +614,7 @@ def main():
     ap.add_argument("--param-dtype", choices=["f32", "bf16"], default="f32",
                     help="parameter dtype (bf16: widened, updated in fp32, rounded once)")
     ap.add_argument("--subnormals", choices=["ieee", "ftz"], default="ieee",
-                    help="ftz: software flush-to-zero of every operand and result")
+                    help="ftz: flush-to-zero arithmetic (subnormal operands and tiny results zeroed)")
     ap.add_argument("--decay-mask", action="store_true",
                     help="per-segment weight decay through a device bitmask")
     ap.add_argument("--hash-mode", choices=["pf61", "blake2b"], default="pf61",

@@ -33,13 +33,18 @@ constexpr uint64_t kP61 = 0x1FFFFFFFFFFFFFFFull;
 constexpr uint64_t kK61 = 0x13C6EF372FE94F82ull;
 
 // ----------------------------------------------------------------------------------
-// Arithmetic policy.  FZ = 0: IEEE binary32 with gradual underflow.  FZ = 1: software
+// Arithmetic policy.  FZ = 0: IEEE binary32 with gradual underflow.  FZ = 1:
 // flush-to-zero ("OPEN-1B", §2.1 "Subnormals": FTZ zeroes a subnormal result, DAZ a
-// subnormal input), read as: every operation's correctly rounded result, and every
-// operand read from memory, is flushed to a zero of the same sign when subnormal.  The
-// flush is one mul.rn.ftz.f32 by 1.0: its .ftz flushes a subnormal operand, and any other
-// value times 1.0 is exact (NaN stays NaN).  Inputs produced by a previous operation are
-// already flushed, so flushing results and loads is the same as flushing every operand.
+// subnormal input), read as: every operation treats a subnormal operand as a zero of the
+// same sign, and zeroes (keeping the sign) a result that is tiny in IEEE 754's sense with
+// tininess detected after rounding -- the exact result rounded to 24 bits as though the
+// exponent were unbounded lies below 2^-126.  The .rn.ftz forms of add, sub, mul, div and
+// sqrt do exactly this, one instruction each: a sum below 2^-126 is exact, a square root
+// of a normal value is normal, and for products and quotients the flush decision was
+// checked against that rule on operands built to land within a few units of 2^-126.
+// So no operand needs a separate flush; flush_subnormal (a .ftz multiply by 1.0: any
+// other value times 1.0 is exact, NaN stays NaN) remains for the few values that leave
+// the kernels without passing through an operation.
 // ----------------------------------------------------------------------------------
 __device__ __forceinline__ float flush_subnormal(float x)
 {
@@ -55,11 +60,41 @@ struct Ar {
         if constexpr (FZ != 0) return flush_subnormal(x);
         else return x;
     }
-    static __device__ __forceinline__ float add(float a, float b) { return in(__fadd_rn(a, b)); }
-    static __device__ __forceinline__ float sub(float a, float b) { return in(__fsub_rn(a, b)); }
-    static __device__ __forceinline__ float mul(float a, float b) { return in(__fmul_rn(a, b)); }
-    static __device__ __forceinline__ float div(float a, float b) { return in(__fdiv_rn(a, b)); }
-    static __device__ __forceinline__ float sqrt(float a) { return in(__fsqrt_rn(a)); }
+    static __device__ __forceinline__ float add(float a, float b)
+    {
+        if constexpr (FZ == 0) return __fadd_rn(a, b);
+        float r;
+        asm("add.rn.ftz.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+        return r;
+    }
+    static __device__ __forceinline__ float sub(float a, float b)
+    {
+        if constexpr (FZ == 0) return __fsub_rn(a, b);
+        float r;
+        asm("sub.rn.ftz.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+        return r;
+    }
+    static __device__ __forceinline__ float mul(float a, float b)
+    {
+        if constexpr (FZ == 0) return __fmul_rn(a, b);
+        float r;
+        asm("mul.rn.ftz.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+        return r;
+    }
+    static __device__ __forceinline__ float div(float a, float b)
+    {
+        if constexpr (FZ == 0) return __fdiv_rn(a, b);
+        float r;
+        asm("div.rn.ftz.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+        return r;
+    }
+    static __device__ __forceinline__ float sqrt(float a)
+    {
+        if constexpr (FZ == 0) return __fsqrt_rn(a);
+        float r;
+        asm("sqrt.rn.ftz.f32 %0, %1;" : "=f"(r) : "f"(a));
+        return r;
+    }
 };
 
 // Device-side scalars kept in the workspace.

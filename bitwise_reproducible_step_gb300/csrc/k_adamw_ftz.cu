@@ -1,4 +1,4 @@
-// k_adamw_ftz.cu -- the software flush-to-zero instantiations of the AdamW / leaf kernel
+// k_adamw_ftz.cu -- the flush-to-zero instantiations of the AdamW / leaf kernel
 // (k_adamw.cuh), a translation unit of their own so that the two arithmetic modes build
 // in parallel.
 #include "k_adamw.cuh"

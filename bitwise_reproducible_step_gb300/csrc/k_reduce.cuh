@@ -1,6 +1,6 @@
 // k_reduce.cuh -- replica reduce + per-chunk sum of squares (one HBM pass over R gradients).
 // The kernel template; k_reduce.cu instantiates the IEEE variants (FZ = 0) and holds the
-// host-side launch helpers, k_reduce_ftz.cu the software flush-to-zero variants (FZ = 1).
+// host-side launch helpers, k_reduce_ftz.cu the flush-to-zero variants (FZ = 1).
 //
 // Computes, for every element i of the active range,
 //     g_i = T_{r<R}(G_r[i]) * fp32(1/R)
@@ -192,14 +192,14 @@ __device__ __forceinline__ float4 load_group_raw(const unsigned char *tile, uint
 
 // One 4-element group of one replica: from the staged tile when the group lies in the
 // bulk-copied interior, else element by element from global memory (zero outside [a, b)).
-// In the flush-to-zero mode every value read is flushed (DAZ).
+// The flush-to-zero mode needs no flush here: every value read reaches g only through
+// .ftz additions and the final multiply by rho, which treat a subnormal operand as zero.
 template <int DT, int FZ>
 __device__ __forceinline__ float4 load_group(const unsigned char *tile, uint32_t off,
                                              bool in_bulk, const void *src, uint64_t e0,
                                              uint64_t a, uint64_t b)
 {
-    const float4 x = load_group_raw<DT>(tile, off, in_bulk, src, e0, a, b);
-    return make_float4(Ar<FZ>::in(x.x), Ar<FZ>::in(x.y), Ar<FZ>::in(x.z), Ar<FZ>::in(x.w));
+    return load_group_raw<DT>(tile, off, in_bulk, src, e0, a, b);
 }
 
 // MODE 0: the canonical tree over all R replicas.  MODE 1: the same tree staged as a

@@ -1,4 +1,4 @@
-// k_reduce_ftz.cu -- the software flush-to-zero instantiations of the replica-reduce
+// k_reduce_ftz.cu -- the flush-to-zero instantiations of the replica-reduce
 // kernel (k_reduce.cuh), compiled as a translation unit of their own so that the two
 // arithmetic modes build in parallel.
 #include "k_reduce.cuh"

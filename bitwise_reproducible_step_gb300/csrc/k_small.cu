@@ -45,7 +45,7 @@ __global__ void __launch_bounds__(256) k_chunk_fix(const float *g, uint64_t n, f
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const uint64_t e = k * kChunk + uint64_t(j) * 1024 + 4u * tid + i;
-            const float x = e < n ? Ar<FZ>::in(g[e]) : 0.0f;
+            const float x = e < n ? g[e] : 0.0f;
             q[i] = e < n ? Ar<FZ>::mul(x, x) : 0.0f;
         }
         part[j] = sum4<FZ>(q[0], q[1], q[2], q[3]);
@@ -118,7 +118,7 @@ __global__ void __launch_bounds__(256) k_norm(const float *in, uint64_t count, f
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const uint64_t e = base + uint64_t(j) * 1024 + 4u * tid + i;
-            q[i] = e < count ? Ar<FZ>::in(in[e]) : 0.0f;
+            q[i] = e < count ? in[e] : 0.0f;        // results of .ftz operations already
         }
         part[j] = sum4<FZ>(q[0], q[1], q[2], q[3]);
     }

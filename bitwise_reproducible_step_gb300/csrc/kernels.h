@@ -34,7 +34,7 @@ struct ReduceShape {
     int mode;        // 0 canonical tree, 1 topology-staged, 2 paper-exact (Algorithm 1)
     int rg;          // replicas per stage group (4 or 8)
     int maxlev;      // carry-stack depth (6 or 9)
-    int fz;          // 0 IEEE, 1 software flush-to-zero
+    int fz;          // 0 IEEE, 1 flush-to-zero (.ftz arithmetic)
 };
 
 using ReduceKernelFn = void (*)(ReduceArgs);
@@ -72,7 +72,7 @@ struct AdamwShape {
     int nt;     // compute threads (128, 256, 512)
     int mode;   // 0 AdamW + PF61 leaves, 1 leaves only, 2 AdamW only
     int pt;     // 1: bf16 parameters
-    int fz;     // 1: software flush-to-zero arithmetic
+    int fz;     // 1: flush-to-zero (.ftz) arithmetic
     int mk;     // 1: per-element weight-decay mask (args.decay_mask)
 };
 size_t adamw_smem_bytes(const AdamwShape &s, AdamwArgs &args);

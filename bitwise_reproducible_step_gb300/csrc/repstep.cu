@@ -82,11 +82,29 @@ bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 bool finite_f(float x) { return std::isfinite(x); }
 
-// Host side of the software flush-to-zero mode: a subnormal becomes a zero of the same
-// sign (fz != 0); used for the hyperparameters and the constants derived from them.
+// Host side of the flush-to-zero mode: a subnormal becomes a zero of the same sign
+// (fz != 0); used for the hyperparameters and the constants derived from them.
 float hflush(int fz, float x)
 {
     return (fz && std::fpclassify(x) == FP_SUBNORMAL) ? std::copysign(0.0f, x) : x;
+}
+
+// A product in the flush-to-zero mode, as the device's mul.rn.ftz computes it: operands
+// flushed, and a tiny result -- the exact product rounded to 24 bits as though the
+// exponent were unbounded is below 2^-126 -- becomes a zero of the product's sign.  The
+// double product of two floats is exact; below 2^-126 it is rounded to 24 bits by hand.
+float hmul(int fz, float a, float b)
+{
+    if (!fz) return a * b;
+    a = hflush(1, a);
+    b = hflush(1, b);
+    const double p = double(a) * double(b);
+    const float r = float(p);
+    if (!(std::fabs(p) < 0x1p-126) || p == 0.0) return r;
+    int e = 0;
+    const double frac = std::frexp(std::fabs(p), &e);                // in [0.5, 1)
+    const double rounded = std::ldexp(std::nearbyint(std::ldexp(frac, 24)), e - 24);
+    return rounded < 0x1p-126 ? std::copysign(0.0f, r) : r;
 }
 
 }  // namespace
@@ -342,7 +360,7 @@ int do_adamw(repstep_ctx *x, void *w, float *m, float *v, const repstep_hparams 
     const float one = 1.0f;
     a.om1 = hflush(fz, one - a.beta1);
     a.om2 = hflush(fz, one - a.beta2);
-    const float lrwd = hflush(fz, a.lr * hflush(fz, hp->weight_decay));
+    const float lrwd = hmul(fz, a.lr, hflush(fz, hp->weight_decay));
     a.delta = hflush(fz, one - lrwd);
     // reciprocals of the bias corrections for the fixed-divisor division in k_adamw
     a.rbc1 = one / a.bc1;

@@ -7,7 +7,7 @@
  * the checkpoint image [int32 step][uint32 n][w][m][v] with per-chunk digests combined in
  * a Merkle tree.  Every output bit is fixed by the definition below, independent of the
  * launch configuration, of how replicas are grouped into nodes, and of how the parameter
- * range is split.  Options: per-segment weight decay, a software flush-to-zero mode, the
+ * range is split.  Options: per-segment weight decay, a flush-to-zero mode, the
  * paper-exact reduction order of OPEN-1B's audit replay, and the hash on a second stream.
  *
  * Sources, by page title and section:
@@ -116,12 +116,15 @@ typedef struct {
                                 §3.2, optimizer-state precision).  m and v are fp32 either
                                 way; the image and the hash hold w widened to fp32.        */
     int32_t subnormals;      /* enum repstep_subnormals: 0 IEEE gradual underflow (default);
-                                1 software flush-to-zero -- every fp32 operation of the
-                                step flushes subnormal operands and results to a zero of the
-                                same sign (OPEN-1B §2.1 "Subnormals", FTZ + DAZ), tininess
-                                judged on the rounded result.  Also the hyperparameters and
-                                the constants derived from them on the host.  Never changes
-                                the hash function, only the values hashed.               */
+                                1 flush-to-zero -- every fp32 operation of the step treats
+                                a subnormal operand as a zero of the same sign, and zeroes
+                                a tiny result, keeping its sign (OPEN-1B §2.1 "Subnormals",
+                                FTZ + DAZ).  Tiny means IEEE 754's tininess after rounding:
+                                the exact result rounded to 24 bits with an unbounded
+                                exponent is below 2^-126 -- the rule of the device's .ftz
+                                instructions.  Also the hyperparameters and the constants
+                                derived from them on the host.  Never changes the hash
+                                function, only the values hashed.                          */
 } repstep_config;
 
 typedef struct {

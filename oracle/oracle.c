@@ -457,8 +457,16 @@ int oracle_adamw_bf16w_segments(uint16_t *w16, float *m, float *v, const float *
 /* applies both on every backend to match the least permissive one).  Readings:     */
 /*   - every fp32 operation of the step flushes its operands and its result;        */
 /*   - a flushed value becomes a zero of the same sign;                              */
-/*   - "subnormal result" means the correctly rounded result is subnormal (tininess  */
-/*     after rounding): a value that rounds up to the smallest normal is kept;      */
+/*   - "subnormal result" means a tiny result in IEEE 754's sense with tininess      */
+/*     detected after rounding (IEEE 754-2008 §7.5): the exact result, rounded to    */
+/*     24 significant bits as though the exponent range were unbounded, is nonzero   */
+/*     and below 2^-126 in magnitude.  Such a result is zeroed; every other result   */
+/*     is the IEEE result.  So a product whose exact value lies just below 2^-126    */
+/*     but rounds (unbounded) to 2^-126 is kept, and one that rounds (unbounded) to  */
+/*     2^-126 - 2^-150 is zeroed although the binary32 rounding would give 2^-126;   */
+/*   - a sum or difference below 2^-126 is exact (both operands are multiples of     */
+/*     2^-149), and a square root of a normal value is normal, so for these the rule */
+/*     is the plain flush of the IEEE result;                                       */
 /*   - the rounding of a bf16 parameter is an operation too, but its input is then  */
 /*     zero or at least the smallest normal, so it never yields a subnormal.          */
 /* The functions below repeat the IEEE-mode definitions above with every operation  */
@@ -470,13 +478,40 @@ static float flush(float x)
     return x;
 }
 
+/* Tininess of a product or quotient r = IEEE(a op b) of two flushed operands.  Only
+   |r| <= 2^-126 can be tiny.  Then a is at most about 4 in magnitude (b is zero or
+   at least 2^-126 for a product; the quotient is at most 2^-126 for a division), so
+   a * 2^64 is exact and the same operation on it rounds the exact result times 2^64
+   to 24 bits in the normal range -- the unbounded-exponent rounding, scaled.  The
+   result is tiny when that is below 2^-62.  (Exact results below 2^-190 leave the
+   scaled rounding subnormal or zero, and are tiny either way.) */
+static float fz_mul(float a, float b)
+{
+    a = flush(a);
+    b = flush(b);
+    float r = a * b;
+    if (!(fabsf(r) <= 0x1p-126f)) return r;          /* normal, infinite or NaN */
+    float s = (a * 0x1p64f) * b;
+    return fabsf(s) < 0x1p-62f ? copysignf(0.0f, r) : r;
+}
+
+static float fz_div(float a, float b)
+{
+    a = flush(a);
+    b = flush(b);
+    float r = a / b;
+    if (!(fabsf(r) <= 0x1p-126f)) return r;
+    float s = (a * 0x1p64f) / b;
+    return fabsf(s) < 0x1p-62f ? copysignf(0.0f, r) : r;
+}
+
 static float fz_add(float a, float b) { return flush(flush(a) + flush(b)); }
 static float fz_sub(float a, float b) { return flush(flush(a) - flush(b)); }
-static float fz_mul(float a, float b) { return flush(flush(a) * flush(b)); }
-static float fz_div(float a, float b) { return flush(flush(a) / flush(b)); }
 static float fz_sqrt(float a) { return flush(sqrtf(flush(a))); }
 
 float oracle_flush(float x) { return flush(x); }
+float oracle_mul_ftz(float a, float b) { return fz_mul(a, b); }
+float oracle_div_ftz(float a, float b) { return fz_div(a, b); }
 
 static float fz_tree_sum_rec(const float *x, uint64_t L)
 {

@@ -92,6 +92,9 @@ def lib():
         L.oracle_adamw_bf16w.restype = None
         L.oracle_flush.argtypes = [C.c_float]
         L.oracle_flush.restype = C.c_float
+        for fn in (L.oracle_mul_ftz, L.oracle_div_ftz):
+            fn.argtypes = [C.c_float, C.c_float]
+            fn.restype = C.c_float
         L.oracle_tree_sum_ftz.argtypes = [fp, C.c_uint64]
         L.oracle_tree_sum_ftz.restype = C.c_float
         L.oracle_reduce_ftz.argtypes = [fp, C.c_int, C.c_uint32, C.c_uint64, fp]
@@ -296,6 +299,16 @@ def adamw_bf16w_segments(w16, m, v, g, scale, lr, beta1, beta2, eps, wd, bc1, bc
 def flush(x) -> np.float32:
     """A subnormal becomes a zero of the same sign; everything else is unchanged."""
     return np.float32(lib().oracle_flush(float(np.float32(x))))
+
+
+def mul_ftz(a, b) -> np.float32:
+    """One product in the flush-to-zero mode (operands flushed, tiny result zeroed)."""
+    return np.float32(lib().oracle_mul_ftz(float(np.float32(a)), float(np.float32(b))))
+
+
+def div_ftz(a, b) -> np.float32:
+    """One quotient in the flush-to-zero mode."""
+    return np.float32(lib().oracle_div_ftz(float(np.float32(a)), float(np.float32(b))))
 
 
 def tree_sum_ftz(x) -> np.float32:

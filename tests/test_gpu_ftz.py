@@ -204,3 +204,63 @@ def test_ftz_launch_shape_invariance(nt, grid):
         assert torch.equal(x.view(torch.int32), y.view(torch.int32))
     assert a[3] == b[3]
     assert torch.equal(a[4].view(torch.int32), b[4].view(torch.int32))
+
+
+def _band_case(n, hp_kw, plant):
+    """One AdamW step with zero gradients on planted moments and weights, on the GPU in
+    the flush-to-zero mode, against the oracle; returns the GPU's (w, m, v)."""
+    ctx = rs.Repstep(n, device=DEV, subnormals=rs.SUBNORMALS_FTZ)
+    w, m, v = I.gen_state(U.F32_WL, n=n, device=DEV)
+    plant(w, m, v)
+    w0, m0, v0 = w.cpu().numpy(), m.cpu().numpy(), v.cpu().numpy()
+    grads = [torch.zeros(n, device=DEV) for _ in range(2)]
+    hp = rs.hparams(t=1, **hp_kw)
+    ctx.reduce(grads)
+    ctx.clip(hp.clip)
+    ctx.adamw(w, m, v, hp)
+    ctx.sync()
+    g0 = np.zeros(n, np.float32)
+    bc1, bc2 = O.bias_corrections_ftz(hp_kw["beta1"], hp_kw["beta2"], 1)
+    ref = O.adamw_ftz(w0, m0, v0, g0, 1.0, hp_kw["lr"], hp_kw["beta1"], hp_kw["beta2"],
+                      hp_kw["eps"], hp_kw["weight_decay"], bc1, bc2)
+    for got, want, nm in zip((w, m, v), ref, "wmv"):
+        U.assert_same_f32(got, want, nm)
+    return w.cpu().numpy(), m.cpu().numpy(), v.cpu().numpy()
+
+
+def test_ftz_products_at_the_tininess_boundary():
+    """b1*m exactly +-(2^-126 - 2^-150) is tiny (zeroed) although its binary32 rounding
+    is 2^-126; b2*v exactly 2^-126 (1 - 2^-46) rounds to 2^-126 with an unbounded
+    exponent and is kept."""
+    n = 4096 + 5
+    tiny = 2.0 ** -126
+
+    def plant(w, m, v):
+        m[0::7] = tiny
+        m[3::7] = -tiny
+        v[1::5] = (1 + 2.0 ** -23) * tiny
+
+    _, m1, v1 = _band_case(n, dict(lr=3e-4, beta1=1 - 2.0 ** -24, beta2=1 - 2.0 ** -23,
+                                   eps=1e-8, weight_decay=0.1, clip=1.0), plant)
+    # both signs end as +0: the zeroed product is added to (1 - b1) * gc = +0
+    assert not m1[0::7].view(np.uint32).any()
+    assert not m1[3::7].view(np.uint32).any()
+    assert np.all(v1[1::5] == np.float32(tiny))
+
+
+def test_ftz_quotient_at_the_tininess_boundary():
+    """u = mh / (sqrt(vh) + eps) exactly 2^-126 - 2^-150 is zeroed, so w' = w; flushing
+    the binary32 quotient instead (2^-126) would give w - 2^-126."""
+    n = 4096 + 5
+
+    def plant(w, m, v):
+        m[2::9] = (1 - 2.0 ** -24) * 2.0 ** -99    # m' = m/2, mh = m'/(1/2) = m
+        v[2::9] = 0.0
+        w[2::9] = 2.0 ** -124
+
+    w1, _, _ = _band_case(n, dict(lr=1.0, beta1=0.5, beta2=0.5, eps=2.0 ** 27,
+                                  weight_decay=0.0, clip=1.0), plant)
+    assert np.all(w1[2::9] == np.float32(2.0 ** -124))
+    with np.errstate(under="ignore"):
+        ieee_u = np.float32(np.float32((1 - 2.0 ** -24) * 2.0 ** -99) / np.float32(2.0 ** 27))
+    assert ieee_u == np.float32(2.0 ** -126)              # the binary32 quotient

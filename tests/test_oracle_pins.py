@@ -821,13 +821,15 @@ def test_ftz_golden_cases():
     # DAZ on a subnormal gradient, sign kept
     g = O.reduce_ftz([np.full(4, -(2.0 ** -140), np.float32)])
     assert np.all(g.view(np.uint32) == 0x80000000)              # -0
-    # tininess after rounding: T = (3*2^22 - 1)*2^-148 times fp32(1/3) = (2^25+1)/3 * 2^-25
-    # is exactly 2^-126 - (5/12)*2^-149, below the smallest normal, but rounds UP to it;
-    # the rounded result is normal and kept
+    # tininess after rounding with an unbounded exponent: T = (3*2^22 - 1)*2^-148 times
+    # fp32(1/3) = (2^25+1)/3 * 2^-25 is exactly 2^-126 - (5/12)*2^-149.  Rounded to 24
+    # bits with an unbounded exponent (spacing 2^-150 below 2^-126) it is 2^-126 - 2^-150:
+    # tiny, so zeroed -- although the binary32 rounding (spacing 2^-149) would give 2^-126
     T = np.full(4, float((3 * 2 ** 22 - 1) * Fraction(2) ** -148), np.float32)
     assert Fraction(float(T[0])) == (3 * 2 ** 22 - 1) * Fraction(2) ** -148
+    assert np.all(O.reduce([T, z, z]) == TINY)                  # IEEE: rounds up to 2^-126
     g = O.reduce_ftz([T, z, z])
-    assert np.all(g == TINY)
+    assert np.all(g.view(np.uint32) == 0)
     # squares below the normal range vanish: a norm of 2^-70 entries is 0 in FTZ mode
     g = np.full(5000, 2.0 ** -70, np.float32)
     assert O.norm(g) > 0 and O.norm_ftz(g) == 0
@@ -844,3 +846,74 @@ def test_ftz_golden_cases():
     assert not m1.view(np.uint32).any() and not v1.view(np.uint32).any()
     wi, mi, _ = O.adamw(w, m, z[:1].repeat(n), z[:1].repeat(n), 1.0, LR, B1, B2, EPS, WD, bc1, bc2)
     assert np.all(mi != 0)
+
+
+def _round24_unbounded(q: Fraction) -> Fraction:
+    """q > 0 rounded to 24 significant bits, ties to even, with no exponent limit."""
+    e = q.numerator.bit_length() - q.denominator.bit_length()
+    while Fraction(2) ** e > q:
+        e -= 1
+    while Fraction(2) ** (e + 1) <= q:
+        e += 1
+    x = q * Fraction(2) ** (23 - e)                 # in [2^23, 2^24)
+    k = x.numerator // x.denominator
+    rem = x - k
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and k % 2 == 1):
+        k += 1
+    return k * Fraction(2) ** (e - 23)
+
+
+def _ftz_expected(exact: Fraction, ieee: np.float32) -> np.float32:
+    """IEEE 754-2008 §7.5 tininess after rounding: zero the result when the exact value,
+    rounded to 24 bits as though the exponent were unbounded, is nonzero and below 2^-126."""
+    if exact != 0 and _round24_unbounded(abs(exact)) < Fraction(2) ** -126:
+        return np.float32(-0.0) if exact < 0 else np.float32(0.0)
+    return ieee
+
+
+def test_ftz_tininess_is_detected_after_rounding_with_unbounded_exponent():
+    one_m24 = np.float32(1 - 2.0 ** -24)            # largest float below 1
+    one_m23 = np.float32(1 - 2.0 ** -23)
+    one_p23_tiny = np.float32((1 + 2.0 ** -23) * 2.0 ** -126)
+    # exact 2^-126 - 2^-150: representable with an unbounded exponent, so tiny; zeroed
+    # with its sign although binary32 rounding gives 2^-126
+    assert X.bits(O.mul_ftz(one_m24, TINY)) == 0
+    assert X.bits(O.mul_ftz(-one_m24, TINY)) == 0x80000000
+    assert np.float32(one_m24) * TINY == TINY
+    # exact 2^-126 (1 - 2^-46): rounds (unbounded) to 2^-126, not tiny; kept.  Detecting
+    # tininess before rounding would zero it
+    assert O.mul_ftz(one_m23, one_p23_tiny) == TINY
+    # exact 2^-126 - 2^-149: subnormal under every reading
+    assert X.bits(O.mul_ftz(one_m23, TINY)) == 0
+    # quotients: (1 - 2^-24) 2^-100 / 2^26 = 2^-126 - 2^-150 is tiny; 2^-100 / 2^26 is not
+    assert X.bits(O.div_ftz(np.float32((1 - 2.0 ** -24) * 2.0 ** -100), 2.0 ** 26)) == 0
+    assert O.div_ftz(2.0 ** -100, 2.0 ** 26) == TINY
+    # DAZ: a subnormal operand is zero first
+    assert X.bits(O.mul_ftz(2.0 ** -130, 2.0 ** 100)) == 0
+    assert X.bits(O.div_ftz(-(2.0 ** -130), 2.0 ** -100)) == 0x80000000
+    assert np.isnan(O.div_ftz(2.0 ** -130, 0.0))    # 0/0 after DAZ
+
+
+def test_ftz_mul_div_against_exact_arithmetic_near_the_boundary():
+    """Products and quotients built to land within a few units of 2^-126, checked
+    against the rule evaluated in exact rational arithmetic."""
+    rng = np.random.default_rng(72)
+    for _ in range(3000):
+        off = int(rng.integers(-40, 41))
+        target = 2.0 ** -126 * (1 + off * 2.0 ** -26)
+        # product: a in [2^-63, 2^-43), b = RN(target / a)
+        a = np.float32(2.0 ** (-63 + int(rng.integers(0, 20))) * (1 + rng.random()))
+        b = np.float32(target / float(a))
+        with np.errstate(under="ignore"):
+            ieee = np.float32(a * b)
+        exact = Fraction(float(a)) * Fraction(float(b))
+        assert X.bits(O.mul_ftz(a, b)) == X.bits(_ftz_expected(exact, ieee)), (a, b)
+        # quotient: x in [1, 2^20), y = RN(target * x), y / x
+        x = np.float32(2.0 ** int(rng.integers(0, 20)) * (1 + rng.random()))
+        y = np.float32(target * float(x))
+        if abs(y) < 2.0 ** -126:
+            continue
+        with np.errstate(under="ignore"):
+            ieee = np.float32(y / x)
+        exact = Fraction(float(y)) / Fraction(float(x))
+        assert X.bits(O.div_ftz(y, x)) == X.bits(_ftz_expected(exact, ieee)), (y, x)
