@@ -341,8 +341,11 @@ def run_ours(args, rank, world, local):
     kt = {"reduce": [], "clip": [], "adamw": [], "root": []}
     if audit:
         kt["leaves"] = []           # the BLAKE2b leaf kernel alone (repstep_leaves)
+    # no synchronisation between repetitions: the host stays ahead of the GPU, so each
+    # interval is device time, not the host's launch latency (which matters for small n)
     reps = max(3, min(args.steps, 20))
-    for _ in range(reps):
+    all_ev = []
+    for _ in range(reps + 1):           # the first repetition starts from an idle GPU: dropped
         t_step[0] += 1
         ev = [torch.cuda.Event(enable_timing=True) for _ in range(len(kt) + 1)]
         h = hp(t_step[0])
@@ -358,7 +361,9 @@ def run_ours(args, rank, world, local):
         if audit:
             ctx.leaves(t_step[0], w, m, v)
             ev[5].record(stream)
-        torch.cuda.synchronize(dev)
+        all_ev.append(ev)
+    torch.cuda.synchronize(dev)
+    for ev in all_ev[1:]:
         for i, k in enumerate(kt):
             kt[k].append(ev[i].elapsed_time(ev[i + 1]))
     kms = {k: statistics.mean(v_) for k, v_ in kt.items()}
@@ -366,17 +371,17 @@ def run_ours(args, rank, world, local):
 
     # ---- checkpoint image emit (timed on its own; not part of the step's bytes) --------
     img = torch.empty(rs.image_bytes(n), dtype=torch.uint8, device=dev)
-    ims = []
-    for _ in range(3):
+    im_ev = []
+    for _ in range(4):                  # back to back, the first dropped as above
         e_a = torch.cuda.Event(enable_timing=True)
         e_b = torch.cuda.Event(enable_timing=True)
         e_a.record(stream)
         ctx.image_write(t_step[0], w, m, v, img)
         e_b.record(stream)
-        torch.cuda.synchronize(dev)
-        ims.append(e_a.elapsed_time(e_b))
+        im_ev.append((e_a, e_b))
+    torch.cuda.synchronize(dev)
     del img
-    im_ms = statistics.mean(ims)
+    im_ms = statistics.mean(a_.elapsed_time(b_) for a_, b_ in im_ev[1:])
     image_emit = {"bytes": rs.image_bytes(n), "dst": "device buffer", "ms": im_ms,
                   "gbs_read_plus_write": (b_w + 8 + 12) * n / (im_ms * 1e-3) / 1e9}
 
