@@ -27,6 +27,7 @@ constexpr uint32_t kFlagNonfinite = 0x1u;
 constexpr uint32_t kFlagTimeoutReduce = 0x2u;
 constexpr uint32_t kFlagTimeoutAdamw = 0x4u;
 constexpr uint32_t kFlagTimeoutLeaves = 0x8u;
+constexpr uint64_t kNoChunk = ~0ull;     // ring-stage marker of the persistent kernels: no chunk follows
 
 // PF61 modulus p = 2^61 - 1 and multiplier K = floor(2^61 (sqrt5 - 1)/2).
 constexpr uint64_t kP61 = 0x1FFFFFFFFFFFFFFFull;
@@ -99,11 +100,13 @@ struct Ar {
 
 // Device-side scalars kept in the workspace.
 struct Scalars {
-    float norm;        // pre-clip global norm of the last clip
-    float scale;       // clip scale of the last clip
-    uint32_t flags;    // REPSTEP_FLAG_* bits
-    uint32_t aux;      // scratch flag of host-driven checks (image narrowing)
-    uint64_t root;     // last Merkle root
+    float norm;           // pre-clip global norm of the last clip
+    float scale;          // clip scale of the last clip
+    uint32_t flags;       // REPSTEP_FLAG_* bits
+    uint32_t aux;         // scratch flag of host-driven checks (image narrowing)
+    uint64_t root;        // last Merkle root
+    uint32_t next_chunk;  // work counter of the running reduce (zeroed before each launch)
+    uint32_t spare;
 };
 
 // ----------------------------------------------------------------------------------
@@ -197,6 +200,21 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
 __device__ __forceinline__ void named_barrier(uint32_t id, uint32_t nthreads)
 {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Named barrier that also returns, to every participating thread, the OR of `pred` over
+// all of them (whole warps only, like bar.sync).
+__device__ __forceinline__ bool named_barrier_or(uint32_t id, uint32_t nthreads, bool pred)
+{
+    uint32_t r;
+    asm volatile("{\n\t.reg .pred p, q;\n\t"
+                 "setp.ne.u32 p, %1, 0;\n\t"
+                 "bar.red.or.pred q, %2, %3, p;\n\t"
+                 "selp.u32 %0, 1, 0, q;\n\t}"
+                 : "=r"(r)
+                 : "r"(pred ? 1u : 0u), "r"(id), "r"(nthreads)
+                 : "memory");
+    return r != 0;
 }
 
 // ----------------------------------------------------------------------------------

@@ -90,6 +90,9 @@ cudaError_t launch_adamw(const AdamwShape &s, const AdamwArgs &args, int grid, s
 {
     AdamwKernelFn f = pick(s);
     if (!f) return cudaErrorInvalidValue;
+    // the kernel hands out chunks from this counter
+    cudaError_t e = cudaMemsetAsync(&args.sc->next_chunk, 0, sizeof(uint32_t), st);
+    if (e != cudaSuccess) return e;
     void *params[] = {const_cast<AdamwArgs *>(&args)};
     return cudaLaunchKernel(reinterpret_cast<const void *>(f), dim3(grid), dim3(s.nt + 64),
                             params, smem, st);

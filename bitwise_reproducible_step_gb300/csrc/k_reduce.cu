@@ -50,6 +50,9 @@ cudaError_t launch_reduce(const ReduceShape &s, const ReduceArgs &args, int grid
 {
     ReduceKernelFn f = pick(s);
     if (!f) return cudaErrorInvalidValue;
+    // the kernel hands out chunks from this counter
+    cudaError_t e = cudaMemsetAsync(&args.sc->next_chunk, 0, sizeof(uint32_t), st);
+    if (e != cudaSuccess) return e;
     void *params[] = {const_cast<ReduceArgs *>(&args)};
     return cudaLaunchKernel(reinterpret_cast<const void *>(f), dim3(grid), dim3(s.nt + 32),
                             params, smem, st);

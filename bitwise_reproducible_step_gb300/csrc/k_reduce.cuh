@@ -219,7 +219,14 @@ __global__ void __launch_bounds__(NT + 32, 1) k_reduce(const __grid_constant__ R
     constexpr uint32_t ESZ = DT == 0 ? 4u : 2u;
     constexpr uint32_t VEC = 16u / ESZ;
     constexpr int LOG2RG = RG == 8 ? 3 : (RG == 4 ? 2 : (RG == 2 ? 1 : 0));
-    static_assert(16 * kMaxStages + 2 * TPC * W * 4 + 8 <= kRingOffset, "smem header");
+    // Chunks handed out at run time (fp32 gradients) or by CTA index (bf16 gradients).
+    // The run-time order lets CTAs on faster or earlier-free SMs take more chunks
+    // (measured: fp32 reduce 6.34 -> 6.02 ms at 1.2e9 parameters); its per-chunk vote and
+    // index read cost the instruction-heavier bf16 reduce more than it gains (3e9 bf16
+    // gradients: 9.12 -> 9.75 ms).
+    constexpr bool DYN = DT == 0;
+    static_assert(16 * kMaxStages + 2 * TPC * W * 4 + 8 + 8 * kMaxStages <= kRingOffset,
+                  "smem header");
 
     extern __shared__ __align__(1024) unsigned char smem[];
     const uint32_t S = A.stages;
@@ -228,6 +235,8 @@ __global__ void __launch_bounds__(NT + 32, 1) k_reduce(const __grid_constant__ R
     float *red = reinterpret_cast<float *>(smem + 16 * kMaxStages);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(red + 2 * TPC * W);
     volatile int *never_flag = abort_flag + 1;   // stays 0: drain waits ignore the abort
+    // the chunk index each ring slot's stage opens (kNoChunk: the end of the work)
+    uint64_t *stage_chunk = reinterpret_cast<uint64_t *>(smem + 16 * kMaxStages + 2 * TPC * W * 4 + 8);
     unsigned char *ring = smem + kRingOffset;
 
     const int tid = threadIdx.x;
@@ -252,7 +261,14 @@ __global__ void __launch_bounds__(NT + 32, 1) k_reduce(const __grid_constant__ R
         uint32_t it = 0;
         RingPos pos;
         bool ok = true;
-        for (uint64_t k = A.chunk_lo + blockIdx.x; ok && k < A.chunk_hi; k += gridDim.x) {
+        // Chunks are handed out one at a time from a counter zeroed before the launch, so
+        // a CTA that starts late (its SM still busy with another stream's kernel) takes
+        // fewer and no SM idles while work is left.  Which CTA sums a chunk changes no bit.
+        // The next index is fetched one chunk ahead.
+        uint64_t k_next = A.chunk_lo + (DYN ? atomicAdd(&A.sc->next_chunk, 1u) : blockIdx.x);
+        while (ok && k_next < A.chunk_hi) {
+            const uint64_t k = k_next;
+            k_next = DYN ? A.chunk_lo + atomicAdd(&A.sc->next_chunk, 1u) : k + gridDim.x;
             const bool whole = k * kChunk >= A.begin && k * kChunk + kChunk <= A.end;
             for (int j = 0; ok && j < TPC; ++j) {
                 const uint64_t tb = k * kChunk + uint64_t(j) * TE;
@@ -269,6 +285,7 @@ __global__ void __launch_bounds__(NT + 32, 1) k_reduce(const __grid_constant__ R
                     }
                     const uint32_t nr = min(uint32_t(RG), R - q * RG);
                     const uint32_t fb = smem_u32(&full[slot]);
+                    if (DYN && j == 0 && q == 0) stage_chunk[slot] = k;   // published by the arrive
                     mbar_arrive_expect_tx(fb, bytes * nr);
                     if (bytes) {
                         const uint32_t dst = smem_u32(ring + slot * A.stage_stride) + soff;
@@ -282,6 +299,18 @@ __global__ void __launch_bounds__(NT + 32, 1) k_reduce(const __grid_constant__ R
                     ++it;
                     pos.advance(S);
                 }
+            }
+        }
+        // with run-time chunks, one more stage, without data, carries the end marker
+        if (DYN && ok) {
+            const uint32_t slot = pos.slot;
+            if (mbar_wait_bounded(smem_u32(&empty[slot]), pos.phase ^ 1u, abort_flag)) {
+                stage_chunk[slot] = kNoChunk;
+                mbar_arrive(smem_u32(&full[slot]));
+                ++it;
+                pos.advance(S);
+            } else {
+                ok = false;
             }
         }
         if (!ok) {
@@ -304,7 +333,30 @@ __global__ void __launch_bounds__(NT + 32, 1) k_reduce(const __grid_constant__ R
     RingPos pos;
     int cb = 0;
     bool aborted = false;
-    for (uint64_t k = A.chunk_lo + blockIdx.x; k < A.chunk_hi; k += gridDim.x) {
+    for (uint32_t ci = 0;; ++ci) {
+        uint64_t k = A.chunk_lo + blockIdx.x + uint64_t(ci) * gridDim.x;
+        if (!DYN && k >= A.chunk_hi) break;
+        if (DYN) {
+            // The stage that opens the next chunk carries its index, or the end marker.
+            // Every compute thread reads it and one barrier vote makes the decision
+            // uniform, so all warps run the same number of chunks through the chunk-tree
+            // barriers below (a failed wait votes for the end too).  The chunk's first
+            // wait below then returns at once.
+            const uint32_t slot0 = pos.slot;
+            bool got = false;
+            if (!aborted) {
+                got = mbar_wait_bounded(smem_u32(&full[slot0]), pos.phase, abort_flag);
+                if (!got) {
+                    aborted = true;
+                    if (lane == 0) {
+                        atomicOr(&A.sc->flags, kFlagTimeoutReduce);
+                        *abort_flag = 1;
+                    }
+                }
+            }
+            k = got ? stage_chunk[slot0] : kNoChunk;
+            if (named_barrier_or(2, NT, k == kNoChunk)) break;
+        }
         float part[TPC];
         const bool whole = k * kChunk >= A.begin && k * kChunk + kChunk <= A.end;
 #pragma unroll

@@ -252,8 +252,19 @@ cudaError_t launch_norm(const float *in, uint64_t count, float *out, Scalars *sc
 
 cudaError_t merkle_prepare()
 {
-    // two 1024-digest buffers are 16 KB of static shared memory: nothing to opt into
-    return cudaSuccess;
+    // The root passes may run on a second stream beside the next reduce, whose persistent
+    // CTAs need most of an SM's shared memory.  An SM whose L1/shared split was set for a
+    // small kernel cannot take such a CTA until it drains, so these kernels ask for the
+    // largest shared-memory carveout too: then a reduce CTA fits beside their blocks
+    // (registers: 544 x 96 + 256 x 48 <= 65536).
+    cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void *>(k_merkle),
+                                         cudaFuncAttributePreferredSharedMemoryCarveout,
+                                         int(cudaSharedmemCarveoutMaxShared));
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(reinterpret_cast<const void *>(k_leaf_fix),
+                                 cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 int(cudaSharedmemCarveoutMaxShared));
+    return e;
 }
 
 cudaError_t launch_merkle(const uint64_t *in, uint64_t count, uint64_t *out, int header_mode,
