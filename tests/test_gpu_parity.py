@@ -544,3 +544,39 @@ def test_workload_flat12m8_student_t_full():
         assert img.cpu().numpy().tobytes() == O.image(t, ow, om, ov)
         clipped += ref["norm"] > 1.0
     assert img.numel() == 153_600_008
+
+
+@pytest.mark.parametrize("hash_stream", [False, True])
+def test_steps_beside_a_busy_stream(hash_stream):
+    """The fp32 reduce and AdamW hand out chunks at run time, so which CTA sums which chunk
+    depends on when each CTA starts.  Steps run while another stream keeps the SMs busy
+    with matrix products; every output bit must still equal the oracle's."""
+    n, R = 4_000_000 + 123, 8
+    dev = torch.device("cuda", 0)
+    ctx = rs.Repstep(n, device=dev)
+    side = torch.cuda.Stream(dev)
+    ctx.set_hash_stream(torch.cuda.Stream(dev) if hash_stream else None)
+    w, m, v = I.gen_state(U.F32_WL, n=n, device=dev)
+    ow, om, ov = w.cpu().numpy(), m.cpu().numpy(), v.cpu().numpy()
+    a = torch.randn(4096, 4096, device=dev)
+    norm = torch.empty(1, dtype=torch.float32, device=dev)
+    root = torch.empty(1, dtype=torch.int64, device=dev)
+    for t in (1, 2):
+        grads = U.gen_grads(n, R, t)
+        gnp = U.oracle_grads(grads)
+        torch.cuda.synchronize(dev)
+        with torch.cuda.stream(side):
+            b = a
+            for _ in range(6):
+                b = b @ a
+        ctx.step(grads, w, m, v, U.hp_for(t), step=t, norm_out=norm, root_out=root)
+        ctx.sync()
+        side.synchronize()
+        ref = U.oracle_step(gnp, ow, om, ov, t)
+        ow, om, ov = ref["w"], ref["m"], ref["v"]
+        U.assert_same_f32(w, ow, f"w step {t}")
+        U.assert_same_f32(m, om, f"m step {t}")
+        U.assert_same_f32(v, ov, f"v step {t}")
+        U.assert_same_f32(norm, np.array([ref["norm"]], np.float32), f"norm step {t}")
+        assert U.root_of(root) == ref["root"], f"root step {t}"
+    del b
