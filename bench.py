@@ -165,10 +165,18 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback (6.8 TB/s, one earlier GB300 copy measurement)"
 
 
+def _code_only(text: str) -> str:
+    """C++ source without comments and blank space, so that editing a comment keeps a
+    recorded traffic figure valid while any change to the code drops it."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_source_hash(kernel: str):
     h = hashlib.sha256()
     for rel in KERNEL_SOURCES[kernel]:
-        h.update(open(os.path.join(ROOT, rel), "rb").read())
+        h.update(_code_only(open(os.path.join(ROOT, rel), encoding="utf-8").read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -18,8 +18,10 @@
 // one 4-element group (a 16-byte float4, or 8 bytes of bf16) per replica per tile, sum
 // the replicas in registers with a binary-carry stack that reproduces the canonical tree
 // for any R, multiply by fp32(1/R), store g with 16-byte stores and fold g*g into the
-// chunk tree.  No atomics touch data: every sum has one fixed order.  The grid size and
-// NT change which CTA does which chunk, never any rounding.
+// chunk tree.  With fp32 gradients the chunks are handed out at run time from a counter
+// (the kernel's only atomic, on an index, never on data); with bf16 gradients by CTA
+// index.  Every sum has one fixed order: the grid size, NT and the chunk order change
+// which CTA does which chunk, never any rounding.
 #pragma once
 
 #include "common.cuh"
