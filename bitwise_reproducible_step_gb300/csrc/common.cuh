@@ -177,6 +177,17 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
     return false;
 }
 
+// Before the producer refills a ring slot: the consumers' reads of the slot are generic-
+// proxy loads, the refill is an async-proxy (bulk-copy) write, and only a proxy fence
+// orders the two.  The producer lane runs it after the slot's empty barrier completes
+// (which makes every consumer read happen before it) and before it issues the copies.
+// Without it a refill overtook a read still in flight: about 1 run in 80 of a 268M-
+// parameter step with 256-thread AdamW CTAs had a warp read part of the next tile.
+__device__ __forceinline__ void fence_reads_before_refill()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // L2 policy for data read exactly once (replica gradients, optimizer state).
 __device__ __forceinline__ uint64_t l2_evict_first()
 {

@@ -28,6 +28,46 @@ __global__ void __launch_bounds__(256) k_selftest_div(uint32_t b_begin, uint32_t
     if (bad) atomicAdd(mismatches, bad);
 }
 
+// Self-test of the branch-free square root, reciprocal and division against the IEEE
+// operations.  which 0: sqrt_rn_fast(x) for the float bit patterns [begin, begin + count);
+// 1: rcp_rn_fast(b) for those patterns; 2: div_rn_fast(a, b) for count x 1024 pseudo-random
+// pairs from `seed`: b in [2^-41, 2^41), a = +-0 or |a| in [2^-85, 2^81), either sign.
+__device__ __forceinline__ uint64_t st_mix(uint64_t z)
+{
+    z += 0x9E3779B97F4A7C15ull;
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    return z ^ (z >> 31);
+}
+
+__global__ void __launch_bounds__(256) k_selftest_fast_math(int which, uint32_t begin,
+                                                            uint32_t count, uint64_t seed,
+                                                            unsigned long long *mismatches)
+{
+    unsigned long long bad = 0;
+    const uint64_t total = which == 2 ? uint64_t(count) * 1024u : uint64_t(count);
+    const uint64_t stride = uint64_t(gridDim.x) * blockDim.x;
+    for (uint64_t i = uint64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < total; i += stride) {
+        if (which == 0) {
+            const float x = __uint_as_float(begin + uint32_t(i));
+            bad += __float_as_uint(sqrt_rn_fast(x)) != __float_as_uint(__fsqrt_rn(x));
+        } else if (which == 1) {
+            const float b = __uint_as_float(begin + uint32_t(i));
+            bad += __float_as_uint(rcp_rn_fast(b)) != __float_as_uint(__frcp_rn(b));
+        } else {
+            const uint64_t r = st_mix(seed ^ (i * 0xD1B54A32D192ED03ull));
+            const uint32_t b_lo = 0x2B000000u, b_hi = 0x54000000u;     // 2^-41, 2^41
+            const uint32_t a_lo = 0x15000000u, a_hi = 0x68000000u;     // 2^-85, 2^81
+            const float b = __uint_as_float(b_lo + uint32_t(r % (b_hi - b_lo)));
+            uint32_t ab = a_lo + uint32_t((r >> 32) % (a_hi - a_lo));
+            if (((r >> 58) & 63u) == 0u) ab = 0u;                       // zeros now and then
+            const float a = __uint_as_float(ab | (uint32_t(r >> 57) & 1u) << 31);
+            bad += __float_as_uint(div_rn_fast(a, b)) != __float_as_uint(__fdiv_rn(a, b));
+        }
+    }
+    if (bad) atomicAdd(mismatches, bad);
+}
+
 // The leaves-only mode has one (IEEE) instantiation; the others follow the arithmetic mode.
 AdamwKernelFn pick(const AdamwShape &s)
 {
@@ -82,6 +122,13 @@ cudaError_t launch_selftest_div(uint32_t b_begin, uint32_t b_count, unsigned lon
                                cudaStream_t st)
 {
     k_selftest_div<<<152 * 8, 256, 0, st>>>(b_begin, b_count, mismatches);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_selftest_fast_math(int which, uint32_t begin, uint32_t count, uint64_t seed,
+                                      unsigned long long *mismatches, cudaStream_t st)
+{
+    k_selftest_fast_math<<<152 * 8, 256, 0, st>>>(which, begin, count, seed, mismatches);
     return cudaGetLastError();
 }
 

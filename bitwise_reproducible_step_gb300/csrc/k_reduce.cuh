@@ -285,6 +285,7 @@ __global__ void __launch_bounds__(NT + 32, 1) k_reduce(const __grid_constant__ R
                         ok = false;
                         break;
                     }
+                    fence_reads_before_refill();
                     const uint32_t nr = min(uint32_t(RG), R - q * RG);
                     const uint32_t fb = smem_u32(&full[slot]);
                     if (DYN && j == 0 && q == 0) stage_chunk[slot] = k;   // published by the arrive
@@ -402,7 +403,7 @@ __global__ void __launch_bounds__(NT + 32, 1) k_reduce(const __grid_constant__ R
                                                           A.grads[q * RG + i], e0, tr.a, tr.b);
                         }
                     }
-                    __syncwarp();
+                            __syncwarp();
                     if (lane == 0) mbar_arrive(smem_u32(&empty[slot]));
                     pos.advance(S);
                     if (R == uint32_t(RG)) {
@@ -454,7 +455,7 @@ __global__ void __launch_bounds__(NT + 32, 1) k_reduce(const __grid_constant__ R
                             }
                         }
                     }
-                    __syncwarp();
+                            __syncwarp();
                     if (lane == 0) mbar_arrive(smem_u32(&empty[slot]));
                     pos.advance(S);
                 }

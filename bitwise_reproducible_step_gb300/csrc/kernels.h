@@ -63,7 +63,7 @@ struct AdamwArgs {
     uint32_t stages, stage_stride;
     float lr, beta1, beta2, eps, bc1, bc2, om1, om2, delta;
     float rbc1, rbc2;         // RN(1/bc1), RN(1/bc2): divisors fixed for the launch
-    int fastdiv;              // both bias corrections in [2^-40, 2]
+    int fastdiv;              // bias corrections in [2^-40, 2], eps in [2^-40, 2^20]
     const uint32_t *decay_mask;   // null: every element decays; else bit e%32 of word e/32
 };
 
@@ -85,6 +85,8 @@ AdamwKernelFn pick_adamw_ieee(const AdamwShape &s);
 AdamwKernelFn pick_adamw_ftz(const AdamwShape &s);
 cudaError_t launch_selftest_div(uint32_t b_begin, uint32_t b_count, unsigned long long *mismatches,
                                cudaStream_t st);
+cudaError_t launch_selftest_fast_math(int which, uint32_t begin, uint32_t count, uint64_t seed,
+                                      unsigned long long *mismatches, cudaStream_t st);
 
 // Small kernels (k_small.cu).
 cudaError_t launch_init_powers(uint64_t *powers, cudaStream_t st);

@@ -365,8 +365,11 @@ int do_adamw(repstep_ctx *x, void *w, float *m, float *v, const repstep_hparams 
     // reciprocals of the bias corrections for the fixed-divisor division in k_adamw
     a.rbc1 = one / a.bc1;
     a.rbc2 = one / a.bc2;
-    const float lo = std::ldexp(1.0f, -40), hi = 2.0f;
-    a.fastdiv = (a.bc1 >= lo && a.bc1 <= hi && a.bc2 >= lo && a.bc2 <= hi) ? 1 : 0;
+    // the branch-free divisions and square roots of k_adamw hold for bias corrections in
+    // [2^-40, 2] and eps in [2^-40, 2^20]; otherwise every element takes the IEEE path
+    const float lo = std::ldexp(1.0f, -40), hi = 2.0f, eps_hi = std::ldexp(1.0f, 20);
+    a.fastdiv = (a.bc1 >= lo && a.bc1 <= hi && a.bc2 >= lo && a.bc2 <= hi && a.eps >= lo &&
+                 a.eps <= eps_hi) ? 1 : 0;
     a.decay_mask = x->decay_mask;
     const int nt = x->nt_adamw;
     // PF61 mode: AdamW fused with the leaf digests; audit mode: AdamW alone (the BLAKE2b
@@ -1093,6 +1096,19 @@ int repstep_selftest_fixed_division(uint32_t b_sig_begin, uint32_t b_sig_count,
 }
 
 uint64_t repstep_launch_count(const repstep_ctx *ctx) { return ctx ? ctx->launches : 0; }
+
+int repstep_selftest_fast_math(int which, uint32_t begin, uint32_t count, uint64_t seed,
+                               uint64_t *d_mismatches, void *stream)
+{
+    if (!d_mismatches || !aligned(d_mismatches, 8)) return REPSTEP_ERR_ARG;
+    if (which < 0 || which > 2) return REPSTEP_ERR_ARG;
+    if (which < 2 && uint64_t(begin) + count > (1ull << 32)) return REPSTEP_ERR_ARG;
+    if (count == 0) return REPSTEP_OK;
+    const cudaError_t e = launch_selftest_fast_math(
+        which, begin, count, seed, reinterpret_cast<unsigned long long *>(d_mismatches),
+        static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? REPSTEP_OK : REPSTEP_ERR_CUDA;
+}
 
 int repstep_last_cuda_error(const repstep_ctx *ctx) { return ctx ? ctx->last_err : 0; }
 

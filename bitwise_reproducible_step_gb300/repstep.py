@@ -73,7 +73,7 @@ EXPORTS = [
     "repstep_selftest_fixed_division", "repstep_reduce_paper", "repstep_checkpoint_save",
     "repstep_checkpoint_load", "repstep_set_decay_mask", "repstep_decay_mask_from_segments",
     "repstep_reduce_paper_accum", "repstep_set_hash_stream", "repstep_wait_hash",
-    "repstep_leaves",
+    "repstep_leaves", "repstep_selftest_fast_math",
 ]
 NOALLOC_MAX_N = 1 << 30
 
@@ -118,6 +118,7 @@ def lib():
     L.repstep_strerror.argtypes = [C.c_int]
     L.repstep_strerror.restype = C.c_char_p
     L.repstep_selftest_fixed_division.argtypes = [u32, u32, vp, vp]
+    L.repstep_selftest_fast_math.argtypes = [C.c_int, u32, u32, u64, vp, vp]
     L.repstep_reduce_paper.argtypes = [vp, C.POINTER(vp), u32, u32, u64, u64]
     L.repstep_checkpoint_save.argtypes = [vp, C.c_char_p, i32, vp, vp, vp]
     L.repstep_checkpoint_load.argtypes = [vp, C.c_char_p, C.POINTER(i32), vp, vp, vp]
@@ -206,6 +207,22 @@ def selftest_fixed_division(b_sig_begin: int = 0, b_sig_count: int = 1 << 23) ->
     _check(lib().repstep_selftest_fixed_division(b_sig_begin, b_sig_count, _ptr(out),
                                                  C.c_void_p(torch.cuda.current_stream().cuda_stream)),
            "selftest_fixed_division")
+    return int(out.item())
+
+
+SQRT_FAST_BITS = (0x0C800000, 0x68000000)     # [2^-102, 2^81): the fast square root's range
+RCP_FAST_BITS = (0x2A800000, 0x54800000)      # [2^-42, 2^42): the fast reciprocal's range
+
+
+def selftest_fast_math(which: int, begin: int = 0, count: int = 0, seed: int = 0) -> int:
+    """Mismatches between the AdamW kernel's branch-free square root (which=0),
+    reciprocal (1) or division (2, count x 1024 random pairs) and the IEEE operations (see
+    repstep_selftest_fast_math)."""
+    out = torch.zeros(1, dtype=torch.int64, device="cuda")
+    _check(lib().repstep_selftest_fast_math(int(which), int(begin), int(count), int(seed),
+                                            _ptr(out),
+                                            C.c_void_p(torch.cuda.current_stream().cuda_stream)),
+           "selftest_fast_math")
     return int(out.item())
 
 

@@ -336,6 +336,23 @@ int repstep_sync(repstep_ctx *ctx, uint32_t *flags_out);
 int repstep_selftest_fixed_division(uint32_t b_sig_begin, uint32_t b_sig_count,
                                     uint64_t *d_mismatches, void *stream);
 
+/* Self-test of the branch-free square root, reciprocal and division of the AdamW kernel's
+ * fast path (Newton iterations from the hardware approximations, then Markstein's
+ * correction).  The kernel takes that path when every lane of a warp has m' zero or of
+ * magnitude in [2^-84, 2^40] and v' zero or in [2^-100, 2^40], and the bias corrections
+ * are in [2^-40, 2] and eps in [2^-40, 2^20]; then sqrt(v'/bc2) has an argument in
+ * [2^-101, 2^80] and the update divides a numerator in [2^-85, 2^80] by a denominator in
+ * [2^-40, 2^41).  which = 0: the square root of every float whose bit pattern is in
+ * [begin, begin+count); 1: the reciprocal of every such float; 2: count x 1024
+ * pseudo-random divisions drawn from `seed`, with divisor in [2^-41, 2^41) and dividend 0
+ * or of magnitude in [2^-85, 2^81), either sign.  Each result is compared with the IEEE
+ * operation, and the number that differ is added to *d_mismatches (a device u64 the
+ * caller zeroes).  The whole square-root range 0x0C800000..0x68000000 ([2^-102, 2^81)) and
+ * reciprocal range 0x2A800000..0x54800000 ([2^-42, 2^42)) find none.  Returns
+ * REPSTEP_ERR_ARG for which outside 0..2 or a bit range past 2^32. */
+int repstep_selftest_fast_math(int which, uint32_t begin, uint32_t count, uint64_t seed,
+                               uint64_t *d_mismatches, void *stream);
+
 /* Kernels this context has launched so far. */
 uint64_t repstep_launch_count(const repstep_ctx *ctx);
 
