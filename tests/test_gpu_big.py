@@ -309,3 +309,33 @@ def test_flat1200m_r8_bf16w_decay_mask_ftz():
         for a, arr in enumerate((O.widen_bf16(w1), m1, v1)):
             assert leaves[1 + a * c + k] == O.pf61(arr.view(np.uint32)), f"leaf {a} chunk {k}"
     assert U.root_of(root) == O.merkle_root(leaves)
+
+
+@pytest.mark.parametrize("nt", [256, 512])
+def test_repeated_steps_are_bit_identical(nt):
+    """The same step, from the same state, 200 times: every output bit must repeat.  This
+    caught a ring-refill race (a bulk copy overtaking a consumer's read of the previous
+    tile) that hit about one run in 80 with 256-thread AdamW CTAs."""
+    wl = I.WORKLOADS["flat268m_r32_topologies"]
+    n, R = wl.n, wl.R
+    dev = torch.device("cuda", 0)
+    grads = [I.gen_grad(wl, 1, r, device=dev) for r in range(R)]
+    w0, m0, v0 = I.gen_state(wl, device=dev)
+    m0.copy_(I.gen_grad(wl, 9, 0, device=dev))
+    v0.copy_(I.gen_grad(wl, 9, 1, device=dev).square())
+    hp = U.hp_for(3)
+    ctx = rs.Repstep(n, device=dev, block_threads=nt)
+    w, m, v = w0.clone(), m0.clone(), v0.clone()
+    root = torch.empty(1, dtype=torch.int64, device=dev)
+    ref = None
+    for _ in range(200):
+        w.copy_(w0); m.copy_(m0); v.copy_(v0)
+        ctx.step(grads, w, m, v, hp, step=3, root_out=root)
+        assert ctx.sync() == 0
+        if ref is None:
+            ref = (w.clone(), m.clone(), v.clone(), U.root_of(root))
+            continue
+        assert U.root_of(root) == ref[3]
+        assert torch.equal(w.view(torch.int32), ref[0].view(torch.int32))
+    assert torch.equal(m.view(torch.int32), ref[1].view(torch.int32))
+    assert torch.equal(v.view(torch.int32), ref[2].view(torch.int32))
