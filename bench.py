@@ -282,6 +282,13 @@ def run_ours(args, rank, world, local):
         t_step[0] += 1
         nr = norm if slot is None else norms[slot:slot + 1]
         rt = root if slot is None else roots[slot:slot + 1]
+        if args.graph:
+            # the kept graphs hold the norm output: a fixed one, copied out for the log
+            ctx.step_graph(grads, w, m, v, hp(t_step[0]), step=t_step[0], norm_out=norm,
+                           root_out=rt, nodes=args.nodes)
+            if slot is not None and args.log:
+                nr.copy_(norm)
+            return
         if not args.paper_shard:
             ctx.step(grads, w, m, v, hp(t_step[0]), step=t_step[0], norm_out=nr, root_out=rt,
                      nodes=args.nodes)
@@ -425,7 +432,8 @@ def run_ours(args, rank, world, local):
     torch.cuda.empty_cache()
     cpu = None
     variant = (args.param_dtype != "f32" or args.decay_mask or args.hash_mode != "pf61"
-               or args.subnormals != "ieee" or bool(args.paper_shard) or args.nodes > 1)
+               or args.subnormals != "ieee" or bool(args.paper_shard) or args.nodes > 1
+               or args.graph)
     if rank == 0 and not args.skip_cpu_baseline and not variant:
         cpu = cpu_baseline(wl, n, R, dev, args.cpu_seconds)
 
@@ -442,10 +450,13 @@ def run_ours(args, rank, world, local):
                          f"{(R * b_g + 32) * n / 1e9:.1f} GB moved per step",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "launch": "persistent grid (SM count x resident CTAs), "
-                             f"{args.block_threads or 512} compute threads",
+                             f"{args.block_threads or 512} compute threads"
+                             + ("; reduce + clip and AdamW as launches of kept CUDA "
+                                "graphs" if args.graph else ""),
                    "hash_leaves": args.hash_mode, "param_dtype": args.param_dtype,
                    "decay_mask": bool(args.decay_mask), "subnormals": args.subnormals,
                    "hash_stream": bool(args.hash_stream),
+                   "step_graph": bool(args.graph),
                    "reduce_order": (f"paper-exact, dp_shard {args.paper_shard}"
                                     + (f", accum {args.accum}" if args.accum else "")
                                     if args.paper_shard else
@@ -646,11 +657,16 @@ def main():
     ap.add_argument("--log", default="",
                     help="append a JSON-lines record per timed step (norm, its bits, root, "
                          "event time) and the summary line to this file")
+    ap.add_argument("--graph", action="store_true",
+                    help="run the timed steps' reduce + clip and AdamW as launches of kept "
+                         "CUDA graphs (repstep_step_graph)")
     ap.add_argument("--n", type=int, default=0,
                     help="override the workload's parameter count (small profiling cases)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.graph and args.paper_shard:
+        ap.error("--graph runs the canonical-tree step; it does not take --paper-shard")
 
     if args.impl == "reference":
         world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -132,6 +132,18 @@ struct repstep_ctx {
     cudaEvent_t ev_state = nullptr, ev_hash = nullptr;
     bool hash_pending = false;
     std::vector<uint64_t> cut_norm, cut_leaf;   // chunks cut by range boundaries
+    // the graphs of repstep_step_graph, captured on a private stream and instantiated:
+    // [0] the reduce and the clip, [1] AdamW, whose node's hyperparameters replays rewrite
+    struct StepGraph {
+        cudaStream_t capture = nullptr;
+        cudaGraph_t graph[2] = {nullptr, nullptr};   // kept: updates address their nodes
+        cudaGraphExec_t exec[2] = {nullptr, nullptr};
+        uint64_t kernels[2] = {0, 0};                // kernels one launch of each runs
+        cudaGraphNode_t adamw = nullptr;
+        std::vector<uintptr_t> key;                  // pointers and shape captured for
+        uint64_t captures = 0, replays = 0;
+        bool recording = false;                      // a capture is in progress
+    } sg;
 
     float *g() const { return reinterpret_cast<float *>(ws + lay.g); }
     float *chunk_sq() const { return reinterpret_cast<float *>(ws + lay.chunk_sq); }
@@ -152,6 +164,21 @@ struct repstep_ctx {
 };
 
 namespace {
+
+// While a step graph is being captured: the node the last launch on the context's stream
+// added (the capture's only dependency at that point).  Left unset when that is not one
+// node, and replays then capture the step again.
+void note_node(repstep_ctx *x, cudaGraphNode_t *slot)
+{
+    if (!x->sg.recording) return;
+    cudaStreamCaptureStatus status = cudaStreamCaptureStatusNone;
+    const cudaGraphNode_t *deps = nullptr;
+    size_t nd = 0;
+    const cudaError_t e = cudaStreamGetCaptureInfo(x->stream, &status, nullptr, nullptr, &deps,
+                                                   nullptr, &nd);
+    *slot = (e == cudaSuccess && status == cudaStreamCaptureStatusActive && nd == 1) ? deps[0]
+                                                                                      : nullptr;
+}
 
 // Order the context's stream after a root still running on the hash stream: called before
 // anything that writes the leaves, the Merkle partials or the state the root passes read.
@@ -316,6 +343,32 @@ int do_clip(repstep_ctx *x, float clip, float *norm_out, float *scale_out)
     return REPSTEP_OK;
 }
 
+// The hyperparameters of an AdamW launch and the constants derived from them, each
+// operation flushed in the flush-to-zero mode like every device operation.
+void adamw_hparams(const repstep_ctx *x, const repstep_hparams *hp, AdamwArgs &a)
+{
+    const int fz = x->fz();
+    a.lr = hflush(fz, hp->lr);
+    a.beta1 = hflush(fz, hp->beta1);
+    a.beta2 = hflush(fz, hp->beta2);
+    a.eps = hflush(fz, hp->eps);
+    a.bc1 = hflush(fz, hp->bc1);
+    a.bc2 = hflush(fz, hp->bc2);
+    const float one = 1.0f;
+    a.om1 = hflush(fz, one - a.beta1);
+    a.om2 = hflush(fz, one - a.beta2);
+    const float lrwd = hmul(fz, a.lr, hflush(fz, hp->weight_decay));
+    a.delta = hflush(fz, one - lrwd);
+    // reciprocals of the bias corrections for the fixed-divisor division in k_adamw
+    a.rbc1 = one / a.bc1;
+    a.rbc2 = one / a.bc2;
+    // the branch-free divisions and square roots of k_adamw hold for bias corrections in
+    // [2^-40, 2] and eps in [2^-40, 2^20]; otherwise every element takes the IEEE path
+    const float lo = std::ldexp(1.0f, -40), hi = 2.0f, eps_hi = std::ldexp(1.0f, 20);
+    a.fastdiv = (a.bc1 >= lo && a.bc1 <= hi && a.bc2 >= lo && a.bc2 <= hi && a.eps >= lo &&
+                 a.eps <= eps_hi) ? 1 : 0;
+}
+
 int do_adamw(repstep_ctx *x, void *w, float *m, float *v, const repstep_hparams *hp,
              uint64_t begin, uint64_t count)
 {
@@ -348,34 +401,13 @@ int do_adamw(repstep_ctx *x, void *w, float *m, float *v, const repstep_hparams 
     a.end = end;
     a.chunk_lo = begin / kChunk;
     a.chunk_hi = (end + kChunk - 1) / kChunk;
-    // hyperparameters and the constants derived from them, each operation flushed in the
-    // flush-to-zero mode like every device operation
-    const int fz = x->fz();
-    a.lr = hflush(fz, hp->lr);
-    a.beta1 = hflush(fz, hp->beta1);
-    a.beta2 = hflush(fz, hp->beta2);
-    a.eps = hflush(fz, hp->eps);
-    a.bc1 = hflush(fz, hp->bc1);
-    a.bc2 = hflush(fz, hp->bc2);
-    const float one = 1.0f;
-    a.om1 = hflush(fz, one - a.beta1);
-    a.om2 = hflush(fz, one - a.beta2);
-    const float lrwd = hmul(fz, a.lr, hflush(fz, hp->weight_decay));
-    a.delta = hflush(fz, one - lrwd);
-    // reciprocals of the bias corrections for the fixed-divisor division in k_adamw
-    a.rbc1 = one / a.bc1;
-    a.rbc2 = one / a.bc2;
-    // the branch-free divisions and square roots of k_adamw hold for bias corrections in
-    // [2^-40, 2] and eps in [2^-40, 2^20]; otherwise every element takes the IEEE path
-    const float lo = std::ldexp(1.0f, -40), hi = 2.0f, eps_hi = std::ldexp(1.0f, 20);
-    a.fastdiv = (a.bc1 >= lo && a.bc1 <= hi && a.bc2 >= lo && a.bc2 <= hi && a.eps >= lo &&
-                 a.eps <= eps_hi) ? 1 : 0;
+    adamw_hparams(x, hp, a);
     a.decay_mask = x->decay_mask;
     const int nt = x->nt_adamw;
     // PF61 mode: AdamW fused with the leaf digests; audit mode: AdamW alone (the BLAKE2b
     // leaves are computed from the final state by repstep_root)
     const int mode = x->cfg.hash_mode == REPSTEP_HASH_BLAKE2B ? 2 : 0;
-    const AdamwShape shape{nt, mode, x->w_bf16(), fz, a.decay_mask ? 1 : 0};
+    const AdamwShape shape{nt, mode, x->w_bf16(), x->fz(), a.decay_mask ? 1 : 0};
     const size_t smem = adamw_smem_bytes(shape, a);
     cudaError_t e = adamw_prepare(shape, smem);
     if (e != cudaSuccess) return x->cuda_fail(e);
@@ -386,6 +418,7 @@ int do_adamw(repstep_ctx *x, void *w, float *m, float *v, const repstep_hparams 
     e = launch_adamw(shape, a, grid, smem, x->stream);
     if (e != cudaSuccess) return x->cuda_fail(e);
     ++x->launches;
+    note_node(x, &x->sg.adamw);
     if (mode == 0) note_cut_chunks(x->cut_leaf, begin, end, x->n);
     return REPSTEP_OK;
 }
@@ -600,6 +633,217 @@ cudaError_t narrow_host_to_device(repstep_ctx *x, unsigned short *d_w, const uns
     return cudaSuccess;
 }
 
+// One whole step: validate everything, then reduce -> clip -> AdamW -> root.
+int do_step(repstep_ctx *x, const void *const *grads, uint32_t R, uint32_t nodes, uint32_t gpn,
+            void *w, float *m, float *v, const repstep_hparams *hp, int32_t step,
+            float *norm_out, uint64_t *root_out)
+{
+    // validate everything before launching anything
+    if (!w || !m || !v) return REPSTEP_ERR_ARG;
+    if (!aligned(w, 16) || !aligned(m, 16) || !aligned(v, 16)) return REPSTEP_ERR_ALIGN;
+    int rc = check_hparams(hp);
+    if (rc) return rc;
+    if (!(hp->clip > 0.0f)) return REPSTEP_ERR_ARG;
+    if (norm_out && !aligned(norm_out, 4)) return REPSTEP_ERR_ALIGN;
+    if (root_out && !aligned(root_out, 8)) return REPSTEP_ERR_ALIGN;
+    x->reduced = 0;
+    x->cut_norm.clear();
+    rc = do_reduce(x, grads, R, nodes, gpn, 0, x->n);
+    if (rc) return rc;
+    rc = do_clip(x, hp->clip, norm_out, nullptr);
+    if (rc) return rc;
+    rc = do_adamw(x, w, m, v, hp, 0, x->n);
+    if (rc) return rc;
+    return do_root(x, step, root_out);
+}
+
+void drop_step_graph(repstep_ctx *x)
+{
+    for (int i = 0; i < 2; ++i) {
+        if (x->sg.exec[i]) cudaGraphExecDestroy(x->sg.exec[i]);
+        if (x->sg.graph[i]) cudaGraphDestroy(x->sg.graph[i]);
+        x->sg.exec[i] = nullptr;
+        x->sg.graph[i] = nullptr;
+        x->sg.kernels[i] = 0;
+    }
+    x->sg.adamw = nullptr;
+    x->sg.key.clear();
+}
+
+// What the step graphs are specific to: every pointer their nodes hold, the replica count
+// and topology, the clip threshold (an argument of the norm kernel) and the decay mask.
+// AdamW's hyperparameters are rewritten on each replay instead.
+std::vector<uintptr_t> step_key(const repstep_ctx *x, const void *const *grads, uint32_t R,
+                                uint32_t nodes, uint32_t gpn, const void *w, const float *m,
+                                const float *v, float clip, const float *norm_out)
+{
+    std::vector<uintptr_t> k;
+    k.reserve(R + 9);
+    uint32_t clip_bits = 0;
+    std::memcpy(&clip_bits, &clip, sizeof clip_bits);
+    k.push_back(R);
+    k.push_back(nodes);
+    k.push_back(gpn);
+    k.push_back(clip_bits);
+    for (const void *p : {static_cast<const void *>(w), static_cast<const void *>(m),
+                          static_cast<const void *>(v), static_cast<const void *>(norm_out),
+                          static_cast<const void *>(x->decay_mask)})
+        k.push_back(reinterpret_cast<uintptr_t>(p));
+    for (uint32_t r = 0; r < R; ++r) k.push_back(reinterpret_cast<uintptr_t>(grads[r]));
+    return k;
+}
+
+// Capture part i of the step (0: reduce + clip, 1: AdamW) on the private stream and
+// instantiate it.  The host-side call-order state moves on as the ordinary calls move it.
+int capture_part(repstep_ctx *x, int i, const void *const *grads, uint32_t R, uint32_t nodes,
+                 uint32_t gpn, void *w, float *m, float *v, const repstep_hparams *hp,
+                 float *norm_out)
+{
+    const cudaStream_t user = x->stream;
+    const uint64_t launches0 = x->launches;
+    // relaxed mode: besides kernels and memsets, the calls make only kernel-attribute and
+    // occupancy queries, which enqueue nothing
+    cudaError_t e = cudaStreamBeginCapture(x->sg.capture, cudaStreamCaptureModeRelaxed);
+    if (e != cudaSuccess) return x->cuda_fail(e);
+    x->stream = x->sg.capture;
+    x->sg.recording = true;
+    int rc;
+    if (i == 0) {
+        x->reduced = 0;
+        x->cut_norm.clear();
+        rc = do_reduce(x, grads, R, nodes, gpn, 0, x->n);
+        if (!rc) rc = do_clip(x, hp->clip, norm_out, nullptr);
+    } else {
+        rc = do_adamw(x, w, m, v, hp, 0, x->n);
+    }
+    x->sg.recording = false;
+    x->stream = user;
+    cudaGraph_t graph = nullptr;
+    e = cudaStreamEndCapture(x->sg.capture, &graph);
+    // nothing captured has run yet: the kernels are counted at each launch of the graph
+    x->sg.kernels[i] = x->launches - launches0;
+    x->launches = launches0;
+    if (rc || e != cudaSuccess) {
+        if (graph) cudaGraphDestroy(graph);
+        (void)cudaGetLastError();   // a failed capture leaves no error behind for others
+        return rc ? rc : x->cuda_fail(e);
+    }
+    size_t count = 0;
+    e = cudaGraphGetNodes(graph, nullptr, &count);
+    if (e != cudaSuccess || count == 0) {   // nothing to run (AdamW over n = 0)
+        cudaGraphDestroy(graph);
+        return e == cudaSuccess ? REPSTEP_OK : x->cuda_fail(e);
+    }
+    x->sg.graph[i] = graph;
+    e = cudaGraphInstantiate(&x->sg.exec[i], graph, 0);
+    if (e != cudaSuccess) {
+        x->sg.exec[i] = nullptr;
+        return x->cuda_fail(e);
+    }
+    return REPSTEP_OK;
+}
+
+// Rewrite AdamW's hyperparameters in the kept AdamW graph.
+cudaError_t update_adamw_node(repstep_ctx *x, const repstep_hparams *hp)
+{
+    cudaKernelNodeParams p{};
+    cudaError_t e = cudaGraphKernelNodeGetParams(x->sg.adamw, &p);
+    if (e != cudaSuccess) return e;
+    if (!p.kernelParams) return cudaErrorInvalidValue;
+    AdamwArgs a = *static_cast<const AdamwArgs *>(p.kernelParams[0]);
+    adamw_hparams(x, hp, a);
+    void *args[1] = {&a};
+    p.kernelParams = args;
+    p.extra = nullptr;
+    return cudaGraphExecKernelNodeSetParams(x->sg.exec[1], x->sg.adamw, &p);
+}
+
+int launch_part(repstep_ctx *x, int i)
+{
+    if (!x->sg.exec[i]) return REPSTEP_OK;   // an empty part
+    const cudaError_t e = cudaGraphLaunch(x->sg.exec[i], x->stream);
+    if (e != cudaSuccess) return x->cuda_fail(e);
+    x->launches += x->sg.kernels[i];
+    return REPSTEP_OK;
+}
+
+// The step as two graph launches and the ordinary root: the reduce and the clip, then
+// AdamW (after any root still reading the state on the hash stream), then the root passes,
+// on the hash stream when one is set -- the streams and the order of the ordinary step.
+int step_graph(repstep_ctx *x, const void *const *grads, uint32_t R, uint32_t nodes,
+               uint32_t gpn, void *w, float *m, float *v, const repstep_hparams *hp,
+               int32_t step, float *norm_out, uint64_t *root_out)
+{
+    // the checks of repstep_step, on every call: a replay launches without them
+    if (!w || !m || !v) return REPSTEP_ERR_ARG;
+    if (!aligned(w, 16) || !aligned(m, 16) || !aligned(v, 16)) return REPSTEP_ERR_ALIGN;
+    int rc = check_hparams(hp);
+    if (rc) return rc;
+    if (!(hp->clip > 0.0f)) return REPSTEP_ERR_ARG;
+    if (norm_out && !aligned(norm_out, 4)) return REPSTEP_ERR_ALIGN;
+    if (root_out && !aligned(root_out, 8)) return REPSTEP_ERR_ALIGN;
+    if (!grads || R == 0) return REPSTEP_ERR_ARG;
+    if (R > uint32_t(kMaxReplicas)) return REPSTEP_ERR_SIZE;
+    std::vector<uintptr_t> key = step_key(x, grads, R, nodes, gpn, w, m, v, hp->clip, norm_out);
+    const bool reuse = x->sg.exec[0] && x->sg.exec[1] && x->sg.adamw && x->sg.key == key;
+    if (reuse) {
+        ++x->sg.replays;
+        rc = launch_part(x, 0);
+        if (rc) return rc;
+        // the call-order state the reduce and the clip leave behind
+        x->reduced = 0;
+        x->scale_ready = true;
+        x->updated = 0;
+        x->sw = x->sm = x->sv = nullptr;
+        x->cut_norm.clear();
+        x->cut_leaf.clear();
+        // AdamW rewrites the state a pending root reads
+        rc = join_hash(x);
+        if (rc) return rc;
+        const cudaError_t e = update_adamw_node(x, hp);
+        if (e != cudaSuccess) {
+            // an ordinary AdamW launch instead (the same bits); the next call captures
+            (void)cudaGetLastError();
+            drop_step_graph(x);
+            rc = do_adamw(x, w, m, v, hp, 0, x->n);
+            return rc ? rc : do_root(x, step, root_out);
+        }
+        rc = launch_part(x, 1);
+        if (rc) return rc;
+        x->updated = x->n;
+        x->sw = w;
+        x->sm = m;
+        x->sv = v;
+        return do_root(x, step, root_out);
+    }
+    drop_step_graph(x);
+    if (!x->sg.capture) {
+        const cudaError_t e = cudaStreamCreateWithFlags(&x->sg.capture, cudaStreamNonBlocking);
+        if (e != cudaSuccess) {
+            x->sg.capture = nullptr;
+            return x->cuda_fail(e);
+        }
+    }
+    rc = capture_part(x, 0, grads, R, nodes, gpn, w, m, v, hp, norm_out);
+    if (!rc) rc = launch_part(x, 0);
+    if (!rc) rc = join_hash(x);
+    // the AdamW node is the last the capture adds; a capture that adds none (n = 0) or
+    // something else is launched, but not kept for replays
+    if (!rc) rc = capture_part(x, 1, grads, R, nodes, gpn, w, m, v, hp, norm_out);
+    if (!rc) rc = launch_part(x, 1);
+    if (rc) {
+        drop_step_graph(x);
+        return rc;
+    }
+    cudaGraphNodeType type = cudaGraphNodeTypeEmpty;
+    if (x->sg.adamw && (cudaGraphNodeGetType(x->sg.adamw, &type) != cudaSuccess ||
+                        type != cudaGraphNodeTypeKernel))
+        x->sg.adamw = nullptr;
+    x->sg.key.swap(key);
+    ++x->sg.captures;
+    return do_root(x, step, root_out);
+}
+
 }  // namespace
 
 extern "C" {
@@ -665,6 +909,8 @@ int repstep_destroy(repstep_ctx *ctx)
     if (!ctx) return REPSTEP_ERR_ARG;
     if (ctx->ev_state) cudaEventDestroy(ctx->ev_state);
     if (ctx->ev_hash) cudaEventDestroy(ctx->ev_hash);
+    drop_step_graph(ctx);
+    if (ctx->sg.capture) cudaStreamDestroy(ctx->sg.capture);
     delete ctx;
     return REPSTEP_OK;
 }
@@ -767,23 +1013,27 @@ int repstep_step(repstep_ctx *ctx, const void *const *d_grads, uint32_t R, uint3
 {
     const NvtxRange nvtx_("repstep_step");
     if (!ctx) return REPSTEP_ERR_ARG;
-    // validate everything before launching anything
-    if (!d_w || !d_m || !d_v) return REPSTEP_ERR_ARG;
-    if (!aligned(d_w, 16) || !aligned(d_m, 16) || !aligned(d_v, 16)) return REPSTEP_ERR_ALIGN;
-    int rc = check_hparams(hp);
-    if (rc) return rc;
-    if (!(hp->clip > 0.0f)) return REPSTEP_ERR_ARG;
-    if (d_norm_out && !aligned(d_norm_out, 4)) return REPSTEP_ERR_ALIGN;
-    if (d_root_out && !aligned(d_root_out, 8)) return REPSTEP_ERR_ALIGN;
-    ctx->reduced = 0;
-    ctx->cut_norm.clear();
-    rc = do_reduce(ctx, d_grads, R, nodes, gpus_per_node, 0, ctx->n);
-    if (rc) return rc;
-    rc = do_clip(ctx, hp->clip, d_norm_out, nullptr);
-    if (rc) return rc;
-    rc = do_adamw(ctx, d_w, d_m, d_v, hp, 0, ctx->n);
-    if (rc) return rc;
-    return do_root(ctx, step, d_root_out);
+    return do_step(ctx, d_grads, R, nodes, gpus_per_node, d_w, d_m, d_v, hp, step, d_norm_out,
+                   d_root_out);
+}
+
+int repstep_step_graph(repstep_ctx *ctx, const void *const *d_grads, uint32_t R, uint32_t nodes,
+                       uint32_t gpus_per_node, void *d_w, float *d_m, float *d_v,
+                       const repstep_hparams *hp, int32_t step, float *d_norm_out,
+                       uint64_t *d_root_out)
+{
+    const NvtxRange nvtx_("repstep_step_graph");
+    if (!ctx) return REPSTEP_ERR_ARG;
+    return step_graph(ctx, d_grads, R, nodes, gpus_per_node, d_w, d_m, d_v, hp, step,
+                      d_norm_out, d_root_out);
+}
+
+int repstep_graph_stats(const repstep_ctx *ctx, uint64_t *captures, uint64_t *replays)
+{
+    if (!ctx) return REPSTEP_ERR_ARG;
+    if (captures) *captures = ctx->sg.captures;
+    if (replays) *replays = ctx->sg.replays;
+    return REPSTEP_OK;
 }
 
 int repstep_set_decay_mask(repstep_ctx *ctx, const uint32_t *d_mask)

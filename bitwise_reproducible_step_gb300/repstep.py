@@ -73,7 +73,8 @@ EXPORTS = [
     "repstep_selftest_fixed_division", "repstep_reduce_paper", "repstep_checkpoint_save",
     "repstep_checkpoint_load", "repstep_set_decay_mask", "repstep_decay_mask_from_segments",
     "repstep_reduce_paper_accum", "repstep_set_hash_stream", "repstep_wait_hash",
-    "repstep_leaves", "repstep_selftest_fast_math",
+    "repstep_leaves", "repstep_selftest_fast_math", "repstep_step_graph",
+    "repstep_graph_stats",
 ]
 NOALLOC_MAX_N = 1 << 30
 
@@ -104,6 +105,8 @@ def lib():
     L.repstep_leaves.argtypes = [vp, i32, vp, vp, vp]
     L.repstep_step.argtypes = [vp, C.POINTER(vp), u32, u32, u32, vp, vp, vp, C.POINTER(HParams),
                                i32, vp, vp]
+    L.repstep_step_graph.argtypes = L.repstep_step.argtypes
+    L.repstep_graph_stats.argtypes = [vp, C.POINTER(u64), C.POINTER(u64)]
     L.repstep_image_bytes.argtypes = [u64]
     L.repstep_image_bytes.restype = u64
     L.repstep_image_write.argtypes = [vp, i32, vp, vp, vp, vp, u64, C.c_int]
@@ -381,6 +384,26 @@ class Repstep:
         _check(lib().repstep_step(self._ctx, arr, R, nodes, gpn, _ptr(w), _ptr(m), _ptr(v),
                                   C.byref(hp), int(step), self._out(norm_out, torch.float32),
                                   self._out(root_out, torch.int64)), "step")
+
+    def step_graph(self, grads, w, m, v, hp: HParams, step: int, norm_out=None, root_out=None,
+                   nodes: int = 1, gpus_per_node: int | None = None):
+        """step() with the reduce + clip and AdamW replayed from CUDA graphs the context
+        keeps (repstep_step_graph): the same bits; once the graphs exist for these
+        buffers, two graph launches and the ordinary root passes per call."""
+        arr, R = self._grads(grads)
+        self._state(w, m, v)
+        gpn = R // max(nodes, 1) if gpus_per_node is None else gpus_per_node
+        self._bind()
+        _check(lib().repstep_step_graph(self._ctx, arr, R, nodes, gpn, _ptr(w), _ptr(m),
+                                        _ptr(v), C.byref(hp), int(step),
+                                        self._out(norm_out, torch.float32),
+                                        self._out(root_out, torch.int64)), "step_graph")
+
+    def graph_stats(self) -> tuple[int, int]:
+        """(steps captured into a graph, steps replayed from a kept one)."""
+        cap, rep = C.c_uint64(), C.c_uint64()
+        _check(lib().repstep_graph_stats(self._ctx, C.byref(cap), C.byref(rep)), "graph_stats")
+        return cap.value, rep.value
 
     def step_from_host(self, host_grads, staging, w, m, v, hp: HParams, step: int,
                        norm_out=None, root_out=None, pieces: int = 8):

@@ -281,6 +281,29 @@ int repstep_step(repstep_ctx *ctx, const void *const *d_grads, uint32_t R, uint3
                  const repstep_hparams *hp, int32_t step, float *d_norm_out,
                  uint64_t *d_root_out);
 
+/* repstep_step with its streaming part replayed from CUDA graphs that the context keeps:
+ * the same arguments, checks, bits, streams and device writes.
+ * - Capture.  The first call captures two graphs on a private stream and instantiates
+ *   them: the reduce with the clip, and AdamW.  So does a call whose gradient, state or
+ *   norm-output pointers, replica count, topology, clip threshold or decay mask differ
+ *   from the kept graphs'.
+ * - Replay.  Other calls launch the first graph, rewrite the hyperparameters in the AdamW
+ *   node of the second (after any root still pending on the hash stream, as the ordinary
+ *   step waits), and launch it: two launches in place of the kernels and memsets, and
+ *   none of the per-kernel host work.
+ * - Root.  The root passes are ordinary launches, on the hash stream when one is set, so
+ *   they overlap the next step's reduce as in repstep_step; d_root_out may change freely.
+ * - Resources.  The first call creates a stream; the graphs are freed by repstep_destroy
+ *   or by the next capture.  Host resources only: no device memory. */
+int repstep_step_graph(repstep_ctx *ctx, const void *const *d_grads, uint32_t R,
+                       uint32_t nodes, uint32_t gpus_per_node, void *d_w, float *d_m,
+                       float *d_v, const repstep_hparams *hp, int32_t step, float *d_norm_out,
+                       uint64_t *d_root_out);
+
+/* Counters of repstep_step_graph (nullable outputs): the steps it captured and
+ * instantiated graphs for, and the steps it replayed from kept graphs. */
+int repstep_graph_stats(const repstep_ctx *ctx, uint64_t *captures, uint64_t *replays);
+
 /* Checkpoint image ("grow_a_language_model_checkpoints", Format):
  * [LE int32 step][LE uint32 n][n fp32 w][n fp32 m][n fp32 v], 8 + 12n bytes, written to
  * dst (device memory, 4-byte aligned, or host memory when dst_is_host != 0) on the
