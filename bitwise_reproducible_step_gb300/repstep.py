@@ -280,9 +280,13 @@ class Repstep:
             raise ValueError(f"workspace: contiguous uint8 on the context's device, at least "
                              f"{nbytes} bytes")
         self.workspace = workspace
+        self._decay_mask = None
+        self._hash_stream = None
+        self._streams_used = {}          # cuda_stream handle -> stream, see _used_on
         self._ctx = C.c_void_p()
         _check(L.repstep_create(C.byref(self.cfg), _ptr(self.workspace), nbytes,
                                 C.c_void_p(self._stream().cuda_stream), C.byref(self._ctx)))
+        self._used_on(self._stream())    # the create's initialisation runs there
         self.c = (self.n + CHUNK - 1) // CHUNK
 
     # ---------------------------------------------------------------- plumbing
@@ -292,7 +296,22 @@ class Repstep:
     def _bind(self):
         if not self._ctx:
             raise RuntimeError("context destroyed")
-        lib().repstep_set_stream(self._ctx, C.c_void_p(self._stream().cuda_stream))
+        st = self._stream()
+        self._used_on(st)
+        lib().repstep_set_stream(self._ctx, C.c_void_p(st.cuda_stream))
+
+    def _used_on(self, st):
+        """Tell PyTorch's caching allocator that the device memory the library reads and
+        writes for this context (the workspace, the decay mask) is used on stream `st`.
+        Freeing a tensor then waits for the work enqueued on every such stream, so that a
+        root still running on the hash stream, or a step on another stream than the one
+        the workspace was allocated on, never writes memory handed to a new tensor."""
+        if st.cuda_stream in self._streams_used:
+            return
+        self._streams_used[st.cuda_stream] = st
+        self.workspace.record_stream(st)
+        if self._decay_mask is not None:
+            self._decay_mask.record_stream(st)
 
     def _state(self, w, m, v):
         for t, want in ((w, self.param_dtype), (m, torch.float32), (v, torch.float32)):
@@ -447,6 +466,8 @@ class Repstep:
         _check(lib().repstep_set_hash_stream(
             self._ctx, None if stream is None else C.c_void_p(stream.cuda_stream)),
             "set_hash_stream")
+        if stream is not None:
+            self._used_on(stream)
         self._hash_stream = stream
 
     def wait_hash(self, stream: torch.cuda.Stream | None = None):
@@ -464,6 +485,9 @@ class Repstep:
             raise ValueError("decay mask: contiguous CUDA int32 on the context's device, "
                              "ceil(n/32) words")
         _check(lib().repstep_set_decay_mask(self._ctx, _ptr(mask)), "set_decay_mask")
+        if mask is not None:
+            for st in self._streams_used.values():
+                mask.record_stream(st)
         self._decay_mask = mask
 
     def image_write(self, step: int, w, m, v, dst: torch.Tensor):

@@ -580,3 +580,37 @@ def test_steps_beside_a_busy_stream(hash_stream):
         U.assert_same_f32(norm, np.array([ref["norm"]], np.float32), f"norm step {t}")
         assert U.root_of(root) == ref["root"], f"root step {t}"
     del b
+
+
+def test_context_memory_is_recorded_on_every_stream_it_uses():
+    """The workspace and the decay mask are marked as used on the creation stream, on each
+    stream a call ran on, and on the hash stream, so that PyTorch's allocator does not hand
+    them to a new tensor while a root is still pending there.  The step's bits do not
+    depend on the stream."""
+    n, R = 3 * 4096 + 17, 4
+    dev = torch.device("cuda", 0)
+    main = torch.cuda.current_stream(dev)
+    side, hs = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ctx = rs.Repstep(n, device=dev)
+    assert set(ctx._streams_used) == {main.cuda_stream}
+    mask = rs.decay_mask_from_segments(n, [(0, False), (5000, True)]).to(dev)
+    ctx.set_decay_mask(mask)
+    ctx.set_hash_stream(hs)
+    w, m, v = I.gen_state(U.F32_WL, n=n, device=dev)
+    grads = U.gen_grads(n, R, 1)
+    norm = torch.empty(1, dtype=torch.float32, device=dev)
+    root = torch.empty(1, dtype=torch.int64, device=dev)
+    side.wait_stream(main)
+    with torch.cuda.stream(side):
+        ctx.step(grads, w, m, v, U.hp_for(1), step=1, norm_out=norm, root_out=root)
+        ctx.sync()
+    assert set(ctx._streams_used) == {main.cuda_stream, side.cuda_stream, hs.cuda_stream}
+    w2, m2, v2 = I.gen_state(U.F32_WL, n=n, device=dev)
+    twin = rs.Repstep(n, device=dev)
+    twin.set_decay_mask(mask)
+    root2 = torch.empty(1, dtype=torch.int64, device=dev)
+    twin.step(grads, w2, m2, v2, U.hp_for(1), step=1, root_out=root2)
+    twin.sync()
+    assert U.root_of(root) == U.root_of(root2)
+    del ctx                           # its root is complete; freeing waits on all streams
+    torch.cuda.synchronize(dev)
