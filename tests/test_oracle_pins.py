@@ -325,6 +325,25 @@ def test_norm_within_error_bound():
         assert abs(float(O.norm(g)) - exact) <= levels * 2.0 ** -24 * exact
 
 
+def test_norm_tree_order_matters():
+    """Negative control: the same squares summed in another order (one sequential fold
+    over the whole vector, no chunks) give other bits on random data, though both stay
+    within their error bounds of the exact norm.  So a bit-exact comparison of norms can
+    fail, and it pins the chunked tree."""
+    rng = np.random.default_rng(10)
+    differing = 0
+    for _ in range(8):
+        g = (rng.standard_normal(3 * 4096 + 777) * 10.0 ** rng.integers(-3, 2)).astype(np.float32)
+        sq = g * g                                             # fp32 products, as the method
+        folded = np.sqrt(np.add.accumulate(sq, dtype=np.float32)[-1], dtype=np.float32)
+        ours = O.norm(g)
+        exact = math.sqrt(math.fsum(float(x) * float(x) for x in g))
+        assert abs(float(ours) - exact) <= 16 * 2.0 ** -24 * exact
+        assert abs(float(folded) - exact) <= g.size * 2.0 ** -24 * exact
+        differing += int(np.float32(ours).view(np.uint32) != np.float32(folded).view(np.uint32))
+    assert differing >= 4
+
+
 def test_norm_empty_is_zero():
     assert O.norm(np.zeros(0, np.float32)) == 0.0
 
