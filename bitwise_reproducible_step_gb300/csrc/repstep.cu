@@ -7,6 +7,7 @@
 //   rho = 1/R   ("OPEN-1B: A Fully Auditable Training Run", App. A.3: every average is a
 //                multiply by a host-computed reciprocal)
 //   1 - b1, 1 - b2, 1 - lr*wd, and the bias corrections 1 - b^t (t repeated products).
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstdio>
@@ -214,15 +215,11 @@ void note_cut_chunks(std::vector<uint64_t> &v, uint64_t b, uint64_t e, uint64_t 
     if (k1 != k0 && cut(k1)) v.push_back(k1);
 }
 
+// Each cut chunk once, in ascending order (a step reduced in many ranges lists many).
 void unique_sort(std::vector<uint64_t> &v)
 {
-    std::vector<uint64_t> out;
-    for (uint64_t k : v) {
-        bool seen = false;
-        for (uint64_t o : out) seen = seen || (o == k);
-        if (!seen) out.push_back(k);
-    }
-    v.swap(out);
+    std::sort(v.begin(), v.end());
+    v.erase(std::unique(v.begin(), v.end()), v.end());
 }
 
 int check_hparams(const repstep_hparams *hp)
