@@ -96,3 +96,21 @@ def test_plain_program_against_the_c_abi(tmp_path, compiler, flags, src):
     # elements 0..39 keep their weight (no decay), 40..69 decay
     assert lines["mask"] == "0 00000000 ffffff00 0000003f"
     assert lines["rejects"] == "1 1 1 1"
+
+
+def test_readme_c_example_compiles(tmp_path):
+    """The C example in README.md compiles as strict C11 against the header."""
+    import re
+    cuda_inc = "/usr/local/cuda/include"
+    if shutil.which("gcc") is None or not os.path.exists(os.path.join(cuda_inc, "cuda_runtime.h")):
+        pytest.skip("gcc or the CUDA headers are missing")
+    text = open(os.path.join(ROOT, "README.md"), encoding="utf-8").read()
+    blocks = re.findall(r"```c\n(.*?)```", text, re.S)
+    assert blocks, "README.md has no C example"
+    src = tmp_path / "readme_example.c"
+    src.write_text(blocks[0])
+    out = subprocess.run(["gcc", "-std=c11", "-Wall", "-Wextra", "-Werror", "-pedantic",
+                          "-I", INCLUDE, "-I", cuda_inc, "-c", str(src),
+                          "-o", str(tmp_path / "readme_example.o")],
+                         capture_output=True, text=True)
+    assert out.returncode == 0, out.stderr
