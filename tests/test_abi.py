@@ -56,6 +56,22 @@ def test_bias_corrections_match_oracle(L):
         assert np.float32(got[1]).view(np.uint32) == want[1].view(np.uint32)
 
 
+def test_bias_corrections_match_golden_bits(L):
+    """The library's host-side bias corrections against the hand-derived bit table for
+    beta1 = 0.9, beta2 = 0.999 (tests/golden/bias_corrections.txt)."""
+    rows = {}
+    for line in open(os.path.join(ROOT, "tests", "golden", "bias_corrections.txt")):
+        parts = [x.strip() for x in line.split("|")]
+        if line.startswith("#") or len(parts) != 3:
+            continue
+        rows[int(parts[0])] = (int(parts[1], 16), int(parts[2], 16))
+    b1, b2 = np.uint32(0x3F666666).view(np.float32), np.uint32(0x3F7FBE77).view(np.float32)
+    assert sorted(rows) == [1, 2, 3, 5, 10]
+    for t, want in rows.items():
+        got = rs.bias_corrections(b1, b2, t)
+        assert tuple(int(np.float32(x).view(np.uint32)) for x in got) == want, t
+
+
 def test_workspace_sizes_and_layout(L):
     for n in [0, 1, 4095, 4096, 4097, 12_800_000, 1_200_000_000, 3_000_000_000, 2 ** 32 - 1]:
         b = rs.workspace_bytes(n)

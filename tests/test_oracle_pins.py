@@ -6,6 +6,7 @@ import hashlib
 import math
 import os
 import random
+import re
 from fractions import Fraction
 
 import numpy as np
@@ -379,6 +380,150 @@ def test_bias_corrections_step_one_and_bound():
         for b, bc in [(B1, bc1), (B2, bc2)]:
             exact = 1 - float(b) ** t
             assert abs(float(bc) - exact) <= (t + 1) * 2.0 ** -24 * max(1.0, float(b) ** t) + 2 ** -24 * exact
+
+
+def _golden_bits(name):
+    consts, rows = {}, {}
+    for line in open(os.path.join(GOLDEN, name)):
+        if not line.strip() or line.startswith("#"):
+            continue
+        parts = [x.strip() for x in line.split("|")]
+        if len(parts) == 2:
+            consts[parts[0]] = int(parts[1], 16)
+        else:
+            rows[int(parts[0])] = (int(parts[1], 16), int(parts[2], 16))
+    return consts, rows
+
+
+def test_bias_corrections_match_golden_bits():
+    """The t = 1, 2, 3, 5, 10 bias corrections of beta1 = 0.9 and beta2 = 0.999, bit for bit
+    against the hand-derived table; the table itself re-derived here in exact rationals,
+    and shown to differ from the two plausible misreadings it is meant to exclude."""
+    _, rows = _golden_bits("bias_corrections.txt")
+    assert sorted(rows) == [1, 2, 3, 5, 10]
+    powf_differs = once_differs = 0
+    for t, (want1, want2) in rows.items():
+        bc1, bc2 = O.bias_corrections(B1, B2, t)
+        assert (X.bits(bc1), X.bits(bc2)) == (want1, want2), t
+        p1 = p2 = np.float32(1.0)
+        for _ in range(t):
+            p1, p2 = X.mul(p1, B1), X.mul(p2, B2)
+        assert (X.bits(X.f32(1 - X.F(p1))), X.bits(X.f32(1 - X.F(p2)))) == (want1, want2)
+        powf = [X.bits(X.f32(1 - X.F(X.f32(X.F(b) ** t)))) for b in (B1, B2)]
+        once = [X.bits(X.f32(1 - X.F(b) ** t)) for b in (B1, B2)]
+        powf_differs += powf != [want1, want2]
+        once_differs += once != [want1, want2]
+    assert powf_differs >= 1 and once_differs >= 1
+
+
+def test_adamw_constants_match_golden_bits():
+    """omega1 = 1 - beta1, omega2 = 1 - beta2 and delta = 1 - lr*wd as the oracle's AdamW
+    uses them, read back through updates that expose each one alone: from m = v = 0 and
+    gc = 1, m' = omega1 and v' = omega2 exactly; with g = 0, w' = w*delta."""
+    consts, _ = _golden_bits("bias_corrections.txt")
+    one = np.ones(1, np.float32)
+    z = np.zeros(1, np.float32)
+    _, m1, v1 = O.adamw(one, z, z, one, 1.0, LR, B1, B2, EPS, WD, 1.0, 1.0)
+    w1, _, _ = O.adamw(one, z, z, z, 1.0, LR, B1, B2, EPS, WD, 1.0, 1.0)
+    assert X.bits(m1[0]) == consts["omega1"]
+    assert X.bits(v1[0]) == consts["omega2"]
+    assert X.bits(w1[0]) == consts["delta"]
+
+
+def _value(tok: str) -> np.float32:
+    tok = tok.strip()
+    sign = -1 if tok.startswith("-") else 1
+    tok = tok.lstrip("-")
+    if tok == "inf":
+        return np.float32(sign * np.inf)
+    head, *tail = re.split(r"(?<=[0-9])-(?=[0-9])", tok)     # '1-2^-20': a difference
+    q = X.parse_exact(head) - sum((X.parse_exact(t) for t in tail), Fraction(0))
+    assert X.F(X.f32(q)) == q, f"{tok} is not an fp32 value"
+    return np.float32(sign * float(q))
+
+
+def _adamw_order_cases():
+    out = []
+    for line in open(os.path.join(GOLDEN, "adamw_order_cases.txt")):
+        if not line.strip() or line.startswith("#"):
+            continue
+        name, state, hyper, want = [x.strip() for x in line.split("|")]
+        out.append((name, [_value(t) for t in state.split(",")],
+                    [_value(t) for t in hyper.split(",")], [_value(t) for t in want.split(",")]))
+    return out
+
+
+def _f32_update(w, m, v, g, scale, lr, b1, b2, eps, wd, bc1, bc2, variant=None):
+    """The update in numpy fp32 scalars (each operation one IEEE rounding), with one
+    misreading of the order switched in by `variant`: the negative controls."""
+    f = np.float32
+    with np.errstate(all="ignore"):
+        om1, om2, delta = f(1) - b1, f(1) - b2, f(1) - lr * wd
+        if variant == "decay_1_minus_wd":
+            delta = f(1) - wd
+        gc = g * scale
+        m1 = b1 * m + om1 * (g if variant == "m_unclipped" else gc)
+        if variant == "m_lerp":
+            m1 = m + om1 * (gc - m)
+        gv = g if variant == "v_unclipped" else gc
+        v1 = b2 * v + om2 * (gv * gv)
+        if variant == "v_omega_first":
+            v1 = b2 * v + (om2 * gv) * gv
+        mhat = m1 if variant == "no_bc1" else m1 / bc1
+        vhat = v1 if variant == "no_bc2" else v1 / bc2
+        den = np.sqrt(vhat) + eps
+        if variant == "eps_in_root":
+            den = np.sqrt(vhat + eps)
+        elif variant == "sqrt_split":
+            den = np.sqrt(v1) / np.sqrt(bc2) + eps
+        u = mhat / den
+        if variant == "bc1_in_denominator":
+            u = m1 / (bc1 * den)
+        step = lr * u
+        if variant == "step_size_folded":
+            step = (lr / bc1) * (m1 / den)
+        w1 = w * delta - step
+        if variant == "decay_after_step":
+            w1 = (w - lr * u) * delta
+        elif variant == "decay_in_step":
+            w1 = w - lr * (u + wd * w)
+    return f(w1), f(m1), f(v1)
+
+
+ADAMW_VARIANTS = ["decay_1_minus_wd", "m_unclipped", "m_lerp", "v_unclipped", "v_omega_first",
+                  "no_bc1", "no_bc2", "eps_in_root", "sqrt_split", "bc1_in_denominator",
+                  "step_size_folded", "decay_after_step", "decay_in_step"]
+
+
+def _same_bits(a, b):
+    return all(X.bits(x) == X.bits(y) for x, y in zip(a, b))
+
+
+def test_adamw_order_matches_golden_cases():
+    """The oracle's AdamW on the hand-derived cases, every output bit equal."""
+    cases = _adamw_order_cases()
+    assert len(cases) == 8
+    for name, (w, m, v, g, scale), (lr, b1, b2, eps, wd, bc1, bc2), want in cases:
+        arr = lambda x: np.full(5, x, np.float32)  # noqa: E731
+        got = O.adamw(arr(w), arr(m), arr(v), arr(g), scale, lr, b1, b2, eps, wd, bc1, bc2)
+        for j in range(5):
+            assert _same_bits([x[j] for x in got], want), (name, [x[j] for x in got], want)
+
+
+def test_adamw_order_golden_rejects_each_misreading():
+    """Negative controls: the definition restated in numpy fp32 reproduces every golden case
+    (a check of the hand derivations), and each misreading of the order -- eps under the
+    root, the decay after the step or inside it, the bias correction folded into the
+    denominator or the step size, the square root split, the interpolation form of m, an
+    unclipped gradient in either moment, a missing bias correction, delta = 1 - wd -- gives
+    other bits on at least one case."""
+    cases = _adamw_order_cases()
+    for name, state, hyper, want in cases:
+        assert _same_bits(_f32_update(*state, *hyper), want), name
+    for variant in ADAMW_VARIANTS:
+        caught = [name for name, state, hyper, want in cases
+                  if not _same_bits(_f32_update(*state, *hyper, variant=variant), want)]
+        assert caught, f"no golden case distinguishes the variant {variant}"
 
 
 def test_adamw_first_step_closed_form():
