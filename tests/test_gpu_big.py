@@ -1,16 +1,21 @@
-"""Full-size workloads on one GB300, in the launch configuration the benchmark times.
+"""Full-size workloads on one GB300, in the launch configuration the benchmark times, with
+every slot of every step compared with the oracle.
 
-The oracle cannot redo a 1.2e9- or 3e9-parameter step in seconds, so each step is checked
-as a chain of pieces the oracle computes exactly:
-  * sampled whole chunks (first, last/ragged, and ~250 seeded random ones): g, the chunk
-    sum of squares, the AdamW outputs and the three leaf digests, from the same gathered
-    inputs, bit for bit;
-  * the pre-clip norm and clip scale: the oracle's canonical tree over ALL chunk sums;
-  * the Merkle root: the oracle's tree over ALL leaf digests;
-and every invariance (launch shape, topology, shard ranges) is checked on the full arrays
+The oracle runs chunk-parallel on the host cores (tests/oracle_full.py; its functions are
+unchanged and single-threaded per call) and follows its own trajectory from the same
+initial state and the same gradients.  After each GPU step every slot of g, the chunk sums
+of squares, w, m, v and the leaf digests is compared, and the pre-clip norm and the Merkle
+root -- formed from the oracle's own chunk sums and leaves -- must be equal: 0 differing
+slots and relFro 0, the statistics of "Cross-process reproducibility, settled by
+measurement" (section "The measurement").  Each step's norm and root are also checked
+against the fingerprints tests/golden/make_full_size_fingerprints.py wrote from the oracle
+alone.  Invariances (launch shape, topology, shard ranges) are checked on the full arrays
 by exact equality on the device.
+
+Set REPSTEP_FULL_ORACLE_LOG to a file name to append one JSON line per compared step.
 """
-import hashlib
+import json
+import os
 
 import numpy as np
 import pytest
@@ -18,12 +23,13 @@ import torch
 
 from bitwise_reproducible_step_gb300 import inputs as I
 from bitwise_reproducible_step_gb300 import repstep as rs
-from oracle import oracle as O
 from tests import gpu_util as U
+from tests import oracle_full as OF
 
 pytestmark = [pytest.mark.gpu, pytest.mark.big]
 
 CH = 4096
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "full_size_fingerprints.txt")
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -34,90 +40,66 @@ def _built():
     torch.cuda.empty_cache()
 
 
-def sample_chunks(c, k=254, seed=0):
-    rng = np.random.default_rng(seed)
-    pick = set(rng.choice(c, size=min(k, c), replace=False).tolist())
-    pick.update([0, c - 1])
-    return np.array(sorted(pick), dtype=np.int64)
+def fingerprints():
+    """(workload, variant, step) -> (norm bits, root) from the committed golden file."""
+    out = {}
+    if not os.path.exists(GOLDEN):
+        return out
+    for line in open(GOLDEN):
+        if not line.strip() or line.startswith("#"):
+            continue
+        wl, variant, t, norm, root = [x.strip() for x in line.split("|")]
+        out[(wl, variant, int(t))] = (norm, root)
+    return out
 
 
-def gather(t: torch.Tensor, chunks, n):
-    """Host copy of whole chunks of a device array (ragged last chunk kept short)."""
-    out = []
-    for k in chunks:
-        lo, hi = int(k) * CH, min(int(k) * CH + CH, n)
-        out.append(t[lo:hi])
-    return [x.cpu() for x in out]
+def record(rep, what):
+    path = os.environ.get("REPSTEP_FULL_ORACLE_LOG")
+    if path:
+        with open(path, "a") as f:
+            f.write(json.dumps(dict(what=what, **rep)) + "\n")
 
 
-def leaf_of(words: np.ndarray, hash_mode: int) -> int:
-    if hash_mode == 0:
-        return O.pf61(words.view(np.uint32))
-    return int.from_bytes(hashlib.blake2b(words.astype("<f4").tobytes(), digest_size=8).digest(),
-                          "little")
+def check(rep, wl_name, variant, t):
+    what = f"{wl_name}/{variant} step {t}"
+    record(rep, what)
+    OF.assert_identical(rep, what)
+    fp = fingerprints().get((wl_name, variant, t))
+    if fp is not None:
+        assert (rep["norm"]["oracle"], rep["root"]["oracle"]) == fp, (what, fp)
 
 
-def check_step_chain(ctx, grads_before, state_before, w, m, v, t, chunks, n, norm_t, root_t,
-                     hash_mode=0, reducer=O.reduce):
-    """grads_before / state_before: host chunk lists gathered before the step."""
-    c = (n + CH - 1) // CH
-    chunk_sums = ctx.chunk_sums_view().cpu().numpy()
-    # norm and scale: oracle tree over all GPU chunk sums
-    S = O.tree_sum(chunk_sums)
-    norm = np.sqrt(S, dtype=np.float32)
-    norm_o = np.float32(np.sqrt(np.float32(S)))
-    assert np.float32(norm_t.item()) == norm_o == norm
-    scale = O.clip_scale(norm_o, U.HP["clip"])
-    bc1, bc2 = O.bias_corrections(U.HP["beta1"], U.HP["beta2"], t)
-    leaves = ctx.leaves_view().cpu().numpy().view(np.uint64)
-    g_dev = ctx.g_view()
-    new_w, new_m, new_v = gather(w, chunks, n), gather(m, chunks, n), gather(v, chunks, n)
-    g_got = gather(g_dev, chunks, n)
-    for i, k in enumerate(chunks):
-        G = [I.to_numpy(gr[i]) for gr in grads_before]
-        g = reducer(G)
-        U.assert_same_f32(g_got[i], g, f"g chunk {k}")
-        _, s = O.norm(g, with_chunks=True)
-        assert s.view(np.uint32)[0] == chunk_sums[k:k + 1].view(np.uint32)[0], f"chunk sum {k}"
-        w0, m0, v0 = (x[i].numpy() for x in state_before)
-        w1, m1, v1 = O.adamw(w0, m0, v0, g, scale, U.HP["lr"], U.HP["beta1"], U.HP["beta2"],
-                             U.HP["eps"], U.HP["wd"], bc1, bc2)
-        U.assert_same_f32(new_w[i], w1, f"w chunk {k}")
-        U.assert_same_f32(new_m[i], m1, f"m chunk {k}")
-        U.assert_same_f32(new_v[i], v1, f"v chunk {k}")
-        for a, arr in enumerate((w1, m1, v1)):
-            assert leaves[1 + a * c + k] == leaf_of(arr, hash_mode), f"leaf {a} chunk {k}"
-    hdr_words = np.array([t, n], dtype=np.uint64).astype(np.uint32)
-    hdr = O.pf61(hdr_words) if hash_mode == 0 else int.from_bytes(
-        hashlib.blake2b(hdr_words.astype("<u4").tobytes(), digest_size=8).digest(), "little")
-    assert leaves[0] == hdr
-    assert U.root_of(root_t) == O.merkle_root(leaves)
-    return float(norm_o)
+def host_state(w, m, v):
+    if w.dtype == torch.bfloat16:
+        w_h = w.view(torch.int16).cpu().numpy().view(np.uint16)
+    else:
+        w_h = w.cpu().numpy()
+    return w_h, m.cpu().numpy(), v.cpu().numpy()
 
 
-def run_big(wl, steps, ranges=None, compare_unsharded=False, hash_mode=0):
+def gpu_views(ctx, w, m, v, norm, root):
+    return dict(g=ctx.g_view(), chunk_sums=ctx.chunk_sums_view(), leaves=ctx.leaves_view(),
+                w=w, m=m, v=v, norm=norm, root=root)
+
+
+def run_big(wl, steps, variant="default", ranges=None, compare_unsharded=False, hash_mode=0):
     n, R = wl.n, wl.R
     dev = torch.device("cuda", 0)
     gdt = torch.bfloat16 if wl.grad_dtype == "bf16" else torch.float32
-    c = (n + CH - 1) // CH
-    chunks = sample_chunks(c)
-    if ranges:   # also sample the chunks the shard boundaries cut
-        extra = {lo // CH for lo, _ in ranges[1:]}
-        chunks = np.array(sorted(set(chunks.tolist()) | extra), dtype=np.int64)
     ctx = rs.Repstep(n, grad_dtype=gdt, device=dev, hash_mode=hash_mode)
     w, m, v = I.gen_state(wl, device=dev)
+    fo = OF.FullOracle(n, R, *host_state(w, m, v), grad_dtype=wl.grad_dtype,
+                       hash_mode=hash_mode)
     twin = None
     if compare_unsharded:
         twin = (rs.Repstep(n, grad_dtype=gdt, device=dev), w.clone(), m.clone(), v.clone())
     grads = [torch.empty(n, dtype=gdt, device=dev) for _ in range(R)]
     norm = torch.empty(1, dtype=torch.float32, device=dev)
     root = torch.empty(1, dtype=torch.int64, device=dev)
-    norms = []
+    reps = []
     for t in range(1, steps + 1):
         for r in range(R):
             I.gen_grad(wl, t, r, device=dev, out=grads[r])
-        g_before = [gather(gr, chunks, n) for gr in grads]
-        s_before = (gather(w, chunks, n), gather(m, chunks, n), gather(v, chunks, n))
         hp = U.hp_for(t)
         if ranges:
             for lo, hi in ranges:
@@ -129,8 +111,9 @@ def run_big(wl, steps, ranges=None, compare_unsharded=False, hash_mode=0):
         else:
             ctx.step(grads, w, m, v, hp, step=t, norm_out=norm, root_out=root)
         assert ctx.sync() & ~rs.FLAG_NONFINITE_NORM == 0
-        norms.append(check_step_chain(ctx, g_before, s_before, w, m, v, t, chunks, n, norm, root,
-                                      hash_mode))
+        rep = fo.step(grads, t, U.HP, gpu_views(ctx, w, m, v, norm, root))
+        check(rep, wl.name, variant, t)
+        reps.append(rep)
         if twin is not None:
             tc, tw, tm, tv = twin
             tn = torch.empty(1, dtype=torch.float32, device=dev)
@@ -141,30 +124,59 @@ def run_big(wl, steps, ranges=None, compare_unsharded=False, hash_mode=0):
             assert torch.equal(tm.view(torch.int32), m.view(torch.int32))
             assert torch.equal(tv.view(torch.int32), v.view(torch.int32))
             assert tn.item() == norm.item() and U.root_of(tr) == U.root_of(root)
-    return norms
+    fo.close()
+    return [float(np.uint32(int(r["norm"]["oracle"], 16)).view(np.float32)) for r in reps]
 
 
 def test_flat1200m_r8_segscale():
+    """The benchmark workload: 1.2e9 parameters, R = 8, all 5 steps."""
     wl = I.WORKLOADS["flat1200m_r8_segscale"]
-    norms = run_big(wl, steps=2)
+    norms = run_big(wl, steps=wl.steps)
     assert all(x < 1.0 for x in norms)              # tiny segment-scaled grads: no clip
 
 
 def test_flat1200m_r8_segscale_audit_mode():
-    """The bench workload with BLAKE2b-64 audit-mode leaves, one step."""
+    """The benchmark workload with BLAKE2b-64 audit-mode leaves, two steps."""
     wl = I.WORKLOADS["flat1200m_r8_segscale"]
-    run_big(wl, steps=1, hash_mode=rs.HASH_BLAKE2B)
+    run_big(wl, steps=2, variant="audit", hash_mode=rs.HASH_BLAKE2B)
 
 
 def test_flat3000m_r8_bf16_spiked_shards():
+    """3e9 parameters, R = 8 bf16 gradients, all 3 steps reduced and updated as 8 contiguous
+    shard ranges; equal to the unsharded run on the device and to the oracle everywhere."""
     wl = I.WORKLOADS["flat3000m_r8_bf16_spiked_shards"]
-    norms = run_big(wl, steps=2, ranges=I.shard_ranges(wl.n, wl.shards), compare_unsharded=True)
+    norms = run_big(wl, steps=wl.steps, ranges=I.shard_ranges(wl.n, wl.shards),
+                    compare_unsharded=True)
     assert all(x > 1.0 for x in norms)              # 1% spikes x 1e3 force the clip
 
 
+def test_flat268m_r32_three_steps_three_topologies():
+    """268M parameters, R = 32: the workload's 3 steps, step t summed as the t-th staged
+    topology (1 x 32, 4 x 8, 8 x 4 nodes x GPUs), against the oracle's staged sum."""
+    wl = I.WORKLOADS["flat268m_r32_topologies"]
+    n, R = wl.n, wl.R
+    dev = torch.device("cuda", 0)
+    ctx = rs.Repstep(n, device=dev)
+    w, m, v = I.gen_state(wl, device=dev)
+    fo = OF.FullOracle(n, R, *host_state(w, m, v))
+    grads = [torch.empty(n, dtype=torch.float32, device=dev) for _ in range(R)]
+    norm = torch.empty(1, dtype=torch.float32, device=dev)
+    root = torch.empty(1, dtype=torch.int64, device=dev)
+    for t, (nodes, gpn) in zip(range(1, wl.steps + 1), wl.topologies):
+        for r in range(R):
+            I.gen_grad(wl, t, r, device=dev, out=grads[r])
+        ctx.step(grads, w, m, v, U.hp_for(t), step=t, norm_out=norm, root_out=root,
+                 nodes=nodes, gpus_per_node=gpn)
+        assert ctx.sync() == 0
+        rep = fo.step(grads, t, U.HP, gpu_views(ctx, w, m, v, norm, root), reducer="topology",
+                      nodes=nodes, gpus_per_node=gpn)
+        check(rep, wl.name, "topologies", t)
+    fo.close()
+
+
 def test_flat268m_r32_topologies_grids_blocks():
-    """4 topologies x 5 grid sizes x 3 block sizes: every output bit equal, and the
-    default configuration equal to the oracle on the sampled chain."""
+    """4 topologies x 5 grid sizes x 3 block sizes from a mid-run state: every output bit
+    equal, and the default configuration equal to the oracle in every slot."""
     wl = I.WORKLOADS["flat268m_r32_topologies"]
     n, R = wl.n, wl.R
     dev = torch.device("cuda", 0)
@@ -174,9 +186,6 @@ def test_flat268m_r32_topologies_grids_blocks():
     w0, m0, v0 = I.gen_state(wl, device=dev)
     m0.copy_(I.gen_grad(wl, 9, 0, device=dev))       # non-zero moments: a mid-run step
     v0.copy_(I.gen_grad(wl, 9, 1, device=dev).square())
-    chunks = sample_chunks(c, k=126, seed=4)
-    g_before = [gather(gr, chunks, n) for gr in grads]
-    s_before = (gather(w0, chunks, n), gather(m0, chunks, n), gather(v0, chunks, n))
     hp = U.hp_for(3)
     w, m, v = w0.clone(), m0.clone(), v0.clone()
     ref = None
@@ -191,7 +200,10 @@ def test_flat268m_r32_topologies_grids_blocks():
                          nodes=nodes, gpus_per_node=gpn)
                 ctx.sync()
                 if ref is None:
-                    check_step_chain(ctx, g_before, s_before, w, m, v, 3, chunks, n, norm, root)
+                    fo = OF.FullOracle(n, R, *host_state(w0, m0, v0))
+                    rep = fo.step(grads, 3, U.HP, gpu_views(ctx, w, m, v, norm, root))
+                    fo.close()
+                    check(rep, wl.name, "mid_run_sweep_reference", 3)
                     ref = (w.clone(), m.clone(), v.clone(), norm.item(), U.root_of(root))
                 else:
                     assert torch.equal(w.view(torch.int32), ref[0].view(torch.int32)), (nodes, grid, nt)
@@ -209,16 +221,13 @@ def test_fixed_division_is_ieee_for_every_significand_pair():
 
 def test_flat268m_r32_paper_exact_order():
     """OPEN-1B Algorithm 1 order on 268M parameters: 4 replicas x 8 shards (linear shard
-    sums, TreeFold over replicas), sampled chunks against the oracle's restatement."""
+    sums, TreeFold over replicas), every slot against the oracle's restatement."""
     wl = I.WORKLOADS["flat268m_r32_topologies"]
     n, R, dps = wl.n, wl.R, 8
     dev = torch.device("cuda", 0)
-    c = (n + CH - 1) // CH
     grads = [I.gen_grad(wl, 1, r, device=dev) for r in range(R)]
     w, m, v = I.gen_state(wl, device=dev)
-    chunks = sample_chunks(c, k=126, seed=5)
-    g_before = [gather(gr, chunks, n) for gr in grads]
-    s_before = (gather(w, chunks, n), gather(m, chunks, n), gather(v, chunks, n))
+    fo = OF.FullOracle(n, R, *host_state(w, m, v))
     ctx = rs.Repstep(n, device=dev)
     hp = U.hp_for(1)
     norm = torch.empty(1, dtype=torch.float32, device=dev)
@@ -228,8 +237,10 @@ def test_flat268m_r32_paper_exact_order():
     ctx.adamw(w, m, v, hp)
     ctx.root(1, root_out=root)
     ctx.sync()
-    check_step_chain(ctx, g_before, s_before, w, m, v, 1, chunks, n, norm, root,
-                     reducer=lambda G: O.reduce_alg1(G, dps))
+    rep = fo.step(grads, 1, U.HP, gpu_views(ctx, w, m, v, norm, root), reducer="alg1",
+                  dp_shard=dps)
+    fo.close()
+    check(rep, wl.name, "paper_exact_4x8", 1)
 
 
 def bench_segments(n):
@@ -245,31 +256,14 @@ def bench_segments(n):
     return segs
 
 
-def local_segments(segs, lo, hi):
-    """The segment list restricted to [lo, hi), re-based to lo."""
-    starts = [b for b, _ in segs]
-    k = int(np.searchsorted(starts, lo, side="right")) - 1
-    out = [(0, segs[k][1])]
-    for b, d in segs[k + 1:]:
-        if b >= hi:
-            break
-        out.append((b - lo, d))
-    return out
-
-
 def test_flat1200m_r8_bf16w_decay_mask_ftz():
     """The bench workload with all three optimizer variants at once -- bf16 parameters,
-    the benchmark's decay segments and software flush-to-zero -- one step, checked on
-    sampled whole chunks against the oracle's FTZ functions, the norm over all chunk sums
-    and the root over all leaves."""
+    the benchmark's decay segments and software flush-to-zero -- one mid-run step, every
+    slot against the oracle's flush-to-zero functions."""
     wl = I.WORKLOADS["flat1200m_r8_segscale"]
     n, R = wl.n, wl.R
     dev = torch.device("cuda", 0)
-    c = (n + CH - 1) // CH
-    chunks = sample_chunks(c, k=190, seed=7)
     segs = bench_segments(n)
-    # also sample the chunks that hold segment boundaries
-    chunks = np.array(sorted(set(chunks.tolist()) | {b // CH for b, _ in segs[1:8]}), np.int64)
     ctx = rs.Repstep(n, device=dev, param_dtype=torch.bfloat16, subnormals=rs.SUBNORMALS_FTZ)
     ctx.set_decay_mask(rs.decay_mask_from_segments(n, segs).to(dev))
     w32, m, v = I.gen_state(wl, device=dev)
@@ -277,38 +271,17 @@ def test_flat1200m_r8_bf16w_decay_mask_ftz():
     del w32
     m.copy_(I.gen_grad(wl, 9, 0, device=dev))           # non-zero moments: a mid-run step
     v.copy_(I.gen_grad(wl, 9, 1, device=dev).square())
+    fo = OF.FullOracle(n, R, *host_state(w, m, v), param_dtype="bf16", ftz=True,
+                       segments=segs)
     grads = [I.gen_grad(wl, 3, r, device=dev) for r in range(R)]
-    g_before = [gather(gr, chunks, n) for gr in grads]
-    s_before = (gather(w, chunks, n), gather(m, chunks, n), gather(v, chunks, n))
     hp = U.hp_for(3)
     norm = torch.empty(1, dtype=torch.float32, device=dev)
     root = torch.empty(1, dtype=torch.int64, device=dev)
     ctx.step(grads, w, m, v, hp, step=3, norm_out=norm, root_out=root)
     assert ctx.sync() & ~rs.FLAG_NONFINITE_NORM == 0
-    chunk_sums = ctx.chunk_sums_view().cpu().numpy()
-    norm_o = O.flush(np.sqrt(O.tree_sum_ftz(chunk_sums), dtype=np.float32))
-    assert np.float32(norm.item()) == norm_o
-    scale = O.clip_scale_ftz(norm_o, U.HP["clip"])
-    bc1, bc2 = O.bias_corrections_ftz(U.HP["beta1"], U.HP["beta2"], 3)
-    leaves = ctx.leaves_view().cpu().numpy().view(np.uint64)
-    new_w, new_m, new_v = gather(w, chunks, n), gather(m, chunks, n), gather(v, chunks, n)
-    g_got = gather(ctx.g_view(), chunks, n)
-    for i, k in enumerate(chunks):
-        lo, hi = int(k) * CH, min(int(k) * CH + CH, n)
-        g = O.reduce_ftz([I.to_numpy(gr[i]) for gr in g_before])
-        U.assert_same_f32(g_got[i], g, f"g chunk {k}")
-        _, s = O.norm_ftz(g, with_chunks=True)
-        assert s.view(np.uint32)[0] == chunk_sums[k:k + 1].view(np.uint32)[0], f"chunk sum {k}"
-        w0 = I.to_numpy(s_before[0][i])
-        w1, m1, v1 = O.adamw_ftz(w0, s_before[1][i].numpy(), s_before[2][i].numpy(), g, scale,
-                                 U.HP["lr"], U.HP["beta1"], U.HP["beta2"], U.HP["eps"],
-                                 U.HP["wd"], bc1, bc2, segments=local_segments(segs, lo, hi))
-        U.assert_same_bf16(new_w[i], w1, f"w chunk {k}")
-        U.assert_same_f32(new_m[i], m1, f"m chunk {k}")
-        U.assert_same_f32(new_v[i], v1, f"v chunk {k}")
-        for a, arr in enumerate((O.widen_bf16(w1), m1, v1)):
-            assert leaves[1 + a * c + k] == O.pf61(arr.view(np.uint32)), f"leaf {a} chunk {k}"
-    assert U.root_of(root) == O.merkle_root(leaves)
+    rep = fo.step(grads, 3, U.HP, gpu_views(ctx, w, m, v, norm, root))
+    fo.close()
+    check(rep, wl.name, "bf16w_decay_ftz_mid_run", 3)
 
 
 @pytest.mark.parametrize("nt", [256, 512])
