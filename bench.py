@@ -17,7 +17,8 @@ the step's algorithmic HBM bytes R*b_g*n + 24n per step as GB/s.
 --impl reference times the CPU oracle (the plain single-threaded restatement of the same
 step, the test suite's reference) on the host cores, on a bounded sample of the workload.
 Under torchrun with N > 1 every rank runs an independent replica of the whole step (the
-single-GPU path does not exchange data); value is the sum over ranks.
+single-GPU path does not exchange data); value is the sum over ranks.  --shard runs the
+sharded step instead: one model split over the ranks' GPUs, value = n / step time.
 """
 from __future__ import annotations
 
@@ -292,13 +293,6 @@ def run_ours(args, rank, world, local):
         t_step[0] += 1
         nr = norm if slot is None else norms[slot:slot + 1]
         rt = root if slot is None else roots[slot:slot + 1]
-        if args.graph:
-            # the kept graphs hold the norm output: a fixed one, copied out for the log
-            ctx.step_graph(grads, w, m, v, hp(t_step[0]), step=t_step[0], norm_out=norm,
-                           root_out=rt, nodes=args.nodes)
-            if slot is not None and args.log:
-                nr.copy_(norm)
-            return
         if not args.paper_shard:
             ctx.step(grads, w, m, v, hp(t_step[0]), step=t_step[0], norm_out=nr, root_out=rt,
                      nodes=args.nodes)
@@ -442,8 +436,7 @@ def run_ours(args, rank, world, local):
     torch.cuda.empty_cache()
     cpu = None
     variant = (args.param_dtype != "f32" or args.decay_mask or args.hash_mode != "pf61"
-               or args.subnormals != "ieee" or bool(args.paper_shard) or args.nodes > 1
-               or args.graph)
+               or args.subnormals != "ieee" or bool(args.paper_shard) or args.nodes > 1)
     if rank == 0 and not args.skip_cpu_baseline and not variant:
         cpu = cpu_baseline(wl, n, R, dev, args.cpu_seconds)
 
@@ -460,13 +453,10 @@ def run_ours(args, rank, world, local):
                          f"{(R * b_g + 32) * n / 1e9:.1f} GB moved per step",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "launch": "persistent grid (SM count x resident CTAs), "
-                             f"{args.block_threads or 512} compute threads"
-                             + ("; reduce + clip and AdamW as launches of kept CUDA "
-                                "graphs" if args.graph else ""),
+                             f"{args.block_threads or 512} compute threads",
                    "hash_leaves": args.hash_mode, "param_dtype": args.param_dtype,
                    "decay_mask": bool(args.decay_mask), "subnormals": args.subnormals,
                    "hash_stream": bool(args.hash_stream),
-                   "step_graph": bool(args.graph),
                    "reduce_order": (f"paper-exact, dp_shard {args.paper_shard}"
                                     + (f", accum {args.accum}" if args.accum else "")
                                     if args.paper_shard else
@@ -497,10 +487,108 @@ def run_ours(args, rank, world, local):
     return res
 
 
+def run_sharded(args, rank, world, local):
+    """The sharded step (bitwise_reproducible_step_gb300/shard.py): the workload's n split
+    into `world` chunk-aligned ranges, one per GPU; each rank holds R/world replica gradients
+    of the whole model and its range of the state.  A step is the routing of gradient
+    slices, the local reduce, the chunk-sum all-gather, the gathered norm and clip, AdamW on
+    the range, the leaf all-gather and the gathered root.  Total work is fixed as the world
+    grows (strong scaling): value = n / step time.  One rank routes nothing: it reads its own
+    replicas' slices in place."""
+    import torch.distributed as dist
+    from bitwise_reproducible_step_gb300 import inputs as I
+    from bitwise_reproducible_step_gb300 import repstep as rs
+    from bitwise_reproducible_step_gb300 import shard as S
+
+    wl = I.WORKLOADS[args.workload]
+    if args.n:
+        import dataclasses
+        wl = dataclasses.replace(wl, n=args.n)
+    n, R = wl.n, wl.R
+    if R % world:
+        raise SystemExit(f"--shard needs the replica count {R} to be a multiple of {world}")
+    dev = torch.device("cuda", local)
+    gdt = torch.bfloat16 if wl.grad_dtype == "bf16" else torch.float32
+    b_g = 2 if wl.grad_dtype == "bf16" else 4
+    hpv = I.default_hparams()
+    step = S.ShardedStep(n, R, rank, world, dev, grad_dtype=gdt)
+    plan, Rl = step.plan, R // world
+    lo, hi = plan.range_of(rank)
+    log(f"[rank {rank}] sharded {wl.name}: n={n:,} R={R}, range [{lo:,}, {hi:,}) of {world}")
+    grads = []
+    for j in range(Rl):
+        grads.append(I.gen_grad(wl, 1, rank * Rl + j, device=dev))
+    w_all, m_all, v_all = I.gen_state(wl, device=dev)
+    w, m, v = (x[lo:hi].clone() for x in (w_all, m_all, v_all))
+    del w_all, m_all, v_all
+    torch.cuda.empty_cache()
+    norm = torch.empty(1, dtype=torch.float32, device=dev)
+    root = torch.empty(1, dtype=torch.int64, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    t_step = [0]
+
+    def one():
+        t_step[0] += 1
+        h = rs.hparams(lr=hpv["lr"], beta1=hpv["beta1"], beta2=hpv["beta2"], eps=hpv["eps"],
+                       weight_decay=hpv["wd"], clip=hpv["clip"], t=t_step[0])
+        step.step(grads, w, m, v, h, t_step[0], norm_out=norm, root_out=root)
+
+    repro = {}
+    for i in range(args.warmup):
+        one()
+        if i == 0:
+            step.ctx.sync()
+            repro = {"step1_norm_bits": f"{int(norm.view(torch.int32).item()) & 0xFFFFFFFF:08x}",
+                     "step1_root": f"{int(root.item()) & (2**64 - 1):016x}"}
+    step.ctx.sync()
+    clocks = ClockSampler(local)
+    clocks.start()
+    dist.barrier()
+    torch.cuda.synchronize(dev)
+    launches0 = step.ctx.launch_count()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        one()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    dist.barrier()
+    clk = clocks.stop()
+    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world)
+    peak, peak_src = hbm_peak()
+    alg_step = (R * b_g + 24) * n
+    step_gbs = alg_step / (ms * 1e-3) / 1e9
+    return {
+        "metric": METRIC, "value": n / (ms * 1e-3), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "strong", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": wl.name, "n_params": n, "replicas": R,
+                   "grad_dtype": wl.grad_dtype, "bytes_alg_per_step": alg_step,
+                   "parallelism": f"sharded over {world} chunk-aligned ranges (point-to-point "
+                                  "routing of gradient slices, all-gathers of chunk sums "
+                                  "and leaves)",
+                   "l2": f"inputs larger than L2: {(R * b_g + 32) * n / 1e9:.1f} GB per step"},
+        "hbm_gbs_step": step_gbs,
+        "roofline_step": {"bound": "hbm", "achieved": step_gbs / world, "peak": peak,
+                          "unit": "GB/s per GPU", "frac": step_gbs / world / peak,
+                          "peak_source": peak_src},
+        "clocks": clk,
+        "gpu_launches": step.ctx.launch_count() - launches0,
+        "repro": repro,
+        "e2e": {"value": None, "unit": UNIT,
+                "skipped": "sharded mode: gradients resident on the device"},
+        "cpu_baseline": None,
+    }
+
+
 def run_e2e(args, ctx, wl, grads, w, m, v, hp, t_step, dev, R, b_g, n):
-    """Same step through the public API (Repstep.step_from_host) with the gradients copied
-    from pinned host memory every step -- range by range, each range reduced as it lands --
-    and the pre-clip norm and Merkle root read back to the host."""
+    """The same step end to end through the C ABI's host-buffer call
+    (repstep_step_from_host): every step copies the R gradients from pinned host memory --
+    pipelined over chunk-aligned ranges and copy streams, each range reduced as it lands --
+    and returns the pre-clip norm and the Merkle root in host memory.  The state (w, m, v)
+    stays resident on the device, as an optimizer's state does."""
     need = R * b_g * n
     try:
         avail = int(re.search(r"MemAvailable:\s+(\d+)", open("/proc/meminfo").read()).group(1)) * 1024
@@ -512,21 +600,12 @@ def run_e2e(args, ctx, wl, grads, w, m, v, hp, t_step, dev, R, b_g, n):
     host = [torch.empty(g.shape, dtype=g.dtype, pin_memory=True) for g in grads]
     for h, g in zip(host, grads):
         h.copy_(g)
-    out_h = torch.empty(2, dtype=torch.int64, pin_memory=True)
-    nr = torch.empty(1, dtype=torch.float32, device=dev)
-    rt = torch.empty(1, dtype=torch.int64, device=dev)
     steps = max(2, min(args.e2e_steps, args.steps))
-    stream = torch.cuda.current_stream(dev)
 
     def one():
         t_step[0] += 1
-        ctx.step_from_host(host, grads, w, m, v, hp(t_step[0]), step=t_step[0], norm_out=nr,
-                           root_out=rt)
-        out_h[0:1].view(torch.float32)[0:1].copy_(nr, non_blocking=True)
-        ctx.wait_hash(stream)          # the root is read after the root passes
-        out_h[1:2].copy_(rt, non_blocking=True)
-        stream.synchronize()
-        return float(out_h[0:1].view(torch.float32)[0])
+        return ctx.step_from_host(host, grads, w, m, v, hp(t_step[0]), step=t_step[0],
+                                  pieces=args.e2e_pieces, copy_streams=args.e2e_copy_streams)
 
     # the copy floor on this machine: the same bytes host-to-device with nothing else running
     side = torch.cuda.Stream(dev)
@@ -549,11 +628,17 @@ def run_e2e(args, ctx, wl, grads, w, m, v, hp, t_step, dev, R, b_g, n):
         per_step.append((time.perf_counter() - t1) * 1e3)
     dt = (time.perf_counter() - t0) / steps
     del host
+    fl = min(floor)
     return {"value": n / dt, "unit": UNIT, "ms_per_step": dt * 1e3, "steps": steps,
-            "h2d_bytes_per_step": need, "d2h_bytes_per_step": 8 + 4,
+            "h2d_bytes_per_step": need, "d2h_bytes_per_step": 4 + 8,
+            "api": "repstep_step_from_host (C ABI, host gradient buffers, host norm and root)",
+            "state": "w, m, v resident on the device",
+            "pieces": args.e2e_pieces, "copy_streams": args.e2e_copy_streams,
             "step_ms": [round(x, 2) for x in per_step],
-            "h2d_copy_floor_ms": round(min(floor) * 1e3, 2),
-            "h2d_copy_gbs": round(need / min(floor) / 1e9, 1)}
+            "h2d_gbs_achieved": round(need / dt / 1e9, 1),
+            "h2d_copy_floor_ms": round(fl * 1e3, 2),
+            "h2d_copy_gbs": round(need / fl / 1e9, 1),
+            "frac_of_copy_floor": round(fl / dt, 3)}
 
 
 def cpu_baseline(wl, n, R, dev, seconds):
@@ -642,6 +727,10 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="flat1200m_r8_segscale")
     ap.add_argument("--e2e-steps", type=int, default=6)
+    ap.add_argument("--e2e-pieces", type=int, default=8,
+                    help="chunk-aligned ranges the e2e step pipelines its copies over")
+    ap.add_argument("--e2e-copy-streams", type=int, default=2,
+                    help="streams the e2e step spreads each range's copies over")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--skip-cpu-baseline", action="store_true")
     ap.add_argument("--skip-e2e", action="store_true")
@@ -667,16 +756,14 @@ def main():
     ap.add_argument("--log", default="",
                     help="append a JSON-lines record per timed step (norm, its bits, root, "
                          "event time) and the summary line to this file")
-    ap.add_argument("--graph", action="store_true",
-                    help="run the timed steps' reduce + clip and AdamW as launches of kept "
-                         "CUDA graphs (repstep_step_graph)")
+    ap.add_argument("--shard", action="store_true",
+                    help="the sharded step: n split over the ranks' GPUs (all-to-all + "
+                         "all-gathers); with one process, a one-rank NCCL group")
     ap.add_argument("--n", type=int, default=0,
                     help="override the workload's parameter count (small profiling cases)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
-    if args.graph and args.paper_shard:
-        ap.error("--graph runs the canonical-tree step; it does not take --paper-shard")
 
     if args.impl == "reference":
         world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -687,6 +774,20 @@ def main():
         return
 
     rank, world, local = dist_init(args.gpus)
+    if args.shard:
+        import torch.distributed as dist
+        if not dist.is_initialized():          # one process: a one-rank group of its own
+            import socket
+            with socket.socket() as s_:
+                s_.bind(("127.0.0.1", 0))
+                port = s_.getsockname()[1]
+            dist.init_process_group("nccl", init_method=f"tcp://127.0.0.1:{port}", rank=0,
+                                    world_size=1, device_id=torch.device("cuda", local))
+        res = run_sharded(args, rank, world, local)
+        if rank == 0:
+            print(json.dumps(res), flush=True)
+        dist.destroy_process_group()
+        return
     res = run_ours(args, rank, world, local)
     if rank == 0:
         print(json.dumps(res), flush=True)

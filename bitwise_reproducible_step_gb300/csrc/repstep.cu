@@ -27,6 +27,9 @@ using namespace repstep;
 
 namespace {
 
+constexpr uint32_t kMaxCopyStreams = 8;   // repstep_step_from_host: copy streams
+constexpr uint32_t kMaxPieces = 64;        // ... and pipelined ranges
+
 struct Layout {
     uint64_t g, chunk_sq, norm_part, leaves, merkle_part, powers, scalars, total;
 };
@@ -61,8 +64,12 @@ bool valid_config(const repstep_config *cfg)
 Layout layout_of(uint64_t n)
 {
     const uint64_t c = (n + kChunk - 1) / kChunk;
-    const uint64_t nb2 = c > kChunk ? (c + kChunk - 1) / kChunk : 1;
-    const uint64_t L = 1 + 3 * c;
+    // The norm and Merkle partials are sized for the largest n (2^32 - 1, c = 2^20 chunks),
+    // not for this context's: repstep_clip_gathered and repstep_root_gathered run the same
+    // passes over all shards' chunk sums and leaves (about 26 KB in all).
+    const uint64_t c_max = ((uint64_t(1) << 32) - 1 + kChunk - 1) / kChunk;
+    const uint64_t nb2 = (c_max + kChunk - 1) / kChunk;
+    const uint64_t L = 1 + 3 * c_max;
     // Merkle partials, ping-pong: the first pass's block roots, then the second pass's
     const uint64_t mb1 = (L + kMerkleBlock - 1) / kMerkleBlock;
     const uint64_t mb2 = (mb1 + kMerkleBlock - 1) / kMerkleBlock;
@@ -133,18 +140,14 @@ struct repstep_ctx {
     cudaEvent_t ev_state = nullptr, ev_hash = nullptr;
     bool hash_pending = false;
     std::vector<uint64_t> cut_norm, cut_leaf;   // chunks cut by range boundaries
-    // the graphs of repstep_step_graph, captured on a private stream and instantiated:
-    // [0] the reduce and the clip, [1] AdamW, whose node's hyperparameters replays rewrite
-    struct StepGraph {
-        cudaStream_t capture = nullptr;
-        cudaGraph_t graph[2] = {nullptr, nullptr};   // kept: updates address their nodes
-        cudaGraphExec_t exec[2] = {nullptr, nullptr};
-        uint64_t kernels[2] = {0, 0};                // kernels one launch of each runs
-        cudaGraphNode_t adamw = nullptr;
-        std::vector<uintptr_t> key;                  // pointers and shape captured for
-        uint64_t captures = 0, replays = 0;
-        bool recording = false;                      // a capture is in progress
-    } sg;
+
+    // repstep_step_from_host: copy streams and events, created on first use (host resources
+    // only).  ev_free orders the copies after earlier readers of the staging buffers on the
+    // context's stream; copy_ev[p * kMaxCopyStreams + k] marks the end of range p's copies on
+    // copy stream k, which the reduce of range p waits for.
+    cudaStream_t copy_st[kMaxCopyStreams] = {};
+    std::vector<cudaEvent_t> copy_ev;
+    cudaEvent_t ev_free = nullptr;
 
     float *g() const { return reinterpret_cast<float *>(ws + lay.g); }
     float *chunk_sq() const { return reinterpret_cast<float *>(ws + lay.chunk_sq); }
@@ -165,21 +168,6 @@ struct repstep_ctx {
 };
 
 namespace {
-
-// While a step graph is being captured: the node the last launch on the context's stream
-// added (the capture's only dependency at that point).  Left unset when that is not one
-// node, and replays then capture the step again.
-void note_node(repstep_ctx *x, cudaGraphNode_t *slot)
-{
-    if (!x->sg.recording) return;
-    cudaStreamCaptureStatus status = cudaStreamCaptureStatusNone;
-    const cudaGraphNode_t *deps = nullptr;
-    size_t nd = 0;
-    const cudaError_t e = cudaStreamGetCaptureInfo(x->stream, &status, nullptr, nullptr, &deps,
-                                                   nullptr, &nd);
-    *slot = (e == cudaSuccess && status == cudaStreamCaptureStatusActive && nd == 1) ? deps[0]
-                                                                                      : nullptr;
-}
 
 // Order the context's stream after a root still running on the hash stream: called before
 // anything that writes the leaves, the Merkle partials or the state the root passes read.
@@ -246,7 +234,7 @@ int do_reduce(repstep_ctx *x, const void *const *grads, uint32_t R, uint32_t nod
     if (!paper && nodes > 1 && (gpn & (gpn - 1)) != 0) return REPSTEP_ERR_TOPOLOGY;
     if (begin > x->n || count > x->n - begin) return REPSTEP_ERR_ARG;
     R = uint32_t(inputs);     // the kernel streams every input
-    for (uint32_t r = 0; r < R; ++r) {
+    for (uint32_t r = 0; r < R && count > 0; ++r) {   // an empty range reads no buffer
         if (!grads[r]) return REPSTEP_ERR_ARG;
         if (!aligned(grads[r], 16)) return REPSTEP_ERR_ALIGN;
     }
@@ -299,6 +287,30 @@ int do_reduce(repstep_ctx *x, const void *const *grads, uint32_t R, uint32_t nod
     return REPSTEP_OK;
 }
 
+// The canonical tree over `c` chunk sums, its square root and the clip scale (one or two
+// passes), into the context's scalars and the optional outputs.
+int norm_passes(repstep_ctx *x, const float *sums, uint64_t c, float clip, float *norm_out,
+                float *scale_out)
+{
+    const int fz = x->fz();
+    cudaError_t e;
+    if (c > kChunk) {
+        const int nb = int((c + kChunk - 1) / kChunk);
+        e = launch_norm(sums, c, x->norm_part(), x->sc(), 0, clip, nullptr, nullptr, nb, fz,
+                        x->stream);
+        if (e != cudaSuccess) return x->cuda_fail(e);
+        ++x->launches;
+        e = launch_norm(x->norm_part(), uint64_t(nb), nullptr, x->sc(), 1, clip, norm_out,
+                        scale_out, 1, fz, x->stream);
+    } else {
+        e = launch_norm(sums, c, nullptr, x->sc(), 1, clip, norm_out, scale_out, 1, fz,
+                        x->stream);
+    }
+    if (e != cudaSuccess) return x->cuda_fail(e);
+    ++x->launches;
+    return REPSTEP_OK;
+}
+
 int do_clip(repstep_ctx *x, float clip, float *norm_out, float *scale_out)
 {
     if (!(clip > 0.0f)) return REPSTEP_ERR_ARG;   // also rejects NaN; +inf is allowed
@@ -317,21 +329,8 @@ int do_clip(repstep_ctx *x, float clip, float *norm_out, float *scale_out)
         ++x->launches;
     }
     x->cut_norm.clear();
-    const uint64_t c = x->c;
-    if (c > kChunk) {
-        const int nb = int((c + kChunk - 1) / kChunk);
-        e = launch_norm(x->chunk_sq(), c, x->norm_part(), x->sc(), 0, clip, nullptr, nullptr, nb,
-                        fz, x->stream);
-        if (e != cudaSuccess) return x->cuda_fail(e);
-        ++x->launches;
-        e = launch_norm(x->norm_part(), uint64_t(nb), nullptr, x->sc(), 1, clip, norm_out,
-                        scale_out, 1, fz, x->stream);
-    } else {
-        e = launch_norm(x->chunk_sq(), c, nullptr, x->sc(), 1, clip, norm_out, scale_out, 1,
-                        fz, x->stream);
-    }
-    if (e != cudaSuccess) return x->cuda_fail(e);
-    ++x->launches;
+    const int rc = norm_passes(x, x->chunk_sq(), x->c, clip, norm_out, scale_out);
+    if (rc) return rc;
     x->reduced = 0;
     x->scale_ready = true;
     x->updated = 0;
@@ -369,7 +368,7 @@ void adamw_hparams(const repstep_ctx *x, const repstep_hparams *hp, AdamwArgs &a
 int do_adamw(repstep_ctx *x, void *w, float *m, float *v, const repstep_hparams *hp,
              uint64_t begin, uint64_t count)
 {
-    if (!w || !m || !v) return REPSTEP_ERR_ARG;
+    if (x->n > 0 && (!w || !m || !v)) return REPSTEP_ERR_ARG;   // n = 0 reads no array
     if (!aligned(w, 16) || !aligned(m, 16) || !aligned(v, 16)) return REPSTEP_ERR_ALIGN;
     int rc = check_hparams(hp);
     if (rc) return rc;
@@ -415,30 +414,32 @@ int do_adamw(repstep_ctx *x, void *w, float *m, float *v, const repstep_hparams 
     e = launch_adamw(shape, a, grid, smem, x->stream);
     if (e != cudaSuccess) return x->cuda_fail(e);
     ++x->launches;
-    note_node(x, &x->sg.adamw);
     if (mode == 0) note_cut_chunks(x->cut_leaf, begin, end, x->n);
     return REPSTEP_OK;
 }
 
 // Merkle root over the leaves.  In the PF61 mode the first Merkle pass computes the header
 // leaf itself; in the audit mode the leaf kernel has already written it.
-int merkle(repstep_ctx *x, int32_t step, uint64_t *root_out, cudaStream_t st)
+// The Merkle passes over L leaves (the first pass also writes the PF61 header leaf of
+// {step, n32} to leaves[0] in the PF61 mode) until one block remains: its root goes to the
+// context's scalars and to root_out.
+int merkle_over(repstep_ctx *x, uint64_t *leaves, uint64_t L, int32_t step, uint32_t n32,
+                uint64_t *root_out, cudaStream_t st)
 {
-    const uint64_t L = 1 + 3 * x->c;
     const uint64_t mb1 = (L + kMerkleBlock - 1) / kMerkleBlock;
     // passes until one block remains; the block roots alternate between two regions (the
     // second pass's roots fit the second region, and every later pass's fit either)
     uint64_t *part[2] = {x->merkle_part(), x->merkle_part() + mb1};
-    const uint64_t *in = x->leaves();
+    const uint64_t *in = leaves;
     uint64_t count = L;
     int header = x->cfg.hash_mode == REPSTEP_HASH_PF61 ? 1 : 0;
     for (int pass = 0;; ++pass) {
         const uint64_t nb = (count + kMerkleBlock - 1) / kMerkleBlock;
         const bool last = nb == 1;
         uint64_t *out = last ? nullptr : part[pass & 1];
-        cudaError_t e = launch_merkle(in, count, out, header, x->leaves(), uint32_t(step),
-                                      uint32_t(x->n), x->powers(), x->sc(),
-                                      last ? root_out : nullptr, int(nb), st);
+        cudaError_t e = launch_merkle(in, count, out, header, leaves, uint32_t(step), n32,
+                                      x->powers(), x->sc(), last ? root_out : nullptr, int(nb),
+                                      st);
         if (e != cudaSuccess) return x->cuda_fail(e);
         ++x->launches;
         if (last) return REPSTEP_OK;
@@ -446,6 +447,11 @@ int merkle(repstep_ctx *x, int32_t step, uint64_t *root_out, cudaStream_t st)
         count = nb;
         header = 0;
     }
+}
+
+int merkle(repstep_ctx *x, int32_t step, uint64_t *root_out, cudaStream_t st)
+{
+    return merkle_over(x, x->leaves(), 1 + 3 * x->c, step, uint32_t(x->n), root_out, st);
 }
 
 // Audit mode: BLAKE2b-64 leaves of the whole state (header included).
@@ -636,7 +642,7 @@ int do_step(repstep_ctx *x, const void *const *grads, uint32_t R, uint32_t nodes
             float *norm_out, uint64_t *root_out)
 {
     // validate everything before launching anything
-    if (!w || !m || !v) return REPSTEP_ERR_ARG;
+    if (x->n > 0 && (!w || !m || !v)) return REPSTEP_ERR_ARG;
     if (!aligned(w, 16) || !aligned(m, 16) || !aligned(v, 16)) return REPSTEP_ERR_ALIGN;
     int rc = check_hparams(hp);
     if (rc) return rc;
@@ -654,191 +660,153 @@ int do_step(repstep_ctx *x, const void *const *grads, uint32_t R, uint32_t nodes
     return do_root(x, step, root_out);
 }
 
-void drop_step_graph(repstep_ctx *x)
+// Copy streams and events of repstep_step_from_host, created once per context.
+int ensure_copy_resources(repstep_ctx *x)
 {
-    for (int i = 0; i < 2; ++i) {
-        if (x->sg.exec[i]) cudaGraphExecDestroy(x->sg.exec[i]);
-        if (x->sg.graph[i]) cudaGraphDestroy(x->sg.graph[i]);
-        x->sg.exec[i] = nullptr;
-        x->sg.graph[i] = nullptr;
-        x->sg.kernels[i] = 0;
+    cudaError_t e = cudaSuccess;
+    if (!x->ev_free) e = cudaEventCreateWithFlags(&x->ev_free, cudaEventDisableTiming);
+    for (uint32_t k = 0; e == cudaSuccess && k < kMaxCopyStreams; ++k)
+        if (!x->copy_st[k]) e = cudaStreamCreateWithFlags(&x->copy_st[k], cudaStreamNonBlocking);
+    if (e == cudaSuccess && x->copy_ev.empty()) {
+        x->copy_ev.assign(size_t(kMaxPieces) * kMaxCopyStreams, nullptr);
+        for (cudaEvent_t &ev : x->copy_ev) {
+            e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
+            if (e != cudaSuccess) break;
+        }
     }
-    x->sg.adamw = nullptr;
-    x->sg.key.clear();
+    return e == cudaSuccess ? REPSTEP_OK : x->cuda_fail(e);
 }
 
-// What the step graphs are specific to: every pointer their nodes hold, the replica count
-// and topology, the clip threshold (an argument of the norm kernel) and the decay mask.
-// AdamW's hyperparameters are rewritten on each replay instead.
-std::vector<uintptr_t> step_key(const repstep_ctx *x, const void *const *grads, uint32_t R,
-                                uint32_t nodes, uint32_t gpn, const void *w, const float *m,
-                                const float *v, float clip, const float *norm_out)
+// One step whose gradients start in host memory: the parameter range is cut into `pieces`
+// chunk-aligned ranges; range p of replica r is copied host-to-device into d_staging[r] on
+// copy stream r mod K, and the reduce of range p waits for exactly those copies, so it runs
+// while later ranges are still crossing the host link.  Then clip, AdamW and the root, as
+// in do_step.  A range split that follows the chunk grid gives the bits of one reduce.
+int step_from_host(repstep_ctx *x, const void *const *h_grads, uint32_t R,
+                   void *const *d_staging, uint32_t pieces, uint32_t copy_streams, void *w,
+                   float *m, float *v, const repstep_hparams *hp, int32_t step,
+                   float *h_norm_out, uint64_t *h_root_out)
 {
-    std::vector<uintptr_t> k;
-    k.reserve(R + 9);
-    uint32_t clip_bits = 0;
-    std::memcpy(&clip_bits, &clip, sizeof clip_bits);
-    k.push_back(R);
-    k.push_back(nodes);
-    k.push_back(gpn);
-    k.push_back(clip_bits);
-    for (const void *p : {static_cast<const void *>(w), static_cast<const void *>(m),
-                          static_cast<const void *>(v), static_cast<const void *>(norm_out),
-                          static_cast<const void *>(x->decay_mask)})
-        k.push_back(reinterpret_cast<uintptr_t>(p));
-    for (uint32_t r = 0; r < R; ++r) k.push_back(reinterpret_cast<uintptr_t>(grads[r]));
-    return k;
-}
-
-// Capture part i of the step (0: reduce + clip, 1: AdamW) on the private stream and
-// instantiate it.  The host-side call-order state moves on as the ordinary calls move it.
-int capture_part(repstep_ctx *x, int i, const void *const *grads, uint32_t R, uint32_t nodes,
-                 uint32_t gpn, void *w, float *m, float *v, const repstep_hparams *hp,
-                 float *norm_out)
-{
-    const cudaStream_t user = x->stream;
-    const uint64_t launches0 = x->launches;
-    // relaxed mode: besides kernels and memsets, the calls make only kernel-attribute and
-    // occupancy queries, which enqueue nothing
-    cudaError_t e = cudaStreamBeginCapture(x->sg.capture, cudaStreamCaptureModeRelaxed);
-    if (e != cudaSuccess) return x->cuda_fail(e);
-    x->stream = x->sg.capture;
-    x->sg.recording = true;
-    int rc;
-    if (i == 0) {
-        x->reduced = 0;
-        x->cut_norm.clear();
-        rc = do_reduce(x, grads, R, nodes, gpn, 0, x->n);
-        if (!rc) rc = do_clip(x, hp->clip, norm_out, nullptr);
-    } else {
-        rc = do_adamw(x, w, m, v, hp, 0, x->n);
-    }
-    x->sg.recording = false;
-    x->stream = user;
-    cudaGraph_t graph = nullptr;
-    e = cudaStreamEndCapture(x->sg.capture, &graph);
-    // nothing captured has run yet: the kernels are counted at each launch of the graph
-    x->sg.kernels[i] = x->launches - launches0;
-    x->launches = launches0;
-    if (rc || e != cudaSuccess) {
-        if (graph) cudaGraphDestroy(graph);
-        (void)cudaGetLastError();   // a failed capture leaves no error behind for others
-        return rc ? rc : x->cuda_fail(e);
-    }
-    size_t count = 0;
-    e = cudaGraphGetNodes(graph, nullptr, &count);
-    if (e != cudaSuccess || count == 0) {   // nothing to run (AdamW over n = 0)
-        cudaGraphDestroy(graph);
-        return e == cudaSuccess ? REPSTEP_OK : x->cuda_fail(e);
-    }
-    x->sg.graph[i] = graph;
-    e = cudaGraphInstantiate(&x->sg.exec[i], graph, 0);
-    if (e != cudaSuccess) {
-        x->sg.exec[i] = nullptr;
-        return x->cuda_fail(e);
-    }
-    return REPSTEP_OK;
-}
-
-// Rewrite AdamW's hyperparameters in the kept AdamW graph.
-cudaError_t update_adamw_node(repstep_ctx *x, const repstep_hparams *hp)
-{
-    cudaKernelNodeParams p{};
-    cudaError_t e = cudaGraphKernelNodeGetParams(x->sg.adamw, &p);
-    if (e != cudaSuccess) return e;
-    if (!p.kernelParams) return cudaErrorInvalidValue;
-    AdamwArgs a = *static_cast<const AdamwArgs *>(p.kernelParams[0]);
-    adamw_hparams(x, hp, a);
-    void *args[1] = {&a};
-    p.kernelParams = args;
-    p.extra = nullptr;
-    return cudaGraphExecKernelNodeSetParams(x->sg.exec[1], x->sg.adamw, &p);
-}
-
-int launch_part(repstep_ctx *x, int i)
-{
-    if (!x->sg.exec[i]) return REPSTEP_OK;   // an empty part
-    const cudaError_t e = cudaGraphLaunch(x->sg.exec[i], x->stream);
-    if (e != cudaSuccess) return x->cuda_fail(e);
-    x->launches += x->sg.kernels[i];
-    return REPSTEP_OK;
-}
-
-// The step as two graph launches and the ordinary root: the reduce and the clip, then
-// AdamW (after any root still reading the state on the hash stream), then the root passes,
-// on the hash stream when one is set -- the streams and the order of the ordinary step.
-int step_graph(repstep_ctx *x, const void *const *grads, uint32_t R, uint32_t nodes,
-               uint32_t gpn, void *w, float *m, float *v, const repstep_hparams *hp,
-               int32_t step, float *norm_out, uint64_t *root_out)
-{
-    // the checks of repstep_step, on every call: a replay launches without them
+    // validate everything before enqueuing anything
+    if (!h_grads || !d_staging || R == 0) return REPSTEP_ERR_ARG;
+    if (R > kMaxReplicas) return REPSTEP_ERR_SIZE;
+    if (pieces > kMaxPieces || copy_streams > kMaxCopyStreams) return REPSTEP_ERR_ARG;
     if (!w || !m || !v) return REPSTEP_ERR_ARG;
     if (!aligned(w, 16) || !aligned(m, 16) || !aligned(v, 16)) return REPSTEP_ERR_ALIGN;
+    for (uint32_t r = 0; r < R; ++r) {
+        if (!h_grads[r] || !d_staging[r]) return REPSTEP_ERR_ARG;
+        if (!aligned(d_staging[r], 16)) return REPSTEP_ERR_ALIGN;
+    }
     int rc = check_hparams(hp);
     if (rc) return rc;
     if (!(hp->clip > 0.0f)) return REPSTEP_ERR_ARG;
+    rc = ensure_copy_resources(x);
+    if (rc) return rc;
+    const uint32_t P = pieces ? pieces : 8;
+    uint32_t K = copy_streams ? copy_streams : 2;
+    if (K > R) K = R;
+    const uint64_t esz = x->cfg.grad_dtype == REPSTEP_BF16 ? 2 : 4;
+    uint64_t per = (x->n + P - 1) / P;
+    per = (per + kChunk - 1) / kChunk * kChunk;
+    if (per == 0) per = kChunk;
+
+    // the copies overwrite the staging buffers: after the work already on the context's
+    // stream (an earlier step's reduce reads them)
+    cudaError_t e = cudaEventRecord(x->ev_free, x->stream);
+    for (uint32_t k = 0; e == cudaSuccess && k < K; ++k)
+        e = cudaStreamWaitEvent(x->copy_st[k], x->ev_free, 0);
+    if (e != cudaSuccess) return x->cuda_fail(e);
+    x->reduced = 0;
+    x->cut_norm.clear();
+    if (x->n == 0) {
+        rc = do_reduce(x, d_staging, R, 1, R, 0, 0);
+        if (rc) return rc;
+    }
+    uint32_t p = 0;
+    for (uint64_t lo = 0; lo < x->n; lo += per, ++p) {
+        const uint64_t hi = lo + per < x->n ? lo + per : x->n;
+        for (uint32_t r = 0; r < R; ++r) {
+            e = cudaMemcpyAsync(static_cast<unsigned char *>(d_staging[r]) + lo * esz,
+                                static_cast<const unsigned char *>(h_grads[r]) + lo * esz,
+                                (hi - lo) * esz, cudaMemcpyHostToDevice, x->copy_st[r % K]);
+            if (e != cudaSuccess) return x->cuda_fail(e);
+        }
+        for (uint32_t k = 0; k < K; ++k) {
+            cudaEvent_t ev = x->copy_ev[size_t(p) * kMaxCopyStreams + k];
+            e = cudaEventRecord(ev, x->copy_st[k]);
+            if (e == cudaSuccess) e = cudaStreamWaitEvent(x->stream, ev, 0);
+            if (e != cudaSuccess) return x->cuda_fail(e);
+        }
+        rc = do_reduce(x, d_staging, R, 1, R, lo, hi - lo);
+        if (rc) return rc;
+    }
+    rc = do_clip(x, hp->clip, nullptr, nullptr);
+    if (rc) return rc;
+    rc = do_adamw(x, w, m, v, hp, 0, x->n);
+    if (rc) return rc;
+    rc = do_root(x, step, nullptr);
+    if (rc) return rc;
+    if (!h_norm_out && !h_root_out) return REPSTEP_OK;
+    // the results to the host: the root may still be running on the hash stream
+    rc = join_hash(x);
+    if (rc) return rc;
+    if (h_norm_out) e = cudaMemcpyAsync(h_norm_out, &x->sc()->norm, sizeof(float),
+                                        cudaMemcpyDeviceToHost, x->stream);
+    if (e == cudaSuccess && h_root_out)
+        e = cudaMemcpyAsync(h_root_out, &x->sc()->root, sizeof(uint64_t), cudaMemcpyDeviceToHost,
+                            x->stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(x->stream);
+    return e == cudaSuccess ? REPSTEP_OK : x->cuda_fail(e);
+}
+
+// Sharded steps.  The norm and clip scale from the chunk sums of every shard, gathered by
+// the caller into one array in chunk order; the local reduce must have covered this
+// context's range along the chunk grid (its own chunk sums complete).
+int clip_gathered(repstep_ctx *x, const float *sums, uint64_t c_total, float clip,
+                  float *norm_out, float *scale_out)
+{
+    if (!(clip > 0.0f)) return REPSTEP_ERR_ARG;
+    if (!sums && c_total > 0) return REPSTEP_ERR_ARG;
+    if (c_total > (uint64_t(1) << 20)) return REPSTEP_ERR_SIZE;
+    if (c_total < x->c) return REPSTEP_ERR_ARG;
+    if (!aligned(sums, 4)) return REPSTEP_ERR_ALIGN;
     if (norm_out && !aligned(norm_out, 4)) return REPSTEP_ERR_ALIGN;
-    if (root_out && !aligned(root_out, 8)) return REPSTEP_ERR_ALIGN;
-    if (!grads || R == 0) return REPSTEP_ERR_ARG;
-    if (R > uint32_t(kMaxReplicas)) return REPSTEP_ERR_SIZE;
-    std::vector<uintptr_t> key = step_key(x, grads, R, nodes, gpn, w, m, v, hp->clip, norm_out);
-    const bool reuse = x->sg.exec[0] && x->sg.exec[1] && x->sg.adamw && x->sg.key == key;
-    if (reuse) {
-        ++x->sg.replays;
-        rc = launch_part(x, 0);
-        if (rc) return rc;
-        // the call-order state the reduce and the clip leave behind
-        x->reduced = 0;
-        x->scale_ready = true;
-        x->updated = 0;
-        x->sw = x->sm = x->sv = nullptr;
-        x->cut_norm.clear();
-        x->cut_leaf.clear();
-        // AdamW rewrites the state a pending root reads
-        rc = join_hash(x);
-        if (rc) return rc;
-        const cudaError_t e = update_adamw_node(x, hp);
-        if (e != cudaSuccess) {
-            // an ordinary AdamW launch instead (the same bits); the next call captures
-            (void)cudaGetLastError();
-            drop_step_graph(x);
-            rc = do_adamw(x, w, m, v, hp, 0, x->n);
-            return rc ? rc : do_root(x, step, root_out);
-        }
-        rc = launch_part(x, 1);
-        if (rc) return rc;
-        x->updated = x->n;
-        x->sw = w;
-        x->sm = m;
-        x->sv = v;
-        return do_root(x, step, root_out);
+    if (scale_out && !aligned(scale_out, 4)) return REPSTEP_ERR_ALIGN;
+    if (x->reduced != x->n || !x->cut_norm.empty()) return REPSTEP_ERR_STATE;
+    const int rc = norm_passes(x, sums, c_total, hflush(x->fz(), clip), norm_out, scale_out);
+    if (rc) return rc;
+    x->reduced = 0;
+    x->scale_ready = true;
+    x->updated = 0;
+    x->cut_leaf.clear();
+    x->sw = x->sm = x->sv = nullptr;
+    return REPSTEP_OK;
+}
+
+// The Merkle root over the leaves of every shard, gathered by the caller into
+// leaves[1 .. 3 c_total] in image order; leaves[0] receives the header leaf of
+// (step, n_total).  The local AdamW must have covered this context's range along the chunk
+// grid (so its own chunk leaves were complete when they were gathered).
+int root_gathered(repstep_ctx *x, int32_t step, uint64_t n_total, uint64_t *leaves,
+                  uint64_t *root_out)
+{
+    if (!leaves) return REPSTEP_ERR_ARG;
+    if (!aligned(leaves, 8) || (root_out && !aligned(root_out, 8))) return REPSTEP_ERR_ALIGN;
+    if (n_total > 0xFFFFFFFFull) return REPSTEP_ERR_SIZE;
+    if (n_total < x->n) return REPSTEP_ERR_ARG;
+    if (!x->scale_ready || x->updated != x->n || !x->cut_leaf.empty()) return REPSTEP_ERR_STATE;
+    int rc = join_hash(x);
+    if (rc) return rc;
+    const uint64_t c_total = (n_total + kChunk - 1) / kChunk;
+    if (x->cfg.hash_mode == REPSTEP_HASH_BLAKE2B) {
+        // the BLAKE2b-64 header leaf alone: the leaf kernel with no chunks
+        const cudaError_t e = launch_leaves_b2(nullptr, 0, nullptr, nullptr, n_total, 0, leaves,
+                                               uint32_t(step), x->sm_count, x->stream);
+        if (e != cudaSuccess) return x->cuda_fail(e);
+        ++x->launches;
     }
-    drop_step_graph(x);
-    if (!x->sg.capture) {
-        const cudaError_t e = cudaStreamCreateWithFlags(&x->sg.capture, cudaStreamNonBlocking);
-        if (e != cudaSuccess) {
-            x->sg.capture = nullptr;
-            return x->cuda_fail(e);
-        }
-    }
-    rc = capture_part(x, 0, grads, R, nodes, gpn, w, m, v, hp, norm_out);
-    if (!rc) rc = launch_part(x, 0);
-    if (!rc) rc = join_hash(x);
-    // the AdamW node is the last the capture adds; a capture that adds none (n = 0) or
-    // something else is launched, but not kept for replays
-    if (!rc) rc = capture_part(x, 1, grads, R, nodes, gpn, w, m, v, hp, norm_out);
-    if (!rc) rc = launch_part(x, 1);
-    if (rc) {
-        drop_step_graph(x);
-        return rc;
-    }
-    cudaGraphNodeType type = cudaGraphNodeTypeEmpty;
-    if (x->sg.adamw && (cudaGraphNodeGetType(x->sg.adamw, &type) != cudaSuccess ||
-                        type != cudaGraphNodeTypeKernel))
-        x->sg.adamw = nullptr;
-    x->sg.key.swap(key);
-    ++x->sg.captures;
-    return do_root(x, step, root_out);
+    return merkle_over(x, leaves, 1 + 3 * c_total, step, uint32_t(n_total), root_out,
+                       x->stream);
 }
 
 }  // namespace
@@ -906,8 +874,11 @@ int repstep_destroy(repstep_ctx *ctx)
     if (!ctx) return REPSTEP_ERR_ARG;
     if (ctx->ev_state) cudaEventDestroy(ctx->ev_state);
     if (ctx->ev_hash) cudaEventDestroy(ctx->ev_hash);
-    drop_step_graph(ctx);
-    if (ctx->sg.capture) cudaStreamDestroy(ctx->sg.capture);
+    if (ctx->ev_free) cudaEventDestroy(ctx->ev_free);
+    for (cudaEvent_t ev : ctx->copy_ev)
+        if (ev) cudaEventDestroy(ev);
+    for (cudaStream_t st : ctx->copy_st)
+        if (st) cudaStreamDestroy(st);
     delete ctx;
     return REPSTEP_OK;
 }
@@ -1014,23 +985,31 @@ int repstep_step(repstep_ctx *ctx, const void *const *d_grads, uint32_t R, uint3
                    d_root_out);
 }
 
-int repstep_step_graph(repstep_ctx *ctx, const void *const *d_grads, uint32_t R, uint32_t nodes,
-                       uint32_t gpus_per_node, void *d_w, float *d_m, float *d_v,
-                       const repstep_hparams *hp, int32_t step, float *d_norm_out,
-                       uint64_t *d_root_out)
+int repstep_step_from_host(repstep_ctx *ctx, const void *const *h_grads, uint32_t R,
+                           void *const *d_staging, uint32_t pieces, uint32_t copy_streams,
+                           void *d_w, float *d_m, float *d_v, const repstep_hparams *hp,
+                           int32_t step, float *h_norm_out, uint64_t *h_root_out)
 {
-    const NvtxRange nvtx_("repstep_step_graph");
+    const NvtxRange nvtx_("repstep_step_from_host");
     if (!ctx) return REPSTEP_ERR_ARG;
-    return step_graph(ctx, d_grads, R, nodes, gpus_per_node, d_w, d_m, d_v, hp, step,
-                      d_norm_out, d_root_out);
+    return step_from_host(ctx, h_grads, R, d_staging, pieces, copy_streams, d_w, d_m, d_v, hp,
+                          step, h_norm_out, h_root_out);
 }
 
-int repstep_graph_stats(const repstep_ctx *ctx, uint64_t *captures, uint64_t *replays)
+int repstep_clip_gathered(repstep_ctx *ctx, const float *d_chunk_sums, uint64_t c_total,
+                          float clip, float *d_norm_out, float *d_scale_out)
 {
+    const NvtxRange nvtx_("repstep_clip_gathered");
     if (!ctx) return REPSTEP_ERR_ARG;
-    if (captures) *captures = ctx->sg.captures;
-    if (replays) *replays = ctx->sg.replays;
-    return REPSTEP_OK;
+    return clip_gathered(ctx, d_chunk_sums, c_total, clip, d_norm_out, d_scale_out);
+}
+
+int repstep_root_gathered(repstep_ctx *ctx, int32_t step, uint64_t n_total, uint64_t *d_leaves,
+                          uint64_t *d_root_out)
+{
+    const NvtxRange nvtx_("repstep_root_gathered");
+    if (!ctx) return REPSTEP_ERR_ARG;
+    return root_gathered(ctx, step, n_total, d_leaves, d_root_out);
 }
 
 int repstep_set_decay_mask(repstep_ctx *ctx, const uint32_t *d_mask)

@@ -73,8 +73,9 @@ EXPORTS = [
     "repstep_selftest_fixed_division", "repstep_reduce_paper", "repstep_checkpoint_save",
     "repstep_checkpoint_load", "repstep_set_decay_mask", "repstep_decay_mask_from_segments",
     "repstep_reduce_paper_accum", "repstep_set_hash_stream", "repstep_wait_hash",
-    "repstep_leaves", "repstep_selftest_fast_math", "repstep_step_graph",
-    "repstep_graph_stats",
+    "repstep_leaves", "repstep_selftest_fast_math", "repstep_step_from_host",
+    "repstep_clip_gathered",
+    "repstep_root_gathered",
 ]
 NOALLOC_MAX_N = 1 << 30
 
@@ -105,8 +106,10 @@ def lib():
     L.repstep_leaves.argtypes = [vp, i32, vp, vp, vp]
     L.repstep_step.argtypes = [vp, C.POINTER(vp), u32, u32, u32, vp, vp, vp, C.POINTER(HParams),
                                i32, vp, vp]
-    L.repstep_step_graph.argtypes = L.repstep_step.argtypes
-    L.repstep_graph_stats.argtypes = [vp, C.POINTER(u64), C.POINTER(u64)]
+    L.repstep_clip_gathered.argtypes = [vp, vp, u64, C.c_float, vp, vp]
+    L.repstep_root_gathered.argtypes = [vp, i32, u64, vp, vp]
+    L.repstep_step_from_host.argtypes = [vp, C.POINTER(vp), u32, C.POINTER(vp), u32, u32, vp, vp,
+                                         vp, C.POINTER(HParams), i32, vp, vp]
     L.repstep_image_bytes.argtypes = [u64]
     L.repstep_image_bytes.restype = u64
     L.repstep_image_write.argtypes = [vp, i32, vp, vp, vp, vp, u64, C.c_int]
@@ -368,6 +371,31 @@ class Repstep:
         _check(lib().repstep_clip(self._ctx, clip, self._out(norm_out, torch.float32),
                                   self._out(scale_out, torch.float32)), "clip")
 
+    def clip_gathered(self, chunk_sums, clip: float, norm_out=None, scale_out=None):
+        """Norm and clip scale from every range's chunk sums, gathered in chunk order (a
+        CUDA fp32 tensor of ceil(n_total/4096) slots), in place of clip() in a sharded step
+        (repstep_clip_gathered)."""
+        if not chunk_sums.is_cuda or chunk_sums.dtype != torch.float32 \
+                or not chunk_sums.is_contiguous():
+            raise ValueError("chunk sums: a contiguous CUDA fp32 tensor")
+        self._bind()
+        _check(lib().repstep_clip_gathered(self._ctx, _ptr(chunk_sums), chunk_sums.numel(),
+                                           clip, self._out(norm_out, torch.float32),
+                                           self._out(scale_out, torch.float32)),
+               "clip_gathered")
+
+    def root_gathered(self, step: int, n_total: int, leaves, root_out=None):
+        """Merkle root of a sharded state from every range's leaves gathered in image order
+        into leaves[1:] (a CUDA int64 tensor of 1 + 3 ceil(n_total/4096) slots; slot 0
+        receives the header leaf) (repstep_root_gathered)."""
+        c_total = (n_total + CHUNK - 1) // CHUNK
+        if not leaves.is_cuda or leaves.dtype != torch.int64 or not leaves.is_contiguous() \
+                or leaves.numel() < 1 + 3 * c_total:
+            raise ValueError("leaves: a contiguous CUDA int64 tensor of 1 + 3c slots")
+        self._bind()
+        _check(lib().repstep_root_gathered(self._ctx, int(step), n_total, _ptr(leaves),
+                                           self._out(root_out, torch.int64)), "root_gathered")
+
     def adamw(self, w, m, v, hp: HParams, begin: int = 0, count: int | None = None):
         self._state(w, m, v)
         count = self.n - begin if count is None else count
@@ -404,60 +432,32 @@ class Repstep:
                                   C.byref(hp), int(step), self._out(norm_out, torch.float32),
                                   self._out(root_out, torch.int64)), "step")
 
-    def step_graph(self, grads, w, m, v, hp: HParams, step: int, norm_out=None, root_out=None,
-                   nodes: int = 1, gpus_per_node: int | None = None):
-        """step() with the reduce + clip and AdamW replayed from CUDA graphs the context
-        keeps (repstep_step_graph): the same bits; once the graphs exist for these
-        buffers, two graph launches and the ordinary root passes per call."""
-        arr, R = self._grads(grads)
-        self._state(w, m, v)
-        gpn = R // max(nodes, 1) if gpus_per_node is None else gpus_per_node
-        self._bind()
-        _check(lib().repstep_step_graph(self._ctx, arr, R, nodes, gpn, _ptr(w), _ptr(m),
-                                        _ptr(v), C.byref(hp), int(step),
-                                        self._out(norm_out, torch.float32),
-                                        self._out(root_out, torch.int64)), "step_graph")
-
-    def graph_stats(self) -> tuple[int, int]:
-        """(steps captured into a graph, steps replayed from a kept one)."""
-        cap, rep = C.c_uint64(), C.c_uint64()
-        _check(lib().repstep_graph_stats(self._ctx, C.byref(cap), C.byref(rep)), "graph_stats")
-        return cap.value, rep.value
-
     def step_from_host(self, host_grads, staging, w, m, v, hp: HParams, step: int,
-                       norm_out=None, root_out=None, pieces: int = 8):
-        """One step whose replica gradients start in pinned host memory.
-
-        The parameter range is split into `pieces` chunk-aligned ranges; each range of every
-        replica is copied host-to-device on a side stream into `staging` (R device buffers of
-        n elements) and reduced as soon as it lands, so the reduce overlaps the copies.
-        Then clip, AdamW and the root run on the current stream.  Bit-identical to step()
-        on the same gradients (a reduce split into ranges gives the same bits)."""
+                       pieces: int = 8, copy_streams: int = 2):
+        """One step whose replica gradients start in host memory (repstep_step_from_host):
+        host_grads are R contiguous CPU tensors of the gradient dtype (pinned for
+        asynchronous copies), staging R device buffers of n elements they are copied into.
+        The library pipelines the copies over `pieces` chunk-aligned ranges and
+        `copy_streams` streams, reducing each range as it lands; then clip, AdamW and the
+        root.  Returns (pre-clip norm, root) read back to the host; the call returns after
+        the step has finished.  Bit-identical to step() on the same gradients."""
         host_grads, staging = list(host_grads), list(staging)
         if len(host_grads) != len(staging):
             raise ValueError("one staging buffer per replica")
         for h in host_grads:
-            if h.is_cuda or not h.is_pinned() or not h.is_contiguous() or h.numel() < self.n:
-                raise ValueError("host gradients: contiguous pinned host tensors")
-        main = self._stream()
-        side = torch.cuda.Stream(self.device)
-        side.wait_stream(main)                       # staging buffers free to overwrite
-        per = -(-self.n // max(1, pieces))
-        per = -(-per // CHUNK) * CHUNK               # chunk-aligned ranges
-        for lo in range(0, self.n, per):
-            hi = min(self.n, lo + per)
-            with torch.cuda.stream(side):
-                for h, d in zip(host_grads, staging):
-                    d[lo:hi].copy_(h[lo:hi], non_blocking=True)
-                ev = torch.cuda.Event()
-                ev.record(side)
-            main.wait_event(ev)
-            self.reduce(staging, begin=lo, count=hi - lo)
-        for d in staging:
-            d.record_stream(side)
-        self.clip(hp.clip, norm_out=norm_out)
-        self.adamw(w, m, v, hp)
-        self.root(step, root_out=root_out)
+            if h.is_cuda or h.dtype != self.grad_dtype or not h.is_contiguous() \
+                    or h.numel() < self.n:
+                raise ValueError(f"host gradients: contiguous CPU {self.grad_dtype} tensors of "
+                                 f"at least n={self.n} elements")
+        arr, R = self._grads(staging)
+        self._state(w, m, v)
+        harr = (C.c_void_p * max(R, 1))(*[h.data_ptr() for h in host_grads])
+        nrm, root = C.c_float(), C.c_uint64()
+        self._bind()
+        _check(lib().repstep_step_from_host(self._ctx, harr, R, arr, pieces, copy_streams,
+                                            _ptr(w), _ptr(m), _ptr(v), C.byref(hp), int(step),
+                                            C.byref(nrm), C.byref(root)), "step_from_host")
+        return float(nrm.value), int(root.value)
 
     def set_hash_stream(self, stream: torch.cuda.Stream | None):
         """Run the root passes on `stream`, beside the next step's work on the context's

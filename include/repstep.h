@@ -135,7 +135,9 @@ typedef struct {
 
 /* Bytes of device workspace a context with this configuration needs (0 on a bad config).
  * Layout: g[n] fp32 | chunk sums fp32[c] | norm partials | leaf digests u64[1+3c] |
- * Merkle partials | PF61 power table u64[4096] | device scalars. */
+ * Merkle partials | PF61 power table u64[4096] | device scalars.  The norm and Merkle
+ * partials are sized for the largest n (about 26 KB), so that the gathered calls of a
+ * sharded step can run over every range's chunk sums and leaves. */
 size_t repstep_workspace_bytes(const repstep_config *cfg);
 
 /* Byte offsets of the workspace regions (for inspection and tests): g fp32[n], chunk sums
@@ -186,7 +188,8 @@ int repstep_wait_hash(repstep_ctx *ctx, void *stream);
  * nodes x gpus_per_node (replica r = node*gpus_per_node + gpu) selects a staged sum: each
  * node's replicas first, then the node partials -- the same bits as the flat tree, which
  * the call guarantees by rejecting shapes that would differ (REPSTEP_ERR_TOPOLOGY).
- * Pass nodes = 1, gpus_per_node = R for the flat tree.  Ranges of one step may be reduced
+ * Pass nodes = 1, gpus_per_node = R for the flat tree.  With count = 0 nothing is read, and
+ * the R pointers may be NULL.  Ranges of one step may be reduced
  * in separate calls (reduce-scatter into shards, OPEN-1B App. A.2); chunks cut by a range
  * boundary are summed at clip time from the complete g. */
 int repstep_reduce(repstep_ctx *ctx, const void *const *d_grads, uint32_t R, uint32_t nodes,
@@ -226,12 +229,43 @@ int repstep_clip(repstep_ctx *ctx, float clip, float *d_norm_out, float *d_scale
 
 /* Clipped AdamW over [begin, begin+count) of the full-length arrays w (param_dtype), m, v
  * (fp32), updated in place, using g and the scale from the last reduce/clip.  All three
- * pointers 16-byte aligned.  Also writes the PF61 leaf
+ * pointers 16-byte aligned (and non-NULL unless the context's n is 0).  Also writes the PF61 leaf
  * digest of every new w, m and v chunk lying wholly inside the range; repstep_root()
  * completes the others.  All calls of one step must pass the same w, m, v base pointers.
  * Requires repstep_clip() since the last reduce (else REPSTEP_ERR_STATE). */
 int repstep_adamw(repstep_ctx *ctx, void *d_w, float *d_m, float *d_v,
                   const repstep_hparams *hp, uint64_t begin, uint64_t count);
+
+/* Sharded steps ("OPEN-1B: A Fully Auditable Training Run", App. A.2: reduce-scatter over
+ * shards -- each shard owner receives every replica's slice of its range and sums it in a
+ * fixed order).  Each GPU owns one chunk-aligned range of the flat parameters and a context
+ * whose n is that range's length; the exchanges between GPUs are the caller's collective
+ * library, and carry data only: a routing of gradient slices before repstep_reduce, an
+ * all-gather of the ranges' chunk sums before repstep_clip_gathered, an all-gather of
+ * their leaf digests before repstep_root_gathered.  Every floating-point sum stays in this
+ * library's canonical trees, so the bits equal the unsharded step's.
+ *
+ * repstep_clip_gathered: the global pre-clip norm and clip scale from d_chunk_sums, the
+ * c_total = ceil(n_total/4096) chunk sums of every range in chunk order (fp32, 4-byte
+ * aligned; this context's own are at repstep_layout.chunk_sums after its reduce).  Takes
+ * the place of repstep_clip: the reduce calls since the last clip must have covered this
+ * context's n along the chunk grid (REPSTEP_ERR_STATE otherwise), and the scale is kept for
+ * repstep_adamw.  c_total below this context's chunk count is REPSTEP_ERR_ARG, above 2^20
+ * REPSTEP_ERR_SIZE. */
+int repstep_clip_gathered(repstep_ctx *ctx, const float *d_chunk_sums, uint64_t c_total,
+                          float clip, float *d_norm_out, float *d_scale_out);
+
+/* repstep_root_gathered: the Merkle root of the whole sharded state.  d_leaves (u64,
+ * 8-byte aligned) holds 1 + 3 c_total slots: slots 1 .. 3 c_total the chunk leaf digests of
+ * every range, gathered by the caller in image order (all w chunks, then all m chunks,
+ * then all v chunks; this context's own are at repstep_layout.leaves + 1 after
+ * repstep_adamw, or after repstep_leaves in audit mode); slot 0 receives the header leaf
+ * of (step, n_total).  Requires the AdamW calls since the clip to have covered this
+ * context's n along the chunk grid (REPSTEP_ERR_STATE).  Writes the root to d_root_out
+ * (nullable) and to the context's scalars.  n_total below this context's n is
+ * REPSTEP_ERR_ARG, at or above 2^32 REPSTEP_ERR_SIZE. */
+int repstep_root_gathered(repstep_ctx *ctx, int32_t step, uint64_t n_total, uint64_t *d_leaves,
+                          uint64_t *d_root_out);
 
 /* Per-segment weight decay (OPEN-1B §3.2, optimizer paragraph: the embeddings, the
  * normalisation gains and RoPE take no weight decay).  d_mask is a device bitmask of
@@ -281,28 +315,37 @@ int repstep_step(repstep_ctx *ctx, const void *const *d_grads, uint32_t R, uint3
                  const repstep_hparams *hp, int32_t step, float *d_norm_out,
                  uint64_t *d_root_out);
 
-/* repstep_step with its streaming part replayed from CUDA graphs that the context keeps:
- * the same arguments, checks, bits, streams and device writes.
- * - Capture.  The first call captures two graphs on a private stream and instantiates
- *   them: the reduce with the clip, and AdamW.  So does a call whose gradient, state or
- *   norm-output pointers, replica count, topology, clip threshold or decay mask differ
- *   from the kept graphs'.
- * - Replay.  Other calls launch the first graph, rewrite the hyperparameters in the AdamW
- *   node of the second (after any root still pending on the hash stream, as the ordinary
- *   step waits), and launch it: two launches in place of the kernels and memsets, and
- *   none of the per-kernel host work.
- * - Root.  The root passes are ordinary launches, on the hash stream when one is set, so
- *   they overlap the next step's reduce as in repstep_step; d_root_out may change freely.
- * - Resources.  The first call creates a stream; the graphs are freed by repstep_destroy
- *   or by the next capture.  Host resources only: no device memory. */
-int repstep_step_graph(repstep_ctx *ctx, const void *const *d_grads, uint32_t R,
-                       uint32_t nodes, uint32_t gpus_per_node, void *d_w, float *d_m,
-                       float *d_v, const repstep_hparams *hp, int32_t step, float *d_norm_out,
-                       uint64_t *d_root_out);
-
-/* Counters of repstep_step_graph (nullable outputs): the steps it captured and
- * instantiated graphs for, and the steps it replayed from kept graphs. */
-int repstep_graph_stats(const repstep_ctx *ctx, uint64_t *captures, uint64_t *replays);
+/* One whole step whose R replica gradients start in HOST memory, with the norm and the
+ * root returned to host memory: the end-to-end form of repstep_step for a caller whose
+ * gradients arrive on the host side ("OPEN-1B: A Fully Auditable Training Run", §5: the
+ * paper's step moves state to the host to hash it; here only the gradients cross the host
+ * link, once, and everything after them runs on the device).
+ * - h_grads: host array of R host pointers, each to n gradient elements of grad_dtype, in
+ *   global replica order.  Page-locked memory (cudaHostAlloc, cudaHostRegister) lets the
+ *   copies run asynchronously; pageable memory works, but each copy then blocks the host.
+ * - d_staging: host array of R device pointers to caller-owned buffers of n elements
+ *   (16-byte aligned) that the gradients are copied into and reduced from.  They must not
+ *   be written by other code while the call's work runs.
+ * - pieces: the parameter range is cut into this many chunk-aligned ranges (0: 8; at most
+ *   64); range p of every replica is copied, and its reduce starts as soon as those copies
+ *   are done, while later ranges are still being copied.
+ * - copy_streams: the copies of a range are spread over this many streams, replica r on
+ *   stream r mod copy_streams (0: 2; at most 8; at most R are used).  The streams and
+ *   their events are created on the first call (host resources; no device memory) and
+ *   wait for the work already on the context's stream before overwriting the staging.
+ * - d_w, d_m, d_v, hp, step: as repstep_step.  The state stays on the device.
+ * - h_norm_out (fp32), h_root_out (u64): host outputs, nullable.  When either is given,
+ *   the call copies the pre-clip norm and the root there and returns after the step has
+ *   finished (it synchronises the context's stream, after joining a pending root on the
+ *   hash stream).  With both NULL it returns once everything is enqueued.
+ * Bits: identical to repstep_step on the same gradients (a reduce split along the chunk
+ * grid gives the bits of one reduce).  Errors: REPSTEP_ERR_ARG (null pointer, R == 0,
+ * pieces > 64, copy_streams > 8, bad hyperparameter), REPSTEP_ERR_SIZE (R > 256),
+ * REPSTEP_ERR_ALIGN, REPSTEP_ERR_CUDA; nothing is enqueued on an argument error. */
+int repstep_step_from_host(repstep_ctx *ctx, const void *const *h_grads, uint32_t R,
+                           void *const *d_staging, uint32_t pieces, uint32_t copy_streams,
+                           void *d_w, float *d_m, float *d_v, const repstep_hparams *hp,
+                           int32_t step, float *h_norm_out, uint64_t *h_root_out);
 
 /* Checkpoint image ("grow_a_language_model_checkpoints", Format):
  * [LE int32 step][LE uint32 n][n fp32 w][n fp32 m][n fp32 v], 8 + 12n bytes, written to
@@ -405,9 +448,12 @@ const char *repstep_strerror(int code);
  * cudaMalloc, cudaFree or allocating library routine.  Every call on a device shares the
  * same array and leaves its contents behind (each call clears what must start at zero), so
  * calls whose GPU work overlaps -- on different streams or host threads -- race and give
- * undefined results: serialise them.  The first call on each device looks up the array's
- * device address (cudaGetSymbolAddress) with that device current; make that first call
- * before any stream capture.  Returns REPSTEP_OK, REPSTEP_ERR_ARG, REPSTEP_ERR_ALIGN,
+ * undefined results: serialise them.  The first call on each device, with that device
+ * current, looks up the array's device address (cudaGetSymbolAddress) and -- since CUDA
+ * loads device code lazily by default -- may load the library's device code and this array
+ * onto the device, which does take device memory.  So make that first call at start-up,
+ * before the device's memory is taken and before any stream capture; from then until the
+ * process exits the array stays held and later calls allocate nothing.  Returns REPSTEP_OK, REPSTEP_ERR_ARG, REPSTEP_ERR_ALIGN,
  * REPSTEP_ERR_SIZE or REPSTEP_ERR_CUDA. */
 #define REPSTEP_NOALLOC_MAX_N (1ull << 30)
 int repstep_reduce_norm_noalloc(const void *const *d_grads, uint32_t R, int32_t grad_dtype,

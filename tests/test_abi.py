@@ -123,12 +123,12 @@ def test_create_rejects_before_touching_a_device(L):
     assert L.repstep_clip(None, 1.0, None, None) == 1
     assert L.repstep_sync(None, None) == 1
     hp = rs.HParams()
-    for name in ("repstep_step", "repstep_step_graph"):
-        assert getattr(L, name)(None, None, 1, 1, 1, None, None, None, C.byref(hp), 1, None,
-                                None) == 1
-    cap, rep = C.c_uint64(7), C.c_uint64(7)
-    assert L.repstep_graph_stats(None, C.byref(cap), C.byref(rep)) == 1
-    assert (cap.value, rep.value) == (7, 7)
+    assert L.repstep_step(None, None, 1, 1, 1, None, None, None, C.byref(hp), 1, None,
+                          None) == 1
+    assert L.repstep_step_from_host(None, None, 1, None, 0, 0, None, None, None, C.byref(hp), 1,
+                                    None, None) == 1
+    assert L.repstep_clip_gathered(None, None, 0, 1.0, None, None) == 1
+    assert L.repstep_root_gathered(None, 1, 0, None, None) == 1
 
 
 def test_image_bytes(L):

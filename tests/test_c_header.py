@@ -51,7 +51,8 @@ int main(void)
     printf("rejects %d %d %d %d\n",
            repstep_create(&cfg, NULL, ws, NULL, &ctx),
            repstep_step(NULL, NULL, 1, 1, 1, NULL, NULL, NULL, &hp, 1, NULL, NULL),
-           repstep_step_graph(NULL, NULL, 1, 1, 1, NULL, NULL, NULL, &hp, 1, NULL, NULL),
+           repstep_step_from_host(NULL, NULL, 1, NULL, 0, 0, NULL, NULL, NULL, &hp, 1, NULL,
+                                  NULL),
            repstep_sync(NULL, NULL));
     return ctx == NULL ? 0 : 1;
 }

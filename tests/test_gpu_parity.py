@@ -347,32 +347,6 @@ def test_fused_equals_separate_calls_and_standalone_hash():
         assert rr[0] == rr[1] == rr[2]
 
 
-def test_step_from_host_equals_step():
-    """Gradients uploaded range by range from pinned host memory, each range reduced as it
-    lands: the same bits as the fused step on device-resident gradients."""
-    n, R = 5 * 4096 * 3 + 77, 8
-    dev = torch.device("cuda", 0)
-    a, b = rs.Repstep(n, device=dev), rs.Repstep(n, device=dev)
-    wa, ma, va = I.gen_state(U.F32_WL, n=n, device=dev)
-    wb, mb, vb = wa.clone(), ma.clone(), va.clone()
-    staging = [torch.empty(n, dtype=torch.float32, device=dev) for _ in range(R)]
-    r = torch.empty(2, dtype=torch.int64, device=dev)
-    nrm = torch.empty(2, dtype=torch.float32, device=dev)
-    for t in (1, 2):
-        grads = U.gen_grads(n, R, t, scale=1000.0)
-        host = [g.cpu().pin_memory() for g in grads]
-        hp = U.hp_for(t)
-        a.step(grads, wa, ma, va, hp, step=t, norm_out=nrm[0:1], root_out=r[0:1])
-        b.step_from_host(host, staging, wb, mb, vb, hp, step=t, norm_out=nrm[1:2],
-                         root_out=r[1:2], pieces=5)
-        a.sync(); b.sync()
-        U.assert_same_f32(wb, wa.cpu().numpy(), "w")
-        U.assert_same_f32(vb, va.cpu().numpy(), "v")
-        assert nrm[0].item() == nrm[1].item()
-        rr = r.cpu().numpy().view(np.uint64)
-        assert rr[0] == rr[1]
-
-
 def test_call_order_is_enforced():
     n = 5000
     dev = torch.device("cuda", 0)

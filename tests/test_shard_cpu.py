@@ -1,0 +1,154 @@
+"""The sharded step's exchange layer (bitwise_reproducible_step_gb300/shard.py) on CPU
+processes over gloo, world sizes 2 and 4.
+
+Each rank holds R/N replica gradients of the whole model and one chunk-aligned range of the
+state.  The test checks the three exchanges byte for byte:
+  * route_gradients delivers every replica's slice of the rank's range, in global replica
+    order, bit-exact (fp32 and bf16), its own replicas' slices read in place;
+  * gather_chunk_sums returns every chunk's sum of squares in chunk order;
+  * gather_leaves returns every chunk leaf in image order.
+The per-rank arithmetic here is the oracle's (the test's stand-in for the GPU kernels): the
+reduce of the routed slices, the chunk sums and AdamW of the local range, its leaves.  Fed
+the gathered arrays, the oracle's tree over the chunk sums and its Merkle tree must give the
+unsharded step's norm and root, and every rank the same ones ("OPEN-1B: A Fully Auditable
+Training Run", App. A.2: reduce-scatter into shards before the optimizer step)."""
+import os
+import socket
+
+import numpy as np
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+from bitwise_reproducible_step_gb300 import shard as S
+
+CH = 4096
+HP = dict(lr=np.float32(3e-4), beta1=np.float32(0.9), beta2=np.float32(0.999),
+          eps=np.float32(1e-8), wd=np.float32(0.1), clip=np.float32(1.0))
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _inputs(n, R, bf16, seed):
+    """Every replica's gradient (host numpy: fp32, or bf16 as uint16 bits) and the state."""
+    rng = np.random.default_rng(seed)
+    grads = []
+    for r in range(R):
+        x = (rng.standard_normal(n) * 10.0 ** (-3 + r % 3)).astype(np.float32)
+        if bf16:
+            x = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+        grads.append(x)
+    w = (rng.standard_normal(n) * 0.02).astype(np.float32)
+    m = (rng.standard_normal(n) * 1e-3).astype(np.float32)
+    v = ((rng.standard_normal(n) * 1e-3) ** 2).astype(np.float32)
+    return grads, w, m, v
+
+
+def _as_tensor(x, bf16):
+    """A gradient buffer as the exchange takes it."""
+    if bf16:
+        return torch.from_numpy(x.view(np.int16).copy()).view(torch.bfloat16)
+    return torch.from_numpy(x.copy())
+
+
+def _host(t):
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy().view(np.uint16)
+    return t.numpy()
+
+
+def _rank_main(rank, world, port, n, R, bf16, t, seed):
+    from oracle import oracle as O
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        plan = S.ShardPlan(n, world)
+        grads, w, m, v = _inputs(n, R, bf16, seed)
+        Rl = R // world
+        mine = [_as_tensor(grads[rank * Rl + j], bf16) for j in range(Rl)]
+        lo, hi = plan.range_of(rank)
+
+        # 1. routing: every replica's slice of this range, global replica order, bit-exact
+        slices = S.route_gradients(mine, plan, rank, R)
+        assert len(slices) == R
+        for r in range(R):
+            got = _host(slices[r])
+            assert got.shape == (hi - lo,)
+            assert np.array_equal(got.view(np.uint16 if bf16 else np.uint32),
+                                  grads[r][lo:hi].view(np.uint16 if bf16 else np.uint32)), r
+
+        # the rank's arithmetic (oracle as the stand-in for the GPU kernels)
+        g_loc = O.reduce([_host(s) for s in slices]) if hi > lo else np.zeros(0, np.float32)
+        _, sums_loc = O.norm(g_loc, with_chunks=True) if hi > lo else (0, np.zeros(0, np.float32))
+
+        # 2. chunk sums gathered in chunk order = the unsharded oracle's
+        sums = S.gather_chunk_sums(torch.from_numpy(np.ascontiguousarray(sums_loc)), plan, rank)
+        g_all = O.reduce(grads)
+        norm_all, sums_all = O.norm(g_all, with_chunks=True)
+        assert np.array_equal(sums.numpy().view(np.uint32), sums_all.view(np.uint32))
+        norm = np.sqrt(O.tree_sum(sums.numpy()), dtype=np.float32)
+        assert norm.view(np.uint32) == np.float32(norm_all).view(np.uint32)
+
+        # 3. AdamW of the local range, its leaves, gathered in image order
+        scale = O.clip_scale(norm, HP["clip"])
+        bc1, bc2 = O.bias_corrections(HP["beta1"], HP["beta2"], t)
+        hpv = (scale, HP["lr"], HP["beta1"], HP["beta2"], HP["eps"], HP["wd"], bc1, bc2)
+        w1, m1, v1 = O.adamw(w[lo:hi], m[lo:hi], v[lo:hi], g_loc, *hpv)
+        leaves_loc = O.leaves(t, w1, m1, v1) if hi > lo else np.zeros(1, np.uint64)
+        leaves = S.gather_leaves(torch.from_numpy(leaves_loc.view(np.int64)), plan, rank)
+        W, M, V = O.adamw(w, m, v, g_all, *hpv)
+        want = O.leaves(t, W, M, V)
+        got = leaves.numpy().view(np.uint64)
+        assert got[0] == 0 and np.array_equal(got[1:], want[1:])
+        got = got.copy()
+        got[0] = O.pf61(np.array([t, n], np.uint32))
+        assert O.merkle_root(got) == O.state_hash(t, W, M, V)
+        # every rank ends with the same norm and root
+        both = torch.tensor([int(norm.view(np.uint32)), O.merkle_root(got) & (2 ** 62 - 1)],
+                            dtype=torch.int64)
+        allv = [torch.empty_like(both) for _ in range(world)]
+        dist.all_gather(allv, both)
+        assert all(torch.equal(x, allv[0]) for x in allv)
+    finally:
+        dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("world,n,R,bf16", [
+    (2, 5 * CH * 2 + 1234, 8, False),        # ragged last chunk
+    (2, 3 * CH, 2, True),                    # one replica per rank, bf16
+    (4, 7 * CH + 17, 8, False),              # uneven: cr = 2, the last rank owns 2 chunks
+    (4, 2 * CH + 5, 4, True),                # c = 3 < world: the last rank owns nothing
+])
+def test_sharded_exchange_equals_unsharded_oracle(world, n, R, bf16):
+    mp.spawn(_rank_main, args=(world, _free_port(), n, R, bf16, 2, 11 + world), nprocs=world,
+             join=True)
+
+
+def test_plan_ranges_cover_the_chunk_grid():
+    for n, N in [(1, 1), (4096, 3), (5 * CH + 7, 2), (10 ** 6, 8), (1_200_000_000, 8),
+                 (3_000_000_000, 8), (2 * CH + 5, 4)]:
+        p = S.ShardPlan(n, N)
+        ranges = [p.range_of(s) for s in range(N)]
+        assert ranges[0][0] == 0 and ranges[-1][1] == n
+        for (a, b), (c, d) in zip(ranges, ranges[1:]):
+            assert b == c
+        for lo, hi in ranges:
+            assert (lo % CH == 0 or lo == n) and (hi % CH == 0 or hi == n) and hi - lo <= p.stride
+        assert sum(p.chunks_of(s) for s in range(N)) == p.c
+        assert p.stride % CH == 0 and N * p.stride >= n
+
+
+def test_route_rejects_short_or_miscounted_buffers():
+    p = S.ShardPlan(3 * CH + 1, 2)
+    with pytest.raises(ValueError):
+        S.route_gradients([torch.zeros(3 * CH)], p, 0, 2)            # shorter than n
+    with pytest.raises(ValueError):
+        S.route_gradients([torch.zeros(p.n)] * 2, p, 0, 2)           # R/N = 1 expected
+    with pytest.raises(ValueError):
+        S.route_gradients([torch.zeros(p.n)], p, 0, 3)               # N does not divide R
