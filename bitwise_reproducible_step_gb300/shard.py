@@ -180,12 +180,17 @@ class ShardedStep:
     are the whole model's, the same on every rank and equal to the unsharded step's."""
 
     def __init__(self, n: int, R: int, rank: int, world: int, device, group=None,
-                 grad_dtype=torch.float32, **ctx_kw):
-        from . import repstep as rs
+                 grad_dtype=torch.float32, ctx=None, **ctx_kw):
+        """ctx: the rank's context over its range (default: a new Repstep of n = the
+        range's length on `device`, built with ctx_kw); anything with the same calls
+        works, which lets the exchanges be exercised without a GPU."""
         self.plan = ShardPlan(n, world)
         self.R, self.rank, self.group = R, rank, group
         self.lo, self.hi = self.plan.range_of(rank)
-        self.ctx = rs.Repstep(self.hi - self.lo, grad_dtype=grad_dtype, device=device, **ctx_kw)
+        if ctx is None:
+            from . import repstep as rs
+            ctx = rs.Repstep(self.hi - self.lo, grad_dtype=grad_dtype, device=device, **ctx_kw)
+        self.ctx = ctx
         self.recv = torch.empty((R // world, world - 1, self.plan.stride), dtype=grad_dtype,
                                 device=device)
         self.audit = self.ctx.hash_mode != 0

@@ -152,3 +152,107 @@ def test_route_rejects_short_or_miscounted_buffers():
         S.route_gradients([torch.zeros(p.n)] * 2, p, 0, 2)           # R/N = 1 expected
     with pytest.raises(ValueError):
         S.route_gradients([torch.zeros(p.n)], p, 0, 3)               # N does not divide R
+
+
+class OracleCtx:
+    """The test's stand-in for one rank's repstep context on the CPU: the calls ShardedStep
+    makes, computed by the oracle on CPU tensors.  It lets ShardedStep's own sequence of
+    exchanges and calls run across gloo ranks without a GPU."""
+
+    def __init__(self, n, hash_mode=0):
+        self.n, self.c, self.hash_mode = n, (n + CH - 1) // CH, hash_mode
+        self.g = np.zeros(n, np.float32)
+        self.cs = np.zeros(self.c, np.float32)
+        self.lv = np.zeros(1 + 3 * self.c, np.uint64)
+        self.scale = np.float32(1.0)
+
+    def reduce(self, slices):
+        from oracle import oracle as O
+        if self.n:
+            self.g = O.reduce([_host(s) for s in slices])
+            _, self.cs = O.norm(self.g, with_chunks=True)
+
+    def chunk_sums_view(self):
+        return torch.from_numpy(self.cs)
+
+    def clip_gathered(self, sums, clip, norm_out=None):
+        from oracle import oracle as O
+        norm = np.sqrt(O.tree_sum(sums.numpy()), dtype=np.float32)
+        self.scale = O.clip_scale(norm, clip)
+        if norm_out is not None:
+            norm_out[0] = float(norm)
+
+    def adamw(self, w, m, v, hp):
+        from oracle import oracle as O
+        if not self.n:
+            return
+        w1, m1, v1 = O.adamw(w.numpy(), m.numpy(), v.numpy(), self.g, self.scale, hp.lr,
+                             hp.beta1, hp.beta2, hp.eps, hp.weight_decay, hp.bc1, hp.bc2)
+        w.copy_(torch.from_numpy(w1)); m.copy_(torch.from_numpy(m1)); v.copy_(torch.from_numpy(v1))
+        self.lv = O.leaves(0, w1, m1, v1)          # the chunk leaves; the header is not used
+
+    def leaves(self, step, w, m, v):
+        from oracle import oracle as O
+        if self.n:
+            self.lv = O.leaves(step, w.numpy(), m.numpy(), v.numpy(), self.hash_mode)
+
+    def leaves_view(self):
+        return torch.from_numpy(self.lv.view(np.int64))
+
+    def root_gathered(self, step, n_total, leaves, root_out=None):
+        from oracle import oracle as O
+        L = leaves.numpy().view(np.uint64).copy()
+        hdr = np.array([step, n_total], np.uint32)
+        L[0] = O.pf61(hdr) if self.hash_mode == 0 else \
+            int.from_bytes(O.blake2b(hdr.astype("<u4").tobytes(), 8), "little")
+        if root_out is not None:
+            root_out[0] = int(np.array([O.merkle_root(L)], np.uint64).view(np.int64)[0])
+
+
+def _sharded_step_main(rank, world, port, n, R, bf16, hash_mode, seed):
+    from bitwise_reproducible_step_gb300 import repstep as rs
+    from oracle import oracle as O
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        gdt = torch.bfloat16 if bf16 else torch.float32
+        lo, hi = S.ShardPlan(n, world).range_of(rank)
+        step = S.ShardedStep(n, R, rank, world, "cpu", grad_dtype=gdt,
+                             ctx=OracleCtx(hi - lo, hash_mode))
+        assert (step.lo, step.hi) == (lo, hi)
+        _, W, M, V = _inputs(n, R, bf16, seed)
+        w, m, v = (torch.from_numpy(x[lo:hi].copy()) for x in (W, M, V))
+        Rl = R // world
+        for t in (1, 2):
+            grads, _, _, _ = _inputs(n, R, bf16, seed + 100 * t)
+            mine = [_as_tensor(grads[rank * Rl + j], bf16) for j in range(Rl)]
+            hp = rs.hparams(lr=HP["lr"], beta1=HP["beta1"], beta2=HP["beta2"], eps=HP["eps"],
+                            weight_decay=HP["wd"], clip=HP["clip"], t=t)
+            norm = torch.zeros(1, dtype=torch.float32)
+            root = torch.zeros(1, dtype=torch.int64)
+            step.step(mine, w, m, v, hp, t, norm_out=norm, root_out=root)
+            ref = O.step(grads, W, M, V, lr=HP["lr"], beta1=HP["beta1"], beta2=HP["beta2"],
+                         eps=HP["eps"], wd=HP["wd"], clip=HP["clip"], t=t, hash_mode=hash_mode)
+            W, M, V = ref["w"], ref["m"], ref["v"]
+            assert np.float32(norm.item()).view(np.uint32) == np.float32(ref["norm"]).view(np.uint32)
+            assert int(root.numpy().view(np.uint64)[0]) == ref["root"], (rank, t)
+            for a, b in ((w, W), (m, M), (v, V)):
+                assert np.array_equal(a.numpy().view(np.uint32), b[lo:hi].view(np.uint32))
+    finally:
+        dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("world,n,R,bf16,hash_mode", [
+    (2, 4 * CH * 2 + 999, 4, False, 0),
+    (4, 9 * CH + 1, 8, True, 1),             # bf16 gradients, audit-mode leaves
+    (4, 2 * CH + 5, 4, False, 0),            # the last rank owns nothing
+])
+def test_sharded_step_across_ranks_equals_unsharded_oracle(world, n, R, bf16, hash_mode):
+    """ShardedStep's own sequence -- routing, local reduce, chunk-sum gather, gathered clip,
+    AdamW, leaf gather, gathered root -- over gloo ranks, two steps, against the unsharded
+    oracle step: every rank's norm, root and state range bit for bit."""
+    from bitwise_reproducible_step_gb300 import build
+    build.build()                             # the host-side bias corrections
+    mp.spawn(_sharded_step_main, args=(world, _free_port(), n, R, bf16, hash_mode, 31 + world),
+             nprocs=world, join=True)
