@@ -64,7 +64,18 @@ def log(*a):
 # ------------------------------------------------------------------------------------
 # distributed plumbing (one process per GPU; independent replicas)
 # ------------------------------------------------------------------------------------
+def quiet_nccl():
+    """Keep stdout to the one JSON line.  NCCL_DEBUG=VERSION (set in some images) prints a
+    version banner on stdout that NCCL_DEBUG_FILE does not redirect, so that level becomes
+    WARN for this process; NCCL's debug lines go to stderr."""
+    if os.environ.get("NCCL_DEBUG", "").upper() == "VERSION":
+        os.environ["NCCL_DEBUG"] = "WARN"
+    if os.environ.get("NCCL_DEBUG") and not os.environ.get("NCCL_DEBUG_FILE"):
+        os.environ["NCCL_DEBUG_FILE"] = "/dev/stderr"
+
+
 def dist_init(n_gpus):
+    quiet_nccl()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
