@@ -441,7 +441,7 @@ def run_ours(args, rank, world, local):
     # ---- end to end: grads from pinned host memory each step, norm+root read back ----
     ctx.set_hash_stream(hash_side)
     e2e = None if args.skip_e2e else run_e2e(args, ctx, wl, grads, w, m, v, hp, t_step, dev,
-                                              R, b_g, n)
+                                              R, b_g, n, world)
 
     del grads
     torch.cuda.empty_cache()
@@ -594,20 +594,38 @@ def run_sharded(args, rank, world, local):
     }
 
 
-def run_e2e(args, ctx, wl, grads, w, m, v, hp, t_step, dev, R, b_g, n):
+def host_fits(need: int, world: int, avail: int | None = None, device="cuda"):
+    """Whether every rank can pin `need` bytes of host memory for the end-to-end leg: the
+    ranks of one host (LOCAL_WORLD_SIZE) pin theirs at the same time, so together they may
+    take at most 60% of the host's available memory.  Every rank gets the same answer (a
+    max over ranks), so none waits in a collective that another one skipped.  Returns
+    (fits, reason)."""
+    on_node = int(os.environ.get("LOCAL_WORLD_SIZE", "1"))
+    if avail is None:
+        try:
+            avail = int(re.search(r"MemAvailable:\s+(\d+)",
+                                  open("/proc/meminfo").read()).group(1)) * 1024
+        except (OSError, AttributeError):
+            avail = 0
+    fits = not (avail and need * on_node > 0.6 * avail)
+    if max_over_ranks(0.0 if fits else 1.0, world, device=device) > 0.0:
+        return False, (f"pinned host gradients need {need * on_node / 1e9:.1f} GB on a host; "
+                       f"a rank's host has {avail / 1e9:.1f} GB available")
+    return True, ""
+
+
+def run_e2e(args, ctx, wl, grads, w, m, v, hp, t_step, dev, R, b_g, n, world=1):
     """The same step end to end through the C ABI's host-buffer call
     (repstep_step_from_host): every step copies the R gradients from pinned host memory --
     pipelined over chunk-aligned ranges and copy streams, each range reduced as it lands --
     and returns the pre-clip norm and the Merkle root in host memory.  The state (w, m, v)
-    stays resident on the device, as an optimizer's state does."""
+    stays resident on the device, as an optimizer's state does.  Under torchrun every rank
+    does the same on its own replica; the value is the job's (n x world over the slowest
+    rank's step time)."""
     need = R * b_g * n
-    try:
-        avail = int(re.search(r"MemAvailable:\s+(\d+)", open("/proc/meminfo").read()).group(1)) * 1024
-    except (OSError, AttributeError):
-        avail = 0
-    if avail and need > 0.6 * avail:
-        return {"value": None, "unit": UNIT, "skipped": f"pinned host gradients need {need / 1e9:.1f} GB, "
-                f"host has {avail / 1e9:.1f} GB available"}
+    fits, why = host_fits(need, world)
+    if not fits:
+        return {"value": None, "unit": UNIT, "skipped": why}
     host = [torch.empty(g.shape, dtype=g.dtype, pin_memory=True) for g in grads]
     for h, g in zip(host, grads):
         h.copy_(g)
@@ -637,10 +655,10 @@ def run_e2e(args, ctx, wl, grads, w, m, v, hp, t_step, dev, R, b_g, n):
         t1 = time.perf_counter()
         one()
         per_step.append((time.perf_counter() - t1) * 1e3)
-    dt = (time.perf_counter() - t0) / steps
+    dt = max_over_ranks((time.perf_counter() - t0) / steps, world)
     del host
     fl = min(floor)
-    return {"value": n / dt, "unit": UNIT, "ms_per_step": dt * 1e3, "steps": steps,
+    return {"value": n * world / dt, "unit": UNIT, "ms_per_step": dt * 1e3, "steps": steps,
             "h2d_bytes_per_step": need, "d2h_bytes_per_step": 4 + 8,
             "api": "repstep_step_from_host (C ABI, host gradient buffers, host norm and root)",
             "state": "w, m, v resident on the device",

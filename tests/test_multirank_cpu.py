@@ -49,3 +49,35 @@ def test_single_rank_value():
     import bench
     assert bench.job_value(1000, 1.0, 1) == pytest.approx(1e6)
     assert bench.max_over_ranks(3.0, 1) == 3.0
+
+
+def _fits_worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_WORLD_SIZE=str(world))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    import bench
+    need = 10 * 2 ** 30
+    # both ranks' hosts have room for both ranks' buffers: run
+    a = bench.host_fits(need, world, avail=100 * 2 ** 30, device="cpu")[0]
+    # rank 1's host cannot hold both: every rank skips the leg
+    b = bench.host_fits(need, world, avail=[100, 30][rank] * 2 ** 30, device="cpu")[0]
+    q.put((rank, a, b))
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_end_to_end_leg_is_skipped_on_every_rank_or_none():
+    """The end-to-end leg pins the gradients in host memory on every rank of a host at
+    once; the ranks agree on running it, so that none waits in a collective another one
+    skipped."""
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_fits_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    out = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert out == [(0, True, False), (1, True, False)]
