@@ -229,10 +229,10 @@ int repstep_clip(repstep_ctx *ctx, float clip, float *d_norm_out, float *d_scale
 
 /* Clipped AdamW over [begin, begin+count) of the full-length arrays w (param_dtype), m, v
  * (fp32), updated in place, using g and the scale from the last reduce/clip.  All three
- * pointers 16-byte aligned (and non-NULL unless the context's n is 0).  Also writes the PF61 leaf
- * digest of every new w, m and v chunk lying wholly inside the range; repstep_root()
- * completes the others.  All calls of one step must pass the same w, m, v base pointers.
- * Requires repstep_clip() since the last reduce (else REPSTEP_ERR_STATE). */
+ * pointers 16-byte aligned, and non-NULL unless the context's n is 0.  Also writes the
+ * PF61 leaf digest of every new w, m and v chunk lying wholly inside the range;
+ * repstep_root() completes the others.  All calls of one step must pass the same w, m, v
+ * base pointers.  Requires repstep_clip() since the last reduce (else REPSTEP_ERR_STATE). */
 int repstep_adamw(repstep_ctx *ctx, void *d_w, float *d_m, float *d_v,
                   const repstep_hparams *hp, uint64_t begin, uint64_t count);
 
@@ -385,8 +385,9 @@ int repstep_checkpoint_load(repstep_ctx *ctx, const char *path, int32_t *step_ou
 void repstep_bias_corrections(float beta1, float beta2, int32_t t, float *bc1, float *bc2);
 
 /* Synchronise the context's stream (and the pending root passes of the hash stream, if
- * any) and read the device flags (REPSTEP_FLAG_*; nullable output).  Returns REPSTEP_ERR_CUDA if the stream reported an error, REPSTEP_ERR_TIMEOUT
- * if a kernel's bounded wait expired, else REPSTEP_OK.  Clears the timeout flags. */
+ * any) and read the device flags (REPSTEP_FLAG_*; nullable output).  Returns
+ * REPSTEP_ERR_CUDA if the stream reported an error, REPSTEP_ERR_TIMEOUT if a kernel's
+ * bounded wait expired, else REPSTEP_OK.  Clears the timeout flags. */
 int repstep_sync(repstep_ctx *ctx, uint32_t *flags_out);
 
 /* Self-test of the fixed-divisor division inside the AdamW kernel.  The bias corrections
@@ -453,8 +454,8 @@ const char *repstep_strerror(int code);
  * loads device code lazily by default -- may load the library's device code and this array
  * onto the device, which does take device memory.  So make that first call at start-up,
  * before the device's memory is taken and before any stream capture; from then until the
- * process exits the array stays held and later calls allocate nothing.  Returns REPSTEP_OK, REPSTEP_ERR_ARG, REPSTEP_ERR_ALIGN,
- * REPSTEP_ERR_SIZE or REPSTEP_ERR_CUDA. */
+ * process exits the array stays held and later calls allocate nothing.  Returns
+ * REPSTEP_OK, REPSTEP_ERR_ARG, REPSTEP_ERR_ALIGN, REPSTEP_ERR_SIZE or REPSTEP_ERR_CUDA. */
 #define REPSTEP_NOALLOC_MAX_N (1ull << 30)
 int repstep_reduce_norm_noalloc(const void *const *d_grads, uint32_t R, int32_t grad_dtype,
                                 uint64_t n, float clip, float *d_g, float *d_norm_out,
