@@ -46,9 +46,11 @@ SPEC_HBM_GBS = 8000.0          # the HBM3e figure the metric's own percentage is
 _CSRC = "bitwise_reproducible_step_gb300/csrc/"
 # the sources each profiled kernel is built from: a traffic figure recorded under their
 # hash stays valid until one of them changes
-KERNEL_SOURCES = {k: [_CSRC + f for f in (src, "common.cuh", "kernels.h")]
-                  for k, src in (("k_reduce", "k_reduce.cuh"), ("k_adamw", "k_adamw.cuh"),
-                                 ("k_leaves_b2", "k_blake2b.cu"))}
+KERNEL_SOURCES = {k: [_CSRC + f for f in (*srcs, "common.cuh", "kernels.h")]
+                  for k, srcs in (("k_reduce", ("k_reduce.cuh",)),
+                                  ("k_adamw", ("k_adamw.cuh", "adamw_math.cuh")),
+                                  ("k_leaves_b2", ("k_blake2b.cu",)),
+                                  ("k_fused", ("k_fused.cu", "adamw_math.cuh")))}
 # BLAKE2b-64 leaves (audit mode) are bound by the SM's integer ALU pipe: per 128-byte block,
 # 12 rounds x 8 G functions x 22 32-bit operations (two 3-input and two 2-input 64-bit
 # additions at 2 each, four 64-bit XORs at 2, rotations by 24, 16 and 63 at 2 funnel shifts
@@ -300,10 +302,21 @@ def run_ours(args, rank, world, local):
     norms = torch.empty(max(args.steps, 1), dtype=torch.float32, device=dev)
     roots = torch.empty(max(args.steps, 1), dtype=torch.int64, device=dev)
 
+    # the single-pass step writes a second state buffer; the two alternate
+    fused_state = None
+    if args.fused:
+        fused_state = [(w, m, v), (torch.empty_like(w), torch.empty_like(m), torch.empty_like(v))]
+    cur = [0]
+
     def one_step(slot=None):
         t_step[0] += 1
         nr = norm if slot is None else norms[slot:slot + 1]
         rt = root if slot is None else roots[slot:slot + 1]
+        if fused_state is not None:
+            ctx.step_fused(grads, *fused_state[cur[0]], *fused_state[1 - cur[0]],
+                           hp(t_step[0]), step=t_step[0], norm_out=nr, root_out=rt)
+            cur[0] ^= 1
+            return
         if not args.paper_shard:
             ctx.step(grads, w, m, v, hp(t_step[0]), step=t_step[0], norm_out=nr, root_out=rt,
                      nodes=args.nodes)
@@ -397,6 +410,22 @@ def run_ours(args, rank, world, local):
         for i, k in enumerate(kt):
             kt[k].append(ev[i].elapsed_time(ev[i + 1]))
     kms = {k: statistics.mean(v_) for k, v_ in kt.items()}
+    if fused_state is not None:
+        # the whole single-pass call (the pass, the norm passes, the two second-pass kernels
+        # that return at once, and the root), back to back on one stream
+        fev = []
+        for _ in range(reps + 1):
+            t_step[0] += 1
+            e_a = torch.cuda.Event(enable_timing=True)
+            e_b = torch.cuda.Event(enable_timing=True)
+            e_a.record(stream)
+            ctx.step_fused(grads, *fused_state[cur[0]], *fused_state[1 - cur[0]],
+                           hp(t_step[0]), step=t_step[0], norm_out=norm, root_out=root)
+            cur[0] ^= 1
+            e_b.record(stream)
+            fev.append((e_a, e_b))
+        torch.cuda.synchronize(dev)
+        kms["fused_step"] = statistics.mean(a_.elapsed_time(b_) for a_, b_ in fev[1:])
     ctx.sync()
 
     # ---- checkpoint image emit (timed on its own; not part of the step's bytes) --------
@@ -418,10 +447,14 @@ def run_ours(args, rank, world, local):
     peak, peak_src = hbm_peak()
     mask_b = 0.125 if args.decay_mask else 0.0
     alg_step = int((R * b_g + 16 + 2 * b_w + mask_b) * n)
-    alg = {"reduce": (R * b_g + 4) * n, "adamw": int((20 + 2 * b_w + mask_b) * n)}
+    alg = {"reduce": (R * b_g + 4) * n, "adamw": int((20 + 2 * b_w + mask_b) * n),
+           "fused_step": int((R * b_g + 16 + 2 * b_w) * n)}
     dom = max(("reduce", "adamw", "leaves") if audit else ("reduce", "adamw"),
               key=lambda k: kms[k])
-    kname = {"reduce": "k_reduce", "adamw": "k_adamw", "leaves": "k_leaves_b2"}[dom]
+    if fused_state is not None and not audit:
+        dom = "fused_step"
+    kname = {"reduce": "k_reduce", "adamw": "k_adamw", "leaves": "k_leaves_b2",
+             "fused_step": "k_fused"}[dom]
     traffic = profiled_traffic(kname)
     if dom == "leaves":
         apeak, apeak_src = alu_peak(dev)
@@ -437,6 +470,10 @@ def run_ours(args, rank, world, local):
                     "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
                     "alg_bytes_per_launch": alg[dom], "avg_launch_ms": kms[dom],
                     "peak_source": peak_src}
+        if dom == "fused_step":
+            roofline["timed"] = ("the whole repstep_step_fused call: the single pass, the norm "
+                                 "passes, the two second-pass kernels (which return at once "
+                                 "when the step does not clip) and the root")
 
     # ---- end to end: grads from pinned host memory each step, norm+root read back ----
     ctx.set_hash_stream(hash_side)
@@ -468,6 +505,9 @@ def run_ours(args, rank, world, local):
                    "hash_leaves": args.hash_mode, "param_dtype": args.param_dtype,
                    "decay_mask": bool(args.decay_mask), "subnormals": args.subnormals,
                    "hash_stream": bool(args.hash_stream),
+                   "step": ("repstep_step_fused: one HBM pass when the step does not clip, "
+                            "two state buffers alternating" if args.fused else
+                            "repstep_step: reduce, then clip and AdamW (two HBM passes)"),
                    "reduce_order": (f"paper-exact, dp_shard {args.paper_shard}"
                                     + (f", accum {args.accum}" if args.accum else "")
                                     if args.paper_shard else
@@ -785,6 +825,9 @@ def main():
     ap.add_argument("--log", default="",
                     help="append a JSON-lines record per timed step (norm, its bits, root, "
                          "event time) and the summary line to this file")
+    ap.add_argument("--fused", action="store_true",
+                    help="time repstep_step_fused: one HBM pass from one state buffer into a "
+                         "second when the step does not clip (same bits)")
     ap.add_argument("--shard", action="store_true",
                     help="the sharded step: n split over the ranks' GPUs (all-to-all + "
                          "all-gathers); with one process, a one-rank NCCL group")

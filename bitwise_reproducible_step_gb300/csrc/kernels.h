@@ -26,6 +26,8 @@ struct ReduceArgs {
     uint32_t accum;           // paper-exact mode: 0 = one gradient per virtual rank; else
                               // microbatches per rank, accumulated from +0
     float rho3;               // fp32(1/accum)
+    int only_if_clipped;      // 1: return at once when sc->scale is 1 (the fallback pass of
+                              // a speculative step, repstep_step_fused)
 };
 
 struct ReduceShape {
@@ -54,7 +56,11 @@ cudaError_t launch_reduce(const ReduceShape &s, const ReduceArgs &args, int grid
 struct AdamwArgs {
     const float *g;           // MODE adamw: workspace g
     void *w;                  // parameters: fp32, or bf16 when the kernel's PT is 1
-    float *m, *v;             // Adam moments (fp32); updated in place in the AdamW modes
+    float *m, *v;             // Adam moments (fp32), read
+    void *wo;                 // where the AdamW modes write w', m', v': w, m, v themselves
+    float *mo, *vo;           // (in place), or a second state buffer (repstep_step_fused)
+    int only_if_clipped;      // 1: return at once when sc->scale is 1 (a speculative step's
+                              // second pass)
     uint64_t *leaves;         // workspace u64[1 + 3c]
     const uint64_t *powers;   // workspace K^1..K^4096 mod p
     Scalars *sc;              // device scalars (scale, flags)
@@ -83,6 +89,29 @@ cudaError_t launch_adamw(const AdamwShape &s, const AdamwArgs &args, int grid, s
 using AdamwKernelFn = void (*)(AdamwArgs);
 AdamwKernelFn pick_adamw_ieee(const AdamwShape &s);
 AdamwKernelFn pick_adamw_ftz(const AdamwShape &s);
+// The speculative single-pass step (k_fused.cu): replica reduce, chunk sums of squares,
+// AdamW with clip scale 1 from (w, m, v) into (wo, mo, vo), and the PF61 leaves of the new
+// state.  R is one full replica group (4 or 8).
+struct FusedArgs {
+    const void *grads[8];     // the R replica gradients, global replica order
+    float *chunk_sq;          // workspace fp32[c]
+    uint32_t R;
+    float rho;                // fp32(1/R)
+    AdamwArgs adam;           // state in and out, leaves, powers, scalars, n, c, constants,
+                              // ring depth and stage size
+};
+
+struct FusedShape {
+    int dtype;    // gradients: 0 fp32, 1 bf16
+    int rg;       // R: 4 or 8
+    int leaves;   // 1: PF61 leaves fused (hash mode PF61); 0: none (audit mode)
+};
+size_t fused_smem_bytes(const FusedShape &s, FusedArgs &args);
+cudaError_t fused_prepare(const FusedShape &s, size_t smem);
+cudaError_t fused_occupancy(const FusedShape &s, size_t smem, int *blocks_per_sm);
+cudaError_t launch_fused(const FusedShape &s, const FusedArgs &args, int grid, size_t smem,
+                         cudaStream_t st);
+
 cudaError_t launch_selftest_div(uint32_t b_begin, uint32_t b_count, unsigned long long *mismatches,
                                cudaStream_t st);
 cudaError_t launch_selftest_fast_math(int which, uint32_t begin, uint32_t count, uint64_t seed,

@@ -224,8 +224,11 @@ int check_hparams(const repstep_hparams *hp)
 // OPEN-1B Algorithm 1 with dp_replicate = nodes and dp_shard = gpn.
 // R replicas (virtual ranks) = nodes x gpn; with accum > 0 (paper mode only) `grads`
 // holds R * accum microbatch gradients, rank-major.
+// only_if_clipped: the second pass of a speculative step -- the kernel returns at once when
+// the clip scale is 1, and the call-order state is left as the caller set it.
 int do_reduce(repstep_ctx *x, const void *const *grads, uint32_t R, uint32_t nodes,
-              uint32_t gpn, uint64_t begin, uint64_t count, int paper = 0, uint32_t accum = 0)
+              uint32_t gpn, uint64_t begin, uint64_t count, int paper = 0, uint32_t accum = 0,
+              int only_if_clipped = 0)
 {
     if (!grads || R == 0) return REPSTEP_ERR_ARG;
     const uint64_t inputs = uint64_t(R) * (accum ? accum : 1);
@@ -238,12 +241,14 @@ int do_reduce(repstep_ctx *x, const void *const *grads, uint32_t R, uint32_t nod
         if (!grads[r]) return REPSTEP_ERR_ARG;
         if (!aligned(grads[r], 16)) return REPSTEP_ERR_ALIGN;
     }
-    if (x->scale_ready || x->updated) {   // a new step starts
-        x->scale_ready = false;
-        x->updated = 0;
-        x->cut_leaf.clear();
+    if (!only_if_clipped) {
+        if (x->scale_ready || x->updated) {   // a new step starts
+            x->scale_ready = false;
+            x->updated = 0;
+            x->cut_leaf.clear();
+        }
+        x->reduced += count;
     }
-    x->reduced += count;
     if (count == 0) return REPSTEP_OK;
 
     const uint64_t end = begin + count;
@@ -266,6 +271,7 @@ int do_reduce(repstep_ctx *x, const void *const *grads, uint32_t R, uint32_t nod
     a.rho2 = hflush(fz, paper ? one / float(gpn) : one);
     a.accum = paper ? accum : 0;
     a.rho3 = hflush(fz, accum ? one / float(accum) : one);
+    a.only_if_clipped = only_if_clipped;
     ReduceShape s{};
     s.nt = x->nt_reduce;
     s.dtype = x->cfg.grad_dtype;
@@ -283,7 +289,7 @@ int do_reduce(repstep_ctx *x, const void *const *grads, uint32_t R, uint32_t nod
     e = launch_reduce(s, a, grid, smem, x->stream);
     if (e != cudaSuccess) return x->cuda_fail(e);
     ++x->launches;
-    note_cut_chunks(x->cut_norm, begin, end, x->n);
+    if (!only_if_clipped) note_cut_chunks(x->cut_norm, begin, end, x->n);
     return REPSTEP_OK;
 }
 
@@ -365,21 +371,29 @@ void adamw_hparams(const repstep_ctx *x, const repstep_hparams *hp, AdamwArgs &a
                  a.eps <= eps_hi) ? 1 : 0;
 }
 
-int do_adamw(repstep_ctx *x, void *w, float *m, float *v, const repstep_hparams *hp,
-             uint64_t begin, uint64_t count)
+// AdamW over [begin, begin+count): reads w, m, v and writes w', m', v' to wo, mo, vo (the
+// same arrays for the in-place update).  only_if_clipped: the kernel returns at once when
+// the clip scale is 1 (a speculative step's second pass); the call-order state moves on
+// either way.
+int do_adamw_to(repstep_ctx *x, void *w, float *m, float *v, void *wo, float *mo, float *vo,
+                const repstep_hparams *hp, uint64_t begin, uint64_t count,
+                int only_if_clipped = 0)
 {
-    if (x->n > 0 && (!w || !m || !v)) return REPSTEP_ERR_ARG;   // n = 0 reads no array
-    if (!aligned(w, 16) || !aligned(m, 16) || !aligned(v, 16)) return REPSTEP_ERR_ALIGN;
+    if (x->n > 0 && (!w || !m || !v || !wo || !mo || !vo)) return REPSTEP_ERR_ARG;
+    if (!aligned(w, 16) || !aligned(m, 16) || !aligned(v, 16) || !aligned(wo, 16) ||
+        !aligned(mo, 16) || !aligned(vo, 16))
+        return REPSTEP_ERR_ALIGN;
     int rc = check_hparams(hp);
     if (rc) return rc;
     if (begin > x->n || count > x->n - begin) return REPSTEP_ERR_ARG;
     if (!x->scale_ready) return REPSTEP_ERR_STATE;
     rc = join_hash(x);      // the update rewrites the state and leaves a pending root reads
     if (rc) return rc;
-    if (x->sw && (x->sw != w || x->sm != m || x->sv != v)) return REPSTEP_ERR_ARG;
-    x->sw = w;
-    x->sm = m;
-    x->sv = v;
+    // the state the root hashes is the one written
+    if (x->sw && (x->sw != wo || x->sm != mo || x->sv != vo)) return REPSTEP_ERR_ARG;
+    x->sw = wo;
+    x->sm = mo;
+    x->sv = vo;
     x->updated += count;
     if (count == 0) return REPSTEP_OK;
     const uint64_t end = begin + count;
@@ -388,6 +402,10 @@ int do_adamw(repstep_ctx *x, void *w, float *m, float *v, const repstep_hparams 
     a.w = w;
     a.m = m;
     a.v = v;
+    a.wo = wo;
+    a.mo = mo;
+    a.vo = vo;
+    a.only_if_clipped = only_if_clipped;
     a.leaves = x->leaves();
     a.powers = x->powers();
     a.sc = x->sc();
@@ -416,6 +434,12 @@ int do_adamw(repstep_ctx *x, void *w, float *m, float *v, const repstep_hparams 
     ++x->launches;
     if (mode == 0) note_cut_chunks(x->cut_leaf, begin, end, x->n);
     return REPSTEP_OK;
+}
+
+int do_adamw(repstep_ctx *x, void *w, float *m, float *v, const repstep_hparams *hp,
+             uint64_t begin, uint64_t count)
+{
+    return do_adamw_to(x, w, m, v, w, m, v, hp, begin, count);
 }
 
 // Merkle root over the leaves.  In the PF61 mode the first Merkle pass computes the header
@@ -521,9 +545,9 @@ int hash_leaves(repstep_ctx *x, int32_t step, const void *w, const float *m, con
     if (x->cfg.hash_mode == REPSTEP_HASH_BLAKE2B) return audit_leaves(x, step, w, m, v, x->stream);
     if (x->n > 0) {
         AdamwArgs a{};
-        a.w = const_cast<void *>(w);
-        a.m = const_cast<float *>(m);
-        a.v = const_cast<float *>(v);
+        a.w = a.wo = const_cast<void *>(w);
+        a.m = a.mo = const_cast<float *>(m);
+        a.v = a.vo = const_cast<float *>(v);
         a.leaves = x->leaves();
         a.powers = x->powers();
         a.sc = x->sc();
@@ -757,6 +781,119 @@ int step_from_host(repstep_ctx *x, const void *const *h_grads, uint32_t R,
                             x->stream);
     if (e == cudaSuccess) e = cudaStreamSynchronize(x->stream);
     return e == cudaSuccess ? REPSTEP_OK : x->cuda_fail(e);
+}
+
+// Whether [a, a+na) and [b, b+nb) share a byte.
+bool overlaps(const void *a, uint64_t na, const void *b, uint64_t nb)
+{
+    const uintptr_t pa = reinterpret_cast<uintptr_t>(a), pb = reinterpret_cast<uintptr_t>(b);
+    return na && nb && pa < pb + nb && pb < pa + na;
+}
+
+// The speculative single-pass step (k_fused.cu) where its kernel covers the configuration:
+// R one full replica group of 4 or 8, fp32 parameters, IEEE arithmetic, no decay mask, the
+// default launch shape.  Elsewhere the same result comes from the ordinary passes, with
+// AdamW writing the second state buffer.
+bool fused_supported(const repstep_ctx *x, uint32_t R)
+{
+    return (R == 4 || R == 8) && x->cfg.param_dtype == REPSTEP_F32 && !x->fz() &&
+           !x->decay_mask && x->cfg.grid_blocks == 0 &&
+           (x->cfg.block_threads == 0 || x->cfg.block_threads == 512) && x->n > 0;
+}
+
+int step_fused(repstep_ctx *x, const void *const *grads, uint32_t R, const void *w,
+               const float *m, const float *v, void *wo, float *mo, float *vo,
+               const repstep_hparams *hp, int32_t step, float *norm_out, uint64_t *root_out)
+{
+    // validate everything before launching anything
+    if (!grads || R == 0) return REPSTEP_ERR_ARG;
+    if (R > uint32_t(kMaxReplicas)) return REPSTEP_ERR_SIZE;
+    if (x->n > 0 && (!w || !m || !v || !wo || !mo || !vo)) return REPSTEP_ERR_ARG;
+    if (!aligned(w, 16) || !aligned(m, 16) || !aligned(v, 16) || !aligned(wo, 16) ||
+        !aligned(mo, 16) || !aligned(vo, 16))
+        return REPSTEP_ERR_ALIGN;
+    for (uint32_t r = 0; r < R && x->n > 0; ++r) {
+        if (!grads[r]) return REPSTEP_ERR_ARG;
+        if (!aligned(grads[r], 16)) return REPSTEP_ERR_ALIGN;
+    }
+    // the input state must survive the first pass: no output may share a byte with it
+    const uint64_t wb = x->w_bytes(), fb = 4 * x->n;
+    const void *ins[3] = {w, m, v};
+    const uint64_t in_bytes[3] = {wb, fb, fb};
+    const void *outs[3] = {wo, mo, vo};
+    for (int i = 0; i < 3; ++i)
+        for (int j = 0; j < 3; ++j)
+            if (overlaps(ins[i], in_bytes[i], outs[j], in_bytes[j])) return REPSTEP_ERR_ARG;
+    int rc = check_hparams(hp);
+    if (rc) return rc;
+    if (!(hp->clip > 0.0f)) return REPSTEP_ERR_ARG;
+    if (norm_out && !aligned(norm_out, 4)) return REPSTEP_ERR_ALIGN;
+    if (root_out && !aligned(root_out, 8)) return REPSTEP_ERR_ALIGN;
+    void *w_in = const_cast<void *>(w);
+    float *m_in = const_cast<float *>(m), *v_in = const_cast<float *>(v);
+
+    if (!fused_supported(x, R)) {
+        x->reduced = 0;
+        x->cut_norm.clear();
+        rc = do_reduce(x, grads, R, 1, R, 0, x->n);
+        if (!rc) rc = do_clip(x, hp->clip, norm_out, nullptr);
+        if (!rc) rc = do_adamw_to(x, w_in, m_in, v_in, wo, mo, vo, hp, 0, x->n);
+        return rc ? rc : do_root(x, step, root_out);
+    }
+
+    rc = join_hash(x);      // the pass writes the leaves, which a pending root may still read
+    if (rc) return rc;
+    FusedArgs f{};
+    for (uint32_t r = 0; r < R; ++r) f.grads[r] = grads[r];
+    f.chunk_sq = x->chunk_sq();
+    f.R = R;
+    const float one = 1.0f;
+    f.rho = one / float(R);
+    AdamwArgs &a = f.adam;
+    a.w = w_in;
+    a.m = m_in;
+    a.v = v_in;
+    a.wo = wo;
+    a.mo = mo;
+    a.vo = vo;
+    a.leaves = x->leaves();
+    a.powers = x->powers();
+    a.sc = x->sc();
+    a.n = x->n;
+    a.c = x->c;
+    a.begin = 0;
+    a.end = x->n;
+    a.chunk_lo = 0;
+    a.chunk_hi = x->c;
+    adamw_hparams(x, hp, a);
+    const FusedShape shape{x->cfg.grad_dtype == REPSTEP_BF16 ? 1 : 0, int(R),
+                           x->cfg.hash_mode == REPSTEP_HASH_PF61 ? 1 : 0};
+    const size_t smem = fused_smem_bytes(shape, f);
+    cudaError_t e = fused_prepare(shape, smem);
+    if (e != cudaSuccess) return x->cuda_fail(e);
+    int bps = 1;
+    e = fused_occupancy(shape, smem, &bps);
+    if (e != cudaSuccess) return x->cuda_fail(e);
+    e = launch_fused(shape, f, grid_for(x, bps, x->c), smem, x->stream);
+    if (e != cudaSuccess) return x->cuda_fail(e);
+    ++x->launches;
+    // the global norm and the true clip scale from the chunk sums the pass wrote
+    rc = norm_passes(x, x->chunk_sq(), x->c, hflush(x->fz(), hp->clip), norm_out, nullptr);
+    if (rc) return rc;
+    // the step's call-order state from here on is that of a finished clip
+    x->reduced = 0;
+    x->cut_norm.clear();
+    x->scale_ready = true;
+    x->updated = 0;
+    x->cut_leaf.clear();
+    x->sw = x->sm = x->sv = nullptr;
+    // the second pass, run only when the scale is not 1: g from the gradients, then AdamW
+    // from the untouched input state into the output state, with its leaves
+    rc = do_reduce(x, grads, R, 1, R, 0, x->n, 0, 0, 1);
+    if (rc) return rc;
+    rc = do_adamw_to(x, w_in, m_in, v_in, wo, mo, vo, hp, 0, x->n, 1);
+    if (rc) return rc;
+    return do_root(x, step, root_out);
 }
 
 // Sharded steps.  The norm and clip scale from the chunk sums of every shard, gathered by
@@ -994,6 +1131,17 @@ int repstep_step_from_host(repstep_ctx *ctx, const void *const *h_grads, uint32_
     if (!ctx) return REPSTEP_ERR_ARG;
     return step_from_host(ctx, h_grads, R, d_staging, pieces, copy_streams, d_w, d_m, d_v, hp,
                           step, h_norm_out, h_root_out);
+}
+
+int repstep_step_fused(repstep_ctx *ctx, const void *const *d_grads, uint32_t R,
+                       const void *d_w, const float *d_m, const float *d_v, void *d_w_out,
+                       float *d_m_out, float *d_v_out, const repstep_hparams *hp, int32_t step,
+                       float *d_norm_out, uint64_t *d_root_out)
+{
+    const NvtxRange nvtx_("repstep_step_fused");
+    if (!ctx) return REPSTEP_ERR_ARG;
+    return step_fused(ctx, d_grads, R, d_w, d_m, d_v, d_w_out, d_m_out, d_v_out, hp, step,
+                      d_norm_out, d_root_out);
 }
 
 int repstep_clip_gathered(repstep_ctx *ctx, const float *d_chunk_sums, uint64_t c_total,

@@ -74,7 +74,7 @@ EXPORTS = [
     "repstep_checkpoint_load", "repstep_set_decay_mask", "repstep_decay_mask_from_segments",
     "repstep_reduce_paper_accum", "repstep_set_hash_stream", "repstep_wait_hash",
     "repstep_leaves", "repstep_selftest_fast_math", "repstep_step_from_host",
-    "repstep_clip_gathered",
+    "repstep_clip_gathered", "repstep_step_fused",
     "repstep_root_gathered",
 ]
 NOALLOC_MAX_N = 1 << 30
@@ -107,6 +107,8 @@ def lib():
     L.repstep_step.argtypes = [vp, C.POINTER(vp), u32, u32, u32, vp, vp, vp, C.POINTER(HParams),
                                i32, vp, vp]
     L.repstep_clip_gathered.argtypes = [vp, vp, u64, C.c_float, vp, vp]
+    L.repstep_step_fused.argtypes = [vp, C.POINTER(vp), u32, vp, vp, vp, vp, vp, vp,
+                                     C.POINTER(HParams), i32, vp, vp]
     L.repstep_root_gathered.argtypes = [vp, i32, u64, vp, vp]
     L.repstep_step_from_host.argtypes = [vp, C.POINTER(vp), u32, C.POINTER(vp), u32, u32, vp, vp,
                                          vp, C.POINTER(HParams), i32, vp, vp]
@@ -431,6 +433,20 @@ class Repstep:
         _check(lib().repstep_step(self._ctx, arr, R, nodes, gpn, _ptr(w), _ptr(m), _ptr(v),
                                   C.byref(hp), int(step), self._out(norm_out, torch.float32),
                                   self._out(root_out, torch.int64)), "step")
+
+    def step_fused(self, grads, w, m, v, w_out, m_out, v_out, hp: HParams, step: int,
+                   norm_out=None, root_out=None):
+        """One step from (w, m, v) into (w_out, m_out, v_out), in a single HBM pass when it
+        does not clip (repstep_step_fused); the inputs are left untouched and the bits
+        equal step()'s.  Alternate the two state buffers from step to step."""
+        arr, R = self._grads(grads)
+        self._state(w, m, v)
+        self._state(w_out, m_out, v_out)
+        self._bind()
+        _check(lib().repstep_step_fused(self._ctx, arr, R, _ptr(w), _ptr(m), _ptr(v),
+                                        _ptr(w_out), _ptr(m_out), _ptr(v_out), C.byref(hp),
+                                        int(step), self._out(norm_out, torch.float32),
+                                        self._out(root_out, torch.int64)), "step_fused")
 
     def step_from_host(self, host_grads, staging, w, m, v, hp: HParams, step: int,
                        pieces: int = 8, copy_streams: int = 2):

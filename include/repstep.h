@@ -315,6 +315,29 @@ int repstep_step(repstep_ctx *ctx, const void *const *d_grads, uint32_t R, uint3
                  const repstep_hparams *hp, int32_t step, float *d_norm_out,
                  uint64_t *d_root_out);
 
+/* One whole step in a single HBM pass when it does not clip, from the state (d_w, d_m, d_v)
+ * into a second state buffer (d_w_out, d_m_out, d_v_out); the inputs are left untouched
+ * (d_w and d_w_out of param_dtype, the others fp32; all 16-byte aligned, and no output may
+ * share a byte with an input -- REPSTEP_ERR_ARG).  A caller alternates the two buffers
+ * from step to step.
+ * - The pass reduces the R gradients, forms the chunk sums of squares, applies AdamW with
+ *   the clip scale taken as 1 and writes the new state and its PF61 leaves, reading the
+ *   gradients and the state once and never writing g.  Then the norm passes compute the
+ *   true scale.  Whenever the pre-clip norm does not exceed the clip threshold the scale
+ *   is exactly 1 and those bits are the step's ("OPEN-1B: A Fully Auditable Training
+ *   Run", §3.2: clipping to a global norm); otherwise the reduce and AdamW run again from
+ *   the untouched inputs and overwrite the outputs.  The result is bit for bit
+ *   repstep_step's on the same inputs either way; only the time differs (one pass over
+ *   R*b_g + 24 bytes per parameter without clipping, about twice that with).
+ * - The single pass covers R = 4 or 8, fp32 parameters, IEEE arithmetic, no decay mask and
+ *   the default launch shape; any other configuration runs the two passes of
+ *   repstep_step, writing the output buffers.
+ * - `step`, hp, d_norm_out and d_root_out as repstep_step; the root is the output state's. */
+int repstep_step_fused(repstep_ctx *ctx, const void *const *d_grads, uint32_t R,
+                       const void *d_w, const float *d_m, const float *d_v, void *d_w_out,
+                       float *d_m_out, float *d_v_out, const repstep_hparams *hp, int32_t step,
+                       float *d_norm_out, uint64_t *d_root_out);
+
 /* One whole step whose R replica gradients start in HOST memory, with the norm and the
  * root returned to host memory: the end-to-end form of repstep_step for a caller whose
  * gradients arrive on the host side ("OPEN-1B: A Fully Auditable Training Run", §5: the

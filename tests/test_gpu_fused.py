@@ -1,0 +1,183 @@
+"""repstep_step_fused through the C ABI: the single-pass step (reduce, chunk sums, AdamW with
+the clip scale taken as 1 into a second state buffer, PF61 leaves) with its second pass when
+the step clips.  Every output bit -- the new w, m, v, the pre-clip norm, the root and the
+leaves -- must equal repstep_step's on the same inputs, step after step with the two state
+buffers alternating, whether or not the step clips; the input state must be left untouched.
+Configurations the single pass does not cover (other R, bf16 parameters, flush-to-zero, a
+decay mask) take the two ordinary passes into the output buffers, with the same bits."""
+import ctypes as C
+
+import numpy as np
+import pytest
+import torch
+
+from bitwise_reproducible_step_gb300 import inputs as I
+from bitwise_reproducible_step_gb300 import repstep as rs
+from tests import gpu_util as U
+
+pytestmark = pytest.mark.gpu
+
+CH = 4096
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    U.ensure_built()
+    torch.cuda.set_device(0)
+
+
+def run_pair(n, R, gdt=torch.float32, steps=4, clip_steps=(2,), ctx_kw=None, hash_stream=False,
+             mask_segs=None):
+    """Steps of repstep_step (in place) and of repstep_step_fused (alternating buffers) on the
+    same gradients; steps in clip_steps get gradients large enough to clip."""
+    dev = torch.device("cuda", 0)
+    ctx_kw = dict(ctx_kw or {})
+    a = rs.Repstep(n, grad_dtype=gdt, device=dev, **ctx_kw)
+    b = rs.Repstep(n, grad_dtype=gdt, device=dev, **ctx_kw)
+    if hash_stream:
+        a.set_hash_stream(torch.cuda.Stream(dev))
+        b.set_hash_stream(torch.cuda.Stream(dev))
+    if mask_segs:
+        mask = rs.decay_mask_from_segments(n, mask_segs).to(dev)
+        a.set_decay_mask(mask)
+        b.set_decay_mask(mask)
+    pdt = ctx_kw.get("param_dtype", torch.float32)
+    w, m, v = I.gen_state(U.F32_WL, n=n, device=dev)
+    m.copy_(I.gen_grad(U.F32_WL, 9, 0, n=n, device=dev))           # mid-run moments
+    v.copy_(I.gen_grad(U.F32_WL, 9, 1, n=n, device=dev).square())
+    w = w.to(pdt)
+    bufs = [(w.clone(), m.clone(), v.clone()),
+            (torch.full_like(w, float("nan")), torch.full_like(m, float("nan")),
+             torch.full_like(v, float("nan")))]
+    nr = torch.empty(2, dtype=torch.float32, device=dev)
+    rr = torch.empty(2, dtype=torch.int64, device=dev)
+    clipped = 0
+    for t in range(1, steps + 1):
+        scale = 3000.0 if t in clip_steps else 1e-3
+        grads = U.gen_grads(n, R, 60 + t, gdt, scale=scale)
+        hp = U.hp_for(t)
+        a.step(grads, w, m, v, hp, step=t, norm_out=nr[0:1], root_out=rr[0:1])
+        src, dst = bufs[(t - 1) % 2], bufs[t % 2]
+        before = [x.clone() for x in src]
+        b.step_fused(grads, *src, *dst, hp, step=t, norm_out=nr[1:2], root_out=rr[1:2])
+        assert a.sync() & ~rs.FLAG_NONFINITE_NORM == 0
+        assert b.sync() & ~rs.FLAG_NONFINITE_NORM == 0
+        for x, y in zip(before, src):                         # the inputs are untouched
+            assert torch.equal(x.view(torch.int16 if x.dtype == torch.bfloat16 else torch.int32),
+                               y.view(torch.int16 if y.dtype == torch.bfloat16 else torch.int32))
+        nb = nr.cpu().numpy().view(np.uint32)
+        assert nb[0] == nb[1], (t, nr)
+        rh = rr.cpu().numpy().view(np.uint64)
+        assert rh[0] == rh[1], t
+        for x, y, what in zip((w, m, v), dst, "wmv"):
+            xi = x.view(torch.int16 if x.dtype == torch.bfloat16 else torch.int32)
+            yi = y.view(torch.int16 if y.dtype == torch.bfloat16 else torch.int32)
+            assert torch.equal(xi, yi), (what, t)
+        assert torch.equal(a.leaves_view(), b.leaves_view()), t
+        clipped += float(nr[0].item()) > 1.0
+    return clipped
+
+
+@pytest.mark.parametrize("n,R,gdt", [
+    (5 * CH * 3 + 77, 8, torch.float32),
+    (5 * CH * 3 + 77, 4, torch.float32),
+    (300_001, 8, torch.bfloat16),
+    (2 * CH + 2049, 4, torch.bfloat16),       # the last chunk's second tile is partial
+    (1000, 8, torch.float32),                 # one short chunk: its second tile is empty
+    (1, 4, torch.float32),
+    (64 * CH, 8, torch.float32),
+])
+def test_fused_equals_two_pass_step(n, R, gdt):
+    clipped = run_pair(n, R, gdt)
+    assert clipped >= 1 or n == 1              # the clipping step took the second pass
+
+
+def test_fused_audit_mode_and_hash_stream():
+    run_pair(5 * CH * 3 + 77, 8, ctx_kw=dict(hash_mode=rs.HASH_BLAKE2B), hash_stream=True)
+    run_pair(5 * CH * 3 + 77, 4, torch.bfloat16, hash_stream=True)
+
+
+@pytest.mark.parametrize("kw,R", [
+    (dict(), 3),                                               # R not 4 or 8
+    (dict(param_dtype=torch.bfloat16), 8),
+    (dict(subnormals=rs.SUBNORMALS_FTZ), 8),
+    (dict(block_threads=256), 8),
+])
+def test_configurations_outside_the_single_pass(kw, R):
+    run_pair(3 * CH + 5, R, ctx_kw=kw)
+
+
+def test_decay_mask_takes_the_two_passes():
+    run_pair(3 * CH + 5, 8, mask_segs=[(0, False), (CH + 3, True)])
+
+
+def test_fused_matches_the_oracle():
+    n, R = 2 * CH + 333, 8
+    dev = torch.device("cuda", 0)
+    ctx = rs.Repstep(n, device=dev)
+    w, m, v = I.gen_state(U.F32_WL, n=n, device=dev)
+    ow, om, ov = (x.cpu().numpy() for x in (w, m, v))
+    bufs = [(w, m, v), (torch.empty_like(w), torch.empty_like(m), torch.empty_like(v))]
+    nr = torch.empty(1, dtype=torch.float32, device=dev)
+    rr = torch.empty(1, dtype=torch.int64, device=dev)
+    for t in (1, 2, 3):
+        grads = U.gen_grads(n, R, 70 + t, scale=3000.0 if t == 2 else 1.0)
+        ctx.step_fused(grads, *bufs[(t - 1) % 2], *bufs[t % 2], U.hp_for(t), step=t,
+                       norm_out=nr, root_out=rr)
+        ctx.sync()
+        ref = U.oracle_step(U.oracle_grads(grads), ow, om, ov, t)
+        ow, om, ov = ref["w"], ref["m"], ref["v"]
+        for got, want, what in zip(bufs[t % 2], (ow, om, ov), "wmv"):
+            U.assert_same_f32(got, want, f"{what} step {t}")
+        assert np.float32(nr.item()) == ref["norm"] and U.root_of(rr) == ref["root"]
+
+
+def test_fused_rejects_overlapping_buffers():
+    n, R = CH, 4
+    dev = torch.device("cuda", 0)
+    ctx = rs.Repstep(n, device=dev)
+    w, m, v = I.gen_state(U.F32_WL, n=n, device=dev)
+    grads = U.gen_grads(n, R, 1)
+    hp = U.hp_for(1)
+    big = torch.zeros(2 * n, device=dev)
+    with pytest.raises(rs.RepstepError):
+        ctx.step_fused(grads, w, m, v, w, torch.empty_like(m), torch.empty_like(v), hp, 1)
+    with pytest.raises(rs.RepstepError):             # partial overlap
+        ctx.step_fused(grads, big[:n], m, v, big[n // 2:n // 2 + n], torch.empty_like(m),
+                       torch.empty_like(v), hp, 1)
+    L = rs.lib()
+    arr = (C.c_void_p * R)(*[g.data_ptr() for g in grads])
+    rc = L.repstep_step_fused(ctx._ctx, arr, R, C.c_void_p(w.data_ptr() + 4), None, None, None,
+                              None, None, C.byref(hp), 1, None, None)
+    assert rc in (1, 2)
+    assert ctx.sync() == 0
+
+
+@pytest.mark.big
+def test_flat1200m_r8_fused_equals_two_pass():
+    """The benchmark workload, 3 steps: the single pass every step (no clipping), equal to
+    repstep_step bit for bit, and the input state untouched."""
+    wl = I.WORKLOADS["flat1200m_r8_segscale"]
+    n, R = wl.n, wl.R
+    dev = torch.device("cuda", 0)
+    a, b = rs.Repstep(n, device=dev), rs.Repstep(n, device=dev)
+    w, m, v = I.gen_state(wl, device=dev)
+    bufs = [(w.clone(), m.clone(), v.clone()),
+            (torch.empty_like(w), torch.empty_like(m), torch.empty_like(v))]
+    grads = [torch.empty(n, device=dev) for _ in range(R)]
+    nr = torch.empty(2, dtype=torch.float32, device=dev)
+    rr = torch.empty(2, dtype=torch.int64, device=dev)
+    for t in (1, 2, 3):
+        for r in range(R):
+            I.gen_grad(wl, t, r, device=dev, out=grads[r])
+        hp = U.hp_for(t)
+        a.step(grads, w, m, v, hp, step=t, norm_out=nr[0:1], root_out=rr[0:1])
+        b.step_fused(grads, *bufs[(t - 1) % 2], *bufs[t % 2], hp, step=t, norm_out=nr[1:2],
+                     root_out=rr[1:2])
+        a.sync()
+        b.sync()
+        assert nr[0].item() == nr[1].item() < 1.0
+        rh = rr.cpu().numpy().view(np.uint64)
+        assert rh[0] == rh[1]
+        for x, y in zip((w, m, v), bufs[t % 2]):
+            assert torch.equal(x.view(torch.int32), y.view(torch.int32))
