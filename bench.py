@@ -2,7 +2,10 @@
 """Benchmark of the bitwise-reproducible optimizer step on GB300.
 
 One step = replica reduce (R gradient buffers, canonical tree, reciprocal multiply) +
-global norm + clip + fused AdamW + Merkle state hash, through the C ABI.  Default workload:
+global norm + clip + fused AdamW + Merkle state hash, through the C ABI: by default
+repstep_step_fused, one HBM pass from one state buffer into a second whenever the step
+does not clip (the benchmark workload never does), else a second pass -- the same bits as
+repstep_step, which --two-pass times instead.  Default workload:
 n = 1,200,000,000 fp32 parameters, R = 8 fp32 replica gradients N(0, 1e-4) with per-4M-
 segment log-uniform scales, hyperparameters lr 3e-4, betas 0.9/0.999, eps 1e-8, wd 0.1,
 clip 1.0.  Inputs are synthetic (seeded) and resident in HBM for the device-timed value;
@@ -825,15 +828,19 @@ def main():
     ap.add_argument("--log", default="",
                     help="append a JSON-lines record per timed step (norm, its bits, root, "
                          "event time) and the summary line to this file")
-    ap.add_argument("--fused", action="store_true",
-                    help="time repstep_step_fused: one HBM pass from one state buffer into a "
-                         "second when the step does not clip (same bits)")
+    ap.add_argument("--two-pass", action="store_true",
+                    help="time repstep_step (reduce, then clip and AdamW in place) instead of "
+                         "the default repstep_step_fused (one HBM pass from one state buffer "
+                         "into a second when the step does not clip; the same bits)")
     ap.add_argument("--shard", action="store_true",
                     help="the sharded step: n split over the ranks' GPUs (all-to-all + "
                          "all-gathers); with one process, a one-rank NCCL group")
     ap.add_argument("--n", type=int, default=0,
                     help="override the workload's parameter count (small profiling cases)")
     args = ap.parse_args()
+    # the single pass covers the canonical tree; the paper-exact and staged orders run the
+    # two passes
+    args.fused = not args.two_pass and not args.paper_shard and args.nodes == 1
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
 
