@@ -12,9 +12,10 @@
 // scale from the chunk sums.  The scale is exactly 1 whenever norm <= clip (and for a
 // non-finite norm), and then every bit written here is the step's: gc = g * 1 is the
 // same operation with the same operands as the two-pass step's gc = g * scale.  When the
-// scale is not 1, the reduce and AdamW kernels run again (flag only_if_clipped) from the
-// untouched (w, m, v) and overwrite (wo, mo, vo) and the leaves; otherwise they return at
-// once.
+// scale is not 1, the reduce and AdamW kernels run again (gates kGateRedo, kGateUpdate)
+// from the untouched (w, m, v) and overwrite (wo, mo, vo) and the leaves; otherwise they
+// return at once.  The pass itself runs only when the context's latest clip did not clip
+// (gate kGateSpeculate); after one that did, the step takes the two passes directly.
 //
 // The arithmetic is the two-pass kernels' own, element for element: the same
 // element-to-thread mapping as k_reduce (a thread holds 4 consecutive elements of each
@@ -115,6 +116,7 @@ __global__ void __launch_bounds__(NT + 64, 1) k_fused(const __grid_constant__ Fu
     static_assert(GS * NGS == RG, "gradient stages hold whole groups");
     static_assert(TPC * TE == kChunk && TPC * 4 <= 32, "tiles divide the chunk; limb bound");
     const AdamwArgs &A = F.adam;
+    if (!gate_open(F.gate, A.sc)) return;     // the step takes the two passes
 
     extern __shared__ __align__(1024) unsigned char smem[];
     const uint32_t S = A.stages;
@@ -491,16 +493,19 @@ cudaError_t fused_occupancy(const FusedShape &s, size_t smem, int *blocks_per_sm
 }
 
 cudaError_t launch_fused(const FusedShape &s, const FusedArgs &args, int grid, size_t smem,
-                         cudaStream_t st)
+                         cudaStream_t st, cudaEvent_t ev_begin, cudaEvent_t ev_end)
 {
     FusedKernelFn f = pick_fused(s);
     if (!f) return cudaErrorInvalidValue;
     // the kernel hands out chunks from this counter
     cudaError_t e = cudaMemsetAsync(&args.adam.sc->next_chunk, 0, sizeof(uint32_t), st);
+    if (e == cudaSuccess && ev_begin) e = cudaEventRecord(ev_begin, st);
     if (e != cudaSuccess) return e;
     void *params[] = {const_cast<FusedArgs *>(&args)};
-    return cudaLaunchKernel(reinterpret_cast<const void *>(f), dim3(grid), dim3(kFusedNT + 64),
-                            params, smem, st);
+    e = cudaLaunchKernel(reinterpret_cast<const void *>(f), dim3(grid), dim3(kFusedNT + 64),
+                         params, smem, st);
+    if (e == cudaSuccess && ev_end) e = cudaEventRecord(ev_end, st);
+    return e;
 }
 
 }  // namespace repstep

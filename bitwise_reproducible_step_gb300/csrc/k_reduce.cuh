@@ -229,8 +229,8 @@ __global__ void __launch_bounds__(NT + 32, 1) k_reduce(const __grid_constant__ R
     constexpr bool DYN = DT == 0;
     static_assert(16 * kMaxStages + 2 * TPC * W * 4 + 8 + 8 * kMaxStages <= kRingOffset,
                   "smem header");
-    // the second pass of a speculative step: nothing to do when the clip scale is 1
-    if (A.only_if_clipped && __float_as_uint(A.sc->scale) == 0x3F800000u) return;
+    // a launch of the single-pass step that this step does not need returns at once
+    if (!gate_open(A.gate, A.sc)) return;
 
     extern __shared__ __align__(1024) unsigned char smem[];
     const uint32_t S = A.stages;

@@ -136,6 +136,7 @@ __global__ void __launch_bounds__(256) k_norm(const float *in, uint64_t count, f
     const bool finite = isfinite(norm);
     sc->norm = norm;
     sc->scale = scale;
+    sc->clip_hist = ((sc->clip_hist & 1u) << 1) | (__float_as_uint(scale) != 0x3F800000u ? 1u : 0u);
     sc->flags = (sc->flags & ~kFlagNonfinite) | (finite ? 0u : kFlagNonfinite);
     if (norm_out) *norm_out = norm;
     if (scale_out) *scale_out = scale;

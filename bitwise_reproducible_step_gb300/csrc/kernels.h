@@ -26,8 +26,7 @@ struct ReduceArgs {
     uint32_t accum;           // paper-exact mode: 0 = one gradient per virtual rank; else
                               // microbatches per rank, accumulated from +0
     float rho3;               // fp32(1/accum)
-    int only_if_clipped;      // 1: return at once when sc->scale is 1 (the fallback pass of
-                              // a speculative step, repstep_step_fused)
+    int gate;                 // kGate*: whether the launch runs (repstep_step_fused)
 };
 
 struct ReduceShape {
@@ -59,8 +58,7 @@ struct AdamwArgs {
     float *m, *v;             // Adam moments (fp32), read
     void *wo;                 // where the AdamW modes write w', m', v': w, m, v themselves
     float *mo, *vo;           // (in place), or a second state buffer (repstep_step_fused)
-    int only_if_clipped;      // 1: return at once when sc->scale is 1 (a speculative step's
-                              // second pass)
+    int gate;                 // kGate*: whether the launch runs (repstep_step_fused)
     uint64_t *leaves;         // workspace u64[1 + 3c]
     const uint64_t *powers;   // workspace K^1..K^4096 mod p
     Scalars *sc;              // device scalars (scale, flags)
@@ -97,6 +95,7 @@ struct FusedArgs {
     float *chunk_sq;          // workspace fp32[c]
     uint32_t R;
     float rho;                // fp32(1/R)
+    int gate;                 // kGateSpeculate
     AdamwArgs adam;           // state in and out, leaves, powers, scalars, n, c, constants,
                               // ring depth and stage size
 };
@@ -109,8 +108,10 @@ struct FusedShape {
 size_t fused_smem_bytes(const FusedShape &s, FusedArgs &args);
 cudaError_t fused_prepare(const FusedShape &s, size_t smem);
 cudaError_t fused_occupancy(const FusedShape &s, size_t smem, int *blocks_per_sm);
+// ev_begin / ev_end (both or neither): recorded on st just before and after the kernel
 cudaError_t launch_fused(const FusedShape &s, const FusedArgs &args, int grid, size_t smem,
-                         cudaStream_t st);
+                         cudaStream_t st, cudaEvent_t ev_begin = nullptr,
+                         cudaEvent_t ev_end = nullptr);
 
 cudaError_t launch_selftest_div(uint32_t b_begin, uint32_t b_count, unsigned long long *mismatches,
                                cudaStream_t st);

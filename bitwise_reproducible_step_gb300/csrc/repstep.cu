@@ -31,7 +31,7 @@ constexpr uint32_t kMaxCopyStreams = 8;   // repstep_step_from_host: copy stream
 constexpr uint32_t kMaxPieces = 64;        // ... and pipelined ranges
 
 struct Layout {
-    uint64_t g, chunk_sq, norm_part, leaves, merkle_part, powers, scalars, total;
+    uint64_t g, chunk_sq, norm_part, leaves, merkle_part, leaf_snap, powers, scalars, total;
 };
 
 // An NVTX range over one public call, for timeline tools (a no-op when none is attached).
@@ -69,17 +69,18 @@ Layout layout_of(uint64_t n)
     // passes over all shards' chunk sums and leaves (about 26 KB in all).
     const uint64_t c_max = ((uint64_t(1) << 32) - 1 + kChunk - 1) / kChunk;
     const uint64_t nb2 = (c_max + kChunk - 1) / kChunk;
-    const uint64_t L = 1 + 3 * c_max;
+    const uint64_t L_max = 1 + 3 * c_max;
     // Merkle partials, ping-pong: the first pass's block roots, then the second pass's
-    const uint64_t mb1 = (L + kMerkleBlock - 1) / kMerkleBlock;
+    const uint64_t mb1 = (L_max + kMerkleBlock - 1) / kMerkleBlock;
     const uint64_t mb2 = (mb1 + kMerkleBlock - 1) / kMerkleBlock;
     Layout l{};
     uint64_t off = 0;
     l.g = off;           off = align_up(off + 4 * (n ? n : 1));
     l.chunk_sq = off;    off = align_up(off + 4 * (c ? c : 1));
     l.norm_part = off;   off = align_up(off + 4 * nb2);
-    l.leaves = off;      off = align_up(off + 8 * L);
+    l.leaves = off;      off = align_up(off + 8 * (1 + 3 * c));
     l.merkle_part = off; off = align_up(off + 8 * (mb1 + mb2));
+    l.leaf_snap = off;   off = align_up(off + 8 * (1 + 3 * c));
     l.powers = off;      off = align_up(off + 8 * kChunk);
     l.scalars = off;     off = align_up(off + sizeof(Scalars));
     l.total = off;
@@ -138,7 +139,12 @@ struct repstep_ctx {
     // the state they read, ev_hash their end, which later writers of that state wait for
     cudaStream_t hash_stream = nullptr;
     cudaEvent_t ev_state = nullptr, ev_hash = nullptr;
+    // caller's events recorded around the single pass (repstep_set_pass_events)
+    cudaEvent_t pass_ev[2] = {nullptr, nullptr};
     bool hash_pending = false;
+    // the pending root passes read the leaves or the state (the audit mode); otherwise
+    // they read only the leaf snapshot and the Merkle partials
+    bool hash_reads_live = false;
     std::vector<uint64_t> cut_norm, cut_leaf;   // chunks cut by range boundaries
 
     // repstep_step_from_host: copy streams and events, created on first use (host resources
@@ -154,6 +160,8 @@ struct repstep_ctx {
     float *norm_part() const { return reinterpret_cast<float *>(ws + lay.norm_part); }
     uint64_t *leaves() const { return reinterpret_cast<uint64_t *>(ws + lay.leaves); }
     uint64_t *merkle_part() const { return reinterpret_cast<uint64_t *>(ws + lay.merkle_part); }
+    // the leaves the Merkle passes read on the hash stream in the PF61 mode (repstep_root)
+    uint64_t *leaf_snap() const { return reinterpret_cast<uint64_t *>(ws + lay.leaf_snap); }
     uint64_t *powers() const { return reinterpret_cast<uint64_t *>(ws + lay.powers); }
     Scalars *sc() const { return reinterpret_cast<Scalars *>(ws + lay.scalars); }
     int w_bf16() const { return cfg.param_dtype == REPSTEP_BF16 ? 1 : 0; }
@@ -170,7 +178,8 @@ struct repstep_ctx {
 namespace {
 
 // Order the context's stream after a root still running on the hash stream: called before
-// anything that writes the leaves, the Merkle partials or the state the root passes read.
+// anything that writes the leaves, the leaf snapshot, the Merkle partials or the state the
+// root passes read.
 int join_hash(repstep_ctx *x)
 {
     if (!x->hash_pending) return REPSTEP_OK;
@@ -178,6 +187,14 @@ int join_hash(repstep_ctx *x)
     if (e != cudaSuccess) return x->cuda_fail(e);
     x->hash_pending = false;
     return REPSTEP_OK;
+}
+
+// Before an update writes the state and the leaves: only a pending root that reads them
+// (the audit mode) must end first.  A PF61 root reads the leaf snapshot its call took,
+// so the next update runs beside it.
+int join_hash_for_update(repstep_ctx *x)
+{
+    return x->hash_reads_live ? join_hash(x) : REPSTEP_OK;
 }
 
 // Persistent grid: SM count x resident CTAs, never more CTAs than chunks to process.
@@ -224,11 +241,11 @@ int check_hparams(const repstep_hparams *hp)
 // OPEN-1B Algorithm 1 with dp_replicate = nodes and dp_shard = gpn.
 // R replicas (virtual ranks) = nodes x gpn; with accum > 0 (paper mode only) `grads`
 // holds R * accum microbatch gradients, rank-major.
-// only_if_clipped: the second pass of a speculative step -- the kernel returns at once when
-// the clip scale is 1, and the call-order state is left as the caller set it.
+// gate: a gated launch of the single-pass step (kGate*), which runs or returns at once by
+// the clip history on the device; the call-order state is left as the caller set it.
 int do_reduce(repstep_ctx *x, const void *const *grads, uint32_t R, uint32_t nodes,
               uint32_t gpn, uint64_t begin, uint64_t count, int paper = 0, uint32_t accum = 0,
-              int only_if_clipped = 0)
+              int gate = kGateAlways)
 {
     if (!grads || R == 0) return REPSTEP_ERR_ARG;
     const uint64_t inputs = uint64_t(R) * (accum ? accum : 1);
@@ -241,7 +258,7 @@ int do_reduce(repstep_ctx *x, const void *const *grads, uint32_t R, uint32_t nod
         if (!grads[r]) return REPSTEP_ERR_ARG;
         if (!aligned(grads[r], 16)) return REPSTEP_ERR_ALIGN;
     }
-    if (!only_if_clipped) {
+    if (gate == kGateAlways) {
         if (x->scale_ready || x->updated) {   // a new step starts
             x->scale_ready = false;
             x->updated = 0;
@@ -271,7 +288,7 @@ int do_reduce(repstep_ctx *x, const void *const *grads, uint32_t R, uint32_t nod
     a.rho2 = hflush(fz, paper ? one / float(gpn) : one);
     a.accum = paper ? accum : 0;
     a.rho3 = hflush(fz, accum ? one / float(accum) : one);
-    a.only_if_clipped = only_if_clipped;
+    a.gate = gate;
     ReduceShape s{};
     s.nt = x->nt_reduce;
     s.dtype = x->cfg.grad_dtype;
@@ -289,7 +306,7 @@ int do_reduce(repstep_ctx *x, const void *const *grads, uint32_t R, uint32_t nod
     e = launch_reduce(s, a, grid, smem, x->stream);
     if (e != cudaSuccess) return x->cuda_fail(e);
     ++x->launches;
-    if (!only_if_clipped) note_cut_chunks(x->cut_norm, begin, end, x->n);
+    if (gate == kGateAlways) note_cut_chunks(x->cut_norm, begin, end, x->n);
     return REPSTEP_OK;
 }
 
@@ -372,12 +389,12 @@ void adamw_hparams(const repstep_ctx *x, const repstep_hparams *hp, AdamwArgs &a
 }
 
 // AdamW over [begin, begin+count): reads w, m, v and writes w', m', v' to wo, mo, vo (the
-// same arrays for the in-place update).  only_if_clipped: the kernel returns at once when
-// the clip scale is 1 (a speculative step's second pass); the call-order state moves on
-// either way.
+// same arrays for the in-place update).  gate: kGateUpdate in the single-pass step, where
+// the kernel returns at once when the pass already wrote the update; the call-order state
+// moves on either way.
 int do_adamw_to(repstep_ctx *x, void *w, float *m, float *v, void *wo, float *mo, float *vo,
                 const repstep_hparams *hp, uint64_t begin, uint64_t count,
-                int only_if_clipped = 0)
+                int gate = kGateAlways)
 {
     if (x->n > 0 && (!w || !m || !v || !wo || !mo || !vo)) return REPSTEP_ERR_ARG;
     if (!aligned(w, 16) || !aligned(m, 16) || !aligned(v, 16) || !aligned(wo, 16) ||
@@ -387,7 +404,7 @@ int do_adamw_to(repstep_ctx *x, void *w, float *m, float *v, void *wo, float *mo
     if (rc) return rc;
     if (begin > x->n || count > x->n - begin) return REPSTEP_ERR_ARG;
     if (!x->scale_ready) return REPSTEP_ERR_STATE;
-    rc = join_hash(x);      // the update rewrites the state and leaves a pending root reads
+    rc = join_hash_for_update(x);     // a pending audit-mode root reads the state
     if (rc) return rc;
     // the state the root hashes is the one written
     if (x->sw && (x->sw != wo || x->sm != mo || x->sv != vo)) return REPSTEP_ERR_ARG;
@@ -405,7 +422,7 @@ int do_adamw_to(repstep_ctx *x, void *w, float *m, float *v, void *wo, float *mo
     a.wo = wo;
     a.mo = mo;
     a.vo = vo;
-    a.only_if_clipped = only_if_clipped;
+    a.gate = gate;
     a.leaves = x->leaves();
     a.powers = x->powers();
     a.sc = x->sc();
@@ -448,7 +465,7 @@ int do_adamw(repstep_ctx *x, void *w, float *m, float *v, const repstep_hparams 
 // {step, n32} to leaves[0] in the PF61 mode) until one block remains: its root goes to the
 // context's scalars and to root_out.
 int merkle_over(repstep_ctx *x, uint64_t *leaves, uint64_t L, int32_t step, uint32_t n32,
-                uint64_t *root_out, cudaStream_t st)
+                uint64_t *root_out, cudaStream_t st, int header = -1)
 {
     const uint64_t mb1 = (L + kMerkleBlock - 1) / kMerkleBlock;
     // passes until one block remains; the block roots alternate between two regions (the
@@ -456,7 +473,7 @@ int merkle_over(repstep_ctx *x, uint64_t *leaves, uint64_t L, int32_t step, uint
     uint64_t *part[2] = {x->merkle_part(), x->merkle_part() + mb1};
     const uint64_t *in = leaves;
     uint64_t count = L;
-    int header = x->cfg.hash_mode == REPSTEP_HASH_PF61 ? 1 : 0;
+    if (header < 0) header = x->cfg.hash_mode == REPSTEP_HASH_PF61 ? 1 : 0;
     for (int pass = 0;; ++pass) {
         const uint64_t nb = (count + kMerkleBlock - 1) / kMerkleBlock;
         const bool last = nb == 1;
@@ -490,6 +507,7 @@ int audit_leaves(repstep_ctx *x, int32_t step, const void *w, const float *m, co
 }
 
 int root_passes(repstep_ctx *x, int32_t step, uint64_t *root_out, cudaStream_t st);
+int leaf_fixups(repstep_ctx *x, cudaStream_t st);
 
 int do_root(repstep_ctx *x, int32_t step, uint64_t *root_out)
 {
@@ -498,16 +516,34 @@ int do_root(repstep_ctx *x, int32_t step, uint64_t *root_out)
     int rc = join_hash(x);
     if (rc) return rc;
     if (!x->hash_stream) return root_passes(x, step, root_out, x->stream);
-    // the passes wait for the state on the context's stream, then run on the hash stream;
+    const bool pf61 = x->cfg.hash_mode == REPSTEP_HASH_PF61;
+    if (pf61) {
+        // the leaf array is completed on the context's stream (leaf fix-ups, header leaf)
+        // and copied; the Merkle passes read the copy, so the next update, which rewrites
+        // the leaves, need not wait for them
+        rc = leaf_fixups(x, x->stream);
+        if (rc) return rc;
+        cudaError_t e = launch_header_leaf(x->leaves(), step, uint32_t(x->n), x->powers(),
+                                           x->stream);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(x->leaf_snap(), x->leaves(), 8 * (1 + 3 * x->c),
+                                cudaMemcpyDeviceToDevice, x->stream);
+        if (e != cudaSuccess) return x->cuda_fail(e);
+        ++x->launches;
+    }
+    // the passes wait for the work on the context's stream, then run on the hash stream;
     // the context's stream goes on without them (join_hash orders later writers)
     cudaError_t e = cudaEventRecord(x->ev_state, x->stream);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(x->hash_stream, x->ev_state, 0);
     if (e != cudaSuccess) return x->cuda_fail(e);
-    rc = root_passes(x, step, root_out, x->hash_stream);
+    rc = pf61 ? merkle_over(x, x->leaf_snap(), 1 + 3 * x->c, step, uint32_t(x->n), root_out,
+                            x->hash_stream, 0)
+              : root_passes(x, step, root_out, x->hash_stream);
     if (rc) return rc;
     e = cudaEventRecord(x->ev_hash, x->hash_stream);
     if (e != cudaSuccess) return x->cuda_fail(e);
     x->hash_pending = true;
+    x->hash_reads_live = !pf61;
     return REPSTEP_OK;
 }
 
@@ -520,6 +556,13 @@ int root_passes(repstep_ctx *x, int32_t step, uint64_t *root_out, cudaStream_t s
         if (rc) return rc;
         return merkle(x, step, root_out, st);
     }
+    const int rc = leaf_fixups(x, st);
+    return rc ? rc : merkle(x, step, root_out, st);
+}
+
+// PF61 mode: recompute the leaves of the chunks the AdamW ranges cut, on st.
+int leaf_fixups(repstep_ctx *x, cudaStream_t st)
+{
     unique_sort(x->cut_leaf);
     for (size_t i = 0; i < x->cut_leaf.size(); i += kFixMax) {
         const int cnt = int(x->cut_leaf.size() - i < size_t(kFixMax) ? x->cut_leaf.size() - i : kFixMax);
@@ -530,7 +573,7 @@ int root_passes(repstep_ctx *x, int32_t step, uint64_t *root_out, cudaStream_t s
         ++x->launches;
     }
     x->cut_leaf.clear();
-    return merkle(x, step, root_out, st);
+    return REPSTEP_OK;
 }
 
 // The leaves of (step, w, m, v) into the workspace, on the context's stream: all 1 + 3c in
@@ -841,7 +884,10 @@ int step_fused(repstep_ctx *x, const void *const *grads, uint32_t R, const void 
         return rc ? rc : do_root(x, step, root_out);
     }
 
-    rc = join_hash(x);      // the pass writes the leaves, which a pending root may still read
+    // Launch order: the single pass (when the latest clip did not clip) or the two-pass
+    // reduce (when it did), the norm passes, then the reduce again and AdamW, each gated
+    // on the device by the clip history, so the host never waits for the norm.
+    rc = join_hash_for_update(x);     // a pending audit-mode root reads the state
     if (rc) return rc;
     FusedArgs f{};
     for (uint32_t r = 0; r < R; ++r) f.grads[r] = grads[r];
@@ -849,6 +895,7 @@ int step_fused(repstep_ctx *x, const void *const *grads, uint32_t R, const void 
     f.R = R;
     const float one = 1.0f;
     f.rho = one / float(R);
+    f.gate = kGateSpeculate;
     AdamwArgs &a = f.adam;
     a.w = w_in;
     a.m = m_in;
@@ -874,10 +921,13 @@ int step_fused(repstep_ctx *x, const void *const *grads, uint32_t R, const void 
     int bps = 1;
     e = fused_occupancy(shape, smem, &bps);
     if (e != cudaSuccess) return x->cuda_fail(e);
-    e = launch_fused(shape, f, grid_for(x, bps, x->c), smem, x->stream);
+    e = launch_fused(shape, f, grid_for(x, bps, x->c), smem, x->stream, x->pass_ev[0],
+                     x->pass_ev[1]);
     if (e != cudaSuccess) return x->cuda_fail(e);
     ++x->launches;
-    // the global norm and the true clip scale from the chunk sums the pass wrote
+    rc = do_reduce(x, grads, R, 1, R, 0, x->n, 0, 0, kGateTwoPass);
+    if (rc) return rc;
+    // the global norm and the true clip scale from the chunk sums either kernel wrote
     rc = norm_passes(x, x->chunk_sq(), x->c, hflush(x->fz(), hp->clip), norm_out, nullptr);
     if (rc) return rc;
     // the step's call-order state from here on is that of a finished clip
@@ -887,11 +937,12 @@ int step_fused(repstep_ctx *x, const void *const *grads, uint32_t R, const void 
     x->updated = 0;
     x->cut_leaf.clear();
     x->sw = x->sm = x->sv = nullptr;
-    // the second pass, run only when the scale is not 1: g from the gradients, then AdamW
-    // from the untouched input state into the output state, with its leaves
-    rc = do_reduce(x, grads, R, 1, R, 0, x->n, 0, 0, 1);
+    // when the single pass ran and the scale is not 1: g again from the gradients; then,
+    // unless the single pass wrote the update, AdamW from the untouched input state into
+    // the output state, with its leaves
+    rc = do_reduce(x, grads, R, 1, R, 0, x->n, 0, 0, kGateRedo);
     if (rc) return rc;
-    rc = do_adamw_to(x, w_in, m_in, v_in, wo, mo, vo, hp, 0, x->n, 1);
+    rc = do_adamw_to(x, w_in, m_in, v_in, wo, mo, vo, hp, 0, x->n, kGateUpdate);
     if (rc) return rc;
     return do_root(x, step, root_out);
 }
@@ -1029,6 +1080,14 @@ int repstep_set_hash_stream(repstep_ctx *ctx, void *hash_stream)
         if (e != cudaSuccess) return ctx->cuda_fail(e);
     }
     ctx->hash_stream = static_cast<cudaStream_t>(hash_stream);
+    return REPSTEP_OK;
+}
+
+int repstep_set_pass_events(repstep_ctx *ctx, void *ev_begin, void *ev_end)
+{
+    if (!ctx || (!ev_begin) != (!ev_end)) return REPSTEP_ERR_ARG;
+    ctx->pass_ev[0] = static_cast<cudaEvent_t>(ev_begin);
+    ctx->pass_ev[1] = static_cast<cudaEvent_t>(ev_end);
     return REPSTEP_OK;
 }
 

@@ -75,7 +75,7 @@ EXPORTS = [
     "repstep_reduce_paper_accum", "repstep_set_hash_stream", "repstep_wait_hash",
     "repstep_leaves", "repstep_selftest_fast_math", "repstep_step_from_host",
     "repstep_clip_gathered", "repstep_step_fused",
-    "repstep_root_gathered",
+    "repstep_root_gathered", "repstep_set_pass_events",
 ]
 NOALLOC_MAX_N = 1 << 30
 
@@ -134,6 +134,7 @@ def lib():
                                               vp, vp]
     L.repstep_set_decay_mask.argtypes = [vp, vp]
     L.repstep_set_hash_stream.argtypes = [vp, vp]
+    L.repstep_set_pass_events.argtypes = [vp, vp, vp]
     L.repstep_wait_hash.argtypes = [vp, vp]
     L.repstep_reduce_paper_accum.argtypes = [vp, C.POINTER(vp), u32, u32, u32, u64, u64]
     L.repstep_decay_mask_from_segments.argtypes = [u64, vp, vp, u32, vp]
@@ -437,8 +438,9 @@ class Repstep:
     def step_fused(self, grads, w, m, v, w_out, m_out, v_out, hp: HParams, step: int,
                    norm_out=None, root_out=None):
         """One step from (w, m, v) into (w_out, m_out, v_out), in a single HBM pass when it
-        does not clip (repstep_step_fused); the inputs are left untouched and the bits
-        equal step()'s.  Alternate the two state buffers from step to step."""
+        does not clip (repstep_step_fused); after a clip that clipped, in the two passes at
+        once.  The inputs are left untouched and the bits equal step()'s.  Alternate the
+        two state buffers from step to step."""
         arr, R = self._grads(grads)
         self._state(w, m, v)
         self._state(w_out, m_out, v_out)
@@ -485,6 +487,20 @@ class Repstep:
         if stream is not None:
             self._used_on(stream)
         self._hash_stream = stream
+
+    def set_pass_events(self, begin: torch.cuda.Event | None, end: torch.cuda.Event | None):
+        """Record these timing events around the single pass of every step_fused() call
+        while set (repstep_set_pass_events); None, None clears.  The events must have been
+        recorded once, so that they exist."""
+        def handle(ev):
+            if ev is None:
+                return None
+            h = ev.cuda_event
+            if not h:
+                raise RepstepError(1, "record the event once before passing it")
+            return C.c_void_p(h)
+        _check(lib().repstep_set_pass_events(self._ctx, handle(begin), handle(end)),
+               "set_pass_events")
 
     def wait_hash(self, stream: torch.cuda.Stream | None = None):
         """Make `stream` (default: the current stream) wait for the pending root passes."""

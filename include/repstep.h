@@ -162,20 +162,33 @@ int repstep_destroy(repstep_ctx *ctx);
 int repstep_set_stream(repstep_ctx *ctx, void *stream);
 
 /* Optional second stream for the state hash (NULL, the default: none).  When set,
- * repstep_root (and the root of repstep_step) waits on the hash stream for the work
- * already on the context's stream, then runs its passes there: the leaf fix-ups of cut
- * chunks (or the audit-mode leaves) and the Merkle passes.  The context's stream does not
- * wait for them, so the next step's reduce overlaps them; it is the ALU-bound hash beside
- * an HBM-bound reduce.  The bits are the same either way.
- * Ordering, handled by the library: the next call that writes the leaves or the state
- * (repstep_adamw, repstep_step, repstep_hash, repstep_root, repstep_image_read,
- * repstep_checkpoint_load) first makes the context's stream wait for the pending passes.
+ * repstep_root (and the root of repstep_step and repstep_step_fused) runs its Merkle
+ * passes on the hash stream, after the work already on the context's stream, which does
+ * not wait for them: the next step overlaps them, the ALU-bound hash beside HBM-bound
+ * kernels.  The bits are the same either way.
+ * - PF61 mode: the call first completes the leaf array on the context's stream (the leaf
+ *   fix-ups of cut chunks and the header leaf) and copies it to a snapshot in the
+ *   workspace, which the Merkle passes read.  The next update (repstep_adamw,
+ *   repstep_step, repstep_step_fused) therefore runs beside them.
+ * - Audit mode: the BLAKE2b leaves are computed from w, m, v on the hash stream too, and
+ *   the next call that writes the leaves or the state waits for them.
+ * Ordering, handled by the library: repstep_root, repstep_hash, repstep_leaves,
+ * repstep_root_gathered, repstep_image_read and repstep_checkpoint_load (and, in the audit
+ * mode, the updates) first make the context's stream wait for the pending passes.
  * Ordering left to the caller: d_root_out is complete when the hash stream reaches the
  * end of the passes -- order a stream after them with repstep_wait_hash, or call
- * repstep_sync, which waits for both streams -- and w, m, v must not be written by other
- * code until then, because the leaf fix-ups and the audit leaves read them.
+ * repstep_sync, which waits for both streams -- and in the audit mode w, m, v must not be
+ * written by other code until then, because the leaf kernel reads them.
  * Creates two CUDA events on first use (host resources; no device memory). */
 int repstep_set_hash_stream(repstep_ctx *ctx, void *hash_stream);
+
+/* Profiling: while set, repstep_step_fused records ev_begin on the context's stream just
+ * before its single pass and ev_end just after it, so that the caller can time that one
+ * kernel (cudaEventElapsedTime).  Both are cudaEvent_t handles the caller created and
+ * keeps alive while set; both null clears (one null and one not: REPSTEP_ERR_ARG).  The
+ * events are recorded whenever the single pass is launched, also when its gate skips it;
+ * configurations without the single pass record nothing. */
+int repstep_set_pass_events(repstep_ctx *ctx, void *ev_begin, void *ev_end);
 
 /* Make `stream` wait for the root passes last enqueued on the hash stream (no-op when none
  * is pending). */
@@ -326,9 +339,15 @@ int repstep_step(repstep_ctx *ctx, const void *const *d_grads, uint32_t R, uint3
  *   true scale.  Whenever the pre-clip norm does not exceed the clip threshold the scale
  *   is exactly 1 and those bits are the step's ("OPEN-1B: A Fully Auditable Training
  *   Run", §3.2: clipping to a global norm); otherwise the reduce and AdamW run again from
- *   the untouched inputs and overwrite the outputs.  The result is bit for bit
- *   repstep_step's on the same inputs either way; only the time differs (one pass over
- *   R*b_g + 24 bytes per parameter without clipping, about twice that with).
+ *   the untouched inputs and overwrite the outputs.
+ * - The context predicts from its latest clip (by any call): after one whose scale was
+ *   not 1, the step takes the two passes of repstep_step at once (into the output
+ *   buffers), and the single pass is skipped.  Every launch decides on the device from the
+ *   clip history, so the host never waits.  A right prediction costs one pass over
+ *   R*b_g + 24 bytes per parameter without clipping, or the two passes' R*b_g + 32 with
+ *   it; a wrong one costs the two passes, or the single pass and then the two.
+ * - The result is bit for bit repstep_step's on the same inputs either way; only the
+ *   time differs.
  * - The single pass covers R = 4 or 8, fp32 parameters, IEEE arithmetic, no decay mask and
  *   the default launch shape; any other configuration runs the two passes of
  *   repstep_step, writing the output buffers.

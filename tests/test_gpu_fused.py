@@ -1,8 +1,10 @@
 """repstep_step_fused through the C ABI: the single-pass step (reduce, chunk sums, AdamW with
 the clip scale taken as 1 into a second state buffer, PF61 leaves) with its second pass when
-the step clips.  Every output bit -- the new w, m, v, the pre-clip norm, the root and the
-leaves -- must equal repstep_step's on the same inputs, step after step with the two state
-buffers alternating, whether or not the step clips; the input state must be left untouched.
+the step clips, and the two passes taken directly after a step that clipped.  Every output
+bit -- the new w, m, v, the pre-clip norm, the root and the leaves -- must equal
+repstep_step's on the same inputs, step after step with the two state buffers alternating,
+on all four paths (predicted no clip and none; predicted no clip and a clip; predicted a
+clip and one; predicted a clip and none); the input state must be left untouched.
 Configurations the single pass does not cover (other R, bf16 parameters, flush-to-zero, a
 decay mask) take the two ordinary passes into the output buffers, with the same bits."""
 import ctypes as C
@@ -26,8 +28,12 @@ def _built():
     torch.cuda.set_device(0)
 
 
-def run_pair(n, R, gdt=torch.float32, steps=4, clip_steps=(2,), ctx_kw=None, hash_stream=False,
-             mask_segs=None):
+# no clip, then three that clip, then two that do not: every path of the prediction
+CLIPS = (2, 3, 4)
+
+
+def run_pair(n, R, gdt=torch.float32, steps=6, clip_steps=CLIPS, ctx_kw=None,
+             hash_stream=False, mask_segs=None):
     """Steps of repstep_step (in place) and of repstep_step_fused (alternating buffers) on the
     same gradients; steps in clip_steps get gradients large enough to clip."""
     dev = torch.device("cuda", 0)
@@ -78,6 +84,41 @@ def run_pair(n, R, gdt=torch.float32, steps=4, clip_steps=(2,), ctx_kw=None, has
     return clipped
 
 
+@pytest.mark.parametrize("n,R,hm", [(64 * CH + 1234, 8, rs.HASH_PF61),
+                                    (300 * CH + 5, 4, rs.HASH_PF61),
+                                    (64 * CH + 1234, 4, rs.HASH_BLAKE2B)])
+def test_fused_steps_beside_pending_roots(n, R, hm):
+    """With the hash stream, step t+1's single pass runs while step t's Merkle passes may
+    still read their leaf snapshot: the fused steps are enqueued with no synchronisation
+    between them, and every step's norm and root, and the final state and leaves, must
+    equal repstep_step's run step by step on one stream."""
+    dev = torch.device("cuda", 0)
+    steps, clips = 7, (3, 4)
+    a = rs.Repstep(n, device=dev, hash_mode=hm)
+    b = rs.Repstep(n, device=dev, hash_mode=hm)
+    b.set_hash_stream(torch.cuda.Stream(dev))
+    w, m, v = I.gen_state(U.F32_WL, n=n, device=dev)
+    bufs = [(w.clone(), m.clone(), v.clone()), tuple(torch.empty_like(x) for x in (w, m, v))]
+    grads = [U.gen_grads(n, R, 90 + t, scale=3000.0 if t in clips else 1e-3)
+             for t in range(1, steps + 1)]
+    na = torch.empty(steps, dtype=torch.float32, device=dev)
+    ra = torch.empty(steps, dtype=torch.int64, device=dev)
+    nb, rb = torch.empty_like(na), torch.empty_like(ra)
+    for t in range(1, steps + 1):
+        a.step(grads[t - 1], w, m, v, U.hp_for(t), step=t, norm_out=na[t - 1:t],
+               root_out=ra[t - 1:t])
+        a.sync()
+    for t in range(1, steps + 1):
+        b.step_fused(grads[t - 1], *bufs[(t - 1) % 2], *bufs[t % 2], U.hp_for(t), step=t,
+                     norm_out=nb[t - 1:t], root_out=rb[t - 1:t])
+    assert b.sync() & ~rs.FLAG_NONFINITE_NORM == 0
+    assert torch.equal(na.view(torch.int32), nb.view(torch.int32))
+    assert torch.equal(ra, rb)
+    for x, y in zip((w, m, v), bufs[steps % 2]):
+        assert torch.equal(x.view(torch.int32), y.view(torch.int32))
+    assert torch.equal(a.leaves_view(), b.leaves_view())
+
+
 @pytest.mark.parametrize("n,R,gdt", [
     (5 * CH * 3 + 77, 8, torch.float32),
     (5 * CH * 3 + 77, 4, torch.float32),
@@ -89,7 +130,7 @@ def run_pair(n, R, gdt=torch.float32, steps=4, clip_steps=(2,), ctx_kw=None, has
 ])
 def test_fused_equals_two_pass_step(n, R, gdt):
     clipped = run_pair(n, R, gdt)
-    assert clipped >= 1 or n == 1              # the clipping step took the second pass
+    assert clipped == 3 or n == 1              # the clipping steps clipped
 
 
 def test_fused_audit_mode_and_hash_stream():
@@ -109,6 +150,32 @@ def test_configurations_outside_the_single_pass(kw, R):
 
 def test_decay_mask_takes_the_two_passes():
     run_pair(3 * CH + 5, 8, mask_segs=[(0, False), (CH + 3, True)])
+
+
+def test_prediction_follows_other_calls():
+    """The clip history is the context's: a two-pass step or a lone clip between fused
+    steps moves the prediction, and the bits stay repstep_step's."""
+    n, R = 3 * CH + 5, 8
+    dev = torch.device("cuda", 0)
+    a, b = rs.Repstep(n, device=dev), rs.Repstep(n, device=dev)
+    w, m, v = I.gen_state(U.F32_WL, n=n, device=dev)
+    bufs = [(w.clone(), m.clone(), v.clone()), tuple(torch.empty_like(x) for x in (w, m, v))]
+    cur = 0
+    for t, (clip, via_step) in enumerate([(True, False), (False, True), (True, True),
+                                          (False, False), (True, False)], start=1):
+        grads = U.gen_grads(n, R, 80 + t, scale=3000.0 if clip else 1e-3)
+        hp = U.hp_for(t)
+        a.step(grads, w, m, v, hp, step=t)
+        if via_step:                           # b steps in place on its current buffer
+            b.step(grads, *bufs[cur], hp, step=t)
+        else:
+            b.step_fused(grads, *bufs[cur], *bufs[1 - cur], hp, step=t)
+            cur = 1 - cur
+        a.sync()
+        b.sync()
+        for x, y in zip((w, m, v), bufs[cur]):
+            assert torch.equal(x.view(torch.int32), y.view(torch.int32)), t
+        assert torch.equal(a.leaves_view(), b.leaves_view()), t
 
 
 def test_fused_matches_the_oracle():
@@ -161,6 +228,7 @@ def test_flat1200m_r8_fused_equals_two_pass():
     n, R = wl.n, wl.R
     dev = torch.device("cuda", 0)
     a, b = rs.Repstep(n, device=dev), rs.Repstep(n, device=dev)
+    b.set_hash_stream(torch.cuda.Stream(dev))          # the roots beside the next pass
     w, m, v = I.gen_state(wl, device=dev)
     bufs = [(w.clone(), m.clone(), v.clone()),
             (torch.empty_like(w), torch.empty_like(m), torch.empty_like(v))]
@@ -181,3 +249,35 @@ def test_flat1200m_r8_fused_equals_two_pass():
         assert rh[0] == rh[1]
         for x, y in zip((w, m, v), bufs[t % 2]):
             assert torch.equal(x.view(torch.int32), y.view(torch.int32))
+
+
+def test_pass_events_time_the_single_pass():
+    """repstep_set_pass_events: the events bracket the single pass of each call while set;
+    cleared, they are left alone; one null and one event is an argument error."""
+    n, R = 64 * CH, 8
+    dev = torch.device("cuda", 0)
+    ctx = rs.Repstep(n, device=dev)
+    st = torch.cuda.current_stream(dev)
+    w, m, v = I.gen_state(U.F32_WL, n=n, device=dev)
+    bufs = [(w, m, v), tuple(torch.empty_like(x) for x in (w, m, v))]
+    ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with pytest.raises(rs.RepstepError):          # not yet created
+        ctx.set_pass_events(ea, eb)
+    ea.record(st)
+    eb.record(st)
+    with pytest.raises(rs.RepstepError):
+        rs._check(rs.lib().repstep_set_pass_events(ctx._ctx, C.c_void_p(ea.cuda_event), None),
+                  "one event")
+    grads = U.gen_grads(n, R, 5, scale=1e-3)
+    outer_a, outer_b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ctx.set_pass_events(ea, eb)
+    outer_a.record(st)
+    ctx.step_fused(grads, *bufs[0], *bufs[1], U.hp_for(1), step=1)
+    outer_b.record(st)
+    ctx.set_pass_events(None, None)
+    ctx.sync()
+    inner = ea.elapsed_time(eb)
+    assert 0.0 < inner <= outer_a.elapsed_time(outer_b)
+    ctx.step_fused(grads, *bufs[1], *bufs[0], U.hp_for(2), step=2)   # cleared: not recorded
+    ctx.sync()
+    assert ea.elapsed_time(eb) == inner
