@@ -53,7 +53,7 @@ KERNEL_SOURCES = {k: [_CSRC + f for f in (*srcs, "common.cuh", "kernels.h")]
                   for k, srcs in (("k_reduce", ("k_reduce.cuh",)),
                                   ("k_adamw", ("k_adamw.cuh", "adamw_math.cuh")),
                                   ("k_leaves_b2", ("k_blake2b.cu",)),
-                                  ("k_fused", ("k_fused.cu", "adamw_math.cuh")))}
+                                  ("k_fused", ("k_fused.cuh", "adamw_math.cuh")))}
 # BLAKE2b-64 leaves (audit mode) are bound by the SM's integer ALU pipe: per 128-byte block,
 # 12 rounds x 8 G functions x 22 32-bit operations (two 3-input and two 2-input 64-bit
 # additions at 2 each, four 64-bit XORs at 2, rotations by 24, 16 and 63 at 2 funnel shifts
@@ -468,7 +468,7 @@ def run_ours(args, rank, world, local):
     mask_b = 0.125 if args.decay_mask else 0.0
     alg_step = int((R * b_g + 16 + 2 * b_w + mask_b) * n)
     alg = {"reduce": (R * b_g + 4) * n, "adamw": int((20 + 2 * b_w + mask_b) * n),
-           "fused_pass": int((R * b_g + 16 + 2 * b_w) * n)}
+           "fused_pass": int((R * b_g + 16 + 2 * b_w + mask_b) * n)}
     dom = max(("reduce", "adamw", "leaves") if audit else ("reduce", "adamw"),
               key=lambda k: kms[k])
     # the single pass carries the step when no timed step clipped (a step after one that
@@ -568,8 +568,9 @@ def run_sharded(args, rank, world, local):
     """The sharded step (bitwise_reproducible_step_gb300/shard.py): the workload's n split
     into `world` chunk-aligned ranges, one per GPU; each rank holds R/world replica gradients
     of the whole model and its range of the state.  A step is the routing of gradient
-    slices, the local reduce, the chunk-sum all-gather, the gathered norm and clip, AdamW on
-    the range, the leaf all-gather and the gathered root.  Total work is fixed as the world
+    slices, the local reduce (by default the single pass, into a second state buffer), the
+    chunk-sum all-gather, the gathered norm and clip, AdamW on the range (when the single
+    pass does not stand), the leaf all-gather and the gathered root.  Total work is fixed as the world
     grows (strong scaling): value = n / step time.  One rank routes nothing: it reads its own
     replicas' slices in place."""
     import torch.distributed as dist
@@ -599,6 +600,8 @@ def run_sharded(args, rank, world, local):
     w, m, v = (x[lo:hi].clone() for x in (w_all, m_all, v_all))
     del w_all, m_all, v_all
     torch.cuda.empty_cache()
+    # the single-pass step writes a second state buffer; the two alternate
+    bufs = [(w, m, v), tuple(torch.empty_like(x) for x in (w, m, v))] if args.fused else None
     norm = torch.empty(1, dtype=torch.float32, device=dev)
     root = torch.empty(1, dtype=torch.int64, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -608,7 +611,11 @@ def run_sharded(args, rank, world, local):
         t_step[0] += 1
         h = rs.hparams(lr=hpv["lr"], beta1=hpv["beta1"], beta2=hpv["beta2"], eps=hpv["eps"],
                        weight_decay=hpv["wd"], clip=hpv["clip"], t=t_step[0])
-        step.step(grads, w, m, v, h, t_step[0], norm_out=norm, root_out=root)
+        if bufs is not None:
+            step.step_fused(grads, *bufs[(t_step[0] - 1) % 2], *bufs[t_step[0] % 2], h,
+                            t_step[0], norm_out=norm, root_out=root)
+        else:
+            step.step(grads, w, m, v, h, t_step[0], norm_out=norm, root_out=root)
 
     repro = {}
     for i in range(args.warmup):
@@ -646,7 +653,10 @@ def run_sharded(args, rank, world, local):
                    "parallelism": f"sharded over {world} chunk-aligned ranges (point-to-point "
                                   "routing of gradient slices, all-gathers of chunk sums "
                                   "and leaves)",
-                   "l2": f"inputs larger than L2: {(R * b_g + 32) * n / 1e9:.1f} GB per step"},
+                   "step": ("ShardedStep.step_fused: the single pass on each range, state "
+                            "buffers alternating" if args.fused else "ShardedStep.step"),
+                   "l2": f"inputs larger than L2: {(R * b_g + (24 if args.fused else 32)) * n / 1e9:.1f} "
+                         "GB per step"},
         "hbm_gbs_step": step_gbs,
         "roofline_step": {"bound": "hbm", "achieved": step_gbs / world, "peak": peak,
                           "unit": "GB/s per GPU", "frac": step_gbs / world / peak,

@@ -87,7 +87,7 @@ cudaError_t launch_adamw(const AdamwShape &s, const AdamwArgs &args, int grid, s
 using AdamwKernelFn = void (*)(AdamwArgs);
 AdamwKernelFn pick_adamw_ieee(const AdamwShape &s);
 AdamwKernelFn pick_adamw_ftz(const AdamwShape &s);
-// The speculative single-pass step (k_fused.cu): replica reduce, chunk sums of squares,
+// The speculative single-pass step (k_fused.cuh): replica reduce, chunk sums of squares,
 // AdamW with clip scale 1 from (w, m, v) into (wo, mo, vo), and the PF61 leaves of the new
 // state.  R is one full replica group (4 or 8).
 struct FusedArgs {
@@ -104,7 +104,13 @@ struct FusedShape {
     int dtype;    // gradients: 0 fp32, 1 bf16
     int rg;       // R: 4 or 8
     int leaves;   // 1: PF61 leaves fused (hash mode PF61); 0: none (audit mode)
+    int pt;       // 1: bf16 parameters
+    int fz;       // 1: flush-to-zero (.ftz) arithmetic
+    int mk;       // 1: per-element weight-decay mask (adam.decay_mask)
 };
+using FusedKernelFn = void (*)(FusedArgs);
+FusedKernelFn pick_fused_ieee(const FusedShape &s);
+FusedKernelFn pick_fused_ftz(const FusedShape &s);
 size_t fused_smem_bytes(const FusedShape &s, FusedArgs &args);
 cudaError_t fused_prepare(const FusedShape &s, size_t smem);
 cudaError_t fused_occupancy(const FusedShape &s, size_t smem, int *blocks_per_sm);

@@ -141,6 +141,14 @@ struct repstep_ctx {
     cudaEvent_t ev_state = nullptr, ev_hash = nullptr;
     // caller's events recorded around the single pass (repstep_set_pass_events)
     cudaEvent_t pass_ev[2] = {nullptr, nullptr};
+    // the single-pass step between its halves (repstep_fused_begin .. repstep_fused_end):
+    // the buffers the second half must be given, and whether the single pass was launched
+    struct FusedCall {
+        bool open = false, single = false;
+        uint32_t R = 0;
+        const void *g[8] = {};
+        const void *st[6] = {};
+    } fused;
     bool hash_pending = false;
     // the pending root passes read the leaves or the state (the audit mode); otherwise
     // they read only the leaf snapshot and the Merkle partials
@@ -259,6 +267,7 @@ int do_reduce(repstep_ctx *x, const void *const *grads, uint32_t R, uint32_t nod
         if (!aligned(grads[r], 16)) return REPSTEP_ERR_ALIGN;
     }
     if (gate == kGateAlways) {
+        x->fused.open = false;                // a single-pass step left between its halves
         if (x->scale_ready || x->updated) {   // a new step starts
             x->scale_ready = false;
             x->updated = 0;
@@ -267,6 +276,13 @@ int do_reduce(repstep_ctx *x, const void *const *grads, uint32_t R, uint32_t nod
         x->reduced += count;
     }
     if (count == 0) return REPSTEP_OK;
+    // The bf16-gradient reduce hands out chunks by CTA index, so CTAs held back by the
+    // Merkle blocks of a pending root finish late and the whole launch waits for them:
+    // it starts after the root instead (measured at 3e9 parameters: 21.7 -> 21.5 ms).
+    if (x->cfg.grad_dtype == REPSTEP_BF16) {
+        const int jr = join_hash(x);
+        if (jr) return jr;
+    }
 
     const uint64_t end = begin + count;
     ReduceArgs a{};
@@ -404,7 +420,9 @@ int do_adamw_to(repstep_ctx *x, void *w, float *m, float *v, void *wo, float *mo
     if (rc) return rc;
     if (begin > x->n || count > x->n - begin) return REPSTEP_ERR_ARG;
     if (!x->scale_ready) return REPSTEP_ERR_STATE;
-    rc = join_hash_for_update(x);     // a pending audit-mode root reads the state
+    // a pending audit-mode root reads the state; the bf16-parameter kernel hands out
+    // chunks by CTA index (see do_reduce)
+    rc = x->w_bf16() ? join_hash(x) : join_hash_for_update(x);
     if (rc) return rc;
     // the state the root hashes is the one written
     if (x->sw && (x->sw != wo || x->sm != mo || x->sv != vo)) return REPSTEP_ERR_ARG;
@@ -833,22 +851,21 @@ bool overlaps(const void *a, uint64_t na, const void *b, uint64_t nb)
     return na && nb && pa < pb + nb && pb < pa + na;
 }
 
-// The speculative single-pass step (k_fused.cu) where its kernel covers the configuration:
-// R one full replica group of 4 or 8, fp32 parameters, IEEE arithmetic, no decay mask, the
-// default launch shape.  Elsewhere the same result comes from the ordinary passes, with
-// AdamW writing the second state buffer.
+// The speculative single-pass step (k_fused.cuh) where its kernel covers the configuration:
+// R one full replica group of 4 or 8 and the default launch shape (any gradient and
+// parameter dtype, arithmetic mode, decay mask and hash mode).  Elsewhere the same result
+// comes from the ordinary passes, with AdamW writing the second state buffer.
 bool fused_supported(const repstep_ctx *x, uint32_t R)
 {
-    return (R == 4 || R == 8) && x->cfg.param_dtype == REPSTEP_F32 && !x->fz() &&
-           !x->decay_mask && x->cfg.grid_blocks == 0 &&
+    return (R == 4 || R == 8) && x->cfg.grid_blocks == 0 &&
            (x->cfg.block_threads == 0 || x->cfg.block_threads == 512) && x->n > 0;
 }
 
-int step_fused(repstep_ctx *x, const void *const *grads, uint32_t R, const void *w,
-               const float *m, const float *v, void *wo, float *mo, float *vo,
-               const repstep_hparams *hp, int32_t step, float *norm_out, uint64_t *root_out)
+// Arguments of the single-pass step, checked before anything is launched.
+int check_fused_args(const repstep_ctx *x, const void *const *grads, uint32_t R,
+                     const void *w, const float *m, const float *v, const void *wo,
+                     const float *mo, const float *vo, const repstep_hparams *hp)
 {
-    // validate everything before launching anything
     if (!grads || R == 0) return REPSTEP_ERR_ARG;
     if (R > uint32_t(kMaxReplicas)) return REPSTEP_ERR_SIZE;
     if (x->n > 0 && (!w || !m || !v || !wo || !mo || !vo)) return REPSTEP_ERR_ARG;
@@ -867,84 +884,133 @@ int step_fused(repstep_ctx *x, const void *const *grads, uint32_t R, const void 
     for (int i = 0; i < 3; ++i)
         for (int j = 0; j < 3; ++j)
             if (overlaps(ins[i], in_bytes[i], outs[j], in_bytes[j])) return REPSTEP_ERR_ARG;
-    int rc = check_hparams(hp);
+    const int rc = check_hparams(hp);
     if (rc) return rc;
-    if (!(hp->clip > 0.0f)) return REPSTEP_ERR_ARG;
-    if (norm_out && !aligned(norm_out, 4)) return REPSTEP_ERR_ALIGN;
-    if (root_out && !aligned(root_out, 8)) return REPSTEP_ERR_ALIGN;
-    void *w_in = const_cast<void *>(w);
-    float *m_in = const_cast<float *>(m), *v_in = const_cast<float *>(v);
+    return hp->clip > 0.0f ? REPSTEP_OK : REPSTEP_ERR_ARG;
+}
 
-    if (!fused_supported(x, R)) {
+// The first half of the single-pass step: the two-pass reduce (when the latest clip
+// clipped) or the single pass (when it did not), both gated on the device by the clip
+// history, leaving the chunk sums for a clip (repstep_clip, or repstep_clip_gathered over
+// every shard's).  Configurations the single pass does not cover run the reduce.
+int fused_begin(repstep_ctx *x, const void *const *grads, uint32_t R, const void *w,
+                const float *m, const float *v, void *wo, float *mo, float *vo,
+                const repstep_hparams *hp)
+{
+    int rc = check_fused_args(x, grads, R, w, m, v, wo, mo, vo, hp);
+    if (rc) return rc;
+    const bool single = fused_supported(x, R);
+    x->fused = repstep_ctx::FusedCall{};
+    if (!single) {
         x->reduced = 0;
         x->cut_norm.clear();
         rc = do_reduce(x, grads, R, 1, R, 0, x->n);
-        if (!rc) rc = do_clip(x, hp->clip, norm_out, nullptr);
-        if (!rc) rc = do_adamw_to(x, w_in, m_in, v_in, wo, mo, vo, hp, 0, x->n);
-        return rc ? rc : do_root(x, step, root_out);
+        if (rc) return rc;
+    } else {
+        rc = join_hash_for_update(x);     // a pending audit-mode root reads the state
+        if (rc) return rc;
+        // the reduce of the two passes first: when its gate is closed it returns at once,
+        // and when it is open the single pass after it returns at once.  (In this order a
+        // step that takes the two passes does not wait for SMs that Merkle blocks of a
+        // pending root hold: the single pass's CTAs, even with their gate closed, need a
+        // whole SM, the reduce's fit beside a Merkle block.)
+        rc = do_reduce(x, grads, R, 1, R, 0, x->n, 0, 0, kGateTwoPass);
+        if (rc) return rc;
+        FusedArgs f{};
+        for (uint32_t r = 0; r < R; ++r) f.grads[r] = grads[r];
+        f.chunk_sq = x->chunk_sq();
+        f.R = R;
+        const float one = 1.0f;
+        f.rho = hflush(x->fz(), one / float(R));
+        f.gate = kGateSpeculate;
+        AdamwArgs &a = f.adam;
+        a.w = const_cast<void *>(w);
+        a.m = const_cast<float *>(m);
+        a.v = const_cast<float *>(v);
+        a.wo = wo;
+        a.mo = mo;
+        a.vo = vo;
+        a.leaves = x->leaves();
+        a.powers = x->powers();
+        a.sc = x->sc();
+        a.n = x->n;
+        a.c = x->c;
+        a.begin = 0;
+        a.end = x->n;
+        a.chunk_lo = 0;
+        a.chunk_hi = x->c;
+        adamw_hparams(x, hp, a);
+        a.decay_mask = x->decay_mask;
+        const FusedShape shape{x->cfg.grad_dtype == REPSTEP_BF16 ? 1 : 0, int(R),
+                               x->cfg.hash_mode == REPSTEP_HASH_PF61 ? 1 : 0, x->w_bf16(),
+                               x->fz(), x->decay_mask ? 1 : 0};
+        const size_t smem = fused_smem_bytes(shape, f);
+        cudaError_t e = fused_prepare(shape, smem);
+        if (e != cudaSuccess) return x->cuda_fail(e);
+        int bps = 1;
+        e = fused_occupancy(shape, smem, &bps);
+        if (e != cudaSuccess) return x->cuda_fail(e);
+        e = launch_fused(shape, f, grid_for(x, bps, x->c), smem, x->stream, x->pass_ev[0],
+                         x->pass_ev[1]);
+        if (e != cudaSuccess) return x->cuda_fail(e);
+        ++x->launches;
+        // the call-order state of a finished reduce over [0, n)
+        x->reduced = x->n;
+        x->cut_norm.clear();
+        x->scale_ready = false;
+        x->updated = 0;
+        x->cut_leaf.clear();
     }
+    // what the second half must be called with
+    x->fused.open = true;
+    x->fused.single = single;
+    x->fused.R = R;
+    for (uint32_t r = 0; r < R && r < 8; ++r) x->fused.g[r] = grads[r];
+    x->fused.st[0] = w;
+    x->fused.st[1] = m;
+    x->fused.st[2] = v;
+    x->fused.st[3] = wo;
+    x->fused.st[4] = mo;
+    x->fused.st[5] = vo;
+    return REPSTEP_OK;
+}
 
-    // Launch order: the single pass (when the latest clip did not clip) or the two-pass
-    // reduce (when it did), the norm passes, then the reduce again and AdamW, each gated
-    // on the device by the clip history, so the host never waits for the norm.
-    rc = join_hash_for_update(x);     // a pending audit-mode root reads the state
+// The second half, after the clip: when the single pass ran and the scale is not 1, g
+// again from the gradients; then, unless the single pass wrote the update, AdamW from the
+// untouched input state into the output state, with its leaves.
+int fused_end(repstep_ctx *x, const void *const *grads, uint32_t R, const void *w,
+              const float *m, const float *v, void *wo, float *mo, float *vo,
+              const repstep_hparams *hp)
+{
+    int rc = check_fused_args(x, grads, R, w, m, v, wo, mo, vo, hp);
     if (rc) return rc;
-    FusedArgs f{};
-    for (uint32_t r = 0; r < R; ++r) f.grads[r] = grads[r];
-    f.chunk_sq = x->chunk_sq();
-    f.R = R;
-    const float one = 1.0f;
-    f.rho = one / float(R);
-    f.gate = kGateSpeculate;
-    AdamwArgs &a = f.adam;
-    a.w = w_in;
-    a.m = m_in;
-    a.v = v_in;
-    a.wo = wo;
-    a.mo = mo;
-    a.vo = vo;
-    a.leaves = x->leaves();
-    a.powers = x->powers();
-    a.sc = x->sc();
-    a.n = x->n;
-    a.c = x->c;
-    a.begin = 0;
-    a.end = x->n;
-    a.chunk_lo = 0;
-    a.chunk_hi = x->c;
-    adamw_hparams(x, hp, a);
-    const FusedShape shape{x->cfg.grad_dtype == REPSTEP_BF16 ? 1 : 0, int(R),
-                           x->cfg.hash_mode == REPSTEP_HASH_PF61 ? 1 : 0};
-    const size_t smem = fused_smem_bytes(shape, f);
-    cudaError_t e = fused_prepare(shape, smem);
-    if (e != cudaSuccess) return x->cuda_fail(e);
-    int bps = 1;
-    e = fused_occupancy(shape, smem, &bps);
-    if (e != cudaSuccess) return x->cuda_fail(e);
-    e = launch_fused(shape, f, grid_for(x, bps, x->c), smem, x->stream, x->pass_ev[0],
-                     x->pass_ev[1]);
-    if (e != cudaSuccess) return x->cuda_fail(e);
-    ++x->launches;
-    rc = do_reduce(x, grads, R, 1, R, 0, x->n, 0, 0, kGateTwoPass);
-    if (rc) return rc;
-    // the global norm and the true clip scale from the chunk sums either kernel wrote
-    rc = norm_passes(x, x->chunk_sq(), x->c, hflush(x->fz(), hp->clip), norm_out, nullptr);
-    if (rc) return rc;
-    // the step's call-order state from here on is that of a finished clip
-    x->reduced = 0;
-    x->cut_norm.clear();
-    x->scale_ready = true;
-    x->updated = 0;
-    x->cut_leaf.clear();
-    x->sw = x->sm = x->sv = nullptr;
-    // when the single pass ran and the scale is not 1: g again from the gradients; then,
-    // unless the single pass wrote the update, AdamW from the untouched input state into
-    // the output state, with its leaves
+    const repstep_ctx::FusedCall &fc = x->fused;
+    bool same = fc.open && fc.R == R && fc.st[0] == w && fc.st[1] == m && fc.st[2] == v &&
+                fc.st[3] == wo && fc.st[4] == mo && fc.st[5] == vo;
+    for (uint32_t r = 0; same && r < R && r < 8; ++r) same = fc.g[r] == grads[r];
+    if (!same || !x->scale_ready) return REPSTEP_ERR_STATE;
+    void *w_in = const_cast<void *>(w);
+    float *m_in = const_cast<float *>(m), *v_in = const_cast<float *>(v);
+    x->fused.open = false;
+    if (!fc.single) return do_adamw_to(x, w_in, m_in, v_in, wo, mo, vo, hp, 0, x->n);
     rc = do_reduce(x, grads, R, 1, R, 0, x->n, 0, 0, kGateRedo);
     if (rc) return rc;
-    rc = do_adamw_to(x, w_in, m_in, v_in, wo, mo, vo, hp, 0, x->n, kGateUpdate);
+    return do_adamw_to(x, w_in, m_in, v_in, wo, mo, vo, hp, 0, x->n, kGateUpdate);
+}
+
+int step_fused(repstep_ctx *x, const void *const *grads, uint32_t R, const void *w,
+               const float *m, const float *v, void *wo, float *mo, float *vo,
+               const repstep_hparams *hp, int32_t step, float *norm_out, uint64_t *root_out)
+{
+    // validate everything before launching anything
+    int rc = check_fused_args(x, grads, R, w, m, v, wo, mo, vo, hp);
     if (rc) return rc;
-    return do_root(x, step, root_out);
+    if (norm_out && !aligned(norm_out, 4)) return REPSTEP_ERR_ALIGN;
+    if (root_out && !aligned(root_out, 8)) return REPSTEP_ERR_ALIGN;
+    rc = fused_begin(x, grads, R, w, m, v, wo, mo, vo, hp);
+    if (!rc) rc = do_clip(x, hp->clip, norm_out, nullptr);
+    if (!rc) rc = fused_end(x, grads, R, w, m, v, wo, mo, vo, hp);
+    return rc ? rc : do_root(x, step, root_out);
 }
 
 // Sharded steps.  The norm and clip scale from the chunk sums of every shard, gathered by
@@ -1201,6 +1267,24 @@ int repstep_step_fused(repstep_ctx *ctx, const void *const *d_grads, uint32_t R,
     if (!ctx) return REPSTEP_ERR_ARG;
     return step_fused(ctx, d_grads, R, d_w, d_m, d_v, d_w_out, d_m_out, d_v_out, hp, step,
                       d_norm_out, d_root_out);
+}
+
+int repstep_fused_begin(repstep_ctx *ctx, const void *const *d_grads, uint32_t R,
+                        const void *d_w, const float *d_m, const float *d_v, void *d_w_out,
+                        float *d_m_out, float *d_v_out, const repstep_hparams *hp)
+{
+    const NvtxRange nvtx_("repstep_fused_begin");
+    if (!ctx) return REPSTEP_ERR_ARG;
+    return fused_begin(ctx, d_grads, R, d_w, d_m, d_v, d_w_out, d_m_out, d_v_out, hp);
+}
+
+int repstep_fused_end(repstep_ctx *ctx, const void *const *d_grads, uint32_t R,
+                      const void *d_w, const float *d_m, const float *d_v, void *d_w_out,
+                      float *d_m_out, float *d_v_out, const repstep_hparams *hp)
+{
+    const NvtxRange nvtx_("repstep_fused_end");
+    if (!ctx) return REPSTEP_ERR_ARG;
+    return fused_end(ctx, d_grads, R, d_w, d_m, d_v, d_w_out, d_m_out, d_v_out, hp);
 }
 
 int repstep_clip_gathered(repstep_ctx *ctx, const float *d_chunk_sums, uint64_t c_total,

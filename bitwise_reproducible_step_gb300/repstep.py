@@ -75,7 +75,8 @@ EXPORTS = [
     "repstep_reduce_paper_accum", "repstep_set_hash_stream", "repstep_wait_hash",
     "repstep_leaves", "repstep_selftest_fast_math", "repstep_step_from_host",
     "repstep_clip_gathered", "repstep_step_fused",
-    "repstep_root_gathered", "repstep_set_pass_events",
+    "repstep_root_gathered", "repstep_set_pass_events", "repstep_fused_begin",
+    "repstep_fused_end",
 ]
 NOALLOC_MAX_N = 1 << 30
 
@@ -110,6 +111,8 @@ def lib():
     L.repstep_step_fused.argtypes = [vp, C.POINTER(vp), u32, vp, vp, vp, vp, vp, vp,
                                      C.POINTER(HParams), i32, vp, vp]
     L.repstep_root_gathered.argtypes = [vp, i32, u64, vp, vp]
+    for fn in (L.repstep_fused_begin, L.repstep_fused_end):
+        fn.argtypes = [vp, C.POINTER(vp), u32, vp, vp, vp, vp, vp, vp, C.POINTER(HParams)]
     L.repstep_step_from_host.argtypes = [vp, C.POINTER(vp), u32, C.POINTER(vp), u32, u32, vp, vp,
                                          vp, C.POINTER(HParams), i32, vp, vp]
     L.repstep_image_bytes.argtypes = [u64]
@@ -449,6 +452,29 @@ class Repstep:
                                         _ptr(w_out), _ptr(m_out), _ptr(v_out), C.byref(hp),
                                         int(step), self._out(norm_out, torch.float32),
                                         self._out(root_out, torch.int64)), "step_fused")
+
+    def fused_begin(self, grads, w, m, v, w_out, m_out, v_out, hp: HParams):
+        """The first half of step_fused (repstep_fused_begin): the single pass, or after a
+        clip that clipped the reduce of the two passes; then clip() or clip_gathered(),
+        then fused_end() with the same arguments."""
+        arr, R = self._grads(grads)
+        self._state(w, m, v)
+        self._state(w_out, m_out, v_out)
+        self._bind()
+        _check(lib().repstep_fused_begin(self._ctx, arr, R, _ptr(w), _ptr(m), _ptr(v),
+                                         _ptr(w_out), _ptr(m_out), _ptr(v_out), C.byref(hp)),
+               "fused_begin")
+
+    def fused_end(self, grads, w, m, v, w_out, m_out, v_out, hp: HParams):
+        """The second half of step_fused after the clip (repstep_fused_end): the second
+        pass where the clip needs one, and the AdamW of the two passes."""
+        arr, R = self._grads(grads)
+        self._state(w, m, v)
+        self._state(w_out, m_out, v_out)
+        self._bind()
+        _check(lib().repstep_fused_end(self._ctx, arr, R, _ptr(w), _ptr(m), _ptr(v),
+                                       _ptr(w_out), _ptr(m_out), _ptr(v_out), C.byref(hp)),
+               "fused_end")
 
     def step_from_host(self, host_grads, staging, w, m, v, hp: HParams, step: int,
                        pieces: int = 8, copy_streams: int = 2):

@@ -208,3 +208,23 @@ class ShardedStep:
         leaves = gather_leaves(ctx.leaves_view(), self.plan, self.rank, self.group)
         ctx.root_gathered(step, self.plan.n, leaves, root_out=root_out)
         return leaves
+
+    def step_fused(self, local_grads, w, m, v, w_out, m_out, v_out, hp, step: int,
+                   norm_out=None, root_out=None):
+        """The same step from (w, m, v) into (w_out, m_out, v_out) with the single pass:
+        route -> repstep_fused_begin on the received slices -> gather the chunk sums ->
+        repstep_clip_gathered -> repstep_fused_end -> (audit mode: repstep_leaves of the
+        new state) -> gather the leaves -> repstep_root_gathered.  Every rank gets the same
+        norm, so every rank takes the same path; the bits equal step()'s."""
+        slices = route_gradients(local_grads, self.plan, self.rank, self.R, out=self.recv,
+                                 group=self.group)
+        ctx = self.ctx
+        ctx.fused_begin(slices, w, m, v, w_out, m_out, v_out, hp)
+        sums = gather_chunk_sums(ctx.chunk_sums_view(), self.plan, self.rank, self.group)
+        ctx.clip_gathered(sums, hp.clip, norm_out=norm_out)
+        ctx.fused_end(slices, w, m, v, w_out, m_out, v_out, hp)
+        if self.audit:
+            ctx.leaves(step, w_out, m_out, v_out)
+        leaves = gather_leaves(ctx.leaves_view(), self.plan, self.rank, self.group)
+        ctx.root_gathered(step, self.plan.n, leaves, root_out=root_out)
+        return leaves

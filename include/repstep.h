@@ -348,14 +348,33 @@ int repstep_step(repstep_ctx *ctx, const void *const *d_grads, uint32_t R, uint3
  *   it; a wrong one costs the two passes, or the single pass and then the two.
  * - The result is bit for bit repstep_step's on the same inputs either way; only the
  *   time differs.
- * - The single pass covers R = 4 or 8, fp32 parameters, IEEE arithmetic, no decay mask and
- *   the default launch shape; any other configuration runs the two passes of
- *   repstep_step, writing the output buffers.
+ * - The single pass covers R = 4 or 8 with the default launch shape, in every gradient and
+ *   parameter dtype, arithmetic mode, decay mask and hash mode; any other replica count or
+ *   launch shape runs the two passes of repstep_step, writing the output buffers.
  * - `step`, hp, d_norm_out and d_root_out as repstep_step; the root is the output state's. */
 int repstep_step_fused(repstep_ctx *ctx, const void *const *d_grads, uint32_t R,
                        const void *d_w, const float *d_m, const float *d_v, void *d_w_out,
                        float *d_m_out, float *d_v_out, const repstep_hparams *hp, int32_t step,
                        float *d_norm_out, uint64_t *d_root_out);
+
+/* The two halves of repstep_step_fused, for a step whose clip runs between them -- the
+ * sharded step, where the norm comes from every range's chunk sums (repstep_clip_gathered):
+ *   repstep_fused_begin -> repstep_clip or repstep_clip_gathered -> repstep_fused_end ->
+ *   repstep_root, or the leaves' gather and repstep_root_gathered.
+ * repstep_fused_begin launches the single pass over [0, n) (or, after a clip that clipped,
+ * the reduce of the two passes), which leaves the chunk sums at repstep_layout.chunk_sums;
+ * with it the context counts as reduced over [0, n).  repstep_fused_end launches the
+ * second pass where the clip needs one, and the AdamW of the two passes, into the output
+ * buffers.  Both take the same arguments as repstep_step_fused (same rules, same errors);
+ * repstep_fused_end must get exactly the buffers repstep_fused_begin got, after a clip
+ * (REPSTEP_ERR_STATE otherwise).  The three calls together give repstep_step_fused's
+ * bits. */
+int repstep_fused_begin(repstep_ctx *ctx, const void *const *d_grads, uint32_t R,
+                        const void *d_w, const float *d_m, const float *d_v, void *d_w_out,
+                        float *d_m_out, float *d_v_out, const repstep_hparams *hp);
+int repstep_fused_end(repstep_ctx *ctx, const void *const *d_grads, uint32_t R,
+                      const void *d_w, const float *d_m, const float *d_v, void *d_w_out,
+                      float *d_m_out, float *d_v_out, const repstep_hparams *hp);
 
 /* One whole step whose R replica gradients start in HOST memory, with the norm and the
  * root returned to host memory: the end-to-end form of repstep_step for a caller whose

@@ -183,8 +183,9 @@ class FullOracle:
              dp_shard=1):
         """Run the oracle's step t on the device gradients `grads` (R torch tensors) and
         compare with the GPU's results.  hp: dict(lr, beta1, beta2, eps, wd, clip).
-        gpu: None (the oracle's step only), or a dict of device tensors g, chunk_sums, leaves (u64 as int64), w, m, v (the
-        state after the GPU's step), norm (1 fp32) and root (1 int64).  reducer: "tree"
+        gpu: None (the oracle's step only), or a dict of device tensors g (optional: a
+        step that keeps g out of HBM has none to compare), chunk_sums, leaves (u64 as
+        int64), w, m, v (the state after the GPU's step), norm (1 fp32) and root (1 int64).  reducer: "tree"
         (the canonical tree), "topology" (staged nodes x gpus_per_node) or "alg1" (the
         paper-exact order with dp_shard).  Returns the report dict."""
         L, n, c, R = self.L, self.n, self.c, self.R
@@ -225,7 +226,7 @@ class FullOracle:
                 normf(_ptr(self.g, a), b - a, _ptr(self.chunk_sums, a // CH))
 
             self._run(reduce_part, self._parts(lo, hi))
-            if gpu is not None:
+            if gpu is not None and "g" in gpu:
                 tally.add("g", self._host(self.stage_a, gpu["g"][lo:hi], cnt), self.g[lo:hi])
 
         # ---- the global norm and clip scale from the oracle's own chunk sums

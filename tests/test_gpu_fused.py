@@ -5,8 +5,9 @@ bit -- the new w, m, v, the pre-clip norm, the root and the leaves -- must equal
 repstep_step's on the same inputs, step after step with the two state buffers alternating,
 on all four paths (predicted no clip and none; predicted no clip and a clip; predicted a
 clip and one; predicted a clip and none); the input state must be left untouched.
-Configurations the single pass does not cover (other R, bf16 parameters, flush-to-zero, a
-decay mask) take the two ordinary passes into the output buffers, with the same bits."""
+The single pass covers R = 4 and 8 with any gradient and parameter dtype, arithmetic mode,
+decay mask and hash mode; other replica counts and launch shapes take the two ordinary
+passes into the output buffers, with the same bits."""
 import ctypes as C
 
 import numpy as np
@@ -138,18 +139,24 @@ def test_fused_audit_mode_and_hash_stream():
     run_pair(5 * CH * 3 + 77, 4, torch.bfloat16, hash_stream=True)
 
 
-@pytest.mark.parametrize("kw,R", [
-    (dict(), 3),                                               # R not 4 or 8
-    (dict(param_dtype=torch.bfloat16), 8),
-    (dict(subnormals=rs.SUBNORMALS_FTZ), 8),
-    (dict(block_threads=256), 8),
+@pytest.mark.parametrize("kw,R,gdt", [
+    (dict(param_dtype=torch.bfloat16), 8, torch.float32),       # in the single pass
+    (dict(param_dtype=torch.bfloat16), 4, torch.bfloat16),
+    (dict(subnormals=rs.SUBNORMALS_FTZ), 8, torch.float32),
+    (dict(subnormals=rs.SUBNORMALS_FTZ, param_dtype=torch.bfloat16), 4, torch.bfloat16),
+    (dict(), 3, torch.float32),                                 # R not 4 or 8: two passes
+    (dict(block_threads=256), 8, torch.float32),                # launch shape: two passes
 ])
-def test_configurations_outside_the_single_pass(kw, R):
-    run_pair(3 * CH + 5, R, ctx_kw=kw)
+def test_configuration_variants(kw, R, gdt):
+    run_pair(3 * CH + 5, R, gdt, ctx_kw=kw)
+    run_pair(2 * CH + 2049, R, gdt, ctx_kw=kw)                  # ragged: bulk-copy edges
 
 
-def test_decay_mask_takes_the_two_passes():
-    run_pair(3 * CH + 5, 8, mask_segs=[(0, False), (CH + 3, True)])
+@pytest.mark.parametrize("kw", [dict(), dict(param_dtype=torch.bfloat16),
+                                dict(subnormals=rs.SUBNORMALS_FTZ)])
+def test_decay_mask(kw):
+    run_pair(3 * CH + 5, 8, mask_segs=[(0, False), (CH + 3, True), (2 * CH + 7, False)],
+             ctx_kw=kw)
 
 
 def test_prediction_follows_other_calls():

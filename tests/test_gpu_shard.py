@@ -68,6 +68,95 @@ def emulated_step(plan, ctxs, grads, w, m, v, hp, t, audit=False):
     return norms.cpu().numpy(), roots.cpu().numpy().view(np.uint64)
 
 
+def emulated_fused_step(plan, ctxs, grads, src, dst, hp, t, audit=False):
+    """The sharded single-pass step of plan.world virtual ranks in one process, from the
+    state buffers `src` into `dst` (full-length tensors; each rank updates its range)."""
+    n, N = plan.n, plan.world
+    dev = src[0].device
+    sl = [tuple(x[plan.range_of(s)[0]:plan.range_of(s)[1]] for x in (*src, *dst))
+          for s in range(N)]
+    for s in range(N):
+        lo, hi = plan.range_of(s)
+        ctxs[s].fused_begin([g[lo:hi] for g in grads], *sl[s], hp)
+    sums = S.unpack_chunk_sums(
+        torch.stack([S.pack_chunk_sums(ctxs[s].chunk_sums_view(), plan, s) for s in range(N)]),
+        plan)
+    norms = torch.empty(N, dtype=torch.float32, device=dev)
+    roots = torch.empty(N, dtype=torch.int64, device=dev)
+    for s in range(N):
+        lo, hi = plan.range_of(s)
+        ctxs[s].clip_gathered(sums, hp.clip, norm_out=norms[s:s + 1])
+        ctxs[s].fused_end([g[lo:hi] for g in grads], *sl[s], hp)
+        if audit:
+            ctxs[s].leaves(t, *sl[s][3:])
+    leaves = S.unpack_leaves(
+        torch.stack([S.pack_leaves(ctxs[s].leaves_view(), plan, s) for s in range(N)]), plan)
+    for s in range(N):
+        ctxs[s].root_gathered(t, n, leaves, root_out=roots[s:s + 1])
+    for c in ctxs:
+        assert c.sync() & ~rs.FLAG_NONFINITE_NORM == 0
+    return norms.cpu().numpy(), roots.cpu().numpy().view(np.uint64)
+
+
+FUSED_CASES = [
+    # n, N, R, grad dtype, hash mode
+    (5 * 4096 * 4 + 1234, 4, 8, torch.float32, rs.HASH_PF61),
+    (5 * 4096 * 4 + 1234, 2, 4, torch.bfloat16, rs.HASH_BLAKE2B),
+    (2 * 4096 + 5, 4, 4, torch.float32, rs.HASH_PF61),          # the last rank owns nothing
+    (4096 * 4100, 2, 8, torch.float32, rs.HASH_PF61),           # c > 4096: two-pass norm
+]
+
+
+@pytest.mark.parametrize("n,N,R,gdt,hm", FUSED_CASES)
+def test_emulated_ranks_fused_equal_unsharded_step(n, N, R, gdt, hm):
+    """repstep_fused_begin / repstep_clip_gathered / repstep_fused_end on every virtual
+    rank, steps that do not clip, clip, clip and do not (every path of the prediction), the
+    state buffers alternating: the norm, root and state equal repstep_step's."""
+    dev = torch.device("cuda", 0)
+    plan = S.ShardPlan(n, N)
+    ref = rs.Repstep(n, grad_dtype=gdt, device=dev, hash_mode=hm)
+    ctxs = [rs.Repstep(plan.range_of(s)[1] - plan.range_of(s)[0], grad_dtype=gdt, device=dev,
+                       hash_mode=hm) for s in range(N)]
+    wa, ma, va = I.gen_state(U.F32_WL, n=n, device=dev)
+    bufs = [(wa.clone(), ma.clone(), va.clone()),
+            tuple(torch.empty_like(x) for x in (wa, ma, va))]
+    nr = torch.empty(1, dtype=torch.float32, device=dev)
+    rr = torch.empty(1, dtype=torch.int64, device=dev)
+    for t in (1, 2, 3, 4):
+        grads = U.gen_grads(n, R, 40 + t, gdt, scale=2000.0 if t in (2, 3) else 1e-3)
+        hp = U.hp_for(t)
+        ref.step(grads, wa, ma, va, hp, step=t, norm_out=nr, root_out=rr)
+        ref.sync()
+        norms, roots = emulated_fused_step(plan, ctxs, grads, bufs[(t - 1) % 2], bufs[t % 2],
+                                           hp, t, audit=hm != 0)
+        assert all(x.view(np.uint32) == np.float32(nr.item()).view(np.uint32) for x in norms)
+        assert all(int(x) == U.root_of(rr) for x in roots), (roots, U.root_of(rr))
+        for a, b in zip((wa, ma, va), bufs[t % 2]):
+            assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+
+
+def test_fused_halves_check_their_order():
+    dev = torch.device("cuda", 0)
+    n, R = 3 * 4096, 4
+    ctx = rs.Repstep(n, device=dev)
+    w, m, v = I.gen_state(U.F32_WL, n=n, device=dev)
+    out = tuple(torch.empty_like(x) for x in (w, m, v))
+    grads = U.gen_grads(n, R, 1)
+    hp = U.hp_for(1)
+    with pytest.raises(rs.RepstepError):            # no first half
+        ctx.fused_end(grads, w, m, v, *out, hp)
+    ctx.fused_begin(grads, w, m, v, *out, hp)
+    with pytest.raises(rs.RepstepError):            # before the clip
+        ctx.fused_end(grads, w, m, v, *out, hp)
+    ctx.clip(hp.clip)
+    other = tuple(torch.empty_like(x) for x in (w, m, v))
+    with pytest.raises(rs.RepstepError):            # other output buffers than the first half's
+        ctx.fused_end(grads, w, m, v, *other, hp)
+    ctx.fused_end(grads, w, m, v, *out, hp)
+    ctx.root(1)
+    assert ctx.sync() == 0
+
+
 CASES = [
     # n, N, R, grad dtype, hash mode
     (5 * 4096 * 4 + 1234, 4, 8, torch.float32, rs.HASH_PF61),
@@ -153,6 +242,39 @@ def test_world_one_over_nccl_equals_unsharded_step(gdt, hm):
             rh = rr.cpu().numpy().view(np.uint64)
             assert rh[0] == rh[1]
             for a, b in ((wa, wb), (ma, mb), (va, vb)):
+                assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_world_one_over_nccl_fused_equals_unsharded_step():
+    """ShardedStep.step_fused with a real NCCL process group of one rank, the state buffers
+    alternating, over steps that clip and do not."""
+    dev = torch.device("cuda", 0)
+    n, R = 3 * 4096 * 5 + 333, 8
+    os.environ.setdefault("NCCL_NVLS_ENABLE", "0")
+    dist.init_process_group("nccl", init_method=f"tcp://127.0.0.1:{_free_port()}", rank=0,
+                            world_size=1, device_id=dev)
+    try:
+        step = S.ShardedStep(n, R, 0, 1, dev)
+        ref = rs.Repstep(n, device=dev)
+        wa, ma, va = I.gen_state(U.F32_WL, n=n, device=dev)
+        bufs = [(wa.clone(), ma.clone(), va.clone()),
+                tuple(torch.empty_like(x) for x in (wa, ma, va))]
+        nr = torch.empty(2, dtype=torch.float32, device=dev)
+        rr = torch.empty(2, dtype=torch.int64, device=dev)
+        for t in (1, 2, 3):
+            grads = U.gen_grads(n, R, t, scale=2000.0 if t == 2 else 1e-3)
+            hp = U.hp_for(t)
+            ref.step(grads, wa, ma, va, hp, step=t, norm_out=nr[0:1], root_out=rr[0:1])
+            step.step_fused(grads, *bufs[(t - 1) % 2], *bufs[t % 2], hp, t, norm_out=nr[1:2],
+                            root_out=rr[1:2])
+            ref.sync()
+            step.ctx.sync()
+            assert nr[0].item() == nr[1].item()
+            rh = rr.cpu().numpy().view(np.uint64)
+            assert rh[0] == rh[1]
+            for a, b in zip((wa, ma, va), bufs[t % 2]):
                 assert torch.equal(a.view(torch.int32), b.view(torch.int32))
     finally:
         dist.destroy_process_group()

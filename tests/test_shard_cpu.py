@@ -191,6 +191,14 @@ class OracleCtx:
         w.copy_(torch.from_numpy(w1)); m.copy_(torch.from_numpy(m1)); v.copy_(torch.from_numpy(v1))
         self.lv = O.leaves(0, w1, m1, v1)          # the chunk leaves; the header is not used
 
+    def fused_begin(self, slices, w, m, v, w_out, m_out, v_out, hp):
+        self.reduce(slices)
+
+    def fused_end(self, slices, w, m, v, w_out, m_out, v_out, hp):
+        for dst, src in ((w_out, w), (m_out, m), (v_out, v)):
+            dst.copy_(src)
+        self.adamw(w_out, m_out, v_out, hp)
+
     def leaves(self, step, w, m, v):
         from oracle import oracle as O
         if self.n:
@@ -209,7 +217,7 @@ class OracleCtx:
             root_out[0] = int(np.array([O.merkle_root(L)], np.uint64).view(np.int64)[0])
 
 
-def _sharded_step_main(rank, world, port, n, R, bf16, hash_mode, seed):
+def _sharded_step_main(rank, world, port, n, R, bf16, hash_mode, seed, fused=False):
     from bitwise_reproducible_step_gb300 import repstep as rs
     from oracle import oracle as O
     os.environ["MASTER_ADDR"] = "127.0.0.1"
@@ -223,6 +231,7 @@ def _sharded_step_main(rank, world, port, n, R, bf16, hash_mode, seed):
         assert (step.lo, step.hi) == (lo, hi)
         _, W, M, V = _inputs(n, R, bf16, seed)
         w, m, v = (torch.from_numpy(x[lo:hi].copy()) for x in (W, M, V))
+        other = tuple(torch.empty_like(x) for x in (w, m, v))
         Rl = R // world
         for t in (1, 2):
             grads, _, _, _ = _inputs(n, R, bf16, seed + 100 * t)
@@ -231,7 +240,11 @@ def _sharded_step_main(rank, world, port, n, R, bf16, hash_mode, seed):
                             weight_decay=HP["wd"], clip=HP["clip"], t=t)
             norm = torch.zeros(1, dtype=torch.float32)
             root = torch.zeros(1, dtype=torch.int64)
-            step.step(mine, w, m, v, hp, t, norm_out=norm, root_out=root)
+            if fused:                    # from (w, m, v) into the other buffers, then swap
+                step.step_fused(mine, w, m, v, *other, hp, t, norm_out=norm, root_out=root)
+                (w, m, v), other = other, (w, m, v)
+            else:
+                step.step(mine, w, m, v, hp, t, norm_out=norm, root_out=root)
             ref = O.step(grads, W, M, V, lr=HP["lr"], beta1=HP["beta1"], beta2=HP["beta2"],
                          eps=HP["eps"], wd=HP["wd"], clip=HP["clip"], t=t, hash_mode=hash_mode)
             W, M, V = ref["w"], ref["m"], ref["v"]
@@ -255,4 +268,20 @@ def test_sharded_step_across_ranks_equals_unsharded_oracle(world, n, R, bf16, ha
     from bitwise_reproducible_step_gb300 import build
     build.build()                             # the host-side bias corrections
     mp.spawn(_sharded_step_main, args=(world, _free_port(), n, R, bf16, hash_mode, 31 + world),
+             nprocs=world, join=True)
+
+
+@pytest.mark.parametrize("world,n,R,bf16,hash_mode", [
+    (2, 4 * CH * 2 + 999, 4, False, 0),
+    (4, 9 * CH + 1, 8, True, 1),
+])
+def test_sharded_fused_step_across_ranks_equals_unsharded_oracle(world, n, R, bf16, hash_mode):
+    """ShardedStep.step_fused's sequence -- routing, the first half of the single-pass
+    step, chunk-sum gather, gathered clip, the second half into the other state buffer,
+    leaf gather, gathered root -- over gloo ranks, two steps with the buffers alternating,
+    against the unsharded oracle step."""
+    from bitwise_reproducible_step_gb300 import build
+    build.build()
+    mp.spawn(_sharded_step_main,
+             args=(world, _free_port(), n, R, bf16, hash_mode, 77 + world, True),
              nprocs=world, join=True)
