@@ -90,6 +90,15 @@ __global__ void __launch_bounds__(256) k_leaves_b2(const void *w, int w_bf16, co
 
 }  // namespace
 
+cudaError_t leaves_b2_prepare()
+{
+    // On the hash stream the leaves run beside the next step's single pass: their blocks
+    // must not leave an SM configured with less shared memory than its CTAs need.
+    return cudaFuncSetAttribute(reinterpret_cast<const void *>(k_leaves_b2),
+                                cudaFuncAttributePreferredSharedMemoryCarveout,
+                                int(cudaSharedmemCarveoutMaxShared));
+}
+
 cudaError_t launch_leaves_b2(const void *w, int w_bf16, const float *m, const float *v, uint64_t n,
                              uint64_t c, uint64_t *leaves, uint32_t step, int sm_count,
                              cudaStream_t st)

@@ -151,6 +151,7 @@ cudaError_t launch_narrow_bf16(unsigned short *dst, const float *src, uint64_t n
 cudaError_t launch_leaves_b2(const void *w, int w_bf16, const float *m, const float *v, uint64_t n,
                              uint64_t c, uint64_t *leaves, uint32_t step, int sm_count,
                              cudaStream_t st);
+cudaError_t leaves_b2_prepare();   // shared-memory carveout (run beside the single pass)
 
 constexpr int kFixMax = 64;   // chunk indices per fix-up launch
 

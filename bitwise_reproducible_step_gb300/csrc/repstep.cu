@@ -150,9 +150,11 @@ struct repstep_ctx {
         const void *st[6] = {};
     } fused;
     bool hash_pending = false;
-    // the pending root passes read the leaves or the state (the audit mode); otherwise
-    // they read only the leaf snapshot and the Merkle partials
+    // the pending root passes read the state (the audit mode: hash_st, the three arrays
+    // and their bytes); otherwise they read only the leaf snapshot and the Merkle partials
     bool hash_reads_live = false;
+    const void *hash_st[3] = {nullptr, nullptr, nullptr};
+    uint64_t hash_st_bytes[3] = {0, 0, 0};
     std::vector<uint64_t> cut_norm, cut_leaf;   // chunks cut by range boundaries
 
     // repstep_step_from_host: copy streams and events, created on first use (host resources
@@ -197,12 +199,22 @@ int join_hash(repstep_ctx *x)
     return REPSTEP_OK;
 }
 
-// Before an update writes the state and the leaves: only a pending root that reads them
-// (the audit mode) must end first.  A PF61 root reads the leaf snapshot its call took,
-// so the next update runs beside it.
-int join_hash_for_update(repstep_ctx *x)
+bool overlaps(const void *a, uint64_t na, const void *b, uint64_t nb);
+
+// Before an update writes (wo, mo, vo): only a pending root that reads what it writes
+// must end first.  A PF61 root reads the leaf snapshot its call took; an audit-mode root
+// reads the state it hashes, which an update into the other state buffer of the
+// single-pass step leaves alone.  So both run beside such an update.
+int join_hash_for_update(repstep_ctx *x, const void *wo, const void *mo, const void *vo)
 {
-    return x->hash_reads_live ? join_hash(x) : REPSTEP_OK;
+    if (!x->hash_pending || !x->hash_reads_live) return REPSTEP_OK;
+    const void *outs[3] = {wo, mo, vo};
+    const uint64_t out_bytes[3] = {x->w_bytes(), 4 * x->n, 4 * x->n};
+    for (int i = 0; i < 3; ++i)
+        for (int j = 0; j < 3; ++j)
+            if (overlaps(outs[i], out_bytes[i], x->hash_st[j], x->hash_st_bytes[j]))
+                return join_hash(x);
+    return REPSTEP_OK;
 }
 
 // Persistent grid: SM count x resident CTAs, never more CTAs than chunks to process.
@@ -422,7 +434,7 @@ int do_adamw_to(repstep_ctx *x, void *w, float *m, float *v, void *wo, float *mo
     if (!x->scale_ready) return REPSTEP_ERR_STATE;
     // a pending audit-mode root reads the state; the bf16-parameter kernel hands out
     // chunks by CTA index (see do_reduce)
-    rc = x->w_bf16() ? join_hash(x) : join_hash_for_update(x);
+    rc = x->w_bf16() ? join_hash(x) : join_hash_for_update(x, wo, mo, vo);
     if (rc) return rc;
     // the state the root hashes is the one written
     if (x->sw && (x->sw != wo || x->sm != mo || x->sv != vo)) return REPSTEP_ERR_ARG;
@@ -554,6 +566,13 @@ int do_root(repstep_ctx *x, int32_t step, uint64_t *root_out)
     cudaError_t e = cudaEventRecord(x->ev_state, x->stream);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(x->hash_stream, x->ev_state, 0);
     if (e != cudaSuccess) return x->cuda_fail(e);
+    if (!pf61) {          // the state the audit-mode leaves read
+        x->hash_st[0] = x->sw;
+        x->hash_st[1] = x->sm;
+        x->hash_st[2] = x->sv;
+        x->hash_st_bytes[0] = x->w_bytes();
+        x->hash_st_bytes[1] = x->hash_st_bytes[2] = 4 * x->n;
+    }
     rc = pf61 ? merkle_over(x, x->leaf_snap(), 1 + 3 * x->c, step, uint32_t(x->n), root_out,
                             x->hash_stream, 0)
               : root_passes(x, step, root_out, x->hash_stream);
@@ -907,7 +926,7 @@ int fused_begin(repstep_ctx *x, const void *const *grads, uint32_t R, const void
         rc = do_reduce(x, grads, R, 1, R, 0, x->n);
         if (rc) return rc;
     } else {
-        rc = join_hash_for_update(x);     // a pending audit-mode root reads the state
+        rc = join_hash_for_update(x, wo, mo, vo);   // an audit-mode root reads its state
         if (rc) return rc;
         // the reduce of the two passes first: when its gate is closed it returns at once,
         // and when it is open the single pass after it returns at once.  (In this order a
@@ -1112,6 +1131,7 @@ int repstep_create(const repstep_config *cfg, void *d_workspace, size_t workspac
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&x->sm_count, cudaDevAttrMultiProcessorCount, dev);
     if (e == cudaSuccess) e = merkle_prepare();
+    if (e == cudaSuccess) e = leaves_b2_prepare();
     if (e == cudaSuccess) e = cudaMemsetAsync(x->ws + lay.scalars, 0, sizeof(Scalars), x->stream);
     if (e == cudaSuccess) e = launch_init_powers(x->powers(), x->stream);
     if (e != cudaSuccess) {

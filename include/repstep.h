@@ -170,11 +170,13 @@ int repstep_set_stream(repstep_ctx *ctx, void *stream);
  *   fix-ups of cut chunks and the header leaf) and copies it to a snapshot in the
  *   workspace, which the Merkle passes read.  The next update (repstep_adamw,
  *   repstep_step, repstep_step_fused) therefore runs beside them.
- * - Audit mode: the BLAKE2b leaves are computed from w, m, v on the hash stream too, and
- *   the next call that writes the leaves or the state waits for them.
+ * - Audit mode: the BLAKE2b leaves are computed from w, m, v on the hash stream too, so an
+ *   update that writes those arrays waits for them; repstep_step_fused's update into the
+ *   other state buffer runs beside them.
  * Ordering, handled by the library: repstep_root, repstep_hash, repstep_leaves,
  * repstep_root_gathered, repstep_image_read and repstep_checkpoint_load (and, in the audit
- * mode, the updates) first make the context's stream wait for the pending passes.
+ * mode, an update whose outputs share a byte with the hashed state) first make the
+ * context's stream wait for the pending passes.
  * Ordering left to the caller: d_root_out is complete when the hash stream reaches the
  * end of the passes -- order a stream after them with repstep_wait_hash, or call
  * repstep_sync, which waits for both streams -- and in the audit mode w, m, v must not be
