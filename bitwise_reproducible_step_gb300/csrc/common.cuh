@@ -106,32 +106,20 @@ struct Scalars {
     uint32_t aux;         // scratch flag of host-driven checks (image narrowing)
     uint64_t root;        // last Merkle root
     uint32_t next_chunk;  // work counter of the running reduce (zeroed before each launch)
-    uint32_t clip_hist;   // bit 0: the latest clip's scale was not 1; bit 1: the one before
+    uint32_t spare;
 };
 
-// Which launches of the single-pass step run.  Each clip shifts its outcome into
-// Scalars::clip_hist, and the step predicts from it: after a clip that clipped it takes the
-// two passes at once, after one that did not it speculates with the single pass.  The
-// gates read the history before this step's norm (bit 0 is the prediction) or after it
-// (bit 1 the prediction, bit 0 the outcome); a closed gate returns before any access.
+// Whether a launch runs: always, or only when the last clip's scale is not exactly 1 (the
+// second pass of the single-pass step, after it speculated that the step would not clip).
+// A closed gate returns before any access.
 enum : int {
     kGateAlways = 0,
-    kGateSpeculate = 1,   // before the norm: the single pass (the latest clip did not clip)
-    kGateTwoPass = 2,     // before the norm: the reduce of the two passes (it did)
-    kGateRedo = 3,        // after the norm: the reduce again (speculated, and it clipped)
-    kGateUpdate = 4,      // after the norm: AdamW (took the two passes, or it clipped)
+    kGateIfClipped = 1,
 };
 
 __device__ __forceinline__ bool gate_open(int gate, const Scalars *sc)
 {
-    if (gate == kGateAlways) return true;
-    const uint32_t h = sc->clip_hist;
-    switch (gate) {
-    case kGateSpeculate: return (h & 1u) == 0;
-    case kGateTwoPass: return (h & 1u) != 0;
-    case kGateRedo: return (h & 3u) == 1u;
-    default: return (h & 3u) != 0;
-    }
+    return gate == kGateAlways || __float_as_uint(sc->scale) != 0x3F800000u;
 }
 
 // ----------------------------------------------------------------------------------

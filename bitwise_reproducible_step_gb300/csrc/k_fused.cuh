@@ -15,10 +15,10 @@
 // scale from the chunk sums.  The scale is exactly 1 whenever norm <= clip (and for a
 // non-finite norm), and then every bit written here is the step's: gc = g * 1 is the
 // same operation with the same operands as the two-pass step's gc = g * scale.  When the
-// scale is not 1, the reduce and AdamW kernels run again (gates kGateRedo, kGateUpdate)
-// from the untouched (w, m, v) and overwrite (wo, mo, vo) and the leaves; otherwise they
-// return at once.  The pass itself runs only when the context's latest clip did not clip
-// (gate kGateSpeculate); after one that did, the step takes the two passes directly.
+// scale is not 1, the reduce and AdamW kernels run again (gate kGateIfClipped) from the
+// untouched (w, m, v) and overwrite (wo, mo, vo) and the leaves; otherwise they return at
+// once.  The host launches the pass only when the last clip outcome it can see did not
+// clip; after one that did, the step takes the two passes directly.
 //
 // The arithmetic is the two-pass kernels' own, element for element: the same
 // element-to-thread mapping as k_reduce (a thread holds 4 consecutive elements of each
@@ -132,7 +132,6 @@ __global__ void __launch_bounds__(NT + 64, 2) k_fused(const __grid_constant__ Fu
     static_assert(GS * NGS == RG, "gradient stages hold whole groups");
     static_assert(TPC * TE == kChunk && TPC * 4 <= 32, "tiles divide the chunk; limb bound");
     const AdamwArgs &A = F.adam;
-    if (!gate_open(F.gate, A.sc)) return;     // the step takes the two passes
 
     extern __shared__ __align__(1024) unsigned char smem[];
     const uint32_t S = A.stages;

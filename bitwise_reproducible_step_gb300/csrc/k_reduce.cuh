@@ -229,7 +229,7 @@ __global__ void __launch_bounds__(NT + 32, 1) k_reduce(const __grid_constant__ R
     constexpr bool DYN = DT == 0;
     static_assert(16 * kMaxStages + 2 * TPC * W * 4 + 8 + 8 * kMaxStages <= kRingOffset,
                   "smem header");
-    // a launch of the single-pass step that this step does not need returns at once
+    // the second pass of the single-pass step: nothing to do when the clip scale is 1
     if (!gate_open(A.gate, A.sc)) return;
 
     extern __shared__ __align__(1024) unsigned char smem[];

@@ -106,7 +106,8 @@ __global__ void __launch_bounds__(256) k_leaf_fix(const void *w, int w_bf16, con
 template <int FZ>
 __global__ void __launch_bounds__(256) k_norm(const float *in, uint64_t count, float *out,
                                               Scalars *sc, int final_pass, float clip,
-                                              float *norm_out, float *scale_out)
+                                              float *norm_out, float *scale_out,
+                                              volatile uint32_t *clip_flag)
 {
     __shared__ float red[4 * 8];
     const int tid = threadIdx.x;
@@ -136,7 +137,7 @@ __global__ void __launch_bounds__(256) k_norm(const float *in, uint64_t count, f
     const bool finite = isfinite(norm);
     sc->norm = norm;
     sc->scale = scale;
-    sc->clip_hist = ((sc->clip_hist & 1u) << 1) | (__float_as_uint(scale) != 0x3F800000u ? 1u : 0u);
+    if (clip_flag) *clip_flag = __float_as_uint(scale) != 0x3F800000u ? 1u : 0u;
     sc->flags = (sc->flags & ~kFlagNonfinite) | (finite ? 0u : kFlagNonfinite);
     if (norm_out) *norm_out = norm;
     if (scale_out) *scale_out = scale;
@@ -242,12 +243,14 @@ cudaError_t launch_leaf_fix(const void *w, int w_bf16, const float *m, const flo
 
 cudaError_t launch_norm(const float *in, uint64_t count, float *out, Scalars *sc, int final_pass,
                         float clip, float *norm_out, float *scale_out, int blocks, int fz,
-                        cudaStream_t st)
+                        cudaStream_t st, uint32_t *clip_flag)
 {
     if (fz)
-        k_norm<1><<<blocks, 256, 0, st>>>(in, count, out, sc, final_pass, clip, norm_out, scale_out);
+        k_norm<1><<<blocks, 256, 0, st>>>(in, count, out, sc, final_pass, clip, norm_out, scale_out,
+                                         clip_flag);
     else
-        k_norm<0><<<blocks, 256, 0, st>>>(in, count, out, sc, final_pass, clip, norm_out, scale_out);
+        k_norm<0><<<blocks, 256, 0, st>>>(in, count, out, sc, final_pass, clip, norm_out, scale_out,
+                                         clip_flag);
     return cudaGetLastError();
 }
 

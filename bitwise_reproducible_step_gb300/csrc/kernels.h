@@ -26,7 +26,7 @@ struct ReduceArgs {
     uint32_t accum;           // paper-exact mode: 0 = one gradient per virtual rank; else
                               // microbatches per rank, accumulated from +0
     float rho3;               // fp32(1/accum)
-    int gate;                 // kGate*: whether the launch runs (repstep_step_fused)
+    int gate;                 // kGateAlways, or kGateIfClipped (repstep_step_fused)
 };
 
 struct ReduceShape {
@@ -58,7 +58,7 @@ struct AdamwArgs {
     float *m, *v;             // Adam moments (fp32), read
     void *wo;                 // where the AdamW modes write w', m', v': w, m, v themselves
     float *mo, *vo;           // (in place), or a second state buffer (repstep_step_fused)
-    int gate;                 // kGate*: whether the launch runs (repstep_step_fused)
+    int gate;                 // kGateAlways, or kGateIfClipped (repstep_step_fused)
     uint64_t *leaves;         // workspace u64[1 + 3c]
     const uint64_t *powers;   // workspace K^1..K^4096 mod p
     Scalars *sc;              // device scalars (scale, flags)
@@ -95,7 +95,6 @@ struct FusedArgs {
     float *chunk_sq;          // workspace fp32[c]
     uint32_t R;
     float rho;                // fp32(1/R)
-    int gate;                 // kGateSpeculate
     AdamwArgs adam;           // state in and out, leaves, powers, scalars, n, c, constants,
                               // ring depth and stage size
 };
@@ -131,9 +130,11 @@ cudaError_t launch_chunk_fix(const float *g, uint64_t n, float *chunk_sq, const 
 cudaError_t launch_leaf_fix(const void *w, int w_bf16, const float *m, const float *v, uint64_t n,
                             uint64_t c, uint64_t *leaves, const uint64_t *powers,
                             const uint64_t *chunks, int count, cudaStream_t st);
+// clip_flag (nullable, a host-mapped word): the final pass stores 1 there when the scale
+// is not 1, else 0
 cudaError_t launch_norm(const float *in, uint64_t count, float *out, Scalars *sc, int final_pass,
                         float clip, float *norm_out, float *scale_out, int blocks, int fz,
-                        cudaStream_t st);
+                        cudaStream_t st, uint32_t *clip_flag = nullptr);
 cudaError_t merkle_prepare();
 cudaError_t launch_merkle(const uint64_t *in, uint64_t count, uint64_t *out, int header_mode,
                           uint64_t *leaves_rw, uint32_t step, uint32_t n32, const uint64_t *powers,

@@ -141,6 +141,11 @@ struct repstep_ctx {
     cudaEvent_t ev_state = nullptr, ev_hash = nullptr;
     // caller's events recorded around the single pass (repstep_set_pass_events)
     cudaEvent_t pass_ev[2] = {nullptr, nullptr};
+    // the outcome of the last clip that has run, as the host sees it: a word of mapped
+    // pinned host memory (clip_flag_h) that every final norm pass stores 1 (clipped) or 0
+    // into through its device address (clip_flag_d); null where the device maps no host
+    // memory, and then the single-pass step always speculates
+    uint32_t *clip_flag_h = nullptr, *clip_flag_d = nullptr;
     // the single-pass step between its halves (repstep_fused_begin .. repstep_fused_end):
     // the buffers the second half must be given, and whether the single pass was launched
     struct FusedCall {
@@ -261,8 +266,8 @@ int check_hparams(const repstep_hparams *hp)
 // OPEN-1B Algorithm 1 with dp_replicate = nodes and dp_shard = gpn.
 // R replicas (virtual ranks) = nodes x gpn; with accum > 0 (paper mode only) `grads`
 // holds R * accum microbatch gradients, rank-major.
-// gate: a gated launch of the single-pass step (kGate*), which runs or returns at once by
-// the clip history on the device; the call-order state is left as the caller set it.
+// gate: kGateIfClipped for the second pass of the single-pass step, which returns at once
+// when the clip scale is 1; the call-order state is left as the caller set it.
 int do_reduce(repstep_ctx *x, const void *const *grads, uint32_t R, uint32_t nodes,
               uint32_t gpn, uint64_t begin, uint64_t count, int paper = 0, uint32_t accum = 0,
               int gate = kGateAlways)
@@ -352,10 +357,10 @@ int norm_passes(repstep_ctx *x, const float *sums, uint64_t c, float clip, float
         if (e != cudaSuccess) return x->cuda_fail(e);
         ++x->launches;
         e = launch_norm(x->norm_part(), uint64_t(nb), nullptr, x->sc(), 1, clip, norm_out,
-                        scale_out, 1, fz, x->stream);
+                        scale_out, 1, fz, x->stream, x->clip_flag_d);
     } else {
         e = launch_norm(sums, c, nullptr, x->sc(), 1, clip, norm_out, scale_out, 1, fz,
-                        x->stream);
+                        x->stream, x->clip_flag_d);
     }
     if (e != cudaSuccess) return x->cuda_fail(e);
     ++x->launches;
@@ -417,9 +422,9 @@ void adamw_hparams(const repstep_ctx *x, const repstep_hparams *hp, AdamwArgs &a
 }
 
 // AdamW over [begin, begin+count): reads w, m, v and writes w', m', v' to wo, mo, vo (the
-// same arrays for the in-place update).  gate: kGateUpdate in the single-pass step, where
-// the kernel returns at once when the pass already wrote the update; the call-order state
-// moves on either way.
+// same arrays for the in-place update).  gate: kGateIfClipped in the single-pass step,
+// where the kernel returns at once when the pass already wrote the update; the call-order
+// state moves on either way.
 int do_adamw_to(repstep_ctx *x, void *w, float *m, float *v, void *wo, float *mo, float *vo,
                 const repstep_hparams *hp, uint64_t begin, uint64_t count,
                 int gate = kGateAlways)
@@ -908,17 +913,20 @@ int check_fused_args(const repstep_ctx *x, const void *const *grads, uint32_t R,
     return hp->clip > 0.0f ? REPSTEP_OK : REPSTEP_ERR_ARG;
 }
 
-// The first half of the single-pass step: the two-pass reduce (when the latest clip
-// clipped) or the single pass (when it did not), both gated on the device by the clip
-// history, leaving the chunk sums for a clip (repstep_clip, or repstep_clip_gathered over
-// every shard's).  Configurations the single pass does not cover run the reduce.
+// The first half of the single-pass step: the single pass when the last clip outcome the
+// host can see did not clip, else the reduce of the two passes; either leaves the chunk
+// sums for a clip (repstep_clip, or repstep_clip_gathered over every shard's).  The
+// outcome is read without waiting: when the GPU is behind, it is an older step's, which
+// only costs time, never bits.  Configurations the single pass does not cover run the
+// reduce.
 int fused_begin(repstep_ctx *x, const void *const *grads, uint32_t R, const void *w,
                 const float *m, const float *v, void *wo, float *mo, float *vo,
                 const repstep_hparams *hp)
 {
     int rc = check_fused_args(x, grads, R, w, m, v, wo, mo, vo, hp);
     if (rc) return rc;
-    const bool single = fused_supported(x, R);
+    const bool predict_clip = x->clip_flag_h && *static_cast<volatile uint32_t *>(x->clip_flag_h);
+    const bool single = fused_supported(x, R) && !predict_clip;
     x->fused = repstep_ctx::FusedCall{};
     if (!single) {
         x->reduced = 0;
@@ -928,20 +936,12 @@ int fused_begin(repstep_ctx *x, const void *const *grads, uint32_t R, const void
     } else {
         rc = join_hash_for_update(x, wo, mo, vo);   // an audit-mode root reads its state
         if (rc) return rc;
-        // the reduce of the two passes first: when its gate is closed it returns at once,
-        // and when it is open the single pass after it returns at once.  (In this order a
-        // step that takes the two passes does not wait for SMs that Merkle blocks of a
-        // pending root hold: the single pass's CTAs, even with their gate closed, need a
-        // whole SM, the reduce's fit beside a Merkle block.)
-        rc = do_reduce(x, grads, R, 1, R, 0, x->n, 0, 0, kGateTwoPass);
-        if (rc) return rc;
         FusedArgs f{};
         for (uint32_t r = 0; r < R; ++r) f.grads[r] = grads[r];
         f.chunk_sq = x->chunk_sq();
         f.R = R;
         const float one = 1.0f;
         f.rho = hflush(x->fz(), one / float(R));
-        f.gate = kGateSpeculate;
         AdamwArgs &a = f.adam;
         a.w = const_cast<void *>(w);
         a.m = const_cast<float *>(m);
@@ -974,6 +974,7 @@ int fused_begin(repstep_ctx *x, const void *const *grads, uint32_t R, const void
         if (e != cudaSuccess) return x->cuda_fail(e);
         ++x->launches;
         // the call-order state of a finished reduce over [0, n)
+        x->fused.open = false;
         x->reduced = x->n;
         x->cut_norm.clear();
         x->scale_ready = false;
@@ -1012,9 +1013,9 @@ int fused_end(repstep_ctx *x, const void *const *grads, uint32_t R, const void *
     float *m_in = const_cast<float *>(m), *v_in = const_cast<float *>(v);
     x->fused.open = false;
     if (!fc.single) return do_adamw_to(x, w_in, m_in, v_in, wo, mo, vo, hp, 0, x->n);
-    rc = do_reduce(x, grads, R, 1, R, 0, x->n, 0, 0, kGateRedo);
+    rc = do_reduce(x, grads, R, 1, R, 0, x->n, 0, 0, kGateIfClipped);
     if (rc) return rc;
-    return do_adamw_to(x, w_in, m_in, v_in, wo, mo, vo, hp, 0, x->n, kGateUpdate);
+    return do_adamw_to(x, w_in, m_in, v_in, wo, mo, vo, hp, 0, x->n, kGateIfClipped);
 }
 
 int step_fused(repstep_ctx *x, const void *const *grads, uint32_t R, const void *w,
@@ -1132,6 +1133,21 @@ int repstep_create(const repstep_config *cfg, void *d_workspace, size_t workspac
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&x->sm_count, cudaDevAttrMultiProcessorCount, dev);
     if (e == cudaSuccess) e = merkle_prepare();
     if (e == cudaSuccess) e = leaves_b2_prepare();
+    if (e == cudaSuccess) {
+        // the host-visible clip outcome (pinned host memory: no device allocation)
+        void *h = nullptr;
+        if (cudaHostAlloc(&h, sizeof(uint32_t), cudaHostAllocMapped) == cudaSuccess) {
+            *static_cast<volatile uint32_t *>(h) = 0;
+            void *d = nullptr;
+            if (cudaHostGetDevicePointer(&d, h, 0) == cudaSuccess) {
+                x->clip_flag_h = static_cast<uint32_t *>(h);
+                x->clip_flag_d = static_cast<uint32_t *>(d);
+            } else {
+                cudaFreeHost(h);
+            }
+        }
+        cudaGetLastError();   // a device without mapped host memory: no prediction
+    }
     if (e == cudaSuccess) e = cudaMemsetAsync(x->ws + lay.scalars, 0, sizeof(Scalars), x->stream);
     if (e == cudaSuccess) e = launch_init_powers(x->powers(), x->stream);
     if (e != cudaSuccess) {
@@ -1146,6 +1162,11 @@ int repstep_create(const repstep_config *cfg, void *d_workspace, size_t workspac
 int repstep_destroy(repstep_ctx *ctx)
 {
     if (!ctx) return REPSTEP_ERR_ARG;
+    if (ctx->clip_flag_h) {
+        // a norm pass still queued may store the clip outcome into the mapped word
+        cudaStreamSynchronize(ctx->stream);
+        cudaFreeHost(ctx->clip_flag_h);
+    }
     if (ctx->ev_state) cudaEventDestroy(ctx->ev_state);
     if (ctx->ev_hash) cudaEventDestroy(ctx->ev_hash);
     if (ctx->ev_free) cudaEventDestroy(ctx->ev_free);

@@ -155,7 +155,9 @@ int repstep_workspace_layout(const repstep_config *cfg, repstep_layout *out);
 int repstep_create(const repstep_config *cfg, void *d_workspace, size_t workspace_bytes,
                    void *stream, repstep_ctx **out);
 
-/* Destroy the context (host memory only; does not synchronise the stream). */
+/* Destroy the context: its host resources, after the work queued on its stream has
+ * finished (a norm pass there may still store the last clip outcome into the context's
+ * one word of mapped pinned host memory).  The workspace is the caller's. */
 int repstep_destroy(repstep_ctx *ctx);
 
 /* Change the stream later calls enqueue on. */
@@ -342,12 +344,14 @@ int repstep_step(repstep_ctx *ctx, const void *const *d_grads, uint32_t R, uint3
  *   is exactly 1 and those bits are the step's ("OPEN-1B: A Fully Auditable Training
  *   Run", §3.2: clipping to a global norm); otherwise the reduce and AdamW run again from
  *   the untouched inputs and overwrite the outputs.
- * - The context predicts from its latest clip (by any call): after one whose scale was
- *   not 1, the step takes the two passes of repstep_step at once (into the output
- *   buffers), and the single pass is skipped.  Every launch decides on the device from the
- *   clip history, so the host never waits.  A right prediction costs one pass over
- *   R*b_g + 24 bytes per parameter without clipping, or the two passes' R*b_g + 32 with
- *   it; a wrong one costs the two passes, or the single pass and then the two.
+ * - The context predicts from the last clip outcome (by any call) that has run by the time
+ *   of the call: every final norm pass stores it into a word of mapped pinned host
+ *   memory, which the call reads without waiting.  After a clip whose scale was not 1, the
+ *   step takes the two passes of repstep_step at once (into the output buffers), and the
+ *   single pass is not launched.  A right prediction costs one pass over R*b_g + 24 bytes
+ *   per parameter without clipping, or the two passes' R*b_g + 32 with it; a wrong one
+ *   costs the two passes, or the single pass and then the two.  A late outcome (the GPU
+ *   behind the host) can only cost time.
  * - The result is bit for bit repstep_step's on the same inputs either way; only the
  *   time differs.
  * - The single pass covers R = 4 or 8 with the default launch shape, in every gradient and

@@ -160,8 +160,8 @@ def test_decay_mask(kw):
 
 
 def test_prediction_follows_other_calls():
-    """The clip history is the context's: a two-pass step or a lone clip between fused
-    steps moves the prediction, and the bits stay repstep_step's."""
+    """The clip outcome the prediction reads is the context's: a two-pass step or a lone
+    clip between fused steps moves it, and the bits stay repstep_step's."""
     n, R = 3 * CH + 5, 8
     dev = torch.device("cuda", 0)
     a, b = rs.Repstep(n, device=dev), rs.Repstep(n, device=dev)
