@@ -288,3 +288,22 @@ def test_pass_events_time_the_single_pass():
     ctx.step_fused(grads, *bufs[1], *bufs[0], U.hp_for(2), step=2)   # cleared: not recorded
     ctx.sync()
     assert ea.elapsed_time(eb) == inner
+
+
+def test_empty_state():
+    """n = 0: no arrays are read; the root is the header's, as repstep_step's."""
+    dev = torch.device("cuda", 0)
+    a, b = rs.Repstep(0, device=dev), rs.Repstep(0, device=dev)
+    e = torch.empty(0, device=dev)
+    grads = [torch.empty(0, device=dev) for _ in range(4)]
+    nr = torch.empty(2, dtype=torch.float32, device=dev)
+    rr = torch.empty(2, dtype=torch.int64, device=dev)
+    hp = U.hp_for(1)
+    a.step(grads, e, e.clone(), e.clone(), hp, step=1, norm_out=nr[0:1], root_out=rr[0:1])
+    b.step_fused(grads, e, e.clone(), e.clone(), torch.empty(0, device=dev),
+                 torch.empty(0, device=dev), torch.empty(0, device=dev), hp, step=1,
+                 norm_out=nr[1:2], root_out=rr[1:2])
+    assert a.sync() == 0 and b.sync() == 0
+    assert nr[0].item() == nr[1].item() == 0.0
+    rh = rr.cpu().numpy().view(np.uint64)
+    assert rh[0] == rh[1]
