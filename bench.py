@@ -311,20 +311,22 @@ def run_ours(args, rank, world, local):
         fused_state = [(w, m, v), (torch.empty_like(w), torch.empty_like(m), torch.empty_like(v))]
     cur = [0]
 
+    # the timed steps' output slots (tensor views), made before the timed region
+    timed_out = []
+
     def one_step(slot=None):
         t_step[0] += 1
-        nr = norm if slot is None else norms[slot:slot + 1]
-        rt = root if slot is None else roots[slot:slot + 1]
+        h = hp(t_step[0])
+        nr, rt = (norm, root) if slot is None else timed_out[slot]
         if fused_state is not None:
             ctx.step_fused(grads, *fused_state[cur[0]], *fused_state[1 - cur[0]],
-                           hp(t_step[0]), step=t_step[0], norm_out=nr, root_out=rt)
+                           h, step=t_step[0], norm_out=nr, root_out=rt)
             cur[0] ^= 1
             return
         if not args.paper_shard:
-            ctx.step(grads, w, m, v, hp(t_step[0]), step=t_step[0], norm_out=nr, root_out=rt,
+            ctx.step(grads, w, m, v, h, step=t_step[0], norm_out=nr, root_out=rt,
                      nodes=args.nodes)
             return
-        h = hp(t_step[0])
         reduce_only()
         ctx.clip(h.clip, norm_out=nr)
         ctx.adamw(w, m, v, h)
@@ -367,6 +369,7 @@ def run_ours(args, rank, world, local):
             b_.record(stream)
         torch.cuda.synchronize(dev)
     t_first = t_step[0] + 1
+    timed_out.extend((norms[i:i + 1], roots[i:i + 1]) for i in range(args.steps))
     e0.record(stream)
     for i in range(args.steps):
         if pass_ev:
