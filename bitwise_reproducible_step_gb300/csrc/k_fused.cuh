@@ -23,7 +23,7 @@
 // The arithmetic is the two-pass kernels' own, element for element: the same
 // element-to-thread mapping as k_reduce (a thread holds 4 consecutive elements of each
 // 4*NT-element tile), the same replica tree for one full group of RG = R replicas
-// (tree_group), the same chunk tree (chunk_tree), the AdamW of adamw_math.cuh and the same
+// (group_tree), the same chunk tree (chunk_tree), the AdamW of adamw_math.cuh and the same
 // PF61 limb sums, so every bit equals theirs.
 //
 // GB300 design: a persistent grid of two CTAs per SM, each with NT = 256 compute threads.
@@ -33,7 +33,7 @@
 // handed out at run time from a counter.  Two CTAs, each with its own producer and ring,
 // kept the SM's memory pipe fuller than one CTA of 512 threads with a 192 KB ring (measured
 // at 1.2e9 parameters: 10.22 -> 10.02 ms per pass).  The compute threads do the arithmetic
-// and store the new state with 16-byte stores; one leaf warp finishes the chunk digests
+// and store the new state with vector stores; one leaf warp finishes the chunk digests
 // from the compute warps' per-warp piece sums.  Every wait is bounded; a timeout sets a
 // flag.
 #pragma once
