@@ -147,7 +147,8 @@ struct repstep_ctx {
     // memory, and then the single-pass step always speculates
     uint32_t *clip_flag_h = nullptr, *clip_flag_d = nullptr;
     // the single-pass step between its halves (repstep_fused_begin .. repstep_fused_end):
-    // the buffers the second half must be given, and whether the single pass was launched
+    // the buffers the second half must be given (the state and, of the gradients, the
+    // first 8, all the single pass takes), and whether the single pass was launched
     struct FusedCall {
         bool open = false, single = false;
         uint32_t R = 0;
@@ -974,7 +975,6 @@ int fused_begin(repstep_ctx *x, const void *const *grads, uint32_t R, const void
         if (e != cudaSuccess) return x->cuda_fail(e);
         ++x->launches;
         // the call-order state of a finished reduce over [0, n)
-        x->fused.open = false;
         x->reduced = x->n;
         x->cut_norm.clear();
         x->scale_ready = false;
