@@ -15,8 +15,9 @@ between GPUs, gloo between CPU processes):
 
 Every floating-point sum -- the replica tree of each element, the chunk sums, the tree
 over all chunk sums -- and the Merkle tree run in this library's kernels
-(repstep_reduce, repstep_clip_gathered, repstep_root_gathered) in the canonical order of
-the unsharded step, so every bit equals it.  No collective reduces anything.
+(repstep_reduce or the single pass of repstep_fused_begin, repstep_clip_gathered,
+repstep_root_gathered) in the canonical order of the unsharded step, so every bit equals
+it.  No collective reduces anything.
 
 Layout.  With c = ceil(n/4096) chunks and N ranks, rank s owns chunks [s*cr, (s+1)*cr) with
 cr = ceil(c/N) (the last ranges may be shorter or empty): elements [s*S, min((s+1)*S, n))
