@@ -307,3 +307,27 @@ def test_empty_state():
     assert nr[0].item() == nr[1].item() == 0.0
     rh = rr.cpu().numpy().view(np.uint64)
     assert rh[0] == rh[1]
+
+
+def test_prediction_chooses_the_path():
+    """The host's prediction, seen through the library's launch count: after a step that
+    did not clip (or at the start) the call launches the single pass and the two gated
+    second-pass kernels; after one that clipped, the reduce and AdamW of the two passes --
+    one launch fewer.  Synchronising after each step makes the outcome visible to the host
+    before the next call."""
+    n, R = 5 * CH + 77, 8
+    dev = torch.device("cuda", 0)
+    ctx = rs.Repstep(n, device=dev)
+    w, m, v = I.gen_state(U.F32_WL, n=n, device=dev)
+    bufs = [(w, m, v), tuple(torch.empty_like(x) for x in (w, m, v))]
+    launches = []
+    clips = [False, True, True, False, False]
+    for t, clip in enumerate(clips, start=1):
+        grads = U.gen_grads(n, R, 120 + t, scale=3000.0 if clip else 1e-3)
+        before = ctx.launch_count()
+        ctx.step_fused(grads, *bufs[(t - 1) % 2], *bufs[t % 2], U.hp_for(t), step=t)
+        launches.append(ctx.launch_count() - before)
+        ctx.sync()
+    single, two = launches[0], launches[0] - 1
+    # step 2 is predicted not to clip (step 1 did not), step 3 and 4 to clip, step 5 not
+    assert launches == [single, single, two, two, single], launches
