@@ -173,6 +173,16 @@ def test_flat3000m_r8_bf16_spiked_shards():
     assert all(x > 1.0 for x in norms)              # 1% spikes x 1e3 force the clip
 
 
+def test_flat3000m_r8_bf16_single_pass():
+    """3e9 parameters, R = 8 bf16 gradients, all 3 steps through the single-pass step
+    (buffers alternating, roots on a second stream): step 1 speculates, clips and takes the
+    second pass; steps 2 and 3 follow a clip and take the two passes at once.  Every slot
+    against the oracle."""
+    wl = I.WORKLOADS["flat3000m_r8_bf16_spiked_shards"]
+    norms = run_big(wl, steps=wl.steps, single_pass=True)
+    assert all(x > 1.0 for x in norms)
+
+
 def test_flat268m_r32_three_steps_three_topologies():
     """268M parameters, R = 32: the workload's 3 steps, step t summed as the t-th staged
     topology (1 x 32, 4 x 8, 8 x 4 nodes x GPUs), against the oracle's staged sum."""
