@@ -17,7 +17,8 @@ CSRC = os.path.join(PKG, "csrc")
 OUT_DIR = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "librepstep.so")
 SOURCES = ["repstep.cu", "k_reduce.cu", "k_reduce_ftz.cu", "k_adamw.cu", "k_adamw_ftz.cu",
-           "k_small.cu", "k_blake2b.cu", "noalloc.cu", "k_fused.cu", "k_fused_ftz.cu"]
+           "k_small.cu", "k_blake2b.cu", "noalloc.cu", "k_fused.cu", "k_fused_ftz.cu",
+           "k_fused_wide.cu", "k_fused_wide_ftz.cu"]
 HEADERS = ["common.cuh", "kernels.h", "k_reduce.cuh", "k_adamw.cuh", "merkle.h",
            "adamw_math.cuh", "k_fused.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

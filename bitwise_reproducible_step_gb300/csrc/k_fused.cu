@@ -1,15 +1,16 @@
-// k_fused.cu -- the IEEE instantiations of the single-pass kernel (k_fused.cuh) and the
-// host-side helpers that size, prepare and launch any of its variants.
+// k_fused.cu -- the IEEE instantiations of the single-pass kernel (k_fused.cuh) for R = 4
+// and 8, and the host-side helpers that size, prepare and launch any of its variants.
 #include "k_fused.cuh"
 
 namespace repstep {
 
-FusedKernelFn pick_fused_ieee(const FusedShape &s) { return pick_fused<0>(s); }
+FusedKernelFn pick_fused_ieee(const FusedShape &s) { return pick_fused<0, 0>(s); }
 
 namespace {
 
 FusedKernelFn pick_any(const FusedShape &s)
 {
+    if (s.rg == 16) return s.fz ? pick_fused_wide_ftz(s) : pick_fused_wide_ieee(s);
     return s.fz ? pick_fused_ftz(s) : pick_fused_ieee(s);
 }
 
@@ -21,7 +22,8 @@ size_t fused_smem_bytes(const FusedShape &s, FusedArgs &args)
     const uint32_t es = s.dtype == 1 ? 2u : 4u;
     // as the kernel's GS: gradient stages of at most 64 KB
     const uint32_t per = TE * es;
-    const uint32_t gs = uint32_t(s.rg) * per <= 64u * 1024u ? uint32_t(s.rg) : 64u * 1024u / per;
+    const uint32_t gs_bytes = 64u * 1024u / per;
+    const uint32_t gs = s.rg < 8 ? uint32_t(s.rg) : (gs_bytes < 8u ? gs_bytes : 8u);
     const uint32_t grad_stage = gs * per;
     const uint32_t state_stage = 3u * TE * 4u + (s.mk ? TE / 8u : 0u);   // w, m, v, mask bits
     const uint32_t big = grad_stage > state_stage ? grad_stage : state_stage;

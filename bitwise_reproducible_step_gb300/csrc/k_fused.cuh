@@ -1,5 +1,6 @@
 // k_fused.cuh -- the speculative single-pass step (kernel template; k_fused.cu holds the
-// IEEE instantiations and the host helpers, k_fused_ftz.cu the flush-to-zero ones).
+// IEEE instantiations for R = 4 and 8 and the host helpers, k_fused_ftz.cu the
+// flush-to-zero ones, k_fused_wide.cu and k_fused_wide_ftz.cu those for R = 16).
 //
 // One HBM pass computes, for every element i and every 4096-element chunk k:
 //     g_i = T_{r<R}(G_r[i]) * fp32(1/R)                      (the replica reduce)
@@ -127,9 +128,12 @@ __global__ void __launch_bounds__(NT + 64, 2) k_fused(const __grid_constant__ Fu
     constexpr uint32_t VEC = 16u / (ESZ < WSZ ? ESZ : WSZ);
     // replicas per gradient stage: at most 64 KB of gradients per stage (all R replicas of
     // a tile for R <= 8)
-    constexpr int GS = (int(TE * ESZ) * RG <= 64 * 1024) ? RG : 64 * 1024 / int(TE * ESZ);
+    // replicas per gradient stage: at most 8 (the registers of one group) and 64 KB
+    constexpr int GS_BYTES = 64 * 1024 / int(TE * ESZ);
+    constexpr int GS = RG < 8 ? RG : (GS_BYTES < 8 ? GS_BYTES : 8);
     constexpr int NGS = RG / GS;                 // gradient stages per tile
-    static_assert(GS * NGS == RG, "gradient stages hold whole groups");
+    static_assert(GS * NGS == RG && (NGS & (NGS - 1)) == 0,
+                  "gradient stages hold whole groups, a power of two of them");
     static_assert(TPC * TE == kChunk && TPC * 4 <= 32, "tiles divide the chunk; limb bound");
     const AdamwArgs &A = F.adam;
 
@@ -340,8 +344,10 @@ __global__ void __launch_bounds__(NT + 64, 2) k_fused(const __grid_constant__ Fu
             const bool in_bulk = e0 >= tr.a16 && e0 + 4 <= tr.b16;
             const bool all_in = e0 >= tr.a && e0 + 4 <= tr.b;
 
-            // the replica reduce of this thread's 4 elements
-            float4 x[RG];
+            // the replica reduce of this thread's 4 elements: each stage's group of GS
+            // replicas is a perfect subtree of the canonical tree, and the NGS (a power of
+            // two) group sums combine pairwise, the lower replicas on the left
+            float4 grp[NGS];
             uint32_t slot;
             const unsigned char *sb;
 #pragma unroll
@@ -351,17 +357,18 @@ __global__ void __launch_bounds__(NT + 64, 2) k_fused(const __grid_constant__ Fu
                     !mbar_wait_bounded(smem_u32(&full[slot]), pos.phase, abort_flag))
                     fail(kFlagTimeoutReduce);
                 sb = ring + slot * A.stage_stride;
+                float4 x[GS];
 #pragma unroll
                 for (int i = 0; i < GS; ++i)
-                    x[q * GS + i] =
-                        whole ? group_of<ESZ>(sb + i * TE * ESZ, off, true, nullptr, 0, 0, 0)
-                              : group_of<ESZ>(sb + i * TE * ESZ, off, in_bulk,
-                                              F.grads[q * GS + i], e0, tr.a, tr.b);
+                    x[i] = whole ? group_of<ESZ>(sb + i * TE * ESZ, off, true, nullptr, 0, 0, 0)
+                                 : group_of<ESZ>(sb + i * TE * ESZ, off, in_bulk,
+                                                 F.grads[q * GS + i], e0, tr.a, tr.b);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&empty[slot]));
                 pos.advance(S);
+                grp[q] = group_tree<GS, FZ>(x);
             }
-            const float4 s4 = group_tree<RG, FZ>(x);
+            const float4 s4 = group_tree<NGS, FZ>(grp);
             const float4 gv = make_float4(Ar<FZ>::mul(s4.x, rho), Ar<FZ>::mul(s4.y, rho),
                                           Ar<FZ>::mul(s4.z, rho), Ar<FZ>::mul(s4.w, rho));
             float q4[4];
@@ -509,14 +516,29 @@ FusedKernelFn pick_fused_l(const FusedShape &s)
     return s.leaves ? pick_fused_pm<FZ, DT, RG, 1>(s) : pick_fused_pm<FZ, DT, RG, 0>(s);
 }
 
-// The variant of a launch in one arithmetic mode; null for a shape the kernel does not
-// cover.
-template <int FZ>
+// WIDE 0: R = 4 or 8 (one replica stage per tile); WIDE 1: R = 16 (two).  R = 32 (four
+// replica stages per tile, then the state's, in a ring of three slots) was measured slower
+// than the two passes at 268M parameters (7.62 against 6.06 ms) and is left to them.
+template <int FZ, int DT, int WIDE>
+FusedKernelFn pick_fused_r(const FusedShape &s)
+{
+    if constexpr (WIDE == 0) {
+        if (s.rg == 4) return pick_fused_l<FZ, DT, 4>(s);
+        if (s.rg == 8) return pick_fused_l<FZ, DT, 8>(s);
+    } else {
+        if (s.rg == 16) return pick_fused_l<FZ, DT, 16>(s);
+    }
+    return nullptr;
+}
+
+// The variant of a launch in one arithmetic mode and replica-count class; null for a shape
+// the kernel does not cover.  The four classes compile as translation units of their own
+// (k_fused.cu, k_fused_ftz.cu, k_fused_wide.cu, k_fused_wide_ftz.cu), in parallel.
+template <int FZ, int WIDE>
 FusedKernelFn pick_fused(const FusedShape &s)
 {
-    if (s.rg != 4 && s.rg != 8) return nullptr;
-    if (s.dtype == 0) return s.rg == 8 ? pick_fused_l<FZ, 0, 8>(s) : pick_fused_l<FZ, 0, 4>(s);
-    if (s.dtype == 1) return s.rg == 8 ? pick_fused_l<FZ, 1, 8>(s) : pick_fused_l<FZ, 1, 4>(s);
+    if (s.dtype == 0) return pick_fused_r<FZ, 0, WIDE>(s);
+    if (s.dtype == 1) return pick_fused_r<FZ, 1, WIDE>(s);
     return nullptr;
 }
 

@@ -1,0 +1,10 @@
+// k_fused_wide.cu -- the IEEE instantiations of the single-pass kernel (k_fused.cuh) for
+// R = 16, compiled as a translation unit of their own so that the variants build in
+// parallel.
+#include "k_fused.cuh"
+
+namespace repstep {
+
+FusedKernelFn pick_fused_wide_ieee(const FusedShape &s) { return pick_fused<0, 1>(s); }
+
+}  // namespace repstep

@@ -89,9 +89,9 @@ AdamwKernelFn pick_adamw_ieee(const AdamwShape &s);
 AdamwKernelFn pick_adamw_ftz(const AdamwShape &s);
 // The speculative single-pass step (k_fused.cuh): replica reduce, chunk sums of squares,
 // AdamW with clip scale 1 from (w, m, v) into (wo, mo, vo), and the PF61 leaves of the new
-// state.  R is one full replica group (4 or 8).
+// state.  R is 4, 8 or 16.
 struct FusedArgs {
-    const void *grads[8];     // the R replica gradients, global replica order
+    const void *grads[16];    // the R replica gradients, global replica order
     float *chunk_sq;          // workspace fp32[c]
     uint32_t R;
     float rho;                // fp32(1/R)
@@ -101,15 +101,17 @@ struct FusedArgs {
 
 struct FusedShape {
     int dtype;    // gradients: 0 fp32, 1 bf16
-    int rg;       // R: 4 or 8
+    int rg;       // R: 4, 8 or 16
     int leaves;   // 1: PF61 leaves fused (hash mode PF61); 0: none (audit mode)
     int pt;       // 1: bf16 parameters
     int fz;       // 1: flush-to-zero (.ftz) arithmetic
     int mk;       // 1: per-element weight-decay mask (adam.decay_mask)
 };
 using FusedKernelFn = void (*)(FusedArgs);
-FusedKernelFn pick_fused_ieee(const FusedShape &s);
+FusedKernelFn pick_fused_ieee(const FusedShape &s);       // R = 4, 8
 FusedKernelFn pick_fused_ftz(const FusedShape &s);
+FusedKernelFn pick_fused_wide_ieee(const FusedShape &s);  // R = 16
+FusedKernelFn pick_fused_wide_ftz(const FusedShape &s);
 size_t fused_smem_bytes(const FusedShape &s, FusedArgs &args);
 cudaError_t fused_prepare(const FusedShape &s, size_t smem);
 cudaError_t fused_occupancy(const FusedShape &s, size_t smem, int *blocks_per_sm);

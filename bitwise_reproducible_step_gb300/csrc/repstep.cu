@@ -148,11 +148,11 @@ struct repstep_ctx {
     uint32_t *clip_flag_h = nullptr, *clip_flag_d = nullptr;
     // the single-pass step between its halves (repstep_fused_begin .. repstep_fused_end):
     // the buffers the second half must be given (the state and, of the gradients, the
-    // first 8, all the single pass takes), and whether the single pass was launched
+    // first 16, all the single pass takes), and whether the single pass was launched
     struct FusedCall {
         bool open = false, single = false;
         uint32_t R = 0;
-        const void *g[8] = {};
+        const void *g[16] = {};
         const void *st[6] = {};
     } fused;
     bool hash_pending = false;
@@ -877,12 +877,12 @@ bool overlaps(const void *a, uint64_t na, const void *b, uint64_t nb)
 }
 
 // The speculative single-pass step (k_fused.cuh) where its kernel covers the configuration:
-// R one full replica group of 4 or 8 and the default launch shape (any gradient and
-// parameter dtype, arithmetic mode, decay mask and hash mode).  Elsewhere the same result
+// R = 4, 8 or 16 and the default launch shape (any gradient and parameter dtype,
+// arithmetic mode, decay mask and hash mode).  Elsewhere the same result
 // comes from the ordinary passes, with AdamW writing the second state buffer.
 bool fused_supported(const repstep_ctx *x, uint32_t R)
 {
-    return (R == 4 || R == 8) && x->cfg.grid_blocks == 0 &&
+    return (R == 4 || R == 8 || R == 16) && x->cfg.grid_blocks == 0 &&
            (x->cfg.block_threads == 0 || x->cfg.block_threads == 512) && x->n > 0;
 }
 
@@ -985,7 +985,7 @@ int fused_begin(repstep_ctx *x, const void *const *grads, uint32_t R, const void
     x->fused.open = true;
     x->fused.single = single;
     x->fused.R = R;
-    for (uint32_t r = 0; r < R && r < 8; ++r) x->fused.g[r] = grads[r];
+    for (uint32_t r = 0; r < R && r < 16; ++r) x->fused.g[r] = grads[r];
     x->fused.st[0] = w;
     x->fused.st[1] = m;
     x->fused.st[2] = v;
@@ -1007,7 +1007,7 @@ int fused_end(repstep_ctx *x, const void *const *grads, uint32_t R, const void *
     const repstep_ctx::FusedCall &fc = x->fused;
     bool same = fc.open && fc.R == R && fc.st[0] == w && fc.st[1] == m && fc.st[2] == v &&
                 fc.st[3] == wo && fc.st[4] == mo && fc.st[5] == vo;
-    for (uint32_t r = 0; same && r < R && r < 8; ++r) same = fc.g[r] == grads[r];
+    for (uint32_t r = 0; same && r < R && r < 16; ++r) same = fc.g[r] == grads[r];
     if (!same || !x->scale_ready) return REPSTEP_ERR_STATE;
     void *w_in = const_cast<void *>(w);
     float *m_in = const_cast<float *>(m), *v_in = const_cast<float *>(v);

@@ -354,9 +354,9 @@ int repstep_step(repstep_ctx *ctx, const void *const *d_grads, uint32_t R, uint3
  *   behind the host) can only cost time.
  * - The result is bit for bit repstep_step's on the same inputs either way; only the
  *   time differs.
- * - The single pass covers R = 4 or 8 with the default launch shape, in every gradient and
- *   parameter dtype, arithmetic mode, decay mask and hash mode; any other replica count or
- *   launch shape runs the two passes of repstep_step, writing the output buffers.
+ * - The single pass covers R = 4, 8 or 16 with the default launch shape, in every gradient
+ *   and parameter dtype, arithmetic mode, decay mask and hash mode; any other replica count
+ *   or launch shape runs the two passes of repstep_step, writing the output buffers.
  * - `step`, hp, d_norm_out and d_root_out as repstep_step; the root is the output state's. */
 int repstep_step_fused(repstep_ctx *ctx, const void *const *d_grads, uint32_t R,
                        const void *d_w, const float *d_m, const float *d_v, void *d_w_out,

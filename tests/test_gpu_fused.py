@@ -5,9 +5,9 @@ bit -- the new w, m, v, the pre-clip norm, the root and the leaves -- must equal
 repstep_step's on the same inputs, step after step with the two state buffers alternating,
 on all four paths (predicted no clip and none; predicted no clip and a clip; predicted a
 clip and one; predicted a clip and none); the input state must be left untouched.
-The single pass covers R = 4 and 8 with any gradient and parameter dtype, arithmetic mode,
-decay mask and hash mode; other replica counts and launch shapes take the two ordinary
-passes into the output buffers, with the same bits."""
+The single pass covers R = 4, 8 and 16 with any gradient and parameter dtype,
+arithmetic mode, decay mask and hash mode; other replica counts and launch shapes take the
+two ordinary passes into the output buffers, with the same bits."""
 import ctypes as C
 
 import numpy as np
@@ -128,6 +128,9 @@ def test_fused_steps_beside_pending_roots(n, R, hm):
     (1000, 8, torch.float32),                 # one short chunk: its second tile is empty
     (1, 4, torch.float32),
     (64 * CH, 8, torch.float32),
+    (3 * CH + 5, 16, torch.float32),          # two replica stages per tile
+    (2 * CH + 2049, 16, torch.bfloat16),
+    (20 * CH + 999, 32, torch.float32),       # R = 32: the two passes
 ])
 def test_fused_equals_two_pass_step(n, R, gdt):
     clipped = run_pair(n, R, gdt)
@@ -144,7 +147,9 @@ def test_fused_audit_mode_and_hash_stream():
     (dict(param_dtype=torch.bfloat16), 4, torch.bfloat16),
     (dict(subnormals=rs.SUBNORMALS_FTZ), 8, torch.float32),
     (dict(subnormals=rs.SUBNORMALS_FTZ, param_dtype=torch.bfloat16), 4, torch.bfloat16),
-    (dict(), 3, torch.float32),                                 # R not 4 or 8: two passes
+    (dict(subnormals=rs.SUBNORMALS_FTZ, param_dtype=torch.bfloat16), 16, torch.float32),
+    (dict(), 3, torch.float32),                                 # R not 4, 8, 16: two passes
+    (dict(), 12, torch.bfloat16),
     (dict(block_threads=256), 8, torch.float32),                # launch shape: two passes
 ])
 def test_configuration_variants(kw, R, gdt):
