@@ -21,11 +21,12 @@
 // once.  The host launches the pass only when the last clip outcome it can see did not
 // clip; after one that did, the step takes the two passes directly.
 //
-// The arithmetic is the two-pass kernels' own, element for element: the same
+// The arithmetic is the two-pass kernels' own, element for element: the same kind of
 // element-to-thread mapping as k_reduce (a thread holds 4 consecutive elements of each
-// 4*NT-element tile), the same replica tree for one full group of RG = R replicas
-// (group_tree), the same chunk tree (chunk_tree), the AdamW of adamw_math.cuh and the same
-// PF61 limb sums, so every bit equals theirs.
+// 4*NT-element tile), the canonical replica tree (group_tree over a group of RG = R <= 8
+// replicas, or over two groups of 8 for R = 16), the same chunk tree (chunk_tree, defined
+// over element indices), the AdamW of adamw_math.cuh and the same PF61 limb sums, so every
+// bit equals theirs.
 //
 // GB300 design: a persistent grid of two CTAs per SM, each with NT = 256 compute threads.
 // Each CTA's producer lane streams, for each 1024-element tile, a stage with the R gradient
